@@ -1,0 +1,293 @@
+"""CPU fp64 oracle for FlashMask column-wise masked attention.
+
+TEST INFRASTRUCTURE. Only the tests, `__graft_entry__.smoke()` and the
+benchmark's CPU-baseline leg import this module; the library's product path
+never calls it, and it shares no code with the CUDA kernels. It is plain,
+slow and written straight from the definitions:
+
+* the mask comes from the four column-wise boundary vectors
+  (FlashMask-3 project page, "Overview" and §3.1): element (i, j) is masked iff
+  LTS_j <= i < LTE_j or UTS_j <= i < UTE_j, plus i < j in causal mode;
+* attention is softmax(scale * Q K^T + M) V with M in {0, -inf}
+  (FlashMask Guide, §2 "The O(N^2) Memory Explosion of Dense Mask Matrices",
+  the equation S = QK^T/sqrt(d_k) + M);
+* gradients are the analytic ones of that expression (Flash MSA Attention
+  Kernel Implementation, "The Backward Pass": dV = P^T dO, dP = dO V^T,
+  dS = P * (dP - rowsum(P * dP)), dQ = dS K, dK = dS^T Q, each scaled);
+* tiles are classified from block-wise min/max of the vectors (FlashMask-3
+  project page, §3.1, the tile rule under the 64 x 64 / 8 x 8 figure),
+  generalised to intervals that do not reach the sequence edge;
+* localization is the clip-shift-max map of FlashMask-3 project page, §3.2.
+
+Readings where the pages are silent (all pinned by tests/test_oracle.py):
+  - intervals are half-open row ranges; start >= end is an empty interval;
+  - causal masks i < j (the diagonal is visible);
+  - a fully-masked query row has O = 0 and LSE = -inf and contributes no
+    gradient; LSE is the natural log of sum_j exp(scale * q_i . k_j) over
+    visible j;
+  - GQA groups are contiguous: query head h uses kv head h // (H_q / H_kv);
+  - the vectors are (B, N) and shared by every head.
+
+Precision: every input is widened to float64; all arithmetic is float64.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+SKIP, PARTIAL, UNMASKED = 0, 1, 2
+
+
+# ------------------------------------------------------------------ mask
+def masked_rows(lts, lte, uts, ute, causal: bool, rows) -> np.ndarray:
+    """Rows of the dense mask: True where (i, j) is masked, shape (len(rows), N).
+
+    lts..ute are the (N,) boundary vectors of one batch entry.
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    n = lts.shape[0]
+    i = rows[:, None]
+    j = np.arange(n, dtype=np.int64)[None, :]
+    lower = (lts[None, :].astype(np.int64) <= i) & (i < lte[None, :].astype(np.int64))
+    upper = (uts[None, :].astype(np.int64) <= i) & (i < ute[None, :].astype(np.int64))
+    m = lower | upper
+    if causal:
+        m = m | (i < j)
+    return m
+
+
+def dense_mask(lts, lte, uts, ute, causal: bool) -> np.ndarray:
+    """The full N x N boolean mask (True = masked). Small N only."""
+    return masked_rows(lts, lte, uts, ute, causal, np.arange(lts.shape[0]))
+
+
+def masked_cols(lts, lte, uts, ute, causal: bool, cols) -> np.ndarray:
+    """Columns of the dense mask, shape (N, len(cols)): True where masked."""
+    cols = np.asarray(cols, dtype=np.int64)
+    n = lts.shape[0]
+    i = np.arange(n, dtype=np.int64)[:, None]
+    j = cols[None, :]
+    lower = (lts[cols].astype(np.int64)[None, :] <= i) & (i < lte[cols].astype(np.int64)[None, :])
+    upper = (uts[cols].astype(np.int64)[None, :] <= i) & (i < ute[cols].astype(np.int64)[None, :])
+    m = lower | upper
+    if causal:
+        m = m | (i < j)
+    return m
+
+
+# ------------------------------------------------------- tile classes
+def block_minmax(vec, bn: int):
+    """Per KV block of bn columns: (min, max) of vec over the block's valid columns."""
+    n = vec.shape[0]
+    nk = -(-n // bn)
+    mins = np.empty(nk, dtype=np.int64)
+    maxs = np.empty(nk, dtype=np.int64)
+    for kb in range(nk):
+        blk = vec[kb * bn : min((kb + 1) * bn, n)].astype(np.int64)
+        mins[kb] = blk.min()
+        maxs[kb] = blk.max()
+    return mins, maxs
+
+
+def classify_tiles(lts, lte, uts, ute, causal: bool, bm: int, bn: int) -> np.ndarray:
+    """Class of every (Q-block, KV-block) tile of one batch entry: (nQ, nK) uint8.
+
+    Tile rows [q0, q1), columns [k0, k1) (the last block of each axis may be
+    short). With block min/max of the four vectors:
+      skip      iff (q0 >= max LTS and q1 <= min LTE)
+                 or (q0 >= max UTS and q1 <= min UTE)
+                 or (causal and q1 <= k0)
+      unmasked  iff (q1 <= min LTS or q0 >= max LTE)
+                and (q1 <= min UTS or q0 >= max UTE)
+                and (not causal or q0 >= k1 - 1)
+      partial   otherwise.
+    With LTE = N and UTS = 0 this is exactly the printed rule (skip if
+    q0 >= max LTS or q1 <= min UTE; unmasked if q1 <= min LTS and
+    q0 >= max UTE) plus the causal term.
+    """
+    n = lts.shape[0]
+    nq, nk = -(-n // bm), -(-n // bn)
+    mn_lts, mx_lts = block_minmax(lts, bn)
+    mn_lte, mx_lte = block_minmax(lte, bn)
+    mn_uts, mx_uts = block_minmax(uts, bn)
+    mn_ute, mx_ute = block_minmax(ute, bn)
+    cls = np.empty((nq, nk), dtype=np.uint8)
+    for qb in range(nq):
+        q0, q1 = qb * bm, min((qb + 1) * bm, n)
+        for kb in range(nk):
+            k0, k1 = kb * bn, min((kb + 1) * bn, n)
+            skip = (
+                (q0 >= mx_lts[kb] and q1 <= mn_lte[kb])
+                or (q0 >= mx_uts[kb] and q1 <= mn_ute[kb])
+                or (causal and q1 <= k0)
+            )
+            unmasked = (
+                (q1 <= mn_lts[kb] or q0 >= mx_lte[kb])
+                and (q1 <= mn_uts[kb] or q0 >= mx_ute[kb])
+                and ((not causal) or q0 >= k1 - 1)
+            )
+            cls[qb, kb] = SKIP if skip else (UNMASKED if unmasked else PARTIAL)
+    return cls
+
+
+def build_queues(cls_batches):
+    """Compacted queues in CSR form from a list of per-batch (nQ, nK) class tables.
+
+    Q-side: for each (b, qb) in order, the non-skipped KV blocks in DESCENDING
+    kb order (visited right to left), entry = (kb << 1) | is_partial.
+    K-side: for each (b, kb), the non-skipped Q blocks in ASCENDING qb order,
+    entry = (qb << 1) | is_partial.
+    Returns (q_off, q_queue, k_off, k_queue) as int32 arrays; offsets have
+    B*nQ + 1 (resp. B*nK + 1) entries.
+    """
+    q_off, q_queue, k_off, k_queue = [0], [], [0], []
+    for cls in cls_batches:
+        nq, nk = cls.shape
+        for qb in range(nq):
+            for kb in range(nk - 1, -1, -1):
+                c = int(cls[qb, kb])
+                if c != SKIP:
+                    q_queue.append((kb << 1) | (1 if c == PARTIAL else 0))
+            q_off.append(len(q_queue))
+    for cls in cls_batches:
+        nq, nk = cls.shape
+        for kb in range(nk):
+            for qb in range(nq):
+                c = int(cls[qb, kb])
+                if c != SKIP:
+                    k_queue.append((qb << 1) | (1 if c == PARTIAL else 0))
+            k_off.append(len(k_queue))
+    as32 = lambda x: np.asarray(x, dtype=np.int32)
+    return as32(q_off), as32(q_queue), as32(k_off), as32(k_queue)
+
+
+# ------------------------------------------------------------- attention
+def _kv_head(h: int, hq: int, hkv: int) -> int:
+    return h // (hq // hkv)
+
+
+def row_probs(q, k, vec, causal, scale, b, h, rows):
+    """Softmax probabilities P (len(rows), N) and LSE (len(rows),) for one head.
+
+    S = scale * q_i . k_j over all N keys, masked entries set to -inf, then
+    P = exp(S - max) / sum. A fully-masked row gets P = 0 and LSE = -inf.
+    q: (B, Hq, N, d), k: (B, Hkv, N, d), float64.
+    """
+    lts, lte, uts, ute = (x[b] for x in vec)
+    g = _kv_head(h, q.shape[1], k.shape[1])
+    m = masked_rows(lts, lte, uts, ute, causal, rows)
+    s = scale * (q[b, h, rows] @ k[b, g].T)
+    s = np.where(m, -np.inf, s)
+    r = s.max(axis=1)
+    empty = np.isneginf(r)
+    r_safe = np.where(empty, 0.0, r)
+    e = np.exp(s - r_safe[:, None])
+    l = e.sum(axis=1)
+    p = e / np.where(empty, 1.0, l)[:, None]
+    lse = np.where(empty, -np.inf, r_safe + np.log(np.where(empty, 1.0, l)))
+    return p, lse
+
+
+def forward(q, k, v, vec, causal: bool, scale: float, heads=None, rows=None, row_chunk: int = 512):
+    """O and LSE for the selected heads and rows.
+
+    Returns O of shape (B, len(heads), len(rows), d) and LSE (B, len(heads), len(rows)).
+    """
+    B, Hq, N, d = q.shape
+    heads = list(range(Hq)) if heads is None else list(heads)
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    O = np.zeros((B, len(heads), len(rows), d))
+    L = np.zeros((B, len(heads), len(rows)))
+    for b in range(B):
+        for hi, h in enumerate(heads):
+            g = _kv_head(h, Hq, k.shape[1])
+            for c0 in range(0, len(rows), row_chunk):
+                rr = rows[c0 : c0 + row_chunk]
+                p, lse = row_probs(q, k, vec, causal, scale, b, h, rr)
+                O[b, hi, c0 : c0 + len(rr)] = p @ v[b, g]
+                L[b, hi, c0 : c0 + len(rr)] = lse
+    return O, L
+
+
+def backward(q, k, v, do, vec, causal: bool, scale: float, heads=None, rows=None, cols=None, row_chunk=256):
+    """Analytic gradients of sum(O * dO).
+
+    dQ is returned for the selected `rows` of the selected `heads`:
+    shape (B, len(heads), len(rows), d).
+    dK, dV are returned for the selected key `cols` of every kv head,
+    summed over the selected query heads only (so a head subset gives the
+    gradient of that subset): shape (B, Hkv, len(cols), d).
+    Per row i (one query head): P from `row_probs`; dP_ij = dO_i . v_j;
+    D_i = sum_j P_ij dP_ij; dS_ij = P_ij (dP_ij - D_i);
+    dQ_i = scale sum_j dS_ij k_j; dV_j += P_ij dO_i; dK_j += scale dS_ij q_i.
+    """
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    heads = list(range(Hq)) if heads is None else list(heads)
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    cols = np.arange(N) if cols is None else np.asarray(cols)
+    dQ = np.zeros((B, len(heads), len(rows), d))
+    dK = np.zeros((B, Hkv, len(cols), d))
+    dV = np.zeros((B, Hkv, len(cols), d))
+    for b in range(B):
+        lts, lte, uts, ute = (x[b] for x in vec)
+        # rows that see at least one selected column: only they feed dK/dV there
+        mc = masked_cols(lts, lte, uts, ute, causal, cols)
+        feed_rows = np.nonzero(~mc.all(axis=1))[0]
+        need = np.union1d(rows, feed_rows)
+        row_pos = {int(r): t for t, r in enumerate(rows)}
+        want_q = np.isin(need, rows)
+        want_kv = np.isin(need, feed_rows)
+        for hi, h in enumerate(heads):
+            g = _kv_head(h, Hq, Hkv)
+            for c0 in range(0, len(need), row_chunk):
+                rr = need[c0 : c0 + row_chunk]
+                p, _ = row_probs(q, k, vec, causal, scale, b, h, rr)
+                dp = do[b, h, rr] @ v[b, g].T
+                D = (p * dp).sum(axis=1)
+                ds = p * (dp - D[:, None])
+                wq = want_q[c0 : c0 + len(rr)]
+                if wq.any():
+                    dq_rows = scale * (ds[wq] @ k[b, g])
+                    for t, r in enumerate(rr[wq]):
+                        dQ[b, hi, row_pos[int(r)]] = dq_rows[t]
+                wk = want_kv[c0 : c0 + len(rr)]
+                if wk.any():
+                    dV[b, g] += p[wk][:, cols].T @ do[b, h, rr[wk]]
+                    dK[b, g] += scale * (ds[wk][:, cols].T @ q[b, h, rr[wk]])
+    return dQ, dK, dV
+
+
+def unmasked_pairs(vec_b, causal: bool, row_chunk: int = 4096) -> int:
+    """Number of visible (i, j) pairs of one batch entry's mask."""
+    lts, lte, uts, ute = vec_b
+    n = lts.shape[0]
+    tot = 0
+    for r0 in range(0, n, row_chunk):
+        m = masked_rows(lts, lte, uts, ute, causal, np.arange(r0, min(r0 + row_chunk, n)))
+        tot += int((~m).sum())
+    return tot
+
+
+# ---------------------------------------------------------- localization
+def localize(x, offsets, C: int) -> np.ndarray:
+    """Rank-local row boundaries, the clip-shift-max form.
+
+    x^(r) = max_i [ clip(x - O_i, 0, C) + i*C*1(clip(x - O_i, 0, C) > 0) ],
+    with O_i the global start of the rank's i-th chunk (ascending) and C the
+    chunk length; the max over an all-zero set is 0.
+    """
+    x = np.asarray(x, dtype=np.int64)
+    out = np.zeros_like(x)
+    for i, o in enumerate(offsets):
+        c = np.clip(x - int(o), 0, C)
+        out = np.maximum(out, c + i * C * (c > 0))
+    return out.astype(np.int32)
+
+
+def localize_count(x, offsets, C: int) -> np.ndarray:
+    """The same map as a plain count: number of the rank's rows before global row x."""
+    x = np.asarray(x, dtype=np.int64)
+    out = np.zeros_like(x)
+    for o in offsets:
+        out += np.clip(x - int(o), 0, C)
+    return out.astype(np.int32)
