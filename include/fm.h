@@ -1,0 +1,181 @@
+/* fm.h — C ABI of the GB300 (sm_103a) FlashMask column-wise masked attention library.
+ *
+ * The library computes exact scaled-dot-product attention, forward and backward,
+ * under the FlashMask column-wise mask (FlashMask-3 project page, "Overview"):
+ * for key column j the masked query rows are the half-open intervals
+ * [LTS_j, LTE_j) and [UTS_j, UTE_j), plus rows i < j when causal is set.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers unless a comment says otherwise.
+ *     The caller allocates and owns all memory, including workspaces sized by
+ *     the *_workspace_bytes queries; the library never allocates or frees.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every compute entry point only enqueues work on that stream and returns;
+ *     it never synchronizes, except fm_device_status.
+ *   - Layouts: Q, O, dO, dQ are contiguous (B, H_q, N, d) bf16; K, V, dK, dV are
+ *     contiguous (B, H_kv, N, d) bf16; LSE is (B, H_q, N) fp32; the four mask
+ *     vectors are (B, N) int32, shared by every head. Tensor base addresses must
+ *     be 16-byte aligned.
+ *   - GQA: query head h reads kv head h / (H_q / H_kv) (contiguous groups).
+ *   - Errors: arguments are validated on the host and a bad call returns an
+ *     error status without launching anything. Problems found on the device
+ *     (a mask value outside [0, N], a bounded wait that expired) never trap:
+ *     they set bits in a device error word that fm_device_status reads.
+ */
+#ifndef FM_H_
+#define FM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FM_ABI_VERSION 1
+
+typedef enum fm_status {
+  FM_OK = 0,
+  FM_ERR_INVALID_ARG = 1, /* null pointer, bad shape, misaligned tensor */
+  FM_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head dim not 64/128) */
+  FM_ERR_WORKSPACE = 3,   /* workspace pointer null or smaller than required */
+  FM_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
+  FM_ERR_TIMEOUT = 5,     /* device error word: a bounded on-device wait expired */
+  FM_ERR_DEVICE = 6       /* device error word: bad mask values or queue entries */
+} fm_status;
+
+/* Device error word bits (fm_device_status). */
+#define FM_DEVERR_TIMEOUT 1
+#define FM_DEVERR_RANGE 2
+#define FM_DEVERR_QUEUE 4
+
+/* Problem shape. scale multiplies q.k (usually 1/sqrt(d)); causal != 0 adds i < j. */
+typedef struct fm_problem {
+  int32_t B, H_q, H_kv, N, d;
+  float scale;
+  int32_t causal;
+} fm_problem;
+
+/* Tile geometry for classification: block_m query rows x block_n key columns.
+ * Each must be one of 32, 64, 128, 256. The attention kernels need the tiling
+ * returned by fm_attn_tiling. */
+typedef struct fm_tiling {
+  int32_t block_m, block_n;
+} fm_tiling;
+
+/* ABI version (FM_ABI_VERSION of the built library). */
+int32_t fm_abi_version(void);
+
+/* Static, human-readable name of a status code. */
+const char* fm_status_string(fm_status s);
+
+/* The tiling the attention kernels were built for (128 x 128). */
+fm_status fm_attn_tiling(fm_tiling* out);
+
+/* Number of Q blocks ceil(N / block_m) and KV blocks ceil(N / block_n). */
+fm_status fm_tile_counts(const fm_problem* p, const fm_tiling* t, int32_t* n_qblocks, int32_t* n_kblocks);
+
+/* ---------------------------------------------------------------------------
+ * Tile classification and queue construction.
+ *
+ * FlashMask-3 project page, §3.1 ("A third warp role that reads the mask"):
+ * block-wise min/max of the boundary vectors classify every (Q-block, KV-block)
+ * tile as fully-masked (skipped), partial (masked element-wise) or unmasked,
+ * and each Q block gets a queue of its valid KV blocks tagged partial or
+ * unmasked, visited right to left. The rule, for tile rows [q0, q1) and key
+ * columns [k0, k1) (the last block of an axis may be short when N is not a
+ * multiple of the tile):
+ *   skip     iff (q0 >= max LTS and q1 <= min LTE) or (q0 >= max UTS and q1 <= min UTE)
+ *                or (causal and q1 <= k0)
+ *   unmasked iff (q1 <= min LTS or q0 >= max LTE) and (q1 <= min UTS or q0 >= max UTE)
+ *                and (not causal or q0 >= k1 - 1)
+ *   partial  otherwise.
+ * With LTE = N and UTS = 0 this is exactly the printed rule plus the causal term.
+ *
+ * Outputs (device, caller-allocated):
+ *   tile_class  (B, nQ, nK) uint8: 0 = skip, 1 = partial, 2 = unmasked.
+ *   q_off       B*nQ + 1 int32: CSR offsets; row (b, qb) is entry b*nQ + qb.
+ *   q_queue     capacity B*nQ*nK int32: for each row, the non-skipped KV blocks in
+ *               DESCENDING kb order, entry = (kb << 1) | is_partial.
+ *   k_off       B*nK + 1 int32; k_queue capacity B*nQ*nK int32: for each (b, kb),
+ *               the non-skipped Q blocks in ASCENDING qb order, entry =
+ *               (qb << 1) | is_partial (the backward pass walks these).
+ * Mask values outside [0, N] are clamped for classification and flagged
+ * (FM_DEVERR_RANGE). Workspace: fm_classify_workspace_bytes.
+ * ------------------------------------------------------------------------- */
+size_t fm_classify_workspace_bytes(const fm_problem* p, const fm_tiling* t);
+fm_status fm_classify_tiles(const fm_problem* p, const fm_tiling* t, const int32_t* lts, const int32_t* lte,
+                            const int32_t* uts, const int32_t* ute, uint8_t* tile_class, int32_t* q_off,
+                            int32_t* q_queue, int32_t* k_off, int32_t* k_queue, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Forward: O = softmax(scale * Q K^T + M) V and LSE = log sum_j exp(scale q.k_j)
+ * over visible j (natural log), where M is 0 or -inf from the mask.
+ *
+ * FlashMask-3 project page, §3.1 (KV Loader: loads only queued KV blocks;
+ * MMA Consumer: score, softmax and output, row-interval mask applied only on
+ * partial blocks); the online-softmax recurrence (running max m and sum l,
+ * rescaling O) is the one in "Flash MSA Attention Kernel Implementation",
+ * "The Flash Core: Tiling Over the Memory Hierarchy".
+ * A query row with no visible key gets O = 0 and LSE = -inf.
+ *
+ * q_off / q_queue must come from fm_classify_tiles with the fm_attn_tiling
+ * tiling and the same problem and mask. d must be 64 or 128.
+ * Workspace: fm_attn_fwd_workspace_bytes (may be 0 bytes -> ws may be NULL).
+ * ------------------------------------------------------------------------- */
+size_t fm_attn_fwd_workspace_bytes(const fm_problem* p);
+fm_status fm_attn_fwd(const fm_problem* p, const void* q, const void* k, const void* v, const int32_t* lts,
+                      const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
+                      const int32_t* q_queue, void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Backward: given dO, the gradients of sum(O * dO):
+ *   P = exp(scale S - LSE), dV = P^T dO, dP = dO V^T, D = rowsum(dO * O),
+ *   dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q,
+ * recomputing P from LSE ("Flash MSA Attention Kernel Implementation",
+ * "The Backward Pass: The Real Beast"), skipping the same fully-masked tiles
+ * and masking only partial tiles. dK and dV are summed over the query heads
+ * of each GQA group. Rows with LSE = -inf contribute nothing.
+ *
+ * o and lse must be the forward outputs for the same inputs. k_off / k_queue
+ * come from fm_classify_tiles with the fm_attn_tiling tiling.
+ * Workspace: fm_attn_bwd_workspace_bytes (fp32 dQ accumulator, row terms D).
+ * ------------------------------------------------------------------------- */
+size_t fm_attn_bwd_workspace_bytes(const fm_problem* p);
+fm_status fm_attn_bwd(const fm_problem* p, const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, const int32_t* lts, const int32_t* lte,
+                      const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
+                      void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Zero-communication mask localization (FlashMask-3 project page, §3.2):
+ *   x_local = max_i [ clip(x - O_i, 0, C) + i*C*1(clip(x - O_i, 0, C) > 0) ]
+ * = the number of the rank's rows before global row x, for a rank that owns
+ * kappa chunks of C rows starting at global rows chunk_off[0] < chunk_off[1] < ...
+ * x_global: n device int32 values (any of the four boundary vectors, any
+ * number of them concatenated); chunk_off: kappa device int32 offsets, ascending,
+ * 1 <= kappa <= 4096; x_local: n device int32 outputs. C >= 1.
+ * ------------------------------------------------------------------------- */
+fm_status fm_localize(const int32_t* x_global, int64_t n, const int32_t* chunk_off, int32_t kappa, int32_t C,
+                      int32_t* x_local, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Device error word. Synchronizes `stream`, returns the accumulated FM_DEVERR_*
+ * bits in *bits (may be NULL) and clears them. Status: FM_OK when no bit is
+ * set, FM_ERR_TIMEOUT when FM_DEVERR_TIMEOUT is set, else FM_ERR_DEVICE.
+ * The word is per device and shared by all streams of the process.
+ * ------------------------------------------------------------------------- */
+fm_status fm_device_status(void* stream, int32_t* bits);
+
+/* Self-test of the bounded device wait: launches one CTA that waits on an
+ * mbarrier no one arrives at, with a limit of limit_us microseconds
+ * (1 .. 10,000,000). The wait expires, the kernel sets FM_DEVERR_TIMEOUT and
+ * returns normally; the context stays usable. Used by the tests to check the
+ * timeout path without hanging or faulting the GPU. */
+fm_status fm_selftest_wait_timeout(int64_t limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FM_H_ */

@@ -1,0 +1,241 @@
+"""Python binding of libfm (include/fm.h): FlashMask column-wise masked attention on GB300.
+
+Argument marshalling only. Every step of the computation runs in the CUDA
+kernels of libfm.so; torch supplies device memory and the current stream.
+Importing works without a GPU; the first call loads libfm.so and raises if it
+is missing (build it with `mask_aware_sparse_gb300.build.build()`), so there
+is no silent fallback.
+
+Functions carry the names of the C entry points:
+  fm_classify_tiles, fm_attn_fwd, fm_attn_bwd, fm_localize, fm_device_status,
+  fm_selftest_wait_timeout, plus flashmask_attention (autograd wrapper: the
+classification, forward and backward calls in one differentiable op).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfm.so")
+
+FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_WORKSPACE, FM_ERR_CUDA, FM_ERR_TIMEOUT, FM_ERR_DEVICE = range(7)
+FM_DEVERR_TIMEOUT, FM_DEVERR_RANGE, FM_DEVERR_QUEUE = 1, 2, 4
+
+
+class fm_problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32), ("N", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("scale", ctypes.c_float), ("causal", ctypes.c_int32)]
+
+
+class fm_tiling(ctypes.Structure):
+    _fields_ = [("block_m", ctypes.c_int32), ("block_n", ctypes.c_int32)]
+
+
+class FMError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_SIGS = {
+    "fm_abi_version": (ctypes.c_int32, []),
+    "fm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "fm_attn_tiling": (ctypes.c_int, [ctypes.POINTER(fm_tiling)]),
+    "fm_tile_counts": (ctypes.c_int, [ctypes.POINTER(fm_problem), ctypes.POINTER(fm_tiling),
+                                      ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
+    "fm_classify_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem), ctypes.POINTER(fm_tiling)]),
+    "fm_classify_tiles": (ctypes.c_int, [ctypes.POINTER(fm_problem), ctypes.POINTER(fm_tiling)] + [_P] * 9
+                          + [_P, ctypes.c_size_t, _P]),
+    "fm_attn_fwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
+    "fm_attn_fwd": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 11 + [_P, ctypes.c_size_t, _P]),
+    "fm_attn_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
+    "fm_attn_bwd": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 15 + [_P, ctypes.c_size_t, _P]),
+    "fm_localize": (ctypes.c_int, [_P, ctypes.c_int64, _P, ctypes.c_int32, ctypes.c_int32, _P, _P]),
+    "fm_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32)]),
+    "fm_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, _P]),
+}
+EXPORTS = tuple(_SIGS)
+
+
+def lib():
+    """The loaded libfm.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with mask_aware_sparse_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(s: int) -> str:
+    try:
+        return lib().fm_status_string(int(s)).decode()
+    except Exception:  # library not loadable: still give a message
+        return "status"
+
+
+def _check(st: int, what: str):
+    if st != FM_OK:
+        raise FMError(st, what)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _problem(B, H_q, H_kv, N, d, scale, causal) -> fm_problem:
+    return fm_problem(int(B), int(H_q), int(H_kv), int(N), int(d), float(scale), 1 if causal else 0)
+
+
+def _vec_ok(*vs):
+    for v in vs:
+        if v.dtype != torch.int32 or not v.is_contiguous() or not v.is_cuda:
+            raise ValueError("mask vectors must be contiguous int32 CUDA tensors of shape (B, N)")
+
+
+def _bf16_ok(*ts):
+    for t in ts:
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda or t.dim() != 4:
+            raise ValueError("Q/K/V/O/dO must be contiguous bf16 CUDA tensors of shape (B, H, N, d)")
+
+
+def attn_tiling():
+    t = fm_tiling()
+    _check(lib().fm_attn_tiling(ctypes.byref(t)), "fm_attn_tiling")
+    return t.block_m, t.block_n
+
+
+@dataclass
+class TileQueues:
+    """Outputs of fm_classify_tiles (device tensors) and the tiling they were built with."""
+    tile_class: torch.Tensor  # (B, nQ, nK) uint8: 0 skip, 1 partial, 2 unmasked
+    q_off: torch.Tensor       # (B*nQ + 1,) int32
+    q_queue: torch.Tensor     # (capacity,) int32, (kb << 1) | partial, kb descending per row
+    k_off: torch.Tensor       # (B*nK + 1,) int32
+    k_queue: torch.Tensor     # (capacity,) int32, (qb << 1) | partial, qb ascending per column
+    block_m: int
+    block_n: int
+
+
+def fm_classify_tiles(lts, lte, uts, ute, *, causal: bool, block_m: int = 128, block_n: int = 128, stream=None):
+    """Classify every (Q-block, KV-block) tile and build both compacted queues."""
+    _vec_ok(lts, lte, uts, ute)
+    B, N = lts.shape
+    prob = _problem(B, 1, 1, N, 128, 1.0, causal)
+    til = fm_tiling(block_m, block_n)
+    nq, nk = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().fm_tile_counts(ctypes.byref(prob), ctypes.byref(til), ctypes.byref(nq), ctypes.byref(nk)),
+           "fm_tile_counts")
+    nq, nk = nq.value, nk.value
+    dev = lts.device
+    cap = max(1, B * nq * nk)
+    cls = torch.empty((B, nq, nk), dtype=torch.uint8, device=dev)
+    q_off = torch.empty(B * nq + 1, dtype=torch.int32, device=dev)
+    k_off = torch.empty(B * nk + 1, dtype=torch.int32, device=dev)
+    q_queue = torch.empty(cap, dtype=torch.int32, device=dev)
+    k_queue = torch.empty(cap, dtype=torch.int32, device=dev)
+    wsb = lib().fm_classify_workspace_bytes(ctypes.byref(prob), ctypes.byref(til))
+    ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=dev)
+    _check(lib().fm_classify_tiles(ctypes.byref(prob), ctypes.byref(til), _ptr(lts), _ptr(lte), _ptr(uts), _ptr(ute),
+                                   _ptr(cls), _ptr(q_off), _ptr(q_queue), _ptr(k_off), _ptr(k_queue), _ptr(ws),
+                                   ctypes.c_size_t(wsb), _stream(stream)), "fm_classify_tiles")
+    return TileQueues(cls, q_off, q_queue, k_off, k_queue, block_m, block_n)
+
+
+def fm_attn_fwd(q, k, v, lts, lte, uts, ute, queues: TileQueues, *, scale: float, causal: bool, o=None, lse=None,
+                ws=None, stream=None):
+    """Forward: returns (O bf16 (B,H_q,N,d), LSE fp32 (B,H_q,N))."""
+    _bf16_ok(q, k, v)
+    _vec_ok(lts, lte, uts, ute)
+    B, Hq, N, d = q.shape
+    prob = _problem(B, Hq, k.shape[1], N, d, scale, causal)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    wsb = lib().fm_attn_fwd_workspace_bytes(ctypes.byref(prob))
+    if ws is None or ws.numel() < wsb:
+        ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=q.device)
+    _check(lib().fm_attn_fwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(lts), _ptr(lte), _ptr(uts),
+                             _ptr(ute), _ptr(queues.q_off), _ptr(queues.q_queue), _ptr(o), _ptr(lse), _ptr(ws),
+                             ctypes.c_size_t(wsb), _stream(stream)), "fm_attn_fwd")
+    return o, lse
+
+
+def fm_attn_bwd(q, k, v, o, lse, do, lts, lte, uts, ute, queues: TileQueues, *, scale: float, causal: bool,
+                dq=None, dk=None, dv=None, ws=None, stream=None):
+    """Backward: returns (dQ, dK, dV) bf16."""
+    _bf16_ok(q, k, v, o, do)
+    _vec_ok(lts, lte, uts, ute)
+    B, Hq, N, d = q.shape
+    prob = _problem(B, Hq, k.shape[1], N, d, scale, causal)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    wsb = lib().fm_attn_bwd_workspace_bytes(ctypes.byref(prob))
+    if ws is None or ws.numel() < wsb:
+        ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=q.device)
+    _check(lib().fm_attn_bwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(lts),
+                             _ptr(lte), _ptr(uts), _ptr(ute), _ptr(queues.k_off), _ptr(queues.k_queue), _ptr(dq),
+                             _ptr(dk), _ptr(dv), _ptr(ws), ctypes.c_size_t(wsb), _stream(stream)), "fm_attn_bwd")
+    return dq, dk, dv
+
+
+def fm_localize(x, chunk_off, C: int, out=None, stream=None):
+    """Rank-local boundaries of any int32 boundary values x for chunks at chunk_off (ascending)."""
+    if x.dtype != torch.int32 or chunk_off.dtype != torch.int32 or not x.is_contiguous():
+        raise ValueError("x and chunk_off must be contiguous int32 CUDA tensors")
+    out = torch.empty_like(x) if out is None else out
+    _check(lib().fm_localize(_ptr(x), ctypes.c_int64(x.numel()), _ptr(chunk_off), int(chunk_off.numel()), int(C),
+                             _ptr(out), _stream(stream)), "fm_localize")
+    return out
+
+
+def fm_device_status(stream=None):
+    """(status, bits) of the device error word; synchronizes the stream and clears the word."""
+    bits = ctypes.c_int32(0)
+    st = lib().fm_device_status(_stream(stream), ctypes.byref(bits))
+    return st, bits.value
+
+
+def fm_selftest_wait_timeout(limit_us: int, stream=None):
+    _check(lib().fm_selftest_wait_timeout(ctypes.c_int64(limit_us), _stream(stream)), "fm_selftest_wait_timeout")
+
+
+class _FlashMaskFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, lts, lte, uts, ute, scale, causal):
+        bm, bn = attn_tiling()
+        queues = fm_classify_tiles(lts, lte, uts, ute, causal=causal, block_m=bm, block_n=bn)
+        o, lse = fm_attn_fwd(q, k, v, lts, lte, uts, ute, queues, scale=scale, causal=causal)
+        ctx.save_for_backward(q, k, v, o, lse, lts, lte, uts, ute)
+        ctx.queues, ctx.scale, ctx.causal = queues, scale, causal
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse, lts, lte, uts, ute = ctx.saved_tensors
+        dq, dk, dv = fm_attn_bwd(q, k, v, o, lse, do.contiguous(), lts, lte, uts, ute, ctx.queues, scale=ctx.scale,
+                                 causal=ctx.causal)
+        return dq, dk, dv, None, None, None, None, None, None
+
+
+def flashmask_attention(q, k, v, lts, lte, uts, ute, *, causal: bool, scale: float | None = None):
+    """Masked SDPA with the FlashMask column-wise mask; differentiable in q, k, v."""
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    return _FlashMaskFn.apply(q, k, v, lts, lte, uts, ute, float(scale), bool(causal))

@@ -1,0 +1,228 @@
+// fm_api.cu — the extern "C" boundary: argument validation, workspace
+// sizing, tensor-map encoding and the device error word. Every compute entry
+// point validates on the host, then enqueues kernels on the caller's stream.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include "fm_internal.h"
+
+namespace fm {
+
+// One error word per device; kernels OR FM_DEV_ERR_* bits into it.
+static __device__ int g_error_word = 0;
+
+int* device_error_word() {
+  static std::mutex mu;
+  static int* cached[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
+    cached[dev] = static_cast<int*>(ptr);
+  }
+  return cached[dev];
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool make_tmap_bhnd(void* out, const void* base, int64_t BH, int64_t N, int64_t d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)(d * 2), (cuuint64_t)(N * d * 2)};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(static_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace fm
+
+using namespace fm;
+
+namespace {
+
+bool valid_tile(int x) { return x == 32 || x == 64 || x == 128 || x == 256; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Shape checks shared by every attention-side call. *empty is set when there
+// is nothing to compute (B, H_q or N is zero).
+fm_status check_problem(const fm_problem* p, bool* empty) {
+  if (!p) return FM_ERR_INVALID_ARG;
+  if (p->B < 0 || p->H_q < 0 || p->H_kv < 0 || p->N < 0 || p->d <= 0) return FM_ERR_INVALID_ARG;
+  if (!std::isfinite(p->scale)) return FM_ERR_INVALID_ARG;
+  *empty = (p->B == 0 || p->H_q == 0 || p->N == 0);
+  if (*empty) return FM_OK;
+  if (p->H_kv == 0 || p->H_q % p->H_kv != 0) return FM_ERR_INVALID_ARG;
+  // int32 indexing limits of the kernels: rows of one head and heads per batch
+  if ((int64_t)p->B * p->H_q > (1 << 30) || (int64_t)p->N > (1 << 30)) return FM_ERR_UNSUPPORTED;
+  return FM_OK;
+}
+
+fm_status check_attn_shape(const fm_problem* p) {
+  if (p->d != 64 && p->d != 128) return FM_ERR_UNSUPPORTED;
+  return FM_OK;
+}
+
+fm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FM_OK : FM_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t fm_abi_version(void) { return FM_ABI_VERSION; }
+
+const char* fm_status_string(fm_status s) {
+  switch (s) {
+    case FM_OK: return "ok";
+    case FM_ERR_INVALID_ARG: return "invalid argument";
+    case FM_ERR_UNSUPPORTED: return "unsupported shape";
+    case FM_ERR_WORKSPACE: return "workspace missing or too small";
+    case FM_ERR_CUDA: return "CUDA error";
+    case FM_ERR_TIMEOUT: return "device wait timed out";
+    case FM_ERR_DEVICE: return "device reported bad input";
+  }
+  return "unknown status";
+}
+
+fm_status fm_attn_tiling(fm_tiling* out) {
+  if (!out) return FM_ERR_INVALID_ARG;
+  out->block_m = kTile;
+  out->block_n = kTile;
+  return FM_OK;
+}
+
+fm_status fm_tile_counts(const fm_problem* p, const fm_tiling* t, int32_t* nq, int32_t* nk) {
+  bool empty = false;
+  fm_status st = check_problem(p, &empty);
+  if (st != FM_OK) return st;
+  if (!t || !valid_tile(t->block_m) || !valid_tile(t->block_n) || !nq || !nk) return FM_ERR_INVALID_ARG;
+  *nq = (p->N + t->block_m - 1) / t->block_m;
+  *nk = (p->N + t->block_n - 1) / t->block_n;
+  return FM_OK;
+}
+
+size_t fm_classify_workspace_bytes(const fm_problem* p, const fm_tiling* t) {
+  int32_t nq = 0, nk = 0;
+  if (fm_tile_counts(p, t, &nq, &nk) != FM_OK) return 0;
+  return classify_ws_bytes(p->B, nq, nk);
+}
+
+fm_status fm_classify_tiles(const fm_problem* p, const fm_tiling* t, const int32_t* lts, const int32_t* lte,
+                            const int32_t* uts, const int32_t* ute, uint8_t* tile_class, int32_t* q_off,
+                            int32_t* q_queue, int32_t* k_off, int32_t* k_queue, void* ws, size_t ws_bytes,
+                            void* stream) {
+  int32_t nq = 0, nk = 0;
+  fm_status st = fm_tile_counts(p, t, &nq, &nk);
+  if (st != FM_OK) return st;
+  if (p->B == 0 || p->N == 0) return FM_OK;
+  if (!lts || !lte || !uts || !ute || !tile_class || !q_off || !q_queue || !k_off || !k_queue)
+    return FM_ERR_INVALID_ARG;
+  if ((int64_t)p->B * nq * nk > INT32_MAX) return FM_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < classify_ws_bytes(p->B, nq, nk)) return FM_ERR_WORKSPACE;
+  int* err = device_error_word();
+  if (!err) return FM_ERR_CUDA;
+  return from_cuda(launch_classify(*p, t->block_m, t->block_n, nq, nk, lts, lte, uts, ute, tile_class, q_off, q_queue,
+                                   k_off, k_queue, ws, static_cast<cudaStream_t>(stream), err));
+}
+
+size_t fm_attn_fwd_workspace_bytes(const fm_problem* p) {
+  bool empty = false;
+  if (check_problem(p, &empty) != FM_OK || empty) return 0;
+  return fwd_ws_bytes(*p);
+}
+
+fm_status fm_attn_fwd(const fm_problem* p, const void* q, const void* k, const void* v, const int32_t* lts,
+                      const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
+                      const int32_t* q_queue, void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  bool empty = false;
+  fm_status st = check_problem(p, &empty);
+  if (st != FM_OK || empty) return st;
+  if ((st = check_attn_shape(p)) != FM_OK) return st;
+  if (!q || !k || !v || !lts || !lte || !uts || !ute || !q_off || !q_queue || !o || !lse) return FM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FM_ERR_INVALID_ARG;
+  const size_t need = fwd_ws_bytes(*p);
+  if (need > 0 && (!ws || ws_bytes < need)) return FM_ERR_WORKSPACE;
+  int* err = device_error_word();
+  if (!err) return FM_ERR_CUDA;
+  return from_cuda(launch_fwd(*p, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws,
+                              static_cast<cudaStream_t>(stream), err));
+}
+
+size_t fm_attn_bwd_workspace_bytes(const fm_problem* p) {
+  bool empty = false;
+  if (check_problem(p, &empty) != FM_OK || empty) return 0;
+  return bwd_ws_bytes(*p);
+}
+
+fm_status fm_attn_bwd(const fm_problem* p, const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, const int32_t* lts, const int32_t* lte,
+                      const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
+                      void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+  bool empty = false;
+  fm_status st = check_problem(p, &empty);
+  if (st != FM_OK || empty) return st;
+  if ((st = check_attn_shape(p)) != FM_OK) return st;
+  if (!q || !k || !v || !o || !lse || !dout || !lts || !lte || !uts || !ute || !k_off || !k_queue || !dq || !dk ||
+      !dv)
+    return FM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv))
+    return FM_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < bwd_ws_bytes(*p)) return FM_ERR_WORKSPACE;
+  int* err = device_error_word();
+  if (!err) return FM_ERR_CUDA;
+  return from_cuda(launch_bwd(*p, q, k, v, o, lse, dout, lts, lte, uts, ute, k_off, k_queue, dq, dk, dv, ws,
+                              static_cast<cudaStream_t>(stream), err));
+}
+
+fm_status fm_localize(const int32_t* x_global, int64_t n, const int32_t* chunk_off, int32_t kappa, int32_t C,
+                      int32_t* x_local, void* stream) {
+  if (n < 0 || kappa < 1 || kappa > 4096 || C < 1) return FM_ERR_INVALID_ARG;
+  if (n == 0) return FM_OK;
+  if (!x_global || !chunk_off || !x_local) return FM_ERR_INVALID_ARG;
+  return from_cuda(launch_localize(x_global, n, chunk_off, kappa, C, x_local, static_cast<cudaStream_t>(stream)));
+}
+
+fm_status fm_device_status(void* stream, int32_t* bits) {
+  int* err = device_error_word();
+  if (!err) return FM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FM_ERR_CUDA;
+  int host = 0;
+  if (cudaMemcpy(&host, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FM_ERR_CUDA;
+  if (host != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FM_ERR_CUDA;
+  }
+  if (bits) *bits = host;
+  if (host == 0) return FM_OK;
+  return (host & FM_DEVERR_TIMEOUT) ? FM_ERR_TIMEOUT : FM_ERR_DEVICE;
+}
+
+fm_status fm_selftest_wait_timeout(int64_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 10000000) return FM_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (!err) return FM_ERR_CUDA;
+  return from_cuda(launch_wait_selftest((uint64_t)limit_us * 1000ull, static_cast<cudaStream_t>(stream), err));
+}
+
+}  // extern "C"

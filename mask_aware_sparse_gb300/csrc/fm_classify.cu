@@ -1,0 +1,217 @@
+// fm_classify.cu — tile classification and compacted queue construction.
+//
+// FlashMask-3 project page, §3.1: block-wise min/max of LTS/LTE/UTS/UTE
+// classify each (Q-block, KV-block) tile as skip / partial / unmasked and each
+// Q block gets a queue of valid KV blocks tagged partial or unmasked, visited
+// right to left. The rule (generalised to intervals that end inside the
+// sequence, plus the causal term) is stated in include/fm.h.
+//
+// Pipeline (all int32, all on the caller's stream):
+//   1. block_minmax   one warp per KV block: 8 reductions (min/max of the four
+//                     vectors), coalesced loads + warp-shuffle reductions.
+//   2. classify_rows  one CTA per (b, qb): class of every tile of the row,
+//                     count of non-skipped tiles.
+//   3. count_cols     one thread per (b, kb): non-skipped tiles of the column.
+//   4. scan           exclusive prefix sums -> q_off, k_off (one CTA).
+//   5. emit_rows      one warp per (b, qb): descending-kb compaction by ballot.
+//   6. emit_cols      one warp per (b, kb): ascending-qb compaction by ballot.
+#include <climits>
+#include "fm_internal.h"
+#include "sm100.cuh"
+
+namespace fm {
+namespace {
+
+struct Minmax {
+  int v[8];  // min LTS, max LTS, min LTE, max LTE, min UTS, max UTS, min UTE, max UTE
+};
+
+__device__ __forceinline__ int clamp_flag(int x, int n, bool& bad) {
+  if (x < 0) { bad = true; return 0; }
+  if (x > n) { bad = true; return n; }
+  return x;
+}
+
+__global__ void block_minmax_kernel(const int32_t* __restrict__ lts, const int32_t* __restrict__ lte,
+                                    const int32_t* __restrict__ uts, const int32_t* __restrict__ ute, int B, int N,
+                                    int bn, int nK, Minmax* __restrict__ out, int* err) {
+  const int wpb = blockDim.x >> 5;
+  const long long gw = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
+  if (gw >= (long long)B * nK) return;
+  const int lane = threadIdx.x & 31;
+  const int b = (int)(gw / nK), kb = (int)(gw % nK);
+  const int k0 = kb * bn, k1 = min(k0 + bn, N);
+  const size_t base = (size_t)b * N;
+  int mn[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX}, mx[4] = {INT_MIN, INT_MIN, INT_MIN, INT_MIN};
+  bool bad = false;
+  for (int j = k0 + lane; j < k1; j += 32) {
+    const int x[4] = {clamp_flag(lts[base + j], N, bad), clamp_flag(lte[base + j], N, bad),
+                      clamp_flag(uts[base + j], N, bad), clamp_flag(ute[base + j], N, bad)};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      mn[c] = min(mn[c], x[c]);
+      mx[c] = max(mx[c], x[c]);
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(err, FM_DEV_ERR_RANGE);
+  Minmax r;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    r.v[2 * c] = __reduce_min_sync(0xffffffffu, mn[c]);
+    r.v[2 * c + 1] = __reduce_max_sync(0xffffffffu, mx[c]);
+  }
+  if (lane == 0) out[gw] = r;
+}
+
+// Class of tile (q0,q1) x (k0,k1) from the block min/max.
+__device__ __forceinline__ uint8_t tile_class(const Minmax& m, int q0, int q1, int k0, int k1, int causal) {
+  const bool skip = (q0 >= m.v[1] && q1 <= m.v[2]) || (q0 >= m.v[5] && q1 <= m.v[6]) || (causal && q1 <= k0);
+  if (skip) return 0;
+  const bool unm = (q1 <= m.v[0] || q0 >= m.v[3]) && (q1 <= m.v[4] || q0 >= m.v[7]) && (!causal || q0 >= k1 - 1);
+  return unm ? 2 : 1;
+}
+
+__global__ void classify_rows_kernel(const Minmax* __restrict__ mm, int N, int bm, int bn, int nQ, int nK, int causal,
+                                     uint8_t* __restrict__ cls, int32_t* __restrict__ row_cnt) {
+  const int b = blockIdx.y, qb = blockIdx.x;
+  const int q0 = qb * bm, q1 = min(q0 + bm, N);
+  int cnt = 0;
+  uint8_t* crow = cls + ((size_t)b * nQ + qb) * nK;
+  for (int kb = threadIdx.x; kb < nK; kb += blockDim.x) {
+    const int k0 = kb * bn, k1 = min(k0 + bn, N);
+    const uint8_t c = tile_class(mm[(size_t)b * nK + kb], q0, q1, k0, k1, causal);
+    crow[kb] = c;
+    cnt += (c != 0);
+  }
+  cnt = __reduce_add_sync(0xffffffffu, cnt);
+  __shared__ int part[32];
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = cnt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += part[w];
+    row_cnt[(size_t)b * nQ + qb] = t;
+  }
+}
+
+__global__ void count_cols_kernel(const uint8_t* __restrict__ cls, int B, int nQ, int nK, int32_t* __restrict__ col_cnt) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= (long long)B * nK) return;
+  const int b = (int)(t / nK), kb = (int)(t % nK);
+  const uint8_t* c = cls + (size_t)b * nQ * nK + kb;
+  int cnt = 0;
+  for (int qb = 0; qb < nQ; ++qb) cnt += (c[(size_t)qb * nK] != 0);
+  col_cnt[t] = cnt;
+}
+
+// Exclusive scan of cnt[0..n) into off[0..n] by one CTA of 1024 threads.
+__device__ void block_exclusive_scan(const int32_t* __restrict__ cnt, int n, int32_t* __restrict__ off) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const int x = (i < n) ? cnt[i] : 0;
+    int incl = x;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += y;
+    }
+    if (lane == 31) warp_sums[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+      int ws = (lane < (int)(blockDim.x >> 5)) ? warp_sums[lane] : 0;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, ws, d);
+        if (lane >= d) ws += y;
+      }
+      warp_sums[lane] = ws;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = carry + (w > 0 ? warp_sums[w - 1] : 0);
+    if (i < n) off[i] = before + incl - x;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = before + incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) off[n] = carry;
+}
+
+__global__ void scan_kernel(const int32_t* row_cnt, int n_rows, int32_t* q_off, const int32_t* col_cnt, int n_cols,
+                            int32_t* k_off) {
+  if (blockIdx.x == 0)
+    block_exclusive_scan(row_cnt, n_rows, q_off);
+  else
+    block_exclusive_scan(col_cnt, n_cols, k_off);
+}
+
+__global__ void emit_rows_kernel(const uint8_t* __restrict__ cls, int B, int nQ, int nK, const int32_t* __restrict__ q_off,
+                                 int32_t* __restrict__ q_queue) {
+  const int wpb = blockDim.x >> 5;
+  const long long r = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
+  if (r >= (long long)B * nQ) return;
+  const int lane = threadIdx.x & 31;
+  const uint8_t* crow = cls + (size_t)r * nK;
+  int pos = q_off[r];
+  for (int top = nK - 1; top >= 0; top -= 32) {
+    const int kb = top - lane;  // descending within the chunk
+    const uint8_t c = (kb >= 0) ? crow[kb] : 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, c != 0);
+    if (c != 0) q_queue[pos + __popc(bal & ((1u << lane) - 1u))] = (kb << 1) | (c == 1 ? 1 : 0);
+    pos += __popc(bal);
+  }
+}
+
+__global__ void emit_cols_kernel(const uint8_t* __restrict__ cls, int B, int nQ, int nK, const int32_t* __restrict__ k_off,
+                                 int32_t* __restrict__ k_queue) {
+  const int wpb = blockDim.x >> 5;
+  const long long r = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
+  if (r >= (long long)B * nK) return;
+  const int lane = threadIdx.x & 31;
+  const int b = (int)(r / nK), kb = (int)(r % nK);
+  const uint8_t* ccol = cls + (size_t)b * nQ * nK + kb;
+  int pos = k_off[r];
+  for (int lo = 0; lo < nQ; lo += 32) {
+    const int qb = lo + lane;  // ascending
+    const uint8_t c = (qb < nQ) ? ccol[(size_t)qb * nK] : 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, c != 0);
+    if (c != 0) k_queue[pos + __popc(bal & ((1u << lane) - 1u))] = (qb << 1) | (c == 1 ? 1 : 0);
+    pos += __popc(bal);
+  }
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+size_t classify_ws_bytes(int B, int nQ, int nK) {
+  return align256(sizeof(Minmax) * (size_t)B * nK) + align256(4 * (size_t)B * nQ) + align256(4 * (size_t)B * nK);
+}
+
+cudaError_t launch_classify(const fm_problem& p, int bm, int bn, int nQ, int nK, const int32_t* lts,
+                            const int32_t* lte, const int32_t* uts, const int32_t* ute, uint8_t* tile_class,
+                            int32_t* q_off, int32_t* q_queue, int32_t* k_off, int32_t* k_queue, void* ws,
+                            cudaStream_t s, int* err) {
+  const int B = p.B, N = p.N;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  Minmax* mm = reinterpret_cast<Minmax*>(w);
+  w += align256(sizeof(Minmax) * (size_t)B * nK);
+  int32_t* row_cnt = reinterpret_cast<int32_t*>(w);
+  w += align256(4 * (size_t)B * nQ);
+  int32_t* col_cnt = reinterpret_cast<int32_t*>(w);
+
+  const long long nkb = (long long)B * nK, nqb = (long long)B * nQ;
+  block_minmax_kernel<<<(unsigned)((nkb + 7) / 8), 256, 0, s>>>(lts, lte, uts, ute, B, N, bn, nK, mm, err);
+  classify_rows_kernel<<<dim3(nQ, B), 256, 0, s>>>(mm, N, bm, bn, nQ, nK, p.causal, tile_class, row_cnt);
+  count_cols_kernel<<<(unsigned)((nkb + 255) / 256), 256, 0, s>>>(tile_class, B, nQ, nK, col_cnt);
+  scan_kernel<<<2, 1024, 0, s>>>(row_cnt, (int)nqb, q_off, col_cnt, (int)nkb, k_off);
+  emit_rows_kernel<<<(unsigned)((nqb + 7) / 8), 256, 0, s>>>(tile_class, B, nQ, nK, q_off, q_queue);
+  emit_cols_kernel<<<(unsigned)((nkb + 7) / 8), 256, 0, s>>>(tile_class, B, nQ, nK, k_off, k_queue);
+  return cudaGetLastError();
+}
+
+}  // namespace fm

@@ -1,0 +1,512 @@
+// fm_fwd.cu — masked attention forward on sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes: FlashMask-3 project page, §3.1 — only KV blocks in the
+// Q block's queue are loaded ("KV Loader"), scores, softmax and output are
+// computed per block and the row-interval mask is applied only on blocks
+// tagged partial ("MMA Consumer"). The online-softmax recurrence (running max
+// m, running sum l, rescale of O, final O / l) is the one of "Flash MSA
+// Attention Kernel Implementation", "The Flash Core: Tiling Over the Memory
+// Hierarchy".
+//
+// GB300 design (not the pages' Hopper design):
+//   * One CTA = one work unit = (batch b, Q block qb, a PAIR of query heads of
+//     the same GQA group). Both heads share the K/V head and the mask, so they
+//     share every K/V tile load and the same queue.
+//   * Warp roles (320 threads):
+//       warps 0-3  softmax for query tile 0 (one thread per query row)
+//       warps 4-7  softmax for query tile 1
+//       warp  8    producer: TMA loads of Q, K, V and the mask vectors of
+//                  partial blocks into shared memory rings
+//       warp  9    MMA issuer (one elected lane) and TMEM owner
+//   * TMEM (512 columns x 128 lanes): S_t at columns [128t, 128t+128); P_t is
+//     written back as bf16 over the first 64 columns of S_t and consumed from
+//     TMEM by the PV MMA; O_t at [256 + t*d, 256 + (t+1)*d).
+//   * The MMA warp interleaves the two tiles: PV_0(j-1), S_0(j), PV_1(j-1),
+//     S_1(j), so the tensor core works on one tile while softmax works on the
+//     other.
+//   * Rescaling of O is lazy: the running max used for exponentials only moves
+//     when the block max exceeds it by more than 8 (log2 units), so P <= 256;
+//     O and l are always scaled consistently, so O / l is unchanged.
+//   * Work units are launched longest-queue first (an LPT order computed on
+//     the device from the queue offsets).
+#include <climits>
+#include <cmath>
+#include <cuda.h>
+#include "fm_internal.h"
+#include "sm100.cuh"
+
+namespace fm {
+namespace {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int TILE = 128 * D * 2;  // bytes of one 128-row bf16 tile
+  static constexpr int BOXES = D / 64;     // 64-column TMA boxes per tile
+  static constexpr int STAGES = (D == 128) ? 2 : 4;
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + 2 * TILE;
+  static constexpr int V_OFF = K_OFF + STAGES * TILE;
+  static constexpr int M_OFF = V_OFF + STAGES * TILE;
+  static constexpr int M_BYTES = 128 * 16;  // int4 {LTS, LTE, UTS, UTE} per column
+  static constexpr int BAR_OFF = M_OFF + STAGES * M_BYTES;
+  static constexpr int B_QFULL = 0;
+  static constexpr int B_KFULL = 1;
+  static constexpr int B_KEMPTY = B_KFULL + STAGES;
+  static constexpr int B_VFULL = B_KEMPTY + STAGES;
+  static constexpr int B_VEMPTY = B_VFULL + STAGES;
+  static constexpr int B_MFULL = B_VEMPTY + STAGES;
+  static constexpr int B_MEMPTY = B_MFULL + STAGES;
+  static constexpr int B_SFULL = B_MEMPTY + STAGES;  // [2]
+  static constexpr int B_PREADY = B_SFULL + 2;       // [2]
+  static constexpr int B_ODONE = B_PREADY + 2;       // [2]
+  static constexpr int NBAR = B_ODONE + 2;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int BYTES = MISC_OFF + 16;
+  static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
+};
+
+struct FwdParams {
+  const int32_t* lts;
+  const int32_t* lte;
+  const int32_t* uts;
+  const int32_t* ute;
+  const int32_t* q_off;
+  const int32_t* q_queue;
+  const int32_t* order;
+  __nv_bfloat16* o;
+  float* lse;
+  int B, H_q, H_kv, N, nQ, nK, G, PG, causal;
+  float scale_log2;
+  int* err;
+};
+
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+  using C = FwdCfg<D>;
+  constexpr int S = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int units = p.H_kv * p.PG;
+  const int oi = blockIdx.x / units, gp = blockIdx.x - oi * units;
+  const int g = gp / p.PG, pp = gp - g * p.PG;
+  const int bq = p.order[oi];
+  const int b = bq / p.nQ, qb = bq - b * p.nQ;
+  const int h0 = g * p.G + 2 * pp;
+  const int T = (2 * pp + 1 < p.G) ? 2 : 1;
+  const int qbeg = p.q_off[bq];
+  const int n = p.q_off[bq + 1] - qbeg;
+  const int q0 = qb * 128;
+
+  if (n <= 0) {
+    // No visible key for any row of this unit: O = 0, LSE = -inf.
+    if (n < 0 && threadIdx.x == 0) record_error(p.err, FM_DEV_ERR_QUEUE);
+    if (warp < 8) {
+      const int t = warp >> 2, i = q0 + ((warp & 3) << 5) + lane;
+      if (t < T && i < p.N) {
+        const size_t bh = (size_t)b * p.H_q + h0 + t;
+        uint4* orow = reinterpret_cast<uint4*>(p.o + (bh * p.N + i) * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+        p.lse[bh * p.N + i] = -INFINITY;
+      }
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    // an unread timeout from an earlier launch: skip the work, keep the CTA cheap
+    *abort_flag = timeout_pending(p.err) ? 1 : 0;
+    mbar_init(&bars[C::B_QFULL], 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&bars[C::B_KFULL + s], 1);
+      mbar_init(&bars[C::B_KEMPTY + s], 1);
+      mbar_init(&bars[C::B_VFULL + s], 1);
+      mbar_init(&bars[C::B_VEMPTY + s], 1);
+      mbar_init(&bars[C::B_MFULL + s], 1);
+      mbar_init(&bars[C::B_MEMPTY + s], 4 * T);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars[C::B_SFULL + t], 1);
+      mbar_init(&bars[C::B_PREADY + t], 128);
+      mbar_init(&bars[C::B_ODONE + t], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 9) tmem_alloc<512>(tmem_slot);
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (*abort_flag) {
+    // fall through to teardown
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    bool ok = true;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars[C::B_QFULL], T * C::TILE);
+      for (int t = 0; t < T; ++t)
+        for (int x = 0; x < C::BOXES; ++x)
+          tma_load_3d(smem + C::Q_OFF + t * C::TILE + x * 16384, &tq, &bars[C::B_QFULL], x * 64, q0,
+                      b * p.H_q + h0 + t);
+    }
+    int pidx = 0;
+    const size_t vbase = (size_t)b * p.N;
+    for (int j = 0; j < n && ok; ++j) {
+      const int e = p.q_queue[qbeg + j];
+      const int kb = e >> 1;
+      if (kb < 0 || kb >= p.nK) {
+        if (lane == 0) record_error(p.err, FM_DEV_ERR_QUEUE);
+        *abort_flag = 1;
+        break;
+      }
+      const bool part = (e & 1) || (kb == p.nK - 1 && (p.N & 127));
+      const int slot = j % S;
+      const uint32_t ph = (uint32_t)(j / S) & 1u;
+      if (lane == 0) {
+        ok = mbar_wait(&bars[C::B_KEMPTY + slot], ph ^ 1u, abort_flag, p.err);
+        if (ok) {
+          mbar_arrive_expect_tx(&bars[C::B_KFULL + slot], C::TILE);
+          for (int x = 0; x < C::BOXES; ++x)
+            tma_load_3d(smem + C::K_OFF + slot * C::TILE + x * 16384, &tk, &bars[C::B_KFULL + slot], x * 64,
+                        kb * 128, b * p.H_kv + g);
+        }
+      }
+      ok = __shfl_sync(kFull, ok, 0);
+      if (!ok) break;
+      if (part) {
+        const int ms = pidx % S;
+        const uint32_t mph = (uint32_t)(pidx / S) & 1u;
+        ok = __all_sync(kFull, mbar_wait(&bars[C::B_MEMPTY + ms], mph ^ 1u, abort_flag, p.err));
+        if (!ok) break;
+        int4* sm = reinterpret_cast<int4*>(smem + C::M_OFF + ms * C::M_BYTES);
+        bool bad = false;
+        for (int c = lane; c < 128; c += 32) {
+          const int col = kb * 128 + c;
+          int4 v;
+          if (col < p.N) {
+            int a0 = p.lts[vbase + col], a1 = p.lte[vbase + col], u0 = p.uts[vbase + col], u1 = p.ute[vbase + col];
+            bad |= (a0 < 0) | (a0 > p.N) | (a1 < 0) | (a1 > p.N) | (u0 < 0) | (u0 > p.N) | (u1 < 0) | (u1 > p.N);
+            a0 = min(max(a0, 0), p.N);
+            a1 = min(max(a1, 0), p.N);
+            u0 = min(max(u0, 0), p.N);
+            u1 = min(max(u1, 0), p.N);
+            if (a0 >= a1) a0 = a1 = 0;  // empty interval
+            if (u0 >= u1) u0 = u1 = 0;
+            v = make_int4(a0, a1, u0, u1);
+          } else {
+            v = make_int4(0, INT_MAX, 0, 0);  // key beyond N: masked for every row
+          }
+          sm[c] = v;
+        }
+        if (__any_sync(kFull, bad) && lane == 0) record_error(p.err, FM_DEV_ERR_RANGE);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::B_MFULL + ms]);
+        ++pidx;
+      }
+      if (lane == 0) {
+        ok = mbar_wait(&bars[C::B_VEMPTY + slot], ph ^ 1u, abort_flag, p.err);
+        if (ok) {
+          mbar_arrive_expect_tx(&bars[C::B_VFULL + slot], C::TILE);
+          for (int x = 0; x < C::BOXES; ++x)
+            tma_load_3d(smem + C::V_OFF + slot * C::TILE + x * 16384, &tv, &bars[C::B_VFULL + slot], x * 64,
+                        kb * 128, b * p.H_kv + g);
+        }
+      }
+      ok = __shfl_sync(kFull, ok, 0);
+    }
+  } else if (warp == 9) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 0);  // S = Q K^T, both K-major
+      const uint32_t id_o = idesc_bf16_f32(128, D, 0, 1);    // O += P V, V is MN-major
+      const uint32_t sQ = smem_u32(smem + C::Q_OFF), sK = smem_u32(smem + C::K_OFF), sV = smem_u32(smem + C::V_OFF);
+      bool ok = mbar_wait(&bars[C::B_QFULL], 0, abort_flag, p.err);
+      tc_fence_after();
+      for (int j = 0; j <= n && ok; ++j) {
+        const int slot = j % S, pslot = (j + S - 1) % S;
+        if (j < n) {
+          ok = mbar_wait(&bars[C::B_KFULL + slot], (uint32_t)(j / S) & 1u, abort_flag, p.err);
+          tc_fence_after();
+        }
+        if (ok && j > 0) {
+          ok = mbar_wait(&bars[C::B_VFULL + pslot], (uint32_t)((j - 1) / S) & 1u, abort_flag, p.err);
+          tc_fence_after();
+        }
+        for (int t = 0; t < T && ok; ++t) {
+          const uint32_t tS = tbase + (uint32_t)(t * 128);
+          if (j > 0) {
+            ok = mbar_wait(&bars[C::B_PREADY + t], (uint32_t)(j - 1) & 1u, abort_flag, p.err);
+            tc_fence_after();
+            if (!ok) break;
+            const uint32_t tO = tbase + 256u + (uint32_t)(t * D);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t bd = sdesc_sw128(sV + pslot * C::TILE + k * 2048, 16384, 1024);
+              mma_ts(tO, tS + (uint32_t)(k * 8), bd, id_o, (j > 1 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars[C::B_ODONE + t]);
+          }
+          if (j < n) {
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t off = (uint32_t)((k >> 2) * 16384 + (k & 3) * 32);
+              const uint64_t ad = sdesc_sw128(sQ + t * C::TILE + off, 16, 1024);
+              const uint64_t bd = sdesc_sw128(sK + slot * C::TILE + off, 16, 1024);
+              mma_ss(tS, ad, bd, id_s, k > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars[C::B_SFULL + t]);
+          }
+        }
+        if (ok) {
+          if (j > 0) mma_commit(&bars[C::B_VEMPTY + pslot]);
+          if (j < n) mma_commit(&bars[C::B_KEMPTY + slot]);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;
+    if (t < T) {
+      const int row = ((warp & 3) << 5) + lane;
+      const int i = q0 + row;
+      const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+      const uint32_t tS = tbase + lane_off + (uint32_t)(t * 128);
+      const uint32_t tO = tbase + lane_off + 256u + (uint32_t)(t * D);
+      const float sl2 = p.scale_log2;
+      float m_run = -INFINITY, l_run = 0.f;
+      int pidx = 0;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int e = p.q_queue[qbeg + j];
+        const int kb = e >> 1;
+        const bool part = (e & 1) || (kb == p.nK - 1 && (p.N & 127));
+        ok = __all_sync(kFull, mbar_wait(&bars[C::B_SFULL + t], (uint32_t)j & 1u, abort_flag, p.err));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[128];
+        {
+          uint32_t(&r0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+          uint32_t(&r1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+          uint32_t(&r2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
+          uint32_t(&r3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
+          tmem_ld32(tS + 0, r0);
+          tmem_ld32(tS + 32, r1);
+          tmem_ld32(tS + 64, r2);
+          tmem_ld32(tS + 96, r3);
+          tmem_ld_wait();
+        }
+        if (part) {
+          const int ms = pidx % S;
+          ok = __all_sync(kFull, mbar_wait(&bars[C::B_MFULL + ms], (uint32_t)(pidx / S) & 1u, abort_flag, p.err));
+          if (!ok) break;
+          const int4* sm = reinterpret_cast<const int4*>(smem + C::M_OFF + ms * C::M_BYTES);
+          const int kc0 = kb * 128;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int4 v = sm[c];
+            const bool msk = ((unsigned)(i - v.x) < (unsigned)(v.y - v.x)) |
+                             ((unsigned)(i - v.z) < (unsigned)(v.w - v.z)) | (p.causal && i < kc0 + c);
+            if (msk) sr[c] = __float_as_uint(-INFINITY);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[C::B_MEMPTY + ms]);
+          ++pidx;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+        const float m_blk = mx * sl2;
+        const float m_new = fmaxf(m_run, m_blk);
+        const bool resc = m_new > m_run + 8.0f;
+        float factor = 1.f;
+        if (resc) {
+          factor = ex2_approx(m_run - m_new);
+          m_run = m_new;
+        }
+        const float msafe = (m_run == -INFINITY) ? 0.f : m_run;
+        float rs = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float a = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -msafe));
+          const float bb = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -msafe));
+          rs += a + bb;
+          pk[c] = pack_bf16x2(a, bb);
+        }
+        l_run = l_run * factor + rs;
+        {
+          const uint32_t(&p0)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]);
+          const uint32_t(&p1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]);
+          const uint32_t(&p2)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pk[32]);
+          const uint32_t(&p3)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pk[48]);
+          tmem_st16(tS + 0, p0);
+          tmem_st16(tS + 16, p1);
+          tmem_st16(tS + 32, p2);
+          tmem_st16(tS + 48, p3);
+          tmem_st_wait();
+        }
+        if (j > 0 && __any_sync(kFull, resc)) {
+          // O holds PV of blocks < j: wait for the last of them, then rescale the row.
+          ok = __all_sync(kFull, mbar_wait(&bars[C::B_ODONE + t], (uint32_t)(j - 1) & 1u, abort_flag, p.err));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(tO + c0, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * factor);
+            tmem_st32(tO + c0, r);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(&bars[C::B_PREADY + t]);
+      }
+      if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_ODONE + t], (uint32_t)(n - 1) & 1u, abort_flag, p.err));
+      if (ok) {
+        tc_fence_after();
+        const size_t bh = (size_t)b * p.H_q + h0 + t;
+        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(tO + c0, r);
+          tmem_ld_wait();
+          if (i < p.N) {
+            uint4* dst = reinterpret_cast<uint4*>(p.o + (bh * p.N + i) * D + c0);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              const float* f = reinterpret_cast<const float*>(&r[8 * v4]);
+              dst[v4] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
+                                   pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+            }
+          }
+        }
+        if (i < p.N) p.lse[bh * p.N + i] = (l_run > 0.f) ? (m_run * kLn2 + logf(l_run)) : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc<512>(tbase);
+  }
+}
+
+// Longest-queue-first order of the B*nQ query blocks (one CTA, bitonic sort of
+// (queue length, -index) keys, descending). Larger problems keep index order.
+constexpr int kMaxSort = 4096;
+
+__global__ void __launch_bounds__(1024) lpt_order_kernel(const int32_t* __restrict__ off, int count,
+                                                         int32_t* __restrict__ order) {
+  __shared__ unsigned long long key[kMaxSort];
+  if (count > kMaxSort) {
+    for (int i = threadIdx.x; i < count; i += blockDim.x) order[i] = i;
+    return;
+  }
+  int n2 = 1;
+  while (n2 < count) n2 <<= 1;
+  for (int i = threadIdx.x; i < n2; i += blockDim.x)
+    key[i] = (i < count) ? (((unsigned long long)(uint32_t)(off[i + 1] - off[i]) << 32) | (0xFFFFFFFFu - (uint32_t)i))
+                         : 0ull;
+  __syncthreads();
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int ixj = i ^ jj;
+        if (ixj > i) {
+          const bool desc = (i & k) == 0;
+          const unsigned long long a = key[i], c = key[ixj];
+          if ((a < c) == desc) {
+            key[i] = c;
+            key[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < count; i += blockDim.x) order[i] = (int32_t)(0xFFFFFFFFu - (uint32_t)key[i]);
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const fm_problem& P, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdParams& prm, unsigned grid, cudaStream_t s) {
+  using C = FwdCfg<D>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  fwd_kernel<D><<<grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t fwd_ws_bytes(const fm_problem& p) {
+  const size_t nQ = (size_t)(p.N + kTile - 1) / kTile;
+  return ((4 * (size_t)p.B * nQ) + 255) & ~size_t(255);
+}
+
+cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const void* v, const int32_t* lts,
+                       const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
+                       const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err) {
+  const int nQ = (P.N + kTile - 1) / kTile;
+  const int G = P.H_q / P.H_kv;
+  const int PG = (G + 1) / 2;
+  const long long grid = (long long)P.B * nQ * P.H_kv * PG;
+  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
+  int32_t* order = static_cast<int32_t*>(ws);
+  lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, P.B * nQ, order);
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bhnd(&tq, q, (int64_t)P.B * P.H_q, P.N, P.d) || !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, P.N, P.d) ||
+      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, P.N, P.d))
+    return cudaErrorInvalidValue;
+  FwdParams prm;
+  prm.lts = lts;
+  prm.lte = lte;
+  prm.uts = uts;
+  prm.ute = ute;
+  prm.q_off = q_off;
+  prm.q_queue = q_queue;
+  prm.order = order;
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.B = P.B;
+  prm.H_q = P.H_q;
+  prm.H_kv = P.H_kv;
+  prm.N = P.N;
+  prm.nQ = nQ;
+  prm.nK = nQ;
+  prm.G = G;
+  prm.PG = PG;
+  prm.causal = P.causal ? 1 : 0;
+  prm.scale_log2 = P.scale * 1.4426950408889634f;
+  prm.err = err;
+  if (P.d == 128) return launch_fwd_d<128>(P, tq, tk, tv, prm, (unsigned)grid, s);
+  return launch_fwd_d<64>(P, tq, tk, tv, prm, (unsigned)grid, s);
+}
+
+}  // namespace fm

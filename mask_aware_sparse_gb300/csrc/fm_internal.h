@@ -1,0 +1,45 @@
+// fm_internal.h — declarations shared by the library's translation units.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include "../../include/fm.h"
+
+namespace fm {
+
+// Device error word of the current device (address of a __device__ int).
+int* device_error_word();
+
+// Classification (fm_classify.cu).
+size_t classify_ws_bytes(int B, int nQ, int nK);
+cudaError_t launch_classify(const fm_problem& p, int bm, int bn, int nQ, int nK, const int32_t* lts,
+                            const int32_t* lte, const int32_t* uts, const int32_t* ute, uint8_t* tile_class,
+                            int32_t* q_off, int32_t* q_queue, int32_t* k_off, int32_t* k_queue, void* ws,
+                            cudaStream_t s, int* err);
+
+// Localization (fm_localize.cu).
+cudaError_t launch_localize(const int32_t* x, int64_t n, const int32_t* off, int kappa, int C, int32_t* out,
+                            cudaStream_t s);
+
+// Bounded-wait self-test (fm_localize.cu).
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s, int* err);
+
+// Forward (fm_fwd.cu).
+size_t fwd_ws_bytes(const fm_problem& p);
+cudaError_t launch_fwd(const fm_problem& p, const void* q, const void* k, const void* v, const int32_t* lts,
+                       const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
+                       const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err);
+
+// Backward (fm_bwd.cu).
+size_t bwd_ws_bytes(const fm_problem& p);
+cudaError_t launch_bwd(const fm_problem& p, const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, const int32_t* lts, const int32_t* lte,
+                       const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
+                       void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err);
+
+// Tensor maps (fm_api.cu): 3-D bf16 map over a contiguous (BH, N, d) tensor,
+// box {64, 128, 1}, 128-byte swizzle; rows >= N read as zero.
+bool make_tmap_bhnd(void* out_tmap /* CUtensorMap* */, const void* base, int64_t BH, int64_t N, int64_t d);
+
+constexpr int kTile = 128;  // attention tile (block_m = block_n)
+
+}  // namespace fm

@@ -1,0 +1,101 @@
+"""The C ABI library: it builds, loads, exports every declared symbol, and its
+host-side validation rejects bad calls without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mask_aware_sparse_gb300 as fm
+from mask_aware_sparse_gb300 import build as fmbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fmbuild.build()
+    return fm.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "fm.h")).read()
+    return sorted(set(re.findall(r"\b(fm_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_symbols_exported(lib):
+    names = _declared()
+    assert "fm_attn_fwd" in names and "fm_classify_tiles" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    # the binding declares exactly the header's entry points
+    assert sorted(fm.EXPORTS) == names
+
+
+def test_abi_version(lib):
+    assert lib.fm_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert len(fm.status_string(s)) > 0
+
+
+def test_tile_counts_host_only(lib):
+    p = fm._problem(2, 4, 2, 1000, 128, 0.1, 1)
+    t = fm.fm_tiling(128, 64)
+    nq, nk = ctypes.c_int32(), ctypes.c_int32()
+    assert lib.fm_tile_counts(ctypes.byref(p), ctypes.byref(t), ctypes.byref(nq), ctypes.byref(nk)) == fm.FM_OK
+    assert (nq.value, nk.value) == (8, 16)
+    bad = fm.fm_tiling(100, 64)
+    assert lib.fm_tile_counts(ctypes.byref(p), ctypes.byref(bad), ctypes.byref(nq), ctypes.byref(nk)) == \
+        fm.FM_ERR_INVALID_ARG
+
+
+def test_attn_tiling(lib):
+    assert fm.attn_tiling() == (128, 128)
+
+
+def test_validation_rejects_before_any_launch(lib):
+    P = ctypes.POINTER(fm.fm_problem)
+    nul = ctypes.c_void_p(0)
+    # H_q not a multiple of H_kv
+    p = fm._problem(1, 6, 4, 256, 128, 0.1, 1)
+    args = [nul] * 11 + [nul, ctypes.c_size_t(0), nul]
+    assert lib.fm_attn_fwd(ctypes.byref(p), *args) == fm.FM_ERR_INVALID_ARG
+    # unsupported head dim
+    p = fm._problem(1, 4, 2, 256, 96, 0.1, 1)
+    assert lib.fm_attn_fwd(ctypes.byref(p), *args) == fm.FM_ERR_UNSUPPORTED
+    # null tensors
+    p = fm._problem(1, 4, 2, 256, 128, 0.1, 1)
+    assert lib.fm_attn_fwd(ctypes.byref(p), *args) == fm.FM_ERR_INVALID_ARG
+    bargs = [nul] * 15 + [nul, ctypes.c_size_t(0), nul]
+    assert lib.fm_attn_bwd(ctypes.byref(p), *bargs) == fm.FM_ERR_INVALID_ARG
+    # negative sizes
+    p = fm._problem(1, 4, 2, -5, 128, 0.1, 1)
+    assert lib.fm_attn_fwd(ctypes.byref(p), *args) == fm.FM_ERR_INVALID_ARG
+    # non-finite scale
+    p = fm._problem(1, 4, 2, 256, 128, float("nan"), 1)
+    assert lib.fm_attn_fwd(ctypes.byref(p), *args) == fm.FM_ERR_INVALID_ARG
+    # null problem
+    assert lib.fm_attn_fwd(P(), *args) == fm.FM_ERR_INVALID_ARG
+
+
+def test_empty_problems_are_noops(lib):
+    nul = ctypes.c_void_p(0)
+    for shape in ((0, 4, 2, 256), (1, 0, 2, 256), (1, 4, 2, 0)):
+        p = fm._problem(*shape, 128, 0.1, 1)
+        args = [nul] * 11 + [nul, ctypes.c_size_t(0), nul]
+        assert lib.fm_attn_fwd(ctypes.byref(p), *args) == fm.FM_OK
+        bargs = [nul] * 15 + [nul, ctypes.c_size_t(0), nul]
+        assert lib.fm_attn_bwd(ctypes.byref(p), *bargs) == fm.FM_OK
+    assert lib.fm_localize(nul, 0, nul, 1, 4, nul, nul) == fm.FM_OK
+    assert lib.fm_localize(nul, 10, nul, 0, 4, nul, nul) == fm.FM_ERR_INVALID_ARG
+
+
+def test_workspace_queries(lib):
+    p = fm._problem(1, 32, 8, 32768, 128, 0.1, 1)
+    t = fm.fm_tiling(128, 128)
+    assert lib.fm_classify_workspace_bytes(ctypes.byref(p), ctypes.byref(t)) > 0
+    assert lib.fm_attn_fwd_workspace_bytes(ctypes.byref(p)) >= 4 * 256
+    assert lib.fm_attn_bwd_workspace_bytes(ctypes.byref(p)) > 0
