@@ -1,10 +1,647 @@
-// fm_bwd.cu — placeholder until the backward kernels land.
+// fm_bwd.cu — masked attention backward on sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes ("Flash MSA Attention Kernel Implementation", "The
+// Backward Pass: The Real Beast"; the mask and tile skipping of FlashMask-3
+// project page §3.1): with P recomputed from the forward's LSE,
+//   P = exp(scale S - LSE), dV = P^T dO, dP = dO V^T, D = rowsum(dO * O),
+//   dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q,
+// visiting only the tiles in each KV block's queue and masking only partial
+// tiles; dK and dV are summed over the query heads of each GQA group.
+//
+// Kernels:
+//   bwd_pre_kernel   D_i = sum_c dO_ic O_ic and the exponent offset
+//                    -LSE_i*log2(e) per query row (padded rows: -inf, 0);
+//   bwd_kernel       one CTA per (batch, kv head, 128-row KV block), looping
+//                    over every query head of the group and every queued Q
+//                    block in two 64-row halves;
+//   dq_convert       dQ = bf16(scale * dQacc).
+//
+// bwd_kernel (320 threads):
+//   warps 0-3  compute: thread j owns KV row j (its mask boundaries live in
+//              registers); reads S^T and dP^T rows from TMEM, writes P^T and
+//              dS^T (bf16) back to TMEM and dS^T to shared memory;
+//   warps 4-7  dQ drain: thread c owns TMEM lane c = head-dim index c of
+//              dQ^T; reduces it into the fp32 dQ accumulator with coalesced
+//              128-byte atomic adds; also stores dK at the end;
+//   warp 8     TMA producer (K, V once; Q, dO, LSE offsets, D per unit);
+//   warp 9     tcgen05 MMA issuer.
+// Per unit u (64 query rows) the MMAs are, all with M = 128:
+//   S^T  = K Q^T           (TMEM S[u&1], 64 columns)
+//   dP^T = V dO^T          (TMEM dP, 64 columns)
+//   dV  += P^T dO          (A = P^T from TMEM)
+//   dK  += dS^T Q          (A = dS^T from TMEM)
+//   dQ^T = K^T dS^T        (A = K^T, B = dS^T: both MN-major from shared memory)
+// TMEM: S[0] [0,64) S[1] [64,128) dP [128,192) dQ^T [192,256)
+//       dV [256, 256+d) dK [256+d, 256+2d).
+// Issue order per iteration: S(u+1); wait compute(u); dV(u), dK(u); dP(u+1);
+// wait drain(u-1); dQ^T(u). The tensor core works on S(u+1) while the
+// compute warps work on unit u.
+#include <climits>
+#include <cmath>
+#include <cuda.h>
 #include "fm_internal.h"
+#include "sm100.cuh"
+
 namespace fm {
-size_t bwd_ws_bytes(const fm_problem& p) { return 256; }
-cudaError_t launch_bwd(const fm_problem&, const void*, const void*, const void*, const void*, const float*,
-                       const void*, const int32_t*, const int32_t*, const int32_t*, const int32_t*,
-                       const int32_t*, const int32_t*, void*, void*, void*, void*, cudaStream_t, int*) {
-  return cudaErrorNotSupported;
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int KV_TILE = 128 * D * 2;  // K or V block: 128 rows
+  static constexpr int Q_TILE = 64 * D * 2;    // Q or dO half block: 64 rows
+  static constexpr int BOXES = D / 64;
+  static constexpr int STAGES = 3;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + KV_TILE;
+  static constexpr int Q_OFF = V_OFF + KV_TILE;
+  static constexpr int DO_OFF = Q_OFF + STAGES * Q_TILE;
+  static constexpr int DS_OFF = DO_OFF + STAGES * Q_TILE;  // 2 x (128 rows x 128 B)
+  static constexpr int ZERO_OFF = DS_OFF + 2 * 16384;      // d = 64 only: 16 KB of zeros
+  static constexpr int ZERO_BYTES = (D == 64) ? 16384 : 0;
+  static constexpr int ROW_OFF = ZERO_OFF + ZERO_BYTES;    // STAGES x {nl[64], D[64]} fp32
+  static constexpr int BAR_OFF = ROW_OFF + STAGES * 512;
+  static constexpr int B_KV = 0;
+  static constexpr int B_QFULL = 1;
+  static constexpr int B_QEMPTY = B_QFULL + STAGES;
+  static constexpr int B_SFULL = B_QEMPTY + STAGES;  // [2]
+  static constexpr int B_DPFULL = B_SFULL + 2;
+  static constexpr int B_READY = B_DPFULL + 1;
+  static constexpr int B_DQFULL = B_READY + 1;
+  static constexpr int B_DQEMPTY = B_DQFULL + 1;
+  static constexpr int B_FINAL = B_DQEMPTY + 1;
+  static constexpr int NBAR = B_FINAL + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int BYTES = MISC_OFF + 16;
+  static constexpr int SMEM_ALLOC = BYTES + 1024;
+};
+
+struct BwdParams {
+  const int32_t* lts;
+  const int32_t* lte;
+  const int32_t* uts;
+  const int32_t* ute;
+  const int32_t* k_off;
+  const int32_t* k_queue;
+  const int32_t* order;
+  const float* nl;    // (B*H_q, Npad): -LSE*log2(e), -inf for empty / padded rows
+  const float* dsum;  // (B*H_q, Npad): D = rowsum(dO * O)
+  float* dq_acc;      // (B*H_q, N, d) fp32
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int B, H_q, H_kv, N, Npad, nK, G, causal;
+  float scale, scale_log2;
+  int* err;
+};
+
+// Decode unit u of a CTA: query head (h) of the group, queue position, half.
+struct Unit {
+  int h, qb, half, part;
+};
+__device__ __forceinline__ Unit decode_unit(const BwdParams& p, int u, int L, int kbeg, int g, bool force_part) {
+  Unit r;
+  const int hi = u / (2 * L);
+  const int rem = u - hi * 2 * L;
+  const int e = p.k_queue[kbeg + (rem >> 1)];
+  r.h = g * p.G + hi;
+  r.qb = e >> 1;
+  r.half = rem & 1;
+  r.part = (e & 1) | (force_part ? 1 : 0);
+  return r;
 }
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int S = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int oi = blockIdx.x / p.H_kv, g = blockIdx.x - oi * p.H_kv;
+  const int bk = p.order[oi];
+  const int nK = p.nK;
+  const int b = bk / nK, kb = bk - b * nK;
+  const int kbeg = p.k_off[bk];
+  const int L = p.k_off[bk + 1] - kbeg;
+  const int U = 2 * L * p.G;
+  const int k0 = kb * 128;
+  const bool force_part = (kb == nK - 1) && (p.N & 127);
+
+  if (U <= 0) {
+    // No query row sees this KV block: dK = dV = 0.
+    if (L < 0 && threadIdx.x == 0) record_error(p.err, FM_DEV_ERR_QUEUE);
+    if (warp < 4) {
+      const int j = k0 + (warp << 5) + lane;
+      if (j < p.N) {
+        const size_t row = ((size_t)b * p.H_kv + g) * p.N + j;
+        uint4* a = reinterpret_cast<uint4*>(p.dk + row * D);
+        uint4* c = reinterpret_cast<uint4*>(p.dv + row * D);
+#pragma unroll
+        for (int x = 0; x < D / 8; ++x) a[x] = c[x] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    *abort_flag = timeout_pending(p.err) ? 1 : 0;
+    mbar_init(&bars[C::B_KV], 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&bars[C::B_QFULL + s], 1);
+      mbar_init(&bars[C::B_QEMPTY + s], 1);
+    }
+    mbar_init(&bars[C::B_SFULL + 0], 1);
+    mbar_init(&bars[C::B_SFULL + 1], 1);
+    mbar_init(&bars[C::B_DPFULL], 1);
+    mbar_init(&bars[C::B_READY], 128);
+    mbar_init(&bars[C::B_DQFULL], 1);
+    mbar_init(&bars[C::B_DQEMPTY], 128);
+    mbar_init(&bars[C::B_FINAL], 1);
+    fence_mbar_init();
+  }
+  if (C::ZERO_BYTES > 0) {
+    uint4* z = reinterpret_cast<uint4*>(smem + C::ZERO_OFF);
+    for (int x = threadIdx.x; x < C::ZERO_BYTES / 16; x += blockDim.x) z[x] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
+  if (warp == 9) tmem_alloc<512>(tmem_slot);
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    tma_prefetch_desc(&tdo);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  constexpr uint32_t T_S0 = 0, T_DP = 128, T_DQ = 192, T_DV = 256, T_DK = 256 + D;
+
+  if (*abort_flag) {
+    // an unread timeout from an earlier launch: skip the work
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(&bars[C::B_KV], 2 * C::KV_TILE);
+      for (int x = 0; x < C::BOXES; ++x) {
+        tma_load_3d(smem + C::K_OFF + x * 16384, &tk, &bars[C::B_KV], x * 64, k0, b * p.H_kv + g);
+        tma_load_3d(smem + C::V_OFF + x * 16384, &tv, &bars[C::B_KV], x * 64, k0, b * p.H_kv + g);
+      }
+      for (int u = 0; u < U && ok; ++u) {
+        const Unit un = decode_unit(p, u, L, kbeg, g, force_part);
+        const int stage = u % S;
+        ok = mbar_wait(&bars[C::B_QEMPTY + stage], ((uint32_t)(u / S) & 1u) ^ 1u, abort_flag, p.err);
+        if (!ok) break;
+        const int r0 = un.qb * 128 + un.half * 64;
+        const int bh = b * p.H_q + un.h;
+        uint64_t* fb = &bars[C::B_QFULL + stage];
+        mbar_arrive_expect_tx(fb, 2 * C::Q_TILE + 512);
+        for (int x = 0; x < C::BOXES; ++x) {
+          tma_load_3d(smem + C::Q_OFF + stage * C::Q_TILE + x * 8192, &tq, fb, x * 64, r0, bh);
+          tma_load_3d(smem + C::DO_OFF + stage * C::Q_TILE + x * 8192, &tdo, fb, x * 64, r0, bh);
+        }
+        bulk_load(smem + C::ROW_OFF + stage * 512, p.nl + (size_t)bh * p.Npad + r0, 256, fb);
+        bulk_load(smem + C::ROW_OFF + stage * 512 + 256, p.dsum + (size_t)bh * p.Npad + r0, 256, fb);
+      }
+    }
+  } else if (warp == 9) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);  // S^T, dP^T: A K-major, B K-major
+      const uint32_t id_g = idesc_bf16_f32(128, D, 0, 1);   // dV, dK: A from TMEM, B MN-major
+      const uint32_t id_q = idesc_bf16_f32(128, 64, 1, 1);  // dQ^T: A MN-major, B MN-major
+      const uint32_t sK = smem_u32(smem + C::K_OFF), sV = smem_u32(smem + C::V_OFF);
+      const uint32_t sQ = smem_u32(smem + C::Q_OFF), sdO = smem_u32(smem + C::DO_OFF);
+      const uint32_t sdS = smem_u32(smem + C::DS_OFF);
+      const uint32_t lbo_kt = (D == 128) ? 16384u : (uint32_t)(C::ZERO_OFF - C::K_OFF);
+      bool ok = mbar_wait(&bars[C::B_KV], 0, abort_flag, p.err);
+      tc_fence_after();
+      // S^T(u) = K Q_u^T or dP^T(u) = V dO_u^T into TMEM column `dst`
+      auto issue_sk = [&](uint32_t a_base, uint32_t b_base, uint32_t dst) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(b_base + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
+          mma_ss(tbase + dst, ad, bd, id_s, k > 0 ? 1u : 0u);
+        }
+      };
+      if (ok) {
+        ok = mbar_wait(&bars[C::B_QFULL + 0], 0, abort_flag, p.err);
+        tc_fence_after();
+      }
+      if (ok) {
+        issue_sk(sK, sQ, T_S0);
+        mma_commit(&bars[C::B_SFULL + 0]);
+        issue_sk(sV, sdO, T_DP);
+        mma_commit(&bars[C::B_DPFULL]);
+      }
+      for (int u = 0; u < U && ok; ++u) {
+        const int stage = u % S;
+        const int nstage = (u + 1) % S;
+        if (u + 1 < U) {
+          ok = mbar_wait(&bars[C::B_QFULL + nstage], (uint32_t)((u + 1) / S) & 1u, abort_flag, p.err);
+          tc_fence_after();
+          if (!ok) break;
+          issue_sk(sK, sQ + nstage * C::Q_TILE, T_S0 + 64u * ((u + 1) & 1));
+          mma_commit(&bars[C::B_SFULL + ((u + 1) & 1)]);
+        }
+        ok = mbar_wait(&bars[C::B_READY], (uint32_t)u & 1u, abort_flag, p.err);
+        tc_fence_after();
+        if (!ok) break;
+        const uint32_t tP = tbase + T_S0 + 64u * (u & 1);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {  // 64 query rows = 4 k-steps; P^T, dS^T are 32 packed columns
+          const uint64_t bdo = sdesc_sw128(sdO + stage * C::Q_TILE + k * 2048, 8192, 1024);
+          mma_ts(tbase + T_DV, tP + k * 8, bdo, id_g, (u > 0 || k > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t bq = sdesc_sw128(sQ + stage * C::Q_TILE + k * 2048, 8192, 1024);
+          mma_ts(tbase + T_DK, tbase + T_DP + k * 8, bq, id_g, (u > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars[C::B_QEMPTY + stage]);
+        if (u + 1 < U) {
+          issue_sk(sV, sdO + nstage * C::Q_TILE, T_DP);
+          mma_commit(&bars[C::B_DPFULL]);
+        }
+        if (u >= 1) {
+          ok = mbar_wait(&bars[C::B_DQEMPTY], (uint32_t)(u - 1) & 1u, abort_flag, p.err);
+          tc_fence_after();
+          if (!ok) break;
+        }
+        const uint32_t sdsu = sdS + 16384u * (u & 1);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // 128 KV rows
+          const uint64_t ad = sdesc_sw128(sK + k * 2048, lbo_kt, 1024);
+          const uint64_t bd = sdesc_sw128(sdsu + k * 2048, 8192, 1024);
+          mma_ss(tbase + T_DQ, ad, bd, id_q, k > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[C::B_DQFULL]);
+      }
+      if (ok) mma_commit(&bars[C::B_FINAL]);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ compute
+    const int j = (warp << 5) + lane;  // KV row within the block = TMEM lane
+    const int kcol = k0 + j;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    int lo0 = 0, lo1 = 0, up0 = 0, up1 = 0;
+    bool dead = kcol >= p.N;
+    if (!dead) {
+      const size_t vi = (size_t)b * p.N + kcol;
+      int a0 = p.lts[vi], a1 = p.lte[vi], u0 = p.uts[vi], u1 = p.ute[vi];
+      if ((a0 | a1 | u0 | u1) < 0 || a0 > p.N || a1 > p.N || u0 > p.N || u1 > p.N) record_error(p.err, FM_DEV_ERR_RANGE);
+      a0 = min(max(a0, 0), p.N);
+      a1 = min(max(a1, 0), p.N);
+      u0 = min(max(u0, 0), p.N);
+      u1 = min(max(u1, 0), p.N);
+      if (a0 < a1) { lo0 = a0; lo1 = a1; }
+      if (u0 < u1) { up0 = u0; up1 = u1; }
+    }
+    const unsigned lw = (unsigned)(lo1 - lo0), uw = (unsigned)(up1 - up0);
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int u = 0; u < U && ok; ++u) {
+      const Unit un = decode_unit(p, u, L, kbeg, g, force_part);
+      const int stage = u % S;
+      const int r0 = un.qb * 128 + un.half * 64;
+      ok = __all_sync(kFull, mbar_wait(&bars[C::B_QFULL + stage], (uint32_t)(u / S) & 1u, abort_flag, p.err));
+      if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_SFULL + (u & 1)], (uint32_t)(u >> 1) & 1u, abort_flag, p.err));
+      if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_DPFULL], (uint32_t)u & 1u, abort_flag, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      const float* s_nl = reinterpret_cast<const float*>(smem + C::ROW_OFF + stage * 512);
+      const float* s_d = s_nl + 64;
+      const uint32_t tS = tbase + lane_off + T_S0 + 64u * (u & 1);
+      const uint32_t tDP = tbase + lane_off + T_DP;
+      uint8_t* dsrow = smem + C::DS_OFF + 16384 * (u & 1) + (j >> 3) * 1024 + (j & 7) * 128;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {  // two chunks of 32 query rows
+        uint32_t sv[32], pv[32];
+        tmem_ld32(tS + 32 * c, sv);
+        tmem_ld32(tDP + 32 * c, pv);
+        tmem_ld_wait();
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int r = 0; r < 32; r += 2) {
+          float pp[2], dd[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int rr = 32 * c + r + e;
+            const int i = r0 + rr;
+            float x = fmaf(__uint_as_float(sv[r + e]), sl2, s_nl[rr]);
+            if (un.part) {
+              const bool msk = dead | ((unsigned)(i - lo0) < lw) | ((unsigned)(i - up0) < uw) | (p.causal && i < kcol);
+              if (msk) x = -INFINITY;
+            }
+            const float pr = ex2_approx(x);
+            pp[e] = pr;
+            dd[e] = pr * (__uint_as_float(pv[r + e]) - s_d[rr]);
+          }
+          pk[r >> 1] = pack_bf16x2(pp[0], pp[1]);
+          dk[r >> 1] = pack_bf16x2(dd[0], dd[1]);
+        }
+        tmem_st16(tS + 16 * c, pk);
+        tmem_st16(tDP + 16 * c, dk);
+        // dS^T row j, query columns [32c, 32c+32): four 16-byte chunks, 128-byte swizzle
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chunk = 4 * c + q4;
+          *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (j & 7)) << 4)) =
+              make_uint4(dk[4 * q4], dk[4 * q4 + 1], dk[4 * q4 + 2], dk[4 * q4 + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars[C::B_READY]);
+    }
+    // epilogue: dV rows
+    if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_FINAL], 0, abort_flag, p.err));
+    if (ok) {
+      tc_fence_after();
+      const size_t row = ((size_t)b * p.H_kv + g) * p.N + kcol;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tbase + lane_off + T_DV + c0, r);
+        tmem_ld_wait();
+        if (!dead) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dv + row * D + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const float* f = reinterpret_cast<const float*>(&r[8 * v4]);
+            dst[v4] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                                 pack_bf16x2(f[6], f[7]));
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain
+    const int w4 = warp - 4;
+    const int c = (w4 << 5) + lane;  // head-dim index = TMEM lane
+    const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
+    bool ok = true;
+    for (int u = 0; u < U && ok; ++u) {
+      const Unit un = decode_unit(p, u, L, kbeg, g, force_part);
+      ok = __all_sync(kFull, mbar_wait(&bars[C::B_DQFULL], (uint32_t)u & 1u, abort_flag, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v0[32], v1[32];
+      tmem_ld32(tbase + lane_off + T_DQ, v0);
+      tmem_ld32(tbase + lane_off + T_DQ + 32, v1);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bars[C::B_DQEMPTY]);
+      if (c < D) {
+        const int r0 = un.qb * 128 + un.half * 64;
+        float* dst = p.dq_acc + ((size_t)(b * p.H_q + un.h) * p.N + r0) * D + c;
+        const int nrow = min(64, p.N - r0);
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          if (r < nrow) atomicAdd(dst + (size_t)r * D, __uint_as_float(v0[r]));
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          if (32 + r < nrow) atomicAdd(dst + (size_t)(32 + r) * D, __uint_as_float(v1[r]));
+      }
+    }
+    // epilogue: dK rows (thread = KV row j = TMEM lane)
+    if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_FINAL], 0, abort_flag, p.err));
+    if (ok) {
+      tc_fence_after();
+      const int j = c;
+      const int kcol = k0 + j;
+      const size_t row = ((size_t)b * p.H_kv + g) * p.N + kcol;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tbase + lane_off + T_DK + c0, r);
+        tmem_ld_wait();
+        if (kcol < p.N) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dk + row * D + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const float* f = reinterpret_cast<const float*>(&r[8 * v4]);
+            const float s = p.scale;
+            dst[v4] = make_uint4(pack_bf16x2(f[0] * s, f[1] * s), pack_bf16x2(f[2] * s, f[3] * s),
+                                 pack_bf16x2(f[4] * s, f[5] * s), pack_bf16x2(f[6] * s, f[7] * s));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc<512>(tbase);
+  }
+}
+
+// D_i = sum_c dO_ic O_ic and nl_i = -LSE_i log2(e) (-inf for empty rows);
+// padded rows (N <= i < Npad) get nl = -inf, D = 0. One warp per row.
+template <int D>
+__global__ void bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                               const float* __restrict__ lse, int BH, int N, int Npad, float* __restrict__ nl,
+                               float* __restrict__ dsum) {
+  const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (w >= (long long)BH * Npad) return;
+  const int lane = threadIdx.x & 31;
+  const int bh = (int)(w / Npad), i = (int)(w % Npad);
+  float acc = 0.f, nlv = -INFINITY;
+  if (i < N) {
+    const size_t base = ((size_t)bh * N + i) * D;
+    constexpr int PER = D / 32;  // 2 or 4 bf16 per lane
+    if (PER == 4) {
+      const uint2 a = *reinterpret_cast<const uint2*>(o + base + 4 * lane);
+      const uint2 c = *reinterpret_cast<const uint2*>(dout + base + 4 * lane);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(c2[e]);
+        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+      }
+    } else {
+      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base + 2 * lane);
+      const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(dout + base + 2 * lane);
+      const float2 x = __bfloat1622float2(a), y = __bfloat1622float2(c);
+      acc = fmaf(x.x, y.x, x.y * y.y);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+    const float l = lse[(size_t)bh * N + i];
+    nlv = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+  }
+  if (lane == 0) {
+    nl[(size_t)bh * Npad + i] = nlv;
+    dsum[(size_t)bh * Npad + i] = (i < N) ? acc : 0.f;
+  }
+}
+
+__global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long long n8,
+                                  float scale) {
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n8; t += (long long)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * t];
+    const float4 c = reinterpret_cast<const float4*>(acc)[2 * t + 1];
+    reinterpret_cast<uint4*>(dq)[t] =
+        make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                   pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
+  }
+}
+
+// Longest-queue-first order of (b, kb) by KV queue length (shared with the
+// forward's design: one CTA bitonic sort; identity order beyond kMaxSort).
+constexpr int kMaxSort = 4096;
+__global__ void __launch_bounds__(1024) lpt_order_kernel_bwd(const int32_t* __restrict__ off, int count,
+                                                             int32_t* __restrict__ order) {
+  __shared__ unsigned long long key[kMaxSort];
+  if (count > kMaxSort) {
+    for (int i = threadIdx.x; i < count; i += blockDim.x) order[i] = i;
+    return;
+  }
+  int n2 = 1;
+  while (n2 < count) n2 <<= 1;
+  for (int i = threadIdx.x; i < n2; i += blockDim.x)
+    key[i] = (i < count) ? (((unsigned long long)(uint32_t)(off[i + 1] - off[i]) << 32) | (0xFFFFFFFFu - (uint32_t)i))
+                         : 0ull;
+  __syncthreads();
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int ixj = i ^ jj;
+        if (ixj > i) {
+          const bool desc = (i & k) == 0;
+          const unsigned long long a = key[i], c = key[ixj];
+          if ((a < c) == desc) {
+            key[i] = c;
+            key[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < count; i += blockDim.x) order[i] = (int32_t)(0xFFFFFFFFu - (uint32_t)key[i]);
+}
+
+inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct BwdWs {
+  float* dq_acc;
+  float* nl;
+  float* dsum;
+  int32_t* order;
+};
+
+BwdWs carve(const fm_problem& P, void* ws) {
+  const size_t nK = (size_t)(P.N + kTile - 1) / kTile;
+  const size_t Npad = nK * kTile;
+  const size_t BH = (size_t)P.B * P.H_q;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  BwdWs r;
+  r.dq_acc = reinterpret_cast<float*>(w);
+  w += a256(BH * P.N * P.d * 4);
+  r.nl = reinterpret_cast<float*>(w);
+  w += a256(BH * Npad * 4);
+  r.dsum = reinterpret_cast<float*>(w);
+  w += a256(BH * Npad * 4);
+  r.order = reinterpret_cast<int32_t*>(w);
+  return r;
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, const BwdParams& prm0, const BwdWs& w,
+                         cudaStream_t s) {
+  using C = BwdCfg<D>;
+  const int nK = prm0.nK;
+  const long long BH = (long long)P.B * P.H_q;
+  // 1. row terms and a zeroed dQ accumulator
+  cudaError_t e = cudaMemsetAsync(w.dq_acc, 0, (size_t)BH * P.N * D * sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  const long long rows = BH * prm0.Npad;
+  bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                                              static_cast<const __nv_bfloat16*>(dout), lse, (int)BH,
+                                                              P.N, prm0.Npad, w.nl, w.dsum);
+  // 2. LPT order of KV blocks
+  lpt_order_kernel_bwd<<<1, 1024, 0, s>>>(prm0.k_off, P.B * nK, w.order);
+  // 3. main kernel
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_bhnd(&tq, q, BH, P.N, D, 64) || !make_tmap_bhnd(&tdo, dout, BH, P.N, D, 64) ||
+      !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, P.N, D, 128) ||
+      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, P.N, D, 128))
+    return cudaErrorInvalidValue;
+  static bool attr_done = false;
+  if (!attr_done) {
+    e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const long long grid = (long long)P.B * nK * P.H_kv;
+  bwd_kernel<D><<<(unsigned)grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, prm0);
+  // 4. dQ = bf16(scale * dQacc)
+  const long long n8 = BH * P.N * D / 8;
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  dq_convert_kernel<<<(unsigned)blocks, 256, 0, s>>>(w.dq_acc, static_cast<__nv_bfloat16*>(dq), n8, P.scale);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_ws_bytes(const fm_problem& P) {
+  const size_t nK = (size_t)(P.N + kTile - 1) / kTile;
+  const size_t Npad = nK * kTile;
+  const size_t BH = (size_t)P.B * P.H_q;
+  return a256(BH * P.N * P.d * 4) + 2 * a256(BH * Npad * 4) + a256(4 * (size_t)P.B * nK);
+}
+
+cudaError_t launch_bwd(const fm_problem& P, const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, const int32_t* lts, const int32_t* lte,
+                       const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
+                       void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err) {
+  const int nK = (P.N + kTile - 1) / kTile;
+  const long long grid = (long long)P.B * nK * P.H_kv;
+  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
+  const BwdWs w = carve(P, ws);
+  BwdParams prm;
+  prm.lts = lts;
+  prm.lte = lte;
+  prm.uts = uts;
+  prm.ute = ute;
+  prm.k_off = k_off;
+  prm.k_queue = k_queue;
+  prm.order = w.order;
+  prm.nl = w.nl;
+  prm.dsum = w.dsum;
+  prm.dq_acc = w.dq_acc;
+  prm.dk = static_cast<__nv_bfloat16*>(dk);
+  prm.dv = static_cast<__nv_bfloat16*>(dv);
+  prm.B = P.B;
+  prm.H_q = P.H_q;
+  prm.H_kv = P.H_kv;
+  prm.N = P.N;
+  prm.Npad = nK * kTile;
+  prm.nK = nK;
+  prm.G = P.H_q / P.H_kv;
+  prm.causal = P.causal ? 1 : 0;
+  prm.scale = P.scale;
+  prm.scale_log2 = P.scale * kLog2e;
+  prm.err = err;
+  return (P.d == 128) ? launch_bwd_d<128>(P, q, k, v, o, lse, dout, dq, prm, w, s)
+                      : launch_bwd_d<64>(P, q, k, v, o, lse, dout, dq, prm, w, s);
+}
+
 }  // namespace fm

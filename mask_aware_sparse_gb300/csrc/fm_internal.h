@@ -37,8 +37,9 @@ cudaError_t launch_bwd(const fm_problem& p, const void* q, const void* k, const 
                        void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err);
 
 // Tensor maps (fm_api.cu): 3-D bf16 map over a contiguous (BH, N, d) tensor,
-// box {64, 128, 1}, 128-byte swizzle; rows >= N read as zero.
-bool make_tmap_bhnd(void* out_tmap /* CUtensorMap* */, const void* base, int64_t BH, int64_t N, int64_t d);
+// box {64, box_rows, 1}, 128-byte swizzle; rows >= N read as zero.
+bool make_tmap_bhnd(void* out_tmap /* CUtensorMap* */, const void* base, int64_t BH, int64_t N, int64_t d,
+                    int box_rows = 128);
 
 constexpr int kTile = 128;  // attention tile (block_m = block_n)
 
