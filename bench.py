@@ -1,0 +1,497 @@
+#!/usr/bin/env python
+"""Benchmark: fwd+bwd effective TFLOP/s of FlashMask column-wise masked attention on GB300.
+
+One step = the whole hot path over one batch of synthetic input: tile
+classification + queues, mask localization (a 2-rank chunking, the utility
+row), forward, backward (row terms, main kernel, dQ convert). The metric counts
+only unmasked (i, j) pairs: 4*d FLOPs each for the forward and 10*d for the
+backward, per query head.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+Prints ONE JSON line on rank 0. Under torchrun every rank runs its own replica
+of the workload (weak scaling, no collective on the data path); the time is
+the max over ranks and the value the sum of all ranks' work over that time.
+--impl reference times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import configs, tensors  # noqa: E402
+
+DEFAULT_WORKLOAD = "share_question32k"
+METRIC = "effective TFLOP/s (unmasked FLOPs) fwd+bwd, % of GB300 BF16 peak; tile-skip %"
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB of L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ metric
+def visible_pairs(lts, lte, uts, ute, causal: bool) -> int:
+    """Unmasked (i, j) pairs of one (N,) mask: N*N minus, per key column, the
+    length of the union of its masked row intervals (inclusion-exclusion)."""
+    n = lts.shape[0]
+    j = np.arange(n, dtype=np.int64)
+    a = [lts.astype(np.int64), uts.astype(np.int64), np.zeros(n, np.int64)]
+    b = [lte.astype(np.int64), ute.astype(np.int64), j if causal else np.zeros(n, np.int64)]
+    length = lambda lo, hi: np.maximum(0, hi - lo)
+    tot = sum(length(a[k], b[k]) for k in range(3))
+    for x in range(3):
+        for y in range(x + 1, 3):
+            tot = tot - length(np.maximum(a[x], a[y]), np.minimum(b[x], b[y]))
+    tot = tot + length(np.maximum(np.maximum(a[0], a[1]), a[2]), np.minimum(np.minimum(b[0], b[1]), b[2]))
+    return int(n * n - tot.sum())
+
+
+def workload_flops(cfg) -> dict:
+    pairs = sum(visible_pairs(cfg["lts"][b], cfg["lte"][b], cfg["uts"][b], cfg["ute"][b], cfg["causal"])
+                for b in range(cfg["B"]))
+    per_head = pairs
+    d, hq = cfg["d"], cfg["H_q"]
+    return dict(pairs=pairs, fwd=per_head * 4 * d * hq, bwd=per_head * 10 * d * hq)
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background (timestamps kept)."""
+
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 50):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", f"-lms={period_ms}",
+                 f"--id={index}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        inside = [r for (t, r) in self.rows if t0 <= t <= t1 and len(r) >= 9]
+        scope = "timed region"
+        if not inside:
+            inside = [r for (_, r) in self.rows if len(r) >= 9]
+            scope = "whole run (no sample fell inside the timed region)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "scope": "nvidia-smi unavailable"}
+        sm = [num(r[2]) for r in inside if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in inside for k in range(4) if r[5 + k].lower().startswith("active")})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": num(inside[0][3]),
+                "reasons": reasons, "samples": len(inside), "scope": scope,
+                "power_w_max": max((num(r[4]) or 0.0) for r in inside)}
+
+
+# ------------------------------------------------------------- distributed
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, use_cuda):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl" if use_cuda else "gloo")
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_flops: float, per_rank_seconds: float, world: int, device) -> tuple:
+    """(total work over all ranks, max time over ranks) — the weak-scaling value is their ratio."""
+    t = reduce_max(per_rank_seconds, world, device)
+    return per_rank_flops * world, t
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+# ---------------------------------------------------------- oracle baseline
+def closed_blocks(cfg):
+    """Row ranges that only see, and are only seen by, themselves (documents /
+    packed samples): each is an independent sub-problem of the workload."""
+    if "samples" in cfg:
+        out, s = [], 0
+        for p, a, b in cfg["samples"]:
+            out.append((s, s + p + a + b))
+            s += p + a + b
+        return out
+    if "docs" in cfg and cfg["causal"]:
+        out, s = [], 0
+        for L in cfg["docs"]:
+            out.append((s, s + L))
+            s += L
+        return out
+    return None
+
+
+def sub_vectors(cfg, block):
+    """Boundary vectors of a closed block as its own problem (rows renumbered from 0)."""
+    r0, r1 = block
+    L = r1 - r0
+    return tuple(np.clip(cfg[n][0][r0:r1].astype(np.int64) - r0, 0, L).astype(np.int32)[None]
+                 for n in ("lts", "lte", "uts", "ute"))
+
+
+def oracle_unit(cfg, q, k, v, do, h, block):
+    """fwd + bwd of one query head on one closed block with the CPU oracle.
+
+    A closed block is an independent sub-problem (its rows see only its keys
+    and its keys are seen only by its rows), so the oracle runs on the block's
+    own rows, keys and renumbered boundary vectors; the result equals the full
+    problem's restricted to the block. Returns (effective FLOPs, seconds)."""
+    import oracle  # test infrastructure: only the CPU-baseline leg uses it
+
+    r0, r1 = block
+    g = h // (cfg["H_q"] // cfg["H_kv"])
+    vec = sub_vectors(cfg, block)
+    f64 = lambda t: np.ascontiguousarray(t.double().numpy())
+    qq, dd = f64(q[:1, h:h + 1, r0:r1]), f64(do[:1, h:h + 1, r0:r1])
+    kk, vv = f64(k[:1, g:g + 1, r0:r1]), f64(v[:1, g:g + 1, r0:r1])
+    t0 = time.perf_counter()
+    oracle.forward(qq, kk, vv, vec, cfg["causal"], cfg["scale"])
+    oracle.backward(qq, kk, vv, dd, vec, cfg["causal"], cfg["scale"])
+    dt = time.perf_counter() - t0
+    pairs = visible_pairs(*(x[0] for x in vec), cfg["causal"])
+    return pairs * 14 * cfg["d"], dt
+
+
+def cores_used() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_inputs(cfg):
+    small = dict(cfg)
+    return tensors.make_qkvdo(small)  # CPU draws (seeds 1..4)
+
+
+def cpu_baseline(cfg, budget_s: float = 12.0):
+    blocks = closed_blocks(cfg)
+    if not blocks:
+        return None
+    q, k, v, do = cpu_inputs(cfg)
+    flops = secs = 0.0
+    units = 0
+    order = sorted(range(len(blocks)), key=lambda i: blocks[i][1] - blocks[i][0])
+    for h in range(cfg["H_q"]):
+        for bi in order:
+            f, t = oracle_unit(cfg, q, k, v, do, h, blocks[bi])
+            flops += f
+            secs += t
+            units += 1
+            if secs >= budget_s:
+                break
+        if secs >= budget_s:
+            break
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+            "sample": f"{units} (query head, packed sample) fwd+bwd units of {cfg['name']}, "
+                      f"{secs:.1f} s of fp64 numpy on the host (BLAS threads = cores)"}
+
+
+def run_reference(args, cfg):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    blocks = closed_blocks(cfg)
+    if not blocks:
+        print(json.dumps({"impl": "reference", "unavailable": f"no closed sub-problem sample for {cfg['name']}"}))
+        return 0
+    q, k, v, do = cpu_inputs(cfg)
+    units = [(h, bi) for h in range(cfg["H_q"]) for bi in range(len(blocks))]
+    smallest = min(range(len(blocks)), key=lambda i: blocks[i][1] - blocks[i][0])
+    for w in range(args.warmup):
+        oracle_unit(cfg, q, k, v, do, w % cfg["H_q"], blocks[smallest])
+    flops = secs = 0.0
+    for s in range(args.steps):
+        h, bi = units[s % len(units)]
+        f, t = oracle_unit(cfg, q, k, v, do, h, blocks[bi])
+        flops += f
+        secs += t
+    val = flops / secs / 1e12
+    peaks, src = read_peaks()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(cfg, "per step: one (query head, packed sample) fwd+bwd unit, cycling"),
+        "pct_of_bf16_peak": 100.0 * val / peaks["bf16_tflops"],
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": f"{args.steps} units of one query head x one packed sample (fp64 numpy)"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_dict(cfg, note=""):
+    d = {"workload": cfg["name"], "B": cfg["B"], "H_q": cfg["H_q"], "H_kv": cfg["H_kv"], "N": cfg["N"],
+         "d": cfg["d"], "causal": bool(cfg["causal"]), "tile": [128, 128], "mask_seed": 0,
+         "tensor_seeds": "Q,K,V,dO: torch CUDA generators 1..4, N(0,1) -> bf16",
+         "l2": "flushed between timed steps (256 MiB write)"}
+    if note:
+        d["note"] = note
+    return d
+
+
+# -------------------------------------------------------------- our arm
+class Path:
+    """Preallocated buffers and the step = classify, localize, forward, backward."""
+
+    def __init__(self, cfg, dev):
+        import mask_aware_sparse_gb300 as fm
+
+        self.fm = fm
+        self.cfg = cfg
+        self.dev = dev
+        self.q, self.k, self.v, self.do = tensors.make_qkvdo(cfg, device=dev)
+        self.vec = [torch.from_numpy(np.ascontiguousarray(cfg[n])).to(dev) for n in ("lts", "lte", "uts", "ute")]
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = torch.empty_like(self.q), torch.empty_like(self.k), torch.empty_like(self.v)
+        n = cfg["N"]
+        C = (n + 7) // 8  # 8 chunks, a 2-rank round-robin chunking; rank 0 owns chunks 0, 2, 4, 6
+        self.loc_off = torch.tensor([0, 2 * C, 4 * C, 6 * C], dtype=torch.int32, device=dev)
+        self.loc_C = C
+        self.loc_in = torch.cat([x.reshape(-1) for x in self.vec])
+        self.loc_out = torch.empty_like(self.loc_in)
+        self.queues = None
+
+    def step(self):
+        fm, c = self.fm, self.cfg
+        self.queues = fm.fm_classify_tiles(*self.vec, causal=c["causal"])
+        fm.fm_localize(self.loc_in, self.loc_off, self.loc_C, out=self.loc_out)
+        fm.fm_attn_fwd(self.q, self.k, self.v, *self.vec, self.queues, scale=c["scale"], causal=c["causal"],
+                       o=self.o, lse=self.lse)
+        fm.fm_attn_bwd(self.q, self.k, self.v, self.o, self.lse, self.do, *self.vec, self.queues, scale=c["scale"],
+                       causal=c["causal"], dq=self.dq, dk=self.dk, dv=self.dv)
+
+
+def e2e_measure(path: Path, steps: int):
+    """Same metric through the public API from pinned HOST buffers: each step
+    copies the inputs host->device, runs the path and reads every output back."""
+    fm, c, dev = path.fm, path.cfg, path.dev
+    h_in = [t.cpu().pin_memory() for t in (path.q, path.k, path.v, path.do)]
+    h_vec = [t.cpu().pin_memory() for t in path.vec]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (path.o, path.lse, path.dq, path.dk, path.dv)]
+    d_in = [torch.empty_like(t, device=dev) for t in h_in]
+    d_vec = [torch.empty_like(t, device=dev) for t in h_vec]
+    h2d = sum(t.numel() * t.element_size() for t in h_in + h_vec)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def one():
+        for d, h in zip(d_in + d_vec, h_in + h_vec):
+            d.copy_(h, non_blocking=True)
+        q, k, v, do = d_in
+        qs = fm.fm_classify_tiles(*d_vec, causal=c["causal"])
+        o, lse = fm.fm_attn_fwd(q, k, v, *d_vec, qs, scale=c["scale"], causal=c["causal"])
+        dq, dk, dv = fm.fm_attn_bwd(q, k, v, o, lse, do, *d_vec, qs, scale=c["scale"], causal=c["causal"])
+        for h, d in zip(h_out, (o, lse, dq, dk, dv)):
+            h.copy_(d, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / steps, h2d, d2h
+
+
+def run_ours(args, cfg):
+    world, rank, local = dist_info()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, True)
+    from mask_aware_sparse_gb300 import build as fmbuild
+
+    if rank == 0:
+        fmbuild.build()
+    barrier(world)
+    path = Path(cfg, dev)
+    fm = path.fm
+    work = workload_flops(cfg)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    for _ in range(max(3, args.warmup)):
+        path.step()
+    torch.cuda.synchronize()
+    st, bits = fm.fm_device_status()
+    if st != fm.FM_OK:
+        print(json.dumps({"error": f"device status {st} bits {bits} after warm-up"}))
+        return 1
+    fm.fm_profile_read()  # clear
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    fm.fm_profile_enable(True)
+    launches0 = fm.fm_launch_count()
+    t_wall0 = time.time()
+    for k in range(args.steps):
+        flush.zero_()  # evict L2 between timed steps (outside the events)
+        ev[k][0].record()
+        path.step()
+        ev[k][1].record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    launches = fm.fm_launch_count() - launches0
+    fm.fm_profile_enable(False)
+    prof = fm.fm_profile_read()
+    st, bits = fm.fm_device_status()
+    if sampler:
+        sampler.stop()
+    step_s = sum(a.elapsed_time(b) for a, b in ev) / 1e3
+    flops_rank = (work["fwd"] + work["bwd"]) * args.steps
+    tot_flops, tmax = aggregate(flops_rank, step_s, world, dev)
+    value = tot_flops / tmax / 1e12
+
+    e2e_s, h2d, d2h = e2e_measure(path, max(3, min(20, args.steps // 5)))
+    e2e_s = reduce_max(e2e_s, world, dev)
+    e2e_value = (work["fwd"] + work["bwd"]) * world / e2e_s / 1e12
+
+    if rank != 0:
+        return 0
+    peaks, src = read_peaks()
+    cls = path.queues.tile_class.cpu().numpy()
+    counts = np.bincount(cls.ravel(), minlength=3)
+    computed = int(counts[1] + counts[2])
+    fwd_ms = prof["fwd_ms"] / max(1, prof["fwd_launches"])
+    bwd_ms = prof["bwd_ms"] / max(1, prof["bwd_launches"])
+    dom = "bwd" if bwd_ms >= fwd_ms else "fwd"
+    dom_ms = bwd_ms if dom == "bwd" else fwd_ms
+    dom_flops = work[dom]
+    achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = ncu_traffic(dom)
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": tmax / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(cfg),
+        "pct_of_bf16_peak": 100.0 * value / world / peak,
+        "peak_source": f"{src}: bf16_tflops {peak} (burst); sustained {peaks.get('bf16_tflops_sustained')}",
+        "tile_skip_pct": 100.0 * counts[0] / cls.size,
+        "tiles": {"skip": int(counts[0]), "partial": int(counts[1]), "unmasked": int(counts[2])},
+        "computed_tile_tflops": computed * 128 * 128 * 14 * cfg["d"] * cfg["H_q"] * cfg["B"] * args.steps / step_s / 1e12,
+        "kernel_ms": {"fwd_main": fwd_ms, "bwd_main": bwd_ms,
+                      "rest_of_step": tmax / args.steps * 1e3 - fwd_ms - bwd_ms},
+        "roofline": {"kernel": "fm_attn_bwd main" if dom == "bwd" else "fm_attn_fwd main", "bound": "tensor",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": traffic,
+                     "algorithmic": f"{'10' if dom == 'bwd' else '4'}*d FLOPs x {work['pairs']} unmasked pairs x "
+                                    f"{cfg['H_q']} heads per launch"},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "device_status": int(st),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg)
+    print(json.dumps(line))
+    return 0
+
+
+# ncu DRAM traffic (read + write bytes per launch) of the main kernels, valid
+# only while the kernel source is the one the counters were taken from.
+NCU_TRAFFIC = {}
+
+
+def ncu_traffic(kind: str):
+    import hashlib
+
+    ent = NCU_TRAFFIC.get(kind)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "mask_aware_sparse_gb300", "csrc", ent["file"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return ent["bytes"] if h == ent["sha256"] else None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=configs.NAMES)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    cfg = configs.make(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

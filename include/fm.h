@@ -175,6 +175,23 @@ fm_status fm_device_status(void* stream, int32_t* bits);
  * timeout path without hanging or faulting the GPU. */
 fm_status fm_selftest_wait_timeout(int64_t limit_us, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Measurement hooks (no effect on results).
+ *
+ * fm_profile_enable(1): from now on every launch of the forward main kernel
+ * (kind 0) and of the backward main kernel (kind 1) is bracketed by a pair of
+ * CUDA events recorded on its launch stream. fm_profile_enable(0) stops it.
+ * fm_profile_read synchronizes on the recorded events and returns, per kind,
+ * the summed device milliseconds and the number of launches since the last
+ * read, then clears the record. Pointers may be NULL. Host-thread safe.
+ *
+ * fm_launch_count: total number of kernels this library has launched in the
+ * process (every compute entry point counts each kernel it enqueues).
+ * ------------------------------------------------------------------------- */
+fm_status fm_profile_enable(int32_t on);
+fm_status fm_profile_read(double* fwd_ms, int32_t* fwd_launches, double* bwd_ms, int32_t* bwd_launches);
+int64_t fm_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -8,7 +8,8 @@ is no silent fallback.
 
 Functions carry the names of the C entry points:
   fm_classify_tiles, fm_attn_fwd, fm_attn_bwd, fm_localize, fm_device_status,
-  fm_selftest_wait_timeout, plus flashmask_attention (autograd wrapper: the
+  fm_selftest_wait_timeout, fm_profile_enable, fm_profile_read, fm_launch_count,
+  plus flashmask_attention (autograd wrapper: the
 classification, forward and backward calls in one differentiable op).
 """
 from __future__ import annotations
@@ -60,6 +61,10 @@ _SIGS = {
     "fm_localize": (ctypes.c_int, [_P, ctypes.c_int64, _P, ctypes.c_int32, ctypes.c_int32, _P, _P]),
     "fm_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "fm_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, _P]),
+    "fm_profile_enable": (ctypes.c_int, [ctypes.c_int32]),
+    "fm_profile_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32),
+                                       ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)]),
+    "fm_launch_count": (ctypes.c_int64, []),
 }
 EXPORTS = tuple(_SIGS)
 
@@ -215,6 +220,22 @@ def fm_device_status(stream=None):
 
 def fm_selftest_wait_timeout(limit_us: int, stream=None):
     _check(lib().fm_selftest_wait_timeout(ctypes.c_int64(limit_us), _stream(stream)), "fm_selftest_wait_timeout")
+
+
+def fm_profile_enable(on: bool):
+    _check(lib().fm_profile_enable(1 if on else 0), "fm_profile_enable")
+
+
+def fm_profile_read():
+    """{'fwd_ms', 'fwd_launches', 'bwd_ms', 'bwd_launches'} since the last read (synchronizes)."""
+    fm_, fl, bm_, bl = ctypes.c_double(), ctypes.c_int32(), ctypes.c_double(), ctypes.c_int32()
+    _check(lib().fm_profile_read(ctypes.byref(fm_), ctypes.byref(fl), ctypes.byref(bm_), ctypes.byref(bl)),
+           "fm_profile_read")
+    return dict(fwd_ms=fm_.value, fwd_launches=fl.value, bwd_ms=bm_.value, bwd_launches=bl.value)
+
+
+def fm_launch_count() -> int:
+    return int(lib().fm_launch_count())
 
 
 class _FlashMaskFn(torch.autograd.Function):

@@ -1,9 +1,11 @@
 // fm_api.cu — the extern "C" boundary: argument validation, workspace
 // sizing, tensor-map encoding and the device error word. Every compute entry
 // point validates on the host, then enqueues kernels on the caller's stream.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include "fm_internal.h"
@@ -52,6 +54,49 @@ bool make_tmap_bhnd(void* out, const void* base, int64_t BH, int64_t N, int64_t 
                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- measurement
+namespace {
+std::atomic<long long> g_launches{0};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+struct ProfRec {
+  cudaEvent_t a, b;
+  int kind;
+};
+std::vector<ProfRec> g_recs;
+std::vector<cudaEvent_t> g_pool;
+
+cudaEvent_t take_event() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+}  // namespace
+
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+KernelTimer::KernelTimer(cudaStream_t s, int kind) : s_(s), kind_(kind) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (!g_prof_on) return;
+  cudaEvent_t a = take_event(), b = take_event();
+  if (!a || !b) return;
+  if (cudaEventRecord(a, s_) != cudaSuccess) return;
+  a_ = a;
+  b_ = b;
+}
+
+KernelTimer::~KernelTimer() {
+  if (!a_) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  cudaEvent_t a = static_cast<cudaEvent_t>(a_), b = static_cast<cudaEvent_t>(b_);
+  if (cudaEventRecord(b, s_) == cudaSuccess) g_recs.push_back({a, b, kind_});
 }
 
 }  // namespace fm
@@ -224,5 +269,42 @@ fm_status fm_selftest_wait_timeout(int64_t limit_us, void* stream) {
   if (!err) return FM_ERR_CUDA;
   return from_cuda(launch_wait_selftest((uint64_t)limit_us * 1000ull, static_cast<cudaStream_t>(stream), err));
 }
+
+fm_status fm_profile_enable(int32_t on) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_on = on != 0;
+  return FM_OK;
+}
+
+fm_status fm_profile_read(double* fwd_ms, int32_t* fwd_launches, double* bwd_ms, int32_t* bwd_launches) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    recs.swap(g_recs);
+  }
+  double ms[2] = {0.0, 0.0};
+  int32_t cnt[2] = {0, 0};
+  fm_status st = FM_OK;
+  for (const ProfRec& r : recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) st = FM_ERR_CUDA;
+    ms[r.kind] += t;
+    cnt[r.kind] += 1;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    for (const ProfRec& r : recs) {
+      g_pool.push_back(r.a);
+      g_pool.push_back(r.b);
+    }
+  }
+  if (fwd_ms) *fwd_ms = ms[0];
+  if (fwd_launches) *fwd_launches = cnt[0];
+  if (bwd_ms) *bwd_ms = ms[1];
+  if (bwd_launches) *bwd_launches = cnt[1];
+  return st;
+}
+
+int64_t fm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -590,12 +590,16 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
     attr_done = true;
   }
   const long long grid = (long long)P.B * nK * P.H_kv;
-  bwd_kernel<D><<<(unsigned)grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, prm0);
+  {
+    KernelTimer timer(s, kTimedBwd);
+    bwd_kernel<D><<<(unsigned)grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, prm0);
+  }
   // 4. dQ = bf16(scale * dQacc)
   const long long n8 = BH * P.N * D / 8;
   long long blocks = (n8 + 255) / 256;
   if (blocks > 152 * 32) blocks = 152 * 32;
   dq_convert_kernel<<<(unsigned)blocks, 256, 0, s>>>(w.dq_acc, static_cast<__nv_bfloat16*>(dq), n8, P.scale);
+  count_launches(4);  // row terms, LPT order, main kernel, dQ convert
   return cudaGetLastError();
 }
 

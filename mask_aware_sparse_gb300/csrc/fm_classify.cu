@@ -211,6 +211,7 @@ cudaError_t launch_classify(const fm_problem& p, int bm, int bn, int nQ, int nK,
   scan_kernel<<<2, 1024, 0, s>>>(row_cnt, (int)nqb, q_off, col_cnt, (int)nkb, k_off);
   emit_rows_kernel<<<(unsigned)((nqb + 7) / 8), 256, 0, s>>>(tile_class, B, nQ, nK, q_off, q_queue);
   emit_cols_kernel<<<(unsigned)((nkb + 7) / 8), 256, 0, s>>>(tile_class, B, nQ, nK, k_off, k_queue);
+  count_launches(6);
   return cudaGetLastError();
 }
 

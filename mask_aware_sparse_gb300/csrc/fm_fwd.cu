@@ -459,7 +459,11 @@ cudaError_t launch_fwd_d(const fm_problem& P, const CUtensorMap& tq, const CUten
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  fwd_kernel<D><<<grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, prm);
+  {
+    KernelTimer timer(s, kTimedFwd);
+    fwd_kernel<D><<<grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, prm);
+  }
+  count_launches(2);  // LPT order + main kernel
   return cudaGetLastError();
 }
 

@@ -43,4 +43,23 @@ bool make_tmap_bhnd(void* out_tmap /* CUtensorMap* */, const void* base, int64_t
 
 constexpr int kTile = 128;  // attention tile (block_m = block_n)
 
+// Launch accounting and optional event timing of the main kernels (fm_api.cu).
+void count_launches(int n);
+enum { kTimedFwd = 0, kTimedBwd = 1 };
+// Records an event before the launch it brackets and one after (destructor),
+// when fm_profile_enable(1) is in effect.
+class KernelTimer {
+ public:
+  KernelTimer(cudaStream_t s, int kind);
+  ~KernelTimer();
+  KernelTimer(const KernelTimer&) = delete;
+  KernelTimer& operator=(const KernelTimer&) = delete;
+
+ private:
+  cudaStream_t s_;
+  int kind_;
+  void* a_ = nullptr;
+  void* b_ = nullptr;
+};
+
 }  // namespace fm
