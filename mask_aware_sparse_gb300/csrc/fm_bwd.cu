@@ -16,26 +16,32 @@
 //                    block in two 64-row halves;
 //   dq_convert       dQ = bf16(scale * dQacc).
 //
-// bwd_kernel (320 threads):
-//   warps 0-3  compute: thread j owns KV row j (its mask boundaries live in
-//              registers); reads S^T and dP^T rows from TMEM, writes P^T and
-//              dS^T (bf16) back to TMEM and dS^T to shared memory;
-//   warps 4-7  dQ drain: thread c owns TMEM lane c = head-dim index c of
+// bwd_kernel (448 threads):
+//   warps 0-7  compute: thread j of warp w owns KV row j = 32*(w%4) + lane
+//              (its mask boundaries live in registers) and query columns
+//              [32*(w/4), 32*(w/4)+32) of the unit; reads S^T and dP^T from
+//              TMEM, writes P^T (bf16) back to TMEM and dS^T (bf16) to shared
+//              memory. Two compute warps per SM sub-partition hide latency.
+//   warps 8-11 dQ drain: thread c owns TMEM lane c = head-dim index c of
 //              dQ^T; reduces it into the fp32 dQ accumulator with coalesced
 //              128-byte atomic adds; also stores dK at the end;
-//   warp 8     TMA producer (K, V once; Q, dO, LSE offsets, D per unit);
-//   warp 9     tcgen05 MMA issuer.
+//   warp 12    TMA producer (K, V once; Q, dO, LSE offsets, D per unit);
+//   warp 13    tcgen05 MMA issuer.
 // Per unit u (64 query rows) the MMAs are, all with M = 128:
 //   S^T  = K Q^T           (TMEM S[u&1], 64 columns)
 //   dP^T = V dO^T          (TMEM dP, 64 columns)
 //   dV  += P^T dO          (A = P^T from TMEM)
-//   dK  += dS^T Q          (A = dS^T from TMEM)
+//   dK  += dS^T Q          (A = dS^T, K-major, from shared memory)
 //   dQ^T = K^T dS^T        (A = K^T, B = dS^T: both MN-major from shared memory)
 // TMEM: S[0] [0,64) S[1] [64,128) dP [128,192) dQ^T [192,256)
 //       dV [256, 256+d) dK [256+d, 256+2d).
-// Issue order per iteration: S(u+1); wait compute(u); dV(u), dK(u); dP(u+1);
-// wait drain(u-1); dQ^T(u). The tensor core works on S(u+1) while the
-// compute warps work on unit u.
+// Issue order per iteration: S(u+1); wait compute(u); dP(u+1); dV(u), dK(u);
+// wait drain(u-1); dQ^T(u). The tensor core works on S(u+1) while the compute
+// warps work on unit u, and on dV(u), dK(u), dQ^T(u), S(u+2) while they work
+// on unit u+1 (which only needs S(u+1) and dP(u+1)).
+// The dS^T buffer of unit u (128 KV rows x 64 query columns, bf16, 128-byte
+// swizzle) serves both as the K-major A operand of dK and the MN-major B
+// operand of dQ^T.
 #include <climits>
 #include <cmath>
 #include <cuda.h>
@@ -113,7 +119,7 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams& p, int u, int L, in
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const BwdParams p) {
   using C = BwdCfg<D>;
@@ -161,7 +167,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(&bars[C::B_SFULL + 0], 1);
     mbar_init(&bars[C::B_SFULL + 1], 1);
     mbar_init(&bars[C::B_DPFULL], 1);
-    mbar_init(&bars[C::B_READY], 128);
+    mbar_init(&bars[C::B_READY], 256);
     mbar_init(&bars[C::B_DQFULL], 1);
     mbar_init(&bars[C::B_DQEMPTY], 128);
     mbar_init(&bars[C::B_FINAL], 1);
@@ -172,8 +178,8 @@ __global__ void __launch_bounds__(320, 1)
     for (int x = threadIdx.x; x < C::ZERO_BYTES / 16; x += blockDim.x) z[x] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
-  if (warp == 9) tmem_alloc<512>(tmem_slot);
-  if (warp == 8 && lane == 0) {
+  if (warp == 13) tmem_alloc<512>(tmem_slot);
+  if (warp == 12 && lane == 0) {
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
@@ -186,7 +192,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (*abort_flag) {
     // an unread timeout from an earlier launch: skip the work
-  } else if (warp == 8) {
+  } else if (warp == 12) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = true;
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(320, 1)
         bulk_load(smem + C::ROW_OFF + stage * 512 + 256, p.dsum + (size_t)bh * p.Npad + r0, 256, fb);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);  // S^T, dP^T: A K-major, B K-major
@@ -256,28 +262,29 @@ __global__ void __launch_bounds__(320, 1)
         ok = mbar_wait(&bars[C::B_READY], (uint32_t)u & 1u, abort_flag, p.err);
         tc_fence_after();
         if (!ok) break;
+        if (u + 1 < U) {  // the compute warps are done with dP(u): start unit u+1's dP now
+          issue_sk(sV, sdO + nstage * C::Q_TILE, T_DP);
+          mma_commit(&bars[C::B_DPFULL]);
+        }
         const uint32_t tP = tbase + T_S0 + 64u * (u & 1);
+        const uint32_t sdsu = sdS + 16384u * (u & 1);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {  // 64 query rows = 4 k-steps; P^T, dS^T are 32 packed columns
+        for (int k = 0; k < 4; ++k) {  // 64 query rows = 4 k-steps; P^T is 32 packed TMEM columns
           const uint64_t bdo = sdesc_sw128(sdO + stage * C::Q_TILE + k * 2048, 8192, 1024);
           mma_ts(tbase + T_DV, tP + k * 8, bdo, id_g, (u > 0 || k > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
+          const uint64_t ads = sdesc_sw128(sdsu + k * 32, 16, 1024);
           const uint64_t bq = sdesc_sw128(sQ + stage * C::Q_TILE + k * 2048, 8192, 1024);
-          mma_ts(tbase + T_DK, tbase + T_DP + k * 8, bq, id_g, (u > 0 || k > 0) ? 1u : 0u);
+          mma_ss(tbase + T_DK, ads, bq, id_g, (u > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(&bars[C::B_QEMPTY + stage]);
-        if (u + 1 < U) {
-          issue_sk(sV, sdO + nstage * C::Q_TILE, T_DP);
-          mma_commit(&bars[C::B_DPFULL]);
-        }
         if (u >= 1) {
           ok = mbar_wait(&bars[C::B_DQEMPTY], (uint32_t)(u - 1) & 1u, abort_flag, p.err);
           tc_fence_after();
           if (!ok) break;
         }
-        const uint32_t sdsu = sdS + 16384u * (u & 1);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {  // 128 KV rows
           const uint64_t ad = sdesc_sw128(sK + k * 2048, lbo_kt, 1024);
@@ -288,11 +295,12 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (ok) mma_commit(&bars[C::B_FINAL]);
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ compute
-    const int j = (warp << 5) + lane;  // KV row within the block = TMEM lane
+    const int j = ((warp & 3) << 5) + lane;  // KV row within the block = TMEM lane
+    const int half = warp >> 2;              // query columns [32*half, 32*half + 32)
     const int kcol = k0 + j;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     int lo0 = 0, lo1 = 0, up0 = 0, up1 = 0;
     bool dead = kcol >= p.N;
     if (!dead) {
@@ -308,6 +316,8 @@ __global__ void __launch_bounds__(320, 1)
     }
     const unsigned lw = (unsigned)(lo1 - lo0), uw = (unsigned)(up1 - up0);
     const float sl2 = p.scale_log2;
+    const uint32_t s_rows = smem_u32(smem + C::ROW_OFF);
+    const uint32_t s_ds = smem_u32(smem + C::DS_OFF) + (uint32_t)((j >> 3) * 1024 + (j & 7) * 128);
     bool ok = true;
     for (int u = 0; u < U && ok; ++u) {
       const Unit un = decode_unit(p, u, L, kbeg, g, force_part);
@@ -318,55 +328,53 @@ __global__ void __launch_bounds__(320, 1)
       if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_DPFULL], (uint32_t)u & 1u, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
-      const float* s_nl = reinterpret_cast<const float*>(smem + C::ROW_OFF + stage * 512);
-      const float* s_d = s_nl + 64;
+      const uint32_t rows_a = s_rows + stage * 512;  // nl[64] then D[64]
       const uint32_t tS = tbase + lane_off + T_S0 + 64u * (u & 1);
       const uint32_t tDP = tbase + lane_off + T_DP;
-      uint8_t* dsrow = smem + C::DS_OFF + 16384 * (u & 1) + (j >> 3) * 1024 + (j & 7) * 128;
+      const uint32_t ds_row = s_ds + 16384u * (u & 1);
+      uint32_t sv[32], pv[32];
+      tmem_ld32(tS + 32 * half, sv);
+      tmem_ld32(tDP + 32 * half, pv);
+      tmem_ld_wait();
+      uint32_t pk[16], dk[16];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {  // two chunks of 32 query rows
-        uint32_t sv[32], pv[32];
-        tmem_ld32(tS + 32 * c, sv);
-        tmem_ld32(tDP + 32 * c, pv);
-        tmem_ld_wait();
-        uint32_t pk[16], dk[16];
+      for (int r4 = 0; r4 < 8; ++r4) {
+        const float4 nl4 = lds_f32x4(rows_a + 128 * half + 16 * r4);
+        const float4 d4 = lds_f32x4(rows_a + 256 + 128 * half + 16 * r4);
+        const float nlv[4] = {nl4.x, nl4.y, nl4.z, nl4.w};
+        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pp[4], dd[4];
 #pragma unroll
-        for (int r = 0; r < 32; r += 2) {
-          float pp[2], dd[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int rr = 32 * c + r + e;
-            const int i = r0 + rr;
-            float x = fmaf(__uint_as_float(sv[r + e]), sl2, s_nl[rr]);
-            if (un.part) {
-              const bool msk = dead | ((unsigned)(i - lo0) < lw) | ((unsigned)(i - up0) < uw) | (p.causal && i < kcol);
-              if (msk) x = -INFINITY;
-            }
-            const float pr = ex2_approx(x);
-            pp[e] = pr;
-            dd[e] = pr * (__uint_as_float(pv[r + e]) - s_d[rr]);
+        for (int e = 0; e < 4; ++e) {
+          const int rr = 4 * r4 + e;
+          const int i = r0 + 32 * half + rr;
+          float x = fmaf(__uint_as_float(sv[rr]), sl2, nlv[e]);
+          if (un.part) {
+            const bool msk = dead | ((unsigned)(i - lo0) < lw) | ((unsigned)(i - up0) < uw) | (p.causal && i < kcol);
+            if (msk) x = -INFINITY;
           }
-          pk[r >> 1] = pack_bf16x2(pp[0], pp[1]);
-          dk[r >> 1] = pack_bf16x2(dd[0], dd[1]);
+          pp[e] = ex2_approx(x);
+          dd[e] = pp[e] * (__uint_as_float(pv[rr]) - dv4[e]);
         }
-        tmem_st16(tS + 16 * c, pk);
-        tmem_st16(tDP + 16 * c, dk);
-        // dS^T row j, query columns [32c, 32c+32): four 16-byte chunks, 128-byte swizzle
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int chunk = 4 * c + q4;
-          *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (j & 7)) << 4)) =
-              make_uint4(dk[4 * q4], dk[4 * q4 + 1], dk[4 * q4 + 2], dk[4 * q4 + 3]);
-        }
+        pk[2 * r4] = pack_bf16x2(pp[0], pp[1]);
+        pk[2 * r4 + 1] = pack_bf16x2(pp[2], pp[3]);
+        dk[2 * r4] = pack_bf16x2(dd[0], dd[1]);
+        dk[2 * r4 + 1] = pack_bf16x2(dd[2], dd[3]);
       }
+      tmem_st16(tS + 16 * half, pk);  // P^T: 16 packed columns of S[u&1]
+      // dS^T row j, 16-byte chunks 4*half .. 4*half+3 (8 query columns each), 128-byte swizzle
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        sts_b32x4(ds_row + ((uint32_t)((4 * half + q4) ^ (j & 7)) << 4), dk[4 * q4], dk[4 * q4 + 1], dk[4 * q4 + 2],
+                  dk[4 * q4 + 3]);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars[C::B_READY]);
     }
-    // epilogue: dV rows
+    // epilogue: dV rows (warps 0-3; warps 4-7 only load to stay converged)
     if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_FINAL], 0, abort_flag, p.err));
-    if (ok) {
+    if (ok && half == 0) {
       tc_fence_after();
       const size_t row = ((size_t)b * p.H_kv + g) * p.N + kcol;
 #pragma unroll
@@ -387,7 +395,7 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ drain
-    const int w4 = warp - 4;
+    const int w4 = warp - 8;
     const int c = (w4 << 5) + lane;  // head-dim index = TMEM lane
     const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
     bool ok = true;
@@ -406,12 +414,19 @@ __global__ void __launch_bounds__(320, 1)
         const int r0 = un.qb * 128 + un.half * 64;
         float* dst = p.dq_acc + ((size_t)(b * p.H_q + un.h) * p.N + r0) * D + c;
         const int nrow = min(64, p.N - r0);
+        if (nrow == 64) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r)
-          if (r < nrow) atomicAdd(dst + (size_t)r * D, __uint_as_float(v0[r]));
+          for (int r = 0; r < 32; ++r) atomicAdd(dst + r * D, __uint_as_float(v0[r]));
 #pragma unroll
-        for (int r = 0; r < 32; ++r)
-          if (32 + r < nrow) atomicAdd(dst + (size_t)(32 + r) * D, __uint_as_float(v1[r]));
+          for (int r = 0; r < 32; ++r) atomicAdd(dst + (32 + r) * D, __uint_as_float(v1[r]));
+        } else {
+#pragma unroll
+          for (int r = 0; r < 32; ++r)
+            if (r < nrow) atomicAdd(dst + r * D, __uint_as_float(v0[r]));
+#pragma unroll
+          for (int r = 0; r < 32; ++r)
+            if (32 + r < nrow) atomicAdd(dst + (32 + r) * D, __uint_as_float(v1[r]));
+        }
       }
     }
     // epilogue: dK rows (thread = KV row j = TMEM lane)
@@ -442,7 +457,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc<512>(tbase);
@@ -592,7 +607,7 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   const long long grid = (long long)P.B * nK * P.H_kv;
   {
     KernelTimer timer(s, kTimedBwd);
-    bwd_kernel<D><<<(unsigned)grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, prm0);
+    bwd_kernel<D><<<(unsigned)grid, 448, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, prm0);
   }
   // 4. dQ = bf16(scale * dQacc)
   const long long n8 = BH * P.N * D / 8;
