@@ -28,20 +28,21 @@
 //   warp 12    TMA producer (K, V once; Q, dO, LSE offsets, D per unit);
 //   warp 13    tcgen05 MMA issuer.
 // Per unit u (64 query rows) the MMAs are, all with M = 128:
-//   S^T  = K Q^T           (TMEM S[u&1], 64 columns)
+//   S^T  = K Q^T           (TMEM S, 64 columns)
 //   dP^T = V dO^T          (TMEM dP, 64 columns)
-//   dV  += P^T dO          (A = P^T from TMEM)
+//   dV  += P^T dO          (A = P^T from TMEM, written over S by the compute warps)
 //   dK  += dS^T Q          (A = dS^T, K-major, from shared memory)
 //   dQ^T = K^T dS^T        (A = K^T, B = dS^T: both MN-major from shared memory)
-// TMEM: S[0] [0,64) S[1] [64,128) dP [128,192) dQ^T [192,256)
-//       dV [256, 256+d) dK [256+d, 256+2d).
-// Issue order per iteration: S(u+1); wait compute(u); dP(u+1); dV(u), dK(u);
-// wait drain(u-1); dQ^T(u). The tensor core works on S(u+1) while the compute
-// warps work on unit u, and on dV(u), dK(u), dQ^T(u), S(u+2) while they work
-// on unit u+1 (which only needs S(u+1) and dP(u+1)).
+// TMEM: S [0,64) dP [64,128) dQ^T[2] [128,256) dV [256, 256+d) dK [256+d, 256+2d).
+// The compute warps work in two parts per unit: the P part (needs S^T) and
+// the dS part (needs dP^T). Issue order per unit: wait P(u); dV(u); S(u+1);
+// wait dS(u); dP(u+1); dK(u); wait drain(u-2); dQ^T(u). So while the compute
+// warps finish unit u the tensor core runs dV(u) and S(u+1), and while they
+// start unit u+1 it runs dP(u+1), dK(u) and dQ^T(u). The double-buffered dQ^T
+// lets the drain of unit u overlap the MMAs of unit u+1.
 // The dS^T buffer of unit u (128 KV rows x 64 query columns, bf16, 128-byte
-// swizzle) serves both as the K-major A operand of dK and the MN-major B
-// operand of dQ^T.
+// swizzle, two buffers) serves both as the K-major A operand of dK and the
+// MN-major B operand of dQ^T.
 #include <climits>
 #include <cmath>
 #include <cuda.h>
@@ -68,16 +69,19 @@ struct BwdCfg {
   static constexpr int ZERO_OFF = DS_OFF + 2 * 16384;      // d = 64 only: 16 KB of zeros
   static constexpr int ZERO_BYTES = (D == 64) ? 16384 : 0;
   static constexpr int ROW_OFF = ZERO_OFF + ZERO_BYTES;    // STAGES x {nl[64], D[64]} fp32
-  static constexpr int BAR_OFF = ROW_OFF + STAGES * 512;
+  static constexpr int QUEUE_CAP = 1024;                    // queue entries staged in shared memory
+  static constexpr int QUEUE_OFF = ROW_OFF + STAGES * 512;
+  static constexpr int BAR_OFF = QUEUE_OFF + QUEUE_CAP * 4;
   static constexpr int B_KV = 0;
   static constexpr int B_QFULL = 1;
   static constexpr int B_QEMPTY = B_QFULL + STAGES;
-  static constexpr int B_SFULL = B_QEMPTY + STAGES;  // [2]
-  static constexpr int B_DPFULL = B_SFULL + 2;
+  static constexpr int B_SFULL = B_QEMPTY + STAGES;
+  static constexpr int B_PREADY = B_SFULL + 1;
+  static constexpr int B_DPFULL = B_PREADY + 1;
   static constexpr int B_READY = B_DPFULL + 1;
-  static constexpr int B_DQFULL = B_READY + 1;
-  static constexpr int B_DQEMPTY = B_DQFULL + 1;
-  static constexpr int B_FINAL = B_DQEMPTY + 1;
+  static constexpr int B_DQFULL = B_READY + 1;    // [2]
+  static constexpr int B_DQEMPTY = B_DQFULL + 2;  // [2]
+  static constexpr int B_FINAL = B_DQEMPTY + 2;
   static constexpr int NBAR = B_FINAL + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
@@ -103,19 +107,32 @@ struct BwdParams {
 };
 
 // Decode unit u of a CTA: query head (h) of the group, queue position, half.
+// The CTA's queue segment is staged in shared memory (s_queue) when it fits,
+// so no role waits on a dependent global load per unit.
 struct Unit {
   int h, qb, half, part;
 };
-__device__ __forceinline__ Unit decode_unit(const BwdParams& p, int u, int L, int kbeg, int g, bool force_part) {
+__device__ __forceinline__ Unit decode_unit(const BwdParams& p, int u, int L, int kbeg, int g, bool force_part,
+                                            uint32_t s_queue, int qcap) {
   Unit r;
   const int hi = u / (2 * L);
   const int rem = u - hi * 2 * L;
-  const int e = p.k_queue[kbeg + (rem >> 1)];
+  const int pos = rem >> 1;
+  const int e = (pos < qcap) ? lds_s32(s_queue + 4 * pos) : p.k_queue[kbeg + pos];
   r.h = g * p.G + hi;
   r.qb = e >> 1;
   r.half = rem & 1;
   r.part = (e & 1) | (force_part ? 1 : 0);
   return r;
+}
+
+// Bits [a, b) of a 32-bit word (clipped to [0, 32)); 0 when the range is empty.
+__device__ __forceinline__ uint32_t rows_bits(int a, int b) {
+  a = max(a, 0);
+  b = min(b, 32);
+  if (a >= b) return 0u;
+  const uint32_t hi = (b == 32) ? 0xffffffffu : ((1u << b) - 1u);
+  return hi & ~((1u << a) - 1u);
 }
 
 template <int D>
@@ -164,14 +181,21 @@ __global__ void __launch_bounds__(448, 1)
       mbar_init(&bars[C::B_QFULL + s], 1);
       mbar_init(&bars[C::B_QEMPTY + s], 1);
     }
-    mbar_init(&bars[C::B_SFULL + 0], 1);
-    mbar_init(&bars[C::B_SFULL + 1], 1);
+    mbar_init(&bars[C::B_SFULL], 1);
+    mbar_init(&bars[C::B_PREADY], 256);
     mbar_init(&bars[C::B_DPFULL], 1);
     mbar_init(&bars[C::B_READY], 256);
-    mbar_init(&bars[C::B_DQFULL], 1);
-    mbar_init(&bars[C::B_DQEMPTY], 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars[C::B_DQFULL + x], 1);
+      mbar_init(&bars[C::B_DQEMPTY + x], 128);
+    }
     mbar_init(&bars[C::B_FINAL], 1);
     fence_mbar_init();
+  }
+  const uint32_t s_queue = smem_u32(smem + C::QUEUE_OFF);
+  {
+    int* sq = reinterpret_cast<int*>(smem + C::QUEUE_OFF);
+    for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) sq[t] = p.k_queue[kbeg + t];
   }
   if (C::ZERO_BYTES > 0) {
     uint4* z = reinterpret_cast<uint4*>(smem + C::ZERO_OFF);
@@ -188,7 +212,8 @@ __global__ void __launch_bounds__(448, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  constexpr uint32_t T_S0 = 0, T_DP = 128, T_DQ = 192, T_DV = 256, T_DK = 256 + D;
+  // TMEM columns: S^T (P^T written back in place), dP^T, dQ^T x 2, dV, dK
+  constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 256, T_DK = 256 + D;
 
   if (*abort_flag) {
     // an unread timeout from an earlier launch: skip the work
@@ -202,7 +227,7 @@ __global__ void __launch_bounds__(448, 1)
         tma_load_3d(smem + C::V_OFF + x * 16384, &tv, &bars[C::B_KV], x * 64, k0, b * p.H_kv + g);
       }
       for (int u = 0; u < U && ok; ++u) {
-        const Unit un = decode_unit(p, u, L, kbeg, g, force_part);
+        const Unit un = decode_unit(p, u, L, kbeg, g, force_part, s_queue, C::QUEUE_CAP);
         const int stage = u % S;
         ok = mbar_wait(&bars[C::B_QEMPTY + stage], ((uint32_t)(u / S) & 1u) ^ 1u, abort_flag, p.err);
         if (!ok) break;
@@ -222,15 +247,13 @@ __global__ void __launch_bounds__(448, 1)
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);  // S^T, dP^T: A K-major, B K-major
-      const uint32_t id_g = idesc_bf16_f32(128, D, 0, 1);   // dV, dK: A from TMEM, B MN-major
+      const uint32_t id_g = idesc_bf16_f32(128, D, 0, 1);   // dV, dK: B MN-major
       const uint32_t id_q = idesc_bf16_f32(128, 64, 1, 1);  // dQ^T: A MN-major, B MN-major
       const uint32_t sK = smem_u32(smem + C::K_OFF), sV = smem_u32(smem + C::V_OFF);
       const uint32_t sQ = smem_u32(smem + C::Q_OFF), sdO = smem_u32(smem + C::DO_OFF);
       const uint32_t sdS = smem_u32(smem + C::DS_OFF);
       const uint32_t lbo_kt = (D == 128) ? 16384u : (uint32_t)(C::ZERO_OFF - C::K_OFF);
-      bool ok = mbar_wait(&bars[C::B_KV], 0, abort_flag, p.err);
-      tc_fence_after();
-      // S^T(u) = K Q_u^T or dP^T(u) = V dO_u^T into TMEM column `dst`
+      // S^T = K Q_u^T or dP^T = V dO_u^T into TMEM column `dst`
       auto issue_sk = [&](uint32_t a_base, uint32_t b_base, uint32_t dst) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
@@ -239,39 +262,46 @@ __global__ void __launch_bounds__(448, 1)
           mma_ss(tbase + dst, ad, bd, id_s, k > 0 ? 1u : 0u);
         }
       };
+      bool ok = mbar_wait(&bars[C::B_KV], 0, abort_flag, p.err);
+      tc_fence_after();
       if (ok) {
         ok = mbar_wait(&bars[C::B_QFULL + 0], 0, abort_flag, p.err);
         tc_fence_after();
       }
       if (ok) {
-        issue_sk(sK, sQ, T_S0);
-        mma_commit(&bars[C::B_SFULL + 0]);
+        issue_sk(sK, sQ, T_S);
+        mma_commit(&bars[C::B_SFULL]);
         issue_sk(sV, sdO, T_DP);
         mma_commit(&bars[C::B_DPFULL]);
       }
       for (int u = 0; u < U && ok; ++u) {
-        const int stage = u % S;
-        const int nstage = (u + 1) % S;
+        const int stage = u % S, nstage = (u + 1) % S;
+        const uint32_t sdsu = sdS + 16384u * (u & 1);
+        // dV += P^T dO once P^T(u) is in TMEM (two 16-column blocks, one per half)
+        ok = mbar_wait(&bars[C::B_PREADY], (uint32_t)u & 1u, abort_flag, p.err);
+        tc_fence_after();
+        if (!ok) break;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t a_t = tbase + T_S + (uint32_t)((k >> 1) * 32 + (k & 1) * 8);
+          const uint64_t bdo = sdesc_sw128(sdO + stage * C::Q_TILE + k * 2048, 8192, 1024);
+          mma_ts(tbase + T_DV, a_t, bdo, id_g, (u > 0 || k > 0) ? 1u : 0u);
+        }
+        // S^T(u+1) may overwrite P^T(u): dV(u) was issued first
         if (u + 1 < U) {
           ok = mbar_wait(&bars[C::B_QFULL + nstage], (uint32_t)((u + 1) / S) & 1u, abort_flag, p.err);
           tc_fence_after();
           if (!ok) break;
-          issue_sk(sK, sQ + nstage * C::Q_TILE, T_S0 + 64u * ((u + 1) & 1));
-          mma_commit(&bars[C::B_SFULL + ((u + 1) & 1)]);
+          issue_sk(sK, sQ + nstage * C::Q_TILE, T_S);
+          mma_commit(&bars[C::B_SFULL]);
         }
+        // dS^T(u) is in shared memory and dP^T(u) has been read
         ok = mbar_wait(&bars[C::B_READY], (uint32_t)u & 1u, abort_flag, p.err);
         tc_fence_after();
         if (!ok) break;
-        if (u + 1 < U) {  // the compute warps are done with dP(u): start unit u+1's dP now
+        if (u + 1 < U) {
           issue_sk(sV, sdO + nstage * C::Q_TILE, T_DP);
           mma_commit(&bars[C::B_DPFULL]);
-        }
-        const uint32_t tP = tbase + T_S0 + 64u * (u & 1);
-        const uint32_t sdsu = sdS + 16384u * (u & 1);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {  // 64 query rows = 4 k-steps; P^T is 32 packed TMEM columns
-          const uint64_t bdo = sdesc_sw128(sdO + stage * C::Q_TILE + k * 2048, 8192, 1024);
-          mma_ts(tbase + T_DV, tP + k * 8, bdo, id_g, (u > 0 || k > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -280,8 +310,8 @@ __global__ void __launch_bounds__(448, 1)
           mma_ss(tbase + T_DK, ads, bq, id_g, (u > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(&bars[C::B_QEMPTY + stage]);
-        if (u >= 1) {
-          ok = mbar_wait(&bars[C::B_DQEMPTY], (uint32_t)(u - 1) & 1u, abort_flag, p.err);
+        if (u >= 2) {  // dQ^T buffer u&1 was drained for unit u-2
+          ok = mbar_wait(&bars[C::B_DQEMPTY + (u & 1)], (uint32_t)((u >> 1) - 1) & 1u, abort_flag, p.err);
           tc_fence_after();
           if (!ok) break;
         }
@@ -289,9 +319,9 @@ __global__ void __launch_bounds__(448, 1)
         for (int k = 0; k < 8; ++k) {  // 128 KV rows
           const uint64_t ad = sdesc_sw128(sK + k * 2048, lbo_kt, 1024);
           const uint64_t bd = sdesc_sw128(sdsu + k * 2048, 8192, 1024);
-          mma_ss(tbase + T_DQ, ad, bd, id_q, k > 0 ? 1u : 0u);
+          mma_ss(tbase + T_DQ + 64u * (u & 1), ad, bd, id_q, k > 0 ? 1u : 0u);
         }
-        mma_commit(&bars[C::B_DQFULL]);
+        mma_commit(&bars[C::B_DQFULL + (u & 1)]);
       }
       if (ok) mma_commit(&bars[C::B_FINAL]);
     }
@@ -302,7 +332,7 @@ __global__ void __launch_bounds__(448, 1)
     const int kcol = k0 + j;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     int lo0 = 0, lo1 = 0, up0 = 0, up1 = 0;
-    bool dead = kcol >= p.N;
+    const bool dead = kcol >= p.N;
     if (!dead) {
       const size_t vi = (size_t)b * p.N + kcol;
       int a0 = p.lts[vi], a1 = p.lte[vi], u0 = p.uts[vi], u1 = p.ute[vi];
@@ -314,65 +344,83 @@ __global__ void __launch_bounds__(448, 1)
       if (a0 < a1) { lo0 = a0; lo1 = a1; }
       if (u0 < u1) { up0 = u0; up1 = u1; }
     }
-    const unsigned lw = (unsigned)(lo1 - lo0), uw = (unsigned)(up1 - up0);
     const float sl2 = p.scale_log2;
+    const bool causal = p.causal != 0;
     const uint32_t s_rows = smem_u32(smem + C::ROW_OFF);
     const uint32_t s_ds = smem_u32(smem + C::DS_OFF) + (uint32_t)((j >> 3) * 1024 + (j & 7) * 128);
+    const uint32_t tS = tbase + lane_off + T_S + 32u * half;
+    const uint32_t tDP = tbase + lane_off + T_DP + 32u * half;
     bool ok = true;
     for (int u = 0; u < U && ok; ++u) {
-      const Unit un = decode_unit(p, u, L, kbeg, g, force_part);
+      const Unit un = decode_unit(p, u, L, kbeg, g, force_part, s_queue, C::QUEUE_CAP);
       const int stage = u % S;
       const int r0 = un.qb * 128 + un.half * 64;
       ok = __all_sync(kFull, mbar_wait(&bars[C::B_QFULL + stage], (uint32_t)(u / S) & 1u, abort_flag, p.err));
-      if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_SFULL + (u & 1)], (uint32_t)(u >> 1) & 1u, abort_flag, p.err));
-      if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_DPFULL], (uint32_t)u & 1u, abort_flag, p.err));
+      if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_SFULL], (uint32_t)u & 1u, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t rows_a = s_rows + stage * 512;  // nl[64] then D[64]
-      const uint32_t tS = tbase + lane_off + T_S0 + 64u * (u & 1);
-      const uint32_t tDP = tbase + lane_off + T_DP;
-      const uint32_t ds_row = s_ds + 16384u * (u & 1);
-      uint32_t sv[32], pv[32];
-      tmem_ld32(tS + 32 * half, sv);
-      tmem_ld32(tDP + 32 * half, pv);
+      // masked rows of this thread's key column within its 32-row window, one bit per row
+      uint32_t mbits = 0u;
+      if (un.part) {
+        const int w0 = r0 + 32 * half;
+        mbits = rows_bits(lo0 - w0, lo1 - w0) | rows_bits(up0 - w0, up1 - w0) |
+                (causal ? rows_bits(-w0, kcol - w0) : 0u) | (dead ? 0xffffffffu : 0u);
+      }
+      const uint32_t rows_a = s_rows + stage * 512 + 128 * half;  // nl[32*half ..] ; D at +256
+      // P part: P^T = exp2(scale*log2e*S^T - LSE*log2e), written back as bf16 over
+      // this half's own first 16 S columns (the other half's columns are untouched)
+      uint32_t sv[32];
+      tmem_ld32(tS, sv);
       tmem_ld_wait();
-      uint32_t pk[16], dk[16];
+      float pf[32];
+      uint32_t pk[16];
 #pragma unroll
       for (int r4 = 0; r4 < 8; ++r4) {
-        const float4 nl4 = lds_f32x4(rows_a + 128 * half + 16 * r4);
-        const float4 d4 = lds_f32x4(rows_a + 256 + 128 * half + 16 * r4);
+        const float4 nl4 = lds_f32x4(rows_a + 16 * r4);
         const float nlv[4] = {nl4.x, nl4.y, nl4.z, nl4.w};
-        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-        float pp[4], dd[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int rr = 4 * r4 + e;
-          const int i = r0 + 32 * half + rr;
           float x = fmaf(__uint_as_float(sv[rr]), sl2, nlv[e]);
-          if (un.part) {
-            const bool msk = dead | ((unsigned)(i - lo0) < lw) | ((unsigned)(i - up0) < uw) | (p.causal && i < kcol);
-            if (msk) x = -INFINITY;
-          }
-          pp[e] = ex2_approx(x);
-          dd[e] = pp[e] * (__uint_as_float(pv[rr]) - dv4[e]);
+          x = ((mbits >> rr) & 1u) ? -INFINITY : x;
+          pf[rr] = ex2_approx(x);
         }
-        pk[2 * r4] = pack_bf16x2(pp[0], pp[1]);
-        pk[2 * r4 + 1] = pack_bf16x2(pp[2], pp[3]);
+        pk[2 * r4] = pack_bf16x2(pf[4 * r4], pf[4 * r4 + 1]);
+        pk[2 * r4 + 1] = pack_bf16x2(pf[4 * r4 + 2], pf[4 * r4 + 3]);
+      }
+      tmem_st16(tS, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars[C::B_PREADY]);
+      // dS part: dS^T = P^T * (dP^T - D), bf16, to shared memory
+      ok = __all_sync(kFull, mbar_wait(&bars[C::B_DPFULL], (uint32_t)u & 1u, abort_flag, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t pv[32];
+      tmem_ld32(tDP, pv);
+      tmem_ld_wait();
+      uint32_t dk[16];
+#pragma unroll
+      for (int r4 = 0; r4 < 8; ++r4) {
+        const float4 d4 = lds_f32x4(rows_a + 256 + 16 * r4);
+        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+        float dd[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dd[e] = pf[4 * r4 + e] * (__uint_as_float(pv[4 * r4 + e]) - dv4[e]);
         dk[2 * r4] = pack_bf16x2(dd[0], dd[1]);
         dk[2 * r4 + 1] = pack_bf16x2(dd[2], dd[3]);
       }
-      tmem_st16(tS + 16 * half, pk);  // P^T: 16 packed columns of S[u&1]
       // dS^T row j, 16-byte chunks 4*half .. 4*half+3 (8 query columns each), 128-byte swizzle
+      const uint32_t ds_row = s_ds + 16384u * (u & 1);
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4)
         sts_b32x4(ds_row + ((uint32_t)((4 * half + q4) ^ (j & 7)) << 4), dk[4 * q4], dk[4 * q4 + 1], dk[4 * q4 + 2],
                   dk[4 * q4 + 3]);
-      tmem_st_wait();
-      fence_proxy_async_smem();
       tc_fence_before();
+      fence_proxy_async_smem();
       mbar_arrive(&bars[C::B_READY]);
     }
-    // epilogue: dV rows (warps 0-3; warps 4-7 only load to stay converged)
+    // epilogue: dV rows (warps 0-3)
     if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_FINAL], 0, abort_flag, p.err));
     if (ok && half == 0) {
       tc_fence_after();
@@ -400,16 +448,17 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
     bool ok = true;
     for (int u = 0; u < U && ok; ++u) {
-      const Unit un = decode_unit(p, u, L, kbeg, g, force_part);
-      ok = __all_sync(kFull, mbar_wait(&bars[C::B_DQFULL], (uint32_t)u & 1u, abort_flag, p.err));
+      const Unit un = decode_unit(p, u, L, kbeg, g, force_part, s_queue, C::QUEUE_CAP);
+      const int pb = u & 1;
+      ok = __all_sync(kFull, mbar_wait(&bars[C::B_DQFULL + pb], (uint32_t)(u >> 1) & 1u, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
       uint32_t v0[32], v1[32];
-      tmem_ld32(tbase + lane_off + T_DQ, v0);
-      tmem_ld32(tbase + lane_off + T_DQ + 32, v1);
+      tmem_ld32(tbase + lane_off + T_DQ + 64u * pb, v0);
+      tmem_ld32(tbase + lane_off + T_DQ + 64u * pb + 32, v1);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&bars[C::B_DQEMPTY]);
+      mbar_arrive(&bars[C::B_DQEMPTY + pb]);
       if (c < D) {
         const int r0 = un.qb * 128 + un.half * 64;
         float* dst = p.dq_acc + ((size_t)(b * p.H_q + un.h) * p.N + r0) * D + c;
@@ -446,9 +495,9 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
             const float* f = reinterpret_cast<const float*>(&r[8 * v4]);
-            const float s = p.scale;
-            dst[v4] = make_uint4(pack_bf16x2(f[0] * s, f[1] * s), pack_bf16x2(f[2] * s, f[3] * s),
-                                 pack_bf16x2(f[4] * s, f[5] * s), pack_bf16x2(f[6] * s, f[7] * s));
+            const float sc = p.scale;
+            dst[v4] = make_uint4(pack_bf16x2(f[0] * sc, f[1] * sc), pack_bf16x2(f[2] * sc, f[3] * sc),
+                                 pack_bf16x2(f[4] * sc, f[5] * sc), pack_bf16x2(f[6] * sc, f[7] * sc));
           }
         }
       }
@@ -664,3 +713,4 @@ cudaError_t launch_bwd(const fm_problem& P, const void* q, const void* k, const 
 }
 
 }  // namespace fm
+

@@ -48,7 +48,9 @@ struct FwdCfg {
   static constexpr int V_OFF = K_OFF + STAGES * TILE;
   static constexpr int M_OFF = V_OFF + STAGES * TILE;
   static constexpr int M_BYTES = 128 * 16;  // int4 {LTS, LTE, UTS, UTE} per column
-  static constexpr int BAR_OFF = M_OFF + STAGES * M_BYTES;
+  static constexpr int QUEUE_CAP = 1024;    // queue entries staged in shared memory
+  static constexpr int QUEUE_OFF = M_OFF + STAGES * M_BYTES;
+  static constexpr int BAR_OFF = QUEUE_OFF + QUEUE_CAP * 4;
   static constexpr int B_QFULL = 0;
   static constexpr int B_KFULL = 1;
   static constexpr int B_KEMPTY = B_KFULL + STAGES;
@@ -142,6 +144,15 @@ __global__ void __launch_bounds__(320, 1)
     }
     fence_mbar_init();
   }
+  // the unit's queue goes to shared memory once; every role reads it from there
+  const uint32_t s_queue = smem_u32(smem + C::QUEUE_OFF);
+  {
+    int* sq = reinterpret_cast<int*>(smem + C::QUEUE_OFF);
+    for (int t = threadIdx.x; t < n && t < C::QUEUE_CAP; t += blockDim.x) sq[t] = p.q_queue[qbeg + t];
+  }
+  auto queue_at = [&](int j) -> int {
+    return (j < C::QUEUE_CAP) ? lds_s32(s_queue + 4 * j) : p.q_queue[qbeg + j];
+  };
   if (warp == 9) tmem_alloc<512>(tmem_slot);
   if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tq);
@@ -167,7 +178,7 @@ __global__ void __launch_bounds__(320, 1)
     int pidx = 0;
     const size_t vbase = (size_t)b * p.N;
     for (int j = 0; j < n && ok; ++j) {
-      const int e = p.q_queue[qbeg + j];
+      const int e = queue_at(j);
       const int kb = e >> 1;
       if (kb < 0 || kb >= p.nK) {
         if (lane == 0) record_error(p.err, FM_DEV_ERR_QUEUE);
@@ -292,7 +303,7 @@ __global__ void __launch_bounds__(320, 1)
       int pidx = 0;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
-        const int e = p.q_queue[qbeg + j];
+        const int e = queue_at(j);
         const int kb = e >> 1;
         const bool part = (e & 1) || (kb == p.nK - 1 && (p.N & 127));
         ok = __all_sync(kFull, mbar_wait(&bars[C::B_SFULL + t], (uint32_t)j & 1u, abort_flag, p.err));
@@ -314,14 +325,16 @@ __global__ void __launch_bounds__(320, 1)
           const int ms = pidx % S;
           ok = __all_sync(kFull, mbar_wait(&bars[C::B_MFULL + ms], (uint32_t)(pidx / S) & 1u, abort_flag, p.err));
           if (!ok) break;
-          const int4* sm = reinterpret_cast<const int4*>(smem + C::M_OFF + ms * C::M_BYTES);
+          const uint32_t sm = smem_u32(smem + C::M_OFF + ms * C::M_BYTES);
           const int kc0 = kb * 128;
+          const bool causal = p.causal != 0;
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
-            const int4 v = sm[c];
+            const int4 v = lds_s32x4(sm + 16 * c);  // {LTS, LTE, UTS, UTE} of key column kc0 + c
+            // branch-free: the predicate differs between the rows (threads) of a warp
             const bool msk = ((unsigned)(i - v.x) < (unsigned)(v.y - v.x)) |
-                             ((unsigned)(i - v.z) < (unsigned)(v.w - v.z)) | (p.causal && i < kc0 + c);
-            if (msk) sr[c] = __float_as_uint(-INFINITY);
+                             ((unsigned)(i - v.z) < (unsigned)(v.w - v.z)) | (causal & (i < kc0 + c));
+            sr[c] = msk ? __float_as_uint(-INFINITY) : sr[c];
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[C::B_MEMPTY + ms]);
