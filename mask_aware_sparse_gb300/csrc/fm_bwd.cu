@@ -36,10 +36,11 @@
 // TMEM: S [0,64) dP [64,128) dQ^T[2] [128,256) dV [256, 256+d) dK [256+d, 256+2d).
 // The compute warps work in two parts per unit: the P part (needs S^T) and
 // the dS part (needs dP^T). Issue order per unit: wait P(u); dV(u); S(u+1);
-// wait dS(u); dP(u+1); dK(u); wait drain(u-2); dQ^T(u). So while the compute
-// warps finish unit u the tensor core runs dV(u) and S(u+1), and while they
-// start unit u+1 it runs dP(u+1), dK(u) and dQ^T(u). The double-buffered dQ^T
-// lets the drain of unit u overlap the MMAs of unit u+1.
+// [wait drain(u-3)] dQ^T(u-1); wait dS(u); dP(u+1); dK(u). The chain that
+// sets the pace is P(u) -> dV(u), S(u+1) -> P part of u+1; dQ^T(u-1), dP(u+1)
+// and dK(u) fill the tensor core while the compute warps run. dQ^T is double
+// buffered and issued one unit late, so the drain of a unit overlaps the MMAs
+// of the next two.
 // The dS^T buffer of unit u (128 KV rows x 64 query columns, bf16, 128-byte
 // swizzle, two buffers) serves both as the K-major A operand of dK and the
 // MN-major B operand of dQ^T.
@@ -61,6 +62,7 @@ struct BwdCfg {
   static constexpr int Q_TILE = 64 * D * 2;    // Q or dO half block: 64 rows
   static constexpr int BOXES = D / 64;
   static constexpr int STAGES = 3;
+  static constexpr int PREFETCH = 6;  // units ahead for the L2 prefetch of Q / dO tiles
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + KV_TILE;
   static constexpr int Q_OFF = V_OFF + KV_TILE;
@@ -241,6 +243,19 @@ __global__ void __launch_bounds__(448, 1)
         }
         bulk_load(smem + C::ROW_OFF + stage * 512, p.nl + (size_t)bh * p.Npad + r0, 256, fb);
         bulk_load(smem + C::ROW_OFF + stage * 512 + 256, p.dsum + (size_t)bh * p.Npad + r0, 256, fb);
+        // warm L2 for a unit further ahead: tile loads from HBM take several
+        // unit periods, more than the shared-memory ring covers
+        if (u + C::PREFETCH < U) {
+          const Unit pf = decode_unit(p, u + C::PREFETCH, L, kbeg, g, force_part, s_queue, C::QUEUE_CAP);
+          const int pr0 = pf.qb * 128 + pf.half * 64;
+          const int pbh = b * p.H_q + pf.h;
+          for (int x = 0; x < C::BOXES; ++x) {
+            tma_prefetch_l2_3d(&tq, x * 64, pr0, pbh);
+            tma_prefetch_l2_3d(&tdo, x * 64, pr0, pbh);
+          }
+          bulk_prefetch_l2(p.nl + (size_t)pbh * p.Npad + pr0, 256);
+          bulk_prefetch_l2(p.dsum + (size_t)pbh * p.Npad + pr0, 256);
+        }
       }
     }
   } else if (warp == 13) {
@@ -261,6 +276,22 @@ __global__ void __launch_bounds__(448, 1)
           const uint64_t bd = sdesc_sw128(b_base + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
           mma_ss(tbase + dst, ad, bd, id_s, k > 0 ? 1u : 0u);
         }
+      };
+      // dQ^T(v) = K^T dS^T(v) into TMEM buffer v&1, after the drain of unit v-2
+      auto issue_dq = [&](int v) -> bool {
+        if (v >= 2) {
+          if (!mbar_wait(&bars[C::B_DQEMPTY + (v & 1)], (uint32_t)((v >> 1) - 1) & 1u, abort_flag, p.err)) return false;
+          tc_fence_after();
+        }
+        const uint32_t sdsv = sdS + 16384u * (v & 1);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // 128 KV rows
+          const uint64_t ad = sdesc_sw128(sK + k * 2048, lbo_kt, 1024);
+          const uint64_t bd = sdesc_sw128(sdsv + k * 2048, 8192, 1024);
+          mma_ss(tbase + T_DQ + 64u * (v & 1), ad, bd, id_q, k > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[C::B_DQFULL + (v & 1)]);
+        return true;
       };
       bool ok = mbar_wait(&bars[C::B_KV], 0, abort_flag, p.err);
       tc_fence_after();
@@ -287,13 +318,21 @@ __global__ void __launch_bounds__(448, 1)
           const uint64_t bdo = sdesc_sw128(sdO + stage * C::Q_TILE + k * 2048, 8192, 1024);
           mma_ts(tbase + T_DV, a_t, bdo, id_g, (u > 0 || k > 0) ? 1u : 0u);
         }
-        // S^T(u+1) may overwrite P^T(u): dV(u) was issued first
+        // S^T(u+1) may overwrite P^T(u): dV(u) was issued first. It goes right
+        // after dV(u) because the compute warps' next P part waits for it.
         if (u + 1 < U) {
           ok = mbar_wait(&bars[C::B_QFULL + nstage], (uint32_t)((u + 1) / S) & 1u, abort_flag, p.err);
           tc_fence_after();
           if (!ok) break;
           issue_sk(sK, sQ + nstage * C::Q_TILE, T_S);
           mma_commit(&bars[C::B_SFULL]);
+        }
+        // dQ^T(u-1), deferred by one unit so that the drain of unit u-3 (same
+        // TMEM buffer) has a whole unit of slack; dS^T(u-1) stays in shared
+        // memory until dP(u+1), issued later, completes
+        if (u >= 1) {
+          ok = issue_dq(u - 1);
+          if (!ok) break;
         }
         // dS^T(u) is in shared memory and dP^T(u) has been read
         ok = mbar_wait(&bars[C::B_READY], (uint32_t)u & 1u, abort_flag, p.err);
@@ -310,19 +349,8 @@ __global__ void __launch_bounds__(448, 1)
           mma_ss(tbase + T_DK, ads, bq, id_g, (u > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(&bars[C::B_QEMPTY + stage]);
-        if (u >= 2) {  // dQ^T buffer u&1 was drained for unit u-2
-          ok = mbar_wait(&bars[C::B_DQEMPTY + (u & 1)], (uint32_t)((u >> 1) - 1) & 1u, abort_flag, p.err);
-          tc_fence_after();
-          if (!ok) break;
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {  // 128 KV rows
-          const uint64_t ad = sdesc_sw128(sK + k * 2048, lbo_kt, 1024);
-          const uint64_t bd = sdesc_sw128(sdsu + k * 2048, 8192, 1024);
-          mma_ss(tbase + T_DQ + 64u * (u & 1), ad, bd, id_q, k > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars[C::B_DQFULL + (u & 1)]);
       }
+      if (ok && U > 0) ok = issue_dq(U - 1);
       if (ok) mma_commit(&bars[C::B_FINAL]);
     }
   } else if (warp < 8) {
