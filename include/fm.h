@@ -149,6 +149,34 @@ fm_status fm_attn_bwd(const fm_problem* p, const void* q, const void* k, const v
                       void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Forward without a caller-provided workspace. (No counterpart in the pages:
+ * this is a convenience of the library, not part of the method.)
+ *
+ * Same computation, arguments and results as fm_attn_fwd, minus ws/ws_bytes.
+ * It is meant for callers that cannot allocate device memory at call time:
+ * for example a plugin inside a host framework that owns all device memory and
+ * gives its plugins no allocator, or a service that reserves its memory once
+ * at start-up and must not call cudaMalloc afterwards. Nothing here calls
+ * cudaMalloc, cudaFree or any allocating library routine.
+ *
+ * The forward's only scratch (its launch-order table, one int32 per Q block)
+ * lives instead in a fixed array inside the library, FM_NOALLOC_MAX_QBLOCKS
+ * entries (256 KiB) per GPU, held by every GPU that loads the library until the
+ * process exits. Problems with B * ceil(N / 128) > FM_NOALLOC_MAX_QBLOCKS are
+ * rejected with FM_ERR_WORKSPACE before anything is launched.
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.
+ * All calls on a device share the one array: calls that can overlap on the GPU
+ * (different streams without ordering between them) race on it and must be
+ * serialized by the caller. Every call rewrites the entries it uses, so nothing
+ * needs clearing between calls.
+ * ------------------------------------------------------------------------- */
+#define FM_NOALLOC_MAX_QBLOCKS 65536
+fm_status fm_attn_fwd_noalloc(const fm_problem* p, const void* q, const void* k, const void* v, const int32_t* lts,
+                              const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
+                              const int32_t* q_queue, void* o, float* lse, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Zero-communication mask localization (FlashMask-3 project page, §3.2):
  *   x_local = max_i [ clip(x - O_i, 0, C) + i*C*1(clip(x - O_i, 0, C) > 0) ]
  * = the number of the rank's rows before global row x, for a rank that owns

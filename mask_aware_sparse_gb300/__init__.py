@@ -56,6 +56,7 @@ _SIGS = {
                           + [_P, ctypes.c_size_t, _P]),
     "fm_attn_fwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
     "fm_attn_fwd": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 11 + [_P, ctypes.c_size_t, _P]),
+    "fm_attn_fwd_noalloc": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 11 + [_P]),
     "fm_attn_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
     "fm_attn_bwd": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 15 + [_P, ctypes.c_size_t, _P]),
     "fm_localize": (ctypes.c_int, [_P, ctypes.c_int64, _P, ctypes.c_int32, ctypes.c_int32, _P, _P]),

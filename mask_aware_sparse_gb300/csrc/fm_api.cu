@@ -212,6 +212,25 @@ fm_status fm_attn_fwd(const fm_problem* p, const void* q, const void* k, const v
                               static_cast<cudaStream_t>(stream), err));
 }
 
+fm_status fm_attn_fwd_noalloc(const fm_problem* p, const void* q, const void* k, const void* v, const int32_t* lts,
+                              const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
+                              const int32_t* q_queue, void* o, float* lse, void* stream) {
+  bool empty = false;
+  fm_status st = check_problem(p, &empty);
+  if (st != FM_OK || empty) return st;
+  if ((st = check_attn_shape(p)) != FM_OK) return st;
+  if (!q || !k || !v || !lts || !lte || !uts || !ute || !q_off || !q_queue || !o || !lse) return FM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FM_ERR_INVALID_ARG;
+  // the fixed scratch holds one entry per Q block of the whole batch
+  const int64_t qblocks = (int64_t)p->B * ((p->N + kTile - 1) / kTile);
+  if (qblocks > FM_NOALLOC_MAX_QBLOCKS) return FM_ERR_WORKSPACE;
+  int32_t* scratch = fwd_noalloc_scratch();
+  int* err = device_error_word();
+  if (!scratch || !err) return FM_ERR_CUDA;
+  return from_cuda(launch_fwd(*p, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, scratch,
+                              static_cast<cudaStream_t>(stream), err));
+}
+
 size_t fm_attn_bwd_workspace_bytes(const fm_problem* p) {
   bool empty = false;
   if (check_problem(p, &empty) != FM_OK || empty) return 0;

@@ -31,6 +31,7 @@
 //     the device from the queue offsets).
 #include <climits>
 #include <cmath>
+#include <mutex>
 #include <cuda.h>
 #include "fm_internal.h"
 #include "sm100.cuh"
@@ -480,7 +481,29 @@ cudaError_t launch_fwd_d(const fm_problem& P, const CUtensorMap& tq, const CUten
   return cudaGetLastError();
 }
 
+// Library-owned scratch for fm_attn_fwd_noalloc: the launch-order table
+// (one int32 per Q block). Fixed size, present on every device that loads the
+// library, shared by all calls on that device.
+static __device__ __align__(256) int32_t g_noalloc_order[FM_NOALLOC_MAX_QBLOCKS];
+
 }  // namespace
+
+int32_t* fwd_noalloc_scratch() {
+  // Host code cannot hand g_noalloc_order to a kernel directly (that name is
+  // a host-side stand-in); the device address is looked up once per device,
+  // with the device current, and cached.
+  static std::mutex mu;
+  static int32_t* cached[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_order) != cudaSuccess) return nullptr;
+    cached[dev] = static_cast<int32_t*>(ptr);
+  }
+  return cached[dev];
+}
 
 size_t fwd_ws_bytes(const fm_problem& p) {
   const size_t nQ = (size_t)(p.N + kTile - 1) / kTile;
