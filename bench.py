@@ -459,7 +459,10 @@ def run_ours(args, cfg):
 
 # ncu DRAM traffic (read + write bytes per launch) of the main kernels, valid
 # only while the kernel source is the one the counters were taken from.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    "bwd": {"file": "fm_bwd.cu", "sha256": "7464e9e10875c29009b4d3dc0898f6f2929c1c7b5d50f0f0ead148c35610337e", "bytes": 5852000000},
+    "fwd": {"file": "fm_fwd.cu", "sha256": "20a2a25436ffc25103fc53ff9704a62e0b45fd018dda97a46493feea4f2f5a50", "bytes": 599600000},
+}
 
 
 def ncu_traffic(kind: str):
