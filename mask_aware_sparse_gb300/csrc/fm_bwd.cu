@@ -541,44 +541,68 @@ __global__ void __launch_bounds__(448, 1)
   }
 }
 
-// D_i = sum_c dO_ic O_ic and nl_i = -LSE_i log2(e) (-inf for empty rows);
-// padded rows (N <= i < Npad) get nl = -inf, D = 0. One warp per row.
+// Row terms of the backward and a zeroed dQ accumulator, in one pass:
+//   D_i = sum_c dO_ic O_ic, nl_i = -LSE_i log2(e) (-inf for empty rows),
+//   dQacc row i = 0.
+// Padded rows (N <= i < Npad) get nl = -inf, D = 0. Each warp handles
+// kRowsPerWarp rows; a row of d bf16 is read as 16-byte vectors by d/8 lanes.
+constexpr int kRowsPerWarp = 8;
+
 template <int D>
-__global__ void bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-                               const float* __restrict__ lse, int BH, int N, int Npad, float* __restrict__ nl,
-                               float* __restrict__ dsum) {
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                      const __nv_bfloat16* __restrict__ dout,
+                                                      const float* __restrict__ lse, int BH, int N, int Npad,
+                                                      float* __restrict__ nl, float* __restrict__ dsum,
+                                                      float* __restrict__ dq_acc) {
+  constexpr int LPR = D / 8;         // lanes per row (16 bytes each)
+  constexpr int RPI = 32 / LPR;      // rows per warp-wide load
   const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (w >= (long long)BH * Npad) return;
+  const long long row0 = w * kRowsPerWarp;
+  const long long total = (long long)BH * Npad;
+  if (row0 >= total) return;
   const int lane = threadIdx.x & 31;
-  const int bh = (int)(w / Npad), i = (int)(w % Npad);
-  float acc = 0.f, nlv = -INFINITY;
-  if (i < N) {
-    const size_t base = ((size_t)bh * N + i) * D;
-    constexpr int PER = D / 32;  // 2 or 4 bf16 per lane
-    if (PER == 4) {
-      const uint2 a = *reinterpret_cast<const uint2*>(o + base + 4 * lane);
-      const uint2 c = *reinterpret_cast<const uint2*>(dout + base + 4 * lane);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+  const int sub = lane / LPR, col = (lane % LPR) * 8;
+  uint4 a[kRowsPerWarp / RPI], c[kRowsPerWarp / RPI];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(c2[e]);
-        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
-      }
+  for (int t = 0; t < kRowsPerWarp / RPI; ++t) {
+    const long long r = row0 + t * RPI + sub;
+    const int bh = (int)(r / Npad), i = (int)(r % Npad);
+    if (r < total && i < N) {
+      const size_t base = ((size_t)bh * N + i) * D + col;
+      a[t] = *reinterpret_cast<const uint4*>(o + base);
+      c[t] = *reinterpret_cast<const uint4*>(dout + base);
     } else {
-      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base + 2 * lane);
-      const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(dout + base + 2 * lane);
-      const float2 x = __bfloat1622float2(a), y = __bfloat1622float2(c);
-      acc = fmaf(x.x, y.x, x.y * y.y);
+      a[t] = c[t] = make_uint4(0, 0, 0, 0);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kRowsPerWarp / RPI; ++t) {
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[t]);
+    const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c[t]);
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(c2[e]);
+      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
-    const float l = lse[(size_t)bh * N + i];
-    nlv = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
-  }
-  if (lane == 0) {
-    nl[(size_t)bh * Npad + i] = nlv;
-    dsum[(size_t)bh * Npad + i] = (i < N) ? acc : 0.f;
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+    const long long r = row0 + t * RPI + sub;
+    const int bh = (int)(r / Npad), i = (int)(r % Npad);
+    if (r < total && lane % LPR == 0) {
+      float nlv = -INFINITY;
+      if (i < N) {
+        const float l = lse[(size_t)bh * N + i];
+        nlv = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+      }
+      nl[(size_t)bh * Npad + i] = nlv;
+      dsum[(size_t)bh * Npad + i] = (i < N) ? acc : 0.f;
+    }
+    if (r < total && i < N) {  // zero this row of the fp32 dQ accumulator (d floats = 2*LPR x 16 bytes)
+      float4* z = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * N + i) * D);
+      z[lane % LPR] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[lane % LPR + LPR] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 }
 
@@ -661,12 +685,12 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   const int nK = prm0.nK;
   const long long BH = (long long)P.B * P.H_q;
   // 1. row terms and a zeroed dQ accumulator
-  cudaError_t e = cudaMemsetAsync(w.dq_acc, 0, (size_t)BH * P.N * D * sizeof(float), s);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
   const long long rows = BH * prm0.Npad;
-  bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
-                                                              static_cast<const __nv_bfloat16*>(dout), lse, (int)BH,
-                                                              P.N, prm0.Npad, w.nl, w.dsum);
+  const long long warps = (rows + kRowsPerWarp - 1) / kRowsPerWarp;
+  bwd_pre_kernel<D><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                                               static_cast<const __nv_bfloat16*>(dout), lse,
+                                                               (int)BH, P.N, prm0.Npad, w.nl, w.dsum, w.dq_acc);
   // 2. LPT order of KV blocks
   lpt_order_kernel_bwd<<<1, 1024, 0, s>>>(prm0.k_off, P.B * nK, w.order);
   // 3. main kernel

@@ -11,10 +11,11 @@
 //                     vectors), coalesced loads + warp-shuffle reductions.
 //   2. classify_rows  one CTA per (b, qb): class of every tile of the row,
 //                     count of non-skipped tiles.
-//   3. count_cols     one thread per (b, kb): non-skipped tiles of the column.
-//   4. scan           exclusive prefix sums -> q_off, k_off (one CTA).
-//   5. emit_rows      one warp per (b, qb): descending-kb compaction by ballot.
-//   6. emit_cols      one warp per (b, kb): ascending-qb compaction by ballot.
+//      (the same kernel counts each column's non-skipped tiles with integer
+//      atomics; block_minmax zeroes those counters first)
+//   3. scan           exclusive prefix sums -> q_off, k_off (one CTA).
+//   4. emit_rows      one warp per (b, qb): descending-kb compaction by ballot.
+//   5. emit_cols      one warp per (b, kb): ascending-qb compaction by ballot.
 #include <climits>
 #include "fm_internal.h"
 #include "sm100.cuh"
@@ -34,7 +35,8 @@ __device__ __forceinline__ int clamp_flag(int x, int n, bool& bad) {
 
 __global__ void block_minmax_kernel(const int32_t* __restrict__ lts, const int32_t* __restrict__ lte,
                                     const int32_t* __restrict__ uts, const int32_t* __restrict__ ute, int B, int N,
-                                    int bn, int nK, Minmax* __restrict__ out, int* err) {
+                                    int bn, int nK, Minmax* __restrict__ out, int32_t* __restrict__ col_cnt,
+                                    int* err) {
   const int wpb = blockDim.x >> 5;
   const long long gw = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
   if (gw >= (long long)B * nK) return;
@@ -60,7 +62,10 @@ __global__ void block_minmax_kernel(const int32_t* __restrict__ lts, const int32
     r.v[2 * c] = __reduce_min_sync(0xffffffffu, mn[c]);
     r.v[2 * c + 1] = __reduce_max_sync(0xffffffffu, mx[c]);
   }
-  if (lane == 0) out[gw] = r;
+  if (lane == 0) {
+    out[gw] = r;
+    col_cnt[gw] = 0;  // per-column tile counts, accumulated by classify_rows_kernel
+  }
 }
 
 // Class of tile (q0,q1) x (k0,k1) from the block min/max.
@@ -72,7 +77,8 @@ __device__ __forceinline__ uint8_t tile_class(const Minmax& m, int q0, int q1, i
 }
 
 __global__ void classify_rows_kernel(const Minmax* __restrict__ mm, int N, int bm, int bn, int nQ, int nK, int causal,
-                                     uint8_t* __restrict__ cls, int32_t* __restrict__ row_cnt) {
+                                     uint8_t* __restrict__ cls, int32_t* __restrict__ row_cnt,
+                                     int32_t* __restrict__ col_cnt) {
   const int b = blockIdx.y, qb = blockIdx.x;
   const int q0 = qb * bm, q1 = min(q0 + bm, N);
   int cnt = 0;
@@ -82,6 +88,7 @@ __global__ void classify_rows_kernel(const Minmax* __restrict__ mm, int N, int b
     const uint8_t c = tile_class(mm[(size_t)b * nK + kb], q0, q1, k0, k1, causal);
     crow[kb] = c;
     cnt += (c != 0);
+    if (c != 0) atomicAdd(&col_cnt[(size_t)b * nK + kb], 1);
   }
   cnt = __reduce_add_sync(0xffffffffu, cnt);
   __shared__ int part[32];
@@ -92,16 +99,6 @@ __global__ void classify_rows_kernel(const Minmax* __restrict__ mm, int N, int b
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += part[w];
     row_cnt[(size_t)b * nQ + qb] = t;
   }
-}
-
-__global__ void count_cols_kernel(const uint8_t* __restrict__ cls, int B, int nQ, int nK, int32_t* __restrict__ col_cnt) {
-  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= (long long)B * nK) return;
-  const int b = (int)(t / nK), kb = (int)(t % nK);
-  const uint8_t* c = cls + (size_t)b * nQ * nK + kb;
-  int cnt = 0;
-  for (int qb = 0; qb < nQ; ++qb) cnt += (c[(size_t)qb * nK] != 0);
-  col_cnt[t] = cnt;
 }
 
 // Exclusive scan of cnt[0..n) into off[0..n] by one CTA of 1024 threads.
@@ -205,13 +202,12 @@ cudaError_t launch_classify(const fm_problem& p, int bm, int bn, int nQ, int nK,
   int32_t* col_cnt = reinterpret_cast<int32_t*>(w);
 
   const long long nkb = (long long)B * nK, nqb = (long long)B * nQ;
-  block_minmax_kernel<<<(unsigned)((nkb + 7) / 8), 256, 0, s>>>(lts, lte, uts, ute, B, N, bn, nK, mm, err);
-  classify_rows_kernel<<<dim3(nQ, B), 256, 0, s>>>(mm, N, bm, bn, nQ, nK, p.causal, tile_class, row_cnt);
-  count_cols_kernel<<<(unsigned)((nkb + 255) / 256), 256, 0, s>>>(tile_class, B, nQ, nK, col_cnt);
+  block_minmax_kernel<<<(unsigned)((nkb + 7) / 8), 256, 0, s>>>(lts, lte, uts, ute, B, N, bn, nK, mm, col_cnt, err);
+  classify_rows_kernel<<<dim3(nQ, B), 256, 0, s>>>(mm, N, bm, bn, nQ, nK, p.causal, tile_class, row_cnt, col_cnt);
   scan_kernel<<<2, 1024, 0, s>>>(row_cnt, (int)nqb, q_off, col_cnt, (int)nkb, k_off);
   emit_rows_kernel<<<(unsigned)((nqb + 7) / 8), 256, 0, s>>>(tile_class, B, nQ, nK, q_off, q_queue);
   emit_cols_kernel<<<(unsigned)((nkb + 7) / 8), 256, 0, s>>>(tile_class, B, nQ, nK, k_off, k_queue);
-  count_launches(6);
+  count_launches(5);
   return cudaGetLastError();
 }
 
