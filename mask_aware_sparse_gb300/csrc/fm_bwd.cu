@@ -86,7 +86,8 @@ struct BwdCfg {
   static constexpr int B_FINAL = B_DQEMPTY + 2;
   static constexpr int NBAR = B_FINAL + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int BYTES = MISC_OFF + 16;
+  static constexpr int XPOSE_OFF = (MISC_OFF + 16 + 127) / 128 * 128;  // 4 drain warps x 32 x 32 fp32
+  static constexpr int BYTES = XPOSE_OFF + 4 * 4096;
   static constexpr int SMEM_ALLOC = BYTES + 1024;
 };
 
@@ -264,18 +265,27 @@ __global__ void __launch_bounds__(448, 1)
       const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);  // S^T, dP^T: A K-major, B K-major
       const uint32_t id_g = idesc_bf16_f32(128, D, 0, 1);   // dV, dK: B MN-major
       const uint32_t id_q = idesc_bf16_f32(128, 64, 1, 1);  // dQ^T: A MN-major, B MN-major
-      const uint32_t sK = smem_u32(smem + C::K_OFF), sV = smem_u32(smem + C::V_OFF);
-      const uint32_t sQ = smem_u32(smem + C::Q_OFF), sdO = smem_u32(smem + C::DO_OFF);
-      const uint32_t sdS = smem_u32(smem + C::DS_OFF);
+      // Shared-memory descriptors are built once; per MMA only the start
+      // address field (bits 0-13, in 16-byte units) moves, so each issue is a
+      // 64-bit add of a constant. A slow issue path leaves the tensor core idle.
+      constexpr uint64_t kQStep = C::Q_TILE >> 4;  // one Q / dO stage
+      constexpr uint64_t kDsStep = 16384 >> 4;     // one dS^T buffer
       const uint32_t lbo_kt = (D == 128) ? 16384u : (uint32_t)(C::ZERO_OFF - C::K_OFF);
-      // S^T = K Q_u^T or dP^T = V dO_u^T into TMEM column `dst`
-      auto issue_sk = [&](uint32_t a_base, uint32_t b_base, uint32_t dst) {
+      const uint64_t dKk = sdesc_sw128(smem_u32(smem + C::K_OFF), 16, 1024);       // K, K-major A
+      const uint64_t dVk = sdesc_sw128(smem_u32(smem + C::V_OFF), 16, 1024);       // V, K-major A
+      const uint64_t dKt = sdesc_sw128(smem_u32(smem + C::K_OFF), lbo_kt, 1024);   // K^T, MN-major A
+      const uint64_t dQk = sdesc_sw128(smem_u32(smem + C::Q_OFF), 16, 1024);       // Q, K-major B
+      const uint64_t dOk = sdesc_sw128(smem_u32(smem + C::DO_OFF), 16, 1024);      // dO, K-major B
+      const uint64_t dQm = sdesc_sw128(smem_u32(smem + C::Q_OFF), 8192, 1024);     // Q, MN-major B
+      const uint64_t dOm = sdesc_sw128(smem_u32(smem + C::DO_OFF), 8192, 1024);    // dO, MN-major B
+      const uint64_t dSk = sdesc_sw128(smem_u32(smem + C::DS_OFF), 16, 1024);      // dS^T, K-major A
+      const uint64_t dSm = sdesc_sw128(smem_u32(smem + C::DS_OFF), 8192, 1024);    // dS^T, MN-major B
+      // S^T = K Q^T or dP^T = V dO^T (A, B K-major) into TMEM column `dst`
+      auto issue_sk = [&](uint64_t ad0, uint64_t bd0, uint32_t dst) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(b_base + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
-          mma_ss(tbase + dst, ad, bd, id_s, k > 0 ? 1u : 0u);
-        }
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tbase + dst, ad0 + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
+                 bd0 + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), id_s, k > 0 ? 1u : 0u);
       };
       // dQ^T(v) = K^T dS^T(v) into TMEM buffer v&1, after the drain of unit v-2
       auto issue_dq = [&](int v) -> bool {
@@ -283,13 +293,11 @@ __global__ void __launch_bounds__(448, 1)
           if (!mbar_wait(&bars[C::B_DQEMPTY + (v & 1)], (uint32_t)((v >> 1) - 1) & 1u, abort_flag, p.err)) return false;
           tc_fence_after();
         }
-        const uint32_t sdsv = sdS + 16384u * (v & 1);
+        const uint64_t bd0 = dSm + kDsStep * (uint64_t)(v & 1);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {  // 128 KV rows
-          const uint64_t ad = sdesc_sw128(sK + k * 2048, lbo_kt, 1024);
-          const uint64_t bd = sdesc_sw128(sdsv + k * 2048, 8192, 1024);
-          mma_ss(tbase + T_DQ + 64u * (v & 1), ad, bd, id_q, k > 0 ? 1u : 0u);
-        }
+        for (int k = 0; k < 8; ++k)  // 128 KV rows
+          mma_ss(tbase + T_DQ + 64u * (v & 1), dKt + (uint64_t)(k * 128), bd0 + (uint64_t)(k * 128), id_q,
+                 k > 0 ? 1u : 0u);
         mma_commit(&bars[C::B_DQFULL + (v & 1)]);
         return true;
       };
@@ -300,14 +308,15 @@ __global__ void __launch_bounds__(448, 1)
         tc_fence_after();
       }
       if (ok) {
-        issue_sk(sK, sQ, T_S);
+        issue_sk(dKk, dQk, T_S);
         mma_commit(&bars[C::B_SFULL]);
-        issue_sk(sV, sdO, T_DP);
+        issue_sk(dVk, dOk, T_DP);
         mma_commit(&bars[C::B_DPFULL]);
       }
       for (int u = 0; u < U && ok; ++u) {
         const int stage = u % S, nstage = (u + 1) % S;
-        const uint32_t sdsu = sdS + 16384u * (u & 1);
+        const uint64_t qoff = kQStep * (uint64_t)stage, nqoff = kQStep * (uint64_t)nstage;
+        const uint64_t dsoff = kDsStep * (uint64_t)(u & 1);
         // dV += P^T dO once P^T(u) is in TMEM (two 16-column blocks, one per half)
         ok = mbar_wait(&bars[C::B_PREADY], (uint32_t)u & 1u, abort_flag, p.err);
         tc_fence_after();
@@ -315,8 +324,7 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t a_t = tbase + T_S + (uint32_t)((k >> 1) * 32 + (k & 1) * 8);
-          const uint64_t bdo = sdesc_sw128(sdO + stage * C::Q_TILE + k * 2048, 8192, 1024);
-          mma_ts(tbase + T_DV, a_t, bdo, id_g, (u > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tbase + T_DV, a_t, dOm + qoff + (uint64_t)(k * 128), id_g, (u > 0 || k > 0) ? 1u : 0u);
         }
         // S^T(u+1) may overwrite P^T(u): dV(u) was issued first. It goes right
         // after dV(u) because the compute warps' next P part waits for it.
@@ -324,7 +332,7 @@ __global__ void __launch_bounds__(448, 1)
           ok = mbar_wait(&bars[C::B_QFULL + nstage], (uint32_t)((u + 1) / S) & 1u, abort_flag, p.err);
           tc_fence_after();
           if (!ok) break;
-          issue_sk(sK, sQ + nstage * C::Q_TILE, T_S);
+          issue_sk(dKk, dQk + nqoff, T_S);
           mma_commit(&bars[C::B_SFULL]);
         }
         // dQ^T(u-1), deferred by one unit so that the drain of unit u-3 (same
@@ -339,14 +347,13 @@ __global__ void __launch_bounds__(448, 1)
         tc_fence_after();
         if (!ok) break;
         if (u + 1 < U) {
-          issue_sk(sV, sdO + nstage * C::Q_TILE, T_DP);
+          issue_sk(dVk, dOk + nqoff, T_DP);
           mma_commit(&bars[C::B_DPFULL]);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint64_t ads = sdesc_sw128(sdsu + k * 32, 16, 1024);
-          const uint64_t bq = sdesc_sw128(sQ + stage * C::Q_TILE + k * 2048, 8192, 1024);
-          mma_ss(tbase + T_DK, ads, bq, id_g, (u > 0 || k > 0) ? 1u : 0u);
+          mma_ss(tbase + T_DK, dSk + dsoff + (uint64_t)(k * 2), dQm + qoff + (uint64_t)(k * 128), id_g,
+                 (u > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(&bars[C::B_QEMPTY + stage]);
       }
@@ -474,6 +481,7 @@ __global__ void __launch_bounds__(448, 1)
     const int w4 = warp - 8;
     const int c = (w4 << 5) + lane;  // head-dim index = TMEM lane
     const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
+    const uint32_t xp = smem_u32(smem + C::XPOSE_OFF) + w4 * 4096;
     bool ok = true;
     for (int u = 0; u < U && ok; ++u) {
       const Unit un = decode_unit(p, u, L, kbeg, g, force_part, s_queue, C::QUEUE_CAP);
@@ -487,22 +495,25 @@ __global__ void __launch_bounds__(448, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bars[C::B_DQEMPTY + pb]);
-      if (c < D) {
-        const int r0 = un.qb * 128 + un.half * 64;
-        float* dst = p.dq_acc + ((size_t)(b * p.H_q + un.h) * p.N + r0) * D + c;
-        const int nrow = min(64, p.N - r0);
-        if (nrow == 64) {
+      // Transpose through this warp's 4 KB of shared memory, 32 rows at a
+      // time, so that each lane adds four consecutive head-dim entries of one
+      // row: a warp instruction then covers four 128-byte row segments.
+      if ((w4 << 5) >= D) continue;  // d = 64: warps 10-11 hold no head-dim lanes
+      const int r0 = un.qb * 128 + un.half * 64;
+      const int nrow = min(64, p.N - r0);
+      float* dst = p.dq_acc + ((size_t)(b * p.H_q + un.h) * p.N + r0) * D + (w4 << 5) + ((lane & 7) << 2);
 #pragma unroll
-          for (int r = 0; r < 32; ++r) atomicAdd(dst + r * D, __uint_as_float(v0[r]));
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t* v = hh ? v1 : v0;
+        __syncwarp();
 #pragma unroll
-          for (int r = 0; r < 32; ++r) atomicAdd(dst + (32 + r) * D, __uint_as_float(v1[r]));
-        } else {
+        for (int r = 0; r < 32; ++r) sts_f32(xp + r * 128 + lane * 4, __uint_as_float(v[r]));
+        __syncwarp();
 #pragma unroll
-          for (int r = 0; r < 32; ++r)
-            if (r < nrow) atomicAdd(dst + r * D, __uint_as_float(v0[r]));
-#pragma unroll
-          for (int r = 0; r < 32; ++r)
-            if (32 + r < nrow) atomicAdd(dst + (32 + r) * D, __uint_as_float(v1[r]));
+        for (int i = 0; i < 8; ++i) {
+          const int row = 4 * i + (lane >> 3);
+          const float4 x = lds_f32x4(xp + row * 128 + (lane & 7) * 16);
+          if (32 * hh + row < nrow) red_add_v4_f32(dst + (size_t)(32 * hh + row) * D, x);
         }
       }
     }

@@ -246,7 +246,12 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 0);  // S = Q K^T, both K-major
       const uint32_t id_o = idesc_bf16_f32(128, D, 0, 1);    // O += P V, V is MN-major
-      const uint32_t sQ = smem_u32(smem + C::Q_OFF), sK = smem_u32(smem + C::K_OFF), sV = smem_u32(smem + C::V_OFF);
+      // descriptors built once; per MMA only the start-address field moves
+      // (a 64-bit add of a constant), which keeps the issue ahead of the tensor core
+      constexpr uint64_t kTileStep = C::TILE >> 4;
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + C::Q_OFF), 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::K_OFF), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::V_OFF), 16384, 1024);
       bool ok = mbar_wait(&bars[C::B_QFULL], 0, abort_flag, p.err);
       tc_fence_after();
       for (int j = 0; j <= n && ok; ++j) {
@@ -266,20 +271,18 @@ __global__ void __launch_bounds__(320, 1)
             tc_fence_after();
             if (!ok) break;
             const uint32_t tO = tbase + 256u + (uint32_t)(t * D);
+            const uint64_t vd = dV0 + kTileStep * (uint64_t)pslot;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint64_t bd = sdesc_sw128(sV + pslot * C::TILE + k * 2048, 16384, 1024);
-              mma_ts(tO, tS + (uint32_t)(k * 8), bd, id_o, (j > 1 || k > 0) ? 1u : 0u);
-            }
+            for (int k = 0; k < 8; ++k)
+              mma_ts(tO, tS + (uint32_t)(k * 8), vd + (uint64_t)(k * 128), id_o, (j > 1 || k > 0) ? 1u : 0u);
             mma_commit(&bars[C::B_ODONE + t]);
           }
           if (j < n) {
+            const uint64_t qd = dQ0 + kTileStep * (uint64_t)t, kd = dK0 + kTileStep * (uint64_t)slot;
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
-              const uint32_t off = (uint32_t)((k >> 2) * 16384 + (k & 3) * 32);
-              const uint64_t ad = sdesc_sw128(sQ + t * C::TILE + off, 16, 1024);
-              const uint64_t bd = sdesc_sw128(sK + slot * C::TILE + off, 16, 1024);
-              mma_ss(tS, ad, bd, id_s, k > 0 ? 1u : 0u);
+              const uint64_t off = (uint64_t)((k >> 2) * 1024 + (k & 3) * 2);
+              mma_ss(tS, qd + off, kd + off, id_s, k > 0 ? 1u : 0u);
             }
             mma_commit(&bars[C::B_SFULL + t]);
           }
