@@ -48,6 +48,7 @@
 #include <cmath>
 #include <cuda.h>
 #include "fm_internal.h"
+#include "mask_bits.cuh"
 #include "sm100.cuh"
 
 namespace fm {
@@ -127,15 +128,6 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams& p, int u, int L, in
   r.half = rem & 1;
   r.part = (e & 1) | (force_part ? 1 : 0);
   return r;
-}
-
-// Bits [a, b) of a 32-bit word (clipped to [0, 32)); 0 when the range is empty.
-__device__ __forceinline__ uint32_t rows_bits(int a, int b) {
-  a = max(a, 0);
-  b = min(b, 32);
-  if (a >= b) return 0u;
-  const uint32_t hi = (b == 32) ? 0xffffffffu : ((1u << b) - 1u);
-  return hi & ~((1u << a) - 1u);
 }
 
 template <int D>

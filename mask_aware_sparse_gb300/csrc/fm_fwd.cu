@@ -34,6 +34,7 @@
 #include <mutex>
 #include <cuda.h>
 #include "fm_internal.h"
+#include "mask_bits.cuh"
 #include "sm100.cuh"
 
 namespace fm {
@@ -310,6 +311,31 @@ __global__ void __launch_bounds__(320, 1)
         const int e = queue_at(j);
         const int kb = e >> 1;
         const bool part = (e & 1) || (kb == p.nK - 1 && (p.N & 127));
+        // Partial blocks: masked-row bits of this thread's query row over the
+        // block's 128 key columns, built while S is still being computed. Lane
+        // c of the warp builds the bits of key column 32k + c over the warp's
+        // 32 rows; a bit transpose hands each lane its own row.
+        uint32_t rb[4] = {0u, 0u, 0u, 0u};
+        if (part) {
+          const int ms = pidx % S;
+          ok = __all_sync(kFull, mbar_wait(&bars[C::B_MFULL + ms], (uint32_t)(pidx / S) & 1u, abort_flag, p.err));
+          if (!ok) break;
+          const uint32_t sm = smem_u32(smem + C::M_OFF + ms * C::M_BYTES);
+          const int w0 = q0 + ((warp & 3) << 5);
+          const int kc0 = kb * 128;
+          const bool causal = p.causal != 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int c = 32 * k + lane;
+            const int4 v = lds_s32x4(sm + 16 * c);  // {LTS, LTE, UTS, UTE} of key column kc0 + c
+            const uint32_t colbits = rows_bits(v.x - w0, v.y - w0) | rows_bits(v.z - w0, v.w - w0) |
+                                     (causal ? rows_bits(-w0, kc0 + c - w0) : 0u);
+            rb[k] = warp_transpose32(colbits, lane);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[C::B_MEMPTY + ms]);
+          ++pidx;
+        }
         ok = __all_sync(kFull, mbar_wait(&bars[C::B_SFULL + t], (uint32_t)j & 1u, abort_flag, p.err));
         if (!ok) break;
         tc_fence_after();
@@ -326,23 +352,9 @@ __global__ void __launch_bounds__(320, 1)
           tmem_ld_wait();
         }
         if (part) {
-          const int ms = pidx % S;
-          ok = __all_sync(kFull, mbar_wait(&bars[C::B_MFULL + ms], (uint32_t)(pidx / S) & 1u, abort_flag, p.err));
-          if (!ok) break;
-          const uint32_t sm = smem_u32(smem + C::M_OFF + ms * C::M_BYTES);
-          const int kc0 = kb * 128;
-          const bool causal = p.causal != 0;
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int4 v = lds_s32x4(sm + 16 * c);  // {LTS, LTE, UTS, UTE} of key column kc0 + c
-            // branch-free: the predicate differs between the rows (threads) of a warp
-            const bool msk = ((unsigned)(i - v.x) < (unsigned)(v.y - v.x)) |
-                             ((unsigned)(i - v.z) < (unsigned)(v.w - v.z)) | (causal & (i < kc0 + c));
-            sr[c] = msk ? __float_as_uint(-INFINITY) : sr[c];
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[C::B_MEMPTY + ms]);
-          ++pidx;
+          for (int c = 0; c < 128; ++c)
+            sr[c] = ((rb[c >> 5] >> (c & 31)) & 1u) ? __float_as_uint(-INFINITY) : sr[c];
         }
         float mx = -INFINITY;
 #pragma unroll
