@@ -63,7 +63,6 @@ struct BwdCfg {
   static constexpr int Q_TILE = 64 * D * 2;    // Q or dO half block: 64 rows
   static constexpr int BOXES = D / 64;
   static constexpr int STAGES = 3;
-  static constexpr int PREFETCH = 6;  // units ahead for the L2 prefetch of Q / dO tiles
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + KV_TILE;
   static constexpr int Q_OFF = V_OFF + KV_TILE;
@@ -236,19 +235,6 @@ __global__ void __launch_bounds__(448, 1)
         }
         bulk_load(smem + C::ROW_OFF + stage * 512, p.nl + (size_t)bh * p.Npad + r0, 256, fb);
         bulk_load(smem + C::ROW_OFF + stage * 512 + 256, p.dsum + (size_t)bh * p.Npad + r0, 256, fb);
-        // warm L2 for a unit further ahead: tile loads from HBM take several
-        // unit periods, more than the shared-memory ring covers
-        if (u + C::PREFETCH < U) {
-          const Unit pf = decode_unit(p, u + C::PREFETCH, L, kbeg, g, force_part, s_queue, C::QUEUE_CAP);
-          const int pr0 = pf.qb * 128 + pf.half * 64;
-          const int pbh = b * p.H_q + pf.h;
-          for (int x = 0; x < C::BOXES; ++x) {
-            tma_prefetch_l2_3d(&tq, x * 64, pr0, pbh);
-            tma_prefetch_l2_3d(&tdo, x * 64, pr0, pbh);
-          }
-          bulk_prefetch_l2(p.nl + (size_t)pbh * p.Npad + pr0, 256);
-          bulk_prefetch_l2(p.dsum + (size_t)pbh * p.Npad + pr0, 256);
-        }
       }
     }
   } else if (warp == 13) {
