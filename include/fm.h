@@ -121,7 +121,9 @@ fm_status fm_classify_tiles(const fm_problem* p, const fm_tiling* t, const int32
  * A query row with no visible key gets O = 0 and LSE = -inf.
  *
  * q_off / q_queue must come from fm_classify_tiles with the fm_attn_tiling
- * tiling and the same problem and mask. d must be 64 or 128.
+ * tiling and the same problem and mask. d must be 64 or 128. Mask values
+ * outside [0, N] are clamped; the forward does not flag them again
+ * (fm_classify_tiles on the same vectors does).
  * Workspace: fm_attn_fwd_workspace_bytes (may be 0 bytes -> ws may be NULL).
  * ------------------------------------------------------------------------- */
 size_t fm_attn_fwd_workspace_bytes(const fm_problem* p);

@@ -49,7 +49,7 @@ struct FwdCfg {
   static constexpr int K_OFF = Q_OFF + 2 * TILE;
   static constexpr int V_OFF = K_OFF + STAGES * TILE;
   static constexpr int M_OFF = V_OFF + STAGES * TILE;
-  static constexpr int M_BYTES = 128 * 16;  // int4 {LTS, LTE, UTS, UTE} per column
+  static constexpr int M_BYTES = 4 * 128 * 4;  // LTS[128], LTE[128], UTS[128], UTE[128]
   static constexpr int QUEUE_CAP = 1024;    // queue entries staged in shared memory
   static constexpr int QUEUE_OFF = M_OFF + STAGES * M_BYTES;
   static constexpr int BAR_OFF = QUEUE_OFF + QUEUE_CAP * 4;
@@ -202,33 +202,41 @@ __global__ void __launch_bounds__(320, 1)
       ok = __shfl_sync(kFull, ok, 0);
       if (!ok) break;
       if (part) {
+        // the block's four mask vectors, raw, as 4 x 128 int32 (LTS, LTE, UTS,
+        // UTE); the softmax warps clamp and check them
         const int ms = pidx % S;
         const uint32_t mph = (uint32_t)(pidx / S) & 1u;
         ok = __all_sync(kFull, mbar_wait(&bars[C::B_MEMPTY + ms], mph ^ 1u, abort_flag, p.err));
         if (!ok) break;
-        int4* sm = reinterpret_cast<int4*>(smem + C::M_OFF + ms * C::M_BYTES);
-        bool bad = false;
-        for (int c = lane; c < 128; c += 32) {
-          const int col = kb * 128 + c;
-          int4 v;
-          if (col < p.N) {
-            int a0 = p.lts[vbase + col], a1 = p.lte[vbase + col], u0 = p.uts[vbase + col], u1 = p.ute[vbase + col];
-            bad |= (a0 < 0) | (a0 > p.N) | (a1 < 0) | (a1 > p.N) | (u0 < 0) | (u0 > p.N) | (u1 < 0) | (u1 > p.N);
-            a0 = min(max(a0, 0), p.N);
-            a1 = min(max(a1, 0), p.N);
-            u0 = min(max(u0, 0), p.N);
-            u1 = min(max(u1, 0), p.N);
-            if (a0 >= a1) a0 = a1 = 0;  // empty interval
-            if (u0 >= u1) u0 = u1 = 0;
-            v = make_int4(a0, a1, u0, u1);
-          } else {
-            v = make_int4(0, INT_MAX, 0, 0);  // key beyond N: masked for every row
+        uint8_t* sm = smem + C::M_OFF + ms * C::M_BYTES;
+        const int c0 = kb * 128;
+        const size_t o = vbase + c0;
+        const bool aligned = ((reinterpret_cast<uintptr_t>(p.lts + o) | reinterpret_cast<uintptr_t>(p.lte + o) |
+                               reinterpret_cast<uintptr_t>(p.uts + o) | reinterpret_cast<uintptr_t>(p.ute + o)) &
+                              15u) == 0;
+        if (c0 + 128 <= p.N && aligned) {
+          // whole block in range and 16-byte aligned: four bulk copies
+          if (lane == 0) {
+            uint64_t* fb = &bars[C::B_MFULL + ms];
+            mbar_arrive_expect_tx(fb, 4 * 512);
+            bulk_load(sm + 0, p.lts + o, 512, fb);
+            bulk_load(sm + 512, p.lte + o, 512, fb);
+            bulk_load(sm + 1024, p.uts + o, 512, fb);
+            bulk_load(sm + 1536, p.ute + o, 512, fb);
           }
-          sm[c] = v;
+        } else {
+          int* v = reinterpret_cast<int*>(sm);
+          for (int c = lane; c < 128; c += 32) {
+            const int col = c0 + c;
+            const bool in = col < p.N;  // a key beyond N is masked for every row
+            v[c] = in ? p.lts[vbase + col] : 0;
+            v[128 + c] = in ? p.lte[vbase + col] : p.N;
+            v[256 + c] = in ? p.uts[vbase + col] : 0;
+            v[384 + c] = in ? p.ute[vbase + col] : 0;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[C::B_MFULL + ms]);
         }
-        if (__any_sync(kFull, bad) && lane == 0) record_error(p.err, FM_DEV_ERR_RANGE);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[C::B_MFULL + ms]);
         ++pidx;
       }
       if (lane == 0) {
@@ -324,12 +332,15 @@ __global__ void __launch_bounds__(320, 1)
           const int w0 = q0 + ((warp & 3) << 5);
           const int kc0 = kb * 128;
           const bool causal = p.causal != 0;
+          // Values outside [0, N] only need clamping here: fm_classify_tiles,
+          // run on the same vectors, flags them.
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int c = 32 * k + lane;
-            const int4 v = lds_s32x4(sm + 16 * c);  // {LTS, LTE, UTS, UTE} of key column kc0 + c
-            const uint32_t colbits = rows_bits(v.x - w0, v.y - w0) | rows_bits(v.z - w0, v.w - w0) |
-                                     (causal ? rows_bits(-w0, kc0 + c - w0) : 0u);
+            const int a0 = lds_s32(sm + 4 * c), a1 = lds_s32(sm + 512 + 4 * c);  // LTS, LTE of key column kc0 + c
+            const int u0 = lds_s32(sm + 1024 + 4 * c), u1 = lds_s32(sm + 1536 + 4 * c);  // UTS, UTE
+            const uint32_t colbits = window_bits(a0, a1, w0) | window_bits(u0, u1, w0) |
+                                     (causal ? window_bits(w0, kc0 + c, w0) : 0u);
             rb[k] = warp_transpose32(colbits, lane);
           }
           __syncwarp();

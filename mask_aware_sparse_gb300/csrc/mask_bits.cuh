@@ -15,6 +15,18 @@ __device__ __forceinline__ uint32_t rows_bits(int a, int b) {
   return hi & ~((1u << a) - 1u);
 }
 
+// Bits of the rows [a, b) that fall in the 32-row window [w0, w0 + 32), as
+// offsets from w0. Any int32 a, b (no overflow): the bounds are first clamped
+// to the window, which for rows of the window is the same as clamping them
+// to [0, N].
+__device__ __forceinline__ uint32_t window_bits(int a, int b, int w0) {
+  const int lo = min(max(a, w0), w0 + 32) - w0;
+  const int hi = min(max(b, w0), w0 + 32) - w0;
+  const uint32_t hm = (hi >= 32) ? 0xffffffffu : ((1u << hi) - 1u);
+  const uint32_t lm = (lo >= 32) ? 0xffffffffu : ((1u << lo) - 1u);
+  return hm & ~lm;  // empty when hi <= lo
+}
+
 // Transpose a 32 x 32 bit matrix held one row per lane (bit c of lane r's word
 // is element (r, c)): on return lane r holds column r (bit c = element (c, r)).
 // Recursive block swap: at step j, lanes exchange the off-diagonal j x j blocks
