@@ -460,8 +460,8 @@ def run_ours(args, cfg):
 # ncu DRAM traffic (read + write bytes per launch) of the main kernels, valid
 # only while the kernel source is the one the counters were taken from.
 NCU_TRAFFIC = {
-    "bwd": {"file": "fm_bwd.cu", "sha256": "7464e9e10875c29009b4d3dc0898f6f2929c1c7b5d50f0f0ead148c35610337e", "bytes": 5852000000},
-    "fwd": {"file": "fm_fwd.cu", "sha256": "20a2a25436ffc25103fc53ff9704a62e0b45fd018dda97a46493feea4f2f5a50", "bytes": 599600000},
+    "bwd": {"file": "fm_bwd.cu", "sha256": "d1a1290b91889652b4fe5aa8cad86283896ae56651f670729d396ad6b4e1ffa4", "bytes": 5620876000},
+    "fwd": {"file": "fm_fwd.cu", "sha256": "f8bf50c7d8f8fb8c33a5c71b6c2c5eb1d6814360c389d39095cd4f501400f0e7", "bytes": 607274752},
 }
 
 
