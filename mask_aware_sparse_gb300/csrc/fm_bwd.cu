@@ -551,12 +551,22 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   if (row0 >= total) return;
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, col = (lane % LPR) * 8;
+  // Rows with no visible key (LSE = -inf) have P = 0, hence dS = 0 and dQ = 0:
+  // their O / dO are not read and their accumulator rows are not zeroed
+  // (reductions only ever add exact zeros there; dq_convert writes 0 for them).
   uint4 a[kRowsPerWarp / RPI], c[kRowsPerWarp / RPI];
+  float lrow[kRowsPerWarp / RPI];
 #pragma unroll
   for (int t = 0; t < kRowsPerWarp / RPI; ++t) {
     const long long r = row0 + t * RPI + sub;
     const int bh = (int)(r / Npad), i = (int)(r % Npad);
-    if (r < total && i < N) {
+    lrow[t] = (r < total && i < N) ? lse[(size_t)bh * N + i] : -INFINITY;
+  }
+#pragma unroll
+  for (int t = 0; t < kRowsPerWarp / RPI; ++t) {
+    const long long r = row0 + t * RPI + sub;
+    const int bh = (int)(r / Npad), i = (int)(r % Npad);
+    if (lrow[t] != -INFINITY) {
       const size_t base = ((size_t)bh * N + i) * D + col;
       a[t] = *reinterpret_cast<const uint4*>(o + base);
       c[t] = *reinterpret_cast<const uint4*>(dout + base);
@@ -579,15 +589,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     const long long r = row0 + t * RPI + sub;
     const int bh = (int)(r / Npad), i = (int)(r % Npad);
     if (r < total && lane % LPR == 0) {
-      float nlv = -INFINITY;
-      if (i < N) {
-        const float l = lse[(size_t)bh * N + i];
-        nlv = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
-      }
-      nl[(size_t)bh * Npad + i] = nlv;
-      dsum[(size_t)bh * Npad + i] = (i < N) ? acc : 0.f;
+      const float l = lrow[t];
+      nl[(size_t)bh * Npad + i] = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+      dsum[(size_t)bh * Npad + i] = acc;  // 0 for empty and padded rows
     }
-    if (r < total && i < N) {  // zero this row of the fp32 dQ accumulator (d floats = 2*LPR x 16 bytes)
+    if (lrow[t] != -INFINITY) {  // zero this row of the fp32 dQ accumulator (d floats = 2*LPR x 16 bytes)
       float4* z = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * N + i) * D);
       z[lane % LPR] = make_float4(0.f, 0.f, 0.f, 0.f);
       z[lane % LPR + LPR] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -595,14 +601,22 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   }
 }
 
-__global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long long n8,
-                                  float scale) {
+// dQ = bf16(scale * dQacc); rows with no visible key (exponent offset -inf)
+// are written as 0 without reading their (never zeroed) accumulator rows.
+template <int D>
+__global__ void dq_convert_kernel(const float* __restrict__ acc, const float* __restrict__ nl,
+                                  __nv_bfloat16* __restrict__ dq, long long n8, int N, int Npad, float scale) {
   for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n8; t += (long long)gridDim.x * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(acc)[2 * t];
-    const float4 c = reinterpret_cast<const float4*>(acc)[2 * t + 1];
-    reinterpret_cast<uint4*>(dq)[t] =
-        make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
-                   pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
+    const long long row = (8 * t) / D;  // (bh, i) row of the (B*H_q, N, d) tensors
+    const long long bh = row / N, i = row - bh * N;
+    uint4 out = make_uint4(0, 0, 0, 0);
+    if (nl[bh * Npad + i] != -INFINITY) {
+      const float4 a = reinterpret_cast<const float4*>(acc)[2 * t];
+      const float4 c = reinterpret_cast<const float4*>(acc)[2 * t + 1];
+      out = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                       pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
+    }
+    reinterpret_cast<uint4*>(dq)[t] = out;
   }
 }
 
@@ -703,7 +717,8 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   const long long n8 = BH * P.N * D / 8;
   long long blocks = (n8 + 255) / 256;
   if (blocks > 152 * 32) blocks = 152 * 32;
-  dq_convert_kernel<<<(unsigned)blocks, 256, 0, s>>>(w.dq_acc, static_cast<__nv_bfloat16*>(dq), n8, P.scale);
+  dq_convert_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(w.dq_acc, w.nl, static_cast<__nv_bfloat16*>(dq), n8, P.N,
+                                                        prm0.Npad, P.scale);
   count_launches(4);  // row terms, LPT order, main kernel, dQ convert
   return cudaGetLastError();
 }
