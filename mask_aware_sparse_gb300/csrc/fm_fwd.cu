@@ -63,7 +63,8 @@ struct FwdCfg {
   static constexpr int B_SFULL = B_MEMPTY + STAGES;  // [2]
   static constexpr int B_PREADY = B_SFULL + 2;       // [2]
   static constexpr int B_ODONE = B_PREADY + 2;       // [2]
-  static constexpr int NBAR = B_ODONE + 2;
+  static constexpr int B_OSTAGED = B_ODONE + 2;      // [2]
+  static constexpr int NBAR = B_OSTAGED + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
@@ -90,7 +91,7 @@ constexpr unsigned kFull = 0xffffffffu;
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-               const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, const FwdParams p) {
   using C = FwdCfg<D>;
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -143,6 +144,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&bars[C::B_SFULL + t], 1);
       mbar_init(&bars[C::B_PREADY + t], 128);
       mbar_init(&bars[C::B_ODONE + t], 1);
+      mbar_init(&bars[C::B_OSTAGED + t], 128);
     }
     fence_mbar_init();
   }
@@ -421,23 +423,34 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_ODONE + t], (uint32_t)(n - 1) & 1u, abort_flag, p.err));
       if (ok) {
+        // O rows go through this head's Q tile in shared memory (free: every S
+        // MMA finished before the last PV) in the 128-byte-swizzled box layout,
+        // then one TMA store writes the tile; rows beyond N are clipped by it.
         tc_fence_after();
         const size_t bh = (size_t)b * p.H_q + h0 + t;
         const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        uint8_t* stage = smem + C::Q_OFF + t * C::TILE;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t r[32];
           tmem_ld32(tO + c0, r);
           tmem_ld_wait();
-          if (i < p.N) {
-            uint4* dst = reinterpret_cast<uint4*>(p.o + (bh * p.N + i) * D + c0);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              const float* f = reinterpret_cast<const float*>(&r[8 * v4]);
-              dst[v4] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
-                                   pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
-            }
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const float* f = reinterpret_cast<const float*>(&r[8 * v4]);
+            const int col = c0 + 8 * v4;  // first of 8 columns = one 16-byte chunk
+            const uint32_t addr = smem_u32(stage + (col >> 6) * 16384 + row * 128 +
+                                           ((((col & 63) >> 3) ^ (row & 7)) << 4));
+            sts_b32x4(addr, pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
+                      pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
           }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[C::B_OSTAGED + t]);
+        if (row == 0 && mbar_wait(&bars[C::B_OSTAGED + t], 0, abort_flag, p.err)) {
+          for (int x = 0; x < C::BOXES; ++x) tma_store_3d(&to, stage + x * 16384, x * 64, q0, (int)bh);
+          bulk_commit_group();
+          bulk_wait_group_read0();
         }
         if (i < p.N) p.lse[bh * p.N + i] = (l_run > 0.f) ? (m_run * kLn2 + logf(l_run)) : -INFINITY;
       }
@@ -491,7 +504,7 @@ __global__ void __launch_bounds__(1024) lpt_order_kernel(const int32_t* __restri
 
 template <int D>
 cudaError_t launch_fwd_d(const fm_problem& P, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdParams& prm, unsigned grid, cudaStream_t s) {
+                         const CUtensorMap& to, const FwdParams& prm, unsigned grid, cudaStream_t s) {
   using C = FwdCfg<D>;
   static bool attr_done = false;
   if (!attr_done) {
@@ -501,7 +514,7 @@ cudaError_t launch_fwd_d(const fm_problem& P, const CUtensorMap& tq, const CUten
   }
   {
     KernelTimer timer(s, kTimedFwd);
-    fwd_kernel<D><<<grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, prm);
+    fwd_kernel<D><<<grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, to, prm);
   }
   count_launches(2);  // LPT order + main kernel
   return cudaGetLastError();
@@ -546,9 +559,9 @@ cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const 
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
   int32_t* order = static_cast<int32_t*>(ws);
   lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, P.B * nQ, order);
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!make_tmap_bhnd(&tq, q, (int64_t)P.B * P.H_q, P.N, P.d) || !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, P.N, P.d) ||
-      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, P.N, P.d))
+      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, P.N, P.d) || !make_tmap_bhnd(&to, o, (int64_t)P.B * P.H_q, P.N, P.d))
     return cudaErrorInvalidValue;
   FwdParams prm;
   prm.lts = lts;
@@ -571,8 +584,8 @@ cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const 
   prm.causal = P.causal ? 1 : 0;
   prm.scale_log2 = P.scale * 1.4426950408889634f;
   prm.err = err;
-  if (P.d == 128) return launch_fwd_d<128>(P, tq, tk, tv, prm, (unsigned)grid, s);
-  return launch_fwd_d<64>(P, tq, tk, tv, prm, (unsigned)grid, s);
+  if (P.d == 128) return launch_fwd_d<128>(P, tq, tk, tv, to, prm, (unsigned)grid, s);
+  return launch_fwd_d<64>(P, tq, tk, tv, to, prm, (unsigned)grid, s);
 }
 
 }  // namespace fm
