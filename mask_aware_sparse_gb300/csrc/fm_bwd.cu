@@ -85,7 +85,9 @@ struct BwdCfg {
   static constexpr int B_DQFULL = B_READY + 1;    // [2]
   static constexpr int B_DQEMPTY = B_DQFULL + 2;  // [2]
   static constexpr int B_FINAL = B_DQEMPTY + 2;
-  static constexpr int NBAR = B_FINAL + 1;
+  static constexpr int B_VSTAGED = B_FINAL + 1;  // dV rows staged for the TMA store
+  static constexpr int B_KSTAGED = B_VSTAGED + 1;
+  static constexpr int NBAR = B_KSTAGED + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int XPOSE_OFF = (MISC_OFF + 16 + 127) / 128 * 128;  // 4 drain warps x 32 x 32 fp32
   static constexpr int BYTES = XPOSE_OFF + 4 * 4096;
@@ -133,7 +135,8 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams& p, int u, int L, in
 template <int D>
 __global__ void __launch_bounds__(480, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const BwdParams p) {
+               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+               const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv, const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -185,6 +188,8 @@ __global__ void __launch_bounds__(480, 1)
       mbar_init(&bars[C::B_DQEMPTY + x], 128);
     }
     mbar_init(&bars[C::B_FINAL], 2);
+    mbar_init(&bars[C::B_VSTAGED], 128);
+    mbar_init(&bars[C::B_KSTAGED], 128);
     fence_mbar_init();
   }
   const uint32_t s_queue = smem_u32(smem + C::QUEUE_OFF);
@@ -448,25 +453,32 @@ __global__ void __launch_bounds__(480, 1)
       fence_proxy_async_smem();
       mbar_arrive(&bars[C::B_READY]);
     }
-    // epilogue: dV rows (warps 0-3)
+    // epilogue: dV rows (warps 0-3), staged in the V tile (free once every MMA
+    // is done) in the 128-byte-swizzled box layout and written by a TMA store
     if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_FINAL], 0, abort_flag, p.err));
     if (ok && half == 0) {
       tc_fence_after();
-      const size_t row = ((size_t)b * p.H_kv + g) * p.N + kcol;
+      uint8_t* stage = smem + C::V_OFF;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(tbase + lane_off + T_DV + c0, r);
         tmem_ld_wait();
-        if (!dead) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dv + row * D + c0);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            const float* f = reinterpret_cast<const float*>(&r[8 * v4]);
-            dst[v4] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                                 pack_bf16x2(f[6], f[7]));
-          }
+        for (int v4 = 0; v4 < 4; ++v4) {
+          const float* f = reinterpret_cast<const float*>(&r[8 * v4]);
+          const int col = c0 + 8 * v4;
+          sts_b32x4(smem_u32(stage + (col >> 6) * 16384 + j * 128 + ((((col & 63) >> 3) ^ (j & 7)) << 4)),
+                    pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
         }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[C::B_VSTAGED]);
+      if (threadIdx.x == 0 && mbar_wait(&bars[C::B_VSTAGED], 0, abort_flag, p.err)) {
+        for (int x = 0; x < C::BOXES; ++x) tma_store_3d(&tdv, stage + x * 16384, x * 64, k0, b * p.H_kv + g);
+        bulk_commit_group();
+        bulk_wait_group_read0();
       }
     }
   } else {
@@ -510,28 +522,33 @@ __global__ void __launch_bounds__(480, 1)
         }
       }
     }
-    // epilogue: dK rows (thread = KV row j = TMEM lane)
+    // epilogue: dK rows (thread = KV row j = TMEM lane), staged in the K tile
     if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_FINAL], 0, abort_flag, p.err));
     if (ok) {
       tc_fence_after();
       const int j = c;
-      const int kcol = k0 + j;
-      const size_t row = ((size_t)b * p.H_kv + g) * p.N + kcol;
+      uint8_t* stage = smem + C::K_OFF;
+      const float sc = p.scale;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(tbase + lane_off + T_DK + c0, r);
         tmem_ld_wait();
-        if (kcol < p.N) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dk + row * D + c0);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            const float* f = reinterpret_cast<const float*>(&r[8 * v4]);
-            const float sc = p.scale;
-            dst[v4] = make_uint4(pack_bf16x2(f[0] * sc, f[1] * sc), pack_bf16x2(f[2] * sc, f[3] * sc),
-                                 pack_bf16x2(f[4] * sc, f[5] * sc), pack_bf16x2(f[6] * sc, f[7] * sc));
-          }
+        for (int v4 = 0; v4 < 4; ++v4) {
+          const float* f = reinterpret_cast<const float*>(&r[8 * v4]);
+          const int col = c0 + 8 * v4;
+          sts_b32x4(smem_u32(stage + (col >> 6) * 16384 + j * 128 + ((((col & 63) >> 3) ^ (j & 7)) << 4)),
+                    pack_bf16x2(f[0] * sc, f[1] * sc), pack_bf16x2(f[2] * sc, f[3] * sc),
+                    pack_bf16x2(f[4] * sc, f[5] * sc), pack_bf16x2(f[6] * sc, f[7] * sc));
         }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[C::B_KSTAGED]);
+      if (threadIdx.x == 256 && mbar_wait(&bars[C::B_KSTAGED], 0, abort_flag, p.err)) {
+        for (int x = 0; x < C::BOXES; ++x) tma_store_3d(&tdk, stage + x * 16384, x * 64, k0, b * p.H_kv + g);
+        bulk_commit_group();
+        bulk_wait_group_read0();
       }
     }
   }
@@ -712,10 +729,12 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   // 2. LPT order of KV blocks
   lpt_order_kernel_bwd<<<1, 1024, 0, s>>>(prm0.k_off, P.B * nK, w.order);
   // 3. main kernel
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if (!make_tmap_bhnd(&tq, q, BH, P.N, D, 64) || !make_tmap_bhnd(&tdo, dout, BH, P.N, D, 64) ||
       !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, P.N, D, 128) ||
-      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, P.N, D, 128))
+      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, P.N, D, 128) ||
+      !make_tmap_bhnd(&tdk, prm0.dk, (int64_t)P.B * P.H_kv, P.N, D, 128) ||
+      !make_tmap_bhnd(&tdv, prm0.dv, (int64_t)P.B * P.H_kv, P.N, D, 128))
     return cudaErrorInvalidValue;
   static bool attr_done = false;
   if (!attr_done) {
@@ -726,7 +745,7 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   const long long grid = (long long)P.B * nK * P.H_kv;
   {
     KernelTimer timer(s, kTimedBwd);
-    bwd_kernel<D><<<(unsigned)grid, 480, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, prm0);
+    bwd_kernel<D><<<(unsigned)grid, 480, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, prm0);
   }
   // 4. dQ = bf16(scale * dQacc)
   const long long n8 = BH * P.N * D / 8;
