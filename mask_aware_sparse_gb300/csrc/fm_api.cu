@@ -56,6 +56,19 @@ bool make_tmap_bhnd(void* out, const void* base, int64_t BH, int64_t N, int64_t 
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_f32_bhnd(void* out, const void* base, int64_t BH, int64_t N, int64_t d, int box_cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)(d * 4), (cuuint64_t)(N * d * 4)};
+  cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(static_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- measurement
 namespace {
 std::atomic<long long> g_launches{0};

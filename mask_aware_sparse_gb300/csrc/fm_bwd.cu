@@ -136,7 +136,8 @@ template <int D>
 __global__ void __launch_bounds__(480, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-               const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv, const BwdParams p) {
+               const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
+               const __grid_constant__ CUtensorMap tdq, const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -500,28 +501,28 @@ __global__ void __launch_bounds__(480, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bars[C::B_DQEMPTY + pb]);
-      // Transpose through this warp's 4 KB of shared memory, 32 rows at a
-      // time, so that each lane adds four consecutive head-dim entries of one
-      // row: a warp instruction then covers four 128-byte row segments.
+      // The 32 x 64 slice goes through this warp's 4 KB of shared memory, 32
+      // rows at a time, in row-major order, and a TMA reduce-add sends each
+      // 32 x 32 box to the fp32 accumulator (rows beyond N are skipped by it).
       if ((w4 << 5) >= D) continue;  // d = 64: warps 10-11 hold no head-dim lanes
       const int r0 = un.qb * 128 + un.half * 64;
-      const int nrow = min(64, p.N - r0);
-      float* dst = p.dq_acc + ((size_t)(b * p.H_q + un.h) * p.N + r0) * D + (w4 << 5) + ((lane & 7) << 2);
+      const int bh = b * p.H_q + un.h;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const uint32_t* v = hh ? v1 : v0;
+        if (lane == 0) bulk_wait_group_read0();  // the previous box has been read out
         __syncwarp();
 #pragma unroll
         for (int r = 0; r < 32; ++r) sts_f32(xp + r * 128 + lane * 4, __uint_as_float(v[r]));
+        fence_proxy_async_smem();
         __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int row = 4 * i + (lane >> 3);
-          const float4 x = lds_f32x4(xp + row * 128 + (lane & 7) * 16);
-          if (32 * hh + row < nrow) red_add_v4_f32(dst + (size_t)(32 * hh + row) * D, x);
+        if (lane == 0) {
+          tma_reduce_add_3d(&tdq, smem + C::XPOSE_OFF + w4 * 4096, w4 << 5, r0 + 32 * hh, bh);
+          bulk_commit_group();
         }
       }
     }
+    if (lane == 0) bulk_wait_group_read0();
     // epilogue: dK rows (thread = KV row j = TMEM lane), staged in the K tile
     if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_FINAL], 0, abort_flag, p.err));
     if (ok) {
@@ -736,6 +737,9 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
       !make_tmap_bhnd(&tdk, prm0.dk, (int64_t)P.B * P.H_kv, P.N, D, 128) ||
       !make_tmap_bhnd(&tdv, prm0.dv, (int64_t)P.B * P.H_kv, P.N, D, 128))
     return cudaErrorInvalidValue;
+  CUtensorMap tdq;
+  if (!make_tmap_f32_bhnd(&tdq, w.dq_acc, BH, P.N, D, 32, 32))
+    return cudaErrorInvalidValue;
   static bool attr_done = false;
   if (!attr_done) {
     e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
@@ -745,7 +749,7 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   const long long grid = (long long)P.B * nK * P.H_kv;
   {
     KernelTimer timer(s, kTimedBwd);
-    bwd_kernel<D><<<(unsigned)grid, 480, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, prm0);
+    bwd_kernel<D><<<(unsigned)grid, 480, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm0);
   }
   // 4. dQ = bf16(scale * dQacc)
   const long long n8 = BH * P.N * D / 8;

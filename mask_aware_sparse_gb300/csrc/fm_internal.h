@@ -45,6 +45,10 @@ cudaError_t launch_bwd(const fm_problem& p, const void* q, const void* k, const 
 // box {64, box_rows, 1}, 128-byte swizzle; rows >= N read as zero.
 bool make_tmap_bhnd(void* out_tmap /* CUtensorMap* */, const void* base, int64_t BH, int64_t N, int64_t d,
                     int box_rows = 128);
+// Same for an fp32 (BH, N, d) tensor, box {box_cols, box_rows, 1}, no swizzle
+// (used as the destination of TMA reduce-adds).
+bool make_tmap_f32_bhnd(void* out_tmap /* CUtensorMap* */, const void* base, int64_t BH, int64_t N, int64_t d,
+                        int box_cols, int box_rows);
 
 constexpr int kTile = 128;  // attention tile (block_m = block_n)
 

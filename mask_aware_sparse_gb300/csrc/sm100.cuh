@@ -132,6 +132,14 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, 
                "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// 3-D tiled reduce-add (fp32) of a shared-memory box into global memory
+// (bulk group; rows outside the tensor are skipped).
+__device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, const void* src, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 // 3-D tiled load: coordinates are (x = innermost element, y, z).
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y,
                                             int32_t z) {
