@@ -23,9 +23,9 @@
 //              TMEM, writes P^T (bf16) back to TMEM and dS^T (bf16) to shared
 //              memory. Two compute warps per SM sub-partition hide latency.
 //   warps 8-11 dQ drain: thread c owns TMEM lane c = head-dim index c of
-//              dQ^T; each warp transposes its slice through shared memory and
-//              adds it to the fp32 dQ accumulator with 16-byte vector
-//              reductions; also stores dK at the end;
+//              dQ^T; each warp writes its slice row-major to shared memory
+//              and adds it to the fp32 dQ accumulator with TMA tensor
+//              reduce-adds (32 x 32 boxes); also stores dK at the end;
 //   warp 12    TMA producer (K, V once; Q, dO, LSE offsets, D per unit);
 //   warps 13-14 tcgen05 MMA issuers, one per dependency chain.
 // Per unit u (64 query rows) the MMAs are, all with M = 128:
@@ -34,14 +34,14 @@
 //   dV  += P^T dO          (A = P^T from TMEM, written over S by the compute warps)
 //   dK  += dS^T Q          (A = dS^T, K-major, from shared memory)
 //   dQ^T = K^T dS^T        (A = K^T, B = dS^T: both MN-major from shared memory)
-// TMEM: S [0,64) dP [64,128) dQ^T[2] [128,256) dV [256, 256+d) dK [256+d, 256+2d).
+// TMEM: S[2] [0,128) dP [128,192) dQ^T [192,256) dV [256, 256+d) dK [256+d, 256+2d).
 // The compute warps work in two parts per unit: the P part (needs S^T) and
 // the dS part (needs dP^T). Warp 13 issues dV(u) once P^T(u) is ready, then
-// S^T(u+1) (which overwrites P^T(u)); warp 14 issues dP^T(u+1), dK(u) and
-// dQ^T(u) once dS^T(u) is ready. The tensor core's instruction queue holds
-// only ~150 cycles of work, so with one issuer every wait on one chain would
-// idle it. dQ^T is double buffered so the drain of unit u overlaps the MMAs
-// of the next units.
+// S^T(u+2) into the same S buffer (which held P^T(u)), so S^T runs two units
+// ahead; warp 14 issues dP^T(u+1), dK(u) and dQ^T(u) once dS^T(u) is ready.
+// The tensor core's instruction queue holds only ~150 cycles of work, so with
+// one issuer every wait on one chain would idle it. dQ^T has one buffer: the
+// drain releases it right after its TMEM load.
 // The dS^T buffer of unit u (128 KV rows x 64 query columns, bf16, 128-byte
 // swizzle, two buffers) serves both as the K-major A operand of dK and the
 // MN-major B operand of dQ^T.
@@ -78,13 +78,13 @@ struct BwdCfg {
   static constexpr int B_KV = 0;
   static constexpr int B_QFULL = 1;
   static constexpr int B_QEMPTY = B_QFULL + STAGES;
-  static constexpr int B_SFULL = B_QEMPTY + STAGES;
-  static constexpr int B_PREADY = B_SFULL + 1;
-  static constexpr int B_DPFULL = B_PREADY + 1;
+  static constexpr int B_SFULL = B_QEMPTY + STAGES;  // [2]: one per S buffer
+  static constexpr int B_PREADY = B_SFULL + 2;        // [2]
+  static constexpr int B_DPFULL = B_PREADY + 2;
   static constexpr int B_READY = B_DPFULL + 1;
-  static constexpr int B_DQFULL = B_READY + 1;    // [2]
-  static constexpr int B_DQEMPTY = B_DQFULL + 2;  // [2]
-  static constexpr int B_FINAL = B_DQEMPTY + 2;
+  static constexpr int B_DQFULL = B_READY + 1;
+  static constexpr int B_DQEMPTY = B_DQFULL + 1;
+  static constexpr int B_FINAL = B_DQEMPTY + 1;
   static constexpr int B_VSTAGED = B_FINAL + 1;  // dV rows staged for the TMA store
   static constexpr int B_KSTAGED = B_VSTAGED + 1;
   static constexpr int NBAR = B_KSTAGED + 1;
@@ -180,14 +180,14 @@ __global__ void __launch_bounds__(480, 1)
       mbar_init(&bars[C::B_QFULL + s], 1);
       mbar_init(&bars[C::B_QEMPTY + s], 2);  // one commit from each MMA issuer
     }
-    mbar_init(&bars[C::B_SFULL], 1);
-    mbar_init(&bars[C::B_PREADY], 256);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars[C::B_SFULL + x], 1);
+      mbar_init(&bars[C::B_PREADY + x], 256);
+    }
     mbar_init(&bars[C::B_DPFULL], 1);
     mbar_init(&bars[C::B_READY], 256);
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&bars[C::B_DQFULL + x], 1);
-      mbar_init(&bars[C::B_DQEMPTY + x], 128);
-    }
+    mbar_init(&bars[C::B_DQFULL], 1);
+    mbar_init(&bars[C::B_DQEMPTY], 128);
     mbar_init(&bars[C::B_FINAL], 2);
     mbar_init(&bars[C::B_VSTAGED], 128);
     mbar_init(&bars[C::B_KSTAGED], 128);
@@ -213,8 +213,8 @@ __global__ void __launch_bounds__(480, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  // TMEM columns: S^T (P^T written back in place), dP^T, dQ^T x 2, dV, dK
-  constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 256, T_DK = 256 + D;
+  // TMEM columns: S^T x 2 (P^T written back in place), dP^T, dQ^T, dV, dK
+  constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 192, T_DV = 256, T_DK = 256 + D;
 
   if (*abort_flag) {
     // an unread timeout from an earlier launch: skip the work
@@ -279,18 +279,17 @@ __global__ void __launch_bounds__(480, 1)
           mma_ss(tbase + dst, ad0 + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
                  bd0 + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), id_s, k > 0 ? 1u : 0u);
       };
-      // dQ^T(v) = K^T dS^T(v) into TMEM buffer v&1, after the drain of unit v-2
+      // dQ^T(v) = K^T dS^T(v) into TMEM, once the drain has read dQ^T(v-1)
       auto issue_dq = [&](int v) -> bool {
-        if (v >= 2) {
-          if (!mbar_wait(&bars[C::B_DQEMPTY + (v & 1)], (uint32_t)((v >> 1) - 1) & 1u, abort_flag, p.err)) return false;
+        if (v >= 1) {
+          if (!mbar_wait(&bars[C::B_DQEMPTY], (uint32_t)(v - 1) & 1u, abort_flag, p.err)) return false;
           tc_fence_after();
         }
         const uint64_t bd0 = dSm + kDsStep * (uint64_t)(v & 1);
 #pragma unroll
         for (int k = 0; k < 8; ++k)  // 128 KV rows
-          mma_ss(tbase + T_DQ + 64u * (v & 1), dKt + (uint64_t)(k * 128), bd0 + (uint64_t)(k * 128), id_q,
-                 k > 0 ? 1u : 0u);
-        mma_commit(&bars[C::B_DQFULL + (v & 1)]);
+          mma_ss(tbase + T_DQ, dKt + (uint64_t)(k * 128), bd0 + (uint64_t)(k * 128), id_q, k > 0 ? 1u : 0u);
+        mma_commit(&bars[C::B_DQFULL]);
         return true;
       };
       bool ok = mbar_wait(&bars[C::B_KV], 0, abort_flag, p.err);
@@ -300,30 +299,42 @@ __global__ void __launch_bounds__(480, 1)
         tc_fence_after();
       }
       if (warp == 13) {
+        // S^T runs two units ahead in two buffers: S^T(u+2) reuses the buffer
+        // of S^T(u) / P^T(u) once dV(u) has been issued, so the compute warps
+        // find S^T(u+1) ready when they finish unit u.
         if (ok) {
           issue_sk(dKk, dQk, T_S);
           mma_commit(&bars[C::B_SFULL]);
         }
+        if (ok && U > 1) {
+          ok = mbar_wait(&bars[C::B_QFULL + 1], 0, abort_flag, p.err);
+          tc_fence_after();
+          if (ok) {
+            issue_sk(dKk, dQk + kQStep, T_S + 64);
+            mma_commit(&bars[C::B_SFULL + 1]);
+          }
+        }
         for (int u = 0; u < U && ok; ++u) {
-          const int stage = u % S, nstage = (u + 1) % S;
-          const uint64_t qoff = kQStep * (uint64_t)stage, nqoff = kQStep * (uint64_t)nstage;
+          const int stage = u % S, b2 = u & 1;
+          const uint64_t qoff = kQStep * (uint64_t)stage;
+          const uint32_t t_s = T_S + 64u * (uint32_t)b2;
           // dV += P^T dO once P^T(u) is in TMEM (two 16-column blocks, one per half)
-          ok = mbar_wait(&bars[C::B_PREADY], (uint32_t)u & 1u, abort_flag, p.err);
+          ok = mbar_wait(&bars[C::B_PREADY + b2], (uint32_t)(u >> 1) & 1u, abort_flag, p.err);
           tc_fence_after();
           if (!ok) break;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint32_t a_t = tbase + T_S + (uint32_t)((k >> 1) * 32 + (k & 1) * 8);
+            const uint32_t a_t = tbase + t_s + (uint32_t)((k >> 1) * 32 + (k & 1) * 8);
             mma_ts(tbase + T_DV, a_t, dOm + qoff + (uint64_t)(k * 128), id_g, (u > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit(&bars[C::B_QEMPTY + stage]);  // S^T(u) and dV(u) were this issuer's readers
-          // S^T(u+1) may overwrite P^T(u): dV(u) was issued first
-          if (u + 1 < U) {
-            ok = mbar_wait(&bars[C::B_QFULL + nstage], (uint32_t)((u + 1) / S) & 1u, abort_flag, p.err);
+          if (u + 2 < U) {
+            const int s2 = (u + 2) % S;
+            ok = mbar_wait(&bars[C::B_QFULL + s2], (uint32_t)((u + 2) / S) & 1u, abort_flag, p.err);
             tc_fence_after();
             if (!ok) break;
-            issue_sk(dKk, dQk + nqoff, T_S);
-            mma_commit(&bars[C::B_SFULL]);
+            issue_sk(dKk, dQk + kQStep * (uint64_t)s2, t_s);
+            mma_commit(&bars[C::B_SFULL + b2]);
           }
         }
       } else {
@@ -382,7 +393,7 @@ __global__ void __launch_bounds__(480, 1)
     const bool causal = p.causal != 0;
     const uint32_t s_rows = smem_u32(smem + C::ROW_OFF);
     const uint32_t s_ds = smem_u32(smem + C::DS_OFF) + (uint32_t)((j >> 3) * 1024 + (j & 7) * 128);
-    const uint32_t tS = tbase + lane_off + T_S + 32u * half;
+    const uint32_t tS0 = tbase + lane_off + T_S + 32u * half;  // + 64 for S buffer 1
     const uint32_t tDP = tbase + lane_off + T_DP + 32u * half;
     bool ok = true;
     for (int u = 0; u < U && ok; ++u) {
@@ -390,7 +401,8 @@ __global__ void __launch_bounds__(480, 1)
       const int stage = u % S;
       const int r0 = un.qb * 128 + un.half * 64;
       ok = __all_sync(kFull, mbar_wait(&bars[C::B_QFULL + stage], (uint32_t)(u / S) & 1u, abort_flag, p.err));
-      if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_SFULL], (uint32_t)u & 1u, abort_flag, p.err));
+      if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_SFULL + (u & 1)], (uint32_t)(u >> 1) & 1u, abort_flag, p.err));
+      const uint32_t tS = tS0 + 64u * (uint32_t)(u & 1);
       if (!ok) break;
       tc_fence_after();
       // masked rows of this thread's key column within its 32-row window, one bit per row
@@ -425,7 +437,7 @@ __global__ void __launch_bounds__(480, 1)
       tmem_st16(tS, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars[C::B_PREADY]);
+      mbar_arrive(&bars[C::B_PREADY + (u & 1)]);
       // dS part: dS^T = P^T * (dP^T - D), bf16, to shared memory
       ok = __all_sync(kFull, mbar_wait(&bars[C::B_DPFULL], (uint32_t)u & 1u, abort_flag, p.err));
       if (!ok) break;
@@ -491,16 +503,15 @@ __global__ void __launch_bounds__(480, 1)
     bool ok = true;
     for (int u = 0; u < U && ok; ++u) {
       const Unit un = decode_unit(p, u, L, kbeg, g, force_part, s_queue, C::QUEUE_CAP);
-      const int pb = u & 1;
-      ok = __all_sync(kFull, mbar_wait(&bars[C::B_DQFULL + pb], (uint32_t)(u >> 1) & 1u, abort_flag, p.err));
+      ok = __all_sync(kFull, mbar_wait(&bars[C::B_DQFULL], (uint32_t)u & 1u, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
       uint32_t v0[32], v1[32];
-      tmem_ld32(tbase + lane_off + T_DQ + 64u * pb, v0);
-      tmem_ld32(tbase + lane_off + T_DQ + 64u * pb + 32, v1);
+      tmem_ld32(tbase + lane_off + T_DQ, v0);
+      tmem_ld32(tbase + lane_off + T_DQ + 32, v1);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&bars[C::B_DQEMPTY + pb]);
+      mbar_arrive(&bars[C::B_DQEMPTY]);
       // The 32 x 64 slice goes through this warp's 4 KB of shared memory, 32
       // rows at a time, in row-major order, and a TMA reduce-add sends each
       // 32 x 32 box to the fp32 accumulator (rows beyond N are skipped by it).
