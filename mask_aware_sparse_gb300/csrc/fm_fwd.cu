@@ -369,9 +369,16 @@ __global__ void __launch_bounds__(320, 1)
           for (int c = 0; c < 128; ++c)
             sr[c] = ((rb[c >> 5] >> (c & 31)) & 1u) ? __float_as_uint(-INFINITY) : sr[c];
         }
-        float mx = -INFINITY;
+        // row max with three-input max, four independent chains
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+        for (int c = 0; c < 128; c += 8) {
+          mx0 = max3f(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+          mx1 = max3f(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+          mx2 = max3f(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+          mx3 = max3f(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+        }
+        const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3));
         const float m_blk = mx * sl2;
         const float m_new = fmaxf(m_run, m_blk);
         const bool resc = m_new > m_run + 8.0f;
@@ -381,16 +388,23 @@ __global__ void __launch_bounds__(320, 1)
           m_run = m_new;
         }
         const float msafe = (m_run == -INFINITY) ? 0.f : m_run;
-        float rs = 0.f;
+        // exponent arguments and the row sum on column pairs (f32x2)
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-msafe, -msafe);
+        uint64_t rs0 = f2_pack(0.f, 0.f), rs1 = rs0;
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float a = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -msafe));
-          const float bb = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -msafe));
-          rs += a + bb;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sl2x2, nm2), x0, x1);
+          const float a = ex2_approx(x0), bb = ex2_approx(x1);
+          if (c & 1) rs1 = f2_add(rs1, f2_pack(a, bb));
+          else rs0 = f2_add(rs0, f2_pack(a, bb));
           pk[c] = pack_bf16x2(a, bb);
         }
-        l_run = l_run * factor + rs;
+        float r0a, r0b, r1a, r1b;
+        f2_unpack(rs0, r0a, r0b);
+        f2_unpack(rs1, r1a, r1b);
+        l_run = l_run * factor + ((r0a + r0b) + (r1a + r1b));
         {
           const uint32_t(&p0)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]);
           const uint32_t(&p1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]);
