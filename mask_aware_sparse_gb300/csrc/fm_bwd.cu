@@ -420,16 +420,20 @@ __global__ void __launch_bounds__(480, 1)
       tmem_ld_wait();
       float pf[32];
       uint32_t pk[16];
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
       for (int r4 = 0; r4 < 8; ++r4) {
         const float4 nl4 = lds_f32x4(rows_a + 16 * r4);
-        const float nlv[4] = {nl4.x, nl4.y, nl4.z, nl4.w};
+        const uint64_t nlp[2] = {f2_pack(nl4.x, nl4.y), f2_pack(nl4.z, nl4.w)};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int rr = 4 * r4 + e;
-          float x = fmaf(__uint_as_float(sv[rr]), sl2, nlv[e]);
-          x = ((mbits >> rr) & 1u) ? -INFINITY : x;
-          pf[rr] = ex2_approx(x);
+        for (int e2 = 0; e2 < 2; ++e2) {  // exponent arguments of a column pair in one f32x2 FMA
+          const int rr = 4 * r4 + 2 * e2;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[rr]), __uint_as_float(sv[rr + 1])), sl2x2, nlp[e2]), x0, x1);
+          x0 = ((mbits >> rr) & 1u) ? -INFINITY : x0;
+          x1 = ((mbits >> (rr + 1)) & 1u) ? -INFINITY : x1;
+          pf[rr] = ex2_approx(x0);
+          pf[rr + 1] = ex2_approx(x1);
         }
         pk[2 * r4] = pack_bf16x2(pf[4 * r4], pf[4 * r4 + 1]);
         pk[2 * r4 + 1] = pack_bf16x2(pf[4 * r4 + 2], pf[4 * r4 + 3]);
@@ -449,12 +453,15 @@ __global__ void __launch_bounds__(480, 1)
 #pragma unroll
       for (int r4 = 0; r4 < 8; ++r4) {
         const float4 d4 = lds_f32x4(rows_a + 256 + 16 * r4);
-        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-        float dd[4];
+        const uint64_t dp[2] = {f2_pack(d4.x, d4.y), f2_pack(d4.z, d4.w)};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) dd[e] = pf[4 * r4 + e] * (__uint_as_float(pv[4 * r4 + e]) - dv4[e]);
-        dk[2 * r4] = pack_bf16x2(dd[0], dd[1]);
-        dk[2 * r4 + 1] = pack_bf16x2(dd[2], dd[3]);
+        for (int e2 = 0; e2 < 2; ++e2) {  // dS = P * (dP - D) on a column pair in two f32x2 ops
+          const int rr = 4 * r4 + 2 * e2;
+          const uint64_t t = f2_sub(f2_pack(__uint_as_float(pv[rr]), __uint_as_float(pv[rr + 1])), dp[e2]);
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(pf[rr], pf[rr + 1]), t), d0, d1);
+          dk[2 * r4 + e2] = pack_bf16x2(d0, d1);
+        }
       }
       // dS^T row j, 16-byte chunks 4*half .. 4*half+3 (8 query columns each), 128-byte swizzle
       const uint32_t ds_row = s_ds + 16384u * (u & 1);
