@@ -499,8 +499,8 @@ def run_ours(args, cfg):
 # ncu DRAM traffic (read + write bytes per launch) of the main kernels, valid
 # only while the kernel source is the one the counters were taken from.
 NCU_TRAFFIC = {
-    "bwd": {"file": "fm_bwd.cu", "sha256": "d1a1290b91889652b4fe5aa8cad86283896ae56651f670729d396ad6b4e1ffa4", "bytes": 5620876000},
-    "fwd": {"file": "fm_fwd.cu", "sha256": "f8bf50c7d8f8fb8c33a5c71b6c2c5eb1d6814360c389d39095cd4f501400f0e7", "bytes": 607274752},
+    "bwd": {"file": "fm_bwd.cu", "sha256": "07effe293a71a12aa47472f57d39c5a28677782796b49ef58c1c62c8319866fe", "bytes": 5291612000},
+    "fwd": {"file": "fm_fwd.cu", "sha256": "4c9c599d41d3e1cbda1fbd0df0ea3136e2a5b49486aa154fbc0b6ae52bf59e17", "bytes": 639160832},
 }
 
 
