@@ -101,7 +101,7 @@ struct BwdParams {
   const int32_t* ute;
   const int32_t* k_off;
   const int32_t* k_queue;
-  const int32_t* order;
+  const int32_t* order;  // launch order of (b, kb), or null: natural order
   const float* nl;    // (B*H_q, Npad): -LSE*log2(e), -inf for empty / padded rows
   const float* dsum;  // (B*H_q, Npad): D = rowsum(dO * O)
   float* dq_acc;      // (B*H_q, N, d) fp32
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(480, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int oi = blockIdx.x / p.H_kv, g = blockIdx.x - oi * p.H_kv;
-  const int bk = p.order[oi];
+  const int bk = p.order ? p.order[oi] : oi;
   const int nK = p.nK;
   const int b = bk / nK, kb = bk - b * nK;
   const int kbeg = p.k_off[bk];
@@ -745,8 +745,14 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   bwd_pre_kernel<D><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
                                                                static_cast<const __nv_bfloat16*>(dout), lse,
                                                                (int)BH, P.N, prm0.Npad, w.nl, w.dsum, w.dq_acc);
-  // 2. LPT order of KV blocks
-  lpt_order_kernel_bwd<<<1, 1024, 0, s>>>(prm0.k_off, P.B * nK, w.order);
+  // 2. launch order of the KV blocks. With at least four (batch, kv head)
+  // groups running side by side, natural KV order is the faster one (CTAs
+  // that run together share Q / dO tiles in L2 and the masks here put the
+  // long queues first); with fewer groups, many CTAs of one group would
+  // reduce into the same dQ rows at once, and the longest-queue-first order
+  // spreads them (measured: 11-16% faster, resp. 19% faster).
+  const bool natural = (long long)P.B * P.H_kv >= 4;
+  if (!natural) lpt_order_kernel_bwd<<<1, 1024, 0, s>>>(prm0.k_off, P.B * nK, w.order);
   // 3. main kernel
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if (!make_tmap_bhnd(&tq, q, BH, P.N, D, 64) || !make_tmap_bhnd(&tdo, dout, BH, P.N, D, 64) ||
@@ -767,7 +773,9 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   const long long grid = (long long)P.B * nK * P.H_kv;
   {
     KernelTimer timer(s, kTimedBwd);
-    bwd_kernel<D><<<(unsigned)grid, 480, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm0);
+    BwdParams prm = prm0;
+    if (natural) prm.order = nullptr;
+    bwd_kernel<D><<<(unsigned)grid, 480, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
   }
   // 4. dQ = bf16(scale * dQacc)
   const long long n8 = BH * P.N * D / 8;
@@ -775,7 +783,7 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   if (blocks > 152 * 32) blocks = 152 * 32;
   dq_convert_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(w.dq_acc, w.nl, static_cast<__nv_bfloat16*>(dq), n8, P.N,
                                                         prm0.Npad, P.scale);
-  count_launches(4);  // row terms, LPT order, main kernel, dQ convert
+  count_launches(natural ? 3 : 4);  // row terms, [LPT order], main kernel, dQ convert
   return cudaGetLastError();
 }
 
