@@ -51,6 +51,7 @@
 #include "fm_internal.h"
 #include "mask_bits.cuh"
 #include "sm100.cuh"
+#include "lpt_order.cuh"
 
 namespace fm {
 namespace {
@@ -671,40 +672,6 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, const float* __
   }
 }
 
-// Longest-queue-first order of (b, kb) by KV queue length (shared with the
-// forward's design: one CTA bitonic sort; identity order beyond kMaxSort).
-constexpr int kMaxSort = 4096;
-__global__ void __launch_bounds__(1024) lpt_order_kernel_bwd(const int32_t* __restrict__ off, int count,
-                                                             int32_t* __restrict__ order) {
-  __shared__ unsigned long long key[kMaxSort];
-  if (count > kMaxSort) {
-    for (int i = threadIdx.x; i < count; i += blockDim.x) order[i] = i;
-    return;
-  }
-  int n2 = 1;
-  while (n2 < count) n2 <<= 1;
-  for (int i = threadIdx.x; i < n2; i += blockDim.x)
-    key[i] = (i < count) ? (((unsigned long long)(uint32_t)(off[i + 1] - off[i]) << 32) | (0xFFFFFFFFu - (uint32_t)i))
-                         : 0ull;
-  __syncthreads();
-  for (int k = 2; k <= n2; k <<= 1) {
-    for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
-        const int ixj = i ^ jj;
-        if (ixj > i) {
-          const bool desc = (i & k) == 0;
-          const unsigned long long a = key[i], c = key[ixj];
-          if ((a < c) == desc) {
-            key[i] = c;
-            key[ixj] = a;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-  for (int i = threadIdx.x; i < count; i += blockDim.x) order[i] = (int32_t)(0xFFFFFFFFu - (uint32_t)key[i]);
-}
 
 inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -752,7 +719,7 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   // reduce into the same dQ rows at once, and the longest-queue-first order
   // spreads them (measured: 11-16% faster, resp. 19% faster).
   const bool natural = (long long)P.B * P.H_kv >= 4;
-  if (!natural) lpt_order_kernel_bwd<<<1, 1024, 0, s>>>(prm0.k_off, P.B * nK, w.order);
+  if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(prm0.k_off, P.B * nK, w.order);
   // 3. main kernel
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if (!make_tmap_bhnd(&tq, q, BH, P.N, D, 64) || !make_tmap_bhnd(&tdo, dout, BH, P.N, D, 64) ||

@@ -14,8 +14,8 @@
 //      (the same kernel counts each column's non-skipped tiles with integer
 //      atomics; block_minmax zeroes those counters first)
 //   3. scan           exclusive prefix sums -> q_off, k_off (one CTA).
-//   4. emit_rows      one warp per (b, qb): descending-kb compaction by ballot.
-//   5. emit_cols      one warp per (b, kb): ascending-qb compaction by ballot.
+//   4. emit_queues    one warp per queue: (b, qb) rows in descending kb and
+//                     (b, kb) columns in ascending qb, compaction by ballot.
 #include <climits>
 #include "fm_internal.h"
 #include "sm100.cuh"
@@ -146,38 +146,57 @@ __global__ void scan_kernel(const int32_t* row_cnt, int n_rows, int32_t* q_off, 
     block_exclusive_scan(col_cnt, n_cols, k_off);
 }
 
-__global__ void emit_rows_kernel(const uint8_t* __restrict__ cls, int B, int nQ, int nK, const int32_t* __restrict__ q_off,
-                                 int32_t* __restrict__ q_queue) {
+// Queue emission, one warp per queue: warps [0, B*nQ) emit the Q-side queues
+// (descending kb), warps [B*nQ, B*nQ + B*nK) the KV-side queues (ascending qb).
+// Class bytes are loaded eight 32-entry chunks at a time before the ballots,
+// so the loads are not serialised behind the running position.
+__global__ void emit_queues_kernel(const uint8_t* __restrict__ cls, int B, int nQ, int nK,
+                                   const int32_t* __restrict__ q_off, int32_t* __restrict__ q_queue,
+                                   const int32_t* __restrict__ k_off, int32_t* __restrict__ k_queue) {
   const int wpb = blockDim.x >> 5;
-  const long long r = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
-  if (r >= (long long)B * nQ) return;
+  const long long w = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
+  const long long nrow = (long long)B * nQ;
+  if (w >= nrow + (long long)B * nK) return;
   const int lane = threadIdx.x & 31;
-  const uint8_t* crow = cls + (size_t)r * nK;
-  int pos = q_off[r];
-  for (int top = nK - 1; top >= 0; top -= 32) {
-    const int kb = top - lane;  // descending within the chunk
-    const uint8_t c = (kb >= 0) ? crow[kb] : 0;
-    const unsigned bal = __ballot_sync(0xffffffffu, c != 0);
-    if (c != 0) q_queue[pos + __popc(bal & ((1u << lane) - 1u))] = (kb << 1) | (c == 1 ? 1 : 0);
-    pos += __popc(bal);
-  }
-}
-
-__global__ void emit_cols_kernel(const uint8_t* __restrict__ cls, int B, int nQ, int nK, const int32_t* __restrict__ k_off,
-                                 int32_t* __restrict__ k_queue) {
-  const int wpb = blockDim.x >> 5;
-  const long long r = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
-  if (r >= (long long)B * nK) return;
-  const int lane = threadIdx.x & 31;
-  const int b = (int)(r / nK), kb = (int)(r % nK);
-  const uint8_t* ccol = cls + (size_t)b * nQ * nK + kb;
-  int pos = k_off[r];
-  for (int lo = 0; lo < nQ; lo += 32) {
-    const int qb = lo + lane;  // ascending
-    const uint8_t c = (qb < nQ) ? ccol[(size_t)qb * nK] : 0;
-    const unsigned bal = __ballot_sync(0xffffffffu, c != 0);
-    if (c != 0) k_queue[pos + __popc(bal & ((1u << lane) - 1u))] = (qb << 1) | (c == 1 ? 1 : 0);
-    pos += __popc(bal);
+  const unsigned below = (1u << lane) - 1u;
+  if (w < nrow) {
+    const uint8_t* crow = cls + (size_t)w * nK;
+    int pos = q_off[w];
+    for (int top = nK - 1; top >= 0; top -= 256) {
+      uint8_t c[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int kb = top - 32 * i - lane;  // descending
+        c[i] = (kb >= 0) ? crow[kb] : 0;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int kb = top - 32 * i - lane;
+        const unsigned bal = __ballot_sync(0xffffffffu, c[i] != 0);
+        if (c[i] != 0) q_queue[pos + __popc(bal & below)] = (kb << 1) | (c[i] == 1 ? 1 : 0);
+        pos += __popc(bal);
+      }
+    }
+  } else {
+    const long long r = w - nrow;
+    const int b = (int)(r / nK), kb = (int)(r % nK);
+    const uint8_t* ccol = cls + (size_t)b * nQ * nK + kb;
+    int pos = k_off[r];
+    for (int lo = 0; lo < nQ; lo += 256) {
+      uint8_t c[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int qb = lo + 32 * i + lane;  // ascending
+        c[i] = (qb < nQ) ? ccol[(size_t)qb * nK] : 0;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int qb = lo + 32 * i + lane;
+        const unsigned bal = __ballot_sync(0xffffffffu, c[i] != 0);
+        if (c[i] != 0) k_queue[pos + __popc(bal & below)] = (qb << 1) | (c[i] == 1 ? 1 : 0);
+        pos += __popc(bal);
+      }
+    }
   }
 }
 
@@ -205,9 +224,9 @@ cudaError_t launch_classify(const fm_problem& p, int bm, int bn, int nQ, int nK,
   block_minmax_kernel<<<(unsigned)((nkb + 7) / 8), 256, 0, s>>>(lts, lte, uts, ute, B, N, bn, nK, mm, col_cnt, err);
   classify_rows_kernel<<<dim3(nQ, B), 256, 0, s>>>(mm, N, bm, bn, nQ, nK, p.causal, tile_class, row_cnt, col_cnt);
   scan_kernel<<<2, 1024, 0, s>>>(row_cnt, (int)nqb, q_off, col_cnt, (int)nkb, k_off);
-  emit_rows_kernel<<<(unsigned)((nqb + 7) / 8), 256, 0, s>>>(tile_class, B, nQ, nK, q_off, q_queue);
-  emit_cols_kernel<<<(unsigned)((nkb + 7) / 8), 256, 0, s>>>(tile_class, B, nQ, nK, k_off, k_queue);
-  count_launches(5);
+  emit_queues_kernel<<<(unsigned)((nqb + nkb + 7) / 8), 256, 0, s>>>(tile_class, B, nQ, nK, q_off, q_queue, k_off,
+                                                                     k_queue);
+  count_launches(4);
   return cudaGetLastError();
 }
 

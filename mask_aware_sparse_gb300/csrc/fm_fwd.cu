@@ -36,6 +36,7 @@
 #include "fm_internal.h"
 #include "mask_bits.cuh"
 #include "sm100.cuh"
+#include "lpt_order.cuh"
 
 namespace fm {
 namespace {
@@ -480,41 +481,6 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-// Longest-queue-first order of the B*nQ query blocks (one CTA, bitonic sort of
-// (queue length, -index) keys, descending). Larger problems keep index order.
-constexpr int kMaxSort = 4096;
-
-__global__ void __launch_bounds__(1024) lpt_order_kernel(const int32_t* __restrict__ off, int count,
-                                                         int32_t* __restrict__ order) {
-  __shared__ unsigned long long key[kMaxSort];
-  if (count > kMaxSort) {
-    for (int i = threadIdx.x; i < count; i += blockDim.x) order[i] = i;
-    return;
-  }
-  int n2 = 1;
-  while (n2 < count) n2 <<= 1;
-  for (int i = threadIdx.x; i < n2; i += blockDim.x)
-    key[i] = (i < count) ? (((unsigned long long)(uint32_t)(off[i + 1] - off[i]) << 32) | (0xFFFFFFFFu - (uint32_t)i))
-                         : 0ull;
-  __syncthreads();
-  for (int k = 2; k <= n2; k <<= 1) {
-    for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
-        const int ixj = i ^ jj;
-        if (ixj > i) {
-          const bool desc = (i & k) == 0;
-          const unsigned long long a = key[i], c = key[ixj];
-          if ((a < c) == desc) {
-            key[i] = c;
-            key[ixj] = a;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-  for (int i = threadIdx.x; i < count; i += blockDim.x) order[i] = (int32_t)(0xFFFFFFFFu - (uint32_t)key[i]);
-}
 
 template <int D>
 cudaError_t launch_fwd_d(const fm_problem& P, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
