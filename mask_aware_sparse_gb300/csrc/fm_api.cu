@@ -69,6 +69,20 @@ bool make_tmap_f32_bhnd(void* out, const void* base, int64_t BH, int64_t N, int6
   return r == CUDA_SUCCESS;
 }
 
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 // ---------------------------------------------------------------- measurement
 namespace {
 std::atomic<long long> g_launches{0};

@@ -712,13 +712,13 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   bwd_pre_kernel<D><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
                                                                static_cast<const __nv_bfloat16*>(dout), lse,
                                                                (int)BH, P.N, prm0.Npad, w.nl, w.dsum, w.dq_acc);
-  // 2. launch order of the KV blocks. With at least four (batch, kv head)
-  // groups running side by side, natural KV order is the faster one (CTAs
-  // that run together share Q / dO tiles in L2 and the masks here put the
-  // long queues first); with fewer groups, many CTAs of one group would
-  // reduce into the same dQ rows at once, and the longest-queue-first order
-  // spreads them (measured: 11-16% faster, resp. 19% faster).
-  const bool natural = (long long)P.B * P.H_kv >= 4;
+  // 2. launch order of the KV blocks: longest queue first for passes of a
+  // few waves; natural KV order for long passes, where CTAs that run
+  // together share Q / dO tiles in L2 (measured: 11-16% faster on the 32K
+  // and 64K workloads; the one-kv-head 128K workload, 6.7 waves, stays LPT,
+  // where natural order was 19% slower: its CTAs then reduce into the same
+  // dQ rows at once).
+  const bool natural = use_natural_order((long long)P.B * nK * P.H_kv);
   if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(prm0.k_off, P.B * nK, w.order);
   // 3. main kernel
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;

@@ -78,7 +78,7 @@ struct FwdParams {
   const int32_t* ute;
   const int32_t* q_off;
   const int32_t* q_queue;
-  const int32_t* order;
+  const int32_t* order;  // launch order of (b, qb), or null: natural order
   __nv_bfloat16* o;
   float* lse;
   int B, H_q, H_kv, N, nQ, nK, G, PG, causal;
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(320, 1)
   const int units = p.H_kv * p.PG;
   const int oi = blockIdx.x / units, gp = blockIdx.x - oi * units;
   const int g = gp / p.PG, pp = gp - g * p.PG;
-  const int bq = p.order[oi];
+  const int bq = p.order ? p.order[oi] : oi;
   const int b = bq / p.nQ, qb = bq - b * p.nQ;
   const int h0 = g * p.G + 2 * pp;
   const int T = (2 * pp + 1 < p.G) ? 2 : 1;
@@ -496,7 +496,7 @@ cudaError_t launch_fwd_d(const fm_problem& P, const CUtensorMap& tq, const CUten
     KernelTimer timer(s, kTimedFwd);
     fwd_kernel<D><<<grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, to, prm);
   }
-  count_launches(2);  // LPT order + main kernel
+  count_launches(prm.order ? 2 : 1);  // [LPT order] + main kernel
   return cudaGetLastError();
 }
 
@@ -537,8 +537,11 @@ cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const 
   const int PG = (G + 1) / 2;
   const long long grid = (long long)P.B * nQ * P.H_kv * PG;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  int32_t* order = static_cast<int32_t*>(ws);
-  lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, P.B * nQ, order);
+  // launch order: longest queue first, or natural order for long passes
+  // (CTAs that run together then share K / V tiles in L2)
+  const bool natural = use_natural_order(grid);
+  int32_t* order = natural ? nullptr : static_cast<int32_t*>(ws);
+  if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, P.B * nQ, order);
   CUtensorMap tq, tk, tv, to;
   if (!make_tmap_bhnd(&tq, q, (int64_t)P.B * P.H_q, P.N, P.d) || !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, P.N, P.d) ||
       !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, P.N, P.d) || !make_tmap_bhnd(&to, o, (int64_t)P.B * P.H_q, P.N, P.d))

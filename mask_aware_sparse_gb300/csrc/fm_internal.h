@@ -43,6 +43,14 @@ cudaError_t launch_bwd(const fm_problem& p, const void* q, const void* k, const 
 
 // Tensor maps (fm_api.cu): 3-D bf16 map over a contiguous (BH, N, d) tensor,
 // box {64, box_rows, 1}, 128-byte swizzle; rows >= N read as zero.
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Natural launch order beats longest-queue-first once a pass spans many
+// waves of CTAs: CTAs that run together then share K / V (forward) or Q / dO
+// (backward) tiles in L2, and the tail is a small part of the pass.
+inline bool use_natural_order(long long ctas) { return ctas >= 8LL * sm_count(); }
+
 bool make_tmap_bhnd(void* out_tmap /* CUtensorMap* */, const void* base, int64_t BH, int64_t N, int64_t d,
                     int box_rows = 128);
 // Same for an fp32 (BH, N, d) tensor, box {box_cols, box_rows, 1}, no swizzle
