@@ -499,8 +499,8 @@ def run_ours(args, cfg):
 # ncu DRAM traffic (read + write bytes per launch) of the main kernels, valid
 # only while the kernel source is the one the counters were taken from.
 NCU_TRAFFIC = {
-    "bwd": {"file": "fm_bwd.cu", "sha256": "07effe293a71a12aa47472f57d39c5a28677782796b49ef58c1c62c8319866fe", "bytes": 5291612000},
-    "fwd": {"file": "fm_fwd.cu", "sha256": "4c9c599d41d3e1cbda1fbd0df0ea3136e2a5b49486aa154fbc0b6ae52bf59e17", "bytes": 639160832},
+    "bwd": {"file": "fm_bwd.cu", "sha256": "ddac91c410bf1b64f4ff2524b0f2b5e543b5721417247545c4d8b06ebfcf7f04", "bytes": 1269846784},
+    "fwd": {"file": "fm_fwd.cu", "sha256": "5b04914804106c11b947f1a749c089b1d88b76534baee7a81c8d1fd2aef8b704", "bytes": 481385216},
 }
 
 
