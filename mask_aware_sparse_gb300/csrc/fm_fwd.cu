@@ -27,8 +27,10 @@
 //   * Rescaling of O is lazy: the running max used for exponentials only moves
 //     when the block max exceeds it by more than 8 (log2 units), so P <= 256;
 //     O and l are always scaled consistently, so O / l is unchanged.
-//   * Work units are launched longest-queue first (an LPT order computed on
-//     the device from the queue offsets).
+//   * Launch order: longest queue first (an LPT order computed on the device
+//     from the queue offsets) for passes of a few waves, natural order for
+//     long passes, where CTAs of neighbouring query blocks share K / V tiles
+//     in L2.
 #include <climits>
 #include <cmath>
 #include <mutex>
