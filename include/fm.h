@@ -124,7 +124,8 @@ fm_status fm_classify_tiles(const fm_problem* p, const fm_tiling* t, const int32
  * tiling and the same problem and mask. d must be 64 or 128. Mask values
  * outside [0, N] are clamped; the forward does not flag them again
  * (fm_classify_tiles on the same vectors does).
- * Workspace: fm_attn_fwd_workspace_bytes (may be 0 bytes -> ws may be NULL).
+ * Workspace: fm_attn_fwd_workspace_bytes (the unit-order table and a work
+ * counter; every call rewrites what it uses, so it needs no clearing).
  * ------------------------------------------------------------------------- */
 size_t fm_attn_fwd_workspace_bytes(const fm_problem* p);
 fm_status fm_attn_fwd(const fm_problem* p, const void* q, const void* k, const void* v, const int32_t* lts,
@@ -161,10 +162,10 @@ fm_status fm_attn_bwd(const fm_problem* p, const void* q, const void* k, const v
  * at start-up and must not call cudaMalloc afterwards. Nothing here calls
  * cudaMalloc, cudaFree or any allocating library routine.
  *
- * The forward's only scratch (its launch-order table, one int32 per Q block)
- * lives instead in a fixed array inside the library, FM_NOALLOC_MAX_QBLOCKS
- * entries (256 KiB) per GPU, held by every GPU that loads the library until the
- * process exits. Problems with B * ceil(N / 128) > FM_NOALLOC_MAX_QBLOCKS are
+ * The forward's only scratch (its unit-order table, one int32 per Q block, and
+ * a work counter) lives instead in a fixed array inside the library,
+ * FM_NOALLOC_MAX_QBLOCKS + 64 entries (256 KiB + 256 B) per GPU, held by every
+ * GPU that loads the library until the process exits. Problems with B * ceil(N / 128) > FM_NOALLOC_MAX_QBLOCKS are
  * rejected with FM_ERR_WORKSPACE before anything is launched.
  * The first call on each device looks up the array's device address (with that
  * device current); make that first call before any stream capture.

@@ -69,6 +69,19 @@ bool make_tmap_f32_bhnd(void* out, const void* base, int64_t BH, int64_t N, int6
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_bhnd_w32(void* out, const void* base, int64_t BH, int64_t N, int64_t d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)(d * 2), (cuuint64_t)(N * d * 2)};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(static_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static std::mutex mu;
   static int cached[64] = {0};

@@ -31,6 +31,7 @@
 //     from the queue offsets) for passes of a few waves, natural order for
 //     long passes, where CTAs of neighbouring query blocks share K / V tiles
 //     in L2.
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <mutex>
@@ -53,11 +54,22 @@ struct FwdCfg {
   static constexpr int V_OFF = K_OFF + STAGES * TILE;
   static constexpr int M_OFF = V_OFF + STAGES * TILE;
   static constexpr int M_BYTES = 4 * 128 * 4;  // LTS[128], LTE[128], UTS[128], UTE[128]
-  static constexpr int QUEUE_CAP = 1024;    // queue entries staged in shared memory
-  static constexpr int QUEUE_OFF = M_OFF + STAGES * M_BYTES;
-  static constexpr int BAR_OFF = QUEUE_OFF + QUEUE_CAP * 4;
+  // O staging: one 2 KB slot per softmax warp (32 rows x 32 columns bf16,
+  // 64-byte swizzle), the source of that warp's TMA stores
+  static constexpr int O_OFF = M_OFF + STAGES * M_BYTES;
+  static constexpr int O_SLOT = 32 * 32 * 2;
+  // unit ring: the producer decodes each unit once into one of two slots (a
+  // header and the first QUEUE_CAP queue entries); the other roles read it there
+  static constexpr int QUEUE_CAP = 512;
+  static constexpr int U_HDR = 16;  // int32 header words
+  static constexpr int U_BYTES = (U_HDR + QUEUE_CAP) * 4;
+  static constexpr int U_OFF = O_OFF + 8 * O_SLOT;
+  static constexpr int BAR_OFF = U_OFF + 2 * U_BYTES;
   static constexpr int B_QFULL = 0;
-  static constexpr int B_KFULL = 1;
+  static constexpr int B_QFREE = 1;
+  static constexpr int B_UFULL = 2;   // [2]
+  static constexpr int B_UEMPTY = 4;  // [2]
+  static constexpr int B_KFULL = 6;
   static constexpr int B_KEMPTY = B_KFULL + STAGES;
   static constexpr int B_VFULL = B_KEMPTY + STAGES;
   static constexpr int B_VEMPTY = B_VFULL + STAGES;
@@ -66,12 +78,14 @@ struct FwdCfg {
   static constexpr int B_SFULL = B_MEMPTY + STAGES;  // [2]
   static constexpr int B_PREADY = B_SFULL + 2;       // [2]
   static constexpr int B_ODONE = B_PREADY + 2;       // [2]
-  static constexpr int B_OSTAGED = B_ODONE + 2;      // [2]
-  static constexpr int NBAR = B_OSTAGED + 2;
+  static constexpr int NBAR = B_ODONE + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
 };
+
+// unit header words in the unit ring
+enum { UH_N = 0, UH_T = 1, UH_QB = 2, UH_B = 3, UH_H0 = 4, UH_G = 5, UH_QBEG = 6, UH_END = 7 };
 
 struct FwdParams {
   const int32_t* lts;
@@ -80,16 +94,47 @@ struct FwdParams {
   const int32_t* ute;
   const int32_t* q_off;
   const int32_t* q_queue;
-  const int32_t* order;  // launch order of (b, qb), or null: natural order
+  const int32_t* order;  // order of (b, qb) in the unit sequence, or null: natural order
+  int* next_unit;        // work counter, zero at launch: units handed out past the first gridDim.x
   __nv_bfloat16* o;
   float* lse;
   int B, H_q, H_kv, N, nQ, nK, G, PG, causal;
+  int units;  // B * nQ * H_kv * PG work units
   float scale_log2;
   int* err;
 };
 
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr unsigned kFull = 0xffffffffu;
+
+// One work unit: (batch b, Q block qb, a pair of query heads h0, h0 + 1 of KV
+// head g; T = 1 when the group has an odd head left over) and its queue.
+struct Unit {
+  int b, qb, g, h0, T, qbeg, n;
+};
+
+__device__ __forceinline__ Unit decode_unit(const FwdParams& p, int k) {
+  Unit u;
+  const int per = p.H_kv * p.PG;
+  const int oi = k / per, gp = k - oi * per;
+  u.g = gp / p.PG;
+  const int pp = gp - u.g * p.PG;
+  const int bq = p.order ? p.order[oi] : oi;
+  u.b = bq / p.nQ;
+  u.qb = bq - u.b * p.nQ;
+  u.h0 = u.g * p.G + 2 * pp;
+  u.T = (2 * pp + 1 < p.G) ? 2 : 1;
+  u.qbeg = p.q_off[bq];
+  u.n = p.q_off[bq + 1] - u.qbeg;
+  return u;
+}
+
+// A queue block is partial when the classification tagged it so, or when it
+// is the last key block and N is not a multiple of 128 (its tail columns are
+// masked for every row).
+__device__ __forceinline__ bool block_partial(const FwdParams& p, int e) {
+  return (e & 1) || ((e >> 1) == p.nK - 1 && (p.N & 127));
+}
 
 template <int D>
 __global__ void __launch_bounds__(320, 1)
@@ -104,62 +149,34 @@ __global__ void __launch_bounds__(320, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int units = p.H_kv * p.PG;
-  const int oi = blockIdx.x / units, gp = blockIdx.x - oi * units;
-  const int g = gp / p.PG, pp = gp - g * p.PG;
-  const int bq = p.order ? p.order[oi] : oi;
-  const int b = bq / p.nQ, qb = bq - b * p.nQ;
-  const int h0 = g * p.G + 2 * pp;
-  const int T = (2 * pp + 1 < p.G) ? 2 : 1;
-  const int qbeg = p.q_off[bq];
-  const int n = p.q_off[bq + 1] - qbeg;
-  const int q0 = qb * 128;
-
-  if (n <= 0) {
-    // No visible key for any row of this unit: O = 0, LSE = -inf.
-    if (n < 0 && threadIdx.x == 0) record_error(p.err, FM_DEV_ERR_QUEUE);
-    if (warp < 8) {
-      const int t = warp >> 2, i = q0 + ((warp & 3) << 5) + lane;
-      if (t < T && i < p.N) {
-        const size_t bh = (size_t)b * p.H_q + h0 + t;
-        uint4* orow = reinterpret_cast<uint4*>(p.o + (bh * p.N + i) * D);
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
-        p.lse[bh * p.N + i] = -INFINITY;
-      }
-    }
-    return;
-  }
+  // heads per unit for the whole grid: 2 when the GQA group has two or more
+  // query heads; an odd group also has single-head units
+  const int tmax = p.G >= 2 ? 2 : 1;
 
   if (threadIdx.x == 0) {
     // an unread timeout from an earlier launch: skip the work, keep the CTA cheap
     *abort_flag = timeout_pending(p.err) ? 1 : 0;
     mbar_init(&bars[C::B_QFULL], 1);
+    mbar_init(&bars[C::B_QFREE], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[C::B_UFULL + s], 1);
+      mbar_init(&bars[C::B_UEMPTY + s], 1 + 4 * tmax);  // the MMA lane and the softmax warps
+    }
     for (int s = 0; s < S; ++s) {
       mbar_init(&bars[C::B_KFULL + s], 1);
       mbar_init(&bars[C::B_KEMPTY + s], 1);
       mbar_init(&bars[C::B_VFULL + s], 1);
       mbar_init(&bars[C::B_VEMPTY + s], 1);
       mbar_init(&bars[C::B_MFULL + s], 1);
-      mbar_init(&bars[C::B_MEMPTY + s], 4 * T);
+      mbar_init(&bars[C::B_MEMPTY + s], 4 * tmax);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars[C::B_SFULL + t], 1);
       mbar_init(&bars[C::B_PREADY + t], 128);
       mbar_init(&bars[C::B_ODONE + t], 1);
-      mbar_init(&bars[C::B_OSTAGED + t], 128);
     }
     fence_mbar_init();
   }
-  // the unit's queue goes to shared memory once; every role reads it from there
-  const uint32_t s_queue = smem_u32(smem + C::QUEUE_OFF);
-  {
-    int* sq = reinterpret_cast<int*>(smem + C::QUEUE_OFF);
-    for (int t = threadIdx.x; t < n && t < C::QUEUE_CAP; t += blockDim.x) sq[t] = p.q_queue[qbeg + t];
-  }
-  auto queue_at = [&](int j) -> int {
-    return (j < C::QUEUE_CAP) ? lds_s32(s_queue + 4 * j) : p.q_queue[qbeg + j];
-  };
   if (warp == 9) tmem_alloc<512>(tmem_slot);
   if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tq);
@@ -170,90 +187,163 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
+  // unit ring slot us: header word w, queue entry j (entries past the
+  // staged prefix come from global memory)
+  auto hdr_at = [&](int us, int w) -> int { return lds_s32(smem_u32(smem + C::U_OFF + us * C::U_BYTES) + 4 * w); };
+  auto queue_at = [&](int us, int j) -> int {
+    return (j < C::QUEUE_CAP) ? lds_s32(smem_u32(smem + C::U_OFF + us * C::U_BYTES) + 4 * (C::U_HDR + j))
+                              : p.q_queue[hdr_at(us, UH_QBEG) + j];
+  };
+
+  // Every role walks the CTA's unit sequence through the unit ring (filled by
+  // the producer). Rings (units, K, V, mask vectors) and per-head barriers
+  // keep counting across units, so the loads and MMAs of the next unit start
+  // while the softmax warps finish the current one.
   if (*abort_flag) {
     // fall through to teardown
   } else if (warp == 8) {
     // ------------------------------------------------------------ producer
     bool ok = true;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bars[C::B_QFULL], T * C::TILE);
-      for (int t = 0; t < T; ++t)
-        for (int x = 0; x < C::BOXES; ++x)
-          tma_load_3d(smem + C::Q_OFF + t * C::TILE + x * 16384, &tq, &bars[C::B_QFULL], x * 64, q0,
-                      b * p.H_q + h0 + t);
-    }
-    int pidx = 0;
-    const size_t vbase = (size_t)b * p.N;
-    for (int j = 0; j < n && ok; ++j) {
-      const int e = queue_at(j);
-      const int kb = e >> 1;
-      if (kb < 0 || kb >= p.nK) {
-        if (lane == 0) record_error(p.err, FM_DEV_ERR_QUEUE);
-        *abort_flag = 1;
+    uint32_t jt = 0, pidx = 0, uq = 0;  // K/V blocks, partial blocks, non-empty units so far
+    // Units are handed out dynamically: each CTA starts with unit blockIdx.x,
+    // then takes the next unhandled one from the work counter, so CTAs that
+    // drew short queues take more units and the units in flight stay close
+    // to the sequence order (neighbours share K / V tiles in L2).
+    int k = blockIdx.x;
+    for (uint32_t ui = 0; ok; ++ui) {
+      // decode the unit into the ring (its queue staged in shared memory)
+      const int us = ui & 1;
+      ok = __all_sync(kFull, mbar_wait(&bars[C::B_UEMPTY + us], ((ui >> 1) & 1u) ^ 1u, abort_flag, p.err));
+      if (!ok) break;
+      int* h = reinterpret_cast<int*>(smem + C::U_OFF + us * C::U_BYTES);
+      if (k >= p.units) {
+        // no work left: tell the other roles
+        if (lane == 0) h[UH_END] = 1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::B_UFULL + us]);
         break;
       }
-      const bool part = (e & 1) || (kb == p.nK - 1 && (p.N & 127));
-      const int slot = j % S;
-      const uint32_t ph = (uint32_t)(j / S) & 1u;
-      if (lane == 0) {
-        ok = mbar_wait(&bars[C::B_KEMPTY + slot], ph ^ 1u, abort_flag, p.err);
-        if (ok) {
-          mbar_arrive_expect_tx(&bars[C::B_KFULL + slot], C::TILE);
-          for (int x = 0; x < C::BOXES; ++x)
-            tma_load_3d(smem + C::K_OFF + slot * C::TILE + x * 16384, &tk, &bars[C::B_KFULL + slot], x * 64,
-                        kb * 128, b * p.H_kv + g);
+      // the next unit's index, requested now and used after this unit
+      int k_next = 0;
+      if (lane == 0) k_next = (int)gridDim.x + atomicAdd(p.next_unit, 1);
+      const Unit u = decode_unit(p, k);
+      {
+        if (lane == 0) {
+          h[UH_END] = 0;
+          h[UH_N] = u.n;
+          h[UH_T] = u.T;
+          h[UH_QB] = u.qb;
+          h[UH_B] = u.b;
+          h[UH_H0] = u.h0;
+          h[UH_G] = u.g;
+          h[UH_QBEG] = u.qbeg;
         }
+        int* sq = h + C::U_HDR;
+        const int m = min(u.n, C::QUEUE_CAP);
+        for (int j0 = 0; j0 < m; j0 += 128) {
+          int e[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int j = j0 + 32 * r + lane;
+            e[r] = (j < m) ? p.q_queue[u.qbeg + j] : 0;
+          }
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int j = j0 + 32 * r + lane;
+            if (j < m) sq[j] = e[r];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::B_UFULL + us]);
       }
-      ok = __shfl_sync(kFull, ok, 0);
-      if (!ok) break;
-      if (part) {
-        // the block's four mask vectors, raw, as 4 x 128 int32 (LTS, LTE, UTS,
-        // UTE); the softmax warps clamp and check them
-        const int ms = pidx % S;
-        const uint32_t mph = (uint32_t)(pidx / S) & 1u;
-        ok = __all_sync(kFull, mbar_wait(&bars[C::B_MEMPTY + ms], mph ^ 1u, abort_flag, p.err));
+      k = __shfl_sync(kFull, k_next, 0);
+      if (u.n <= 0) continue;
+      const size_t vbase = (size_t)u.b * p.N;
+      for (int j = 0; j < u.n && ok; ++j) {
+        const int e = queue_at(us, j);
+        const int kb = e >> 1;
+        if (kb < 0 || kb >= p.nK) {
+          if (lane == 0) record_error(p.err, FM_DEV_ERR_QUEUE);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        const bool part = block_partial(p, e);
+        const int slot = jt % S;
+        const uint32_t ph = (jt / S) & 1u;
+        if (lane == 0) {
+          ok = mbar_wait(&bars[C::B_KEMPTY + slot], ph ^ 1u, abort_flag, p.err);
+          if (ok) {
+            mbar_arrive_expect_tx(&bars[C::B_KFULL + slot], C::TILE);
+            for (int x = 0; x < C::BOXES; ++x)
+              tma_load_3d(smem + C::K_OFF + slot * C::TILE + x * 16384, &tk, &bars[C::B_KFULL + slot], x * 64,
+                          kb * 128, u.b * p.H_kv + u.g);
+          }
+          if (ok && j == 0) {
+            // the Q tiles of this unit, once the last S MMA of the previous one is done
+            if (uq > 0) ok = mbar_wait(&bars[C::B_QFREE], (uq - 1) & 1u, abort_flag, p.err);
+            if (ok) {
+              mbar_arrive_expect_tx(&bars[C::B_QFULL], u.T * C::TILE);
+              for (int t = 0; t < u.T; ++t)
+                for (int x = 0; x < C::BOXES; ++x)
+                  tma_load_3d(smem + C::Q_OFF + t * C::TILE + x * 16384, &tq, &bars[C::B_QFULL], x * 64,
+                              u.qb * 128, u.b * p.H_q + u.h0 + t);
+            }
+          }
+        }
+        ok = __shfl_sync(kFull, ok, 0);
         if (!ok) break;
-        uint8_t* sm = smem + C::M_OFF + ms * C::M_BYTES;
-        const int c0 = kb * 128;
-        const size_t o = vbase + c0;
-        const bool aligned = ((reinterpret_cast<uintptr_t>(p.lts + o) | reinterpret_cast<uintptr_t>(p.lte + o) |
-                               reinterpret_cast<uintptr_t>(p.uts + o) | reinterpret_cast<uintptr_t>(p.ute + o)) &
-                              15u) == 0;
-        if (c0 + 128 <= p.N && aligned) {
-          // whole block in range and 16-byte aligned: four bulk copies
-          if (lane == 0) {
-            uint64_t* fb = &bars[C::B_MFULL + ms];
-            mbar_arrive_expect_tx(fb, 4 * 512);
-            bulk_load(sm + 0, p.lts + o, 512, fb);
-            bulk_load(sm + 512, p.lte + o, 512, fb);
-            bulk_load(sm + 1024, p.uts + o, 512, fb);
-            bulk_load(sm + 1536, p.ute + o, 512, fb);
+        if (part) {
+          // the block's four mask vectors, raw, as 4 x 128 int32 (LTS, LTE, UTS,
+          // UTE); the softmax warps clamp and check them
+          const int ms = pidx % S;
+          const uint32_t mph = (pidx / S) & 1u;
+          ok = __all_sync(kFull, mbar_wait(&bars[C::B_MEMPTY + ms], mph ^ 1u, abort_flag, p.err));
+          if (!ok) break;
+          uint8_t* sm = smem + C::M_OFF + ms * C::M_BYTES;
+          const int c0 = kb * 128;
+          const size_t o = vbase + c0;
+          const bool aligned = ((reinterpret_cast<uintptr_t>(p.lts + o) | reinterpret_cast<uintptr_t>(p.lte + o) |
+                                 reinterpret_cast<uintptr_t>(p.uts + o) | reinterpret_cast<uintptr_t>(p.ute + o)) &
+                                15u) == 0;
+          if (c0 + 128 <= p.N && aligned) {
+            // whole block in range and 16-byte aligned: four bulk copies
+            if (lane == 0) {
+              uint64_t* fb = &bars[C::B_MFULL + ms];
+              mbar_arrive_expect_tx(fb, 4 * 512);
+              bulk_load(sm + 0, p.lts + o, 512, fb);
+              bulk_load(sm + 512, p.lte + o, 512, fb);
+              bulk_load(sm + 1024, p.uts + o, 512, fb);
+              bulk_load(sm + 1536, p.ute + o, 512, fb);
+            }
+          } else {
+            int* v = reinterpret_cast<int*>(sm);
+            for (int c = lane; c < 128; c += 32) {
+              const int col = c0 + c;
+              const bool in = col < p.N;  // a key beyond N is masked for every row
+              v[c] = in ? p.lts[vbase + col] : 0;
+              v[128 + c] = in ? p.lte[vbase + col] : p.N;
+              v[256 + c] = in ? p.uts[vbase + col] : 0;
+              v[384 + c] = in ? p.ute[vbase + col] : 0;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[C::B_MFULL + ms]);
           }
-        } else {
-          int* v = reinterpret_cast<int*>(sm);
-          for (int c = lane; c < 128; c += 32) {
-            const int col = c0 + c;
-            const bool in = col < p.N;  // a key beyond N is masked for every row
-            v[c] = in ? p.lts[vbase + col] : 0;
-            v[128 + c] = in ? p.lte[vbase + col] : p.N;
-            v[256 + c] = in ? p.uts[vbase + col] : 0;
-            v[384 + c] = in ? p.ute[vbase + col] : 0;
+          ++pidx;
+        }
+        if (lane == 0) {
+          ok = mbar_wait(&bars[C::B_VEMPTY + slot], ph ^ 1u, abort_flag, p.err);
+          if (ok) {
+            mbar_arrive_expect_tx(&bars[C::B_VFULL + slot], C::TILE);
+            for (int x = 0; x < C::BOXES; ++x)
+              tma_load_3d(smem + C::V_OFF + slot * C::TILE + x * 16384, &tv, &bars[C::B_VFULL + slot], x * 64,
+                          kb * 128, u.b * p.H_kv + u.g);
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[C::B_MFULL + ms]);
         }
-        ++pidx;
+        ok = __shfl_sync(kFull, ok, 0);
+        ++jt;
       }
-      if (lane == 0) {
-        ok = mbar_wait(&bars[C::B_VEMPTY + slot], ph ^ 1u, abort_flag, p.err);
-        if (ok) {
-          mbar_arrive_expect_tx(&bars[C::B_VFULL + slot], C::TILE);
-          for (int x = 0; x < C::BOXES; ++x)
-            tma_load_3d(smem + C::V_OFF + slot * C::TILE + x * 16384, &tv, &bars[C::B_VFULL + slot], x * 64,
-                        kb * 128, b * p.H_kv + g);
-        }
-      }
-      ok = __shfl_sync(kFull, ok, 0);
+      ++uq;
     }
   } else if (warp == 9) {
     // --------------------------------------------------------- MMA issuer
@@ -266,64 +356,136 @@ __global__ void __launch_bounds__(320, 1)
       const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + C::Q_OFF), 16, 1024);
       const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::K_OFF), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::V_OFF), 16384, 1024);
-      bool ok = mbar_wait(&bars[C::B_QFULL], 0, abort_flag, p.err);
-      tc_fence_after();
-      for (int j = 0; j <= n && ok; ++j) {
-        const int slot = j % S, pslot = (j + S - 1) % S;
-        if (j < n) {
-          ok = mbar_wait(&bars[C::B_KFULL + slot], (uint32_t)(j / S) & 1u, abort_flag, p.err);
-          tc_fence_after();
-        }
-        if (ok && j > 0) {
-          ok = mbar_wait(&bars[C::B_VFULL + pslot], (uint32_t)((j - 1) / S) & 1u, abort_flag, p.err);
-          tc_fence_after();
-        }
-        for (int t = 0; t < T && ok; ++t) {
-          const uint32_t tS = tbase + (uint32_t)(t * 128);
-          if (j > 0) {
-            ok = mbar_wait(&bars[C::B_PREADY + t], (uint32_t)(j - 1) & 1u, abort_flag, p.err);
-            tc_fence_after();
-            if (!ok) break;
-            const uint32_t tO = tbase + 256u + (uint32_t)(t * D);
-            const uint64_t vd = dV0 + kTileStep * (uint64_t)pslot;
+      bool ok = true;
+      uint32_t jt = 0, uq = 0, ui = 0;
+      uint32_t npv0 = 0u, npv1 = 0u;  // PV MMAs issued per head so far
+      // PV of one block for head t: V from ring slot vs; the unit's first
+      // block overwrites O instead of accumulating
+      auto issue_pv = [&](int t, uint32_t vs, bool first) -> bool {
+        if (!mbar_wait(&bars[C::B_PREADY + t], (t ? npv1 : npv0) & 1u, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t tS = tbase + (uint32_t)(t * 128);
+        const uint32_t tO = tbase + 256u + (uint32_t)(t * D);
+        const uint64_t vd = dV0 + kTileStep * (uint64_t)vs;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_ts(tO, tS + (uint32_t)(k * 8), vd + (uint64_t)(k * 128), id_o, (j > 1 || k > 0) ? 1u : 0u);
-            mma_commit(&bars[C::B_ODONE + t]);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tO, tS + (uint32_t)(kk * 8), vd + (uint64_t)(kk * 128), id_o, (!first || kk > 0) ? 1u : 0u);
+        mma_commit(&bars[C::B_ODONE + t]);
+        if (t) ++npv1;
+        else ++npv0;
+        return true;
+      };
+      for (; ok; ++ui) {
+        const int us = ui & 1;
+        ok = mbar_wait(&bars[C::B_UFULL + us], (ui >> 1) & 1u, abort_flag, p.err);
+        if (!ok || hdr_at(us, UH_END)) break;
+        const int n = hdr_at(us, UH_N), T = hdr_at(us, UH_T);
+        mbar_arrive(&bars[C::B_UEMPTY + us]);
+        if (n <= 0) continue;
+        ok = mbar_wait(&bars[C::B_QFULL], uq & 1u, abort_flag, p.err);
+        tc_fence_after();
+        uint32_t pslot = 0;
+        for (int j = 0; j < n && ok; ++j) {
+          const int slot = jt % S;
+          ok = mbar_wait(&bars[C::B_KFULL + slot], (jt / S) & 1u, abort_flag, p.err);
+          tc_fence_after();
+          if (ok && j > 0) {
+            ok = mbar_wait(&bars[C::B_VFULL + pslot], ((jt - 1) / S) & 1u, abort_flag, p.err);
+            tc_fence_after();
           }
-          if (j < n) {
+          // per head: the previous block's PV, then this block's S into the
+          // same TMEM columns (the tensor core runs them in issue order)
+          for (int t = 0; t < T && ok; ++t) {
+            if (j > 0) ok = issue_pv(t, pslot, j == 1);
+            if (!ok) break;
+            const uint32_t tS = tbase + (uint32_t)(t * 128);
             const uint64_t qd = dQ0 + kTileStep * (uint64_t)t, kd = dK0 + kTileStep * (uint64_t)slot;
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              const uint64_t off = (uint64_t)((k >> 2) * 1024 + (k & 3) * 2);
-              mma_ss(tS, qd + off, kd + off, id_s, k > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t off = (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);
+              mma_ss(tS, qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
             }
             mma_commit(&bars[C::B_SFULL + t]);
           }
-        }
-        if (ok) {
+          if (!ok) break;
           if (j > 0) mma_commit(&bars[C::B_VEMPTY + pslot]);
-          if (j < n) mma_commit(&bars[C::B_KEMPTY + slot]);
+          mma_commit(&bars[C::B_KEMPTY + slot]);
+          if (j == n - 1) mma_commit(&bars[C::B_QFREE]);
+          pslot = slot;
+          ++jt;
         }
+        if (!ok) break;
+        // the unit's last PV, before anything of the next unit: the softmax
+        // warps' epilogue waits for it
+        ok = mbar_wait(&bars[C::B_VFULL + pslot], ((jt - 1) / S) & 1u, abort_flag, p.err);
+        tc_fence_after();
+        for (int t = 0; t < T && ok; ++t) ok = issue_pv(t, pslot, n == 1);
+        if (!ok) break;
+        mma_commit(&bars[C::B_VEMPTY + pslot]);
+        ++uq;
       }
     }
   } else {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;
-    if (t < T) {
-      const int row = ((warp & 3) << 5) + lane;
+    const int row = ((warp & 3) << 5) + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tbase + lane_off + (uint32_t)(t * 128);
+    const uint32_t tO = tbase + lane_off + 256u + (uint32_t)(t * D);
+    const float sl2 = p.scale_log2;
+    const bool causal = p.causal != 0;
+    const uint32_t oslot = smem_u32(smem + C::O_OFF + warp * C::O_SLOT);
+    bool ok = t < tmax;
+    uint32_t jh = 0, pidx = 0, ui = 0;  // blocks of this head, partial blocks, units so far
+    for (; ok; ++ui) {
+      const int us = ui & 1;
+      ok = __all_sync(kFull, mbar_wait(&bars[C::B_UFULL + us], (ui >> 1) & 1u, abort_flag, p.err));
+      if (!ok || hdr_at(us, UH_END)) break;
+      const int n = hdr_at(us, UH_N), T = hdr_at(us, UH_T);
+      const int q0 = hdr_at(us, UH_QB) * 128;
       const int i = q0 + row;
-      const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-      const uint32_t tS = tbase + lane_off + (uint32_t)(t * 128);
-      const uint32_t tO = tbase + lane_off + 256u + (uint32_t)(t * D);
-      const float sl2 = p.scale_log2;
+      const int w0 = q0 + ((warp & 3) << 5);  // the warp's first row
+      if (n <= 0) {
+        // No visible key for any row of this unit: O = 0 (the warp's staging
+        // slot, zeroed, is the source of all its stores), LSE = -inf.
+        if (n < 0 && threadIdx.x == 0) record_error(p.err, FM_DEV_ERR_QUEUE);
+        if (t < T) {
+          const int bh = hdr_at(us, UH_B) * p.H_q + hdr_at(us, UH_H0) + t;
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) sts_b32x4(oslot + 64 * lane + 16 * c, 0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            for (int c0 = 0; c0 < D; c0 += 32) tma_store_3d(&to, oslot, c0, w0, bh);
+            bulk_commit_group();
+          }
+          if (i < p.N) p.lse[(size_t)bh * p.N + i] = -INFINITY;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::B_UEMPTY + us]);
+        continue;
+      }
+      if (t >= T) {
+        // a single-head unit: the second head's warps only advance the
+        // partial-block count (head 0 releases the mask ring for both)
+        uint32_t c = 0;
+        for (int j0 = 0; j0 < n; j0 += 32) {
+          const bool part = (j0 + lane < n) && block_partial(p, queue_at(us, j0 + lane));
+          c += __popc(__ballot_sync(kFull, part));
+        }
+        pidx += c;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::B_UEMPTY + us]);
+        continue;
+      }
+      const uint32_t mrel = (T < tmax) ? 2u : 1u;  // MEMPTY arrivals per warp
       float m_run = -INFINITY, l_run = 0.f;
-      int pidx = 0;
-      bool ok = true;
       for (int j = 0; j < n; ++j) {
-        const int e = queue_at(j);
+        const int e = queue_at(us, j);
         const int kb = e >> 1;
-        const bool part = (e & 1) || (kb == p.nK - 1 && (p.N & 127));
+        const bool part = block_partial(p, e);
         // Partial blocks: masked-row bits of this thread's query row over the
         // block's 128 key columns, built while S is still being computed. Lane
         // c of the warp builds the bits of key column 32k + c over the warp's
@@ -331,28 +493,26 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t rb[4] = {0u, 0u, 0u, 0u};
         if (part) {
           const int ms = pidx % S;
-          ok = __all_sync(kFull, mbar_wait(&bars[C::B_MFULL + ms], (uint32_t)(pidx / S) & 1u, abort_flag, p.err));
+          ok = __all_sync(kFull, mbar_wait(&bars[C::B_MFULL + ms], (pidx / S) & 1u, abort_flag, p.err));
           if (!ok) break;
           const uint32_t sm = smem_u32(smem + C::M_OFF + ms * C::M_BYTES);
-          const int w0 = q0 + ((warp & 3) << 5);
           const int kc0 = kb * 128;
-          const bool causal = p.causal != 0;
           // Values outside [0, N] only need clamping here: fm_classify_tiles,
           // run on the same vectors, flags them.
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int c = 32 * k + lane;
+          for (int kq = 0; kq < 4; ++kq) {
+            const int c = 32 * kq + lane;
             const int a0 = lds_s32(sm + 4 * c), a1 = lds_s32(sm + 512 + 4 * c);  // LTS, LTE of key column kc0 + c
             const int u0 = lds_s32(sm + 1024 + 4 * c), u1 = lds_s32(sm + 1536 + 4 * c);  // UTS, UTE
             const uint32_t colbits = window_bits(a0, a1, w0) | window_bits(u0, u1, w0) |
                                      (causal ? window_bits(w0, kc0 + c, w0) : 0u);
-            rb[k] = warp_transpose32(colbits, lane);
+            rb[kq] = warp_transpose32(colbits, lane);
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[C::B_MEMPTY + ms]);
+          if (lane == 0) mbar_arrive_cnt(&bars[C::B_MEMPTY + ms], mrel);
           ++pidx;
         }
-        ok = __all_sync(kFull, mbar_wait(&bars[C::B_SFULL + t], (uint32_t)j & 1u, abort_flag, p.err));
+        ok = __all_sync(kFull, mbar_wait(&bars[C::B_SFULL + t], jh & 1u, abort_flag, p.err));
         if (!ok) break;
         tc_fence_after();
         uint32_t sr[128];
@@ -420,8 +580,9 @@ __global__ void __launch_bounds__(320, 1)
           tmem_st_wait();
         }
         if (j > 0 && __any_sync(kFull, resc)) {
-          // O holds PV of blocks < j: wait for the last of them, then rescale the row.
-          ok = __all_sync(kFull, mbar_wait(&bars[C::B_ODONE + t], (uint32_t)(j - 1) & 1u, abort_flag, p.err));
+          // O holds PV of the unit's earlier blocks: wait for the last of them,
+          // then rescale the row.
+          ok = __all_sync(kFull, mbar_wait(&bars[C::B_ODONE + t], (jh - 1) & 1u, abort_flag, p.err));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -437,43 +598,49 @@ __global__ void __launch_bounds__(320, 1)
         }
         tc_fence_before();
         mbar_arrive(&bars[C::B_PREADY + t]);
+        ++jh;
       }
-      if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_ODONE + t], (uint32_t)(n - 1) & 1u, abort_flag, p.err));
-      if (ok) {
-        // O rows go through this head's Q tile in shared memory (free: every S
-        // MMA finished before the last PV) in the 128-byte-swizzled box layout,
-        // then one TMA store writes the tile; rows beyond N are clipped by it.
-        tc_fence_after();
-        const size_t bh = (size_t)b * p.H_q + h0 + t;
-        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-        uint8_t* stage = smem + C::Q_OFF + t * C::TILE;
+      if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_ODONE + t], (jh - 1) & 1u, abort_flag, p.err));
+      if (!ok) break;
+      // Epilogue: O / l, 32 columns at a time, from TMEM through the warp's
+      // staging slot (64-byte swizzle: row r's 16-byte chunk c sits at chunk
+      // c ^ ((r >> 1) & 3), which keeps the row-per-lane stores conflict-free)
+      // to one TMA store of the warp's 32 rows; rows past N are clipped by it.
+      // The next unit's first PV overwrites O only after this thread's next
+      // PREADY arrival, which follows these loads.
+      tc_fence_after();
+      const int bh = hdr_at(us, UH_B) * p.H_q + hdr_at(us, UH_H0) + t;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C::B_UEMPTY + us]);
+      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(tO + c0, r);
-          tmem_ld_wait();
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tO + c0, r);
+        tmem_ld_wait();
+        const float* f = reinterpret_cast<const float*>(r);
+        uint32_t w[16];
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            const float* f = reinterpret_cast<const float*>(&r[8 * v4]);
-            const int col = c0 + 8 * v4;  // first of 8 columns = one 16-byte chunk
-            const uint32_t addr = smem_u32(stage + (col >> 6) * 16384 + row * 128 +
-                                           ((((col & 63) >> 3) ^ (row & 7)) << 4));
-            sts_b32x4(addr, pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
-                      pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
-          }
-        }
+        for (int c = 0; c < 16; ++c) w[c] = pack_bf16x2(f[2 * c] * inv, f[2 * c + 1] * inv);
+        if (lane == 0) bulk_wait_group_read0();  // the slot's previous store has read it
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          sts_b32x4(oslot + 64 * lane + 16 * (c ^ ((lane >> 1) & 3)), w[4 * c], w[4 * c + 1], w[4 * c + 2],
+                    w[4 * c + 3]);
         fence_proxy_async_smem();
-        mbar_arrive(&bars[C::B_OSTAGED + t]);
-        if (row == 0 && mbar_wait(&bars[C::B_OSTAGED + t], 0, abort_flag, p.err)) {
-          for (int x = 0; x < C::BOXES; ++x) tma_store_3d(&to, stage + x * 16384, x * 64, q0, (int)bh);
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&to, oslot, c0, w0, bh);
           bulk_commit_group();
-          bulk_wait_group_read0();
         }
-        if (i < p.N) p.lse[bh * p.N + i] = (l_run > 0.f) ? (m_run * kLn2 + logf(l_run)) : -INFINITY;
       }
+      if (i < p.N) p.lse[(size_t)bh * p.N + i] = (l_run > 0.f) ? (m_run * kLn2 + logf(l_run)) : -INFINITY;
     }
   }
 
+  // the staging slots stay valid until the TMA stores have read them
+  if (warp < 8 && lane == 0) bulk_wait_group_read0();
   tc_fence_before();
   __syncthreads();
   if (warp == 9) {
@@ -502,10 +669,11 @@ cudaError_t launch_fwd_d(const fm_problem& P, const CUtensorMap& tq, const CUten
   return cudaGetLastError();
 }
 
-// Library-owned scratch for fm_attn_fwd_noalloc: the launch-order table
-// (one int32 per Q block). Fixed size, present on every device that loads the
-// library, shared by all calls on that device.
-static __device__ __align__(256) int32_t g_noalloc_order[FM_NOALLOC_MAX_QBLOCKS];
+// Library-owned scratch for fm_attn_fwd_noalloc, laid out like the forward
+// workspace: the unit-order table (one int32 per Q block) and the work
+// counter. Fixed size, present on every device that loads the library, shared
+// by all calls on that device.
+static __device__ __align__(256) int32_t g_noalloc_order[FM_NOALLOC_MAX_QBLOCKS + 64];
 
 }  // namespace
 
@@ -526,10 +694,14 @@ int32_t* fwd_noalloc_scratch() {
   return cached[dev];
 }
 
-size_t fwd_ws_bytes(const fm_problem& p) {
+// Forward workspace: the unit-order table (one int32 per Q block, padded to
+// 256 bytes), then the work counter (256 bytes).
+static size_t fwd_order_bytes(const fm_problem& p) {
   const size_t nQ = (size_t)(p.N + kTile - 1) / kTile;
   return ((4 * (size_t)p.B * nQ) + 255) & ~size_t(255);
 }
+
+size_t fwd_ws_bytes(const fm_problem& p) { return fwd_order_bytes(p) + 256; }
 
 cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const void* v, const int32_t* lts,
                        const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
@@ -537,16 +709,22 @@ cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const 
   const int nQ = (P.N + kTile - 1) / kTile;
   const int G = P.H_q / P.H_kv;
   const int PG = (G + 1) / 2;
-  const long long grid = (long long)P.B * nQ * P.H_kv * PG;
-  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  // launch order: longest queue first, or natural order for long passes
-  // (CTAs that run together then share K / V tiles in L2)
-  const bool natural = use_natural_order(grid);
+  const long long units = (long long)P.B * nQ * P.H_kv * PG;
+  if (units > INT_MAX) return cudaErrorInvalidConfiguration;
+  // unit order: longest queue first, or natural order for long passes
+  // (units that run together then share K / V tiles in L2)
+  const bool natural = use_natural_order(units);
   int32_t* order = natural ? nullptr : static_cast<int32_t*>(ws);
+  int* next_unit = reinterpret_cast<int*>(static_cast<char*>(ws) + fwd_order_bytes(P));
+  {
+    cudaError_t e = cudaMemsetAsync(next_unit, 0, sizeof(int), s);
+    if (e != cudaSuccess) return e;
+  }
   if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, P.B * nQ, order);
   CUtensorMap tq, tk, tv, to;
   if (!make_tmap_bhnd(&tq, q, (int64_t)P.B * P.H_q, P.N, P.d) || !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, P.N, P.d) ||
-      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, P.N, P.d) || !make_tmap_bhnd(&to, o, (int64_t)P.B * P.H_q, P.N, P.d))
+      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, P.N, P.d) ||
+      !make_tmap_bhnd_w32(&to, o, (int64_t)P.B * P.H_q, P.N, P.d))
     return cudaErrorInvalidValue;
   FwdParams prm;
   prm.lts = lts;
@@ -556,6 +734,7 @@ cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const 
   prm.q_off = q_off;
   prm.q_queue = q_queue;
   prm.order = order;
+  prm.next_unit = next_unit;
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
   prm.B = P.B;
@@ -567,10 +746,13 @@ cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const 
   prm.G = G;
   prm.PG = PG;
   prm.causal = P.causal ? 1 : 0;
+  prm.units = (int)units;
   prm.scale_log2 = P.scale * 1.4426950408889634f;
   prm.err = err;
-  if (P.d == 128) return launch_fwd_d<128>(P, tq, tk, tv, to, prm, (unsigned)grid, s);
-  return launch_fwd_d<64>(P, tq, tk, tv, to, prm, (unsigned)grid, s);
+  // persistent: one CTA per SM (the kernel's shared memory and TMEM fill an SM)
+  const unsigned grid = (unsigned)std::min<long long>(units, (long long)sm_count());
+  if (P.d == 128) return launch_fwd_d<128>(P, tq, tk, tv, to, prm, grid, s);
+  return launch_fwd_d<64>(P, tq, tk, tv, to, prm, grid, s);
 }
 
 }  // namespace fm

@@ -41,8 +41,6 @@ cudaError_t launch_bwd(const fm_problem& p, const void* q, const void* k, const 
                        const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
                        void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err);
 
-// Tensor maps (fm_api.cu): 3-D bf16 map over a contiguous (BH, N, d) tensor,
-// box {64, box_rows, 1}, 128-byte swizzle; rows >= N read as zero.
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
@@ -51,12 +49,17 @@ int sm_count();
 // (backward) tiles in L2, and the tail is a small part of the pass.
 inline bool use_natural_order(long long ctas) { return ctas >= 8LL * sm_count(); }
 
+// Tensor maps (fm_api.cu): 3-D bf16 map over a contiguous (BH, N, d) tensor,
+// box {64, box_rows, 1}, 128-byte swizzle; rows >= N read as zero.
 bool make_tmap_bhnd(void* out_tmap /* CUtensorMap* */, const void* base, int64_t BH, int64_t N, int64_t d,
                     int box_rows = 128);
 // Same for an fp32 (BH, N, d) tensor, box {box_cols, box_rows, 1}, no swizzle
 // (used as the destination of TMA reduce-adds).
 bool make_tmap_f32_bhnd(void* out_tmap /* CUtensorMap* */, const void* base, int64_t BH, int64_t N, int64_t d,
                         int box_cols, int box_rows);
+// Same bf16 tensor, box {32, 32, 1}, 64-byte swizzle: one warp's 32 rows x 32
+// columns of a store (rows >= N are not written).
+bool make_tmap_bhnd_w32(void* out_tmap /* CUtensorMap* */, const void* base, int64_t BH, int64_t N, int64_t d);
 
 constexpr int kTile = 128;  // attention tile (block_m = block_n)
 

@@ -69,6 +69,10 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// one arrival worth `count` of the barrier's expected arrivals
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
@@ -126,11 +130,14 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
 }
 // 3-D tiled store from shared memory (bulk group; rows outside the tensor
 // are not written). Wait with bulk_wait_group_read0 before reusing the source.
-__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, int32_t x, int32_t y, int32_t z) {
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int32_t x, int32_t y, int32_t z) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(tmap)),
-               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, int32_t x, int32_t y, int32_t z) {
+  tma_store_3d(tmap, smem_u32(src), x, y, z);
 }
 // 3-D tiled reduce-add (fp32) of a shared-memory box into global memory
 // (bulk group; rows outside the tensor are skipped).
@@ -349,6 +356,14 @@ __device__ __forceinline__ int lds_s32(uint32_t addr) {
 }
 __device__ __forceinline__ void sts_b32x4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// 32-byte global store (one full sector); the address must be 32-byte aligned
+__device__ __forceinline__ void stg_b32x8(void* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                          uint32_t f, uint32_t g, uint32_t h) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a), "r"(b), "r"(c),
+               "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+               : "memory");
 }
 
 // ------------------------------------------------------------ arithmetic
