@@ -465,7 +465,7 @@ def run_ours(args, cfg):
     dom_flops = work[dom]
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops"]
-    traffic = ncu_traffic(dom)
+    traffic = ncu_traffic(dom, args.workload)
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -496,19 +496,22 @@ def run_ours(args, cfg):
     return 0
 
 
-# ncu DRAM traffic (read + write bytes per launch) of the main kernels, valid
-# only while the kernel source is the one the counters were taken from.
+# ncu DRAM traffic (read + write bytes per launch) of the main kernels on the
+# workload it was captured on, valid only while the kernel source is the one
+# the counters were taken from.
 NCU_TRAFFIC = {
-    "bwd": {"file": "fm_bwd.cu", "sha256": "ddac91c410bf1b64f4ff2524b0f2b5e543b5721417247545c4d8b06ebfcf7f04", "bytes": 1269846784},
-    "fwd": {"file": "fm_fwd.cu", "sha256": "e3a20e852c94a6914948f63b7531b75617a7ceee642d81493bbed8574bd9c040", "bytes": 481385216},
+    "bwd": {"file": "fm_bwd.cu", "workload": "share_question32k",
+            "sha256": "ddac91c410bf1b64f4ff2524b0f2b5e543b5721417247545c4d8b06ebfcf7f04", "bytes": 1269846784},
+    "fwd": {"file": "fm_fwd.cu", "workload": "share_question32k",
+            "sha256": "e11f01009db33344bf913b9d612db8238b24f5b8ed99b1955972d1efd466ced4", "bytes": 482938880},
 }
 
 
-def ncu_traffic(kind: str):
+def ncu_traffic(kind: str, workload: str):
     import hashlib
 
     ent = NCU_TRAFFIC.get(kind)
-    if not ent:
+    if not ent or ent["workload"] != workload:
         return None
     src = os.path.join(ROOT, "mask_aware_sparse_gb300", "csrc", ent["file"])
     try:

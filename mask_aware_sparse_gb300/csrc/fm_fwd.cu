@@ -9,27 +9,38 @@
 // Hierarchy".
 //
 // GB300 design (not the pages' Hopper design):
-//   * One CTA = one work unit = (batch b, Q block qb, a PAIR of query heads of
-//     the same GQA group). Both heads share the K/V head and the mask, so they
-//     share every K/V tile load and the same queue.
+//   * Work unit = (batch b, Q block qb, a PAIR of query heads of the same GQA
+//     group). Both heads share the K/V head and the mask, so they share every
+//     K/V tile load and the same queue.
+//   * Persistent: one CTA per SM. Each CTA starts with unit blockIdx.x and
+//     then takes the next unhandled unit from a work counter, so load balance
+//     is dynamic and the units in flight stay close to the sequence order.
+//     The producer decodes each unit into a two-slot unit ring in shared
+//     memory (header + queue); all rings and barriers keep counting across
+//     units, so the next unit's loads and first S MMAs overlap the current
+//     unit's last softmax and epilogue, and the setup (barriers, TMEM
+//     allocation) is paid once per SM.
 //   * Warp roles (320 threads):
 //       warps 0-3  softmax for query tile 0 (one thread per query row)
 //       warps 4-7  softmax for query tile 1
-//       warp  8    producer: TMA loads of Q, K, V and the mask vectors of
-//                  partial blocks into shared memory rings
+//       warp  8    producer: unit ring, TMA loads of Q, K, V and the mask
+//                  vectors of partial blocks into shared memory rings
 //       warp  9    MMA issuer (one elected lane) and TMEM owner
 //   * TMEM (512 columns x 128 lanes): S_t at columns [128t, 128t+128); P_t is
 //     written back as bf16 over the first 64 columns of S_t and consumed from
 //     TMEM by the PV MMA; O_t at [256 + t*d, 256 + (t+1)*d).
 //   * The MMA warp interleaves the two tiles: PV_0(j-1), S_0(j), PV_1(j-1),
 //     S_1(j), so the tensor core works on one tile while softmax works on the
-//     other.
+//     other. A unit's last PV goes out before anything of the next unit.
 //   * Rescaling of O is lazy: the running max used for exponentials only moves
 //     when the block max exceeds it by more than 8 (log2 units), so P <= 256;
 //     O and l are always scaled consistently, so O / l is unchanged.
-//   * Launch order: longest queue first (an LPT order computed on the device
+//   * Epilogue: each softmax warp writes its 32 rows of O / l, 32 columns at
+//     a time, into its own 2 KB shared-memory slot and stores them with one
+//     TMA store (the Q tiles already hold the next unit's Q).
+//   * Unit order: longest queue first (an LPT order computed on the device
 //     from the queue offsets) for passes of a few waves, natural order for
-//     long passes, where CTAs of neighbouring query blocks share K / V tiles
+//     long passes, where units of neighbouring query blocks share K / V tiles
 //     in L2.
 #include <algorithm>
 #include <climits>
@@ -613,12 +624,13 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C::B_UEMPTY + us]);
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      uint32_t orow[D];  // the thread's O row, all columns loaded with one wait
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(&orow[c0]));
+      tmem_ld_wait();
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tO + c0, r);
-        tmem_ld_wait();
-        const float* f = reinterpret_cast<const float*>(r);
+        const float* f = reinterpret_cast<const float*>(&orow[c0]);
         uint32_t w[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) w[c] = pack_bf16x2(f[2 * c] * inv, f[2 * c + 1] * inv);
