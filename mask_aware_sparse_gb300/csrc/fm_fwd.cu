@@ -75,7 +75,10 @@ struct FwdCfg {
   static constexpr int U_HDR = 16;  // int32 header words
   static constexpr int U_BYTES = (U_HDR + QUEUE_CAP) * 4;
   static constexpr int U_OFF = O_OFF + 8 * O_SLOT;
-  static constexpr int BAR_OFF = U_OFF + 2 * U_BYTES;
+  // deferred epilogue: per softmax thread {l, m, output row head, q0} of the
+  // unit whose O is still in TMEM
+  static constexpr int EPI_OFF = U_OFF + 2 * U_BYTES;
+  static constexpr int BAR_OFF = EPI_OFF + 256 * 16;
   static constexpr int B_QFULL = 0;
   static constexpr int B_QFREE = 1;
   static constexpr int B_UFULL = 2;   // [2]
@@ -446,16 +449,75 @@ __global__ void __launch_bounds__(320, 1)
     const float sl2 = p.scale_log2;
     const bool causal = p.causal != 0;
     const uint32_t oslot = smem_u32(smem + C::O_OFF + warp * C::O_SLOT);
+    const uint32_t sepi = smem_u32(smem + C::EPI_OFF) + 16u * threadIdx.x;
     bool ok = t < tmax;
     uint32_t jh = 0, pidx = 0, ui = 0;  // blocks of this head, partial blocks, units so far
+    // Epilogue of a finished unit, deferred: its O stays in TMEM until the
+    // next unit's first P is written, so the O loads sit after that block's
+    // softmax (the last PV has finished by then) and the stores overlap the
+    // tensor core's next PV and S. pend: a unit's O is waiting.
+    bool pend = false;
+    // O / l of the unit in sepi, 32 columns at a time, through the warp's
+    // staging slot (64-byte swizzle: row r's 16-byte chunk c sits at chunk
+    // c ^ ((r >> 1) & 3), which keeps the row-per-lane stores conflict-free)
+    // to one TMA store of the warp's 32 rows (rows past N are clipped by it),
+    // then the row's LSE.
+    auto store_o = [&](const uint32_t(&orow)[D]) {
+      const int4 st = lds_s32x4(sepi);
+      const float l = __int_as_float(st.x), m = __int_as_float(st.y);
+      const int bh = st.z, q0e = st.w;
+      const int w0e = q0e + ((warp & 3) << 5), ie = q0e + row;
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        const float* f = reinterpret_cast<const float*>(&orow[c0]);
+        uint32_t w[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) w[c] = pack_bf16x2(f[2 * c] * inv, f[2 * c + 1] * inv);
+        if (lane == 0) bulk_wait_group_read0();  // the slot's previous store has read it
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          sts_b32x4(oslot + 64 * lane + 16 * (c ^ ((lane >> 1) & 3)), w[4 * c], w[4 * c + 1], w[4 * c + 2],
+                    w[4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&to, oslot, c0, w0e, bh);
+          bulk_commit_group();
+        }
+      }
+      if (ie < p.N) p.lse[(size_t)bh * p.N + ie] = (l > 0.f) ? (m * kLn2 + logf(l)) : -INFINITY;
+    };
+    // the pending epilogue with nothing to hide behind: wait for the last PV
+    auto flush = [&]() -> bool {
+      if (!pend) return true;
+      pend = false;
+      if (!__all_sync(kFull, mbar_wait(&bars[C::B_ODONE + t], (jh - 1) & 1u, abort_flag, p.err))) return false;
+      tc_fence_after();
+      uint32_t orow[D];
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(&orow[c0]));
+      tmem_ld_wait();
+      store_o(orow);
+      return true;
+    };
     for (; ok; ++ui) {
       const int us = ui & 1;
       ok = __all_sync(kFull, mbar_wait(&bars[C::B_UFULL + us], (ui >> 1) & 1u, abort_flag, p.err));
-      if (!ok || hdr_at(us, UH_END)) break;
+      if (!ok) break;
+      if (hdr_at(us, UH_END)) {
+        ok = flush();
+        break;
+      }
       const int n = hdr_at(us, UH_N), T = hdr_at(us, UH_T);
       const int q0 = hdr_at(us, UH_QB) * 128;
       const int i = q0 + row;
       const int w0 = q0 + ((warp & 3) << 5);  // the warp's first row
+      if (n <= 0 || t >= T) {
+        ok = flush();
+        if (!ok) break;
+      }
       if (n <= 0) {
         // No visible key for any row of this unit: O = 0 (the warp's staging
         // slot, zeroed, is the source of all its stores), LSE = -inf.
@@ -607,47 +669,33 @@ __global__ void __launch_bounds__(320, 1)
           }
           tmem_st_wait();
         }
-        tc_fence_before();
-        mbar_arrive(&bars[C::B_PREADY + t]);
+        if (j == 0 && pend) {
+          // the previous unit's O: its last PV is done once ODONE shows it
+          pend = false;
+          ok = __all_sync(kFull, mbar_wait(&bars[C::B_ODONE + t], (jh - 1) & 1u, abort_flag, p.err));
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t orow[D];
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(&orow[c0]));
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&bars[C::B_PREADY + t]);  // PV of this block may now overwrite O
+          store_o(orow);
+        } else {
+          tc_fence_before();
+          mbar_arrive(&bars[C::B_PREADY + t]);
+        }
         ++jh;
       }
-      if (ok) ok = __all_sync(kFull, mbar_wait(&bars[C::B_ODONE + t], (jh - 1) & 1u, abort_flag, p.err));
       if (!ok) break;
-      // Epilogue: O / l, 32 columns at a time, from TMEM through the warp's
-      // staging slot (64-byte swizzle: row r's 16-byte chunk c sits at chunk
-      // c ^ ((r >> 1) & 3), which keeps the row-per-lane stores conflict-free)
-      // to one TMA store of the warp's 32 rows; rows past N are clipped by it.
-      // The next unit's first PV overwrites O only after this thread's next
-      // PREADY arrival, which follows these loads.
-      tc_fence_after();
-      const int bh = hdr_at(us, UH_B) * p.H_q + hdr_at(us, UH_H0) + t;
+      // defer this unit's epilogue (its O stays in TMEM until the next unit's
+      // first P is written); keep what it needs and release the ring slot
+      sts_b32x4(sepi, __float_as_uint(l_run), __float_as_uint(m_run),
+                (uint32_t)(hdr_at(us, UH_B) * p.H_q + hdr_at(us, UH_H0) + t), (uint32_t)q0);
+      pend = true;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C::B_UEMPTY + us]);
-      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      uint32_t orow[D];  // the thread's O row, all columns loaded with one wait
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(&orow[c0]));
-      tmem_ld_wait();
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        const float* f = reinterpret_cast<const float*>(&orow[c0]);
-        uint32_t w[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) w[c] = pack_bf16x2(f[2 * c] * inv, f[2 * c + 1] * inv);
-        if (lane == 0) bulk_wait_group_read0();  // the slot's previous store has read it
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          sts_b32x4(oslot + 64 * lane + 16 * (c ^ ((lane >> 1) & 3)), w[4 * c], w[4 * c + 1], w[4 * c + 2],
-                    w[4 * c + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&to, oslot, c0, w0, bh);
-          bulk_commit_group();
-        }
-      }
-      if (i < p.N) p.lse[(size_t)bh * p.N + i] = (l_run > 0.f) ? (m_run * kLn2 + logf(l_run)) : -INFINITY;
     }
   }
 
