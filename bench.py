@@ -503,7 +503,7 @@ NCU_TRAFFIC = {
     "bwd": {"file": "fm_bwd.cu", "workload": "share_question32k",
             "sha256": "ddac91c410bf1b64f4ff2524b0f2b5e543b5721417247545c4d8b06ebfcf7f04", "bytes": 1269846784},
     "fwd": {"file": "fm_fwd.cu", "workload": "share_question32k",
-            "sha256": "e11f01009db33344bf913b9d612db8238b24f5b8ed99b1955972d1efd466ced4", "bytes": 482938880},
+            "sha256": "0d491e37f2b9f9134e7cba5624df579b5ddd98c57f14067ed590bb9787f236d0", "bytes": 481980928},
 }
 
 
