@@ -399,6 +399,21 @@ __global__ void __launch_bounds__(320, 1)
         ok = mbar_wait(&bars[C::B_QFULL], uq & 1u, abort_flag, p.err);
         tc_fence_after();
         uint32_t pslot = 0;
+        // S of one head into its TMEM columns (the tensor core runs it after
+        // that head's PV, issued just before, which reads the same columns).
+        // The head loop below is written out (two heads known at compile
+        // time): with a runtime head loop the issue ran measurably behind
+        // the tensor core on long unmasked units.
+        auto issue_s = [&](int t, int slot) {
+          const uint32_t tS = tbase + (uint32_t)(t * 128);
+          const uint64_t qd = dQ0 + kTileStep * (uint64_t)t, kd = dK0 + kTileStep * (uint64_t)slot;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);
+            mma_ss(tS, qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars[C::B_SFULL + t]);
+        };
         for (int j = 0; j < n && ok; ++j) {
           const int slot = jt % S;
           ok = mbar_wait(&bars[C::B_KFULL + slot], (jt / S) & 1u, abort_flag, p.err);
@@ -407,21 +422,13 @@ __global__ void __launch_bounds__(320, 1)
             ok = mbar_wait(&bars[C::B_VFULL + pslot], ((jt - 1) / S) & 1u, abort_flag, p.err);
             tc_fence_after();
           }
-          // per head: the previous block's PV, then this block's S into the
-          // same TMEM columns (the tensor core runs them in issue order)
-          for (int t = 0; t < T && ok; ++t) {
-            if (j > 0) ok = issue_pv(t, pslot, j == 1);
-            if (!ok) break;
-            const uint32_t tS = tbase + (uint32_t)(t * 128);
-            const uint64_t qd = dQ0 + kTileStep * (uint64_t)t, kd = dK0 + kTileStep * (uint64_t)slot;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t off = (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);
-              mma_ss(tS, qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&bars[C::B_SFULL + t]);
-          }
           if (!ok) break;
+          if (j > 0 && !issue_pv(0, pslot, j == 1)) { ok = false; break; }
+          issue_s(0, slot);
+          if (T == 2) {
+            if (j > 0 && !issue_pv(1, pslot, j == 1)) { ok = false; break; }
+            issue_s(1, slot);
+          }
           if (j > 0) mma_commit(&bars[C::B_VEMPTY + pslot]);
           mma_commit(&bars[C::B_KEMPTY + slot]);
           if (j == n - 1) mma_commit(&bars[C::B_QFREE]);
