@@ -503,7 +503,7 @@ NCU_TRAFFIC = {
     "bwd": {"file": "fm_bwd.cu", "workload": "share_question32k",
             "sha256": "ddac91c410bf1b64f4ff2524b0f2b5e543b5721417247545c4d8b06ebfcf7f04", "bytes": 1269846784},
     "fwd": {"file": "fm_fwd.cu", "workload": "share_question32k",
-            "sha256": "0d491e37f2b9f9134e7cba5624df579b5ddd98c57f14067ed590bb9787f236d0", "bytes": 481980928},
+            "sha256": "7d738a7bb0e91c28335bc30e46b7d55e247964a352dfb4e38ce6fe1fc4c1dd8f", "bytes": 482761216},
 }
 
 
