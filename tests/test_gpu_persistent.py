@@ -92,3 +92,59 @@ def test_persistent_forward_unit_sequences(hq, hkv, n, d, zone):
     st, bits = fm.fm_device_status()
     assert st == fm.FM_OK, bits
     assert torch.all(dq[:, :, a:b] == 0).item()
+
+
+def test_persistent_forward_batches():
+    """Three batch entries, each with its own dead zone: units of different
+    batch entries interleave in every CTA's sequence (natural order, 1536 units)."""
+    B, hq, hkv, n, d = 3, 16, 4, 8192, 128
+    cfg = dict(B=B, H_q=hq, H_kv=hkv, N=n, d=d, causal=True)
+    scale = 1.0 / np.sqrt(d)
+    zones = [(1024, 1024 + 8 * 128), (4096, 4096 + 12 * 128), (0, 5 * 128)]
+    per = [dead_zone_vectors(n, a, b) for a, b in zones]
+    vec_np = tuple(np.concatenate([p[i] for p in per]) for i in range(4))
+    vec = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in vec_np]
+    q, k, v, do = tensors.make_qkvdo(cfg, device="cuda")
+    qs = fm.fm_classify_tiles(*vec, causal=True)
+    o, lse = fm.fm_attn_fwd(q, k, v, *vec, qs, scale=scale, causal=True)
+    st, bits = fm.fm_device_status()
+    assert st == fm.FM_OK, bits
+    rng = np.random.default_rng(11)
+    G = hq // hkv
+    for bi, (a, b) in enumerate(zones):
+        assert torch.all(o[bi, :, a:b] == 0).item()
+        assert torch.all(torch.isneginf(lse[bi, :, a:b])).item()
+        rows = np.unique(np.concatenate([rng.choice(n, size=24, replace=False), [a, b - 1, min(b, n - 1)]]))
+        trows = torch.as_tensor(rows, device="cuda")
+        h = int(rng.integers(hq))
+        g = h // G
+        O_ref, L_ref = oracle.forward(f64(q[bi:bi + 1, h:h + 1]), f64(k[bi:bi + 1, g:g + 1]), f64(v[bi:bi + 1, g:g + 1]),
+                                      tuple(x[bi:bi + 1] for x in vec_np), True, scale, rows=rows)
+        assert_out(f64(o[bi:bi + 1, h:h + 1, trows]), O_ref)
+        assert_lse(f64(lse[bi:bi + 1, h:h + 1, trows]), L_ref)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_persistent_forward_general_masks(causal):
+    """Random two-interval masks: nearly every tile partial, many units per CTA."""
+    from helpers import random_vectors
+    B, hq, hkv, n, d = 1, 32, 8, 4096, 128
+    cfg = dict(B=B, H_q=hq, H_kv=hkv, N=n, d=d, causal=causal)
+    scale = 1.0 / np.sqrt(d)
+    rng = np.random.default_rng(5)
+    vec_np = random_vectors(rng, B, n, "general")
+    vec = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in vec_np]
+    q, k, v, do = tensors.make_qkvdo(cfg, device="cuda")
+    qs = fm.fm_classify_tiles(*vec, causal=causal)
+    o, lse = fm.fm_attn_fwd(q, k, v, *vec, qs, scale=scale, causal=causal)
+    st, bits = fm.fm_device_status()
+    assert st == fm.FM_OK, bits
+    rows = np.unique(np.concatenate([rng.choice(n, size=40, replace=False), [0, n - 1]]))
+    trows = torch.as_tensor(rows, device="cuda")
+    G = hq // hkv
+    for h in (0, hq - 1):
+        g = h // G
+        O_ref, L_ref = oracle.forward(f64(q[:, h:h + 1]), f64(k[:, g:g + 1]), f64(v[:, g:g + 1]), vec_np, causal,
+                                      scale, rows=rows)
+        assert_out(f64(o[:, h:h + 1, trows]), O_ref)
+        assert_lse(f64(lse[:, h:h + 1, trows]), L_ref)
