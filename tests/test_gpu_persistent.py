@@ -139,12 +139,14 @@ def test_persistent_forward_general_masks(causal):
     o, lse = fm.fm_attn_fwd(q, k, v, *vec, qs, scale=scale, causal=causal)
     st, bits = fm.fm_device_status()
     assert st == fm.FM_OK, bits
-    rows = np.unique(np.concatenate([rng.choice(n, size=40, replace=False), [0, n - 1]]))
-    trows = torch.as_tensor(rows, device="cuda")
+    # every row of two heads: a unit's output is written by four row groups
+    # at different times, and the last unit of each CTA takes its own path
     G = hq // hkv
     for h in (0, hq - 1):
         g = h // G
         O_ref, L_ref = oracle.forward(f64(q[:, h:h + 1]), f64(k[:, g:g + 1]), f64(v[:, g:g + 1]), vec_np, causal,
-                                      scale, rows=rows)
-        assert_out(f64(o[:, h:h + 1, trows]), O_ref)
-        assert_lse(f64(lse[:, h:h + 1, trows]), L_ref)
+                                      scale)
+        og = f64(o[:, h:h + 1])
+        for q0 in range(0, n, 128):
+            assert_out(og[:, :, q0:q0 + 128], O_ref[:, :, q0:q0 + 128])
+        assert_lse(f64(lse[:, h:h + 1]), L_ref)
