@@ -1,0 +1,178 @@
+"""Pins of the chunk-balancer oracle (oracle/balance.py) against what the pages
+and the mathematics fix (FlashMask-3 project page, §3.3 "Balance the work, not
+the length", and the "IPO phase ablation" table of §4): closed forms of the
+tile cost model, hand-worked LPT / repartition cases, exhaustive optima on tiny
+instances, and the table's LPT statistic."""
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import balance as ob
+from workloads import chunks
+
+
+def brute_optimum(w, P, kappa):
+    """Smallest makespan over every owner vector with kappa chunks per rank
+    (plain product enumeration, independent of the oracle's deal order)."""
+    n = len(w)
+    best = None
+    for owner in itertools.product(range(P), repeat=n):
+        if any(owner.count(r) != kappa for r in range(P)):
+            continue
+        L = [0] * P
+        for i, r in enumerate(owner):
+            L[r] += int(w[i])
+        best = max(L) if best is None else min(best, max(L))
+    return best
+
+
+def causal_vectors(n):
+    # no interval masks (empty [N, N) and [0, 0)); causal only
+    return (np.full(n, n, np.int32), np.full(n, n, np.int32), np.zeros(n, np.int32), np.zeros(n, np.int32))
+
+
+def test_chunk_loads_causal_closed_form():
+    # Causal, N = 2048, 128 x 128 tiles: Q block qb has qb unmasked tiles left
+    # of the diagonal, one partial diagonal tile, the rest skipped. Chunks of 4
+    # blocks: partial 4, unmasked sum_{qb=4c}^{4c+3} qb = 16c + 6.
+    n = 2048
+    cls = oracle.classify_tiles(*causal_vectors(n), True, 128, 128)[None]
+    w = ob.chunk_loads(cls, 4, 13, 10)
+    assert w.tolist() == [4 * 13 + (16 * c + 6) * 10 for c in range(4)]
+
+
+def test_chunk_loads_batch_and_ragged_tail():
+    n = 1152  # 9 Q blocks: chunks of 4, 4, 1
+    cls = oracle.classify_tiles(*causal_vectors(n), True, 128, 128)
+    w1 = ob.chunk_loads(cls[None], 4, 3, 2)
+    w2 = ob.chunk_loads(np.stack([cls, cls]), 4, 3, 2)
+    assert w1.tolist() == [4 * 3 + 6 * 2, 4 * 3 + 22 * 2, 3 + 8 * 2]
+    assert (w2 == 2 * w1).all()
+    # a skip-only batch entry adds nothing
+    w3 = ob.chunk_loads(np.stack([cls, np.zeros_like(cls)]), 4, 3, 2)
+    assert (w3 == w1).all()
+
+
+def test_lower_bound_hand_values():
+    assert ob.lower_bound([5, 1, 1, 1], 2) == 5        # the largest chunk
+    assert ob.lower_bound([3, 3, 3, 3, 3, 4], 3) == 7  # ceil(19 / 3)
+    assert ob.lower_bound([2, 2, 2, 2], 2) == 4
+
+
+def test_cardinality_bound_hand_values():
+    # [5, 1, 1, 1] on two ranks of two: LB = 5, but the rank with the 5 holds
+    # one more chunk: 6, which the deal {5, 1} {1, 1} reaches
+    assert ob.lower_bound_kappa([5, 1, 1, 1], 2, 2) == 6 == brute_optimum([5, 1, 1, 1], 2, 2)
+    # one light chunk among equal ones (a sliding-window mask's chunks): every
+    # rank without the light chunk carries kappa full chunks
+    P, kappa, x, y = 4, 3, 10, 4
+    w = [y] + [x] * (P * kappa - 1)
+    assert ob.lower_bound(w, P) == -(-(P * kappa * x - (x - y)) // P) < kappa * x
+    assert ob.lower_bound_kappa(w, P, kappa) == kappa * x == brute_optimum(w, P, kappa)
+
+
+def test_cardinality_bound_is_a_lower_bound():
+    rng = np.random.default_rng(8)
+    for P, kappa in [(2, 2), (2, 3), (3, 2), (4, 2), (2, 4)]:
+        for _ in range(15):
+            w = rng.integers(0, 20, size=P * kappa).tolist()
+            opt = brute_optimum(w, P, kappa)
+            assert ob.lower_bound(w, P) <= ob.lower_bound_kappa(w, P, kappa) <= opt
+
+
+def test_lpt_then_pairwise_hand_example():
+    # w = 3 3 2 2 2 0, two ranks of three chunks. LPT: 3 -> r0, 3 -> r1,
+    # 2 -> r0 (tie, lower rank), 2 -> r1, 2 -> r0 (tie), 0 -> r1 (r0 full):
+    # loads 7 and 5. The only pair's first optimal deal gives rank 0 chunks
+    # {0, 1, 5} (3 + 3 + 0) and rank 1 {2, 3, 4}: 6 and 6 = LB.
+    w = [3, 3, 2, 2, 2, 0]
+    assert ob.lpt(w, 2, 3) == [0, 1, 0, 1, 0, 1]
+    owner, rep = ob.ipo(w, 2, 3, phases=1)
+    assert rep["makespan_lpt"] == rep["makespan"] == 7 and not rep["certified"]
+    owner, rep = ob.ipo(w, 2, 3, phases=2)
+    assert owner == [0, 0, 1, 1, 1, 0]
+    assert rep == dict(lower_bound=6, lower_bound_kappa=6, makespan_lpt=7, makespan_pair=6, makespan=6, certified=1,
+                       pair_moves=1, triple_moves=0)
+
+
+def test_lpt_respects_cardinality():
+    # one huge chunk and many small ones: without the cardinality constraint
+    # LPT would pile small chunks on the other ranks
+    w = [100, 1, 1, 1, 1, 1, 1, 1, 1]
+    owner = ob.lpt(w, 3, 3)
+    assert all(owner.count(r) == 3 for r in range(3))
+    assert owner[0] == 0
+
+
+@pytest.mark.parametrize("kappa", [2, 3, 4])
+def test_pairwise_is_exact_on_two_ranks(kappa):
+    # with two ranks the only pair holds the whole instance: the exact pairwise
+    # repartition must reach the global optimum
+    rng = np.random.default_rng(10 + kappa)
+    for _ in range(12):
+        w = rng.integers(1, 60, size=2 * kappa).tolist()
+        owner, rep = ob.ipo(w, 2, kappa, phases=2)
+        assert rep["makespan"] == brute_optimum(w, 2, kappa)
+
+
+@pytest.mark.parametrize("kappa", [2, 3])
+def test_three_rank_is_exact_on_three_ranks(kappa):
+    rng = np.random.default_rng(20 + kappa)
+    for _ in range(8):
+        w = rng.integers(1, 40, size=3 * kappa).tolist()
+        owner, rep = ob.ipo(w, 3, kappa, phases=3)
+        assert rep["makespan"] == brute_optimum(w, 3, kappa)
+
+
+def test_ipo_bounds_and_certificate():
+    rng = np.random.default_rng(3)
+    for it in range(10):
+        w = rng.integers(0, 30, size=8).tolist()
+        opt = brute_optimum(w, 4, 2)
+        for phases in (1, 2, 3):
+            owner, rep = ob.ipo(w, 4, 2, phases=phases)
+            assert all(owner.count(r) == 2 for r in range(4))
+            assert rep["lower_bound"] <= rep["lower_bound_kappa"] <= opt
+            assert opt <= rep["makespan"] <= rep["makespan_pair"] <= rep["makespan_lpt"]
+            if rep["certified"]:
+                assert rep["makespan"] == opt
+        assert ob.optimum(w, 4, 2) == opt
+
+
+def test_pairwise_fixed_point_is_pair_optimal():
+    # after the pairwise phase no pair holding a rank at the makespan can be
+    # dealt below it (checked by enumerating each pair's kappa-subsets)
+    rng = np.random.default_rng(4)
+    P, kappa = 4, 3
+    for _ in range(6):
+        w = rng.integers(1, 100, size=P * kappa).tolist()
+        owner, rep = ob.ipo(w, P, kappa, phases=2)
+        if rep["certified"]:
+            continue
+        L = ob.rank_loads(w, owner, P)
+        phi = max(L)
+        for a, b in itertools.combinations(range(P), 2):
+            if phi not in (L[a], L[b]):
+                continue
+            pool = [i for i in range(len(w)) if owner[i] in (a, b)]
+            tot = sum(w[i] for i in pool)
+            best = min(max(sum(w[i] for i in s), tot - sum(w[i] for i in s))
+                       for s in itertools.combinations(pool, kappa))
+            assert best >= phi
+
+
+def test_table_lpt_statistic_causal():
+    # The table reports LPT alone sub-optimal in 85 to 100% of instances. On the causal family
+    # (64 chunks, 8 ranks, kappa 8, w_max 200) the balancer reaches the lower
+    # bound, so LPT's excess over it is its sub-optimality
+    kind, n, P, kappa, w_max, _ = chunks.TABLE["causal"]
+    rng = np.random.default_rng(0)
+    sub = cert = 0
+    for _ in range(4):
+        w = chunks.random_loads(rng, kind, n, w_max)
+        owner, rep = ob.ipo(w, P, kappa, phases=2)
+        cert += rep["certified"]
+        sub += rep["makespan_lpt"] > rep["lower_bound_kappa"]
+    assert cert == 4 and sub >= 3

@@ -1,6 +1,7 @@
 """Seeded synthetic inputs shared by the tests, the benchmark and the oracle checks.
 
 Holds no attention arithmetic: mask encoders (`masks`), the benchmark
-workloads (`configs`) and seeded bf16 tensors (`tensors`).
+workloads (`configs`), seeded bf16 tensors (`tensors`) and chunk-load
+instances for the chunk balancer (`chunks`).
 """
-from . import configs, masks, tensors  # noqa: F401
+from . import chunks, configs, masks, tensors  # noqa: F401
