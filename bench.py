@@ -8,10 +8,14 @@ only unmasked (i, j) pairs: 4*d FLOPs each for the forward and 10*d for the
 backward, per query head.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+       python bench.py --balance
 Prints ONE JSON line on rank 0. Under torchrun every rank runs its own replica
 of the workload (weak scaling, no collective on the data path); the time is
 the max over ranks and the value the sum of all ranks' work over that time.
 --impl reference times the fp64 CPU oracle on the host cores instead.
+--balance measures the chunk balancer for context parallelism (host code):
+peak / average rank load on the workloads' own chunk loads and the ablation
+table's instance families, and its time per call.
 """
 from __future__ import annotations
 
@@ -521,6 +525,110 @@ def ncu_traffic(kind: str, workload: str):
     return ent["bytes"] if h == ent["sha256"] else None
 
 
+# ------------------------------------------------------- chunk balancer
+BAL_COSTS = (13, 10)  # partial, unmasked tile: the pages' illustrative 1.3 : 1
+BAL_WORKLOADS = ("doc8k", "share_question32k", "prefix_lm64k", "sliding_window64k", "eviction128k")
+
+
+def _rank_peak(w, owner, P):
+    return float(np.bincount(owner, weights=w, minlength=P).max())
+
+
+def _zigzag_owner(P, kappa):
+    """Chunk owners of the zigzag split (kappa = 2: the dual-chunk split):
+    pass p hands chunks p*P .. p*P + P - 1 to ranks 0..P-1, every other pass reversed."""
+    owner = np.empty(P * kappa, dtype=np.int64)
+    for p in range(kappa):
+        for r in range(P):
+            owner[p * P + (r if p % 2 == 0 else P - 1 - r)] = r
+    return owner
+
+
+def _time_call(fn, reps=5):
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        out = fn()
+        ts.append(time.perf_counter() - t0)
+    return out, 1e3 * float(np.median(ts))
+
+
+def run_balance(args):
+    import mask_aware_sparse_gb300 as fm
+    from workloads import chunks
+
+    cp, cu = BAL_COSTS
+    cases = []
+    if torch.cuda.is_available():
+        for name in BAL_WORKLOADS:
+            cfg = configs.make(name)
+            vec = [torch.from_numpy(np.ascontiguousarray(cfg[k])).cuda() for k in ("lts", "lte", "uts", "ute")]
+            qs = fm.fm_classify_tiles(*vec, causal=cfg["causal"])
+            cls = qs.tile_class.cpu().numpy()
+            nq = cls.shape[1]
+            for P in (4, 8, 16):
+                kappa = 4
+                bpc = nq // (P * kappa)
+                if bpc < 1 or nq % (P * kappa):
+                    continue
+                w = fm.fm_chunk_loads(cls, bpc, cp, cu)
+                (owner, rep), ms = _time_call(lambda: fm.fm_balance_chunks(w, P, kappa))
+                avg = float(w.sum()) / P
+                contiguous = np.repeat(np.arange(P), kappa)
+                cases.append(dict(workload=name, P=P, kappa=kappa, q_blocks_per_chunk=bpc,
+                                  peak_over_avg=dict(contiguous=_rank_peak(w, contiguous, P) / avg,
+                                                     zigzag=_rank_peak(w, _zigzag_owner(P, kappa), P) / avg,
+                                                     lpt=rep["makespan_lpt"] / avg, ipo=rep["makespan"] / avg,
+                                                     lower_bound=rep["lower_bound"] / avg,
+                                                     lower_bound_kappa=rep["lower_bound_kappa"] / avg),
+                                  certified=rep["certified"], ms_per_call=ms))
+    table = {}
+    for name, (kind, n, P, kappa, w_max, inst) in chunks.TABLE.items():
+        rng = np.random.default_rng(0)
+        cert = lsub = psub = 0
+        lgap, pgap, fgap, ms = [], [], [], []
+        for _ in range(inst):
+            w = chunks.random_loads(rng, kind, n, w_max)
+            t0 = time.perf_counter()
+            owner, rep = fm.fm_balance_chunks(w, P, kappa)
+            ms.append(1e3 * (time.perf_counter() - t0))
+            lb = rep["lower_bound_kappa"]
+            fgap.append((rep["makespan"] - lb) / lb)
+            if rep["certified"]:
+                cert += 1
+                lsub += rep["makespan_lpt"] > lb
+                psub += rep["makespan_pair"] > lb
+                lgap.append((rep["makespan_lpt"] - lb) / lb)
+                pgap.append((rep["makespan_pair"] - lb) / lb)
+        pct = lambda a: round(100.0 * a / max(cert, 1), 1)  # noqa: E731
+        table[name] = dict(n=n, P=P, kappa=kappa, w_max=w_max, instances=inst, lb_certified=cert,
+                           lpt_subopt_pct_of_certified=pct(lsub), lpt_gap_pct=round(100 * float(np.mean(lgap or [0])), 3),
+                           pair_subopt_pct_of_certified=pct(psub),
+                           pair_gap_pct=round(100 * float(np.mean(pgap or [0])), 3),
+                           final_gap_to_lb_pct=round(100 * float(np.mean(fgap)), 4),
+                           ms_per_call_median=round(float(np.median(ms)), 3), ms_per_call_max=round(max(ms), 3))
+    ipo = [c["peak_over_avg"]["ipo"] for c in cases]
+    line = {"metric": "chunk balancer: peak / average rank load (CP split of the query axis)",
+            "value": float(np.exp(np.mean(np.log(ipo)))) if ipo else None, "unit": "ratio",
+            "higher_is_better": False, "dtype": "int64", "data": "synthetic",
+            "config": {"workload": "workloads' chunk loads (tile costs partial 13, unmasked 10) + ablation table "
+                                   "families", "kappa": 4, "P": [4, 8, 16]},
+            "cases": cases, "table": table}
+    if not args.no_cpu_baseline:
+        from oracle import balance as ob  # the CPU baseline leg: the oracle, as it stands
+        kind, n, P, kappa, w_max, _ = chunks.TABLE["causal"]
+        rng = np.random.default_rng(0)
+        ws = [chunks.random_loads(rng, kind, n, w_max) for _ in range(3)]
+        t0 = time.perf_counter()
+        for w in ws:
+            ob.ipo(w, P, kappa, phases=2)
+        dt = (time.perf_counter() - t0) / len(ws)
+        line["cpu_baseline"] = {"value": 1e3 * dt, "unit": "ms per call", "cores": 1, "kind": "oracle",
+                                "sample": "3 causal-family instances (64 chunks, 8 ranks, kappa 8), LPT + pairwise"}
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -529,7 +637,10 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=configs.NAMES)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--balance", action="store_true", help="measure the chunk balancer instead")
     args = ap.parse_args()
+    if args.balance:
+        return run_balance(args)
     if args.warmup < 3:
         args.warmup = 3
     cfg = configs.make(args.workload)

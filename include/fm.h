@@ -192,6 +192,56 @@ fm_status fm_localize(const int32_t* x_global, int64_t n, const int32_t* chunk_o
                       int32_t* x_local, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Sparsity-aware chunk balancing for context parallelism (FlashMask-3 project
+ * page, §3.3 "Balance the work, not the length"). HOST functions: every
+ * pointer in this section is a host pointer, nothing touches a GPU, and the
+ * calls are synchronous and thread-safe (no shared state).
+ *
+ * The query axis of a problem is cut into chunks of blocks_per_chunk Q blocks;
+ * with n = P * kappa chunks, each of P ranks receives exactly kappa of them.
+ *
+ * fm_chunk_loads: the tile cost model {0, alpha_p, alpha_u}. tile_class is the
+ *   (B, nQ, nK) uint8 output of fm_classify_tiles copied to the host; a tile
+ *   of class 1 (partial) costs cost_partial, class 2 (unmasked) costs
+ *   cost_unmasked, anything else 0. Chunk c holds Q blocks
+ *   [c * blocks_per_chunk, (c + 1) * blocks_per_chunk) of every batch entry
+ *   (the last chunk may be short); w[c] (ceil(nQ / blocks_per_chunk) int64
+ *   outputs) is the sum of its tiles' costs. Costs must be >= 0.
+ *
+ * fm_balance_chunks: Stage 1 of HCC-IPO on loads w[0..n_chunks): LPT under the
+ *   cardinality constraint, then exact pairwise repartition (phases >= 2),
+ *   then exact three-rank repartition (phases == 3); owner[i] (n_chunks int32
+ *   outputs) is the rank of chunk i. The pages' lower bound LB =
+ *   max(ceil(sum w / P), max w) and a stronger one that also uses the
+ *   cardinality constraint, LB_kappa >= LB (a pigeonhole bound, defined in
+ *   csrc/fm_balance.cpp), certify the result optimal when the makespan
+ *   reaches LB_kappa; every phase stops there. Exact
+ *   rules (tie-breaking, the order groups are visited in): the header of
+ *   csrc/fm_balance.cpp. node_budget caps the branch-and-bound nodes of one
+ *   group's repartition (<= 0: 4,000,000); a group whose search exceeds it is
+ *   left unchanged and report->budget_exhausted is set. Requires
+ *   n_chunks == P * kappa, w[i] >= 0, 2 * kappa <= 64 when the pairwise phase
+ *   runs and 3 * kappa <= 64 when the three-rank phase runs
+ *   (FM_ERR_UNSUPPORTED otherwise). report may be NULL.
+ * ------------------------------------------------------------------------- */
+typedef struct fm_balance_report {
+  int64_t lower_bound;   /* LB = max(ceil(sum w / P), max w) */
+  int64_t lower_bound_kappa; /* LB_kappa >= LB, which also uses kappa chunks per rank */
+  int64_t makespan_lpt;  /* max rank load after LPT */
+  int64_t makespan_pair; /* after the pairwise phase (= makespan_lpt when it does not run) */
+  int64_t makespan;      /* final max rank load */
+  int32_t certified;     /* makespan == lower_bound_kappa: the assignment is optimal */
+  int32_t pair_moves;    /* pairwise repartitions applied */
+  int32_t triple_moves;  /* three-rank repartitions applied */
+  int32_t budget_exhausted;
+} fm_balance_report;
+
+fm_status fm_chunk_loads(const uint8_t* tile_class, int32_t B, int32_t nQ, int32_t nK, int32_t blocks_per_chunk,
+                         int64_t cost_partial, int64_t cost_unmasked, int64_t* w);
+fm_status fm_balance_chunks(const int64_t* w, int32_t n_chunks, int32_t P, int32_t kappa, int32_t phases,
+                            int64_t node_budget, int32_t* owner, fm_balance_report* report);
+
+/* ---------------------------------------------------------------------------
  * Device error word. Synchronizes `stream`, returns the accumulated FM_DEVERR_*
  * bits in *bits (may be NULL) and clears them. Status: FM_OK when no bit is
  * set, FM_ERR_TIMEOUT when FM_DEVERR_TIMEOUT is set, else FM_ERR_DEVICE.

@@ -9,7 +9,8 @@ is no silent fallback.
 Functions carry the names of the C entry points:
   fm_classify_tiles, fm_attn_fwd, fm_attn_bwd, fm_localize, fm_device_status,
   fm_selftest_wait_timeout, fm_profile_enable, fm_profile_read, fm_launch_count,
-  plus flashmask_attention (autograd wrapper: the
+  fm_chunk_loads, fm_balance_chunks (host code: the chunk balancer for context
+  parallelism), plus flashmask_attention (autograd wrapper: the
 classification, forward and backward calls in one differentiable op).
 """
 from __future__ import annotations
@@ -18,6 +19,7 @@ import ctypes
 import os
 from dataclasses import dataclass
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,6 +36,13 @@ class fm_problem(ctypes.Structure):
 
 class fm_tiling(ctypes.Structure):
     _fields_ = [("block_m", ctypes.c_int32), ("block_n", ctypes.c_int32)]
+
+
+class fm_balance_report(ctypes.Structure):
+    _fields_ = [("lower_bound", ctypes.c_int64), ("lower_bound_kappa", ctypes.c_int64),
+                ("makespan_lpt", ctypes.c_int64), ("makespan_pair", ctypes.c_int64),
+                ("makespan", ctypes.c_int64), ("certified", ctypes.c_int32), ("pair_moves", ctypes.c_int32),
+                ("triple_moves", ctypes.c_int32), ("budget_exhausted", ctypes.c_int32)]
 
 
 class FMError(RuntimeError):
@@ -66,6 +75,10 @@ _SIGS = {
     "fm_profile_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32),
                                        ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)]),
     "fm_launch_count": (ctypes.c_int64, []),
+    "fm_chunk_loads": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int64, ctypes.c_int64, _P]),
+    "fm_balance_chunks": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int64, _P, ctypes.POINTER(fm_balance_report)]),
 }
 EXPORTS = tuple(_SIGS)
 
@@ -237,6 +250,40 @@ def fm_profile_read():
 
 def fm_launch_count() -> int:
     return int(lib().fm_launch_count())
+
+
+def _host_array(x, dtype):
+    """A contiguous host numpy array of `dtype` holding x (numpy array or torch tensor, any device)."""
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().numpy()
+    a = np.ascontiguousarray(x)
+    if a.dtype != dtype:
+        raise ValueError(f"expected {np.dtype(dtype).name} values, got {a.dtype}")
+    return a
+
+
+def fm_chunk_loads(tile_class, blocks_per_chunk: int, cost_partial: int, cost_unmasked: int) -> np.ndarray:
+    """Per-chunk loads (int64) from the (B, nQ, nK) tile classes (copied to the host if on a GPU)."""
+    cls = _host_array(tile_class, np.uint8)
+    if cls.ndim != 3:
+        raise ValueError("tile_class must be (B, nQ, nK)")
+    B, nq, nk = cls.shape
+    w = np.empty(-(-nq // int(blocks_per_chunk)) if blocks_per_chunk > 0 else 0, dtype=np.int64)
+    _check(lib().fm_chunk_loads(ctypes.c_void_p(cls.ctypes.data), B, nq, nk, int(blocks_per_chunk),
+                                int(cost_partial), int(cost_unmasked), ctypes.c_void_p(w.ctypes.data)),
+           "fm_chunk_loads")
+    return w
+
+
+def fm_balance_chunks(w, P: int, kappa: int, phases: int = 3, node_budget: int = 0):
+    """HCC-IPO Stage 1 on chunk loads w: returns (owner int32 array, report dict)."""
+    wa = _host_array(w, np.int64)
+    owner = np.empty(wa.size, dtype=np.int32)
+    rep = fm_balance_report()
+    _check(lib().fm_balance_chunks(ctypes.c_void_p(wa.ctypes.data), int(wa.size), int(P), int(kappa), int(phases),
+                                   int(node_budget), ctypes.c_void_p(owner.ctypes.data), ctypes.byref(rep)),
+           "fm_balance_chunks")
+    return owner, {name: int(getattr(rep, name)) for name, _ in fm_balance_report._fields_}
 
 
 class _FlashMaskFn(torch.autograd.Function):

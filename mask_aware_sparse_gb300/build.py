@@ -1,7 +1,8 @@
 """Build libfm.so (the CUDA library behind include/fm.h) in-tree with nvcc.
 
-Every .cu under csrc/ is compiled in parallel for sm_103a only, then linked
-into mask_aware_sparse_gb300/libfm.so. No CMake, no torch extension machinery.
+Every .cu under csrc/ is compiled in parallel for sm_103a only (the .cpp
+files, host code, with the same driver), then linked into
+mask_aware_sparse_gb300/libfm.so. No CMake, no torch extension machinery.
 """
 from __future__ import annotations
 
@@ -39,14 +40,14 @@ def _stale(lib: str, srcs) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     if not force and not _stale(LIB, srcs):
         return LIB
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
