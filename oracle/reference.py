@@ -26,7 +26,10 @@ Readings where the pages are silent (all pinned by tests/test_oracle.py):
     gradient; LSE is the natural log of sum_j exp(scale * q_i . k_j) over
     visible j;
   - GQA groups are contiguous: query head h uses kv head h // (H_q / H_kv);
-  - the vectors are (B, N) and shared by every head.
+  - the vectors are (B, N_kv), one entry per key column, shared by every head;
+    the query rows may number N != N_kv (one rank of a context-parallel split:
+    its own rows against every key, FlashMask-3 project page, §3.2), with
+    causal comparing the problem's own row and key indices.
 
 Precision: every input is widened to float64; all arithmetic is float64.
 """
@@ -60,10 +63,11 @@ def dense_mask(lts, lte, uts, ute, causal: bool) -> np.ndarray:
     return masked_rows(lts, lte, uts, ute, causal, np.arange(lts.shape[0]))
 
 
-def masked_cols(lts, lte, uts, ute, causal: bool, cols) -> np.ndarray:
-    """Columns of the dense mask, shape (N, len(cols)): True where masked."""
+def masked_cols(lts, lte, uts, ute, causal: bool, cols, n_rows=None) -> np.ndarray:
+    """Columns of the dense mask, shape (n_rows, len(cols)): True where masked
+    (n_rows defaults to the number of key columns)."""
     cols = np.asarray(cols, dtype=np.int64)
-    n = lts.shape[0]
+    n = lts.shape[0] if n_rows is None else int(n_rows)
     i = np.arange(n, dtype=np.int64)[:, None]
     j = cols[None, :]
     lower = (lts[cols].astype(np.int64)[None, :] <= i) & (i < lte[cols].astype(np.int64)[None, :])
@@ -88,8 +92,9 @@ def block_minmax(vec, bn: int):
     return mins, maxs
 
 
-def classify_tiles(lts, lte, uts, ute, causal: bool, bm: int, bn: int) -> np.ndarray:
-    """Class of every (Q-block, KV-block) tile of one batch entry: (nQ, nK) uint8.
+def classify_tiles(lts, lte, uts, ute, causal: bool, bm: int, bn: int, n_rows=None) -> np.ndarray:
+    """Class of every (Q-block, KV-block) tile of one batch entry: (nQ, nK) uint8
+    (n_rows query rows, default: as many as key columns).
 
     Tile rows [q0, q1), columns [k0, k1) (the last block of each axis may be
     short). With block min/max of the four vectors:
@@ -105,14 +110,15 @@ def classify_tiles(lts, lte, uts, ute, causal: bool, bm: int, bn: int) -> np.nda
     q0 >= max UTE) plus the causal term.
     """
     n = lts.shape[0]
-    nq, nk = -(-n // bm), -(-n // bn)
+    nr = n if n_rows is None else int(n_rows)
+    nq, nk = -(-nr // bm), -(-n // bn)
     mn_lts, mx_lts = block_minmax(lts, bn)
     mn_lte, mx_lte = block_minmax(lte, bn)
     mn_uts, mx_uts = block_minmax(uts, bn)
     mn_ute, mx_ute = block_minmax(ute, bn)
     cls = np.empty((nq, nk), dtype=np.uint8)
     for qb in range(nq):
-        q0, q1 = qb * bm, min((qb + 1) * bm, n)
+        q0, q1 = qb * bm, min((qb + 1) * bm, nr)
         for kb in range(nk):
             k0, k1 = kb * bn, min((kb + 1) * bn, n)
             skip = (
@@ -170,7 +176,7 @@ def row_probs(q, k, vec, causal, scale, b, h, rows):
 
     S = scale * q_i . k_j over all N keys, masked entries set to -inf, then
     P = exp(S - max) / sum. A fully-masked row gets P = 0 and LSE = -inf.
-    q: (B, Hq, N, d), k: (B, Hkv, N, d), float64.
+    q: (B, Hq, N, d), k: (B, Hkv, N_kv, d), float64.
     """
     lts, lte, uts, ute = (x[b] for x in vec)
     g = _kv_head(h, q.shape[1], k.shape[1])
@@ -224,14 +230,14 @@ def backward(q, k, v, do, vec, causal: bool, scale: float, heads=None, rows=None
     Hkv = k.shape[1]
     heads = list(range(Hq)) if heads is None else list(heads)
     rows = np.arange(N) if rows is None else np.asarray(rows)
-    cols = np.arange(N) if cols is None else np.asarray(cols)
+    cols = np.arange(k.shape[2]) if cols is None else np.asarray(cols)
     dQ = np.zeros((B, len(heads), len(rows), d))
     dK = np.zeros((B, Hkv, len(cols), d))
     dV = np.zeros((B, Hkv, len(cols), d))
     for b in range(B):
         lts, lte, uts, ute = (x[b] for x in vec)
         # rows that see at least one selected column: only they feed dK/dV there
-        mc = masked_cols(lts, lte, uts, ute, causal, cols)
+        mc = masked_cols(lts, lte, uts, ute, causal, cols, n_rows=N)
         feed_rows = np.nonzero(~mc.all(axis=1))[0]
         need = np.union1d(rows, feed_rows)
         row_pos = {int(r): t for t, r in enumerate(rows)}
