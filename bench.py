@@ -505,9 +505,9 @@ def run_ours(args, cfg):
 # the counters were taken from.
 NCU_TRAFFIC = {
     "bwd": {"file": "fm_bwd.cu", "workload": "share_question32k",
-            "sha256": "ddac91c410bf1b64f4ff2524b0f2b5e543b5721417247545c4d8b06ebfcf7f04", "bytes": 1269846784},
+            "sha256": "32cce9b8470330696795da8c94b76d79631891d97b238005bc623937716d6df3", "bytes": 1264590336},
     "fwd": {"file": "fm_fwd.cu", "workload": "share_question32k",
-            "sha256": "7d738a7bb0e91c28335bc30e46b7d55e247964a352dfb4e38ce6fe1fc4c1dd8f", "bytes": 482761216},
+            "sha256": "017b14501532a86517f02dab2e88b636e156ea33593b1eabc929fa2ca0c607aa", "bytes": 482228480},
 }
 
 

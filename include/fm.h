@@ -13,9 +13,10 @@
  *     Every compute entry point only enqueues work on that stream and returns;
  *     it never synchronizes, except fm_device_status.
  *   - Layouts: Q, O, dO, dQ are contiguous (B, H_q, N, d) bf16; K, V, dK, dV are
- *     contiguous (B, H_kv, N, d) bf16; LSE is (B, H_q, N) fp32; the four mask
- *     vectors are (B, N) int32, shared by every head. Tensor base addresses must
- *     be 16-byte aligned.
+ *     contiguous (B, H_kv, N_kv, d) bf16 (N_kv = N unless fm_problem says
+ *     otherwise); LSE is (B, H_q, N) fp32; the four mask vectors are (B, N_kv)
+ *     int32, one entry per key column, shared by every head, holding query-row
+ *     boundaries in [0, N]. Tensor base addresses must be 16-byte aligned.
  *   - GQA: query head h reads kv head h / (H_q / H_kv) (contiguous groups).
  *   - Errors: arguments are validated on the host and a bad call returns an
  *     error status without launching anything. Problems found on the device
@@ -32,7 +33,7 @@
 extern "C" {
 #endif
 
-#define FM_ABI_VERSION 1
+#define FM_ABI_VERSION 2
 
 typedef enum fm_status {
   FM_OK = 0,
@@ -49,11 +50,18 @@ typedef enum fm_status {
 #define FM_DEVERR_RANGE 2
 #define FM_DEVERR_QUEUE 4
 
-/* Problem shape. scale multiplies q.k (usually 1/sqrt(d)); causal != 0 adds i < j. */
+/* Problem shape. N query rows against N_kv key / value rows; N_kv = 0 means
+ * N_kv = N (the square problem). A rectangular problem is what one rank of a
+ * context-parallel split computes: its own query rows against every key, with
+ * the mask vectors localized to its rows (fm_localize). scale multiplies q.k
+ * (usually 1/sqrt(d)); causal != 0 adds i < j with i and j counted in the
+ * problem's own rows and keys (a split that needs the global diagonal folds it
+ * into the vectors instead: UTS_j = 0, UTE_j = j before localizing). */
 typedef struct fm_problem {
   int32_t B, H_q, H_kv, N, d;
   float scale;
   int32_t causal;
+  int32_t N_kv;
 } fm_problem;
 
 /* Tile geometry for classification: block_m query rows x block_n key columns.
@@ -72,7 +80,7 @@ const char* fm_status_string(fm_status s);
 /* The tiling the attention kernels were built for (128 x 128). */
 fm_status fm_attn_tiling(fm_tiling* out);
 
-/* Number of Q blocks ceil(N / block_m) and KV blocks ceil(N / block_n). */
+/* Number of Q blocks ceil(N / block_m) and KV blocks ceil(N_kv / block_n). */
 fm_status fm_tile_counts(const fm_problem* p, const fm_tiling* t, int32_t* n_qblocks, int32_t* n_kblocks);
 
 /* ---------------------------------------------------------------------------
@@ -83,8 +91,8 @@ fm_status fm_tile_counts(const fm_problem* p, const fm_tiling* t, int32_t* n_qbl
  * tile as fully-masked (skipped), partial (masked element-wise) or unmasked,
  * and each Q block gets a queue of its valid KV blocks tagged partial or
  * unmasked, visited right to left. The rule, for tile rows [q0, q1) and key
- * columns [k0, k1) (the last block of an axis may be short when N is not a
- * multiple of the tile):
+ * columns [k0, k1) (the last block of an axis may be short when N or N_kv is
+ * not a multiple of the tile):
  *   skip     iff (q0 >= max LTS and q1 <= min LTE) or (q0 >= max UTS and q1 <= min UTE)
  *                or (causal and q1 <= k0)
  *   unmasked iff (q1 <= min LTS or q0 >= max LTE) and (q1 <= min UTS or q0 >= max UTE)
@@ -100,7 +108,7 @@ fm_status fm_tile_counts(const fm_problem* p, const fm_tiling* t, int32_t* n_qbl
  *   k_off       B*nK + 1 int32; k_queue capacity B*nQ*nK int32: for each (b, kb),
  *               the non-skipped Q blocks in ASCENDING qb order, entry =
  *               (qb << 1) | is_partial (the backward pass walks these).
- * Mask values outside [0, N] are clamped for classification and flagged
+ * Mask values outside [0, N] (N = query rows) are clamped for classification and flagged
  * (FM_DEVERR_RANGE). Workspace: fm_classify_workspace_bytes.
  * ------------------------------------------------------------------------- */
 size_t fm_classify_workspace_bytes(const fm_problem* p, const fm_tiling* t);

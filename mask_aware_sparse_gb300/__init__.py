@@ -31,7 +31,7 @@ FM_DEVERR_TIMEOUT, FM_DEVERR_RANGE, FM_DEVERR_QUEUE = 1, 2, 4
 
 class fm_problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32), ("N", ctypes.c_int32),
-                ("d", ctypes.c_int32), ("scale", ctypes.c_float), ("causal", ctypes.c_int32)]
+                ("d", ctypes.c_int32), ("scale", ctypes.c_float), ("causal", ctypes.c_int32), ("N_kv", ctypes.c_int32)]
 
 
 class fm_tiling(ctypes.Structure):
@@ -119,14 +119,14 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _problem(B, H_q, H_kv, N, d, scale, causal) -> fm_problem:
-    return fm_problem(int(B), int(H_q), int(H_kv), int(N), int(d), float(scale), 1 if causal else 0)
+def _problem(B, H_q, H_kv, N, d, scale, causal, N_kv=0) -> fm_problem:
+    return fm_problem(int(B), int(H_q), int(H_kv), int(N), int(d), float(scale), 1 if causal else 0, int(N_kv))
 
 
 def _vec_ok(*vs):
     for v in vs:
         if v.dtype != torch.int32 or not v.is_contiguous() or not v.is_cuda:
-            raise ValueError("mask vectors must be contiguous int32 CUDA tensors of shape (B, N)")
+            raise ValueError("mask vectors must be contiguous int32 CUDA tensors of shape (B, N_kv)")
 
 
 def _bf16_ok(*ts):
@@ -153,11 +153,16 @@ class TileQueues:
     block_n: int
 
 
-def fm_classify_tiles(lts, lte, uts, ute, *, causal: bool, block_m: int = 128, block_n: int = 128, stream=None):
-    """Classify every (Q-block, KV-block) tile and build both compacted queues."""
+def fm_classify_tiles(lts, lte, uts, ute, *, causal: bool, block_m: int = 128, block_n: int = 128, n_rows=None,
+                      stream=None):
+    """Classify every (Q-block, KV-block) tile and build both compacted queues.
+
+    The vectors are (B, N_kv); n_rows is the number of query rows N (default
+    N_kv: the square problem)."""
     _vec_ok(lts, lte, uts, ute)
-    B, N = lts.shape
-    prob = _problem(B, 1, 1, N, 128, 1.0, causal)
+    B, Nk = lts.shape
+    N = Nk if n_rows is None else int(n_rows)
+    prob = _problem(B, 1, 1, N, 128, 1.0, causal, Nk)
     til = fm_tiling(block_m, block_n)
     nq, nk = ctypes.c_int32(), ctypes.c_int32()
     _check(lib().fm_tile_counts(ctypes.byref(prob), ctypes.byref(til), ctypes.byref(nq), ctypes.byref(nk)),
@@ -180,11 +185,11 @@ def fm_classify_tiles(lts, lte, uts, ute, *, causal: bool, block_m: int = 128, b
 
 def fm_attn_fwd(q, k, v, lts, lte, uts, ute, queues: TileQueues, *, scale: float, causal: bool, o=None, lse=None,
                 ws=None, stream=None):
-    """Forward: returns (O bf16 (B,H_q,N,d), LSE fp32 (B,H_q,N))."""
+    """Forward: returns (O bf16 (B,H_q,N,d), LSE fp32 (B,H_q,N)); K, V may hold N_kv != N rows."""
     _bf16_ok(q, k, v)
     _vec_ok(lts, lte, uts, ute)
     B, Hq, N, d = q.shape
-    prob = _problem(B, Hq, k.shape[1], N, d, scale, causal)
+    prob = _problem(B, Hq, k.shape[1], N, d, scale, causal, k.shape[2])
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if lse is None else lse
     wsb = lib().fm_attn_fwd_workspace_bytes(ctypes.byref(prob))
@@ -202,7 +207,7 @@ def fm_attn_bwd(q, k, v, o, lse, do, lts, lte, uts, ute, queues: TileQueues, *, 
     _bf16_ok(q, k, v, o, do)
     _vec_ok(lts, lte, uts, ute)
     B, Hq, N, d = q.shape
-    prob = _problem(B, Hq, k.shape[1], N, d, scale, causal)
+    prob = _problem(B, Hq, k.shape[1], N, d, scale, causal, k.shape[2])
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -290,7 +295,7 @@ class _FlashMaskFn(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, lts, lte, uts, ute, scale, causal):
         bm, bn = attn_tiling()
-        queues = fm_classify_tiles(lts, lte, uts, ute, causal=causal, block_m=bm, block_n=bn)
+        queues = fm_classify_tiles(lts, lte, uts, ute, causal=causal, block_m=bm, block_n=bn, n_rows=q.shape[2])
         o, lse = fm_attn_fwd(q, k, v, lts, lte, uts, ute, queues, scale=scale, causal=causal)
         ctx.save_for_backward(q, k, v, o, lse, lts, lte, uts, ute)
         ctx.queues, ctx.scale, ctx.causal = queues, scale, causal

@@ -152,13 +152,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 // is nothing to compute (B, H_q or N is zero).
 fm_status check_problem(const fm_problem* p, bool* empty) {
   if (!p) return FM_ERR_INVALID_ARG;
-  if (p->B < 0 || p->H_q < 0 || p->H_kv < 0 || p->N < 0 || p->d <= 0) return FM_ERR_INVALID_ARG;
+  if (p->B < 0 || p->H_q < 0 || p->H_kv < 0 || p->N < 0 || p->N_kv < 0 || p->d <= 0) return FM_ERR_INVALID_ARG;
   if (!std::isfinite(p->scale)) return FM_ERR_INVALID_ARG;
   *empty = (p->B == 0 || p->H_q == 0 || p->N == 0);
   if (*empty) return FM_OK;
   if (p->H_kv == 0 || p->H_q % p->H_kv != 0) return FM_ERR_INVALID_ARG;
   // int32 indexing limits of the kernels: rows of one head and heads per batch
-  if ((int64_t)p->B * p->H_q > (1 << 30) || (int64_t)p->N > (1 << 30)) return FM_ERR_UNSUPPORTED;
+  if ((int64_t)p->B * p->H_q > (1 << 30) || (int64_t)p->N > (1 << 30) || (int64_t)p->N_kv > (1 << 30))
+    return FM_ERR_UNSUPPORTED;
   return FM_OK;
 }
 
@@ -201,7 +202,7 @@ fm_status fm_tile_counts(const fm_problem* p, const fm_tiling* t, int32_t* nq, i
   if (st != FM_OK) return st;
   if (!t || !valid_tile(t->block_m) || !valid_tile(t->block_n) || !nq || !nk) return FM_ERR_INVALID_ARG;
   *nq = (p->N + t->block_m - 1) / t->block_m;
-  *nk = (p->N + t->block_n - 1) / t->block_n;
+  *nk = (kv_rows(*p) + t->block_n - 1) / t->block_n;
   return FM_OK;
 }
 

@@ -108,7 +108,7 @@ struct BwdParams {
   float* dq_acc;      // (B*H_q, N, d) fp32
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  int B, H_q, H_kv, N, Npad, nK, G, causal;
+  int B, H_q, H_kv, N, Nk, Npad, nK, G, causal;  // N query rows (Npad rounded up to the tile), Nk key rows
   float scale, scale_log2;
   int* err;
 };
@@ -156,15 +156,15 @@ __global__ void __launch_bounds__(480, 1)
   const int L = p.k_off[bk + 1] - kbeg;
   const int U = 2 * L * p.G;
   const int k0 = kb * 128;
-  const bool force_part = (kb == nK - 1) && (p.N & 127);
+  const bool force_part = (kb == nK - 1) && (p.Nk & 127);
 
   if (U <= 0) {
     // No query row sees this KV block: dK = dV = 0.
     if (L < 0 && threadIdx.x == 0) record_error(p.err, FM_DEV_ERR_QUEUE);
     if (warp < 4) {
       const int j = k0 + (warp << 5) + lane;
-      if (j < p.N) {
-        const size_t row = ((size_t)b * p.H_kv + g) * p.N + j;
+      if (j < p.Nk) {
+        const size_t row = ((size_t)b * p.H_kv + g) * p.Nk + j;
         uint4* a = reinterpret_cast<uint4*>(p.dk + row * D);
         uint4* c = reinterpret_cast<uint4*>(p.dv + row * D);
 #pragma unroll
@@ -378,9 +378,9 @@ __global__ void __launch_bounds__(480, 1)
     const int kcol = k0 + j;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     int lo0 = 0, lo1 = 0, up0 = 0, up1 = 0;
-    const bool dead = kcol >= p.N;
+    const bool dead = kcol >= p.Nk;
     if (!dead) {
-      const size_t vi = (size_t)b * p.N + kcol;
+      const size_t vi = (size_t)b * p.Nk + kcol;
       int a0 = p.lts[vi], a1 = p.lte[vi], u0 = p.uts[vi], u1 = p.ute[vi];
       if ((a0 | a1 | u0 | u1) < 0 || a0 > p.N || a1 > p.N || u0 > p.N || u1 > p.N) record_error(p.err, FM_DEV_ERR_RANGE);
       a0 = min(max(a0, 0), p.N);
@@ -683,8 +683,7 @@ struct BwdWs {
 };
 
 BwdWs carve(const fm_problem& P, void* ws) {
-  const size_t nK = (size_t)(P.N + kTile - 1) / kTile;
-  const size_t Npad = nK * kTile;
+  const size_t Npad = (size_t)(P.N + kTile - 1) / kTile * kTile;
   const size_t BH = (size_t)P.B * P.H_q;
   uint8_t* w = static_cast<uint8_t*>(ws);
   BwdWs r;
@@ -723,10 +722,10 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   // 3. main kernel
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if (!make_tmap_bhnd(&tq, q, BH, P.N, D, 64) || !make_tmap_bhnd(&tdo, dout, BH, P.N, D, 64) ||
-      !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, P.N, D, 128) ||
-      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, P.N, D, 128) ||
-      !make_tmap_bhnd(&tdk, prm0.dk, (int64_t)P.B * P.H_kv, P.N, D, 128) ||
-      !make_tmap_bhnd(&tdv, prm0.dv, (int64_t)P.B * P.H_kv, P.N, D, 128))
+      !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, prm0.Nk, D, 128) ||
+      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, prm0.Nk, D, 128) ||
+      !make_tmap_bhnd(&tdk, prm0.dk, (int64_t)P.B * P.H_kv, prm0.Nk, D, 128) ||
+      !make_tmap_bhnd(&tdv, prm0.dv, (int64_t)P.B * P.H_kv, prm0.Nk, D, 128))
     return cudaErrorInvalidValue;
   CUtensorMap tdq;
   if (!make_tmap_f32_bhnd(&tdq, w.dq_acc, BH, P.N, D, 32, 32))
@@ -757,8 +756,8 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
 }  // namespace
 
 size_t bwd_ws_bytes(const fm_problem& P) {
-  const size_t nK = (size_t)(P.N + kTile - 1) / kTile;
-  const size_t Npad = nK * kTile;
+  const size_t nK = (size_t)(kv_rows(P) + kTile - 1) / kTile;
+  const size_t Npad = (size_t)(P.N + kTile - 1) / kTile * kTile;
   const size_t BH = (size_t)P.B * P.H_q;
   return a256(BH * P.N * P.d * 4) + 2 * a256(BH * Npad * 4) + a256(4 * (size_t)P.B * nK);
 }
@@ -767,7 +766,8 @@ cudaError_t launch_bwd(const fm_problem& P, const void* q, const void* k, const 
                        const float* lse, const void* dout, const int32_t* lts, const int32_t* lte,
                        const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
                        void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err) {
-  const int nK = (P.N + kTile - 1) / kTile;
+  const int Nk = kv_rows(P);
+  const int nK = (Nk + kTile - 1) / kTile;
   const long long grid = (long long)P.B * nK * P.H_kv;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
   const BwdWs w = carve(P, ws);
@@ -788,7 +788,8 @@ cudaError_t launch_bwd(const fm_problem& P, const void* q, const void* k, const 
   prm.H_q = P.H_q;
   prm.H_kv = P.H_kv;
   prm.N = P.N;
-  prm.Npad = nK * kTile;
+  prm.Nk = Nk;
+  prm.Npad = (P.N + kTile - 1) / kTile * kTile;
   prm.nK = nK;
   prm.G = P.H_q / P.H_kv;
   prm.causal = P.causal ? 1 : 0;

@@ -33,17 +33,18 @@ __device__ __forceinline__ int clamp_flag(int x, int n, bool& bad) {
   return x;
 }
 
+// N: query rows (the range of the values); Nk: key columns (the vectors' length)
 __global__ void block_minmax_kernel(const int32_t* __restrict__ lts, const int32_t* __restrict__ lte,
                                     const int32_t* __restrict__ uts, const int32_t* __restrict__ ute, int B, int N,
-                                    int bn, int nK, Minmax* __restrict__ out, int32_t* __restrict__ col_cnt,
+                                    int Nk, int bn, int nK, Minmax* __restrict__ out, int32_t* __restrict__ col_cnt,
                                     int* err) {
   const int wpb = blockDim.x >> 5;
   const long long gw = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
   if (gw >= (long long)B * nK) return;
   const int lane = threadIdx.x & 31;
   const int b = (int)(gw / nK), kb = (int)(gw % nK);
-  const int k0 = kb * bn, k1 = min(k0 + bn, N);
-  const size_t base = (size_t)b * N;
+  const int k0 = kb * bn, k1 = min(k0 + bn, Nk);
+  const size_t base = (size_t)b * Nk;
   int mn[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX}, mx[4] = {INT_MIN, INT_MIN, INT_MIN, INT_MIN};
   bool bad = false;
   for (int j = k0 + lane; j < k1; j += 32) {
@@ -76,7 +77,8 @@ __device__ __forceinline__ uint8_t tile_class(const Minmax& m, int q0, int q1, i
   return unm ? 2 : 1;
 }
 
-__global__ void classify_rows_kernel(const Minmax* __restrict__ mm, int N, int bm, int bn, int nQ, int nK, int causal,
+__global__ void classify_rows_kernel(const Minmax* __restrict__ mm, int N, int Nk, int bm, int bn, int nQ, int nK,
+                                     int causal,
                                      uint8_t* __restrict__ cls, int32_t* __restrict__ row_cnt,
                                      int32_t* __restrict__ col_cnt) {
   const int b = blockIdx.y, qb = blockIdx.x;
@@ -84,7 +86,7 @@ __global__ void classify_rows_kernel(const Minmax* __restrict__ mm, int N, int b
   int cnt = 0;
   uint8_t* crow = cls + ((size_t)b * nQ + qb) * nK;
   for (int kb = threadIdx.x; kb < nK; kb += blockDim.x) {
-    const int k0 = kb * bn, k1 = min(k0 + bn, N);
+    const int k0 = kb * bn, k1 = min(k0 + bn, Nk);
     const uint8_t c = tile_class(mm[(size_t)b * nK + kb], q0, q1, k0, k1, causal);
     crow[kb] = c;
     cnt += (c != 0);
@@ -212,7 +214,7 @@ cudaError_t launch_classify(const fm_problem& p, int bm, int bn, int nQ, int nK,
                             const int32_t* lte, const int32_t* uts, const int32_t* ute, uint8_t* tile_class,
                             int32_t* q_off, int32_t* q_queue, int32_t* k_off, int32_t* k_queue, void* ws,
                             cudaStream_t s, int* err) {
-  const int B = p.B, N = p.N;
+  const int B = p.B, N = p.N, Nk = kv_rows(p);
   uint8_t* w = static_cast<uint8_t*>(ws);
   Minmax* mm = reinterpret_cast<Minmax*>(w);
   w += align256(sizeof(Minmax) * (size_t)B * nK);
@@ -221,8 +223,10 @@ cudaError_t launch_classify(const fm_problem& p, int bm, int bn, int nQ, int nK,
   int32_t* col_cnt = reinterpret_cast<int32_t*>(w);
 
   const long long nkb = (long long)B * nK, nqb = (long long)B * nQ;
-  block_minmax_kernel<<<(unsigned)((nkb + 7) / 8), 256, 0, s>>>(lts, lte, uts, ute, B, N, bn, nK, mm, col_cnt, err);
-  classify_rows_kernel<<<dim3(nQ, B), 256, 0, s>>>(mm, N, bm, bn, nQ, nK, p.causal, tile_class, row_cnt, col_cnt);
+  block_minmax_kernel<<<(unsigned)((nkb + 7) / 8), 256, 0, s>>>(lts, lte, uts, ute, B, N, Nk, bn, nK, mm, col_cnt,
+                                                                err);
+  classify_rows_kernel<<<dim3(nQ, B), 256, 0, s>>>(mm, N, Nk, bm, bn, nQ, nK, p.causal, tile_class, row_cnt,
+                                                   col_cnt);
   scan_kernel<<<2, 1024, 0, s>>>(row_cnt, (int)nqb, q_off, col_cnt, (int)nkb, k_off);
   emit_queues_kernel<<<(unsigned)((nqb + nkb + 7) / 8), 256, 0, s>>>(tile_class, B, nQ, nK, q_off, q_queue, k_off,
                                                                      k_queue);

@@ -112,7 +112,7 @@ struct FwdParams {
   int* next_unit;        // work counter, zero at launch: units handed out past the first gridDim.x
   __nv_bfloat16* o;
   float* lse;
-  int B, H_q, H_kv, N, nQ, nK, G, PG, causal;
+  int B, H_q, H_kv, N, Nk, nQ, nK, G, PG, causal;  // N query rows, Nk key rows
   int units;  // B * nQ * H_kv * PG work units
   float scale_log2;
   int* err;
@@ -147,7 +147,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int k) {
 // is the last key block and N is not a multiple of 128 (its tail columns are
 // masked for every row).
 __device__ __forceinline__ bool block_partial(const FwdParams& p, int e) {
-  return (e & 1) || ((e >> 1) == p.nK - 1 && (p.N & 127));
+  return (e & 1) || ((e >> 1) == p.nK - 1 && (p.Nk & 127));
 }
 
 template <int D>
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       k = __shfl_sync(kFull, k_next, 0);
       if (u.n <= 0) continue;
-      const size_t vbase = (size_t)u.b * p.N;
+      const size_t vbase = (size_t)u.b * p.Nk;
       for (int j = 0; j < u.n && ok; ++j) {
         const int e = queue_at(us, j);
         const int kb = e >> 1;
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(320, 1)
           const bool aligned = ((reinterpret_cast<uintptr_t>(p.lts + o) | reinterpret_cast<uintptr_t>(p.lte + o) |
                                  reinterpret_cast<uintptr_t>(p.uts + o) | reinterpret_cast<uintptr_t>(p.ute + o)) &
                                 15u) == 0;
-          if (c0 + 128 <= p.N && aligned) {
+          if (c0 + 128 <= p.Nk && aligned) {
             // whole block in range and 16-byte aligned: four bulk copies
             if (lane == 0) {
               uint64_t* fb = &bars[C::B_MFULL + ms];
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(320, 1)
             int* v = reinterpret_cast<int*>(sm);
             for (int c = lane; c < 128; c += 32) {
               const int col = c0 + c;
-              const bool in = col < p.N;  // a key beyond N is masked for every row
+              const bool in = col < p.Nk;  // a key beyond Nk is masked for every row
               v[c] = in ? p.lts[vbase + col] : 0;
               v[128 + c] = in ? p.lte[vbase + col] : p.N;
               v[256 + c] = in ? p.uts[vbase + col] : 0;
@@ -789,8 +789,9 @@ cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const 
   }
   if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, P.B * nQ, order);
   CUtensorMap tq, tk, tv, to;
-  if (!make_tmap_bhnd(&tq, q, (int64_t)P.B * P.H_q, P.N, P.d) || !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, P.N, P.d) ||
-      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, P.N, P.d) ||
+  const int Nk = kv_rows(P);
+  if (!make_tmap_bhnd(&tq, q, (int64_t)P.B * P.H_q, P.N, P.d) || !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, Nk, P.d) ||
+      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, Nk, P.d) ||
       !make_tmap_bhnd_w32(&to, o, (int64_t)P.B * P.H_q, P.N, P.d))
     return cudaErrorInvalidValue;
   FwdParams prm;
@@ -808,8 +809,9 @@ cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const 
   prm.H_q = P.H_q;
   prm.H_kv = P.H_kv;
   prm.N = P.N;
+  prm.Nk = Nk;
   prm.nQ = nQ;
-  prm.nK = nQ;
+  prm.nK = (Nk + kTile - 1) / kTile;
   prm.G = G;
   prm.PG = PG;
   prm.causal = P.causal ? 1 : 0;

@@ -63,6 +63,9 @@ bool make_tmap_bhnd_w32(void* out_tmap /* CUtensorMap* */, const void* base, int
 
 constexpr int kTile = 128;  // attention tile (block_m = block_n)
 
+// Key / value rows of a problem (N_kv = 0 stands for N_kv = N).
+inline int kv_rows(const fm_problem& p) { return p.N_kv > 0 ? p.N_kv : p.N; }
+
 // Launch accounting and optional event timing of the main kernels (fm_api.cu).
 void count_launches(int n);
 enum { kTimedFwd = 0, kTimedBwd = 1 };
