@@ -17,7 +17,9 @@ slow and written straight from the definitions:
 * tiles are classified from block-wise min/max of the vectors (FlashMask-3
   project page, §3.1, the tile rule under the 64 x 64 / 8 x 8 figure),
   generalised to intervals that do not reach the sequence edge;
-* localization is the clip-shift-max map of FlashMask-3 project page, §3.2.
+* localization is the clip-shift-max map of FlashMask-3 project page, §3.2;
+* the FlashMask Guide's FMS / FME vectors (one inclusive visible interval per
+  key column) map onto the four vectors as the complement of that interval.
 
 Readings where the pages are silent (all pinned by tests/test_oracle.py):
   - intervals are half-open row ranges; start >= end is an empty interval;
@@ -272,6 +274,26 @@ def unmasked_pairs(vec_b, causal: bool, row_chunk: int = 4096) -> int:
         m = masked_rows(lts, lte, uts, ute, causal, np.arange(r0, min(r0 + row_chunk, n)))
         tot += int((~m).sum())
     return tot
+
+
+# ------------------------------------------------ FMS / FME conversion
+def from_fms_fme(fms, fme, n_rows: int):
+    """The FlashMask Guide's representation ("Column-Wise Sparse Representation"
+    under "The Solution: FlashMask Sparse Mask Representation"): key column j
+    is visible exactly to rows FMS_j <= i <= FME_j (inclusive), one interval,
+    with causality written into FMS. As the four vectors (used with causal
+    off): the masked rows of column j are [0, FMS_j) and [FME_j + 1, N), so
+    UTS = 0, UTE = FMS, LTS = FME + 1, LTE = N, each clipped to [0, N]. An
+    empty interval (FMS_j > FME_j) masks the whole column.
+    """
+    n = int(n_rows)
+    fms = np.asarray(fms, dtype=np.int64)
+    fme = np.asarray(fme, dtype=np.int64)
+    lts = np.clip(fme + 1, 0, n)
+    lte = np.full_like(fms, n)
+    uts = np.zeros_like(fms)
+    ute = np.clip(fms, 0, n)
+    return tuple(x.astype(np.int32) for x in (lts, lte, uts, ute))
 
 
 # ---------------------------------------------------------- localization
