@@ -200,6 +200,21 @@ fm_status fm_localize(const int32_t* x_global, int64_t n, const int32_t* chunk_o
                       int32_t* x_local, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * The FlashMask Guide's representation ("The Solution: FlashMask Sparse Mask
+ * Representation", "Column-Wise Sparse Representation"): key column j is
+ * visible exactly to query rows FMS_j <= i <= FME_j (inclusive, one interval;
+ * causality is written into FMS, e.g. FMS_j = j). fm_from_fms_fme writes the
+ * equivalent four vectors for use with causal = 0: the masked rows [0, FMS_j)
+ * and [FME_j + 1, N) become UTS = 0, UTE = clip(FMS), LTS = clip(FME + 1),
+ * LTE = N, clipped to [0, N]; FMS_j > FME_j masks the whole column. fms, fme
+ * and the four outputs are n_values device int32 values each (any (B, N_kv)
+ * layout); N is the number of query rows. Output buffers must not overlap the
+ * inputs.
+ * ------------------------------------------------------------------------- */
+fm_status fm_from_fms_fme(const int32_t* fms, const int32_t* fme, int64_t n_values, int32_t N, int32_t* lts,
+                          int32_t* lte, int32_t* uts, int32_t* ute, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Sparsity-aware chunk balancing for context parallelism (FlashMask-3 project
  * page, §3.3 "Balance the work, not the length"). HOST functions: every
  * pointer in this section is a host pointer, nothing touches a GPU, and the

@@ -9,8 +9,8 @@ is no silent fallback.
 Functions carry the names of the C entry points:
   fm_classify_tiles, fm_attn_fwd, fm_attn_bwd, fm_localize, fm_device_status,
   fm_selftest_wait_timeout, fm_profile_enable, fm_profile_read, fm_launch_count,
-  fm_chunk_loads, fm_balance_chunks (host code: the chunk balancer for context
-  parallelism), plus flashmask_attention (autograd wrapper: the
+  fm_from_fms_fme, fm_chunk_loads, fm_balance_chunks (host code: the chunk
+  balancer for context parallelism), plus flashmask_attention (autograd wrapper: the
 classification, forward and backward calls in one differentiable op).
 """
 from __future__ import annotations
@@ -69,6 +69,7 @@ _SIGS = {
     "fm_attn_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
     "fm_attn_bwd": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 15 + [_P, ctypes.c_size_t, _P]),
     "fm_localize": (ctypes.c_int, [_P, ctypes.c_int64, _P, ctypes.c_int32, ctypes.c_int32, _P, _P]),
+    "fm_from_fms_fme": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P, _P]),
     "fm_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "fm_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, _P]),
     "fm_profile_enable": (ctypes.c_int, [ctypes.c_int32]),
@@ -228,6 +229,20 @@ def fm_localize(x, chunk_off, C: int, out=None, stream=None):
     _check(lib().fm_localize(_ptr(x), ctypes.c_int64(x.numel()), _ptr(chunk_off), int(chunk_off.numel()), int(C),
                              _ptr(out), _stream(stream)), "fm_localize")
     return out
+
+
+def fm_from_fms_fme(fms, fme, n_rows=None, stream=None):
+    """(lts, lte, uts, ute) for the FlashMask Guide's inclusive visible intervals
+    [FMS_j, FME_j] (int32 CUDA tensors of one shape, e.g. (B, N_kv)); use the
+    result with causal=False. n_rows: query rows N (default: the last dimension)."""
+    if fms.dtype != torch.int32 or fme.dtype != torch.int32 or fms.shape != fme.shape or not fms.is_cuda:
+        raise ValueError("fms and fme must be int32 CUDA tensors of the same shape")
+    fms, fme = fms.contiguous(), fme.contiguous()
+    n = fms.shape[-1] if n_rows is None else int(n_rows)
+    out = [torch.empty_like(fms) for _ in range(4)]
+    _check(lib().fm_from_fms_fme(_ptr(fms), _ptr(fme), ctypes.c_int64(fms.numel()), n, *(_ptr(x) for x in out),
+                                 _stream(stream)), "fm_from_fms_fme")
+    return tuple(out)
 
 
 def fm_device_status(stream=None):

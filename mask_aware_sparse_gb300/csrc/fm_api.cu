@@ -307,6 +307,15 @@ fm_status fm_localize(const int32_t* x_global, int64_t n, const int32_t* chunk_o
   return from_cuda(launch_localize(x_global, n, chunk_off, kappa, C, x_local, static_cast<cudaStream_t>(stream)));
 }
 
+fm_status fm_from_fms_fme(const int32_t* fms, const int32_t* fme, int64_t n_values, int32_t N, int32_t* lts,
+                          int32_t* lte, int32_t* uts, int32_t* ute, void* stream) {
+  if (n_values < 0 || N < 0 || N > (1 << 30)) return FM_ERR_INVALID_ARG;
+  if (n_values == 0) return FM_OK;
+  if (!fms || !fme || !lts || !lte || !uts || !ute) return FM_ERR_INVALID_ARG;
+  return from_cuda(
+      launch_from_fms_fme(fms, fme, n_values, N, lts, lte, uts, ute, static_cast<cudaStream_t>(stream)));
+}
+
 fm_status fm_device_status(void* stream, int32_t* bits) {
   int* err = device_error_word();
   if (!err) return FM_ERR_CUDA;

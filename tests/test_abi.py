@@ -91,6 +91,30 @@ def test_empty_problems_are_noops(lib):
         assert lib.fm_attn_bwd(ctypes.byref(p), *bargs) == fm.FM_OK
     assert lib.fm_localize(nul, 0, nul, 1, 4, nul, nul) == fm.FM_OK
     assert lib.fm_localize(nul, 10, nul, 0, 4, nul, nul) == fm.FM_ERR_INVALID_ARG
+    assert lib.fm_from_fms_fme(nul, nul, 0, 16, nul, nul, nul, nul, nul) == fm.FM_OK
+    assert lib.fm_from_fms_fme(nul, nul, 8, 16, nul, nul, nul, nul, nul) == fm.FM_ERR_INVALID_ARG
+    assert lib.fm_from_fms_fme(nul, nul, -1, 16, nul, nul, nul, nul, nul) == fm.FM_ERR_INVALID_ARG
+
+
+def test_rectangular_problem_shapes(lib):
+    # N query rows, N_kv keys: tile counts follow each axis; N_kv = 0 is N
+    t = fm.fm_tiling(128, 64)
+    nq, nk = ctypes.c_int32(), ctypes.c_int32()
+    p = fm._problem(1, 4, 2, 300, 128, 0.1, 0, 1000)
+    assert lib.fm_tile_counts(ctypes.byref(p), ctypes.byref(t), ctypes.byref(nq), ctypes.byref(nk)) == fm.FM_OK
+    assert (nq.value, nk.value) == (3, 16)
+    p = fm._problem(1, 4, 2, 300, 128, 0.1, 0, 0)
+    assert lib.fm_tile_counts(ctypes.byref(p), ctypes.byref(t), ctypes.byref(nq), ctypes.byref(nk)) == fm.FM_OK
+    assert (nq.value, nk.value) == (3, 5)
+    p = fm._problem(1, 4, 2, 300, 128, 0.1, 0, -1)
+    assert lib.fm_tile_counts(ctypes.byref(p), ctypes.byref(t), ctypes.byref(nq), ctypes.byref(nk)) == \
+        fm.FM_ERR_INVALID_ARG
+    # workspaces follow the axes too: the backward's dQ accumulator by rows,
+    # its launch-order table by key blocks
+    a = fm._problem(1, 4, 2, 256, 128, 0.1, 0, 65536)
+    b = fm._problem(1, 4, 2, 256, 128, 0.1, 0, 256)
+    assert lib.fm_attn_bwd_workspace_bytes(ctypes.byref(a)) > lib.fm_attn_bwd_workspace_bytes(ctypes.byref(b))
+    assert lib.fm_attn_fwd_workspace_bytes(ctypes.byref(a)) == lib.fm_attn_fwd_workspace_bytes(ctypes.byref(b))
 
 
 def test_workspace_queries(lib):

@@ -1,0 +1,60 @@
+"""fm_from_fms_fme against the oracle, bit for bit, and the FlashMask Guide's
+DPO mask through the whole path (FlashMask Guide, "The Solution: FlashMask
+Sparse Mask Representation" and "Real-World Attention Mask Topologies")."""
+import numpy as np
+import pytest
+import torch
+
+import mask_aware_sparse_gb300 as fm
+import oracle
+from workloads import tensors
+
+from helpers import assert_grad, assert_lse, assert_out, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("shape,offset", [((2, 1003), 0), ((3, 512), 1), ((1, 7), 0)])
+def test_from_fms_fme_matches_oracle(shape, offset):
+    rng = np.random.default_rng(shape[1] + offset)
+    n = shape[1]
+    m = int(np.prod(shape))
+    fms = rng.integers(-3, n + 4, size=m + offset).astype(np.int32)
+    fme = rng.integers(-3, n + 4, size=m + offset).astype(np.int32)
+    # offset 1: inputs that are not 16-byte aligned take the element-wise path
+    a = torch.from_numpy(fms).cuda()[offset:].view(shape)
+    b = torch.from_numpy(fme).cuda()[offset:].view(shape)
+    got = fm.fm_from_fms_fme(a, b, n_rows=n)
+    ref = oracle.from_fms_fme(fms[offset:], fme[offset:], n)
+    for g, r in zip(got, ref):
+        assert np.array_equal(g.cpu().numpy().reshape(-1), r)
+
+
+def test_guide_dpo_mask_end_to_end():
+    # one DPO sample as the Guide writes it: prompt keys visible to every later
+    # row, chosen keys to chosen rows, rejected keys to rejected rows
+    P, Cc, R = 700, 500, 848
+    n, d, hq, hkv = P + Cc + R, 128, 4, 2
+    fms = np.arange(n)
+    fme = np.empty(n, np.int64)
+    fme[:P] = n - 1
+    fme[P:P + Cc] = P + Cc - 1
+    fme[P + Cc:] = n - 1
+    t = lambda x: torch.from_numpy(x.astype(np.int32)[None]).cuda()  # noqa: E731
+    vec = fm.fm_from_fms_fme(t(fms), t(fme))
+    vec_np = oracle.from_fms_fme(fms[None], fme[None], n)
+    cfg = dict(B=1, H_q=hq, H_kv=hkv, N=n, d=d)
+    q, k, v, do = tensors.make_qkvdo(cfg)
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    scale = d ** -0.5
+    qs = fm.fm_classify_tiles(*vec, causal=False)
+    o, lse = fm.fm_attn_fwd(qd, kd, vd, *vec, qs, scale=scale, causal=False)
+    dq, dk, dv = fm.fm_attn_bwd(qd, kd, vd, o, lse, dod, *vec, qs, scale=scale, causal=False)
+    st, bits = fm.fm_device_status()
+    assert st == fm.FM_OK, bits
+    O_ref, L_ref = oracle.forward(f64(q), f64(k), f64(v), vec_np, False, scale)
+    assert_out(f64(o), O_ref)
+    assert_lse(f64(lse), L_ref)
+    ref = oracle.backward(f64(q), f64(k), f64(v), f64(do), vec_np, False, scale)
+    for name, a, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert_grad(f64(a), r, name)
