@@ -60,6 +60,27 @@ def masked_rows(lts, lte, uts, ute, causal: bool, rows) -> np.ndarray:
     return m
 
 
+def multi_masked_rows(fms, fme, rows) -> np.ndarray:
+    """Multi-interval masks (FlashMask Guide, after the DPO example: up to M
+    visible intervals per key column): key j is visible to row i iff
+    FMS^(m)_j <= i <= FME^(m)_j for some m. fms, fme: (M, N_kv) of one batch
+    entry. True where masked, shape (len(rows), N_kv)."""
+    rows = np.asarray(rows, dtype=np.int64)[:, None]
+    vis = np.zeros((rows.shape[0], fms.shape[1]), dtype=bool)
+    for m in range(fms.shape[0]):
+        vis |= (fms[m][None, :].astype(np.int64) <= rows) & (rows <= fme[m][None, :].astype(np.int64))
+    return ~vis
+
+
+def _mask_rows(vec, causal, b, rows):
+    """Masked rows of batch entry b for either mask form: the four vectors
+    (a tuple of (B, N_kv) arrays) or {"fms", "fme"}: (B, M, N_kv) arrays."""
+    if isinstance(vec, dict):
+        return multi_masked_rows(vec["fms"][b], vec["fme"][b], rows)
+    lts, lte, uts, ute = (x[b] for x in vec)
+    return masked_rows(lts, lte, uts, ute, causal, rows)
+
+
 def dense_mask(lts, lte, uts, ute, causal: bool) -> np.ndarray:
     """The full N x N boolean mask (True = masked). Small N only."""
     return masked_rows(lts, lte, uts, ute, causal, np.arange(lts.shape[0]))
@@ -180,9 +201,8 @@ def row_probs(q, k, vec, causal, scale, b, h, rows):
     P = exp(S - max) / sum. A fully-masked row gets P = 0 and LSE = -inf.
     q: (B, Hq, N, d), k: (B, Hkv, N_kv, d), float64.
     """
-    lts, lte, uts, ute = (x[b] for x in vec)
     g = _kv_head(h, q.shape[1], k.shape[1])
-    m = masked_rows(lts, lte, uts, ute, causal, rows)
+    m = _mask_rows(vec, causal, b, rows)
     s = scale * (q[b, h, rows] @ k[b, g].T)
     s = np.where(m, -np.inf, s)
     r = s.max(axis=1)
@@ -237,9 +257,12 @@ def backward(q, k, v, do, vec, causal: bool, scale: float, heads=None, rows=None
     dK = np.zeros((B, Hkv, len(cols), d))
     dV = np.zeros((B, Hkv, len(cols), d))
     for b in range(B):
-        lts, lte, uts, ute = (x[b] for x in vec)
         # rows that see at least one selected column: only they feed dK/dV there
-        mc = masked_cols(lts, lte, uts, ute, causal, cols, n_rows=N)
+        if isinstance(vec, dict):
+            mc = multi_masked_rows(vec["fms"][b], vec["fme"][b], np.arange(N))[:, cols]
+        else:
+            lts, lte, uts, ute = (x[b] for x in vec)
+            mc = masked_cols(lts, lte, uts, ute, causal, cols, n_rows=N)
         feed_rows = np.nonzero(~mc.all(axis=1))[0]
         need = np.union1d(rows, feed_rows)
         row_pos = {int(r): t for t, r in enumerate(rows)}

@@ -54,3 +54,45 @@ def test_conversion_brute_force():
         assert np.array_equal(visible(fms, fme, n), want)
         v = oracle.from_fms_fme(fms, fme, n)
         assert all(((x >= 0) & (x <= n)).all() for x in v)
+
+
+def test_multi_interval_mask_brute_force():
+    rng = np.random.default_rng(1)
+    n, M = 23, 3
+    fms = rng.integers(-2, n + 2, size=(M, n))
+    fme = rng.integers(-2, n + 2, size=(M, n))
+    got = oracle.multi_masked_rows(fms, fme, np.arange(n))
+    for i in range(n):
+        for j in range(n):
+            vis = any(fms[m, j] <= i <= fme[m, j] for m in range(M))
+            assert got[i, j] == (not vis)
+    # one interval is the single-interval form
+    one = oracle.multi_masked_rows(fms[:1], fme[:1], np.arange(n))
+    assert np.array_equal(one, oracle.dense_mask(*oracle.from_fms_fme(fms[0], fme[0], n), False))
+
+
+def test_multi_interval_attention_is_the_lse_merge_of_its_parts():
+    # With disjoint intervals per column, a row's visible keys split into
+    # disjoint sets, one per interval: the attention over their union is the
+    # LSE-weighted merge of the per-interval attentions, and its gradients
+    # are the sums of the per-interval backward passes taken with the merged
+    # output and LSE (the row term D then belongs to the merged output).
+    rng = np.random.default_rng(2)
+    n, d, M = 48, 8, 3
+    cuts = np.sort(rng.integers(0, n, size=(2 * M, n)), axis=0)  # disjoint, ascending per column
+    fms, fme = cuts[0::2], cuts[1::2] - 1
+    q, k, v, do = (rng.standard_normal((1, 2, n, d)) for _ in range(4))
+    k, v = k[:, :1], v[:, :1]
+    spec = {"fms": fms[None], "fme": fme[None]}
+    O, L = oracle.forward(q, k, v, spec, False, 0.3)
+    parts = [oracle.forward(q, k, v, tuple(x[None] for x in oracle.from_fms_fme(fms[m], fme[m], n)), False, 0.3)
+             for m in range(M)]
+    Ls = np.stack([p[1] for p in parts])
+    with np.errstate(invalid="ignore", divide="ignore"):
+        top = np.max(Ls, axis=0)
+        Lm = np.where(np.isneginf(top), -np.inf, top + np.log(np.sum(np.exp(Ls - np.where(np.isneginf(top), 0, top)), axis=0)))
+        w = np.where(np.isneginf(Ls), 0.0, np.exp(Ls - np.where(np.isneginf(Lm), 0, Lm)))
+    Om = sum(w[m][..., None] * parts[m][0] for m in range(M))
+    assert np.array_equal(np.isneginf(Lm), np.isneginf(L))
+    fin = ~np.isneginf(L)
+    assert np.allclose(Lm[fin], L[fin], atol=1e-12) and np.allclose(Om, O, atol=1e-12)
