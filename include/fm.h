@@ -215,6 +215,28 @@ fm_status fm_from_fms_fme(const int32_t* fms, const int32_t* fme, int64_t n_valu
                           int32_t* lte, int32_t* uts, int32_t* ute, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Multi-interval masks (FlashMask Guide, after the DPO example: a key column
+ * may be visible to up to M disjoint row intervals [FMS^(m)_j, FME^(m)_j]).
+ * For one query row the keys visible through different intervals are then
+ * disjoint sets, so attention over their union is the log-sum-exp merge of
+ * one single-interval attention per interval (fm_from_fms_fme, classify,
+ * forward on each), and its gradients are the sums of the parts' backward
+ * passes run with the MERGED O and LSE.
+ *
+ * fm_merge_parts: M (1..8) parts, O_m (rows x d bf16) and LSE_m (rows fp32);
+ *   o_parts / lse_parts are HOST arrays of M DEVICE pointers. Writes
+ *   LSE = log sum_m exp(LSE_m) and O = sum_m exp(LSE_m - LSE) O_m (bf16,
+ *   rounded once), or LSE = -inf and O = 0 where every part is -inf.
+ *   rows = B * H_q * N; d a multiple of 8; O pointers 16-byte aligned.
+ * fm_sum_parts: out = sum_m parts[m] over n bf16 elements (fp32 sum, rounded
+ *   once); parts is a HOST array of M DEVICE pointers.
+ * Outputs must not overlap the inputs.
+ * ------------------------------------------------------------------------- */
+fm_status fm_merge_parts(int32_t M, const void* const* o_parts, const float* const* lse_parts, int64_t rows,
+                         int32_t d, void* o, float* lse, void* stream);
+fm_status fm_sum_parts(int32_t M, const void* const* parts, int64_t n, void* out, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Sparsity-aware chunk balancing for context parallelism (FlashMask-3 project
  * page, §3.3 "Balance the work, not the length"). HOST functions: every
  * pointer in this section is a host pointer, nothing touches a GPU, and the

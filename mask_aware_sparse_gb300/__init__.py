@@ -9,9 +9,11 @@ is no silent fallback.
 Functions carry the names of the C entry points:
   fm_classify_tiles, fm_attn_fwd, fm_attn_bwd, fm_localize, fm_device_status,
   fm_selftest_wait_timeout, fm_profile_enable, fm_profile_read, fm_launch_count,
-  fm_from_fms_fme, fm_chunk_loads, fm_balance_chunks (host code: the chunk
-  balancer for context parallelism), plus flashmask_attention (autograd wrapper: the
-classification, forward and backward calls in one differentiable op).
+  fm_from_fms_fme, fm_merge_parts, fm_sum_parts, fm_chunk_loads,
+  fm_balance_chunks (host code: the chunk balancer for context parallelism);
+plus fm_attn_multi_interval (multi-interval masks as a sequence of library
+calls) and flashmask_attention (autograd wrapper: the classification, forward
+and backward calls in one differentiable op).
 """
 from __future__ import annotations
 
@@ -70,6 +72,8 @@ _SIGS = {
     "fm_attn_bwd": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 15 + [_P, ctypes.c_size_t, _P]),
     "fm_localize": (ctypes.c_int, [_P, ctypes.c_int64, _P, ctypes.c_int32, ctypes.c_int32, _P, _P]),
     "fm_from_fms_fme": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P, _P]),
+    "fm_merge_parts": (ctypes.c_int, [ctypes.c_int32, _P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]),
+    "fm_sum_parts": (ctypes.c_int, [ctypes.c_int32, _P, ctypes.c_int64, _P, _P]),
     "fm_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "fm_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, _P]),
     "fm_profile_enable": (ctypes.c_int, [ctypes.c_int32]),
@@ -243,6 +247,63 @@ def fm_from_fms_fme(fms, fme, n_rows=None, stream=None):
     _check(lib().fm_from_fms_fme(_ptr(fms), _ptr(fme), ctypes.c_int64(fms.numel()), n, *(_ptr(x) for x in out),
                                  _stream(stream)), "fm_from_fms_fme")
     return tuple(out)
+
+
+def _ptr_array(ts):
+    return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+
+
+def fm_merge_parts(o_parts, lse_parts, o=None, lse=None, stream=None):
+    """Log-sum-exp merge of M partial attentions (bf16 O_m, fp32 LSE_m of one shape each)."""
+    if len(o_parts) != len(lse_parts) or not o_parts:
+        raise ValueError("one LSE per O part")
+    for t in o_parts:
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != o_parts[0].shape:
+            raise ValueError("O parts must be contiguous bf16 tensors of one shape")
+    for t in lse_parts:
+        if t.dtype != torch.float32 or not t.is_contiguous() or t.shape != o_parts[0].shape[:-1]:
+            raise ValueError("LSE parts must be contiguous fp32 tensors of O's shape without d")
+    o = torch.empty_like(o_parts[0]) if o is None else o
+    lse = torch.empty_like(lse_parts[0]) if lse is None else lse
+    d = o_parts[0].shape[-1]
+    _check(lib().fm_merge_parts(len(o_parts), _ptr_array(o_parts), _ptr_array(lse_parts),
+                                ctypes.c_int64(lse.numel()), d, _ptr(o), _ptr(lse), _stream(stream)),
+           "fm_merge_parts")
+    return o, lse
+
+
+def fm_sum_parts(parts, out=None, stream=None):
+    """Elementwise sum of bf16 tensors of one shape (fp32 accumulation, one rounding)."""
+    for t in parts:
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != parts[0].shape:
+            raise ValueError("parts must be contiguous bf16 tensors of one shape")
+    out = torch.empty_like(parts[0]) if out is None else out
+    _check(lib().fm_sum_parts(len(parts), _ptr_array(parts), ctypes.c_int64(out.numel()), _ptr(out),
+                              _stream(stream)), "fm_sum_parts")
+    return out
+
+
+def fm_attn_multi_interval(q, k, v, fms, fme, *, scale: float, do=None, stream=None):
+    """Attention under multi-interval masks: fms, fme are (M, B, N_kv) int32 CUDA
+    tensors, key j visible to rows [fms[m, b, j], fme[m, b, j]] (inclusive),
+    intervals of one column disjoint. Library calls only: per interval
+    fm_from_fms_fme, fm_classify_tiles and fm_attn_fwd, then fm_merge_parts;
+    with do, per interval fm_attn_bwd on the merged O and LSE, then fm_sum_parts.
+    Returns (o, lse) or (o, lse, dq, dk, dv)."""
+    N = q.shape[2]
+    parts = []
+    for m in range(fms.shape[0]):
+        vec = fm_from_fms_fme(fms[m], fme[m], n_rows=N, stream=stream)
+        qs = fm_classify_tiles(*vec, causal=False, n_rows=N, stream=stream)
+        o_m, lse_m = fm_attn_fwd(q, k, v, *vec, qs, scale=scale, causal=False, stream=stream)
+        parts.append((vec, qs, o_m, lse_m))
+    o, lse = fm_merge_parts([p[2] for p in parts], [p[3] for p in parts], stream=stream)
+    if do is None:
+        return o, lse
+    grads = [fm_attn_bwd(q, k, v, o, lse, do, *vec, qs, scale=scale, causal=False, stream=stream)
+             for vec, qs, _, _ in parts]
+    dq, dk, dv = (fm_sum_parts([g[i] for g in grads], stream=stream) for i in range(3))
+    return o, lse, dq, dk, dv
 
 
 def fm_device_status(stream=None):

@@ -316,6 +316,25 @@ fm_status fm_from_fms_fme(const int32_t* fms, const int32_t* fme, int64_t n_valu
       launch_from_fms_fme(fms, fme, n_values, N, lts, lte, uts, ute, static_cast<cudaStream_t>(stream)));
 }
 
+fm_status fm_merge_parts(int32_t M, const void* const* o_parts, const float* const* lse_parts, int64_t rows,
+                         int32_t d, void* o, float* lse, void* stream) {
+  if (M < 1 || M > kMaxParts || rows < 0 || d < 8 || d % 8 != 0) return FM_ERR_INVALID_ARG;
+  if (rows == 0) return FM_OK;
+  if (!o_parts || !lse_parts || !o || !lse || !aligned16(o)) return FM_ERR_INVALID_ARG;
+  for (int m = 0; m < M; ++m)
+    if (!o_parts[m] || !lse_parts[m] || !aligned16(o_parts[m])) return FM_ERR_INVALID_ARG;
+  return from_cuda(launch_merge_parts(M, o_parts, lse_parts, rows, d, o, lse, static_cast<cudaStream_t>(stream)));
+}
+
+fm_status fm_sum_parts(int32_t M, const void* const* parts, int64_t n, void* out, void* stream) {
+  if (M < 1 || M > kMaxParts || n < 0) return FM_ERR_INVALID_ARG;
+  if (n == 0) return FM_OK;
+  if (!parts || !out) return FM_ERR_INVALID_ARG;
+  for (int m = 0; m < M; ++m)
+    if (!parts[m]) return FM_ERR_INVALID_ARG;
+  return from_cuda(launch_sum_parts(M, parts, n, out, static_cast<cudaStream_t>(stream)));
+}
+
 fm_status fm_device_status(void* stream, int32_t* bits) {
   int* err = device_error_word();
   if (!err) return FM_ERR_CUDA;

@@ -17,6 +17,11 @@ cudaError_t launch_classify(const fm_problem& p, int bm, int bn, int nQ, int nK,
                             cudaStream_t s, int* err);
 
 // Localization (fm_localize.cu).
+// parts of a multi-interval mask (fm_multi.cu)
+constexpr int kMaxParts = 8;
+cudaError_t launch_merge_parts(int M, const void* const* o_parts, const float* const* lse_parts, int64_t rows, int d,
+                               void* o, float* lse, cudaStream_t s);
+cudaError_t launch_sum_parts(int M, const void* const* parts, int64_t n, void* out, cudaStream_t s);
 cudaError_t launch_from_fms_fme(const int32_t* fms, const int32_t* fme, int64_t m, int n, int32_t* lts, int32_t* lte,
                                 int32_t* uts, int32_t* ute, cudaStream_t s);
 cudaError_t launch_localize(const int32_t* x, int64_t n, const int32_t* off, int kappa, int C, int32_t* out,

@@ -58,3 +58,49 @@ def test_guide_dpo_mask_end_to_end():
     ref = oracle.backward(f64(q), f64(k), f64(v), f64(do), vec_np, False, scale)
     for name, a, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         assert_grad(f64(a), r, name)
+
+
+def disjoint_intervals(rng, M, B, n_rows, n_keys):
+    """(M, B, N_kv) inclusive intervals, disjoint and ascending per column
+    (some empty: end < start)."""
+    cuts = np.sort(rng.integers(0, n_rows + 1, size=(2 * M, B, n_keys)), axis=0)
+    return cuts[0::2].astype(np.int32), (cuts[1::2] - 1).astype(np.int32)
+
+
+@pytest.mark.parametrize("M,n,nk,d,hq,hkv", [(3, 1000, 1000, 128, 4, 2), (2, 640, 1300, 64, 2, 1),
+                                             (4, 512, 512, 128, 2, 2)])
+def test_multi_interval_matches_oracle(M, n, nk, d, hq, hkv):
+    rng = np.random.default_rng(M * 1000 + n)
+    B = 2
+    fms, fme = disjoint_intervals(rng, M, B, n, nk)
+    q = tensors.randn_bf16((B, hq, n, d), 40)
+    k = tensors.randn_bf16((B, hkv, nk, d), 41)
+    v = tensors.randn_bf16((B, hkv, nk, d), 42)
+    do = tensors.randn_bf16((B, hq, n, d), 43)
+    scale = d ** -0.5
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    o, lse, dq, dk, dv = fm.fm_attn_multi_interval(qd, kd, vd, torch.from_numpy(fms).cuda(),
+                                                   torch.from_numpy(fme).cuda(), scale=scale, do=dod)
+    st, bits = fm.fm_device_status()
+    assert st == fm.FM_OK, bits
+    spec = {"fms": fms.transpose(1, 0, 2), "fme": fme.transpose(1, 0, 2)}
+    O_ref, L_ref = oracle.forward(f64(q), f64(k), f64(v), spec, False, scale)
+    assert_out(f64(o), O_ref)
+    assert_lse(f64(lse), L_ref)
+    ref = oracle.backward(f64(q), f64(k), f64(v), f64(do), spec, False, scale)
+    for name, a, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert_grad(f64(a), r, name)
+
+
+def test_merge_and_sum_of_one_part_are_identities():
+    rng = np.random.default_rng(5)
+    o = torch.from_numpy(rng.standard_normal((3, 77, 64)).astype(np.float32)).to(torch.bfloat16).cuda()
+    lse = torch.from_numpy(rng.standard_normal((3, 77)).astype(np.float32)).cuda()
+    lse[0, :5] = -float("inf")
+    om, lm = fm.fm_merge_parts([o], [lse])
+    assert torch.equal(lm, lse)
+    assert torch.equal(om[lse != -float("inf")], o[lse != -float("inf")])
+    assert (om[lse == -float("inf")] == 0).all()
+    x = torch.from_numpy(rng.standard_normal(1001).astype(np.float32)).to(torch.bfloat16).cuda()
+    assert torch.equal(fm.fm_sum_parts([x]), x)
+    assert torch.equal(fm.fm_sum_parts([x[1:], x[1:]]), (2 * x[1:].float()).to(torch.bfloat16))
