@@ -357,34 +357,58 @@ def capture_step(path: Path):
 
 
 def e2e_measure(path: Path, steps: int):
-    """Same metric through the public API from pinned HOST buffers: each step
-    copies the inputs host->device, runs the path and reads every output back."""
+    """Same metric through the public API from pinned HOST buffers: every step
+    copies its inputs host->device, runs the path and reads every output back.
+    Steps are pipelined on three streams (copy in, compute, copy out) with two
+    sets of device buffers, so one step's copies overlap the neighbouring
+    steps' compute and the two copy directions overlap each other; events keep
+    a buffer set from being overwritten before its readers are done."""
     fm, c, dev = path.fm, path.cfg, path.dev
     h_in = [t.cpu().pin_memory() for t in (path.q, path.k, path.v, path.do)]
     h_vec = [t.cpu().pin_memory() for t in path.vec]
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (path.o, path.lse, path.dq, path.dk, path.dv)]
-    d_in = [torch.empty_like(t, device=dev) for t in h_in]
-    d_vec = [torch.empty_like(t, device=dev) for t in h_vec]
+    outs = (path.o, path.lse, path.dq, path.dk, path.dv)
+    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _ in range(2)]
+    d_in = [[torch.empty_like(t, device=dev) for t in h_in + h_vec] for _ in range(2)]
+    d_out = [[torch.empty_like(t) for t in outs] for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in h_in + h_vec)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    c_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
 
-    def one():
-        for d, h in zip(d_in + d_vec, h_in + h_vec):
-            d.copy_(h, non_blocking=True)
-        q, k, v, do = d_in
-        qs = fm.fm_classify_tiles(*d_vec, causal=c["causal"])
-        o, lse = fm.fm_attn_fwd(q, k, v, *d_vec, qs, scale=c["scale"], causal=c["causal"])
-        dq, dk, dv = fm.fm_attn_bwd(q, k, v, o, lse, do, *d_vec, qs, scale=c["scale"], causal=c["causal"])
-        for h, d in zip(h_out, (o, lse, dq, dk, dv)):
-            h.copy_(d, non_blocking=True)
+    def one(i):
+        j = i & 1
+        s_in.wait_event(c_done[j])  # the compute two steps back has read this input set
+        with torch.cuda.stream(s_in):
+            for d, h in zip(d_in[j], h_in + h_vec):
+                d.copy_(h, non_blocking=True)
+            in_done[j].record(s_in)
+        s_c.wait_event(in_done[j])
+        s_c.wait_event(out_done[j])  # the copy-out two steps back has read this output set
+        with torch.cuda.stream(s_c):
+            q, k, v, do, *vec = d_in[j]
+            o, lse, dq, dk, dv = d_out[j]
+            qs = fm.fm_classify_tiles(*vec, causal=c["causal"], stream=s_c)
+            fm.fm_attn_fwd(q, k, v, *vec, qs, scale=c["scale"], causal=c["causal"], o=o, lse=lse, stream=s_c)
+            fm.fm_attn_bwd(q, k, v, o, lse, do, *vec, qs, scale=c["scale"], causal=c["causal"], dq=dq, dk=dk, dv=dv,
+                           stream=s_c)
+            c_done[j].record(s_c)
+        s_out.wait_event(c_done[j])
+        with torch.cuda.stream(s_out):
+            for h, d in zip(h_out[j], d_out[j]):
+                h.copy_(d, non_blocking=True)
+            out_done[j].record(s_out)
 
-    one()
+    for i in range(2):
+        one(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        one()
-    b.record()
+    a.record(s_in)
+    for i in range(steps):
+        one(i)
+    s_in.wait_stream(s_out)
+    b.record(s_in)
     torch.cuda.synchronize()
     return a.elapsed_time(b) / 1e3 / steps, h2d, d2h
 
