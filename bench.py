@@ -579,7 +579,10 @@ def _time_call(fn, reps=5):
 
 def run_balance(args):
     import mask_aware_sparse_gb300 as fm
+    from mask_aware_sparse_gb300 import build as fmbuild
     from workloads import chunks
+
+    fmbuild.build()
 
     cp, cu = BAL_COSTS
     cases = []

@@ -91,3 +91,25 @@ def test_closed_block_subproblem_equals_full_problem():
                                         do[:, :, sl].numpy(), sub, True, 0.3)
         assert np.allclose(Os, O[:, :, sl], atol=1e-13) and np.allclose(dQs, dQ[:, :, sl], atol=1e-13)
         assert np.allclose(dKs, dK[:, :, sl], atol=1e-13) and np.allclose(dVs, dV[:, :, sl], atol=1e-13)
+
+
+def test_bench_balance_line_without_gpu():
+    """`bench.py --balance` prints one JSON line; it always measures the
+    ablation table's families, and the workloads' chunk loads where a GPU
+    runs the classifier."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--balance", "--no-cpu-baseline"],
+                       capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["unit"] == "ratio" and line["higher_is_better"] is False
+    assert set(line["table"]) == {"uniform", "uniform_wide", "causal", "uniform_128"}
+    t = line["table"]["causal"]
+    assert t["lb_certified"] == t["instances"] == 200
+    for c in line["cases"]:
+        poa = c["peak_over_avg"]
+        assert poa["ipo"] <= poa["lpt"] + 1e-12 and poa["ipo"] >= poa["lower_bound_kappa"] - 1e-12
