@@ -72,9 +72,14 @@ def multi_masked_rows(fms, fme, rows) -> np.ndarray:
     return ~vis
 
 
-def _mask_rows(vec, causal, b, rows):
-    """Masked rows of batch entry b for either mask form: the four vectors
-    (a tuple of (B, N_kv) arrays) or {"fms", "fme"}: (B, M, N_kv) arrays."""
+def _mask_rows(vec, causal, b, rows, h=0):
+    """Masked rows of batch entry b (query head h) for any mask form: the four
+    vectors shared by every head (a tuple of (B, N_kv) arrays), one set per
+    query head ({"heads": a tuple of (B, H_q, N_kv) arrays}), or multi-interval
+    ({"fms", "fme"}: (B, M, N_kv) arrays)."""
+    if isinstance(vec, dict) and "heads" in vec:
+        lts, lte, uts, ute = (x[b, h] for x in vec["heads"])
+        return masked_rows(lts, lte, uts, ute, causal, rows)
     if isinstance(vec, dict):
         return multi_masked_rows(vec["fms"][b], vec["fme"][b], rows)
     lts, lte, uts, ute = (x[b] for x in vec)
@@ -202,7 +207,7 @@ def row_probs(q, k, vec, causal, scale, b, h, rows):
     q: (B, Hq, N, d), k: (B, Hkv, N_kv, d), float64.
     """
     g = _kv_head(h, q.shape[1], k.shape[1])
-    m = _mask_rows(vec, causal, b, rows)
+    m = _mask_rows(vec, causal, b, rows, h)
     s = scale * (q[b, h, rows] @ k[b, g].T)
     s = np.where(m, -np.inf, s)
     r = s.max(axis=1)
@@ -256,19 +261,25 @@ def backward(q, k, v, do, vec, causal: bool, scale: float, heads=None, rows=None
     dQ = np.zeros((B, len(heads), len(rows), d))
     dK = np.zeros((B, Hkv, len(cols), d))
     dV = np.zeros((B, Hkv, len(cols), d))
-    for b in range(B):
+    per_head = isinstance(vec, dict) and "heads" in vec
+
+    def feed(b, h):
         # rows that see at least one selected column: only they feed dK/dV there
         if isinstance(vec, dict):
-            mc = multi_masked_rows(vec["fms"][b], vec["fme"][b], np.arange(N))[:, cols]
+            mc = _mask_rows(vec, causal, b, np.arange(N), h)[:, cols]
         else:
             lts, lte, uts, ute = (x[b] for x in vec)
             mc = masked_cols(lts, lte, uts, ute, causal, cols, n_rows=N)
-        feed_rows = np.nonzero(~mc.all(axis=1))[0]
-        need = np.union1d(rows, feed_rows)
+        return np.nonzero(~mc.all(axis=1))[0]
+
+    for b in range(B):
         row_pos = {int(r): t for t, r in enumerate(rows)}
-        want_q = np.isin(need, rows)
-        want_kv = np.isin(need, feed_rows)
+        shared = None if per_head else feed(b, 0)
         for hi, h in enumerate(heads):
+            feed_rows = feed(b, h) if per_head else shared
+            need = np.union1d(rows, feed_rows)
+            want_q = np.isin(need, rows)
+            want_kv = np.isin(need, feed_rows)
             g = _kv_head(h, Hq, Hkv)
             for c0 in range(0, len(need), row_chunk):
                 rr = need[c0 : c0 + row_chunk]

@@ -96,3 +96,34 @@ def test_multi_interval_attention_is_the_lse_merge_of_its_parts():
     assert np.array_equal(np.isneginf(Lm), np.isneginf(L))
     fin = ~np.isneginf(L)
     assert np.allclose(Lm[fin], L[fin], atol=1e-12) and np.allclose(Om, O, atol=1e-12)
+
+
+def test_per_head_masks_reduce_to_one_head_problems():
+    # one set of vectors per query head: each head's output is that of a
+    # one-head problem with its own vectors, and each kv head's key gradients
+    # are the sum over its query heads of those problems' gradients
+    rng = np.random.default_rng(3)
+    B, hq, hkv, n, d = 2, 4, 2, 40, 8
+    G = hq // hkv
+    a = rng.integers(0, n + 1, size=(2, B, hq, n))
+    c = rng.integers(0, n + 1, size=(2, B, hq, n))
+    heads = (a.min(0), a.max(0), c.min(0), c.max(0))
+    q, do = (rng.standard_normal((B, hq, n, d)) for _ in range(2))
+    k, v = (rng.standard_normal((B, hkv, n, d)) for _ in range(2))
+    spec = {"heads": heads}
+    for causal in (False, True):
+        O, L = oracle.forward(q, k, v, spec, causal, 0.4)
+        dQ, dK, dV = oracle.backward(q, k, v, do, spec, causal, 0.4)
+        dK_sum, dV_sum = np.zeros_like(dK), np.zeros_like(dV)
+        for h in range(hq):
+            g = h // G
+            one = tuple(x[:, h] for x in heads)
+            sl, gl = slice(h, h + 1), slice(g, g + 1)
+            O1, L1 = oracle.forward(q[:, sl], k[:, gl], v[:, gl], one, causal, 0.4)
+            assert np.allclose(O1, O[:, sl], atol=1e-12)
+            assert np.array_equal(np.isneginf(L1), np.isneginf(L[:, sl]))
+            dq1, dk1, dv1 = oracle.backward(q[:, sl], k[:, gl], v[:, gl], do[:, sl], one, causal, 0.4)
+            assert np.allclose(dq1, dQ[:, sl], atol=1e-12)
+            dK_sum[:, gl] += dk1
+            dV_sum[:, gl] += dv1
+        assert np.allclose(dK_sum, dK, atol=1e-10) and np.allclose(dV_sum, dV, atol=1e-10)
