@@ -11,8 +11,8 @@ Functions carry the names of the C entry points:
   fm_selftest_wait_timeout, fm_profile_enable, fm_profile_read, fm_launch_count,
   fm_from_fms_fme, fm_merge_parts, fm_sum_parts, fm_chunk_loads,
   fm_balance_chunks (host code: the chunk balancer for context parallelism);
-plus fm_attn_multi_interval (multi-interval masks as a sequence of library
-calls) and flashmask_attention (autograd wrapper: the classification, forward
+plus fm_attn_multi_interval and fm_attn_per_head (multi-interval and per-head
+masks as sequences of library calls) and flashmask_attention (autograd wrapper: the classification, forward
 and backward calls in one differentiable op).
 """
 from __future__ import annotations
@@ -303,6 +303,45 @@ def fm_attn_multi_interval(q, k, v, fms, fme, *, scale: float, do=None, stream=N
     grads = [fm_attn_bwd(q, k, v, o, lse, do, *vec, qs, scale=scale, causal=False, stream=stream)
              for vec, qs, _, _ in parts]
     dq, dk, dv = (fm_sum_parts([g[i] for g in grads], stream=stream) for i in range(3))
+    return o, lse, dq, dk, dv
+
+
+def fm_attn_per_head(q, k, v, lts, lte, uts, ute, *, causal: bool, scale: float, do=None, stream=None):
+    """Attention with one set of mask vectors per query head: lts..ute are
+    (B, H_q, N_kv) int32 CUDA tensors. Library calls only: for every (batch
+    entry, query head) a classification and a forward (and backward) of that
+    head's rows against its kv head; each kv head's dK, dV summed over its query
+    heads by fm_sum_parts. Returns (o, lse) or (o, lse, dq, dk, dv)."""
+    _bf16_ok(q, k, v)
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    for x in (lts, lte, uts, ute):
+        if x.dim() != 3 or x.shape[:2] != (B, Hq) or x.dtype != torch.int32 or not x.is_contiguous():
+            raise ValueError("per-head vectors must be contiguous int32 (B, H_q, N_kv) tensors")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    if do is not None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    for b in range(B):
+        for g in range(Hkv):
+            kb, vb = k[b:b + 1, g:g + 1], v[b:b + 1, g:g + 1]
+            dks, dvs = [], []
+            for h in range(g * G, (g + 1) * G):
+                vec = [x[b:b + 1, h] for x in (lts, lte, uts, ute)]
+                qs = fm_classify_tiles(*vec, causal=causal, n_rows=N, stream=stream)
+                qh, oh, lh = q[b:b + 1, h:h + 1], o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1]
+                fm_attn_fwd(qh, kb, vb, *vec, qs, scale=scale, causal=causal, o=oh, lse=lh, stream=stream)
+                if do is not None:
+                    _, dk_h, dv_h = fm_attn_bwd(qh, kb, vb, oh, lh, do[b:b + 1, h:h + 1], *vec, qs, scale=scale,
+                                                causal=causal, dq=dq[b:b + 1, h:h + 1], stream=stream)
+                    dks.append(dk_h)
+                    dvs.append(dv_h)
+            if do is not None:
+                fm_sum_parts(dks, out=dk[b:b + 1, g:g + 1], stream=stream)
+                fm_sum_parts(dvs, out=dv[b:b + 1, g:g + 1], stream=stream)
+    if do is None:
+        return o, lse
     return o, lse, dq, dk, dv
 
 
