@@ -94,6 +94,15 @@ def test_empty_problems_are_noops(lib):
     assert lib.fm_from_fms_fme(nul, nul, 0, 16, nul, nul, nul, nul, nul) == fm.FM_OK
     assert lib.fm_from_fms_fme(nul, nul, 8, 16, nul, nul, nul, nul, nul) == fm.FM_ERR_INVALID_ARG
     assert lib.fm_from_fms_fme(nul, nul, -1, 16, nul, nul, nul, nul, nul) == fm.FM_ERR_INVALID_ARG
+    # merge / sum of parts: 1..8 parts, rows and elements >= 0, d a multiple of 8
+    assert lib.fm_merge_parts(2, nul, nul, 0, 128, nul, nul, nul) == fm.FM_OK
+    for M, rows, d in ((0, 4, 128), (9, 4, 128), (2, -1, 128), (2, 4, 12), (2, 4, 0)):
+        assert lib.fm_merge_parts(M, nul, nul, rows, d, nul, nul, nul) == fm.FM_ERR_INVALID_ARG
+    assert lib.fm_merge_parts(2, nul, nul, 4, 128, nul, nul, nul) == fm.FM_ERR_INVALID_ARG  # null arrays
+    assert lib.fm_sum_parts(3, nul, 0, nul, nul) == fm.FM_OK
+    assert lib.fm_sum_parts(0, nul, 8, nul, nul) == fm.FM_ERR_INVALID_ARG
+    assert lib.fm_sum_parts(9, nul, 8, nul, nul) == fm.FM_ERR_INVALID_ARG
+    assert lib.fm_sum_parts(2, nul, 8, nul, nul) == fm.FM_ERR_INVALID_ARG
 
 
 def test_rectangular_problem_shapes(lib):
