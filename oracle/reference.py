@@ -19,9 +19,12 @@ slow and written straight from the definitions:
   generalised to intervals that do not reach the sequence edge;
 * localization is the clip-shift-max map of FlashMask-3 project page, §3.2;
 * the FlashMask Guide's FMS / FME vectors (one inclusive visible interval per
-  key column) map onto the four vectors as the complement of that interval.
+  key column) map onto the four vectors as the complement of that interval;
+  its multi-interval masks (up to M visible intervals per key column) are
+  evaluated directly (`multi_masked_rows`).
 
-Readings where the pages are silent (all pinned by tests/test_oracle.py):
+Readings where the pages are silent (pinned by tests/test_oracle.py,
+tests/test_cp_oracle.py and tests/test_convert_oracle.py):
   - intervals are half-open row ranges; start >= end is an empty interval;
   - causal masks i < j (the diagonal is visible);
   - a fully-masked query row has O = 0 and LSE = -inf and contributes no
@@ -31,7 +34,9 @@ Readings where the pages are silent (all pinned by tests/test_oracle.py):
   - the vectors are (B, N_kv), one entry per key column, shared by every head;
     the query rows may number N != N_kv (one rank of a context-parallel split:
     its own rows against every key, FlashMask-3 project page, §3.2), with
-    causal comparing the problem's own row and key indices.
+    causal comparing the problem's own row and key indices;
+  - a mask may also be given per query head ({"heads": four (B, H_q, N_kv)
+    arrays}) or as multi-interval vectors ({"fms", "fme"}: (B, M, N_kv)).
 
 Precision: every input is widened to float64; all arithmetic is float64.
 """
