@@ -13,7 +13,8 @@ work, not the length") and the "IPO phase ablation" table of §4:
   Phi = max_j L_j, and LB = max(ceil(sum w / P), max w) is a lower bound:
   an assignment with Phi == LB is optimal (the certificate);
 * Stage 1 runs LPT, then exact pairwise repartition (P2), then exact
-  three-rank repartition (P3).
+  three-rank repartition (P3);
+* the K / V exchange sends a rank only the chunks its rows can see (§3.4).
 
 A second lower bound uses the cardinality constraint that LB ignores (a
 pigeonhole argument, not on the pages): the m lightest chunks are held by at
@@ -70,6 +71,25 @@ def chunk_loads(tile_class, blocks_per_chunk: int, cost_partial: int, cost_unmas
                 elif t == UNMASKED:
                     w[c] += cost_unmasked
     return w
+
+
+def needed_chunks(tile_class, owner, P: int, blocks_per_chunk: int) -> np.ndarray:
+    """Mask-aware pruning of the K / V exchange (FlashMask-3 project page,
+    §3.4: a chunk the mask fully hides is never sent): need[r, c] = 1 iff some
+    tile between the query blocks of rank r's chunks and the key blocks of
+    chunk c, in any batch entry, is not skipped. Chunks cut both axes alike
+    (a chunk is a range of tokens: its query rows and its keys)."""
+    tile_class = np.asarray(tile_class)
+    B, nq, nk = tile_class.shape
+    n = len(owner)
+    need = np.zeros((P, n), dtype=np.uint8)
+    for b in range(B):
+        for qb in range(nq):
+            r = owner[qb // blocks_per_chunk]
+            for kb in range(nk):
+                if tile_class[b, qb, kb] != SKIP:
+                    need[r, kb // blocks_per_chunk] = 1
+    return need
 
 
 def lower_bound(w, P: int) -> int:

@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 from oracle import balance as ob
-from workloads import chunks
+from workloads import chunks, masks
 
 
 def brute_optimum(w, P, kappa):
@@ -67,7 +67,7 @@ def test_cardinality_bound_hand_values():
     assert ob.lower_bound_kappa([5, 1, 1, 1], 2, 2) == 6 == brute_optimum([5, 1, 1, 1], 2, 2)
     # one light chunk among equal ones (a sliding-window mask's chunks): every
     # rank without the light chunk carries kappa full chunks
-    P, kappa, x, y = 4, 3, 10, 4
+    P, kappa, x, y = 3, 3, 10, 4
     w = [y] + [x] * (P * kappa - 1)
     assert ob.lower_bound(w, P) == -(-(P * kappa * x - (x - y)) // P) < kappa * x
     assert ob.lower_bound_kappa(w, P, kappa) == kappa * x == brute_optimum(w, P, kappa)
@@ -176,3 +176,41 @@ def test_table_lpt_statistic_causal():
         cert += rep["certified"]
         sub += rep["makespan_lpt"] > rep["lower_bound_kappa"]
     assert cert == 4 and sub >= 3
+
+
+def test_needed_chunks_causal_closed_form():
+    # causal, contiguous chunks: a rank needs exactly the chunks at or before
+    # its last own chunk (every key at or before a row is visible to it)
+    n, C, P = 1024, 128, 4
+    cls = oracle.classify_tiles(*causal_vectors(n), True, 128, 128)[None]
+    owner = [0, 1, 2, 3, 3, 2, 1, 0]  # zigzag: rank r owns chunks r and 7 - r
+    need = ob.needed_chunks(cls, owner, P, 1)
+    for r in range(P):
+        last = max(c for c in range(8) if owner[c] == r)
+        assert need[r].tolist() == [1 if c <= last else 0 for c in range(8)]
+
+
+def test_needed_chunks_cover_every_visible_pair():
+    # pruning never drops a chunk holding a key that one of the rank's rows sees
+    rng = np.random.default_rng(6)
+    n, C, P = 256, 32, 4
+    for kind in range(3):
+        if kind == 0:
+            vec = masks.causal_documents(masks.draw_fill(rng, n, 20, 90), n)
+            causal = True
+        elif kind == 1:
+            vec = masks.prefix_lm_documents(masks.draw_fill(rng, n, 30, 120), n)
+            causal = False
+        else:
+            a = rng.integers(0, n + 1, size=(2, n))
+            vec = (a.min(0), a.max(0), np.zeros(n, np.int64), np.zeros(n, np.int64))
+            causal = False
+        vec = tuple(np.asarray(x, np.int32) for x in vec)
+        owner = rng.permutation(np.repeat(np.arange(P), 2)).tolist()
+        need = ob.needed_chunks(oracle.classify_tiles(*vec, causal, C, C)[None], owner, P, 1)
+        vis = ~oracle.dense_mask(*vec, causal)
+        for r in range(P):
+            rows = np.concatenate([np.arange(c * C, (c + 1) * C) for c in range(8) if owner[c] == r])
+            for c in range(8):
+                if vis[np.ix_(rows, np.arange(c * C, (c + 1) * C))].any():
+                    assert need[r, c] == 1
