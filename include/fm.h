@@ -286,6 +286,16 @@ fm_status fm_chunk_loads(const uint8_t* tile_class, int32_t B, int32_t nQ, int32
 fm_status fm_balance_chunks(const int64_t* w, int32_t n_chunks, int32_t P, int32_t kappa, int32_t phases,
                             int64_t node_budget, int32_t* owner, fm_balance_report* report);
 
+/* Mask-aware pruning of the K / V exchange (FlashMask-3 project page, §3.4: a
+ * chunk the mask fully hides is never sent). HOST function. Chunks cut both
+ * axes alike (blocks_per_chunk Q blocks and as many KV blocks); owner[c] in
+ * [0, P) is chunk c's rank. need (P x n_chunks uint8, row-major) gets 1 where
+ * some tile between rank r's query blocks and chunk c's key blocks, in any
+ * batch entry of tile_class (B, nQ, nK; fm_classify_tiles classes), is not
+ * skipped: rank r needs chunk c's K / V rows, and only those. */
+fm_status fm_needed_chunks(const uint8_t* tile_class, int32_t B, int32_t nQ, int32_t nK, const int32_t* owner,
+                           int32_t n_chunks, int32_t P, int32_t blocks_per_chunk, uint8_t* need);
+
 /* ---------------------------------------------------------------------------
  * Device error word. Synchronizes `stream`, returns the accumulated FM_DEVERR_*
  * bits in *bits (may be NULL) and clears them. Status: FM_OK when no bit is

@@ -10,7 +10,8 @@ Functions carry the names of the C entry points:
   fm_classify_tiles, fm_attn_fwd, fm_attn_bwd, fm_localize, fm_device_status,
   fm_selftest_wait_timeout, fm_profile_enable, fm_profile_read, fm_launch_count,
   fm_from_fms_fme, fm_merge_parts, fm_sum_parts, fm_chunk_loads,
-  fm_balance_chunks (host code: the chunk balancer for context parallelism);
+  fm_balance_chunks, fm_needed_chunks (host code: the chunk balancer and the
+  K / V exchange plan for context parallelism);
 plus fm_attn_multi_interval and fm_attn_per_head (multi-interval and per-head
 masks as sequences of library calls) and flashmask_attention (autograd wrapper: the classification, forward
 and backward calls in one differentiable op).
@@ -84,6 +85,8 @@ _SIGS = {
                                       ctypes.c_int64, ctypes.c_int64, _P]),
     "fm_balance_chunks": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int64, _P, ctypes.POINTER(fm_balance_report)]),
+    "fm_needed_chunks": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, ctypes.c_int32,
+                                        ctypes.c_int32, ctypes.c_int32, _P]),
 }
 EXPORTS = tuple(_SIGS)
 
@@ -393,6 +396,20 @@ def fm_chunk_loads(tile_class, blocks_per_chunk: int, cost_partial: int, cost_un
                                 int(cost_partial), int(cost_unmasked), ctypes.c_void_p(w.ctypes.data)),
            "fm_chunk_loads")
     return w
+
+
+def fm_needed_chunks(tile_class, owner, P: int, blocks_per_chunk: int) -> np.ndarray:
+    """(P, n_chunks) uint8: 1 where rank r's rows can see some key of chunk c."""
+    cls = _host_array(tile_class, np.uint8)
+    own = _host_array(np.asarray(owner, dtype=np.int32) if not isinstance(owner, torch.Tensor) else owner, np.int32)
+    if cls.ndim != 3:
+        raise ValueError("tile_class must be (B, nQ, nK)")
+    B, nq, nk = cls.shape
+    need = np.empty((int(P), own.size), dtype=np.uint8)
+    _check(lib().fm_needed_chunks(ctypes.c_void_p(cls.ctypes.data), B, nq, nk, ctypes.c_void_p(own.ctypes.data),
+                                  own.size, int(P), int(blocks_per_chunk), ctypes.c_void_p(need.ctypes.data)),
+           "fm_needed_chunks")
+    return need
 
 
 def fm_balance_chunks(w, P: int, kappa: int, phases: int = 3, node_budget: int = 0):

@@ -323,6 +323,29 @@ extern "C" fm_status fm_chunk_loads(const uint8_t* tile_class, int32_t B, int32_
   return FM_OK;
 }
 
+// Mask-aware pruning of the K / V exchange (FlashMask-3 project page, §3.4:
+// a chunk the mask fully hides is never sent): need[r * n_chunks + c] = 1 iff
+// some tile between the query blocks of rank r's chunks and the key blocks of
+// chunk c is not skipped, in any batch entry.
+extern "C" fm_status fm_needed_chunks(const uint8_t* tile_class, int32_t B, int32_t nQ, int32_t nK,
+                                      const int32_t* owner, int32_t n_chunks, int32_t P, int32_t blocks_per_chunk,
+                                      uint8_t* need) {
+  if (!tile_class || !owner || !need || B < 1 || nQ < 1 || nK < 1 || P < 1 || blocks_per_chunk < 1)
+    return FM_ERR_INVALID_ARG;
+  if ((int64_t)n_chunks * blocks_per_chunk < nQ || (int64_t)n_chunks * blocks_per_chunk < nK) return FM_ERR_INVALID_ARG;
+  for (int c = 0; c < n_chunks; ++c)
+    if (owner[c] < 0 || owner[c] >= P) return FM_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < (int64_t)P * n_chunks; ++i) need[i] = 0;
+  for (int b = 0; b < B; ++b)
+    for (int qb = 0; qb < nQ; ++qb) {
+      uint8_t* row_need = need + (int64_t)owner[qb / blocks_per_chunk] * n_chunks;
+      const uint8_t* row = tile_class + ((int64_t)b * nQ + qb) * nK;
+      for (int kb = 0; kb < nK; ++kb)
+        if (row[kb] != 0) row_need[kb / blocks_per_chunk] = 1;
+    }
+  return FM_OK;
+}
+
 extern "C" fm_status fm_balance_chunks(const int64_t* w, int32_t n_chunks, int32_t P, int32_t kappa,
                                        int32_t phases, int64_t node_budget, int32_t* owner,
                                        fm_balance_report* report) {

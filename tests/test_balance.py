@@ -145,3 +145,36 @@ def test_large_instance_is_fast():
     assert np.bincount(owner, minlength=64).tolist() == [16] * 64
     assert rep["makespan"] <= rep["makespan_pair"] <= rep["makespan_lpt"]
     assert dt < 30.0
+
+
+def test_needed_chunks_match_oracle():
+    rng = np.random.default_rng(11)
+    for B, nq, bpc, P in [(1, 16, 2, 4), (2, 24, 3, 2), (3, 9, 1, 3)]:
+        n = -(-nq // bpc)
+        cls = rng.choice(np.array([0, 0, 0, 1, 2], np.uint8), size=(B, nq, nq))
+        owner = rng.integers(0, P, size=n).astype(np.int32)
+        assert np.array_equal(fm.fm_needed_chunks(cls, owner, P, bpc), ob.needed_chunks(cls, owner.tolist(), P, bpc))
+    with pytest.raises(fm.FMError):
+        fm.fm_needed_chunks(np.zeros((1, 8, 8), np.uint8), np.array([0, 5], np.int32), 2, 4)  # owner out of range
+    with pytest.raises(fm.FMError):
+        fm.fm_needed_chunks(np.zeros((1, 8, 8), np.uint8), np.array([0], np.int32), 2, 4)  # too few chunks
+
+
+@pytest.mark.parametrize("name,P", [("doc8k", 8), ("prefix_lm64k", 8)])
+def test_pruned_exchange_on_document_masks(name, P):
+    """The page reports that pruning drops about half of the all-gather /
+    reduce-scatter traffic on causal and prefix-LM document masks. With the
+    balancer's deal (kappa = 4), the share of remote chunks a rank does not
+    need on these workloads is recorded here as a regression bound."""
+    cfg = configs.make(name)
+    vec = tuple(cfg[k][0] for k in ("lts", "lte", "uts", "ute"))
+    cls = oracle.classify_tiles(*vec, cfg["causal"], 128, 128)[None]
+    kappa = 4
+    nq = cls.shape[1]
+    bpc = nq // (P * kappa)
+    owner, _ = fm.fm_balance_chunks(fm.fm_chunk_loads(cls, bpc, 13, 10), P, kappa)
+    need = fm.fm_needed_chunks(cls, owner, P, bpc)
+    remote = np.ones_like(need, dtype=bool)
+    remote[owner, np.arange(owner.size)] = False  # a rank's own chunks are not sent
+    saved = 1.0 - need[remote].sum() / remote.sum()
+    assert saved > 0.3, saved
