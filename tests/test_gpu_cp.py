@@ -1,9 +1,10 @@
 """Rectangular problems (N query rows against N_kv keys) against the oracle,
 and a context-parallel split emulated on one GPU (FlashMask-3 project page,
-§3.2 and §3.3): the balancer deals the query chunks to ranks, each rank's
-vectors are localized to its rows by fm_localize, each rank runs the forward
-and backward on its own rows against every key, and the ranks' outputs and
-summed key gradients match the whole problem."""
+§3.2-3.4): the balancer deals the query chunks to ranks, each rank's vectors
+are localized to its rows by fm_localize, each rank gets only the K / V chunks
+its rows can see (the others zero) and runs the forward and backward on its own
+rows against the keys, and the ranks' outputs and summed key gradients match
+the whole problem."""
 import numpy as np
 import pytest
 import torch
@@ -80,6 +81,9 @@ def test_cp_split_on_one_gpu(name):
     w = fm.fm_chunk_loads(qs.tile_class, C // 128, 13, 10)
     owner, rep = fm.fm_balance_chunks(w, P, kappa)
     assert np.bincount(owner, minlength=P).tolist() == [kappa] * P
+    # each rank receives only the K / V chunks its rows can see (mask-aware
+    # pruning of the exchange); the chunks it does not receive stay zero
+    need = fm.fm_needed_chunks(qs.tile_class, owner, P, C // 128)
     flat = torch.cat([x.reshape(-1) for x in gvec])
     dk_sum = torch.zeros_like(dk, dtype=torch.float32)
     dv_sum = torch.zeros_like(dv, dtype=torch.float32)
@@ -95,9 +99,12 @@ def test_cp_split_on_one_gpu(name):
         tr = torch.from_numpy(rows).cuda()
         q_r = qd[:, :, tr].contiguous()
         do_r = dod[:, :, tr].contiguous()
+        keep = torch.from_numpy(np.repeat(need[r].astype(bool), C)).cuda()
+        k_r = torch.where(keep[None, None, :, None], kd, torch.zeros_like(kd))
+        v_r = torch.where(keep[None, None, :, None], vd, torch.zeros_like(vd))
         qs_r = fm.fm_classify_tiles(*lvec, causal=False, n_rows=len(rows))
-        o_r, lse_r = fm.fm_attn_fwd(q_r, kd, vd, *lvec, qs_r, scale=scale, causal=False)
-        dq_r, dk_r, dv_r = fm.fm_attn_bwd(q_r, kd, vd, o_r, lse_r, do_r, *lvec, qs_r, scale=scale, causal=False)
+        o_r, lse_r = fm.fm_attn_fwd(q_r, k_r, v_r, *lvec, qs_r, scale=scale, causal=False)
+        dq_r, dk_r, dv_r = fm.fm_attn_bwd(q_r, k_r, v_r, o_r, lse_r, do_r, *lvec, qs_r, scale=scale, causal=False)
         st, bits = fm.fm_device_status()
         assert st == fm.FM_OK, bits
         assert_out(f64(o_r), O_ref[:, :, rows])
