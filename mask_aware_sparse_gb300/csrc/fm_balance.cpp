@@ -351,12 +351,9 @@ extern "C" fm_status fm_balance_chunks(const int64_t* w, int32_t n_chunks, int32
                                        fm_balance_report* report) {
   if (!w || !owner || P < 1 || kappa < 1 || phases < 1 || phases > 3) return FM_ERR_INVALID_ARG;
   if (static_cast<int64_t>(P) * kappa != n_chunks) return FM_ERR_INVALID_ARG;
-  int64_t total = 0;
-  for (int i = 0; i < n_chunks; ++i) {
+  // loads >= 0 and small enough that no sum of them can overflow
+  for (int i = 0; i < n_chunks; ++i)
     if (w[i] < 0 || w[i] > LLONG_MAX / 4 / n_chunks) return FM_ERR_INVALID_ARG;
-    total += w[i];
-  }
-  (void)total;
   // a repartition tracks its pool in one 64-bit mask
   if ((phases >= 2 && P >= 2 && 2 * kappa > 64) || (phases >= 3 && P >= 3 && 3 * kappa > 64))
     return FM_ERR_UNSUPPORTED;
