@@ -602,13 +602,19 @@ def run_balance(args):
                 (owner, rep), ms = _time_call(lambda: fm.fm_balance_chunks(w, P, kappa))
                 avg = float(w.sum()) / P
                 contiguous = np.repeat(np.arange(P), kappa)
+                # mask-aware pruning of the K / V exchange: remote chunks a rank's rows never see
+                need = fm.fm_needed_chunks(cls, owner, P, bpc)
+                remote = np.ones(need.shape, dtype=bool)
+                remote[owner, np.arange(owner.size)] = False
+                pruned = 1.0 - float(need[remote].sum()) / float(remote.sum())
                 cases.append(dict(workload=name, P=P, kappa=kappa, q_blocks_per_chunk=bpc,
                                   peak_over_avg=dict(contiguous=_rank_peak(w, contiguous, P) / avg,
                                                      zigzag=_rank_peak(w, _zigzag_owner(P, kappa), P) / avg,
                                                      lpt=rep["makespan_lpt"] / avg, ipo=rep["makespan"] / avg,
                                                      lower_bound=rep["lower_bound"] / avg,
                                                      lower_bound_kappa=rep["lower_bound_kappa"] / avg),
-                                  certified=rep["certified"], ms_per_call=ms))
+                                  certified=rep["certified"], ms_per_call=ms,
+                                  pruned_remote_chunk_fraction=pruned))
     table = {}
     for name, (kind, n, P, kappa, w_max, inst) in chunks.TABLE.items():
         rng = np.random.default_rng(0)
