@@ -132,3 +132,25 @@ def test_workspace_queries(lib):
     assert lib.fm_classify_workspace_bytes(ctypes.byref(p), ctypes.byref(t)) > 0
     assert lib.fm_attn_fwd_workspace_bytes(ctypes.byref(p)) >= 4 * 256
     assert lib.fm_attn_bwd_workspace_bytes(ctypes.byref(p)) > 0
+
+
+def test_binding_refuses_host_tensors(lib):
+    # the product path runs on the GPU only: host tensors are refused up front,
+    # never computed some other way
+    import torch
+
+    q = torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    vec = [torch.zeros(1, 128, dtype=torch.int32) for _ in range(4)]
+    with pytest.raises(ValueError):
+        fm.fm_classify_tiles(*vec, causal=True)
+    with pytest.raises(ValueError):
+        fm.fm_attn_fwd(q, k, k, *vec, None, scale=0.125, causal=True)
+    with pytest.raises(ValueError):
+        fm.fm_attn_per_head(q, k, k, *[torch.zeros(1, 2, 128, dtype=torch.int32)] * 4, causal=True, scale=0.125)
+    with pytest.raises(ValueError):
+        fm.fm_from_fms_fme(vec[0], vec[1])
+    with pytest.raises(ValueError):
+        fm.fm_merge_parts([q], [torch.zeros(1, 2, 127)])  # LSE shape must be O's without d
+    with pytest.raises(ValueError):
+        fm.fm_sum_parts([q, k])  # parts of different shapes
