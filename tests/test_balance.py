@@ -178,3 +178,16 @@ def test_pruned_exchange_on_document_masks(name, P):
     remote[owner, np.arange(owner.size)] = False  # a rank's own chunks are not sent
     saved = 1.0 - need[remote].sum() / remote.sum()
     assert saved > 0.3, saved
+
+
+@pytest.mark.parametrize("P,kappa", [(4, 6), (3, 8)])
+def test_pairwise_phase_matches_oracle_on_wider_ranks(P, kappa):
+    # the pairwise phase at larger kappa (the oracle enumerates C(2 kappa, kappa) deals per pair)
+    rng = np.random.default_rng(P * 10 + kappa)
+    for it in range(3):
+        w = chunks.random_loads(rng, "uniform" if it % 2 == 0 else "causal", P * kappa, 300)
+        owner, rep = fm.fm_balance_chunks(w, P, kappa, phases=2)
+        o_ref, r_ref = ob.ipo(w, P, kappa, phases=2)
+        assert owner.tolist() == o_ref
+        rep.pop("budget_exhausted")
+        assert rep == r_ref
