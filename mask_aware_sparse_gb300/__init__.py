@@ -131,16 +131,83 @@ def _problem(B, H_q, H_kv, N, d, scale, causal, N_kv=0) -> fm_problem:
     return fm_problem(int(B), int(H_q), int(H_kv), int(N), int(d), float(scale), 1 if causal else 0, int(N_kv))
 
 
-def _vec_ok(*vs):
-    for v in vs:
-        if v.dtype != torch.int32 or not v.is_contiguous() or not v.is_cuda:
-            raise ValueError("mask vectors must be contiguous int32 CUDA tensors of shape (B, N_kv)")
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _like(t, name, shape, dtype):
+    """t is a contiguous torch tensor of this shape and dtype (device checked separately)."""
+    _need(isinstance(t, torch.Tensor), f"{name} must be a torch tensor")
+    _need(tuple(t.shape) == tuple(shape), f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+    _need(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def _same_cuda(**ts):
+    """Every given tensor lives on one CUDA device (the library computes on the GPU only)."""
+    dev = None
+    for name, t in ts.items():
+        if t is None:
+            continue
+        _need(t.is_cuda, f"{name} must be a CUDA tensor: the library computes on the GPU only")
+        dev = t.device if dev is None else dev
+        _need(t.device == dev, f"{name} is on {t.device}, the other tensors on {dev}")
+
+
+def _vec_ok(*vs, shape=None):
+    """Mask vectors: contiguous int32 CUDA tensors of one (B, N_kv) shape."""
+    shape = tuple(vs[0].shape) if shape is None else tuple(shape)
+    _need(len(shape) == 2, "mask vectors must be (B, N_kv)")
+    for i, v in enumerate(vs):
+        _like(v, f"mask vector {i}", shape, torch.int32)
+    _same_cuda(**{f"mask vector {i}": v for i, v in enumerate(vs)})
 
 
 def _bf16_ok(*ts):
     for t in ts:
-        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda or t.dim() != 4:
-            raise ValueError("Q/K/V/O/dO must be contiguous bf16 CUDA tensors of shape (B, H, N, d)")
+        _need(isinstance(t, torch.Tensor) and t.dim() == 4,
+              "Q/K/V/O/dO must be contiguous bf16 CUDA tensors of shape (B, H, N, d)")
+        _like(t, "Q/K/V/O/dO", t.shape, torch.bfloat16)
+    _same_cuda(**{f"tensor {i}": t for i, t in enumerate(ts)})
+
+
+def _attn_args(q, k, v, vec, queues, *, backward, o=None, lse=None, do=None, dq=None, dk=None, dv=None, ws=None):
+    """Shapes, dtypes and devices of an attention call, checked before the library
+    sees any pointer (the C ABI receives bare pointers and cannot check them).
+    Shape checks come first, so a mismatch is reported as such."""
+    _need(isinstance(q, torch.Tensor) and q.dim() == 4, "q must be a (B, H_q, N, d) tensor")
+    B, Hq, N, d = q.shape
+    _need(isinstance(k, torch.Tensor) and k.dim() == 4 and k.shape[0] == B and k.shape[3] == d,
+          f"k has shape {tuple(k.shape)}, expected (B={B}, H_kv, N_kv, d={d})")
+    Hkv, Nk = k.shape[1], k.shape[2]
+    _need(Hkv > 0 and Hq % Hkv == 0, f"H_q={Hq} must be a multiple of H_kv={Hkv}")
+    _like(q, "q", (B, Hq, N, d), torch.bfloat16)
+    _like(k, "k", (B, Hkv, Nk, d), torch.bfloat16)
+    _like(v, "v", (B, Hkv, Nk, d), torch.bfloat16)
+    for i, x in enumerate(vec):
+        _like(x, f"mask vector {i}", (B, Nk), torch.int32)
+    for name, t in (("o", o), ("do", do), ("dq", dq)):
+        if t is not None:
+            _like(t, name, (B, Hq, N, d), torch.bfloat16)
+    if lse is not None:
+        _like(lse, "lse", (B, Hq, N), torch.float32)
+    for name, t in (("dk", dk), ("dv", dv)):
+        if t is not None:
+            _like(t, name, (B, Hkv, Nk, d), torch.bfloat16)
+    if ws is not None:
+        _need(isinstance(ws, torch.Tensor) and ws.is_contiguous(), "ws must be a contiguous tensor")
+    _need(isinstance(queues, TileQueues), "queues must come from fm_classify_tiles")
+    bm, bn = attn_tiling()
+    _need((queues.block_m, queues.block_n) == (bm, bn),
+          f"queues were built with {queues.block_m} x {queues.block_n} tiles; the kernels need {bm} x {bn}")
+    nq, nk = -(-N // bm), -(-Nk // bn)
+    off, qu, nrows = (queues.k_off, queues.k_queue, B * nk) if backward else (queues.q_off, queues.q_queue, B * nq)
+    _like(off, "queue offsets", (nrows + 1,), torch.int32)
+    _need(isinstance(qu, torch.Tensor) and qu.dtype == torch.int32 and qu.is_contiguous()
+          and qu.numel() >= max(1, B * nq * nk), "queue entries must be int32 with capacity B * nQ * nK")
+    _same_cuda(q=q, k=k, v=v, o=o, lse=lse, do=do, dq=dq, dk=dk, dv=dv, ws=ws, queue_offsets=off, queue=qu,
+               **{f"mask vector {i}": x for i, x in enumerate(vec)})
 
 
 def attn_tiling():
@@ -194,8 +261,7 @@ def fm_classify_tiles(lts, lte, uts, ute, *, causal: bool, block_m: int = 128, b
 def fm_attn_fwd(q, k, v, lts, lte, uts, ute, queues: TileQueues, *, scale: float, causal: bool, o=None, lse=None,
                 ws=None, stream=None):
     """Forward: returns (O bf16 (B,H_q,N,d), LSE fp32 (B,H_q,N)); K, V may hold N_kv != N rows."""
-    _bf16_ok(q, k, v)
-    _vec_ok(lts, lte, uts, ute)
+    _attn_args(q, k, v, (lts, lte, uts, ute), queues, backward=False, o=o, lse=lse, ws=ws)
     B, Hq, N, d = q.shape
     prob = _problem(B, Hq, k.shape[1], N, d, scale, causal, k.shape[2])
     o = torch.empty_like(q) if o is None else o
@@ -212,8 +278,8 @@ def fm_attn_fwd(q, k, v, lts, lte, uts, ute, queues: TileQueues, *, scale: float
 def fm_attn_bwd(q, k, v, o, lse, do, lts, lte, uts, ute, queues: TileQueues, *, scale: float, causal: bool,
                 dq=None, dk=None, dv=None, ws=None, stream=None):
     """Backward: returns (dQ, dK, dV) bf16."""
-    _bf16_ok(q, k, v, o, do)
-    _vec_ok(lts, lte, uts, ute)
+    _attn_args(q, k, v, (lts, lte, uts, ute), queues, backward=True, o=o, lse=lse, do=do, dq=dq, dk=dk, dv=dv,
+               ws=ws)
     B, Hq, N, d = q.shape
     prob = _problem(B, Hq, k.shape[1], N, d, scale, causal, k.shape[2])
     dq = torch.empty_like(q) if dq is None else dq
@@ -230,8 +296,12 @@ def fm_attn_bwd(q, k, v, o, lse, do, lts, lte, uts, ute, queues: TileQueues, *, 
 
 def fm_localize(x, chunk_off, C: int, out=None, stream=None):
     """Rank-local boundaries of any int32 boundary values x for chunks at chunk_off (ascending)."""
-    if x.dtype != torch.int32 or chunk_off.dtype != torch.int32 or not x.is_contiguous():
-        raise ValueError("x and chunk_off must be contiguous int32 CUDA tensors")
+    _like(x, "x", x.shape, torch.int32)
+    _need(chunk_off.dim() == 1, "chunk_off must be one-dimensional")
+    _like(chunk_off, "chunk_off", chunk_off.shape, torch.int32)
+    if out is not None:
+        _like(out, "out", x.shape, torch.int32)
+    _same_cuda(x=x, chunk_off=chunk_off, out=out)
     out = torch.empty_like(x) if out is None else out
     _check(lib().fm_localize(_ptr(x), ctypes.c_int64(x.numel()), _ptr(chunk_off), int(chunk_off.numel()), int(C),
                              _ptr(out), _stream(stream)), "fm_localize")
@@ -242,8 +312,10 @@ def fm_from_fms_fme(fms, fme, n_rows=None, stream=None):
     """(lts, lte, uts, ute) for the FlashMask Guide's inclusive visible intervals
     [FMS_j, FME_j] (int32 CUDA tensors of one shape, e.g. (B, N_kv)); use the
     result with causal=False. n_rows: query rows N (default: the last dimension)."""
-    if fms.dtype != torch.int32 or fme.dtype != torch.int32 or fms.shape != fme.shape or not fms.is_cuda:
-        raise ValueError("fms and fme must be int32 CUDA tensors of the same shape")
+    _need(isinstance(fms, torch.Tensor) and isinstance(fme, torch.Tensor) and fms.shape == fme.shape,
+          "fms and fme must be tensors of the same shape")
+    _need(fms.dtype == torch.int32 and fme.dtype == torch.int32, "fms and fme must be int32")
+    _same_cuda(fms=fms, fme=fme)
     fms, fme = fms.contiguous(), fme.contiguous()
     n = fms.shape[-1] if n_rows is None else int(n_rows)
     out = [torch.empty_like(fms) for _ in range(4)]
@@ -258,30 +330,39 @@ def _ptr_array(ts):
 
 def fm_merge_parts(o_parts, lse_parts, o=None, lse=None, stream=None):
     """Log-sum-exp merge of M partial attentions (bf16 O_m, fp32 LSE_m of one shape each)."""
-    if len(o_parts) != len(lse_parts) or not o_parts:
-        raise ValueError("one LSE per O part")
-    for t in o_parts:
-        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != o_parts[0].shape:
-            raise ValueError("O parts must be contiguous bf16 tensors of one shape")
-    for t in lse_parts:
-        if t.dtype != torch.float32 or not t.is_contiguous() or t.shape != o_parts[0].shape[:-1]:
-            raise ValueError("LSE parts must be contiguous fp32 tensors of O's shape without d")
+    _need(len(o_parts) == len(lse_parts) and len(o_parts) > 0, "one LSE per O part")
+    oshape = tuple(o_parts[0].shape)
+    _need(len(oshape) >= 1, "O parts must have a head dimension")
+    for i, t in enumerate(o_parts):
+        _like(t, f"O part {i}", oshape, torch.bfloat16)
+    for i, t in enumerate(lse_parts):
+        _like(t, f"LSE part {i}", oshape[:-1], torch.float32)
+    if o is not None:
+        _like(o, "o", oshape, torch.bfloat16)
+    if lse is not None:
+        _like(lse, "lse", oshape[:-1], torch.float32)
+    _same_cuda(o=o, lse=lse, **{f"O part {i}": t for i, t in enumerate(o_parts)},
+               **{f"LSE part {i}": t for i, t in enumerate(lse_parts)})
     o = torch.empty_like(o_parts[0]) if o is None else o
     lse = torch.empty_like(lse_parts[0]) if lse is None else lse
-    d = o_parts[0].shape[-1]
+    d = oshape[-1]
     _check(lib().fm_merge_parts(len(o_parts), _ptr_array(o_parts), _ptr_array(lse_parts),
-                                ctypes.c_int64(lse.numel()), d, _ptr(o), _ptr(lse), _stream(stream)),
+                                ctypes.c_int64(lse_parts[0].numel()), d, _ptr(o), _ptr(lse), _stream(stream)),
            "fm_merge_parts")
     return o, lse
 
 
 def fm_sum_parts(parts, out=None, stream=None):
     """Elementwise sum of bf16 tensors of one shape (fp32 accumulation, one rounding)."""
-    for t in parts:
-        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != parts[0].shape:
-            raise ValueError("parts must be contiguous bf16 tensors of one shape")
+    _need(len(parts) > 0, "at least one part")
+    shape = tuple(parts[0].shape)
+    for i, t in enumerate(parts):
+        _like(t, f"part {i}", shape, torch.bfloat16)
+    if out is not None:
+        _like(out, "out", shape, torch.bfloat16)
+    _same_cuda(out=out, **{f"part {i}": t for i, t in enumerate(parts)})
     out = torch.empty_like(parts[0]) if out is None else out
-    _check(lib().fm_sum_parts(len(parts), _ptr_array(parts), ctypes.c_int64(out.numel()), _ptr(out),
+    _check(lib().fm_sum_parts(len(parts), _ptr_array(parts), ctypes.c_int64(parts[0].numel()), _ptr(out),
                               _stream(stream)), "fm_sum_parts")
     return out
 

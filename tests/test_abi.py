@@ -154,3 +154,94 @@ def test_binding_refuses_host_tensors(lib):
         fm.fm_merge_parts([q], [torch.zeros(1, 2, 127)])  # LSE shape must be O's without d
     with pytest.raises(ValueError):
         fm.fm_sum_parts([q, k])  # parts of different shapes
+
+
+def test_binding_checks_shapes_before_any_library_call(lib):
+    # The C ABI receives bare pointers and cannot see shapes: the binding must
+    # refuse every mismatch before a pointer reaches the library. Shape checks
+    # run before the device check, so these host tensors fail on the shape.
+    import torch
+
+    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+    B, Hq, Hkv, N, d = 1, 4, 2, 256, 64
+    q = torch.zeros(B, Hq, N, d, dtype=bf)
+    k = torch.zeros(B, Hkv, N, d, dtype=bf)
+    vec = [torch.zeros(B, N, dtype=i32) for _ in range(4)]
+    cases = [
+        dict(k=torch.zeros(B, Hkv, N, 2 * d, dtype=bf)),          # K head dim differs from Q
+        dict(k=torch.zeros(B + 1, Hkv, N, d, dtype=bf)),           # K batch differs
+        dict(v=torch.zeros(B, Hkv, N // 2, d, dtype=bf)),          # V rows differ from K
+        dict(k=torch.zeros(B, 3, N, d, dtype=bf), v=torch.zeros(B, 3, N, d, dtype=bf)),  # H_q % H_kv
+        dict(vec=[torch.zeros(B, N + 1, dtype=i32)] * 4),          # vectors not (B, N_kv)
+        dict(vec=[torch.zeros(B, N, dtype=torch.int64)] * 4),      # vectors not int32
+        dict(o=torch.zeros(B, Hq, N + 128, d, dtype=bf)),          # output larger than Q
+        dict(lse=torch.zeros(B, Hq, 2 * N, dtype=f32)),            # LSE larger than (B, H_q, N)
+    ]
+    for c in cases:
+        kk = c.get("k", k)
+        vv = c.get("v", kk if "k" in c else k)
+        with pytest.raises(ValueError, match="shape|multiple|must be torch|expected|int32"):
+            fm.fm_attn_fwd(q, kk, vv, *c.get("vec", vec), None, scale=0.1, causal=True, o=c.get("o"),
+                           lse=c.get("lse"))
+    lse = torch.zeros(B, Hq, N, dtype=f32)
+    bwd_cases = [
+        dict(do=torch.zeros(B, Hq, N, d // 2, dtype=bf)),
+        dict(dq=torch.zeros(B, Hq, N + 1, d, dtype=bf)),
+        dict(dk=torch.zeros(B, Hq, N, d, dtype=bf)),               # dK with H_q heads instead of H_kv
+        dict(dv=torch.zeros(B, Hkv, N, d, dtype=f32)),
+    ]
+    for c in bwd_cases:
+        with pytest.raises(ValueError, match="shape|must be torch"):
+            fm.fm_attn_bwd(q, k, k, q, lse, c.get("do", q), *vec, None, scale=0.1, causal=True,
+                           dq=c.get("dq"), dk=c.get("dk"), dv=c.get("dv"))
+    # all shapes right: the queues object is checked next, then the device
+    with pytest.raises(ValueError, match="fm_classify_tiles"):
+        fm.fm_attn_fwd(q, k, k, *vec, None, scale=0.1, causal=True)
+    nq = N // 128
+    queues = fm.TileQueues(torch.zeros(B, nq, nq, dtype=torch.uint8), torch.zeros(B * nq + 1, dtype=i32),
+                           torch.zeros(B * nq * nq, dtype=i32), torch.zeros(B * nq + 1, dtype=i32),
+                           torch.zeros(B * nq * nq, dtype=i32), 128, 128)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.fm_attn_fwd(q, k, k, *vec, queues, scale=0.1, causal=True)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.fm_attn_bwd(q, k, k, q, lse, q, *vec, queues, scale=0.1, causal=True)
+    short = fm.TileQueues(queues.tile_class, torch.zeros(B * nq, dtype=i32), queues.q_queue, queues.k_off,
+                          queues.k_queue, 128, 128)
+    with pytest.raises(ValueError, match="queue offsets"):
+        fm.fm_attn_fwd(q, k, k, *vec, short, scale=0.1, causal=True)
+    other_tiling = fm.TileQueues(*[getattr(queues, f) for f in ("tile_class", "q_off", "q_queue", "k_off",
+                                                                "k_queue")], 64, 64)
+    with pytest.raises(ValueError, match="tiles"):
+        fm.fm_attn_fwd(q, k, k, *vec, other_tiling, scale=0.1, causal=True)
+
+
+def test_binding_refuses_host_and_mismatched_parts(lib):
+    import torch
+
+    o = torch.zeros(2, 3, 16, 8, dtype=torch.bfloat16)
+    lse = torch.zeros(2, 3, 16, dtype=torch.float32)
+    # host-memory parts: never handed to a kernel as raw pointers
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.fm_merge_parts([o, o], [lse, lse])
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.fm_sum_parts([o, o])
+    # outputs larger or smaller than the parts: the row / element count comes
+    # from the parts, and a mismatched output is refused
+    with pytest.raises(ValueError, match="shape"):
+        fm.fm_merge_parts([o, o], [lse, lse], o=torch.zeros(2, 3, 32, 8, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="shape"):
+        fm.fm_merge_parts([o, o], [lse, lse], lse=torch.zeros(2, 3, 32, dtype=torch.float32))
+    with pytest.raises(ValueError, match="shape"):
+        fm.fm_sum_parts([o, o], out=torch.zeros(2, 3, 16, 16, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="bfloat16"):
+        fm.fm_sum_parts([o, o], out=torch.zeros(2, 3, 16, 8, dtype=torch.float32))
+    # localization and the FMS / FME converter: host tensors are refused
+    x = torch.zeros(64, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.fm_localize(x, torch.zeros(2, dtype=torch.int32), 16)
+    with pytest.raises(ValueError, match="shape"):
+        fm.fm_localize(x, torch.zeros(2, dtype=torch.int32), 16, out=torch.zeros(32, dtype=torch.int32))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.fm_from_fms_fme(x, x)
+    with pytest.raises(ValueError, match="same shape"):
+        fm.fm_from_fms_fme(x, x[:32])

@@ -242,6 +242,108 @@ def test_tile_rule_ragged_edge():
                         assert t.all()
 
 
+# At 1 x 1 tiles the block min and max are the column's own values, so the
+# generalised rule must reproduce the dense mask element for element: skip
+# exactly where masked, unmasked exactly where visible. Soundness pins alone
+# ("skip => all masked", "unmasked => all visible") cannot see a clause written
+# too conservatively; exactness can.
+def _rule_exact_at_1x1(classify, seed=21, n=40, trials=30):
+    rng = np.random.default_rng(seed)
+    for causal in (False, True):
+        for trial in range(trials):
+            vec = _random_vectors(rng, n, general=True)
+            if trial % 3 == 0:  # reversed / empty intervals in both pairs
+                lts, lte, uts, ute = (x.copy() for x in vec)
+                uts[::4], ute[::4] = ute[::4].copy(), uts[::4].copy()
+                vec = (lts, lte, uts, ute)
+            cls = classify(*vec, causal, 1, 1)
+            vis = ~oracle.dense_mask(*vec, causal)
+            want = np.where(vis, oracle.UNMASKED, oracle.SKIP)
+            if not np.array_equal(cls, want):
+                return False
+    return True
+
+
+def _uniform_block_vectors(rng, n, bt):
+    """Vectors whose columns share their four values within each bt-wide block."""
+    nb = n // bt
+    a = rng.integers(0, n + 1, size=(2, nb))
+    c = rng.integers(0, n + 1, size=(2, nb))
+    lts, lte = a.min(0), a.max(0)
+    uts, ute = c.min(0), c.max(0)
+    flip = rng.random(nb) < 0.15
+    lts[flip], lte[flip] = lte[flip], lts[flip]
+    return tuple(np.repeat(x, bt).astype(np.int32) for x in (lts, lte, uts, ute))
+
+
+def _rule_exact_on_uniform_blocks(classify, seed=23, n=64, bt=8, trials=60):
+    """Uniform blocks: the rule's class equals the tile's true class, except in
+    the two places where the rule is conservative by construction: only the
+    union of the masked sets covers the tile (no single term does; the rule
+    tests each term alone), or an empty interval's endpoints straddle the
+    tile's rows (the rule reads an interval by its endpoints). Both then give
+    partial."""
+    rng = np.random.default_rng(seed)
+    for causal in (False, True):
+        for _ in range(trials):
+            vec = _uniform_block_vectors(rng, n, bt)
+            cls = classify(*vec, causal, bt, bt)
+            vis = ~oracle.dense_mask(*vec, causal)
+            for qb in range(n // bt):
+                q0, q1 = qb * bt, (qb + 1) * bt
+                for kb in range(n // bt):
+                    k0, k1 = kb * bt, (kb + 1) * bt
+                    truth = _true_class(vis[q0:q1, k0:k1])
+                    if cls[qb, kb] == truth:
+                        continue
+                    a0, a1, u0, u1 = (int(x[k0]) for x in vec)
+                    one_term_covers = ((a0 <= q0 and q1 <= a1) or (u0 <= q0 and q1 <= u1)
+                                       or (causal and q1 <= k0))
+                    if truth == oracle.SKIP and cls[qb, kb] == oracle.PARTIAL and not one_term_covers:
+                        continue
+                    # an empty interval (start >= end) is judged by its endpoints
+                    # too: one that straddles the tile's rows makes it partial
+                    straddles_empty = any(s >= e and not (q1 <= s or q0 >= e) for s, e in ((a0, a1), (u0, u1)))
+                    if truth == oracle.UNMASKED and cls[qb, kb] == oracle.PARTIAL and straddles_empty:
+                        continue
+                    return False
+    return True
+
+
+def test_tile_rule_exact_at_1x1_tiles():
+    assert _rule_exact_at_1x1(oracle.classify_tiles)
+
+
+def test_tile_rule_exact_on_uniform_blocks():
+    assert _rule_exact_on_uniform_blocks(oracle.classify_tiles)
+
+
+# Conservative slips: each keeps every soundness pin green (the tile is only
+# called partial more often), so only the exactness pins above can catch them.
+_CONSERVATIVE_SLIPS = [
+    ("q1 <= mn_lts[kb] or q0 >= mx_lte[kb]", "q1 <= mn_lts[kb]"),
+    ("q1 <= mn_uts[kb] or q0 >= mx_ute[kb]", "q0 >= mx_ute[kb]"),
+    ("q1 <= mn_uts[kb] or q0 >= mx_ute[kb]", "q1 <= mn_uts[kb]"),
+    ("or (q0 >= mx_uts[kb] and q1 <= mn_ute[kb])", ""),
+    ("(not causal) or q0 >= k1 - 1", "(not causal) or q0 >= k1"),
+]
+
+
+@pytest.mark.parametrize("old,new", _CONSERVATIVE_SLIPS)
+def test_tile_rule_exactness_pins_catch_conservative_slips(old, new):
+    """Plant each slip in a copy of the oracle's classifier (CPU, test-local)."""
+    import inspect
+    import textwrap
+
+    src = textwrap.dedent(inspect.getsource(oracle.classify_tiles))
+    assert old in src
+    ns = dict(vars(oracle.reference))
+    exec(src.replace(old, new), ns)
+    slipped = ns["classify_tiles"]
+    caught = not _rule_exact_at_1x1(slipped) or not _rule_exact_on_uniform_blocks(slipped)
+    assert caught, f"slip not caught: {old!r} -> {new!r}"
+
+
 def test_tiny_tile_counts():
     cfg = configs.make("tiny")
     vec = tuple(x[0] for x in (cfg["lts"], cfg["lte"], cfg["uts"], cfg["ute"]))

@@ -18,7 +18,6 @@ import torch
 import mask_aware_sparse_gb300 as fm
 from workloads import masks, tensors
 
-from helpers import LSE_MAX_ABS, O_MAX_ABS, O_REL_L2, f64, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -41,12 +40,10 @@ def _case(n, hq, hkv, causal, vec_np, seed):
 
 
 def _compare(o, lse, o_ref, lse_ref):
-    a, b = f64(o), f64(o_ref)
-    assert rel_l2(a, b) <= O_REL_L2 and np.abs(a - b).max() <= O_MAX_ABS
-    la, lb = f64(lse), f64(lse_ref)
-    assert np.array_equal(np.isneginf(la), np.isneginf(lb))
-    fin = ~np.isneginf(lb)
-    assert np.abs(la[fin] - lb[fin]).max() <= LSE_MAX_ABS
+    # the same kernel on the same inputs: every unit is computed the same way
+    # whichever CTA takes it, so the results agree bit for bit
+    assert torch.equal(o, o_ref)
+    assert torch.equal(lse, lse_ref)
 
 
 def test_noalloc_forward_matches_forward_twice():
@@ -75,6 +72,24 @@ def test_noalloc_second_problem_after_a_larger_one():
         assert _noalloc(prob, q, k, v, vec, queues, o, lse) == fm.FM_OK
         torch.cuda.synchronize()
         _compare(o, lse, o_ref, lse_ref)
+
+
+def test_noalloc_long_pass_natural_order():
+    # eight or more waves of work units: the forward takes its units in natural
+    # order, so only the work counter of the fixed array is used (no order table)
+    rng = np.random.default_rng(7)
+    n = 32768
+    vec_np = tuple(x[None] for x in masks.causal_documents(masks.draw_fill(rng, n, 256, 2048), n))
+    prob, q, k, v, vec, queues, o_ref, lse_ref = _case(n, 8, 8, True, vec_np, 2)
+    units = 8 * (n // 128)
+    assert units >= 8 * torch.cuda.get_device_properties(0).multi_processor_count
+    for _ in range(2):
+        o = torch.full_like(o_ref, float("nan"))
+        lse = torch.full_like(lse_ref, float("nan"))
+        assert _noalloc(prob, q, k, v, vec, queues, o, lse) == fm.FM_OK
+        torch.cuda.synchronize()
+        _compare(o, lse, o_ref, lse_ref)
+    assert fm.fm_device_status()[0] == fm.FM_OK
 
 
 def test_noalloc_rejects_too_many_q_blocks():
