@@ -225,10 +225,36 @@ def row_probs(q, k, vec, causal, scale, b, h, rows):
     return p, lse
 
 
-def forward(q, k, v, vec, causal: bool, scale: float, heads=None, rows=None, row_chunk: int = 512):
+def row_probs_visible(q, k, vec, causal, scale, b, h, rows):
+    """As `row_probs`, restricted to the key columns that at least one of the
+    given rows sees: returns (P over those columns, LSE, the column indices).
+
+    Every other column is masked for every one of these rows, so its weight
+    exp(-inf) = 0 contributes exactly nothing to O, LSE or any gradient; only
+    the rounding order of the sums changes. This is what lets the oracle reach
+    every row of the long workloads."""
+    g = _kv_head(h, q.shape[1], k.shape[1])
+    m = _mask_rows(vec, causal, b, rows, h)
+    vc = np.nonzero(~m.all(axis=0))[0]
+    s = scale * (q[b, h, rows] @ k[b, g][vc].T)
+    s = np.where(m[:, vc], -np.inf, s)
+    r = s.max(axis=1) if vc.size else np.full(len(rows), -np.inf)
+    empty = np.isneginf(r)
+    r_safe = np.where(empty, 0.0, r)
+    e = np.exp(s - r_safe[:, None])
+    l = e.sum(axis=1)
+    p = e / np.where(empty, 1.0, l)[:, None]
+    lse = np.where(empty, -np.inf, r_safe + np.log(np.where(empty, 1.0, l)))
+    return p, lse, vc
+
+
+def forward(q, k, v, vec, causal: bool, scale: float, heads=None, rows=None, row_chunk: int = 512,
+            visible_only: bool = False):
     """O and LSE for the selected heads and rows.
 
     Returns O of shape (B, len(heads), len(rows), d) and LSE (B, len(heads), len(rows)).
+    visible_only: compute each row chunk over the key columns it sees
+    (`row_probs_visible`), the same result up to rounding order.
     """
     B, Hq, N, d = q.shape
     heads = list(range(Hq)) if heads is None else list(heads)
@@ -240,13 +266,18 @@ def forward(q, k, v, vec, causal: bool, scale: float, heads=None, rows=None, row
             g = _kv_head(h, Hq, k.shape[1])
             for c0 in range(0, len(rows), row_chunk):
                 rr = rows[c0 : c0 + row_chunk]
-                p, lse = row_probs(q, k, vec, causal, scale, b, h, rr)
-                O[b, hi, c0 : c0 + len(rr)] = p @ v[b, g]
+                if visible_only:
+                    p, lse, vc = row_probs_visible(q, k, vec, causal, scale, b, h, rr)
+                    O[b, hi, c0 : c0 + len(rr)] = p @ v[b, g][vc]
+                else:
+                    p, lse = row_probs(q, k, vec, causal, scale, b, h, rr)
+                    O[b, hi, c0 : c0 + len(rr)] = p @ v[b, g]
                 L[b, hi, c0 : c0 + len(rr)] = lse
     return O, L
 
 
-def backward(q, k, v, do, vec, causal: bool, scale: float, heads=None, rows=None, cols=None, row_chunk=256):
+def backward(q, k, v, do, vec, causal: bool, scale: float, heads=None, rows=None, cols=None, row_chunk=256,
+             visible_only: bool = False):
     """Analytic gradients of sum(O * dO).
 
     dQ is returned for the selected `rows` of the selected `heads`:
@@ -257,6 +288,8 @@ def backward(q, k, v, do, vec, causal: bool, scale: float, heads=None, rows=None
     Per row i (one query head): P from `row_probs`; dP_ij = dO_i . v_j;
     D_i = sum_j P_ij dP_ij; dS_ij = P_ij (dP_ij - D_i);
     dQ_i = scale sum_j dS_ij k_j; dV_j += P_ij dO_i; dK_j += scale dS_ij q_i.
+    visible_only: each row chunk over the key columns it sees
+    (`row_probs_visible`); P = dS = 0 on the others.
     """
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
@@ -288,19 +321,30 @@ def backward(q, k, v, do, vec, causal: bool, scale: float, heads=None, rows=None
             g = _kv_head(h, Hq, Hkv)
             for c0 in range(0, len(need), row_chunk):
                 rr = need[c0 : c0 + row_chunk]
-                p, _ = row_probs(q, k, vec, causal, scale, b, h, rr)
-                dp = do[b, h, rr] @ v[b, g].T
+                if visible_only:
+                    p, _, vc = row_probs_visible(q, k, vec, causal, scale, b, h, rr)
+                else:
+                    p, _ = row_probs(q, k, vec, causal, scale, b, h, rr)
+                    vc = np.arange(k.shape[2])
+                dp = do[b, h, rr] @ v[b, g][vc].T
                 D = (p * dp).sum(axis=1)
                 ds = p * (dp - D[:, None])
                 wq = want_q[c0 : c0 + len(rr)]
                 if wq.any():
-                    dq_rows = scale * (ds[wq] @ k[b, g])
+                    dq_rows = scale * (ds[wq] @ k[b, g][vc])
                     for t, r in enumerate(rr[wq]):
                         dQ[b, hi, row_pos[int(r)]] = dq_rows[t]
                 wk = want_kv[c0 : c0 + len(rr)]
                 if wk.any():
-                    dV[b, g] += p[wk][:, cols].T @ do[b, h, rr[wk]]
-                    dK[b, g] += scale * (ds[wk][:, cols].T @ q[b, h, rr[wk]])
+                    # the selected columns among the computed ones (others: P = dS = 0)
+                    pos = np.minimum(np.searchsorted(vc, cols), max(len(vc) - 1, 0))
+                    hit = (vc[pos] == cols) if len(vc) else np.zeros(len(cols), dtype=bool)
+                    p_c = np.zeros((int(wk.sum()), len(cols)))
+                    ds_c = np.zeros_like(p_c)
+                    p_c[:, hit] = p[wk][:, pos[hit]]
+                    ds_c[:, hit] = ds[wk][:, pos[hit]]
+                    dV[b, g] += p_c.T @ do[b, h, rr[wk]]
+                    dK[b, g] += scale * (ds_c.T @ q[b, h, rr[wk]])
     return dQ, dK, dV
 
 

@@ -575,3 +575,79 @@ def test_localize_theorem_1_bruteforce():
 def test_localize_hand_example():
     # chunks of 4 rows at global offsets 0 and 8: global 10 -> 4 + 2 = 6 rows before it
     assert oracle.localize(np.array([10, 0, 3, 4, 8, 12, 20]), [0, 8], 4).tolist() == [6, 0, 3, 4, 4, 8, 8]
+
+
+# ------------------------------------------- visible-columns mode
+# The full-size parity tests run the oracle over only the key columns each row
+# chunk sees (masked columns add exact zeros). It is pinned here against the
+# strict mode and, independently, against torch's own SDPA and autograd.
+def _strict_vs_visible(q, k, v, do, vec, causal, scale, rows=None, cols=None, tol=1e-12):
+    O, L = oracle.forward(q, k, v, vec, causal, scale, rows=rows)
+    Ov, Lv = oracle.forward(q, k, v, vec, causal, scale, rows=rows, visible_only=True, row_chunk=37)
+    assert np.array_equal(np.isneginf(L), np.isneginf(Lv))
+    fin = ~np.isneginf(L)
+    assert np.abs(L[fin] - Lv[fin]).max() <= tol
+    assert np.abs(O - Ov).max() <= tol
+    g = oracle.backward(q, k, v, do, vec, causal, scale, rows=rows, cols=cols)
+    gv = oracle.backward(q, k, v, do, vec, causal, scale, rows=rows, cols=cols, visible_only=True, row_chunk=29)
+    for a, b in zip(g, gv):
+        assert a.shape == b.shape and np.abs(a - b).max() <= tol * max(1.0, np.abs(a).max())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_visible_only_equals_strict_on_general_masks(causal):
+    rng = np.random.default_rng(31)
+    B, hq, hkv, n, d = 2, 4, 2, 96, 16
+    q, k, v, do = (x.numpy() for x in _rand_problem(rng, B, hq, hkv, n, d, seed=7))
+    vec = _stack_vec([_random_vectors(rng, n, True) for _ in range(B)])
+    _strict_vs_visible(q, k, v, do, vec, causal, 0.31)
+    rows = np.sort(rng.choice(n, 20, replace=False))
+    cols = np.sort(rng.choice(n, 12, replace=False))
+    _strict_vs_visible(q, k, v, do, vec, causal, 0.31, rows=rows, cols=cols)
+
+
+def test_visible_only_equals_strict_on_the_workload_families():
+    rng = np.random.default_rng(32)
+    n, d = 512, 32
+    q, k, v, do = (x.numpy() for x in _rand_problem(rng, 1, 2, 1, n, d, seed=8))
+    for t in range(4):
+        vec = _stack_vec([_structured_vectors(rng, n, t)])
+        _strict_vs_visible(q, k, v, do, vec, t != 1, 0.2)
+
+
+def test_visible_only_equals_strict_on_the_tiny_workload():
+    cfg = configs.make("tiny")
+    rng = np.random.default_rng(33)
+    q, k, v, do = (x.numpy() for x in _rand_problem(rng, 1, 2, 2, cfg["N"], cfg["d"], seed=9))
+    vec = (cfg["lts"], cfg["lte"], cfg["uts"], cfg["ute"])
+    _strict_vs_visible(q, k, v, do, vec, True, cfg["scale"])
+
+
+def test_visible_only_per_head_and_multi_interval_forms():
+    rng = np.random.default_rng(34)
+    B, hq, hkv, n, d = 1, 4, 2, 80, 8
+    q, k, v, do = (x.numpy() for x in _rand_problem(rng, B, hq, hkv, n, d, seed=10))
+    heads = tuple(np.stack([np.stack([_random_vectors(rng, n, True)[i] for _ in range(hq)])])
+                  for i in range(4))
+    _strict_vs_visible(q, k, v, do, {"heads": heads}, True, 0.4)
+    cuts = np.sort(rng.integers(0, n, size=(B, 4, n)), axis=1)
+    multi = {"fms": cuts[:, 0::2].astype(np.int32), "fme": cuts[:, 1::2].astype(np.int32)}
+    _strict_vs_visible(q, k, v, do, multi, False, 0.4)
+
+
+def test_visible_only_against_torch_autograd():
+    # independent of the strict mode: torch SDPA + autograd in float64
+    rng = np.random.default_rng(35)
+    B, hq, hkv, n, d = 1, 2, 1, 64, 8
+    q, k, v, do = _rand_problem(rng, B, hq, hkv, n, d, seed=11)
+    vec = _stack_vec([_structured_vectors(rng, n, 0)])
+    vis = ~oracle.dense_mask(*(x[0] for x in vec), True)
+    qq, kk, vv = (x.clone().requires_grad_(True) for x in (q, k, v))
+    out = _torch_sdpa(qq, kk, vv, vis[None], 0.3)
+    out.backward(do)
+    O, _ = oracle.forward(q.numpy(), k.numpy(), v.numpy(), vec, True, 0.3, visible_only=True)
+    dQ, dK, dV = oracle.backward(q.numpy(), k.numpy(), v.numpy(), do.numpy(), vec, True, 0.3, visible_only=True)
+    assert np.allclose(O, out.detach().numpy(), atol=1e-12)
+    assert np.allclose(dQ, qq.grad.numpy(), atol=1e-11)
+    assert np.allclose(dK, kk.grad.numpy(), atol=1e-11)
+    assert np.allclose(dV, vv.grad.numpy(), atol=1e-11)
