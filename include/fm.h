@@ -38,7 +38,7 @@ extern "C" {
 typedef enum fm_status {
   FM_OK = 0,
   FM_ERR_INVALID_ARG = 1, /* null pointer, bad shape, misaligned tensor */
-  FM_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head dim not 64/128) */
+  FM_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. a head dim without a kernel) */
   FM_ERR_WORKSPACE = 3,   /* workspace pointer null or smaller than required */
   FM_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
   FM_ERR_TIMEOUT = 5,     /* device error word: a bounded on-device wait expired */
@@ -129,7 +129,9 @@ fm_status fm_classify_tiles(const fm_problem* p, const fm_tiling* t, const int32
  * A query row with no visible key gets O = 0 and LSE = -inf.
  *
  * q_off / q_queue must come from fm_classify_tiles with the fm_attn_tiling
- * tiling and the same problem and mask. d must be 64 or 128. Mask values
+ * tiling and the same problem and mask. d must be 64, 128 or 256 (256: the
+ * FlashMask Guide's usage example, "Complete PyTorch Implementation",
+ * dim = 256). Mask values
  * outside [0, N] are clamped; the forward does not flag them again
  * (fm_classify_tiles on the same vectors does).
  * Workspace: fm_attn_fwd_workspace_bytes (the unit-order table and a work

@@ -163,8 +163,10 @@ fm_status check_problem(const fm_problem* p, bool* empty) {
   return FM_OK;
 }
 
-fm_status check_attn_shape(const fm_problem* p) {
-  if (p->d != 64 && p->d != 128) return FM_ERR_UNSUPPORTED;
+// Head dimensions with a kernel: the forward takes 64, 128 and 256, the
+// backward 64 and 128.
+fm_status check_attn_shape(const fm_problem* p, bool backward) {
+  if (p->d != 64 && p->d != 128 && (backward || p->d != 256)) return FM_ERR_UNSUPPORTED;
   return FM_OK;
 }
 
@@ -242,7 +244,7 @@ fm_status fm_attn_fwd(const fm_problem* p, const void* q, const void* k, const v
   bool empty = false;
   fm_status st = check_problem(p, &empty);
   if (st != FM_OK || empty) return st;
-  if ((st = check_attn_shape(p)) != FM_OK) return st;
+  if ((st = check_attn_shape(p, false)) != FM_OK) return st;
   if (!q || !k || !v || !lts || !lte || !uts || !ute || !q_off || !q_queue || !o || !lse) return FM_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FM_ERR_INVALID_ARG;
   const size_t need = fwd_ws_bytes(*p);
@@ -259,7 +261,7 @@ fm_status fm_attn_fwd_noalloc(const fm_problem* p, const void* q, const void* k,
   bool empty = false;
   fm_status st = check_problem(p, &empty);
   if (st != FM_OK || empty) return st;
-  if ((st = check_attn_shape(p)) != FM_OK) return st;
+  if ((st = check_attn_shape(p, false)) != FM_OK) return st;
   if (!q || !k || !v || !lts || !lte || !uts || !ute || !q_off || !q_queue || !o || !lse) return FM_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FM_ERR_INVALID_ARG;
   // the fixed scratch holds one entry per Q block of the whole batch
@@ -285,7 +287,7 @@ fm_status fm_attn_bwd(const fm_problem* p, const void* q, const void* k, const v
   bool empty = false;
   fm_status st = check_problem(p, &empty);
   if (st != FM_OK || empty) return st;
-  if ((st = check_attn_shape(p)) != FM_OK) return st;
+  if ((st = check_attn_shape(p, true)) != FM_OK) return st;
   if (!q || !k || !v || !o || !lse || !dout || !lts || !lte || !uts || !ute || !k_off || !k_queue || !dq || !dk ||
       !dv)
     return FM_ERR_INVALID_ARG;

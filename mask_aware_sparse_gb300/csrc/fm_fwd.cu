@@ -773,6 +773,7 @@ size_t fwd_ws_bytes(const fm_problem& p) { return fwd_order_bytes(p) + 256; }
 cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const void* v, const int32_t* lts,
                        const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
                        const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err) {
+  if (P.d == 256) return launch_fwd256(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err);
   const int nQ = (P.N + kTile - 1) / kTile;
   const int G = P.H_q / P.H_kv;
   const int PG = (G + 1) / 2;

@@ -36,6 +36,11 @@ cudaError_t launch_fwd(const fm_problem& p, const void* q, const void* k, const 
                        const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
                        const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err);
 
+// Forward for d = 256 (fm_fwd256.cu): same arguments and workspace as launch_fwd.
+cudaError_t launch_fwd256(const fm_problem& p, const void* q, const void* k, const void* v, const int32_t* lts,
+                          const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
+                          const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err);
+
 // The forward's fixed scratch for fm_attn_fwd_noalloc (fm_fwd.cu): device
 // address of the library-owned launch-order array of the current device, or
 // nullptr if it could not be looked up.
