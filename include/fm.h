@@ -152,7 +152,8 @@ fm_status fm_attn_fwd(const fm_problem* p, const void* q, const void* k, const v
  * of each GQA group. Rows with LSE = -inf contribute nothing.
  *
  * o and lse must be the forward outputs for the same inputs. k_off / k_queue
- * come from fm_classify_tiles with the fm_attn_tiling tiling.
+ * come from fm_classify_tiles with the fm_attn_tiling tiling. d must be 64,
+ * 128 or 256.
  * Workspace: fm_attn_bwd_workspace_bytes (fp32 dQ accumulator, row terms D).
  * ------------------------------------------------------------------------- */
 size_t fm_attn_bwd_workspace_bytes(const fm_problem* p);

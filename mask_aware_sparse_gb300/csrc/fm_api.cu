@@ -163,10 +163,9 @@ fm_status check_problem(const fm_problem* p, bool* empty) {
   return FM_OK;
 }
 
-// Head dimensions with a kernel: the forward takes 64, 128 and 256, the
-// backward 64 and 128.
-fm_status check_attn_shape(const fm_problem* p, bool backward) {
-  if (p->d != 64 && p->d != 128 && (backward || p->d != 256)) return FM_ERR_UNSUPPORTED;
+// Head dimensions with a kernel: 64, 128 and 256.
+fm_status check_attn_shape(const fm_problem* p, bool /*backward*/) {
+  if (p->d != 64 && p->d != 128 && p->d != 256) return FM_ERR_UNSUPPORTED;
   return FM_OK;
 }
 

@@ -15,6 +15,8 @@
 //                    over every query head of the group and every queued Q
 //                    block in two 64-row halves;
 //   dq_convert       dQ = bf16(scale * dQacc).
+// For d = 256 the main kernel is bwd256_kernel (fm_bwd256.cu); the row terms
+// and the conversion are these.
 //
 // bwd_kernel (480 threads):
 //   warps 0-7  compute: thread j of warp w owns KV row j = 32*(w%4) + lane
@@ -701,7 +703,6 @@ template <int D>
 cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, const void* v, const void* o,
                          const float* lse, const void* dout, void* dq, const BwdParams& prm0, const BwdWs& w,
                          cudaStream_t s) {
-  using C = BwdCfg<D>;
   const int nK = prm0.nK;
   const long long BH = (long long)P.B * P.H_q;
   // 1. row terms and a zeroed dQ accumulator
@@ -717,9 +718,15 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   // and 64K workloads; the one-kv-head 128K workload, 6.7 waves, stays LPT,
   // where natural order was 19% slower: its CTAs then reduce into the same
   // dQ rows at once).
-  const bool natural = use_natural_order((long long)P.B * nK * P.H_kv);
+  // (d = 256 runs two CTAs per KV block, one per head-dim half)
+  const bool natural = use_natural_order((D == 256 ? 2LL : 1LL) * P.B * nK * P.H_kv);
   if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(prm0.k_off, P.B * nK, w.order);
   // 3. main kernel
+  if constexpr (D == 256) {
+    e = launch_bwd256_main(P, q, k, v, dout, prm0.lts, prm0.lte, prm0.uts, prm0.ute, prm0.k_off, prm0.k_queue,
+                           natural ? nullptr : w.order, w.nl, w.dsum, w.dq_acc, prm0.dk, prm0.dv, s, prm0.err);
+    if (e != cudaSuccess) return e;
+  } else {
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if (!make_tmap_bhnd(&tq, q, BH, P.N, D, 64) || !make_tmap_bhnd(&tdo, dout, BH, P.N, D, 64) ||
       !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, prm0.Nk, D, 128) ||
@@ -730,6 +737,7 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   CUtensorMap tdq;
   if (!make_tmap_f32_bhnd(&tdq, w.dq_acc, BH, P.N, D, 32, 32))
     return cudaErrorInvalidValue;
+  using C = BwdCfg<D>;
   static bool attr_done = false;
   if (!attr_done) {
     e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
@@ -742,6 +750,7 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
     BwdParams prm = prm0;
     if (natural) prm.order = nullptr;
     bwd_kernel<D><<<(unsigned)grid, 480, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
+  }
   }
   // 4. dQ = bf16(scale * dQacc)
   const long long n8 = BH * P.N * D / 8;
@@ -796,6 +805,7 @@ cudaError_t launch_bwd(const fm_problem& P, const void* q, const void* k, const 
   prm.scale = P.scale;
   prm.scale_log2 = P.scale * kLog2e;
   prm.err = err;
+  if (P.d == 256) return launch_bwd_d<256>(P, q, k, v, o, lse, dout, dq, prm, w, s);
   return (P.d == 128) ? launch_bwd_d<128>(P, q, k, v, o, lse, dout, dq, prm, w, s)
                       : launch_bwd_d<64>(P, q, k, v, o, lse, dout, dq, prm, w, s);
 }

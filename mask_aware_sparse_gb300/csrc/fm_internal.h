@@ -53,6 +53,13 @@ cudaError_t launch_bwd(const fm_problem& p, const void* q, const void* k, const 
                        const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
                        void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err);
 
+// Main kernel of the d = 256 backward (fm_bwd256.cu); row terms, launch
+// order and dQ conversion come from launch_bwd.
+cudaError_t launch_bwd256_main(const fm_problem& P, const void* q, const void* k, const void* v, const void* dout,
+                               const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
+                               const int32_t* k_off, const int32_t* k_queue, const int32_t* order, const float* nl,
+                               const float* dsum, float* dq_acc, void* dk, void* dv, cudaStream_t s, int* err);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

@@ -111,3 +111,46 @@ def test_fwd256_long_pass_natural_order():
         tr = torch.as_tensor(rows, device="cuda")
         assert_out(f64(o[:, h:h + 1, tr]), O_ref)
         assert_lse(f64(lse[:, h:h + 1, tr]), L_ref)
+
+
+# ---------------------------------------------------------------- backward
+def _bwd(vec, B, hq, hkv, n, causal):
+    scale = D ** -0.5
+    cfg = dict(B=B, H_q=hq, H_kv=hkv, N=n, d=D)
+    q, k, v, do = tensors.make_qkvdo(cfg)
+    dv_ = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in vec]
+    qs = fm.fm_classify_tiles(*dv_, causal=causal)
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    o, lse = fm.fm_attn_fwd(qd, kd, vd, *dv_, qs, scale=scale, causal=causal)
+    dq, dk, dv = fm.fm_attn_bwd(qd, kd, vd, o, lse, dod, *dv_, qs, scale=scale, causal=causal)
+    st, bits = fm.fm_device_status()
+    assert st == fm.FM_OK, bits
+    ref = oracle.backward(f64(q), f64(k), f64(v), f64(do), vec, causal, scale)
+    for name, a, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert_grad(f64(a), r, name)
+
+
+def test_bwd256_tiny_config():
+    cfg = configs.make("tiny", d=D)
+    _bwd(tuple(cfg[x] for x in ("lts", "lte", "uts", "ute")), cfg["B"], cfg["H_q"], cfg["H_kv"], cfg["N"], True)
+
+
+@pytest.mark.parametrize("hq,hkv", [(1, 1), (4, 2), (6, 3)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd256_random_masks(hq, hkv, causal):
+    rng = np.random.default_rng(512 + 10 * hq + hkv + causal)
+    for n in (128, 384):
+        _bwd(random_vectors(rng, 1, n, "general"), 1, hq, hkv, n, causal)
+
+
+@pytest.mark.parametrize("n", [1, 100, 300, 389])
+def test_bwd256_ragged_n(n):
+    rng = np.random.default_rng(n + 512)
+    _bwd(random_vectors(rng, 2, n, "lower"), 2, 2, 1, n, True)
+
+
+@pytest.mark.parametrize("kind", ["docs", "share_question", "prefix_lm", "window", "eviction"])
+def test_bwd256_mask_families_2k(kind):
+    rng = np.random.default_rng(13)
+    v, causal = _families(kind, 2048, rng)
+    _bwd(tuple(x[None] for x in v), 1, 4, 2, 2048, causal)
