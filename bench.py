@@ -86,7 +86,7 @@ class ClockSampler:
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int, period_ms: int = 50):
+    def __init__(self, index: int, period_ms: int = 20):
         self.rows = []
         self.proc = None
         try:
@@ -493,8 +493,18 @@ def run_ours(args, cfg):
     dom_flops = work[dom]
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops"]
-    traffic = ncu_traffic(dom, args.workload)
+    traffic = ncu_traffic(dom, args.workload, cfg["d"])
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    # the same work against the tensor cores' per-clock peak at the SM clock
+    # sampled during the timed region (4096 bf16 MACs per clock per SM,
+    # measured by a microbenchmark); the measured cuBLAS peak above was taken
+    # at a lower, power-capped clock
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = (clocks or {}).get("sm_mhz") or peaks.get("sm_max_mhz")
+    clk_peak = 2 * 4096 * sms * mhz * 1e6 / 1e12 if mhz else None
+    per_clock = {"sm_mhz": mhz, "sms": sms, "peak": clk_peak,
+                 "frac_bwd": (work["bwd"] / (bwd_ms / 1e3) / 1e12) / clk_peak if clk_peak else None,
+                 "frac_fwd": (work["fwd"] / (fwd_ms / 1e3) / 1e12) / clk_peak if clk_peak else None}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": tmax / args.steps * 1e3, "higher_is_better": True,
@@ -507,6 +517,9 @@ def run_ours(args, cfg):
         "computed_tile_tflops": computed * 128 * 128 * 14 * cfg["d"] * cfg["H_q"] * cfg["B"] * args.steps / step_s / 1e12,
         "kernel_ms": {"fwd_main": fwd_ms, "bwd_main": bwd_ms,
                       "rest_of_step": tmax / args.steps * 1e3 - fwd_ms - bwd_ms},
+        "kernel_frac_of_measured_peak": {"fwd_main": work["fwd"] / (fwd_ms / 1e3) / 1e12 / peak,
+                                         "bwd_main": work["bwd"] / (bwd_ms / 1e3) / 1e12 / peak},
+        "per_clock_peak": per_clock,
         "roofline": {"kernel": "fm_attn_bwd main" if dom == "bwd" else "fm_attn_fwd main", "bound": "tensor",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "traffic": traffic,
@@ -535,11 +548,11 @@ NCU_TRAFFIC = {
 }
 
 
-def ncu_traffic(kind: str, workload: str):
+def ncu_traffic(kind: str, workload: str, d: int):
     import hashlib
 
     ent = NCU_TRAFFIC.get(kind)
-    if not ent or ent["workload"] != workload:
+    if not ent or ent["workload"] != workload or ent.get("d", 128) != d:
         return None
     src = os.path.join(ROOT, "mask_aware_sparse_gb300", "csrc", ent["file"])
     try:
@@ -547,6 +560,171 @@ def ncu_traffic(kind: str, workload: str):
     except OSError:
         return None
     return ent["bytes"] if h == ent["sha256"] else None
+
+
+# ------------------------------------------------------ FP8 forward
+def _time_steps(fn, steps, flush):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / 1e3 / steps
+
+
+def run_fp8(args, cfg):
+    """The FP8 forward on the workload: one step = classify + fm_attn_fwd_fp8 on
+    e4m3 Q / K / V (per-tensor scales), beside the bf16 forward on the same
+    (dequantized) inputs. Metric: effective forward TFLOP/s (4 d FLOPs per
+    unmasked pair), against the fp8 peak taken as the measured bf16 peak x 2
+    (the nominal dense fp8 : bf16 ratio, 4.5 : 2.25 PFLOP/s)."""
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    from mask_aware_sparse_gb300 import build as fmbuild
+
+    fmbuild.build()
+    import mask_aware_sparse_gb300 as fm
+
+    dev = torch.device("cuda", 0)
+    q, k, v, _ = tensors.make_qkvdo(cfg, device=dev)
+
+    def quant(x):
+        sc = float(x.float().abs().max()) / 448.0
+        return (x.float() / sc).to(torch.float8_e4m3fn), sc
+
+    (q8, sq), (k8, sk), (v8, sv) = quant(q), quant(k), quant(v)
+    qd, kd, vd = ((x.float() * s_).to(torch.bfloat16) for x, s_ in ((q8, sq), (k8, sk), (v8, sv)))
+    vec = [torch.from_numpy(np.ascontiguousarray(cfg[n])).to(dev) for n in ("lts", "lte", "uts", "ute")]
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    c = cfg
+
+    def step8():
+        qs = fm.fm_classify_tiles(*vec, causal=c["causal"])
+        fm.fm_attn_fwd_fp8(q8, k8, v8, *vec, qs, q_scale=sq, k_scale=sk, v_scale=sv, scale=c["scale"],
+                           causal=c["causal"], o=o, lse=lse)
+
+    def step16():
+        qs = fm.fm_classify_tiles(*vec, causal=c["causal"])
+        fm.fm_attn_fwd(qd, kd, vd, *vec, qs, scale=c["scale"], causal=c["causal"], o=o, lse=lse)
+
+    for _ in range(max(3, args.warmup)):
+        step8()
+        step16()
+    torch.cuda.synchronize()
+    st, bits = fm.fm_device_status()
+    if st != fm.FM_OK:
+        print(json.dumps({"error": f"device status {st} bits {bits} after warm-up"}))
+        return 1
+    sampler = ClockSampler(0)
+    time.sleep(0.3)
+    t0 = time.time()
+    t8 = _time_steps(step8, args.steps, flush)
+    t1 = time.time()
+    sampler.stop()
+    t16 = _time_steps(step16, args.steps, flush)
+    fm.fm_profile_read()
+    fm.fm_profile_enable(True)
+    for _ in range(min(args.steps, 10)):
+        flush.zero_()
+        step8()
+    torch.cuda.synchronize()
+    fm.fm_profile_enable(False)
+    prof = fm.fm_profile_read()
+    k8_ms = prof["fwd_ms"] / max(1, prof["fwd_launches"])
+    work = workload_flops(cfg)
+    peaks, src = read_peaks()
+    peak8 = 2 * peaks["bf16_tflops"]
+    value = work["fwd"] / t8 / 1e12
+    achieved = work["fwd"] / (k8_ms / 1e3) / 1e12
+    cfgd = config_dict(cfg, note="Q, K, V e4m3 with per-tensor scales (amax / 448); step = classify + forward")
+    line = {"metric": "effective TFLOP/s (unmasked FLOPs) fwd, FP8 (e4m3) inputs", "value": value, "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": t8 * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": cfgd, "bf16_forward_same_inputs": {"value": work["fwd"] / t16 / 1e12, "ms_per_step": t16 * 1e3},
+            "roofline": {"kernel": "fm_attn_fwd_fp8 main", "bound": "tensor", "achieved": achieved, "peak": peak8,
+                         "unit": "TFLOP/s", "frac": achieved / peak8, "traffic": None,
+                         "peak_source": f"{src} bf16_tflops {peaks['bf16_tflops']} x 2 (nominal fp8 : bf16)",
+                         "algorithmic": f"4*d FLOPs x {work['pairs']} unmasked pairs x {cfg['H_q']} heads per launch"},
+            "kernel_ms": {"fwd_main": k8_ms}, "clocks": sampler.summary(t0, t1)}
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------- mask-form compositions
+def run_compose(args, cfg):
+    """Forward + backward through one of the binding's compositions, on the
+    workload's own mask written in that form (so the work and the metric are
+    the workload's): `per_head` gives every query head its own copy of the
+    vectors (fm_attn_per_head: one classify + forward + backward per batch
+    entry and query head); `multi_interval` writes each key column's visible
+    rows [j, LTS_j) as two inclusive intervals split at their midpoint
+    (fm_attn_multi_interval: per interval classify + forward, the log-sum-exp
+    merge, per interval backward, the sums). The latter needs a causal mask
+    with LTE = N and no upper interval."""
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    from mask_aware_sparse_gb300 import build as fmbuild
+
+    fmbuild.build()
+    import mask_aware_sparse_gb300 as fm
+
+    dev = torch.device("cuda", 0)
+    q, k, v, do = tensors.make_qkvdo(cfg, device=dev)
+    names = ("lts", "lte", "uts", "ute")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    c = cfg
+    if args.compose == "per_head":
+        vec = [torch.from_numpy(np.ascontiguousarray(np.repeat(cfg[n][:, None], cfg["H_q"], axis=1))).to(dev)
+               for n in names]
+
+        def step():
+            fm.fm_attn_per_head(q, k, v, *vec, causal=c["causal"], scale=c["scale"], do=do)
+    else:
+        lts, lte, uts, ute = (cfg[n].astype(np.int64) for n in names)
+        n = cfg["N"]
+        if not (cfg["causal"] and (lte == n).all() and (uts >= ute).all()):
+            print(json.dumps({"error": "multi_interval needs a causal mask with LTE = N and no upper interval"}))
+            return 1
+        j = np.broadcast_to(np.arange(n), lts.shape)
+        last = lts - 1                       # visible rows of column j: [j, LTS_j - 1]
+        mid = (j + last) // 2
+        fms = np.stack([j, mid + 1]).astype(np.int32)
+        fme = np.stack([mid, last]).astype(np.int32)   # empty where start > end
+        fms_t, fme_t = torch.from_numpy(fms).to(dev), torch.from_numpy(fme).to(dev)
+
+        def step():
+            fm.fm_attn_multi_interval(q, k, v, fms_t, fme_t, scale=c["scale"], do=do)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st, bits = fm.fm_device_status()
+    if st != fm.FM_OK:
+        print(json.dumps({"error": f"device status {st} bits {bits} after warm-up"}))
+        return 1
+    sampler = ClockSampler(0)
+    time.sleep(0.3)
+    t0 = time.time()
+    t = _time_steps(step, args.steps, flush)
+    t1 = time.time()
+    sampler.stop()
+    work = workload_flops(cfg)
+    value = (work["fwd"] + work["bwd"]) / t / 1e12
+    peaks, src = read_peaks()
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_dict(cfg, note=f"composition: {args.compose} (eager library calls per step)"),
+            "pct_of_bf16_peak": 100.0 * value / peaks["bf16_tflops"], "clocks": sampler.summary(t0, t1)}
+    print(json.dumps(line))
+    return 0
 
 
 # ------------------------------------------------------- chunk balancer
@@ -665,20 +843,29 @@ def run_balance(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=configs.NAMES)
+    ap.add_argument("--head-dim", type=int, default=None, choices=(64, 128, 256),
+                    help="run the workload's mask and shapes at another head dimension")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--balance", action="store_true", help="measure the chunk balancer instead")
+    ap.add_argument("--fp8", action="store_true", help="measure the FP8 forward instead")
+    ap.add_argument("--compose", choices=("per_head", "multi_interval"), default=None,
+                    help="measure a mask-form composition of the binding instead")
     args = ap.parse_args()
     if args.balance:
         return run_balance(args)
     if args.warmup < 3:
         args.warmup = 3
-    cfg = configs.make(args.workload)
+    cfg = configs.make(args.workload) if args.head_dim is None else configs.make(args.workload, d=args.head_dim)
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if args.fp8:
+        return run_fp8(args, cfg)
+    if args.compose:
+        return run_compose(args, cfg)
     return run_ours(args, cfg)
 
 

@@ -143,6 +143,27 @@ fm_status fm_attn_fwd(const fm_problem* p, const void* q, const void* k, const v
                       const int32_t* q_queue, void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * FP8 forward: the same computation as fm_attn_fwd on e4m3 inputs
+ * ("Flash MSA Attention Kernel Implementation", "Optimization Tricks That
+ * Actually Matter": FP8 matrix products inside the tile, softmax in FP32).
+ *
+ * q, k, v hold e4m3 (OCP E4M3, finite range +-448) values, contiguous
+ * (B, H, N, d) one byte per element; the attention inputs they stand for are
+ * stored value x q_scale (k_scale, v_scale), scales finite and > 0.
+ * S = Q K^T runs on e4m3 operands with fp32 accumulation (exact products);
+ * the softmax, running max and sums are fp32; P is rounded to e4m3 for
+ * O = P V (fp32 accumulation); O is bf16, LSE fp32, in the units of fm_attn_fwd.
+ * P's rounding (3 mantissa bits) puts O about 2.5% (relative L2) from the
+ * exact attention of the dequantized inputs; LSE is not affected.
+ * d must be 128. Queues, mask vectors, workspace: as fm_attn_fwd. There is no
+ * FP8 backward.
+ * ------------------------------------------------------------------------- */
+fm_status fm_attn_fwd_fp8(const fm_problem* p, const void* q, const void* k, const void* v, float q_scale,
+                          float k_scale, float v_scale, const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                          const int32_t* ute, const int32_t* q_off, const int32_t* q_queue, void* o, float* lse,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Backward: given dO, the gradients of sum(O * dO):
  *   P = exp(scale S - LSE), dV = P^T dO, dP = dO V^T, D = rowsum(dO * O),
  *   dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q,

@@ -7,7 +7,7 @@ is missing (build it with `mask_aware_sparse_gb300.build.build()`), so there
 is no silent fallback.
 
 Functions carry the names of the C entry points:
-  fm_classify_tiles, fm_attn_fwd, fm_attn_bwd, fm_localize, fm_device_status,
+  fm_classify_tiles, fm_attn_fwd, fm_attn_fwd_fp8, fm_attn_bwd, fm_localize, fm_device_status,
   fm_selftest_wait_timeout, fm_profile_enable, fm_profile_read, fm_launch_count,
   fm_from_fms_fme, fm_merge_parts, fm_sum_parts, fm_chunk_loads,
   fm_balance_chunks, fm_needed_chunks (host code: the chunk balancer and the
@@ -69,6 +69,8 @@ _SIGS = {
     "fm_attn_fwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
     "fm_attn_fwd": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 11 + [_P, ctypes.c_size_t, _P]),
     "fm_attn_fwd_noalloc": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 11 + [_P]),
+    "fm_attn_fwd_fp8": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 3 + [ctypes.c_float] * 3 + [_P] * 8
+                        + [_P, ctypes.c_size_t, _P]),
     "fm_attn_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
     "fm_attn_bwd": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 15 + [_P, ctypes.c_size_t, _P]),
     "fm_localize": (ctypes.c_int, [_P, ctypes.c_int64, _P, ctypes.c_int32, ctypes.c_int32, _P, _P]),
@@ -272,6 +274,45 @@ def fm_attn_fwd(q, k, v, lts, lte, uts, ute, queues: TileQueues, *, scale: float
     _check(lib().fm_attn_fwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(lts), _ptr(lte), _ptr(uts),
                              _ptr(ute), _ptr(queues.q_off), _ptr(queues.q_queue), _ptr(o), _ptr(lse), _ptr(ws),
                              ctypes.c_size_t(wsb), _stream(stream)), "fm_attn_fwd")
+    return o, lse
+
+
+def fm_attn_fwd_fp8(q, k, v, lts, lte, uts, ute, queues: TileQueues, *, q_scale: float, k_scale: float,
+                    v_scale: float, scale: float, causal: bool, o=None, lse=None, ws=None, stream=None):
+    """FP8 forward: q, k, v are float8_e4m3fn (B, H, N, 128) tensors standing for
+    stored x q_scale (k_scale, v_scale). Returns (O bf16, LSE fp32)."""
+    e4 = torch.float8_e4m3fn
+    _need(isinstance(q, torch.Tensor) and q.dim() == 4, "q must be a (B, H_q, N, d) tensor")
+    B, Hq, N, d = q.shape
+    _need(isinstance(k, torch.Tensor) and k.dim() == 4 and k.shape[0] == B and k.shape[3] == d,
+          f"k has shape {tuple(k.shape)}, expected (B={B}, H_kv, N_kv, d={d})")
+    Hkv, Nk = k.shape[1], k.shape[2]
+    _need(Hkv > 0 and Hq % Hkv == 0, f"H_q={Hq} must be a multiple of H_kv={Hkv}")
+    _like(q, "q", (B, Hq, N, d), e4)
+    _like(k, "k", (B, Hkv, Nk, d), e4)
+    _like(v, "v", (B, Hkv, Nk, d), e4)
+    for i, x in enumerate((lts, lte, uts, ute)):
+        _like(x, f"mask vector {i}", (B, Nk), torch.int32)
+    if o is not None:
+        _like(o, "o", (B, Hq, N, d), torch.bfloat16)
+    if lse is not None:
+        _like(lse, "lse", (B, Hq, N), torch.float32)
+    _need(isinstance(queues, TileQueues) and (queues.block_m, queues.block_n) == attn_tiling(),
+          "queues must come from fm_classify_tiles with the attention tiling")
+    nq = -(-N // queues.block_m)
+    _like(queues.q_off, "queue offsets", (B * nq + 1,), torch.int32)
+    _same_cuda(q=q, k=k, v=v, o=o, lse=lse, ws=ws, queue_offsets=queues.q_off, queue=queues.q_queue,
+               **{f"mask vector {i}": x for i, x in enumerate((lts, lte, uts, ute))})
+    prob = _problem(B, Hq, Hkv, N, d, scale, causal, Nk)
+    o = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=q.device) if o is None else o
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    wsb = lib().fm_attn_fwd_workspace_bytes(ctypes.byref(prob))
+    if ws is None or ws.numel() < wsb:
+        ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=q.device)
+    _check(lib().fm_attn_fwd_fp8(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), float(q_scale), float(k_scale),
+                                 float(v_scale), _ptr(lts), _ptr(lte), _ptr(uts), _ptr(ute), _ptr(queues.q_off),
+                                 _ptr(queues.q_queue), _ptr(o), _ptr(lse), _ptr(ws), ctypes.c_size_t(wsb),
+                                 _stream(stream)), "fm_attn_fwd_fp8")
     return o, lse
 
 

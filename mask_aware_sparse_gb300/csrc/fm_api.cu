@@ -56,6 +56,19 @@ bool make_tmap_bhnd(void* out, const void* base, int64_t BH, int64_t N, int64_t 
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_u8_bhnd(void* out, const void* base, int64_t BH, int64_t N, int64_t d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)(N * d)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(static_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_f32_bhnd(void* out, const void* base, int64_t BH, int64_t N, int64_t d, int box_cols, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -252,6 +265,26 @@ fm_status fm_attn_fwd(const fm_problem* p, const void* q, const void* k, const v
   if (!err) return FM_ERR_CUDA;
   return from_cuda(launch_fwd(*p, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws,
                               static_cast<cudaStream_t>(stream), err));
+}
+
+fm_status fm_attn_fwd_fp8(const fm_problem* p, const void* q, const void* k, const void* v, float q_scale,
+                          float k_scale, float v_scale, const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                          const int32_t* ute, const int32_t* q_off, const int32_t* q_queue, void* o, float* lse,
+                          void* ws, size_t ws_bytes, void* stream) {
+  bool empty = false;
+  fm_status st = check_problem(p, &empty);
+  if (st != FM_OK || empty) return st;
+  if (p->d != 128) return FM_ERR_UNSUPPORTED;
+  for (float x : {q_scale, k_scale, v_scale})
+    if (!std::isfinite(x) || x <= 0.f) return FM_ERR_INVALID_ARG;
+  if (!q || !k || !v || !lts || !lte || !uts || !ute || !q_off || !q_queue || !o || !lse) return FM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FM_ERR_INVALID_ARG;
+  const size_t need = fwd_ws_bytes(*p);
+  if (need > 0 && (!ws || ws_bytes < need)) return FM_ERR_WORKSPACE;
+  int* err = device_error_word();
+  if (!err) return FM_ERR_CUDA;
+  return from_cuda(launch_fwd_fp8(*p, q, k, v, q_scale, k_scale, v_scale, lts, lte, uts, ute, q_off, q_queue, o, lse,
+                                  ws, static_cast<cudaStream_t>(stream), err));
 }
 
 fm_status fm_attn_fwd_noalloc(const fm_problem* p, const void* q, const void* k, const void* v, const int32_t* lts,

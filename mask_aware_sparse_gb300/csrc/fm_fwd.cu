@@ -55,11 +55,14 @@
 namespace fm {
 namespace {
 
-template <int D>
+// F8: Q, K, V (and P) are e4m3 instead of bf16 (the FP8 forward).
+template <int D, bool F8 = false>
 struct FwdCfg {
-  static constexpr int TILE = 128 * D * 2;  // bytes of one 128-row bf16 tile
-  static constexpr int BOXES = D / 64;     // 64-column TMA boxes per tile
-  static constexpr int STAGES = (D == 128) ? 2 : 4;
+  static constexpr int ES = F8 ? 1 : 2;         // bytes per Q / K / V element
+  static constexpr int TILE = 128 * D * ES;     // bytes of one 128-row tile
+  static constexpr int BOX_COLS = 128 / ES;     // elements in one 128-byte swizzled row of a TMA box
+  static constexpr int BOXES = D / BOX_COLS;    // 16 KB TMA boxes per tile
+  static constexpr int STAGES = (F8 || D == 64) ? 4 : 2;
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + 2 * TILE;
   static constexpr int V_OFF = K_OFF + STAGES * TILE;
@@ -115,6 +118,7 @@ struct FwdParams {
   int B, H_q, H_kv, N, Nk, nQ, nK, G, PG, causal;  // N query rows, Nk key rows
   int units;  // B * nQ * H_kv * PG work units
   float scale_log2;
+  float o_scale;  // multiplies O / l (the V dequantization scale of the FP8 forward; 1 otherwise)
   int* err;
 };
 
@@ -150,11 +154,11 @@ __device__ __forceinline__ bool block_partial(const FwdParams& p, int e) {
   return (e & 1) || ((e >> 1) == p.nK - 1 && (p.Nk & 127));
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, const FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, F8>;
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -290,8 +294,8 @@ __global__ void __launch_bounds__(320, 1)
           if (ok) {
             mbar_arrive_expect_tx(&bars[C::B_KFULL + slot], C::TILE);
             for (int x = 0; x < C::BOXES; ++x)
-              tma_load_3d(smem + C::K_OFF + slot * C::TILE + x * 16384, &tk, &bars[C::B_KFULL + slot], x * 64,
-                          kb * 128, u.b * p.H_kv + u.g);
+              tma_load_3d(smem + C::K_OFF + slot * C::TILE + x * 16384, &tk, &bars[C::B_KFULL + slot],
+                          x * C::BOX_COLS, kb * 128, u.b * p.H_kv + u.g);
           }
           if (ok && j == 0) {
             // the Q tiles of this unit, once the last S MMA of the previous one is done
@@ -300,8 +304,8 @@ __global__ void __launch_bounds__(320, 1)
               mbar_arrive_expect_tx(&bars[C::B_QFULL], u.T * C::TILE);
               for (int t = 0; t < u.T; ++t)
                 for (int x = 0; x < C::BOXES; ++x)
-                  tma_load_3d(smem + C::Q_OFF + t * C::TILE + x * 16384, &tq, &bars[C::B_QFULL], x * 64,
-                              u.qb * 128, u.b * p.H_q + u.h0 + t);
+                  tma_load_3d(smem + C::Q_OFF + t * C::TILE + x * 16384, &tq, &bars[C::B_QFULL],
+                              x * C::BOX_COLS, u.qb * 128, u.b * p.H_q + u.h0 + t);
             }
           }
         }
@@ -350,8 +354,8 @@ __global__ void __launch_bounds__(320, 1)
           if (ok) {
             mbar_arrive_expect_tx(&bars[C::B_VFULL + slot], C::TILE);
             for (int x = 0; x < C::BOXES; ++x)
-              tma_load_3d(smem + C::V_OFF + slot * C::TILE + x * 16384, &tv, &bars[C::B_VFULL + slot], x * 64,
-                          kb * 128, u.b * p.H_kv + u.g);
+              tma_load_3d(smem + C::V_OFF + slot * C::TILE + x * 16384, &tv, &bars[C::B_VFULL + slot],
+                          x * C::BOX_COLS, kb * 128, u.b * p.H_kv + u.g);
           }
         }
         ok = __shfl_sync(kFull, ok, 0);
@@ -362,8 +366,9 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 0);  // S = Q K^T, both K-major
-      const uint32_t id_o = idesc_bf16_f32(128, D, 0, 1);    // O += P V, V is MN-major
+      // S = Q K^T, both K-major; O += P V, V MN-major
+      const uint32_t id_s = F8 ? idesc_e4m3_f32(128, 128, 0, 0) : idesc_bf16_f32(128, 128, 0, 0);
+      const uint32_t id_o = F8 ? idesc_e4m3_f32(128, D, 0, 1) : idesc_bf16_f32(128, D, 0, 1);
       // descriptors built once; per MMA only the start-address field moves
       // (a 64-bit add of a constant), which keeps the issue ahead of the tensor core
       constexpr uint64_t kTileStep = C::TILE >> 4;
@@ -381,9 +386,14 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t tS = tbase + (uint32_t)(t * 128);
         const uint32_t tO = tbase + 256u + (uint32_t)(t * D);
         const uint64_t vd = dV0 + kTileStep * (uint64_t)vs;
+        // k-steps of 16 bf16 (32 e4m3) keys: 8 TMEM columns of P, 16 (32) rows of V
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tO, tS + (uint32_t)(kk * 8), vd + (uint64_t)(kk * 128), id_o, (!first || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < (F8 ? 4 : 8); ++kk) {
+          if constexpr (F8)
+            mma_ts_f8(tO, tS + (uint32_t)(kk * 8), vd + (uint64_t)(kk * 256), id_o, (!first || kk > 0) ? 1u : 0u);
+          else
+            mma_ts(tO, tS + (uint32_t)(kk * 8), vd + (uint64_t)(kk * 128), id_o, (!first || kk > 0) ? 1u : 0u);
+        }
         mma_commit(&bars[C::B_ODONE + t]);
         if (t) ++npv1;
         else ++npv0;
@@ -407,10 +417,14 @@ __global__ void __launch_bounds__(320, 1)
         auto issue_s = [&](int t, int slot) {
           const uint32_t tS = tbase + (uint32_t)(t * 128);
           const uint64_t qd = dQ0 + kTileStep * (uint64_t)t, kd = dK0 + kTileStep * (uint64_t)slot;
+          // k-steps of 32 bytes (16 bf16 / 32 e4m3), four per 128-byte swizzled row
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
+          for (int kk = 0; kk < D * C::ES / 32; ++kk) {
             const uint64_t off = (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);
-            mma_ss(tS, qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
+            if constexpr (F8)
+              mma_ss_f8(tS, qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
+            else
+              mma_ss(tS, qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
           }
           mma_commit(&bars[C::B_SFULL + t]);
         };
@@ -474,7 +488,7 @@ __global__ void __launch_bounds__(320, 1)
       const float l = __int_as_float(st.x), m = __int_as_float(st.y);
       const int bh = st.z, q0e = st.w;
       const int w0e = q0e + ((warp & 3) << 5), ie = q0e + row;
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      const float inv = (l > 0.f) ? p.o_scale / l : 0.f;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         const float* f = reinterpret_cast<const float*>(&orow[c0]);
@@ -634,7 +648,9 @@ __global__ void __launch_bounds__(320, 1)
         // exponent arguments and the row sum on column pairs (f32x2)
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-msafe, -msafe);
         uint64_t rs0 = f2_pack(0.f, 0.f), rs1 = rs0;
+        // P as bf16 pairs (e4m3 quadruples for the FP8 forward), key order low to high
         uint32_t pk[64];
+        float pa = 0.f, pb = 0.f;
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           float x0, x1;
@@ -642,7 +658,15 @@ __global__ void __launch_bounds__(320, 1)
           const float a = ex2_approx(x0), bb = ex2_approx(x1);
           if (c & 1) rs1 = f2_add(rs1, f2_pack(a, bb));
           else rs0 = f2_add(rs0, f2_pack(a, bb));
-          pk[c] = pack_bf16x2(a, bb);
+          if constexpr (F8) {
+            if (c & 1) pk[c >> 1] = pack_e4m3x4(pa, pb, a, bb);
+            else {
+              pa = a;
+              pb = bb;
+            }
+          } else {
+            pk[c] = pack_bf16x2(a, bb);
+          }
         }
         float r0a, r0b, r1a, r1b;
         f2_unpack(rs0, r0a, r0b);
@@ -651,12 +675,14 @@ __global__ void __launch_bounds__(320, 1)
         {
           const uint32_t(&p0)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]);
           const uint32_t(&p1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]);
-          const uint32_t(&p2)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pk[32]);
-          const uint32_t(&p3)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pk[48]);
           tmem_st16(tS + 0, p0);
           tmem_st16(tS + 16, p1);
-          tmem_st16(tS + 32, p2);
-          tmem_st16(tS + 48, p3);
+          if constexpr (!F8) {
+            const uint32_t(&p2)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pk[32]);
+            const uint32_t(&p3)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pk[48]);
+            tmem_st16(tS + 32, p2);
+            tmem_st16(tS + 48, p3);
+          }
           tmem_st_wait();
         }
         if (j > 0 && __any_sync(kFull, resc)) {
@@ -718,19 +744,20 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_fwd_d(const fm_problem& P, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, const FwdParams& prm, unsigned grid, cudaStream_t s) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, F8>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    cudaError_t e =
+        cudaFuncSetAttribute(fwd_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   {
     KernelTimer timer(s, kTimedFwd);
-    fwd_kernel<D><<<grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, to, prm);
+    fwd_kernel<D, F8><<<grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, to, prm);
   }
   count_launches(prm.order ? 2 : 1);  // [LPT order] + main kernel
   return cudaGetLastError();
@@ -770,10 +797,13 @@ static size_t fwd_order_bytes(const fm_problem& p) {
 
 size_t fwd_ws_bytes(const fm_problem& p) { return fwd_order_bytes(p) + 256; }
 
-cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const void* v, const int32_t* lts,
-                       const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
-                       const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err) {
-  if (P.d == 256) return launch_fwd256(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err);
+// The persistent forward (d = 64, 128; bf16 or, with fp8, e4m3 Q / K / V whose
+// values are the stored ones times q_scale, k_scale, v_scale).
+static cudaError_t launch_fwd_persistent(const fm_problem& P, const void* q, const void* k, const void* v,
+                                         const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                                         const int32_t* ute, const int32_t* q_off, const int32_t* q_queue, void* o,
+                                         float* lse, void* ws, cudaStream_t s, int* err, bool fp8, float q_scale,
+                                         float k_scale, float v_scale) {
   const int nQ = (P.N + kTile - 1) / kTile;
   const int G = P.H_q / P.H_kv;
   const int PG = (G + 1) / 2;
@@ -791,10 +821,17 @@ cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const 
   if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, P.B * nQ, order);
   CUtensorMap tq, tk, tv, to;
   const int Nk = kv_rows(P);
-  if (!make_tmap_bhnd(&tq, q, (int64_t)P.B * P.H_q, P.N, P.d) || !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, Nk, P.d) ||
-      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, Nk, P.d) ||
-      !make_tmap_bhnd_w32(&to, o, (int64_t)P.B * P.H_q, P.N, P.d))
+  if (fp8) {
+    if (!make_tmap_u8_bhnd(&tq, q, (int64_t)P.B * P.H_q, P.N, P.d) ||
+        !make_tmap_u8_bhnd(&tk, k, (int64_t)P.B * P.H_kv, Nk, P.d) ||
+        !make_tmap_u8_bhnd(&tv, v, (int64_t)P.B * P.H_kv, Nk, P.d))
+      return cudaErrorInvalidValue;
+  } else if (!make_tmap_bhnd(&tq, q, (int64_t)P.B * P.H_q, P.N, P.d) ||
+             !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, Nk, P.d) ||
+             !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, Nk, P.d)) {
     return cudaErrorInvalidValue;
+  }
+  if (!make_tmap_bhnd_w32(&to, o, (int64_t)P.B * P.H_q, P.N, P.d)) return cudaErrorInvalidValue;
   FwdParams prm;
   prm.lts = lts;
   prm.lte = lte;
@@ -817,12 +854,30 @@ cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const 
   prm.PG = PG;
   prm.causal = P.causal ? 1 : 0;
   prm.units = (int)units;
-  prm.scale_log2 = P.scale * 1.4426950408889634f;
+  prm.scale_log2 = P.scale * q_scale * k_scale * 1.4426950408889634f;
+  prm.o_scale = v_scale;
   prm.err = err;
   // persistent: one CTA per SM (the kernel's shared memory and TMEM fill an SM)
   const unsigned grid = (unsigned)std::min<long long>(units, (long long)sm_count());
-  if (P.d == 128) return launch_fwd_d<128>(P, tq, tk, tv, to, prm, grid, s);
-  return launch_fwd_d<64>(P, tq, tk, tv, to, prm, grid, s);
+  if (fp8) return launch_fwd_d<128, true>(P, tq, tk, tv, to, prm, grid, s);
+  if (P.d == 128) return launch_fwd_d<128, false>(P, tq, tk, tv, to, prm, grid, s);
+  return launch_fwd_d<64, false>(P, tq, tk, tv, to, prm, grid, s);
+}
+
+cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const void* v, const int32_t* lts,
+                       const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
+                       const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err) {
+  if (P.d == 256) return launch_fwd256(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err);
+  return launch_fwd_persistent(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err, false, 1.f, 1.f,
+                               1.f);
+}
+
+cudaError_t launch_fwd_fp8(const fm_problem& P, const void* q, const void* k, const void* v, float q_scale,
+                           float k_scale, float v_scale, const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                           const int32_t* ute, const int32_t* q_off, const int32_t* q_queue, void* o, float* lse,
+                           void* ws, cudaStream_t s, int* err) {
+  return launch_fwd_persistent(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err, true, q_scale,
+                               k_scale, v_scale);
 }
 
 }  // namespace fm

@@ -36,6 +36,13 @@ cudaError_t launch_fwd(const fm_problem& p, const void* q, const void* k, const 
                        const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
                        const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err);
 
+// FP8 forward (fm_fwd.cu): e4m3 Q / K / V (value = stored x scale), d = 128,
+// bf16 O; same workspace as launch_fwd.
+cudaError_t launch_fwd_fp8(const fm_problem& P, const void* q, const void* k, const void* v, float q_scale,
+                           float k_scale, float v_scale, const int32_t* lts, const int32_t* lte, const int32_t* uts,
+                           const int32_t* ute, const int32_t* q_off, const int32_t* q_queue, void* o, float* lse,
+                           void* ws, cudaStream_t s, int* err);
+
 // Forward for d = 256 (fm_fwd256.cu): same arguments and workspace as launch_fwd.
 cudaError_t launch_fwd256(const fm_problem& p, const void* q, const void* k, const void* v, const int32_t* lts,
                           const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
@@ -72,6 +79,8 @@ inline bool use_natural_order(long long ctas) { return ctas >= 8LL * sm_count();
 // box {64, box_rows, 1}, 128-byte swizzle; rows >= N read as zero.
 bool make_tmap_bhnd(void* out_tmap /* CUtensorMap* */, const void* base, int64_t BH, int64_t N, int64_t d,
                     int box_rows = 128);
+// Same for a one-byte (e4m3) (BH, N, d) tensor: box {128, 128, 1}, 128-byte swizzle.
+bool make_tmap_u8_bhnd(void* out_tmap /* CUtensorMap* */, const void* base, int64_t BH, int64_t N, int64_t d);
 // Same for an fp32 (BH, N, d) tensor, box {box_cols, box_rows, 1}, no swizzle
 // (used as the destination of TMA reduce-adds).
 bool make_tmap_f32_bhnd(void* out_tmap /* CUtensorMap* */, const void* base, int64_t BH, int64_t N, int64_t d,
