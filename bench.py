@@ -357,58 +357,44 @@ def capture_step(path: Path):
 
 
 def e2e_measure(path: Path, steps: int):
-    """Same metric through the public API from pinned HOST buffers: every step
-    copies its inputs host->device, runs the path and reads every output back.
-    Steps are pipelined on three streams (copy in, compute, copy out) with two
-    sets of device buffers, so one step's copies overlap the neighbouring
-    steps' compute and the two copy directions overlap each other; events keep
-    a buffer set from being overwritten before its readers are done."""
-    fm, c, dev = path.fm, path.cfg, path.dev
+    """Same metric through the C ABI's host-buffer entry point
+    (fm_attn_fwd_bwd_host): every step hands the library pinned HOST buffers;
+    the library copies the step's inputs to its device workspace, classifies,
+    runs forward and backward and copies every output back. Steps rotate over
+    three streams, each with its own device workspace and host output set, so
+    one step's copies overlap its neighbours' compute."""
+    fm, c = path.fm, path.cfg
     h_in = [t.cpu().pin_memory() for t in (path.q, path.k, path.v, path.do)]
     h_vec = [t.cpu().pin_memory() for t in path.vec]
     outs = (path.o, path.lse, path.dq, path.dk, path.dv)
-    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _ in range(2)]
-    d_in = [[torch.empty_like(t, device=dev) for t in h_in + h_vec] for _ in range(2)]
-    d_out = [[torch.empty_like(t) for t in outs] for _ in range(2)]
+    R = 3
+    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _ in range(R)]
     h2d = sum(t.numel() * t.element_size() for t in h_in + h_vec)
     d2h = sum(t.numel() * t.element_size() for t in h_out[0])
-    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    in_done = [torch.cuda.Event() for _ in range(2)]
-    c_done = [torch.cuda.Event() for _ in range(2)]
-    out_done = [torch.cuda.Event() for _ in range(2)]
+    prob = fm._problem(c["B"], c["H_q"], c["H_kv"], c["N"], c["d"], c["scale"], c["causal"], c["N"])
+    wsb = fm.lib().fm_attn_host_workspace_bytes(fm.ctypes.byref(prob))
+    ws = [torch.empty(wsb, dtype=torch.uint8, device=path.dev) for _ in range(R)]
+    streams = [torch.cuda.Stream() for _ in range(R)]
+    q, k, v, do = h_in
 
     def one(i):
-        j = i & 1
-        s_in.wait_event(c_done[j])  # the compute two steps back has read this input set
-        with torch.cuda.stream(s_in):
-            for d, h in zip(d_in[j], h_in + h_vec):
-                d.copy_(h, non_blocking=True)
-            in_done[j].record(s_in)
-        s_c.wait_event(in_done[j])
-        s_c.wait_event(out_done[j])  # the copy-out two steps back has read this output set
-        with torch.cuda.stream(s_c):
-            q, k, v, do, *vec = d_in[j]
-            o, lse, dq, dk, dv = d_out[j]
-            qs = fm.fm_classify_tiles(*vec, causal=c["causal"], stream=s_c)
-            fm.fm_attn_fwd(q, k, v, *vec, qs, scale=c["scale"], causal=c["causal"], o=o, lse=lse, stream=s_c)
-            fm.fm_attn_bwd(q, k, v, o, lse, do, *vec, qs, scale=c["scale"], causal=c["causal"], dq=dq, dk=dk, dv=dv,
-                           stream=s_c)
-            c_done[j].record(s_c)
-        s_out.wait_event(c_done[j])
-        with torch.cuda.stream(s_out):
-            for h, d in zip(h_out[j], d_out[j]):
-                h.copy_(d, non_blocking=True)
-            out_done[j].record(s_out)
+        j = i % R
+        o, lse, dq, dk, dv = h_out[j]
+        fm.fm_attn_fwd_bwd_host(q, k, v, do, *h_vec, scale=c["scale"], causal=c["causal"], o=o, lse=lse, dq=dq,
+                                dk=dk, dv=dv, ws=ws[j], stream=streams[j])
 
-    for i in range(2):
+    for i in range(R):
         one(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(s_in)
+    a.record(streams[0])
+    for st in streams[1:]:
+        st.wait_event(a)
     for i in range(steps):
         one(i)
-    s_in.wait_stream(s_out)
-    b.record(s_in)
+    for st in streams[1:]:
+        streams[0].wait_stream(st)
+    b.record(streams[0])
     torch.cuda.synchronize()
     return a.elapsed_time(b) / 1e3 / steps, h2d, d2h
 

@@ -184,6 +184,28 @@ fm_status fm_attn_bwd(const fm_problem* p, const void* q, const void* k, const v
                       void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * One forward + backward from HOST buffers. (No counterpart in the pages: an
+ * end-to-end convenience over the calls above.)
+ *
+ * q, k, v, dout, the four mask vectors, and the outputs o, lse, dq, dk, dv are
+ * HOST pointers with the layouts above (page-locked memory lets the copies run
+ * asynchronously and overlap other work; pageable memory works but each copy
+ * then blocks the calling thread). On `stream`, in order: one host-to-device
+ * copy per input into the device workspace, fm_classify_tiles (attention
+ * tiling), fm_attn_fwd, fm_attn_bwd, one device-to-host copy per output. The
+ * call returns once everything is enqueued; synchronize the stream before
+ * reading the outputs. ws: DEVICE memory of fm_attn_host_workspace_bytes(p)
+ * bytes (the device copies of inputs and outputs, the queues and the kernels'
+ * workspaces), owned by the caller; two calls in flight need two workspaces.
+ * Errors: as the calls it makes; FM_ERR_CUDA when a copy cannot be enqueued.
+ * ------------------------------------------------------------------------- */
+size_t fm_attn_host_workspace_bytes(const fm_problem* p);
+fm_status fm_attn_fwd_bwd_host(const fm_problem* p, const void* q, const void* k, const void* v, const void* dout,
+                               const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
+                               void* o, float* lse, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                               void* stream);
+
+/* ---------------------------------------------------------------------------
  * Forward without a caller-provided workspace. (No counterpart in the pages:
  * this is a convenience of the library, not part of the method.)
  *

@@ -7,7 +7,8 @@ is missing (build it with `mask_aware_sparse_gb300.build.build()`), so there
 is no silent fallback.
 
 Functions carry the names of the C entry points:
-  fm_classify_tiles, fm_attn_fwd, fm_attn_fwd_fp8, fm_attn_bwd, fm_localize, fm_device_status,
+  fm_classify_tiles, fm_attn_fwd, fm_attn_fwd_fp8, fm_attn_bwd, fm_attn_fwd_bwd_host (host buffers in
+  and out, device workspace), fm_localize, fm_device_status,
   fm_selftest_wait_timeout, fm_profile_enable, fm_profile_read, fm_launch_count,
   fm_from_fms_fme, fm_merge_parts, fm_sum_parts, fm_chunk_loads,
   fm_balance_chunks, fm_needed_chunks (host code: the chunk balancer and the
@@ -72,6 +73,8 @@ _SIGS = {
     "fm_attn_fwd_fp8": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 3 + [ctypes.c_float] * 3 + [_P] * 8
                         + [_P, ctypes.c_size_t, _P]),
     "fm_attn_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
+    "fm_attn_host_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
+    "fm_attn_fwd_bwd_host": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 13 + [_P, ctypes.c_size_t, _P]),
     "fm_attn_bwd": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 15 + [_P, ctypes.c_size_t, _P]),
     "fm_localize": (ctypes.c_int, [_P, ctypes.c_int64, _P, ctypes.c_int32, ctypes.c_int32, _P, _P]),
     "fm_from_fms_fme": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P, _P]),
@@ -333,6 +336,50 @@ def fm_attn_bwd(q, k, v, o, lse, do, lts, lte, uts, ute, queues: TileQueues, *, 
                              _ptr(lte), _ptr(uts), _ptr(ute), _ptr(queues.k_off), _ptr(queues.k_queue), _ptr(dq),
                              _ptr(dk), _ptr(dv), _ptr(ws), ctypes.c_size_t(wsb), _stream(stream)), "fm_attn_bwd")
     return dq, dk, dv
+
+
+def fm_attn_fwd_bwd_host(q, k, v, do, lts, lte, uts, ute, *, scale: float, causal: bool, o=None, lse=None,
+                         dq=None, dk=None, dv=None, ws=None, stream=None):
+    """Forward + backward from HOST tensors (page-locked for asynchronous copies):
+    the library copies the inputs to its device workspace `ws` (a CUDA uint8
+    tensor of fm_attn_host_workspace_bytes bytes, allocated here if None),
+    classifies, runs forward and backward, and copies O, LSE, dQ, dK, dV back
+    into host tensors, all enqueued on `stream`. Returns (o, lse, dq, dk, dv)
+    without waiting: synchronize the stream before reading them."""
+    _need(isinstance(q, torch.Tensor) and q.dim() == 4, "q must be a (B, H_q, N, d) tensor")
+    B, Hq, N, d = q.shape
+    _need(isinstance(k, torch.Tensor) and k.dim() == 4 and k.shape[0] == B and k.shape[3] == d,
+          f"k has shape {tuple(k.shape)}, expected (B={B}, H_kv, N_kv, d={d})")
+    Hkv, Nk = k.shape[1], k.shape[2]
+    bf = torch.bfloat16
+    for name, t, shape, dt in (("q", q, (B, Hq, N, d), bf), ("k", k, (B, Hkv, Nk, d), bf), ("v", v, (B, Hkv, Nk, d), bf),
+                               ("do", do, (B, Hq, N, d), bf)):
+        _like(t, name, shape, dt)
+    for i, x in enumerate((lts, lte, uts, ute)):
+        _like(x, f"mask vector {i}", (B, Nk), torch.int32)
+    host = dict(q=q, k=k, v=v, do=do, lts=lts, lte=lte, uts=uts, ute=ute)
+    o = torch.empty((B, Hq, N, d), dtype=bf, pin_memory=True) if o is None else o
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, pin_memory=True) if lse is None else lse
+    dq = torch.empty((B, Hq, N, d), dtype=bf, pin_memory=True) if dq is None else dq
+    dk = torch.empty((B, Hkv, Nk, d), dtype=bf, pin_memory=True) if dk is None else dk
+    dv = torch.empty((B, Hkv, Nk, d), dtype=bf, pin_memory=True) if dv is None else dv
+    for name, t, shape, dt in (("o", o, (B, Hq, N, d), bf), ("lse", lse, (B, Hq, N), torch.float32),
+                               ("dq", dq, (B, Hq, N, d), bf), ("dk", dk, (B, Hkv, Nk, d), bf),
+                               ("dv", dv, (B, Hkv, Nk, d), bf)):
+        _like(t, name, shape, dt)
+        host[name] = t
+    for name, t in host.items():
+        _need(not t.is_cuda, f"{name} must be a host tensor for the host-buffer entry point")
+    prob = _problem(B, Hq, Hkv, N, d, scale, causal, Nk)
+    wsb = lib().fm_attn_host_workspace_bytes(ctypes.byref(prob))
+    if ws is None:
+        ws = torch.empty(max(1, wsb), dtype=torch.uint8, device="cuda")
+    _need(isinstance(ws, torch.Tensor) and ws.is_cuda and ws.dtype == torch.uint8 and ws.numel() >= wsb,
+          f"ws must be a CUDA uint8 tensor of at least {wsb} bytes")
+    _check(lib().fm_attn_fwd_bwd_host(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lts), _ptr(lte),
+                                      _ptr(uts), _ptr(ute), _ptr(o), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                                      _ptr(ws), ctypes.c_size_t(wsb), _stream(stream)), "fm_attn_fwd_bwd_host")
+    return o, lse, dq, dk, dv
 
 
 def fm_localize(x, chunk_off, C: int, out=None, stream=None):

@@ -35,3 +35,37 @@ def test_bounded_wait_times_out_and_context_survives():
     assert y.cpu().tolist() == [0, 1, 2, 3, 4, 4, 4, 4, 4, 4]
     st, bits = fm.fm_device_status()
     assert st == fm.FM_OK and bits == 0
+
+
+def test_host_buffer_entry_point_matches_device_calls():
+    # fm_attn_fwd_bwd_host runs the same kernels on copies of host buffers:
+    # O, LSE, dK, dV bit for bit; dQ (fp32 reductions in any order) within the
+    # parity tolerance
+    import ctypes
+
+    import mask_aware_sparse_gb300 as fm
+    from workloads import masks, tensors
+
+    from helpers import GRAD_REL_L2, rel_l2
+
+    rng = np.random.default_rng(4)
+    n = 1000
+    v_ = masks.causal_documents(masks.draw_fill(rng, n, 100, 400), n)
+    cfg = dict(B=1, H_q=4, H_kv=2, N=n, d=128)
+    q, k, v, do = tensors.make_qkvdo(cfg)
+    vec = [torch.from_numpy(np.ascontiguousarray(x[None])) for x in v_]
+    scale = 128 ** -0.5
+    pin = lambda t: t.pin_memory()
+    out = fm.fm_attn_fwd_bwd_host(pin(q), pin(k), pin(v), pin(do), *[pin(x) for x in vec], scale=scale, causal=True)
+    torch.cuda.synchronize()
+    dvec = [x.cuda() for x in vec]
+    qs = fm.fm_classify_tiles(*dvec, causal=True)
+    o, lse = fm.fm_attn_fwd(q.cuda(), k.cuda(), v.cuda(), *dvec, qs, scale=scale, causal=True)
+    dq, dk, dv = fm.fm_attn_bwd(q.cuda(), k.cuda(), v.cuda(), o, lse, do.cuda(), *dvec, qs, scale=scale, causal=True)
+    assert fm.fm_device_status()[0] == fm.FM_OK
+    for a, b in ((out[0], o), (out[1], lse), (out[3], dk), (out[4], dv)):
+        assert torch.equal(a, b.cpu())
+    assert rel_l2(out[2].double().numpy(), dq.double().cpu().numpy()) <= GRAD_REL_L2 / 10
+    # host tensors only: a device tensor is refused before any call
+    with pytest.raises(ValueError):
+        fm.fm_attn_fwd_bwd_host(q.cuda(), k, v, do, *vec, scale=scale, causal=True)
