@@ -528,9 +528,9 @@ def run_ours(args, cfg):
 # the counters were taken from.
 NCU_TRAFFIC = {
     "bwd": {"file": "fm_bwd.cu", "workload": "share_question32k",
-            "sha256": "32cce9b8470330696795da8c94b76d79631891d97b238005bc623937716d6df3", "bytes": 1264590336},
+            "sha256": "bef3044d8040e2f71604208f4bbfa352970828ea6170fd9aaa905d8d5601351d", "bytes": 1264013824},
     "fwd": {"file": "fm_fwd.cu", "workload": "share_question32k",
-            "sha256": "017b14501532a86517f02dab2e88b636e156ea33593b1eabc929fa2ca0c607aa", "bytes": 482228480},
+            "sha256": "201fd3db195131393464a502f1d6d380c3c740f0f38beff588077c7fb5d38a76", "bytes": 482497280},
 }
 
 
