@@ -49,6 +49,7 @@ typedef enum fm_status {
 #define FM_DEVERR_TIMEOUT 1
 #define FM_DEVERR_RANGE 2
 #define FM_DEVERR_QUEUE 4
+#define FM_DEVERR_DEBUG 8 /* debug build only: a range check on a shared-memory / TMEM address or TMA coordinate failed */
 
 /* Problem shape. N query rows against N_kv key / value rows; N_kv = 0 means
  * N_kv = N (the square problem). A rectangular problem is what one rank of a

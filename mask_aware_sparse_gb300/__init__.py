@@ -27,10 +27,11 @@ import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libfm.so")
+# FM_LIBRARY=debug selects the range-checked debug build (build.build(debug=True))
+LIB_PATH = os.path.join(_HERE, "libfm_debug.so" if os.environ.get("FM_LIBRARY") == "debug" else "libfm.so")
 
 FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_WORKSPACE, FM_ERR_CUDA, FM_ERR_TIMEOUT, FM_ERR_DEVICE = range(7)
-FM_DEVERR_TIMEOUT, FM_DEVERR_RANGE, FM_DEVERR_QUEUE = 1, 2, 4
+FM_DEVERR_TIMEOUT, FM_DEVERR_RANGE, FM_DEVERR_QUEUE, FM_DEVERR_DEBUG = 1, 2, 4, 8
 
 
 class fm_problem(ctypes.Structure):

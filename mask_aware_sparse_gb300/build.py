@@ -3,6 +3,12 @@
 Every .cu under csrc/ is compiled in parallel for sm_103a only (the .cpp
 files, host code, with the same driver), then linked into
 mask_aware_sparse_gb300/libfm.so. No CMake, no torch extension machinery.
+
+build(debug=True) makes libfm_debug.so instead: the same sources with
+FM_DEBUG defined, whose kernels range-check every shared-memory address, TMA
+coordinate and TMEM lane / column they hand to the hardware and report a
+failed check as FM_DEVERR_DEBUG instead of faulting (csrc/sm100.cuh). The
+binding loads it when FM_LIBRARY=debug is set in the environment.
 """
 from __future__ import annotations
 
@@ -18,6 +24,8 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfm.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libfm_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + os.path.join(ROOT, "include")]
@@ -39,16 +47,18 @@ def _stale(lib: str, srcs) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
-    if not force and not _stale(LIB, srcs):
-        return LIB
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    flags = FLAGS + (["-DFM_DEBUG=1"] if debug else [])
+    if not force and not _stale(lib, srcs):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, os.path.splitext(os.path.basename(src))[0] + ".o")
+        cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr}")
@@ -58,14 +68,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv))

@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(480, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  FM_DEBUG_BEGIN();
   const int oi = blockIdx.x / p.H_kv, g = blockIdx.x - oi * p.H_kv;
   const int bk = p.order ? p.order[oi] : oi;
   const int nK = p.nK;
@@ -577,6 +578,7 @@ __global__ void __launch_bounds__(480, 1)
 
   tc_fence_before();
   __syncthreads();
+  FM_DEBUG_END(p.err);
   if (warp == 13) {
     __syncwarp();
     tc_fence_after();

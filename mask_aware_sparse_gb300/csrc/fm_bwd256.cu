@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(448, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  FM_DEBUG_BEGIN();
   // CTA = (launch-order position, kv head, head-dim half); the two halves of
   // one KV block are neighbours and share every tile in L2
   const int dh = blockIdx.x & 1;
@@ -474,6 +475,7 @@ __global__ void __launch_bounds__(448, 1)
 
   tc_fence_before();
   __syncthreads();
+  FM_DEBUG_END(p.err);
   if (warp == 13) {
     __syncwarp();
     tc_fence_after();

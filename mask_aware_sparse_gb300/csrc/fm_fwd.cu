@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(320, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  FM_DEBUG_BEGIN();
   // heads per unit for the whole grid: 2 when the GQA group has two or more
   // query heads; an odd group also has single-head units
   const int tmax = p.G >= 2 ? 2 : 1;
@@ -736,6 +737,7 @@ __global__ void __launch_bounds__(320, 1)
   if (warp < 8 && lane == 0) bulk_wait_group_read0();
   tc_fence_before();
   __syncthreads();
+  FM_DEBUG_END(p.err);
   if (warp == 9) {
     __syncwarp();
     tc_fence_after();

@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(256, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  FM_DEBUG_BEGIN();
   // unit: (b, qb) from the launch order, query head h (fastest: the heads of
   // one GQA group run side by side and share K / V tiles in L2)
   const int oi = blockIdx.x / p.H_q, h = blockIdx.x - oi * p.H_q;
@@ -434,6 +435,7 @@ __global__ void __launch_bounds__(256, 1)
   if (warp < 4 && lane == 0) bulk_wait_group_read0();
   tc_fence_before();
   __syncthreads();
+  FM_DEBUG_END(p.err);
   if (warp == 5) {
     __syncwarp();
     tc_fence_after();

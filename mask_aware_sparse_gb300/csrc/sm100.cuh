@@ -29,6 +29,55 @@ enum : int {
 
 __device__ __forceinline__ void record_error(int* err, int bits) { atomicOr(err, bits); }
 
+// ------------------------------------------------------------- debug build
+// With FM_DEBUG defined (the library's debug build, libfm_debug.so), every
+// wrapper below checks what it is handed: shared-memory addresses inside the
+// dynamic window and aligned, TMA x coordinates on a 16-byte boundary, TMEM
+// lane / column ranges. A failed check skips the access (a skipped TMA load
+// leaves its barrier short, so the kernel's bounded waits end it) and sets a
+// CTA flag that FM_DEBUG_END turns into FM_DEV_ERR_DEBUG in the device error
+// word: a bad index on a new kernel becomes a status on the host, not a fault.
+// Without FM_DEBUG the checks compile away.
+enum : int { FM_DEV_ERR_DEBUG = 8 };
+#ifdef FM_DEBUG
+extern __shared__ uint8_t fm_debug_dyn_smem[];  // the start of the dynamic shared memory
+static __shared__ int fm_debug_flag;
+__device__ __forceinline__ bool dbg(bool ok) {
+  if (!ok) atomicOr(&fm_debug_flag, 1);
+  return ok;
+}
+__device__ __forceinline__ uint32_t dyn_smem_size() {
+  uint32_t r;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ bool smem_range(uint32_t addr, uint32_t bytes, uint32_t align) {
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(fm_debug_dyn_smem));
+  return (addr % align) == 0 && addr >= base && addr + bytes <= base + dyn_smem_size();
+}
+__device__ __forceinline__ bool tmem_range(uint32_t taddr, uint32_t cols) {
+  const uint32_t lane = taddr >> 16, col = taddr & 0xffffu;
+  return (lane & 31u) == 0 && lane < 128 && col + cols <= 512;
+}
+#define FM_DBG(cond) (::fm::dbg(cond))
+#define FM_DEBUG_BEGIN()                  \
+  do {                                    \
+    if (threadIdx.x == 0) fm_debug_flag = 0; \
+  } while (0)
+#define FM_DEBUG_END(err)                                                              \
+  do {                                                                                 \
+    if (threadIdx.x == 0 && fm_debug_flag) ::fm::record_error((err), ::fm::FM_DEV_ERR_DEBUG); \
+  } while (0)
+#else
+#define FM_DBG(cond) true
+#define FM_DEBUG_BEGIN() \
+  do {                   \
+  } while (0)
+#define FM_DEBUG_END(err) \
+  do {                    \
+  } while (0)
+#endif
+
 // True once any kernel recorded a timeout that the host has not cleared yet.
 // Pipelined kernels check it on entry so that a broken pipeline costs one wave
 // of bounded waits, not one per CTA.
@@ -131,6 +180,7 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
 // 3-D tiled store from shared memory (bulk group; rows outside the tensor
 // are not written). Wait with bulk_wait_group_read0 before reusing the source.
 __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int32_t x, int32_t y, int32_t z) {
+  if (!FM_DBG(smem_range(src, 16, 16) && (x & 7) == 0)) return;
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(tmap)),
                "r"(src), "r"(x), "r"(y), "r"(z)
@@ -142,6 +192,7 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, 
 // 3-D tiled reduce-add (fp32) of a shared-memory box into global memory
 // (bulk group; rows outside the tensor are skipped).
 __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, const void* src, int32_t x, int32_t y, int32_t z) {
+  if (!FM_DBG(smem_range(smem_u32(src), 16, 16) && (x & 3) == 0)) return;
   asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(tmap)),
                "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
@@ -150,6 +201,7 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, const void* 
 // 3-D tiled load: coordinates are (x = innermost element, y, z).
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y,
                                             int32_t z) {
+  if (!FM_DBG(smem_range(smem_u32(dst), 16, 128) && smem_range(smem_u32(bar), 8, 8) && (x & 7) == 0)) return;
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
@@ -158,6 +210,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_
 }
 // Untiled bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  if (!FM_DBG(smem_range(smem_u32(dst), bytes, 16) && (reinterpret_cast<uintptr_t>(src) & 15) == 0 && (bytes & 15) == 0)) return;
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst)),
@@ -188,6 +241,7 @@ __device__ __forceinline__ void red_add_v4_f32(float* dst, float4 v) {
 }
 
 __device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
+  if (!FM_DBG(smem_range(addr, 4, 4))) return;
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
@@ -280,6 +334,7 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accumulate) {
+  if (!FM_DBG(tmem_range(d_tmem, 1))) return;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -290,6 +345,7 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t
 // D[tmem] (+)= A[tmem] * B[smem]
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accumulate) {
+  if (!FM_DBG(tmem_range(d_tmem, 1) && tmem_range(a_tmem, 1))) return;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -300,6 +356,7 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // 8-bit operands (kind::f8f6f4): D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
+  if (!FM_DBG(tmem_range(d_tmem, 1))) return;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -310,6 +367,7 @@ __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t adesc, uint6
 // 8-bit operands: D[tmem] (+)= A[tmem] * B[smem]
 __device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
+  if (!FM_DBG(tmem_range(d_tmem, 1) && tmem_range(a_tmem, 1))) return;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -327,6 +385,7 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 // ------------------------------------------------------- TMEM <-> registers
 // 32 lanes x 32 columns of 32-bit: thread t of the warp gets lane (base+t).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  if (!FM_DBG(__all_sync(0xffffffffu, tmem_range(taddr, 32)))) return;
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -339,6 +398,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  if (!FM_DBG(__all_sync(0xffffffffu, tmem_range(taddr, 16)))) return;
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -349,6 +409,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  if (!FM_DBG(__all_sync(0xffffffffu, tmem_range(taddr, 16)))) return;
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
@@ -357,6 +418,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  if (!FM_DBG(__all_sync(0xffffffffu, tmem_range(taddr, 32)))) return;
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -386,6 +448,7 @@ __device__ __forceinline__ int lds_s32(uint32_t addr) {
   return v;
 }
 __device__ __forceinline__ void sts_b32x4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  if (!FM_DBG(smem_range(addr, 16, 16))) return;
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
