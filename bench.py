@@ -647,8 +647,8 @@ def run_compose(args, cfg):
     """Forward + backward through one of the binding's compositions, on the
     workload's own mask written in that form (so the work and the metric are
     the workload's): `per_head` gives every query head its own copy of the
-    vectors (fm_attn_per_head: one classify + forward + backward per batch
-    entry and query head); `multi_interval` writes each key column's visible
+    vectors (fm_attn_per_head: one classification over the B * H_q vector
+    rows, one forward and one backward launch over every head); `multi_interval` writes each key column's visible
     rows [j, LTS_j) as two inclusive intervals split at their midpoint
     (fm_attn_multi_interval: per interval classify + forward, the log-sum-exp
     merge, per interval backward, the sums). The latter needs a causal mask

@@ -185,6 +185,28 @@ fm_status fm_attn_bwd(const fm_problem* p, const void* q, const void* k, const v
                       void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Per-head mask vectors: one set of four vectors per query head, lts..ute
+ * (B, H_q, N_kv) int32 (the FlashMask Guide's operator takes its vectors per
+ * sample; a mask that differs by head is the same representation one level
+ * finer). Everything else is fm_attn_fwd / fm_attn_bwd, except:
+ *   - the queues come from fm_classify_tiles run on the vectors as B * H_q
+ *     rows (an fm_problem with B' = B * H_q), so row (b * H_q + h) holds
+ *     query head h's tiles;
+ *   - every work unit is one head (two heads of a unit would need one queue);
+ *   - d must be 64 or 128 and H_q / H_kv at most 64.
+ * Workspaces: fm_attn_fwd_heads_workspace_bytes (one order entry per queue
+ * row) and fm_attn_bwd_workspace_bytes.
+ * ------------------------------------------------------------------------- */
+size_t fm_attn_fwd_heads_workspace_bytes(const fm_problem* p);
+fm_status fm_attn_fwd_heads(const fm_problem* p, const void* q, const void* k, const void* v, const int32_t* lts,
+                            const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
+                            const int32_t* q_queue, void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+fm_status fm_attn_bwd_heads(const fm_problem* p, const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, const int32_t* lts, const int32_t* lte,
+                            const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
+                            void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * One forward + backward from HOST buffers. (No counterpart in the pages: an
  * end-to-end convenience over the calls above.)
  *

@@ -7,14 +7,16 @@ is missing (build it with `mask_aware_sparse_gb300.build.build()`), so there
 is no silent fallback.
 
 Functions carry the names of the C entry points:
-  fm_classify_tiles, fm_attn_fwd, fm_attn_fwd_fp8, fm_attn_bwd, fm_attn_fwd_bwd_host (host buffers in
+  fm_classify_tiles, fm_attn_fwd, fm_attn_fwd_fp8, fm_attn_bwd, fm_attn_fwd_heads and
+  fm_attn_bwd_heads (per-head mask vectors), fm_attn_fwd_bwd_host (host buffers in
   and out, device workspace), fm_localize, fm_device_status,
   fm_selftest_wait_timeout, fm_profile_enable, fm_profile_read, fm_launch_count,
   fm_from_fms_fme, fm_merge_parts, fm_sum_parts, fm_chunk_loads,
   fm_balance_chunks, fm_needed_chunks (host code: the chunk balancer and the
   K / V exchange plan for context parallelism);
-plus fm_attn_multi_interval and fm_attn_per_head (multi-interval and per-head
-masks as sequences of library calls) and flashmask_attention (autograd wrapper: the classification, forward
+plus fm_classify_tiles_heads (fm_classify_tiles over the B * H_q rows of
+per-head vectors), fm_attn_multi_interval and fm_attn_per_head (multi-interval
+and per-head masks as sequences of library calls) and flashmask_attention (autograd wrapper: the classification, forward
 and backward calls in one differentiable op).
 """
 from __future__ import annotations
@@ -74,6 +76,9 @@ _SIGS = {
     "fm_attn_fwd_fp8": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 3 + [ctypes.c_float] * 3 + [_P] * 8
                         + [_P, ctypes.c_size_t, _P]),
     "fm_attn_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
+    "fm_attn_fwd_heads_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
+    "fm_attn_fwd_heads": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 11 + [_P, ctypes.c_size_t, _P]),
+    "fm_attn_bwd_heads": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 15 + [_P, ctypes.c_size_t, _P]),
     "fm_attn_host_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
     "fm_attn_fwd_bwd_host": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 13 + [_P, ctypes.c_size_t, _P]),
     "fm_attn_bwd": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 15 + [_P, ctypes.c_size_t, _P]),
@@ -178,10 +183,12 @@ def _bf16_ok(*ts):
     _same_cuda(**{f"tensor {i}": t for i, t in enumerate(ts)})
 
 
-def _attn_args(q, k, v, vec, queues, *, backward, o=None, lse=None, do=None, dq=None, dk=None, dv=None, ws=None):
+def _attn_args(q, k, v, vec, queues, *, backward, o=None, lse=None, do=None, dq=None, dk=None, dv=None, ws=None,
+               heads=False):
     """Shapes, dtypes and devices of an attention call, checked before the library
     sees any pointer (the C ABI receives bare pointers and cannot check them).
-    Shape checks come first, so a mismatch is reported as such."""
+    Shape checks come first, so a mismatch is reported as such. heads: per-head
+    mask vectors (B, H_q, N_kv) and queues over B * H_q rows."""
     _need(isinstance(q, torch.Tensor) and q.dim() == 4, "q must be a (B, H_q, N, d) tensor")
     B, Hq, N, d = q.shape
     _need(isinstance(k, torch.Tensor) and k.dim() == 4 and k.shape[0] == B and k.shape[3] == d,
@@ -191,8 +198,9 @@ def _attn_args(q, k, v, vec, queues, *, backward, o=None, lse=None, do=None, dq=
     _like(q, "q", (B, Hq, N, d), torch.bfloat16)
     _like(k, "k", (B, Hkv, Nk, d), torch.bfloat16)
     _like(v, "v", (B, Hkv, Nk, d), torch.bfloat16)
+    vshape = (B, Hq, Nk) if heads else (B, Nk)
     for i, x in enumerate(vec):
-        _like(x, f"mask vector {i}", (B, Nk), torch.int32)
+        _like(x, f"mask vector {i}", vshape, torch.int32)
     for name, t in (("o", o), ("do", do), ("dq", dq)):
         if t is not None:
             _like(t, name, (B, Hq, N, d), torch.bfloat16)
@@ -208,10 +216,12 @@ def _attn_args(q, k, v, vec, queues, *, backward, o=None, lse=None, do=None, dq=
     _need((queues.block_m, queues.block_n) == (bm, bn),
           f"queues were built with {queues.block_m} x {queues.block_n} tiles; the kernels need {bm} x {bn}")
     nq, nk = -(-N // bm), -(-Nk // bn)
-    off, qu, nrows = (queues.k_off, queues.k_queue, B * nk) if backward else (queues.q_off, queues.q_queue, B * nq)
+    R = B * Hq if heads else B  # queue rows per Q (K) block
+    off, qu, nrows = (queues.k_off, queues.k_queue, R * nk) if backward else (queues.q_off, queues.q_queue, R * nq)
     _like(off, "queue offsets", (nrows + 1,), torch.int32)
     _need(isinstance(qu, torch.Tensor) and qu.dtype == torch.int32 and qu.is_contiguous()
-          and qu.numel() >= max(1, B * nq * nk), "queue entries must be int32 with capacity B * nQ * nK")
+          and qu.numel() >= max(1, R * nq * nk),
+          f"queue entries must be int32 with capacity {'B * H_q' if heads else 'B'} * nQ * nK")
     _same_cuda(q=q, k=k, v=v, o=o, lse=lse, do=do, dq=dq, dk=dk, dv=dv, ws=ws, queue_offsets=off, queue=qu,
                **{f"mask vector {i}": x for i, x in enumerate(vec)})
 
@@ -479,42 +489,67 @@ def fm_attn_multi_interval(q, k, v, fms, fme, *, scale: float, do=None, stream=N
     return o, lse, dq, dk, dv
 
 
+def fm_classify_tiles_heads(lts, lte, uts, ute, *, causal: bool, n_rows=None, stream=None):
+    """Queues for per-head mask vectors (B, H_q, N_kv): fm_classify_tiles over
+    the B * H_q rows, row b * H_q + h holding query head h of batch entry b."""
+    _need(isinstance(lts, torch.Tensor) and lts.dim() == 3, "per-head mask vectors must be (B, H_q, N_kv)")
+    B, Hq, Nk = lts.shape
+    for i, x in enumerate((lts, lte, uts, ute)):
+        _like(x, f"mask vector {i}", (B, Hq, Nk), torch.int32)
+    return fm_classify_tiles(*(x.view(B * Hq, Nk) for x in (lts, lte, uts, ute)), causal=causal, n_rows=n_rows,
+                             stream=stream)
+
+
+def fm_attn_fwd_heads(q, k, v, lts, lte, uts, ute, queues: TileQueues, *, scale: float, causal: bool, o=None,
+                      lse=None, ws=None, stream=None):
+    """Forward with per-head mask vectors (B, H_q, N_kv) and the queues of
+    fm_classify_tiles_heads: returns (O bf16, LSE fp32)."""
+    _attn_args(q, k, v, (lts, lte, uts, ute), queues, backward=False, o=o, lse=lse, ws=ws, heads=True)
+    B, Hq, N, d = q.shape
+    prob = _problem(B, Hq, k.shape[1], N, d, scale, causal, k.shape[2])
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    wsb = lib().fm_attn_fwd_heads_workspace_bytes(ctypes.byref(prob))
+    if ws is None or ws.numel() < wsb:
+        ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=q.device)
+    _check(lib().fm_attn_fwd_heads(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(lts), _ptr(lte), _ptr(uts),
+                                   _ptr(ute), _ptr(queues.q_off), _ptr(queues.q_queue), _ptr(o), _ptr(lse),
+                                   _ptr(ws), ctypes.c_size_t(wsb), _stream(stream)), "fm_attn_fwd_heads")
+    return o, lse
+
+
+def fm_attn_bwd_heads(q, k, v, o, lse, do, lts, lte, uts, ute, queues: TileQueues, *, scale: float, causal: bool,
+                      dq=None, dk=None, dv=None, ws=None, stream=None):
+    """Backward with per-head mask vectors: returns (dQ, dK, dV) bf16."""
+    _attn_args(q, k, v, (lts, lte, uts, ute), queues, backward=True, o=o, lse=lse, do=do, dq=dq, dk=dk, dv=dv,
+               ws=ws, heads=True)
+    B, Hq, N, d = q.shape
+    prob = _problem(B, Hq, k.shape[1], N, d, scale, causal, k.shape[2])
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    wsb = lib().fm_attn_bwd_workspace_bytes(ctypes.byref(prob))
+    if ws is None or ws.numel() < wsb:
+        ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=q.device)
+    _check(lib().fm_attn_bwd_heads(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                   _ptr(lts), _ptr(lte), _ptr(uts), _ptr(ute), _ptr(queues.k_off),
+                                   _ptr(queues.k_queue), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                                   ctypes.c_size_t(wsb), _stream(stream)), "fm_attn_bwd_heads")
+    return dq, dk, dv
+
+
 def fm_attn_per_head(q, k, v, lts, lte, uts, ute, *, causal: bool, scale: float, do=None, stream=None):
     """Attention with one set of mask vectors per query head: lts..ute are
-    (B, H_q, N_kv) int32 CUDA tensors. Library calls only: for every (batch
-    entry, query head) a classification and a forward (and backward) of that
-    head's rows against its kv head; each kv head's dK, dV summed over its query
-    heads by fm_sum_parts. Returns (o, lse) or (o, lse, dq, dk, dv)."""
-    _bf16_ok(q, k, v)
-    B, Hq, N, d = q.shape
-    Hkv = k.shape[1]
-    G = Hq // Hkv
-    for x in (lts, lte, uts, ute):
-        if x.dim() != 3 or x.shape[:2] != (B, Hq) or x.dtype != torch.int32 or not x.is_contiguous():
-            raise ValueError("per-head vectors must be contiguous int32 (B, H_q, N_kv) tensors")
-    o = torch.empty_like(q)
-    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
-    if do is not None:
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    for b in range(B):
-        for g in range(Hkv):
-            kb, vb = k[b:b + 1, g:g + 1], v[b:b + 1, g:g + 1]
-            dks, dvs = [], []
-            for h in range(g * G, (g + 1) * G):
-                vec = [x[b:b + 1, h] for x in (lts, lte, uts, ute)]
-                qs = fm_classify_tiles(*vec, causal=causal, n_rows=N, stream=stream)
-                qh, oh, lh = q[b:b + 1, h:h + 1], o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1]
-                fm_attn_fwd(qh, kb, vb, *vec, qs, scale=scale, causal=causal, o=oh, lse=lh, stream=stream)
-                if do is not None:
-                    _, dk_h, dv_h = fm_attn_bwd(qh, kb, vb, oh, lh, do[b:b + 1, h:h + 1], *vec, qs, scale=scale,
-                                                causal=causal, dq=dq[b:b + 1, h:h + 1], stream=stream)
-                    dks.append(dk_h)
-                    dvs.append(dv_h)
-            if do is not None:
-                fm_sum_parts(dks, out=dk[b:b + 1, g:g + 1], stream=stream)
-                fm_sum_parts(dvs, out=dv[b:b + 1, g:g + 1], stream=stream)
+    (B, H_q, N_kv) int32 CUDA tensors. One classification over the B * H_q
+    vector rows, one forward and (with do) one backward, each a single launch
+    over every head. Returns (o, lse) or (o, lse, dq, dk, dv)."""
+    qs = fm_classify_tiles_heads(lts, lte, uts, ute, causal=causal, n_rows=q.shape[2] if q.dim() == 4 else None,
+                                 stream=stream)
+    o, lse = fm_attn_fwd_heads(q, k, v, lts, lte, uts, ute, qs, scale=scale, causal=causal, stream=stream)
     if do is None:
         return o, lse
+    dq, dk, dv = fm_attn_bwd_heads(q, k, v, o, lse, do, lts, lte, uts, ute, qs, scale=scale, causal=causal,
+                                   stream=stream)
     return o, lse, dq, dk, dv
 
 

@@ -267,6 +267,57 @@ fm_status fm_attn_fwd(const fm_problem* p, const void* q, const void* k, const v
                               static_cast<cudaStream_t>(stream), err));
 }
 
+size_t fm_attn_fwd_heads_workspace_bytes(const fm_problem* p) {
+  bool empty = false;
+  if (check_problem(p, &empty) != FM_OK || empty) return 0;
+  return fwd_heads_ws_bytes(*p);
+}
+
+// Per-head masks: d = 64 or 128 and at most 64 query heads per kv head (the
+// backward stages one queue per head of a group).
+static fm_status check_heads_shape(const fm_problem* p) {
+  if (p->d != 64 && p->d != 128) return FM_ERR_UNSUPPORTED;
+  if (p->H_q / p->H_kv > 64) return FM_ERR_UNSUPPORTED;
+  return FM_OK;
+}
+
+fm_status fm_attn_fwd_heads(const fm_problem* p, const void* q, const void* k, const void* v, const int32_t* lts,
+                            const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
+                            const int32_t* q_queue, void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  bool empty = false;
+  fm_status st = check_problem(p, &empty);
+  if (st != FM_OK || empty) return st;
+  if ((st = check_heads_shape(p)) != FM_OK) return st;
+  if (!q || !k || !v || !lts || !lte || !uts || !ute || !q_off || !q_queue || !o || !lse) return FM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FM_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < fwd_heads_ws_bytes(*p)) return FM_ERR_WORKSPACE;
+  int* err = device_error_word();
+  if (!err) return FM_ERR_CUDA;
+  return from_cuda(launch_fwd_heads(*p, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws,
+                                    static_cast<cudaStream_t>(stream), err));
+}
+
+fm_status fm_attn_bwd_heads(const fm_problem* p, const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, const int32_t* lts, const int32_t* lte,
+                            const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
+                            void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+  bool empty = false;
+  fm_status st = check_problem(p, &empty);
+  if (st != FM_OK || empty) return st;
+  if ((st = check_heads_shape(p)) != FM_OK) return st;
+  if (!q || !k || !v || !o || !lse || !dout || !lts || !lte || !uts || !ute || !k_off || !k_queue || !dq || !dk ||
+      !dv)
+    return FM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv))
+    return FM_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < bwd_ws_bytes(*p)) return FM_ERR_WORKSPACE;
+  int* err = device_error_word();
+  if (!err) return FM_ERR_CUDA;
+  return from_cuda(launch_bwd(*p, q, k, v, o, lse, dout, lts, lte, uts, ute, k_off, k_queue, dq, dk, dv, ws,
+                              static_cast<cudaStream_t>(stream), err, true));
+}
+
 fm_status fm_attn_fwd_fp8(const fm_problem* p, const void* q, const void* k, const void* v, float q_scale,
                           float k_scale, float v_scale, const int32_t* lts, const int32_t* lte, const int32_t* uts,
                           const int32_t* ute, const int32_t* q_off, const int32_t* q_queue, void* o, float* lse,

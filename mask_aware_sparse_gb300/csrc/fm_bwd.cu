@@ -77,7 +77,10 @@ struct BwdCfg {
   static constexpr int ROW_OFF = ZERO_OFF + ZERO_BYTES;    // STAGES x {nl[64], D[64]} fp32
   static constexpr int QUEUE_CAP = 1024;                    // queue entries staged in shared memory
   static constexpr int QUEUE_OFF = ROW_OFF + STAGES * 512;
-  static constexpr int BAR_OFF = QUEUE_OFF + QUEUE_CAP * 4;
+  // per-head masks: each head's first staged entry (prefix, kMaxHeads + 1) and
+  // its queue start in k_queue (kMaxHeads)
+  static constexpr int HEADS_OFF = QUEUE_OFF + QUEUE_CAP * 4;
+  static constexpr int BAR_OFF = HEADS_OFF + 1024;
   static constexpr int B_KV = 0;
   static constexpr int B_QFULL = 1;
   static constexpr int B_QEMPTY = B_QFULL + STAGES;
@@ -115,6 +118,9 @@ struct BwdParams {
   int* err;
 };
 
+// Query heads per GQA group with per-head mask vectors (the staged prefix).
+constexpr int kMaxHeads = 64;
+
 // Decode unit u of a CTA: query head (h) of the group, queue position, half.
 // The CTA's queue segment is staged in shared memory (s_queue) when it fits,
 // so no role waits on a dependent global load per unit.
@@ -135,7 +141,26 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams& p, int u, int L, in
   return r;
 }
 
-template <int D>
+// The same with per-head mask vectors: head hi of the group owns the units
+// [2 hoff[hi], 2 hoff[hi + 1]) (its own queue for this KV block); the staged
+// entries are the heads' queues back to back. hi is the caller's cursor (units
+// are visited in increasing order).
+__device__ __forceinline__ Unit decode_unit_ph(const BwdParams& p, int u, int g, bool force_part, uint32_t s_queue,
+                                               int qcap, const int* hoff, int& hi) {
+  while (u >= 2 * hoff[hi + 1]) ++hi;
+  const int rem = u - 2 * hoff[hi];
+  const int pos = hoff[hi] + (rem >> 1);
+  const int e = (pos < qcap) ? lds_s32(s_queue + 4 * pos) : p.k_queue[hoff[kMaxHeads + 1 + hi] + (rem >> 1)];
+  Unit r;
+  r.h = g * p.G + hi;
+  r.qb = e >> 1;
+  r.half = rem & 1;
+  r.part = (e & 1) | (force_part ? 1 : 0);
+  return r;
+}
+
+// PH: per-head mask vectors (B, H_q, N_kv) and queues over B * H_q rows.
+template <int D, bool PH>
 __global__ void __launch_bounds__(480, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -155,9 +180,17 @@ __global__ void __launch_bounds__(480, 1)
   const int bk = p.order ? p.order[oi] : oi;
   const int nK = p.nK;
   const int b = bk / nK, kb = bk - b * nK;
-  const int kbeg = p.k_off[bk];
-  const int L = p.k_off[bk + 1] - kbeg;
-  const int U = 2 * L * p.G;
+  int kbeg = 0, L = 0;  // per-head masks: L sums the heads' queue lengths
+  if constexpr (PH) {
+    for (int hi = 0; hi < p.G; ++hi) {
+      const int r = (b * p.H_q + g * p.G + hi) * nK + kb;
+      L += p.k_off[r + 1] - p.k_off[r];
+    }
+  } else {
+    kbeg = p.k_off[bk];
+    L = p.k_off[bk + 1] - kbeg;
+  }
+  const int U = PH ? 2 * L : 2 * L * p.G;
   const int k0 = kb * 128;
   const bool force_part = (kb == nK - 1) && (p.Nk & 127);
 
@@ -198,10 +231,35 @@ __global__ void __launch_bounds__(480, 1)
     fence_mbar_init();
   }
   const uint32_t s_queue = smem_u32(smem + C::QUEUE_OFF);
+  int* hoff = reinterpret_cast<int*>(smem + C::HEADS_OFF);
   {
     int* sq = reinterpret_cast<int*>(smem + C::QUEUE_OFF);
-    for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) sq[t] = p.k_queue[kbeg + t];
+    if constexpr (PH) {
+      if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int hi = 0; hi < p.G; ++hi) {
+          const int r = (b * p.H_q + g * p.G + hi) * nK + kb;
+          hoff[hi] = acc;
+          hoff[kMaxHeads + 1 + hi] = p.k_off[r];
+          acc += p.k_off[r + 1] - p.k_off[r];
+        }
+        hoff[p.G] = acc;
+      }
+      __syncthreads();
+      for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) {
+        int hi = 0;
+        while (hi + 1 < p.G && hoff[hi + 1] <= t) ++hi;
+        sq[t] = p.k_queue[hoff[kMaxHeads + 1 + hi] + (t - hoff[hi])];
+      }
+    } else {
+      for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) sq[t] = p.k_queue[kbeg + t];
+    }
   }
+  // the unit decoder of every role (a cursor over the heads with per-head masks)
+  auto decode = [&](int u, int& hcur) -> Unit {
+    if constexpr (PH) return decode_unit_ph(p, u, g, force_part, s_queue, C::QUEUE_CAP, hoff, hcur);
+    else return decode_unit(p, u, L, kbeg, g, force_part, s_queue, C::QUEUE_CAP);
+  };
   if (C::ZERO_BYTES > 0) {
     uint4* z = reinterpret_cast<uint4*>(smem + C::ZERO_OFF);
     for (int x = threadIdx.x; x < C::ZERO_BYTES / 16; x += blockDim.x) z[x] = make_uint4(0, 0, 0, 0);
@@ -231,8 +289,9 @@ __global__ void __launch_bounds__(480, 1)
         tma_load_3d(smem + C::K_OFF + x * 16384, &tk, &bars[C::B_KV], x * 64, k0, b * p.H_kv + g);
         tma_load_3d(smem + C::V_OFF + x * 16384, &tv, &bars[C::B_KV], x * 64, k0, b * p.H_kv + g);
       }
+      int hcur = 0;  // head cursor (per-head masks)
       for (int u = 0; u < U && ok; ++u) {
-        const Unit un = decode_unit(p, u, L, kbeg, g, force_part, s_queue, C::QUEUE_CAP);
+        const Unit un = decode(u, hcur);
         const int stage = u % S;
         ok = mbar_wait(&bars[C::B_QEMPTY + stage], ((uint32_t)(u / S) & 1u) ^ 1u, abort_flag, p.err);
         if (!ok) break;
@@ -382,8 +441,12 @@ __global__ void __launch_bounds__(480, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     int lo0 = 0, lo1 = 0, up0 = 0, up1 = 0;
     const bool dead = kcol >= p.Nk;
-    if (!dead) {
-      const size_t vi = (size_t)b * p.Nk + kcol;
+    // this thread's key column's masked intervals, from vector row vrow (the
+    // batch entry, or with per-head masks the (batch entry, head))
+    auto load_mask = [&](int vrow) {
+      lo0 = lo1 = up0 = up1 = 0;
+      if (dead) return;
+      const size_t vi = (size_t)vrow * p.Nk + kcol;
       int a0 = p.lts[vi], a1 = p.lte[vi], u0 = p.uts[vi], u1 = p.ute[vi];
       if ((a0 | a1 | u0 | u1) < 0 || a0 > p.N || a1 > p.N || u0 > p.N || u1 > p.N) record_error(p.err, FM_DEV_ERR_RANGE);
       a0 = min(max(a0, 0), p.N);
@@ -392,7 +455,9 @@ __global__ void __launch_bounds__(480, 1)
       u1 = min(max(u1, 0), p.N);
       if (a0 < a1) { lo0 = a0; lo1 = a1; }
       if (u0 < u1) { up0 = u0; up1 = u1; }
-    }
+    };
+    int mhead = -1;  // the head whose vectors are loaded (per-head masks)
+    if constexpr (!PH) load_mask(b);
     const float sl2 = p.scale_log2;
     const bool causal = p.causal != 0;
     const uint32_t s_rows = smem_u32(smem + C::ROW_OFF);
@@ -400,8 +465,15 @@ __global__ void __launch_bounds__(480, 1)
     const uint32_t tS0 = tbase + lane_off + T_S + 32u * half;  // + 64 for S buffer 1
     const uint32_t tDP = tbase + lane_off + T_DP + 32u * half;
     bool ok = true;
+    int hcur = 0;  // head cursor (per-head masks)
     for (int u = 0; u < U && ok; ++u) {
-      const Unit un = decode_unit(p, u, L, kbeg, g, force_part, s_queue, C::QUEUE_CAP);
+      const Unit un = decode(u, hcur);
+      if constexpr (PH) {
+        if (un.h != mhead) {
+          load_mask(b * p.H_q + un.h);
+          mhead = un.h;
+        }
+      }
       const int stage = u % S;
       const int r0 = un.qb * 128 + un.half * 64;
       ok = __all_sync(kFull, mbar_wait(&bars[C::B_QFULL + stage], (uint32_t)(u / S) & 1u, abort_flag, p.err));
@@ -512,8 +584,9 @@ __global__ void __launch_bounds__(480, 1)
     const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
     const uint32_t xp = smem_u32(smem + C::XPOSE_OFF) + w4 * 4096;
     bool ok = true;
+    int hcur = 0;  // head cursor (per-head masks)
     for (int u = 0; u < U && ok; ++u) {
-      const Unit un = decode_unit(p, u, L, kbeg, g, force_part, s_queue, C::QUEUE_CAP);
+      const Unit un = decode(u, hcur);
       ok = __all_sync(kFull, mbar_wait(&bars[C::B_DQFULL], (uint32_t)u & 1u, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
@@ -701,7 +774,7 @@ BwdWs carve(const fm_problem& P, void* ws) {
   return r;
 }
 
-template <int D>
+template <int D, bool PH = false>
 cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, const void* v, const void* o,
                          const float* lse, const void* dout, void* dq, const BwdParams& prm0, const BwdWs& w,
                          cudaStream_t s) {
@@ -721,7 +794,8 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   // where natural order was 19% slower: its CTAs then reduce into the same
   // dQ rows at once).
   // (d = 256 runs two CTAs per KV block, one per head-dim half)
-  const bool natural = use_natural_order((D == 256 ? 2LL : 1LL) * P.B * nK * P.H_kv);
+  // (per-head masks: natural order; the order kernel reads one queue per (batch, KV block))
+  const bool natural = PH || use_natural_order((D == 256 ? 2LL : 1LL) * P.B * nK * P.H_kv);
   if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(prm0.k_off, P.B * nK, w.order);
   // 3. main kernel
   if constexpr (D == 256) {
@@ -742,7 +816,7 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   using C = BwdCfg<D>;
   static bool attr_done = false;
   if (!attr_done) {
-    e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    e = cudaFuncSetAttribute(bwd_kernel<D, PH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -751,7 +825,7 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
     KernelTimer timer(s, kTimedBwd);
     BwdParams prm = prm0;
     if (natural) prm.order = nullptr;
-    bwd_kernel<D><<<(unsigned)grid, 480, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
+    bwd_kernel<D, PH><<<(unsigned)grid, 480, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
   }
   }
   // 4. dQ = bf16(scale * dQacc)
@@ -776,7 +850,7 @@ size_t bwd_ws_bytes(const fm_problem& P) {
 cudaError_t launch_bwd(const fm_problem& P, const void* q, const void* k, const void* v, const void* o,
                        const float* lse, const void* dout, const int32_t* lts, const int32_t* lte,
                        const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
-                       void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err) {
+                       void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err, bool per_head) {
   const int Nk = kv_rows(P);
   const int nK = (Nk + kTile - 1) / kTile;
   const long long grid = (long long)P.B * nK * P.H_kv;
@@ -807,6 +881,12 @@ cudaError_t launch_bwd(const fm_problem& P, const void* q, const void* k, const 
   prm.scale = P.scale;
   prm.scale_log2 = P.scale * kLog2e;
   prm.err = err;
+  if (per_head) {
+    if (P.H_q / P.H_kv > kMaxHeads) return cudaErrorInvalidValue;
+    if (P.d == 128) return launch_bwd_d<128, true>(P, q, k, v, o, lse, dout, dq, prm, w, s);
+    if (P.d == 64) return launch_bwd_d<64, true>(P, q, k, v, o, lse, dout, dq, prm, w, s);
+    return cudaErrorInvalidValue;
+  }
   if (P.d == 256) return launch_bwd_d<256>(P, q, k, v, o, lse, dout, dq, prm, w, s);
   return (P.d == 128) ? launch_bwd_d<128>(P, q, k, v, o, lse, dout, dq, prm, w, s)
                       : launch_bwd_d<64>(P, q, k, v, o, lse, dout, dq, prm, w, s);

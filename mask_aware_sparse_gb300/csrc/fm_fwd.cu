@@ -116,7 +116,8 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   int B, H_q, H_kv, N, Nk, nQ, nK, G, PG, causal;  // N query rows, Nk key rows
-  int units;  // B * nQ * H_kv * PG work units
+  int units;  // B * nQ * H_kv * PG work units (per-head masks: B * H_q * nQ)
+  int per_head;  // mask vectors and queues per (batch, query head): one head per unit
   float scale_log2;
   float o_scale;  // multiplies O / l (the V dequantization scale of the FP8 forward; 1 otherwise)
   int* err;
@@ -128,11 +129,25 @@ constexpr unsigned kFull = 0xffffffffu;
 // One work unit: (batch b, Q block qb, a pair of query heads h0, h0 + 1 of KV
 // head g; T = 1 when the group has an odd head left over) and its queue.
 struct Unit {
-  int b, qb, g, h0, T, qbeg, n;
+  int b, qb, g, h0, T, qbeg, n, vrow;  // vrow: the row of the mask vectors
 };
 
 __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int k) {
   Unit u;
+  if (p.per_head) {
+    // queue rows in (batch, head, Q block) order, one head per unit
+    const int r = p.order ? p.order[k] : k;
+    const int bh = r / p.nQ;
+    u.qb = r - bh * p.nQ;
+    u.b = bh / p.H_q;
+    u.h0 = bh - u.b * p.H_q;
+    u.g = u.h0 / p.G;
+    u.T = 1;
+    u.qbeg = p.q_off[r];
+    u.n = p.q_off[r + 1] - u.qbeg;
+    u.vrow = bh;
+    return u;
+  }
   const int per = p.H_kv * p.PG;
   const int oi = k / per, gp = k - oi * per;
   u.g = gp / p.PG;
@@ -144,6 +159,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int k) {
   u.T = (2 * pp + 1 < p.G) ? 2 : 1;
   u.qbeg = p.q_off[bq];
   u.n = p.q_off[bq + 1] - u.qbeg;
+  u.vrow = u.b;
   return u;
 }
 
@@ -170,7 +186,7 @@ __global__ void __launch_bounds__(320, 1)
   FM_DEBUG_BEGIN();
   // heads per unit for the whole grid: 2 when the GQA group has two or more
   // query heads; an odd group also has single-head units
-  const int tmax = p.G >= 2 ? 2 : 1;
+  const int tmax = (p.G >= 2 && !p.per_head) ? 2 : 1;
 
   if (threadIdx.x == 0) {
     // an unread timeout from an earlier launch: skip the work, keep the CTA cheap
@@ -277,7 +293,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       k = __shfl_sync(kFull, k_next, 0);
       if (u.n <= 0) continue;
-      const size_t vbase = (size_t)u.b * p.Nk;
+      const size_t vbase = (size_t)u.vrow * p.Nk;
       for (int j = 0; j < u.n && ok; ++j) {
         const int e = queue_at(us, j);
         const int kb = e >> 1;
@@ -790,14 +806,18 @@ int32_t* fwd_noalloc_scratch() {
   return cached[dev];
 }
 
-// Forward workspace: the unit-order table (one int32 per Q block, padded to
+// Forward workspace: the unit-order table (one int32 per queue row: a Q block
+// of a batch entry, or of a (batch entry, head) with per-head masks; padded to
 // 256 bytes), then the work counter (256 bytes).
+static size_t order_bytes(long long rows) { return ((4 * (size_t)rows) + 255) & ~size_t(255); }
 static size_t fwd_order_bytes(const fm_problem& p) {
-  const size_t nQ = (size_t)(p.N + kTile - 1) / kTile;
-  return ((4 * (size_t)p.B * nQ) + 255) & ~size_t(255);
+  return order_bytes((long long)p.B * ((p.N + kTile - 1) / kTile));
 }
 
 size_t fwd_ws_bytes(const fm_problem& p) { return fwd_order_bytes(p) + 256; }
+size_t fwd_heads_ws_bytes(const fm_problem& p) {
+  return order_bytes((long long)p.B * p.H_q * ((p.N + kTile - 1) / kTile)) + 256;
+}
 
 // The persistent forward (d = 64, 128; bf16 or, with fp8, e4m3 Q / K / V whose
 // values are the stored ones times q_scale, k_scale, v_scale).
@@ -805,22 +825,24 @@ static cudaError_t launch_fwd_persistent(const fm_problem& P, const void* q, con
                                          const int32_t* lts, const int32_t* lte, const int32_t* uts,
                                          const int32_t* ute, const int32_t* q_off, const int32_t* q_queue, void* o,
                                          float* lse, void* ws, cudaStream_t s, int* err, bool fp8, float q_scale,
-                                         float k_scale, float v_scale) {
+                                         float k_scale, float v_scale, bool per_head = false) {
   const int nQ = (P.N + kTile - 1) / kTile;
   const int G = P.H_q / P.H_kv;
   const int PG = (G + 1) / 2;
-  const long long units = (long long)P.B * nQ * P.H_kv * PG;
+  // per-head masks: one unit per (batch, head, Q block), in the queues' row order
+  const long long units = per_head ? (long long)P.B * P.H_q * nQ : (long long)P.B * nQ * P.H_kv * PG;
+  const long long rows = per_head ? (long long)P.B * P.H_q * nQ : (long long)P.B * nQ;  // queue rows
   if (units > INT_MAX) return cudaErrorInvalidConfiguration;
   // unit order: longest queue first, or natural order for long passes
   // (units that run together then share K / V tiles in L2)
   const bool natural = use_natural_order(units);
   int32_t* order = natural ? nullptr : static_cast<int32_t*>(ws);
-  int* next_unit = reinterpret_cast<int*>(static_cast<char*>(ws) + fwd_order_bytes(P));
+  int* next_unit = reinterpret_cast<int*>(static_cast<char*>(ws) + order_bytes(rows));
   {
     cudaError_t e = cudaMemsetAsync(next_unit, 0, sizeof(int), s);
     if (e != cudaSuccess) return e;
   }
-  if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, P.B * nQ, order);
+  if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, (int)rows, order);
   CUtensorMap tq, tk, tv, to;
   const int Nk = kv_rows(P);
   if (fp8) {
@@ -856,6 +878,7 @@ static cudaError_t launch_fwd_persistent(const fm_problem& P, const void* q, con
   prm.PG = PG;
   prm.causal = P.causal ? 1 : 0;
   prm.units = (int)units;
+  prm.per_head = per_head ? 1 : 0;
   prm.scale_log2 = P.scale * q_scale * k_scale * 1.4426950408889634f;
   prm.o_scale = v_scale;
   prm.err = err;
@@ -872,6 +895,13 @@ cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const 
   if (P.d == 256) return launch_fwd256(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err);
   return launch_fwd_persistent(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err, false, 1.f, 1.f,
                                1.f);
+}
+
+cudaError_t launch_fwd_heads(const fm_problem& P, const void* q, const void* k, const void* v, const int32_t* lts,
+                             const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
+                             const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err) {
+  return launch_fwd_persistent(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err, false, 1.f, 1.f,
+                               1.f, true);
 }
 
 cudaError_t launch_fwd_fp8(const fm_problem& P, const void* q, const void* k, const void* v, float q_scale,

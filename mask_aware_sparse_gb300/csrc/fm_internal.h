@@ -36,6 +36,13 @@ cudaError_t launch_fwd(const fm_problem& p, const void* q, const void* k, const 
                        const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
                        const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err);
 
+// Forward with per-head mask vectors (fm_fwd.cu): vectors (B, H_q, N_kv) and
+// queues of a classification over B * H_q rows; one head per work unit.
+size_t fwd_heads_ws_bytes(const fm_problem& p);
+cudaError_t launch_fwd_heads(const fm_problem& P, const void* q, const void* k, const void* v, const int32_t* lts,
+                             const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
+                             const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err);
+
 // FP8 forward (fm_fwd.cu): e4m3 Q / K / V (value = stored x scale), d = 128,
 // bf16 O; same workspace as launch_fwd.
 cudaError_t launch_fwd_fp8(const fm_problem& P, const void* q, const void* k, const void* v, float q_scale,
@@ -58,7 +65,7 @@ size_t bwd_ws_bytes(const fm_problem& p);
 cudaError_t launch_bwd(const fm_problem& p, const void* q, const void* k, const void* v, const void* o,
                        const float* lse, const void* dout, const int32_t* lts, const int32_t* lte,
                        const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
-                       void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err);
+                       void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err, bool per_head = false);
 
 // Main kernel of the d = 256 backward (fm_bwd256.cu); row terms, launch
 // order and dQ conversion come from launch_bwd.

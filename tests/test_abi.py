@@ -245,3 +245,38 @@ def test_binding_refuses_host_and_mismatched_parts(lib):
         fm.fm_from_fms_fme(x, x)
     with pytest.raises(ValueError, match="same shape"):
         fm.fm_from_fms_fme(x, x[:32])
+
+
+def test_binding_checks_per_head_shapes(lib):
+    # per-head entry points: vectors are (B, H_q, N_kv) and the queues have
+    # B * H_q rows per Q (K) block; shared-shape vectors or shared-shape queues
+    # are refused before any pointer reaches the library
+    import torch
+
+    bf, i32 = torch.bfloat16, torch.int32
+    B, Hq, Hkv, N, d = 2, 4, 2, 256, 64
+    q = torch.zeros(B, Hq, N, d, dtype=bf)
+    k = torch.zeros(B, Hkv, N, d, dtype=bf)
+    lse = torch.zeros(B, Hq, N, dtype=torch.float32)
+    shared = [torch.zeros(B, N, dtype=i32) for _ in range(4)]
+    per = [torch.zeros(B, Hq, N, dtype=i32) for _ in range(4)]
+    nq = N // 128
+
+    def queues(rows):
+        return fm.TileQueues(torch.zeros(rows, nq, nq, dtype=torch.uint8), torch.zeros(rows * nq + 1, dtype=i32),
+                             torch.zeros(rows * nq * nq, dtype=i32), torch.zeros(rows * nq + 1, dtype=i32),
+                             torch.zeros(rows * nq * nq, dtype=i32), 128, 128)
+
+    with pytest.raises(ValueError, match="shape"):
+        fm.fm_attn_fwd_heads(q, k, k, *shared, queues(B * Hq), scale=0.1, causal=True)
+    with pytest.raises(ValueError, match="queue offsets"):
+        fm.fm_attn_fwd_heads(q, k, k, *per, queues(B), scale=0.1, causal=True)
+    with pytest.raises(ValueError, match="queue offsets"):
+        fm.fm_attn_bwd_heads(q, k, k, q, lse, q, *per, queues(B), scale=0.1, causal=True)
+    with pytest.raises(ValueError, match="H_q, N_kv"):
+        fm.fm_classify_tiles_heads(*shared, causal=True)
+    # right shapes: only the device is left to refuse
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.fm_attn_fwd_heads(q, k, k, *per, queues(B * Hq), scale=0.1, causal=True)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.fm_attn_bwd_heads(q, k, k, q, lse, q, *per, queues(B * Hq), scale=0.1, causal=True)
