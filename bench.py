@@ -528,9 +528,9 @@ def run_ours(args, cfg):
 # the counters were taken from.
 NCU_TRAFFIC = {
     "bwd": {"file": "fm_bwd.cu", "workload": "share_question32k",
-            "sha256": "bef3044d8040e2f71604208f4bbfa352970828ea6170fd9aaa905d8d5601351d", "bytes": 1264013824},
+            "sha256": "891d619cb78bf460fb78043bd7a42efb687a2f8421f29c4cb1f1aa78a08ccb3b", "bytes": 1265336320},
     "fwd": {"file": "fm_fwd.cu", "workload": "share_question32k",
-            "sha256": "201fd3db195131393464a502f1d6d380c3c740f0f38beff588077c7fb5d38a76", "bytes": 482497280},
+            "sha256": "e1668175cf543a774277f8ffa9b72224b54507a28d62508f2475fb480560d131", "bytes": 481902336},
 }
 
 
