@@ -16,8 +16,14 @@
 // dV [256, 384), dK [384, 512).
 // Shared memory: K and V of the block (64 KB each, for the full-width S^T and
 // dP^T), one stage of Q and dO (32 KB each: 64 query rows), one dS^T buffer
-// (16 KB), the dQ drain's transpose slots (16 KB): the stages cannot be
-// doubled here, so the pipeline runs one unit at a time.
+// (16 KB), the dQ drain's transpose slots (16 KB). The stages cannot be
+// doubled, so each Q / dO tile is handled as two head-dim halves with their
+// own barriers: the other CTA's half (columns this CTA does not output) feeds
+// only S^T and dP^T, and is released as soon as those k-steps are done; this
+// CTA's own half also feeds dK and dV and is released after dK. The MMA lane
+// issues the next unit's other-half k-steps of S^T and dP^T at the end of the
+// current unit, so both halves of the next unit load under the current
+// unit's MMAs.
 //
 // Roles (448 threads):
 //   warps 0-7  compute: thread j of warp w owns KV row j = 32*(w%4) + lane and
@@ -26,9 +32,11 @@
 //   warps 8-11 dQ drain: TMEM lane c = head-dim index 128*dh + c of dQ^T, to
 //              the fp32 accumulator by TMA reduce-adds of 32 x 32 boxes; at
 //              the end the dK half;
-//   warp 12    TMA producer (K, V once; per unit Q, dO and the row terms);
-//   warp 13    MMA issuer and TMEM owner: per unit S^T, dP^T, then dV after
-//              P^T, then dK and dQ^T after dS^T.
+//   warp 12    TMA producer (K, V once; per unit the other halves of Q and
+//              dO with the row terms (two slots), then the own halves);
+//   warp 13    MMA issuer and TMEM owner: per unit u the own-half k-steps of
+//              S^T(u) and dP^T(u), dV(u) after P^T(u), dK(u) and dQ^T(u) after
+//              dS^T(u), then the other-half k-steps of S^T(u+1) and dP^T(u+1).
 #include <climits>
 #include <cmath>
 #include <cuda.h>
@@ -52,23 +60,25 @@ struct B256 {
   static constexpr int DO_OFF = Q_OFF + Q_TILE;
   static constexpr int DS_OFF = DO_OFF + Q_TILE;  // 128 KV rows x 64 query columns bf16
   static constexpr int XPOSE_OFF = DS_OFF + 16384;  // 4 drain warps x 32 x 32 fp32
-  static constexpr int ROW_OFF = XPOSE_OFF + 4 * 4096;  // nl[64], D[64] fp32
+  static constexpr int ROW_OFF = XPOSE_OFF + 4 * 4096;  // two slots of {nl[64], D[64]} fp32
   static constexpr int QUEUE_CAP = 128;
-  static constexpr int QUEUE_OFF = ROW_OFF + 512;
+  static constexpr int QUEUE_OFF = ROW_OFF + 2 * 512;
   static constexpr int BAR_OFF = QUEUE_OFF + QUEUE_CAP * 4;
   static constexpr int B_KV = 0;
-  static constexpr int B_QFULL = 1;
-  static constexpr int B_QEMPTY = 2;
-  static constexpr int B_SFULL = 3;
-  static constexpr int B_PREADY = 4;
-  static constexpr int B_DPFULL = 5;
-  static constexpr int B_READY = 6;
-  static constexpr int B_DQFULL = 7;
-  static constexpr int B_DQEMPTY = 8;
-  static constexpr int B_FINAL = 9;
-  static constexpr int B_VSTAGED = 10;
-  static constexpr int B_KSTAGED = 11;
-  static constexpr int NBAR = 12;
+  static constexpr int B_OFULL = 1;   // [2] other halves of Q, dO + row terms of unit u, by u & 1
+  static constexpr int B_OEMPTY = 3;  // other halves free (S^T(u), dP^T(u) done)
+  static constexpr int B_MFULL = 4;   // own halves of Q, dO
+  static constexpr int B_MEMPTY = 5;  // own halves free (dV(u), dK(u) done)
+  static constexpr int B_SFULL = 6;
+  static constexpr int B_PREADY = 7;
+  static constexpr int B_DPFULL = 8;
+  static constexpr int B_READY = 9;
+  static constexpr int B_DQFULL = 10;
+  static constexpr int B_DQEMPTY = 11;
+  static constexpr int B_FINAL = 12;
+  static constexpr int B_VSTAGED = 13;
+  static constexpr int B_KSTAGED = 14;
+  static constexpr int NBAR = 15;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = BYTES + 1024;
@@ -158,8 +168,11 @@ __global__ void __launch_bounds__(448, 1)
   if (threadIdx.x == 0) {
     *abort_flag = timeout_pending(p.err) ? 1 : 0;
     mbar_init(&bars[C::B_KV], 1);
-    mbar_init(&bars[C::B_QFULL], 1);
-    mbar_init(&bars[C::B_QEMPTY], 1);
+    mbar_init(&bars[C::B_OFULL], 1);
+    mbar_init(&bars[C::B_OFULL + 1], 1);
+    mbar_init(&bars[C::B_OEMPTY], 1);
+    mbar_init(&bars[C::B_MFULL], 1);
+    mbar_init(&bars[C::B_MEMPTY], 1);
     mbar_init(&bars[C::B_SFULL], 1);
     mbar_init(&bars[C::B_PREADY], 256);
     mbar_init(&bars[C::B_DPFULL], 1);
@@ -199,20 +212,32 @@ __global__ void __launch_bounds__(448, 1)
         tma_load_3d(smem + C::K_OFF + x * 16384, &tk, &bars[C::B_KV], x * 64, k0, b * p.H_kv + g);
         tma_load_3d(smem + C::V_OFF + x * 16384, &tv, &bars[C::B_KV], x * 64, k0, b * p.H_kv + g);
       }
+      // Q / dO boxes (64 columns each) of the other CTA's half, then of this one's
+      const int xo = 2 * (1 - dh), xm = 2 * dh;
       for (int u = 0; u < U && ok; ++u) {
         const Unit256 un = decode256(p, u, L, kbeg, g, force_part, s_queue);
-        ok = mbar_wait(&bars[C::B_QEMPTY], ((uint32_t)u & 1u) ^ 1u, abort_flag, p.err);
-        if (!ok) break;
+        const uint32_t pe = ((uint32_t)u & 1u) ^ 1u;
         const int r0 = un.qb * 128 + un.half * 64;
         const int bh = b * p.H_q + un.h;
-        uint64_t* fb = &bars[C::B_QFULL];
-        mbar_arrive_expect_tx(fb, 2 * C::Q_TILE + 512);
-        for (int x = 0; x < 4; ++x) {
-          tma_load_3d(smem + C::Q_OFF + x * 8192, &tq, fb, x * 64, r0, bh);
-          tma_load_3d(smem + C::DO_OFF + x * 8192, &tdo, fb, x * 64, r0, bh);
+        ok = mbar_wait(&bars[C::B_OEMPTY], pe, abort_flag, p.err);
+        if (!ok) break;
+        uint64_t* fo = &bars[C::B_OFULL + (u & 1)];
+        uint8_t* rows = smem + C::ROW_OFF + (u & 1) * 512;
+        mbar_arrive_expect_tx(fo, C::Q_TILE + 512);
+        for (int x = xo; x < xo + 2; ++x) {
+          tma_load_3d(smem + C::Q_OFF + x * 8192, &tq, fo, x * 64, r0, bh);
+          tma_load_3d(smem + C::DO_OFF + x * 8192, &tdo, fo, x * 64, r0, bh);
         }
-        bulk_load(smem + C::ROW_OFF, p.nl + (size_t)bh * p.Npad + r0, 256, fb);
-        bulk_load(smem + C::ROW_OFF + 256, p.dsum + (size_t)bh * p.Npad + r0, 256, fb);
+        bulk_load(rows, p.nl + (size_t)bh * p.Npad + r0, 256, fo);
+        bulk_load(rows + 256, p.dsum + (size_t)bh * p.Npad + r0, 256, fo);
+        ok = mbar_wait(&bars[C::B_MEMPTY], pe, abort_flag, p.err);
+        if (!ok) break;
+        uint64_t* fm_ = &bars[C::B_MFULL];
+        mbar_arrive_expect_tx(fm_, C::Q_TILE);
+        for (int x = xm; x < xm + 2; ++x) {
+          tma_load_3d(smem + C::Q_OFF + x * 8192, &tq, fm_, x * 64, r0, bh);
+          tma_load_3d(smem + C::DO_OFF + x * 8192, &tdo, fm_, x * 64, r0, bh);
+        }
       }
     }
   } else if (warp == 13) {
@@ -230,22 +255,35 @@ __global__ void __launch_bounds__(448, 1)
       const uint64_t dOm = sdesc_sw128(smem_u32(smem + C::DO_OFF + 2 * dh * 8192), 8192, 1024);
       const uint64_t dSk = sdesc_sw128(smem_u32(smem + C::DS_OFF), 16, 1024);
       const uint64_t dSm = sdesc_sw128(smem_u32(smem + C::DS_OFF), 8192, 1024);
-      // S^T = K Q^T or dP^T = V dO^T over the whole head dimension (16 k-steps)
-      auto issue_sk = [&](uint64_t ad0, uint64_t bd0, uint32_t dst) {
+      // S^T = K Q^T or dP^T = V dO^T over one head-dim half (8 of the 16
+      // k-steps): half hs of the columns; fresh: the first k-step overwrites
+      auto issue_sk = [&](uint64_t ad0, uint64_t bd0, uint32_t dst, int hs, bool fresh) {
 #pragma unroll
-        for (int k = 0; k < C::D / 16; ++k)
+        for (int kk = 0; kk < 8; ++kk) {
+          const int k = 8 * hs + kk;
           mma_ss(tbase + dst, ad0 + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
-                 bd0 + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), id_s, k > 0 ? 1u : 0u);
+                 bd0 + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), id_s, (fresh && kk == 0) ? 0u : 1u);
+        }
+      };
+      // the other half's k-steps of S^T(v) and dP^T(v), once its tiles landed
+      auto issue_other = [&](int v) -> bool {
+        if (!mbar_wait(&bars[C::B_OFULL + (v & 1)], ((uint32_t)v >> 1) & 1u, abort_flag, p.err)) return false;
+        tc_fence_after();
+        issue_sk(dKk, dQk, T_S, 1 - dh, true);
+        issue_sk(dVk, dOk, T_DP, 1 - dh, true);
+        mma_commit(&bars[C::B_OEMPTY]);  // the other halves of Q(v), dO(v)
+        return true;
       };
       bool ok = mbar_wait(&bars[C::B_KV], 0, abort_flag, p.err);
+      if (ok) ok = issue_other(0);
       for (int u = 0; u < U && ok; ++u) {
         const uint32_t ph = (uint32_t)u & 1u;
-        ok = mbar_wait(&bars[C::B_QFULL], ph, abort_flag, p.err);
+        ok = mbar_wait(&bars[C::B_MFULL], ph, abort_flag, p.err);
         if (!ok) break;
         tc_fence_after();
-        issue_sk(dKk, dQk, T_S);  // S^T(u) over P^T(u-1), read by dV(u-1) issued earlier
+        issue_sk(dKk, dQk, T_S, dh, false);  // S^T(u) over P^T(u-1), read by dV(u-1) issued earlier
         mma_commit(&bars[C::B_SFULL]);
-        issue_sk(dVk, dOk, T_DP);  // dP^T(u-1) was read before READY(u-1)
+        issue_sk(dVk, dOk, T_DP, dh, false);  // dP^T(u-1) was read before READY(u-1)
         mma_commit(&bars[C::B_DPFULL]);
         // dV += P^T dO (A = P^T from TMEM: two 16-column blocks per compute half)
         ok = mbar_wait(&bars[C::B_PREADY], ph, abort_flag, p.err);
@@ -263,6 +301,7 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_ss(tbase + T_DK, dSk + (uint64_t)(k * 2), dQm + (uint64_t)(k * 128), id_g, (u > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&bars[C::B_MEMPTY]);  // the own halves of Q(u), dO(u)
         if (u >= 1) {
           ok = mbar_wait(&bars[C::B_DQEMPTY], ph ^ 1u, abort_flag, p.err);
           if (!ok) break;
@@ -272,7 +311,10 @@ __global__ void __launch_bounds__(448, 1)
         for (int k = 0; k < 8; ++k)  // 128 KV rows
           mma_ss(tbase + T_DQ, dKt + (uint64_t)(k * 128), dSm + (uint64_t)(k * 128), id_q, k > 0 ? 1u : 0u);
         mma_commit(&bars[C::B_DQFULL]);
-        mma_commit(&bars[C::B_QEMPTY]);  // every reader of Q(u), dO(u), the row terms and dS^T(u)
+        // S^T(u+1) overwrites P^T(u) after dV(u) (issued above: the MMAs of
+        // this lane run in order); dP^T(u+1) after the compute warps read
+        // dP^T(u) (READY(u))
+        if (u + 1 < U) ok = issue_other(u + 1);
       }
       if (ok) mma_commit(&bars[C::B_FINAL]);
     }
@@ -297,7 +339,7 @@ __global__ void __launch_bounds__(448, 1)
     }
     const float sl2 = p.scale_log2;
     const bool causal = p.causal != 0;
-    const uint32_t rows_a = smem_u32(smem + C::ROW_OFF) + 128 * half;  // nl[32*half ..]; D at +256
+    const uint32_t rows_b = smem_u32(smem + C::ROW_OFF) + 128 * half;  // nl[32*half ..]; D at +256
     const uint32_t ds_row = smem_u32(smem + C::DS_OFF) + (uint32_t)((j >> 3) * 1024 + (j & 7) * 128);
     const uint32_t tS = tbase + lane_off + T_S + 32u * half;
     const uint32_t tDP = tbase + lane_off + T_DP + 32u * half;
@@ -306,7 +348,10 @@ __global__ void __launch_bounds__(448, 1)
       const Unit256 un = decode256(p, u, L, kbeg, g, force_part, s_queue);
       const uint32_t ph = (uint32_t)u & 1u;
       const int r0 = un.qb * 128 + un.half * 64;
-      ok = __all_sync(kFullB, mbar_wait(&bars[C::B_QFULL], ph, abort_flag, p.err));
+      // the row terms of unit u (slot u & 1; the slot is reloaded for u + 2 only
+      // after this unit's READY)
+      const uint32_t rows_a = rows_b + 512u * (uint32_t)(u & 1);
+      ok = __all_sync(kFullB, mbar_wait(&bars[C::B_OFULL + (u & 1)], ((uint32_t)u >> 1) & 1u, abort_flag, p.err));
       if (ok) ok = __all_sync(kFullB, mbar_wait(&bars[C::B_SFULL], ph, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
