@@ -139,3 +139,31 @@ def test_per_head_refuses_unsupported_shapes():
         fm.fm_attn_fwd_heads(q, k, k, *vec, qs, scale=0.0625, causal=True)
     st, bits = fm.fm_device_status()
     assert st == fm.FM_OK, bits
+
+
+@pytest.mark.parametrize("n,nk,d,hq,hkv,causal", [(600, 900, 128, 4, 2, False), (900, 384, 64, 2, 1, True)])
+def test_per_head_rectangular(n, nk, d, hq, hkv, causal):
+    # N query rows against N_kv keys (the shape of one context-parallel rank),
+    # with per-head vectors of N_kv entries and values in [0, N]
+    rng = np.random.default_rng(n + nk)
+    B = 2
+    a = rng.integers(0, n + 1, size=(2, B, hq, nk))
+    c = rng.integers(0, n + 1, size=(2, B, hq, nk))
+    heads = tuple(x.astype(np.int32) for x in (a.min(0), a.max(0), c.min(0), c.max(0)))
+    q = tensors.randn_bf16((B, hq, n, d), 41)
+    k = tensors.randn_bf16((B, hkv, nk, d), 42)
+    v = tensors.randn_bf16((B, hkv, nk, d), 43)
+    do = tensors.randn_bf16((B, hq, n, d), 44)
+    vec = [torch.from_numpy(x).cuda() for x in heads]
+    scale = d ** -0.5
+    o, lse, dq, dk, dv = fm.fm_attn_per_head(q.cuda(), k.cuda(), v.cuda(), *vec, causal=causal, scale=scale,
+                                             do=do.cuda())
+    st, bits = fm.fm_device_status()
+    assert st == fm.FM_OK, bits
+    spec = {"heads": heads}
+    O_ref, L_ref = oracle.forward(f64(q), f64(k), f64(v), spec, causal, scale)
+    assert_out(f64(o), O_ref)
+    assert_lse(f64(lse), L_ref)
+    ref = oracle.backward(f64(q), f64(k), f64(v), f64(do), spec, causal, scale)
+    for name, x, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert_grad(f64(x), r, name)
