@@ -1,7 +1,7 @@
 """Pins of the oracle's FMS / FME conversion (FlashMask Guide, "The Solution:
 FlashMask Sparse Mask Representation" and "Real-World Attention Mask
 Topologies"): the Guide's own closed forms for causal, document and DPO masks
-give its printed matrices and the masks of this build's encoders, and the
+give its printed matrices and the masks of the workload encoders, and the
 converted vectors mask exactly the rows outside [FMS_j, FME_j]."""
 import os
 
