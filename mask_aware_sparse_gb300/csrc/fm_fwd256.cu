@@ -31,6 +31,12 @@
 //   warp 7     V producer: V of each queued block.
 // Two producers and two issuers let K(j+1) load and S(j+1) run while V(j)
 // waits for PV(j-1): one thread blocked on one chain would stall the other.
+// With one K and one V slot, a tile could only load once the MMA reading the
+// previous one had finished, and a 64 KB load takes longer than that MMA. So
+// the slots are refilled in quarters with their own barriers: K by its four
+// 64-column boxes (S(j)'s k-steps over box x free it), V by 32-key quarters
+// (PV(j)'s two k-steps over those keys free it); the next block's quarter
+// loads while the rest of the current MMA runs.
 #include <algorithm>
 #include <climits>
 #include <cmath>
@@ -59,16 +65,16 @@ struct F256 {
   static constexpr int O_SLOT = 32 * 32 * 2;
   static constexpr int BAR_OFF = O_OFF + 4 * O_SLOT;
   static constexpr int B_QFULL = 0;
-  static constexpr int B_KFULL = 1;
-  static constexpr int B_KEMPTY = 2;
-  static constexpr int B_VFULL = 3;
-  static constexpr int B_VEMPTY = 4;
-  static constexpr int B_MFULL = 5;   // [2]
-  static constexpr int B_MEMPTY = 7;  // [2]
-  static constexpr int B_SFULL = 9;   // [2]
-  static constexpr int B_PREADY = 11; // [2]
-  static constexpr int B_ODONE = 13;  // [2]
-  static constexpr int NBAR = 15;
+  static constexpr int B_KFULL = 1;    // [4] per 64-column box of K
+  static constexpr int B_KEMPTY = 5;   // [4]
+  static constexpr int B_VFULL = 9;    // [4] per 32-key quarter of V
+  static constexpr int B_VEMPTY = 13;  // [4]
+  static constexpr int B_MFULL = 17;   // [2]
+  static constexpr int B_MEMPTY = 19;  // [2]
+  static constexpr int B_SFULL = 21;   // [2]
+  static constexpr int B_PREADY = 23;  // [2]
+  static constexpr int B_ODONE = 25;   // [2]
+  static constexpr int NBAR = 27;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
@@ -121,10 +127,12 @@ __global__ void __launch_bounds__(256, 1)
   if (threadIdx.x == 0) {
     *abort_flag = timeout_pending(p.err) ? 1 : 0;
     mbar_init(&bars[C::B_QFULL], 1);
-    mbar_init(&bars[C::B_KFULL], 1);
-    mbar_init(&bars[C::B_KEMPTY], 1);
-    mbar_init(&bars[C::B_VFULL], 1);
-    mbar_init(&bars[C::B_VEMPTY], 1);
+    for (int x = 0; x < 4; ++x) {
+      mbar_init(&bars[C::B_KFULL + x], 1);
+      mbar_init(&bars[C::B_KEMPTY + x], 1);
+      mbar_init(&bars[C::B_VFULL + x], 1);
+      mbar_init(&bars[C::B_VEMPTY + x], 1);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[C::B_MFULL + s], 1);
       mbar_init(&bars[C::B_MEMPTY + s], 4);
@@ -166,11 +174,13 @@ __global__ void __launch_bounds__(256, 1)
         break;
       }
       if (lane == 0) {
-        ok = mbar_wait(&bars[C::B_KEMPTY], ((uint32_t)j & 1u) ^ 1u, abort_flag, p.err);
-        if (ok) {
-          mbar_arrive_expect_tx(&bars[C::B_KFULL], C::TILE);
-          for (int x = 0; x < C::BOXES; ++x)
-            tma_load_3d(smem + C::K_OFF + x * 16384, &tk, &bars[C::B_KFULL], x * 64, kb * 128, b * p.H_kv + g);
+        // box by box, each as soon as S(j-1) has read that box
+        for (int x = 0; x < C::BOXES && ok; ++x) {
+          ok = mbar_wait(&bars[C::B_KEMPTY + x], ((uint32_t)j & 1u) ^ 1u, abort_flag, p.err);
+          if (ok) {
+            mbar_arrive_expect_tx(&bars[C::B_KFULL + x], 16384);
+            tma_load_3d(smem + C::K_OFF + x * 16384, &tk, &bars[C::B_KFULL + x], x * 64, kb * 128, b * p.H_kv + g);
+          }
         }
       }
       ok = __shfl_sync(kFull256, ok, 0);
@@ -217,11 +227,16 @@ __global__ void __launch_bounds__(256, 1)
       for (int j = 0; j < n && ok; ++j) {
         const int kb = p.q_queue[qbeg + j] >> 1;
         if (kb < 0 || kb >= p.nK) break;  // flagged by the K producer
-        ok = mbar_wait(&bars[C::B_VEMPTY], ((uint32_t)j & 1u) ^ 1u, abort_flag, p.err);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bars[C::B_VFULL], C::TILE);
-        for (int x = 0; x < C::BOXES; ++x)
-          tma_load_3d(smem + C::V_OFF + x * 16384, &tv, &bars[C::B_VFULL], x * 64, kb * 128, b * p.H_kv + g);
+        // 32 keys at a time (all four 64-column boxes), each quarter as soon
+        // as PV(j-1) has read it
+        for (int qq = 0; qq < 4 && ok; ++qq) {
+          ok = mbar_wait(&bars[C::B_VEMPTY + qq], ((uint32_t)j & 1u) ^ 1u, abort_flag, p.err);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars[C::B_VFULL + qq], 4 * 4096);
+          for (int x = 0; x < C::BOXES; ++x)
+            tma_load_3d(smem + C::V_OFF + x * 16384 + qq * 4096, &tv, &bars[C::B_VFULL + qq], x * 64,
+                        kb * 128 + 32 * qq, b * p.H_kv + g);
+        }
       }
     }
   } else if (warp == 5) {
@@ -232,19 +247,23 @@ __global__ void __launch_bounds__(256, 1)
       const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::K_OFF), 16, 1024);
       bool ok = mbar_wait(&bars[C::B_QFULL], 0, abort_flag, p.err);
       for (int j = 0; j < n && ok; ++j) {
-        ok = mbar_wait(&bars[C::B_KFULL], (uint32_t)j & 1u, abort_flag, p.err);
         // S_(j&1) last held P(j-2): PV(j-2) must have read it
-        if (ok && j >= 2) ok = mbar_wait(&bars[C::B_ODONE + (j & 1)], ((uint32_t)(j - 2) >> 1) & 1u, abort_flag, p.err);
-        if (!ok) break;
-        tc_fence_after();
+        if (j >= 2) ok = mbar_wait(&bars[C::B_ODONE + (j & 1)], ((uint32_t)(j - 2) >> 1) & 1u, abort_flag, p.err);
         const uint32_t tS = tbase + 128u * (uint32_t)(j & 1);
+        // four k-steps per 64-column box of K, each box released once read
+        for (int x = 0; x < C::BOXES && ok; ++x) {
+          ok = mbar_wait(&bars[C::B_KFULL + x], (uint32_t)j & 1u, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t off = (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);
-          mma_ss(tS, dQ0 + off, dK0 + off, id_s, kk > 0 ? 1u : 0u);
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = 4 * x + k4;
+            const uint64_t off = (uint64_t)(x * 1024 + k4 * 2);
+            mma_ss(tS, dQ0 + off, dK0 + off, id_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars[C::B_KEMPTY + x]);
         }
-        mma_commit(&bars[C::B_SFULL + (j & 1)]);
-        mma_commit(&bars[C::B_KEMPTY]);
+        if (ok) mma_commit(&bars[C::B_SFULL + (j & 1)]);
       }
     }
   } else if (warp == 6) {
@@ -255,15 +274,22 @@ __global__ void __launch_bounds__(256, 1)
       bool ok = true;
       for (int j = 0; j < n && ok; ++j) {
         ok = mbar_wait(&bars[C::B_PREADY + (j & 1)], ((uint32_t)j >> 1) & 1u, abort_flag, p.err);
-        if (ok) ok = mbar_wait(&bars[C::B_VFULL], (uint32_t)j & 1u, abort_flag, p.err);
-        if (!ok) break;
-        tc_fence_after();
         const uint32_t tS = tbase + 128u * (uint32_t)(j & 1);
+        // two k-steps (16 keys each) per 32-key quarter of V, each quarter
+        // released once read
+        for (int qq = 0; qq < 4 && ok; ++qq) {
+          ok = mbar_wait(&bars[C::B_VFULL + qq], (uint32_t)j & 1u, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tbase + 256u, tS + (uint32_t)(kk * 8), dV0 + (uint64_t)(kk * 128), id_o, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars[C::B_ODONE + (j & 1)]);
-        mma_commit(&bars[C::B_VEMPTY]);
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int kk = 2 * qq + k2;
+            mma_ts(tbase + 256u, tS + (uint32_t)(kk * 8), dV0 + (uint64_t)(kk * 128), id_o,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars[C::B_VEMPTY + qq]);
+        }
+        if (ok) mma_commit(&bars[C::B_ODONE + (j & 1)]);
       }
     }
   } else if (warp < 4) {
@@ -461,7 +487,7 @@ cudaError_t launch_fwd256(const fm_problem& P, const void* q, const void* k, con
   if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, P.B * nQ, order);
   CUtensorMap tq, tk, tv, to;
   if (!make_tmap_bhnd(&tq, q, (int64_t)P.B * P.H_q, P.N, P.d) || !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, Nk, P.d) ||
-      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, Nk, P.d) ||
+      !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, Nk, P.d, 32) ||
       !make_tmap_bhnd_w32(&to, o, (int64_t)P.B * P.H_q, P.N, P.d))
     return cudaErrorInvalidValue;
   Fwd256Params prm;
