@@ -15,7 +15,8 @@
  *   - Layouts: Q, O, dO, dQ are contiguous (B, H_q, N, d) bf16; K, V, dK, dV are
  *     contiguous (B, H_kv, N_kv, d) bf16 (N_kv = N unless fm_problem says
  *     otherwise); LSE is (B, H_q, N) fp32; the four mask vectors are (B, N_kv)
- *     int32, one entry per key column, shared by every head, holding query-row
+ *     int32, one entry per key column, shared by every head (the *_heads entry
+ *     points take one set per query head, (B, H_q, N_kv)), holding query-row
  *     boundaries in [0, N]. Tensor base addresses must be 16-byte aligned.
  *   - GQA: query head h reads kv head h / (H_q / H_kv) (contiguous groups).
  *   - Errors: arguments are validated on the host and a bad call returns an
