@@ -119,3 +119,28 @@ def test_cp_split_on_one_gpu(name):
     assert_grad(f64(dk_sum), dK_ref, "dK")
     assert_grad(f64(dv_sum), dV_ref, "dV")
     assert same == P
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("n,nk", [(1, 1), (1, 300), (300, 1), (129, 1), (1, 129), (2, 257)])
+def test_extreme_rectangular_shapes(n, nk, d):
+    # one query row or one key, and blocks of a single row or key on either axis
+    rng = np.random.default_rng(7 * n + nk + d)
+    B, hq, hkv = 2, 2, 1
+    for causal in (False, True):
+        vec = rect_vectors(rng, B, n, nk)
+        q, k, v, do = inputs(B, hq, hkv, n, nk, d, seed=30)
+        dv_ = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in vec]
+        qs = fm.fm_classify_tiles(*dv_, causal=causal, n_rows=n)
+        scale = d ** -0.5
+        qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+        o, lse = fm.fm_attn_fwd(qd, kd, vd, *dv_, qs, scale=scale, causal=causal)
+        dq, dk, dv = fm.fm_attn_bwd(qd, kd, vd, o, lse, dod, *dv_, qs, scale=scale, causal=causal)
+        st, bits = fm.fm_device_status()
+        assert st == fm.FM_OK, bits
+        O_ref, L_ref = oracle.forward(f64(q), f64(k), f64(v), vec, causal, scale)
+        assert_out(f64(o), O_ref)
+        assert_lse(f64(lse), L_ref)
+        ref = oracle.backward(f64(q), f64(k), f64(v), f64(do), vec, causal, scale)
+        for name, x, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+            assert_grad(f64(x), r, name)
