@@ -506,6 +506,10 @@ def run_ours(args, cfg):
         "kernel_frac_of_measured_peak": {"fwd_main": work["fwd"] / (fwd_ms / 1e3) / 1e12 / peak,
                                          "bwd_main": work["bwd"] / (bwd_ms / 1e3) / 1e12 / peak},
         "per_clock_peak": per_clock,
+        # tensor pipe active, % of elapsed cycles, from the ncu capture of the
+        # same kernel source on this workload (None once the source changed)
+        "ncu_tensor_pipe_pct": {"fwd_main": ncu_traffic("fwd", args.workload, cfg["d"], "tensor_pipe_pct"),
+                                "bwd_main": ncu_traffic("bwd", args.workload, cfg["d"], "tensor_pipe_pct")},
         "roofline": {"kernel": "fm_attn_bwd main" if dom == "bwd" else "fm_attn_fwd main", "bound": "tensor",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "traffic": traffic,
@@ -528,13 +532,18 @@ def run_ours(args, cfg):
 # the counters were taken from.
 NCU_TRAFFIC = {
     "bwd": {"file": "fm_bwd.cu", "workload": "share_question32k",
-            "sha256": "891d619cb78bf460fb78043bd7a42efb687a2f8421f29c4cb1f1aa78a08ccb3b", "bytes": 1265336320},
+            "sha256": "891d619cb78bf460fb78043bd7a42efb687a2f8421f29c4cb1f1aa78a08ccb3b", "bytes": 1265336320,
+            "tensor_pipe_pct": 58.7},
     "fwd": {"file": "fm_fwd.cu", "workload": "share_question32k",
-            "sha256": "e1668175cf543a774277f8ffa9b72224b54507a28d62508f2475fb480560d131", "bytes": 481902336},
+            "sha256": "e1668175cf543a774277f8ffa9b72224b54507a28d62508f2475fb480560d131", "bytes": 481902336,
+            "tensor_pipe_pct": 48.4},
 }
 
 
-def ncu_traffic(kind: str, workload: str, d: int):
+def ncu_traffic(kind: str, workload: str, d: int, key: str = "bytes"):
+    """A counter of the ncu capture of main kernel `kind` on this workload
+    (DRAM bytes per launch, or the tensor pipe's active % of elapsed cycles),
+    or None when the kernel source has changed since the capture."""
     import hashlib
 
     ent = NCU_TRAFFIC.get(kind)
@@ -545,7 +554,7 @@ def ncu_traffic(kind: str, workload: str, d: int):
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()
     except OSError:
         return None
-    return ent["bytes"] if h == ent["sha256"] else None
+    return ent.get(key) if h == ent["sha256"] else None
 
 
 # ------------------------------------------------------ FP8 forward
