@@ -194,7 +194,8 @@ fm_status fm_attn_bwd(const fm_problem* p, const void* q, const void* k, const v
  *     rows (an fm_problem with B' = B * H_q), so row (b * H_q + h) holds
  *     query head h's tiles;
  *   - every work unit is one head (two heads of a unit would need one queue);
- *   - d must be 64 or 128 and H_q / H_kv at most 64.
+ *   - d is 64, 128 or 256 like fm_attn_fwd, and H_q / H_kv is at most 64
+ *     (FM_ERR_UNSUPPORTED otherwise).
  * Workspaces: fm_attn_fwd_heads_workspace_bytes (one order entry per queue
  * row) and fm_attn_bwd_workspace_bytes.
  * ------------------------------------------------------------------------- */

@@ -273,10 +273,10 @@ size_t fm_attn_fwd_heads_workspace_bytes(const fm_problem* p) {
   return fwd_heads_ws_bytes(*p);
 }
 
-// Per-head masks: d = 64 or 128 and at most 64 query heads per kv head (the
-// backward stages one queue per head of a group).
+// Per-head masks: at most 64 query heads per kv head (the backward stages one
+// queue per head of a group).
 static fm_status check_heads_shape(const fm_problem* p) {
-  if (p->d != 64 && p->d != 128) return FM_ERR_UNSUPPORTED;
+  if (check_attn_shape(p, false) != FM_OK) return FM_ERR_UNSUPPORTED;
   if (p->H_q / p->H_kv > 64) return FM_ERR_UNSUPPORTED;
   return FM_OK;
 }

@@ -800,7 +800,7 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   // 3. main kernel
   if constexpr (D == 256) {
     e = launch_bwd256_main(P, q, k, v, dout, prm0.lts, prm0.lte, prm0.uts, prm0.ute, prm0.k_off, prm0.k_queue,
-                           natural ? nullptr : w.order, w.nl, w.dsum, w.dq_acc, prm0.dk, prm0.dv, s, prm0.err);
+                           natural ? nullptr : w.order, w.nl, w.dsum, w.dq_acc, prm0.dk, prm0.dv, s, prm0.err, PH);
     if (e != cudaSuccess) return e;
   } else {
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
@@ -885,6 +885,7 @@ cudaError_t launch_bwd(const fm_problem& P, const void* q, const void* k, const 
     if (P.H_q / P.H_kv > kMaxHeads) return cudaErrorInvalidValue;
     if (P.d == 128) return launch_bwd_d<128, true>(P, q, k, v, o, lse, dout, dq, prm, w, s);
     if (P.d == 64) return launch_bwd_d<64, true>(P, q, k, v, o, lse, dout, dq, prm, w, s);
+    if (P.d == 256) return launch_bwd_d<256, true>(P, q, k, v, o, lse, dout, dq, prm, w, s);
     return cudaErrorInvalidValue;
   }
   if (P.d == 256) return launch_bwd_d<256>(P, q, k, v, o, lse, dout, dq, prm, w, s);

@@ -63,7 +63,10 @@ struct B256 {
   static constexpr int ROW_OFF = XPOSE_OFF + 4 * 4096;  // two slots of {nl[64], D[64]} fp32
   static constexpr int QUEUE_CAP = 128;
   static constexpr int QUEUE_OFF = ROW_OFF + 2 * 512;
-  static constexpr int BAR_OFF = QUEUE_OFF + QUEUE_CAP * 4;
+  // per-head masks: each group head's first entry in the heads' queues back
+  // to back (a prefix, 65 entries)
+  static constexpr int HEADS_OFF = QUEUE_OFF + QUEUE_CAP * 4;
+  static constexpr int BAR_OFF = HEADS_OFF + 272;
   static constexpr int B_KV = 0;
   static constexpr int B_OFULL = 1;   // [2] other halves of Q, dO + row terms of unit u, by u & 1
   static constexpr int B_OEMPTY = 3;  // other halves free (S^T(u), dP^T(u) done)
@@ -92,7 +95,7 @@ struct Bwd256Params {
   const int32_t* ute;
   const int32_t* k_off;
   const int32_t* k_queue;
-  const int32_t* order;  // launch order of (b, kb), or null: natural order
+  const int32_t* order;  // launch order of (b, kb), or null: natural order (always with per-head masks)
   const float* nl;       // (B*H_q, Npad): -LSE*log2(e), -inf for empty / padded rows
   const float* dsum;     // (B*H_q, Npad): D = rowsum(dO * O)
   __nv_bfloat16* dk;
@@ -101,6 +104,9 @@ struct Bwd256Params {
   float scale, scale_log2;
   int* err;
 };
+
+// Query heads per GQA group with per-head mask vectors (the staged prefix).
+constexpr int kMaxHeads256 = 64;
 
 struct Unit256 {
   int h, qb, half, part;
@@ -118,7 +124,28 @@ __device__ __forceinline__ Unit256 decode256(const Bwd256Params& p, int u, int L
   r.part = (e & 1) | (force_part ? 1 : 0);
   return r;
 }
+// The same with per-head mask vectors: head hi of the group owns the units
+// [2 hoff[hi], 2 hoff[hi + 1]) (its own queue for this KV block); the staged
+// entries are the heads' queues back to back. hi is the caller's cursor (units
+// are visited in increasing order).
+__device__ __forceinline__ Unit256 decode256_ph(const Bwd256Params& p, int u, int b, int kb, int g,
+                                                bool force_part, uint32_t s_queue, const int* hoff, int& hi) {
+  while (u >= 2 * hoff[hi + 1]) ++hi;
+  const int rem = u - 2 * hoff[hi];
+  const int pos = hoff[hi] + (rem >> 1);
+  Unit256 r;
+  r.h = g * p.G + hi;
+  const int e = (pos < B256::QUEUE_CAP)
+                    ? lds_s32(s_queue + 4 * pos)
+                    : p.k_queue[p.k_off[((size_t)b * p.H_q + r.h) * p.nK + kb] + (rem >> 1)];
+  r.qb = e >> 1;
+  r.half = rem & 1;
+  r.part = (e & 1) | (force_part ? 1 : 0);
+  return r;
+}
 
+// PH: per-head mask vectors (B, H_q, N_kv) and queues over B * H_q rows.
+template <bool PH>
 __global__ void __launch_bounds__(448, 1)
     bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -142,9 +169,17 @@ __global__ void __launch_bounds__(448, 1)
   const int bk = p.order ? p.order[oi] : oi;
   const int nK = p.nK;
   const int b = bk / nK, kb = bk - b * nK;
-  const int kbeg = p.k_off[bk];
-  const int L = p.k_off[bk + 1] - kbeg;
-  const int U = 2 * L * p.G;
+  int kbeg = 0, L = 0;  // per-head masks: L sums the heads' queue lengths
+  if constexpr (PH) {
+    for (int hi = 0; hi < p.G; ++hi) {
+      const int r = (b * p.H_q + g * p.G + hi) * nK + kb;
+      L += p.k_off[r + 1] - p.k_off[r];
+    }
+  } else {
+    kbeg = p.k_off[bk];
+    L = p.k_off[bk + 1] - kbeg;
+  }
+  const int U = PH ? 2 * L : 2 * L * p.G;
   const int k0 = kb * 128;
   const int c0h = dh * DH;  // first head-dim column of this CTA's outputs
   const bool force_part = (kb == nK - 1) && (p.Nk & 127);
@@ -185,10 +220,34 @@ __global__ void __launch_bounds__(448, 1)
     fence_mbar_init();
   }
   const uint32_t s_queue = smem_u32(smem + C::QUEUE_OFF);
+  int* hoff = reinterpret_cast<int*>(smem + C::HEADS_OFF);
   {
     int* sq = reinterpret_cast<int*>(smem + C::QUEUE_OFF);
-    for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) sq[t] = p.k_queue[kbeg + t];
+    if constexpr (PH) {
+      if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int hi = 0; hi < p.G; ++hi) {
+          const int r = (b * p.H_q + g * p.G + hi) * nK + kb;
+          hoff[hi] = acc;
+          acc += p.k_off[r + 1] - p.k_off[r];
+        }
+        hoff[p.G] = acc;
+      }
+      __syncthreads();
+      for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) {
+        int hi = 0;
+        while (hi + 1 < p.G && hoff[hi + 1] <= t) ++hi;
+        sq[t] = p.k_queue[p.k_off[(b * p.H_q + g * p.G + hi) * nK + kb] + (t - hoff[hi])];
+      }
+    } else {
+      for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) sq[t] = p.k_queue[kbeg + t];
+    }
   }
+  // the unit decoder of every role (a cursor over the heads with per-head masks)
+  auto decode = [&](int u, int& hcur) -> Unit256 {
+    if constexpr (PH) return decode256_ph(p, u, b, kb, g, force_part, s_queue, hoff, hcur);
+    else return decode256(p, u, L, kbeg, g, force_part, s_queue);
+  };
   if (warp == 13) tmem_alloc<512>(tmem_slot);
   if (warp == 12 && lane == 0) {
     tma_prefetch_desc(&tq);
@@ -214,8 +273,9 @@ __global__ void __launch_bounds__(448, 1)
       }
       // Q / dO boxes (64 columns each) of the other CTA's half, then of this one's
       const int xo = 2 * (1 - dh), xm = 2 * dh;
+      int hcur = 0;  // head cursor (per-head masks)
       for (int u = 0; u < U && ok; ++u) {
-        const Unit256 un = decode256(p, u, L, kbeg, g, force_part, s_queue);
+        const Unit256 un = decode(u, hcur);
         const uint32_t pe = ((uint32_t)u & 1u) ^ 1u;
         const int r0 = un.qb * 128 + un.half * 64;
         const int bh = b * p.H_q + un.h;
@@ -326,8 +386,12 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     int lo0 = 0, lo1 = 0, up0 = 0, up1 = 0;
     const bool dead = kcol >= p.Nk;
-    if (!dead) {
-      const size_t vi = (size_t)b * p.Nk + kcol;
+    // this thread's key column's masked intervals, from vector row vrow (the
+    // batch entry, or with per-head masks the (batch entry, head))
+    auto load_mask = [&](int vrow) {
+      lo0 = lo1 = up0 = up1 = 0;
+      if (dead) return;
+      const size_t vi = (size_t)vrow * p.Nk + kcol;
       int a0 = p.lts[vi], a1 = p.lte[vi], u0 = p.uts[vi], u1 = p.ute[vi];
       if ((a0 | a1 | u0 | u1) < 0 || a0 > p.N || a1 > p.N || u0 > p.N || u1 > p.N) record_error(p.err, FM_DEV_ERR_RANGE);
       a0 = min(max(a0, 0), p.N);
@@ -336,7 +400,9 @@ __global__ void __launch_bounds__(448, 1)
       u1 = min(max(u1, 0), p.N);
       if (a0 < a1) { lo0 = a0; lo1 = a1; }
       if (u0 < u1) { up0 = u0; up1 = u1; }
-    }
+    };
+    int mhead = -1;  // the head whose vectors are loaded (per-head masks)
+    if constexpr (!PH) load_mask(b);
     const float sl2 = p.scale_log2;
     const bool causal = p.causal != 0;
     const uint32_t rows_b = smem_u32(smem + C::ROW_OFF) + 128 * half;  // nl[32*half ..]; D at +256
@@ -344,8 +410,15 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t tS = tbase + lane_off + T_S + 32u * half;
     const uint32_t tDP = tbase + lane_off + T_DP + 32u * half;
     bool ok = true;
+    int hcur = 0;  // head cursor (per-head masks)
     for (int u = 0; u < U && ok; ++u) {
-      const Unit256 un = decode256(p, u, L, kbeg, g, force_part, s_queue);
+      const Unit256 un = decode(u, hcur);
+      if constexpr (PH) {
+        if (un.h != mhead) {
+          load_mask(b * p.H_q + un.h);
+          mhead = un.h;
+        }
+      }
       const uint32_t ph = (uint32_t)u & 1u;
       const int r0 = un.qb * 128 + un.half * 64;
       // the row terms of unit u (slot u & 1; the slot is reloaded for u + 2 only
@@ -455,8 +528,9 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
     const uint32_t xp = smem_u32(smem + C::XPOSE_OFF) + w4 * 4096;
     bool ok = true;
+    int hcur = 0;  // head cursor (per-head masks)
     for (int u = 0; u < U && ok; ++u) {
-      const Unit256 un = decode256(p, u, L, kbeg, g, force_part, s_queue);
+      const Unit256 un = decode(u, hcur);
       ok = __all_sync(kFullB, mbar_wait(&bars[C::B_DQFULL], (uint32_t)u & 1u, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
@@ -537,7 +611,8 @@ __global__ void __launch_bounds__(448, 1)
 cudaError_t launch_bwd256_main(const fm_problem& P, const void* q, const void* k, const void* v, const void* dout,
                                const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
                                const int32_t* k_off, const int32_t* k_queue, const int32_t* order, const float* nl,
-                               const float* dsum, float* dq_acc, void* dk, void* dv, cudaStream_t s, int* err) {
+                               const float* dsum, float* dq_acc, void* dk, void* dv, cudaStream_t s, int* err,
+                               bool per_head) {
   using C = B256;
   const int Nk = kv_rows(P);
   const int nK = (Nk + kTile - 1) / kTile;
@@ -576,15 +651,22 @@ cudaError_t launch_bwd256_main(const fm_problem& P, const void* q, const void* k
   prm.scale = P.scale;
   prm.scale_log2 = P.scale * 1.4426950408889634f;
   prm.err = err;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(bwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  static bool attr_done[2] = {false, false};
+  if (!attr_done[per_head]) {
+    cudaError_t e = cudaFuncSetAttribute(per_head ? bwd256_kernel<true> : bwd256_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_done[per_head] = true;
   }
   {
     KernelTimer timer(s, kTimedBwd);
-    bwd256_kernel<<<(unsigned)grid, 448, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
+    if (per_head) {
+      if (P.H_q / P.H_kv > kMaxHeads256) return cudaErrorInvalidValue;
+      prm.order = nullptr;  // the order table reads one queue per (batch, KV block)
+      bwd256_kernel<true><<<(unsigned)grid, 448, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
+    } else {
+      bwd256_kernel<false><<<(unsigned)grid, 448, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
+    }
   }
   return cudaGetLastError();
 }

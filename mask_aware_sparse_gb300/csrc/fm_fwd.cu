@@ -900,6 +900,7 @@ cudaError_t launch_fwd(const fm_problem& P, const void* q, const void* k, const 
 cudaError_t launch_fwd_heads(const fm_problem& P, const void* q, const void* k, const void* v, const int32_t* lts,
                              const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
                              const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err) {
+  if (P.d == 256) return launch_fwd256(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err, true);
   return launch_fwd_persistent(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err, false, 1.f, 1.f,
                                1.f, true);
 }

@@ -88,9 +88,10 @@ struct Fwd256Params {
   const int32_t* ute;
   const int32_t* q_off;
   const int32_t* q_queue;
-  const int32_t* order;  // order of (b, qb), or null: natural order
+  const int32_t* order;  // order of (b, qb) (per-head masks: of queue rows), or null: natural order
   float* lse;
   int B, H_q, H_kv, N, Nk, nQ, nK, G, causal;
+  int per_head;  // vectors (B, H_q, N_kv), one queue per (b, h, qb) row
   float scale_log2;
   int* err;
 };
@@ -115,14 +116,33 @@ __global__ void __launch_bounds__(256, 1)
   FM_DEBUG_BEGIN();
   // unit: (b, qb) from the launch order, query head h (fastest: the heads of
   // one GQA group run side by side and share K / V tiles in L2)
-  const int oi = blockIdx.x / p.H_q, h = blockIdx.x - oi * p.H_q;
-  const int bq = p.order ? p.order[oi] : oi;
-  const int b = bq / p.nQ, qb = bq - b * p.nQ;
+  int b, qb, h, row;  // row: this unit's queue
+  if (!p.per_head) {
+    const int oi = blockIdx.x / p.H_q;
+    h = blockIdx.x - oi * p.H_q;
+    row = p.order ? p.order[oi] : oi;
+    b = row / p.nQ;
+    qb = row - b * p.nQ;
+  } else {
+    // queue rows (b * H_q + h) * nQ + qb, from the order table or with the
+    // heads of one (b, qb) side by side
+    if (p.order) {
+      row = p.order[blockIdx.x];
+    } else {
+      const int oi = blockIdx.x / p.H_q, hh = blockIdx.x - oi * p.H_q;
+      const int bb = oi / p.nQ;
+      row = (bb * p.H_q + hh) * p.nQ + (oi - bb * p.nQ);
+    }
+    const int bhr = row / p.nQ;
+    qb = row - bhr * p.nQ;
+    b = bhr / p.H_q;
+    h = bhr - b * p.H_q;
+  }
   const int g = h / p.G;
-  const int qbeg = p.q_off[bq];
-  const int n = p.q_off[bq + 1] - qbeg;
+  const int qbeg = p.q_off[row];
+  const int n = p.q_off[row + 1] - qbeg;
   const int bh = b * p.H_q + h;
-  const size_t vbase = (size_t)b * p.Nk;
+  const size_t vbase = (size_t)(p.per_head ? bh : b) * p.Nk;
 
   if (threadIdx.x == 0) {
     *abort_flag = timeout_pending(p.err) ? 1 : 0;
@@ -473,9 +493,11 @@ __global__ void __launch_bounds__(256, 1)
 
 // d = 256: one CTA per (batch, Q block, query head); the workspace is the
 // forward's (unit-order table, then a counter this kernel does not use).
+// per_head: vectors (B, H_q, N_kv) and queues over B * H_q * nQ rows.
 cudaError_t launch_fwd256(const fm_problem& P, const void* q, const void* k, const void* v, const int32_t* lts,
                           const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
-                          const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err) {
+                          const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err,
+                          bool per_head) {
   using C = F256;
   const int nQ = (P.N + kTile - 1) / kTile;
   const int Nk = kv_rows(P);
@@ -484,7 +506,7 @@ cudaError_t launch_fwd256(const fm_problem& P, const void* q, const void* k, con
   // longest queue first for passes of a few waves, natural order for long ones
   const bool natural = use_natural_order(grid);
   int32_t* order = natural ? nullptr : static_cast<int32_t*>(ws);
-  if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, P.B * nQ, order);
+  if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, per_head ? P.B * P.H_q * nQ : P.B * nQ, order);
   CUtensorMap tq, tk, tv, to;
   if (!make_tmap_bhnd(&tq, q, (int64_t)P.B * P.H_q, P.N, P.d) || !make_tmap_bhnd(&tk, k, (int64_t)P.B * P.H_kv, Nk, P.d) ||
       !make_tmap_bhnd(&tv, v, (int64_t)P.B * P.H_kv, Nk, P.d, 32) ||
@@ -508,6 +530,7 @@ cudaError_t launch_fwd256(const fm_problem& P, const void* q, const void* k, con
   prm.nK = (Nk + kTile - 1) / kTile;
   prm.G = P.H_q / P.H_kv;
   prm.causal = P.causal ? 1 : 0;
+  prm.per_head = per_head ? 1 : 0;
   prm.scale_log2 = P.scale * 1.4426950408889634f;
   prm.err = err;
   static bool attr_done = false;

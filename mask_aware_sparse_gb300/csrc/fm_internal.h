@@ -53,7 +53,8 @@ cudaError_t launch_fwd_fp8(const fm_problem& P, const void* q, const void* k, co
 // Forward for d = 256 (fm_fwd256.cu): same arguments and workspace as launch_fwd.
 cudaError_t launch_fwd256(const fm_problem& p, const void* q, const void* k, const void* v, const int32_t* lts,
                           const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
-                          const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err);
+                          const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err,
+                          bool per_head = false);
 
 // The forward's fixed scratch for fm_attn_fwd_noalloc (fm_fwd.cu): device
 // address of the library-owned launch-order array of the current device, or
@@ -72,7 +73,8 @@ cudaError_t launch_bwd(const fm_problem& p, const void* q, const void* k, const 
 cudaError_t launch_bwd256_main(const fm_problem& P, const void* q, const void* k, const void* v, const void* dout,
                                const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
                                const int32_t* k_off, const int32_t* k_queue, const int32_t* order, const float* nl,
-                               const float* dsum, float* dq_acc, void* dk, void* dv, cudaStream_t s, int* err);
+                               const float* dsum, float* dq_acc, void* dk, void* dv, cudaStream_t s, int* err,
+                               bool per_head = false);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

@@ -283,14 +283,15 @@ def test_binding_checks_per_head_shapes(lib):
 
 
 def test_per_head_entry_points_validate_before_any_launch(lib):
-    # the C side refuses head dims other than 64 / 128 and groups of more than
-    # 64 query heads per kv head before touching a pointer; its workspace
+    # the C side refuses groups of more than 64 query heads per kv head and
+    # null tensors before touching a pointer; its workspace
     # query counts one order entry per (batch, head, Q block)
     nul = ctypes.c_void_p(0)
     args = [nul] * 11 + [nul, ctypes.c_size_t(0), nul]
     bargs = [nul] * 15 + [nul, ctypes.c_size_t(0), nul]
     for shape, want in (((1, 130, 2, 256, 128), fm.FM_ERR_UNSUPPORTED),   # 65 heads per kv head
-                        ((1, 4, 2, 256, 256), fm.FM_ERR_UNSUPPORTED),     # d = 256
+                        ((1, 4, 2, 256, 96), fm.FM_ERR_UNSUPPORTED),      # d = 96
+                        ((1, 4, 2, 256, 256), fm.FM_ERR_INVALID_ARG),     # d = 256, null tensors
                         ((1, 4, 2, 256, 128), fm.FM_ERR_INVALID_ARG)):    # null tensors
         p = fm._problem(*shape, 0.1, 1)
         assert lib.fm_attn_fwd_heads(ctypes.byref(p), *args) == want

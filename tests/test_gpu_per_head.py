@@ -71,17 +71,17 @@ def _run(heads, B, hq, hkv, n, d, causal, backward=True):
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,hq,hkv,n,d", [(2, 4, 2, 700, 128), (1, 1, 1, 300, 64), (1, 6, 2, 389, 128),
-                                          (2, 8, 1, 1000, 64)])
+                                          (2, 8, 1, 1000, 64), (1, 4, 2, 389, 256), (2, 2, 1, 600, 256)])
 def test_per_head_random_masks(B, hq, hkv, n, d, causal):
     rng = np.random.default_rng(9 + hq + n)
     _run(_general_heads(rng, B, hq, n), B, hq, hkv, n, d, causal)
 
 
-@pytest.mark.parametrize("hq,hkv", [(6, 1), (6, 3)])
-def test_per_head_mask_families(hq, hkv):
+@pytest.mark.parametrize("hq,hkv,d", [(6, 1, 128), (6, 3, 128), (6, 2, 256)])
+def test_per_head_mask_families(hq, hkv, d):
     rng = np.random.default_rng(31)
     n = 1500
-    _run(_family_heads(rng, 2, hq, n), 2, hq, hkv, n, 128, True)
+    _run(_family_heads(rng, 2, hq, n), 2, hq, hkv, n, d, True)
 
 
 def test_per_head_group_of_64_overflows_the_staged_queue():
@@ -94,12 +94,23 @@ def test_per_head_group_of_64_overflows_the_staged_queue():
     _run(heads, 1, 64, 1, n, 64, True)
 
 
-def test_repeated_vectors_match_the_shared_path():
+def test_per_head_d256_overflows_the_staged_queue():
+    # d = 256 stages 128 queue entries per KV block: 8 query heads per kv head
+    # and 18 Q blocks give up to 8 x 18 = 144
+    rng = np.random.default_rng(256)
+    n = 2200
+    heads = _general_heads(rng, 1, 8, n)
+    heads = (heads[0] // 4, heads[1] // 4, heads[2], heads[2])
+    _run(heads, 1, 8, 1, n, 256, True)
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_repeated_vectors_match_the_shared_path(d):
     # per-head vectors that repeat one mask: each head's arithmetic is the
     # shared path's (same tiles, same order), so O, LSE, dK and dV agree bit for
     # bit; dQ is summed with fp32 reduce-adds whose order between CTAs is free
     rng = np.random.default_rng(77)
-    B, hq, hkv, n, d = 2, 4, 2, 1100, 128
+    B, hq, hkv, n = 2, 4, 2, 1100
     v1 = masks.causal_documents(masks.draw_fill(rng, n, 100, 500), n)
     shared = [torch.from_numpy(np.ascontiguousarray(np.broadcast_to(np.asarray(x, np.int32), (B, n)))).cuda()
               for x in v1]
@@ -130,18 +141,12 @@ def test_per_head_refuses_unsupported_shapes():
         fm.fm_attn_fwd_heads(q, k, k, *vec, qs, scale=0.125, causal=True)
     with pytest.raises(fm.FMError):
         fm.fm_attn_bwd_heads(q, k, k, o, lse, do, *vec, qs, scale=0.125, causal=True)
-    # d = 256 has no per-head kernels
-    vec = [torch.zeros(1, 2, n, dtype=torch.int32, device="cuda") for _ in range(4)]
-    q = torch.zeros(1, 2, n, 256, dtype=torch.bfloat16, device="cuda")
-    k = torch.zeros(1, 1, n, 256, dtype=torch.bfloat16, device="cuda")
-    qs = fm.fm_classify_tiles_heads(*vec, causal=True)
-    with pytest.raises(fm.FMError):
-        fm.fm_attn_fwd_heads(q, k, k, *vec, qs, scale=0.0625, causal=True)
     st, bits = fm.fm_device_status()
     assert st == fm.FM_OK, bits
 
 
-@pytest.mark.parametrize("n,nk,d,hq,hkv,causal", [(600, 900, 128, 4, 2, False), (900, 384, 64, 2, 1, True)])
+@pytest.mark.parametrize("n,nk,d,hq,hkv,causal", [(600, 900, 128, 4, 2, False), (900, 384, 64, 2, 1, True),
+                                                  (700, 500, 256, 2, 1, True)])
 def test_per_head_rectangular(n, nk, d, hq, hkv, causal):
     # N query rows against N_kv keys (the shape of one context-parallel rank),
     # with per-head vectors of N_kv entries and values in [0, N]
