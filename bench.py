@@ -531,12 +531,18 @@ def run_ours(args, cfg):
 # workload it was captured on, valid only while the kernel source is the one
 # the counters were taken from.
 NCU_TRAFFIC = {
-    "bwd": {"file": "fm_bwd.cu", "workload": "share_question32k",
-            "sha256": "891d619cb78bf460fb78043bd7a42efb687a2f8421f29c4cb1f1aa78a08ccb3b", "bytes": 1265336320,
-            "tensor_pipe_pct": 58.7},
-    "fwd": {"file": "fm_fwd.cu", "workload": "share_question32k",
-            "sha256": "e1668175cf543a774277f8ffa9b72224b54507a28d62508f2475fb480560d131", "bytes": 481902336,
-            "tensor_pipe_pct": 48.4},
+    ("bwd", 128): {"file": "fm_bwd.cu", "workload": "share_question32k",
+                   "sha256": "7ff3cb40b92e8b22dd88c7fed4fef9f6fe8fa3a1b6ec99a1b60e1df9ed96205b",
+                   "bytes": 822768640 + 450838784, "tensor_pipe_pct": 58.6},
+    ("fwd", 128): {"file": "fm_fwd.cu", "workload": "share_question32k",
+                   "sha256": "9033b1bc53179d8fe5edf72a09563eeb494eeb8a3e0fff4cdbbeb91de360bbe4",
+                   "bytes": 264743424 + 217453312, "tensor_pipe_pct": 49.4},
+    ("bwd", 256): {"file": "fm_bwd256.cu", "workload": "share_question32k",
+                   "sha256": "70351404ba35dc7671e143ecfa9c56e39e8a83407acaa646756670ca0a29f2b4",
+                   "bytes": 2569365760 + 1446258944, "tensor_pipe_pct": 42.3},
+    ("fwd", 256): {"file": "fm_fwd256.cu", "workload": "share_question32k",
+                   "sha256": "5e321b391679ab32f293ec6b9950b7e4f62b423a76b51f2ce019fcee09da0f6e",
+                   "bytes": 527683072 + 484918528, "tensor_pipe_pct": 48.5},
 }
 
 
@@ -546,8 +552,8 @@ def ncu_traffic(kind: str, workload: str, d: int, key: str = "bytes"):
     or None when the kernel source has changed since the capture."""
     import hashlib
 
-    ent = NCU_TRAFFIC.get(kind)
-    if not ent or ent["workload"] != workload or ent.get("d", 128) != d:
+    ent = NCU_TRAFFIC.get((kind, d))
+    if not ent or ent["workload"] != workload:
         return None
     src = os.path.join(ROOT, "mask_aware_sparse_gb300", "csrc", ent["file"])
     try:
