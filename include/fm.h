@@ -209,6 +209,36 @@ fm_status fm_attn_bwd_heads(const fm_problem* p, const void* q, const void* k, c
                             void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Multi-interval masks (the FlashMask Guide, "The Solution: FlashMask Sparse
+ * Mask Representation": up to four visible intervals [FMS_m,j, FME_m,j] per key
+ * column, disjoint within a column). Each interval m has its own four
+ * vectors, its masked complement (fm_from_fms_fme over the M * B rows of the
+ * (M, B, N_kv) FMS / FME arrays gives them), lts..ute (M, B, N_kv) int32. The
+ * keys a query row sees through different intervals are disjoint, so the
+ * attention over their union is one online softmax over the blocks of every
+ * interval's queue, each block masked with its own interval's vectors, and
+ * the gradients are the sums of the per-interval contributions: one forward
+ * and one backward launch accumulate them all (no per-interval passes, no
+ * merge). Everything else is fm_attn_fwd / fm_attn_bwd, except:
+ *   - the queues come from fm_classify_tiles run on the vectors as M * B rows
+ *     (an fm_problem with B' = M * B), row (m * B + b) holding interval m's
+ *     tiles of batch entry b; a block reached by several intervals is computed
+ *     once per interval;
+ *   - 1 <= M <= 4 (FM_ERR_INVALID_ARG otherwise); M = 1 is fm_attn_fwd /
+ *     fm_attn_bwd.
+ * Workspaces: fm_attn_fwd_workspace_bytes and fm_attn_bwd_workspace_bytes.
+ * ------------------------------------------------------------------------- */
+fm_status fm_attn_fwd_multi(const fm_problem* p, int32_t M, const void* q, const void* k, const void* v,
+                            const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
+                            const int32_t* q_off, const int32_t* q_queue, void* o, float* lse, void* ws,
+                            size_t ws_bytes, void* stream);
+fm_status fm_attn_bwd_multi(const fm_problem* p, int32_t M, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, const void* dout, const int32_t* lts,
+                            const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* k_off,
+                            const int32_t* k_queue, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/* ---------------------------------------------------------------------------
  * One forward + backward from HOST buffers. (No counterpart in the pages: an
  * end-to-end convenience over the calls above.)
  *

@@ -8,16 +8,18 @@ is no silent fallback.
 
 Functions carry the names of the C entry points:
   fm_classify_tiles, fm_attn_fwd, fm_attn_fwd_fp8, fm_attn_bwd, fm_attn_fwd_heads and
-  fm_attn_bwd_heads (per-head mask vectors), fm_attn_fwd_bwd_host (host buffers in
+  fm_attn_bwd_heads (per-head mask vectors), fm_attn_fwd_multi and fm_attn_bwd_multi
+  (multi-interval masks), fm_attn_fwd_bwd_host (host buffers in
   and out, device workspace), fm_localize, fm_device_status,
   fm_selftest_wait_timeout, fm_profile_enable, fm_profile_read, fm_launch_count,
   fm_from_fms_fme, fm_merge_parts, fm_sum_parts, fm_chunk_loads,
   fm_balance_chunks, fm_needed_chunks (host code: the chunk balancer and the
   K / V exchange plan for context parallelism);
 plus fm_classify_tiles_heads (fm_classify_tiles over the B * H_q rows of
-per-head vectors), fm_attn_multi_interval and fm_attn_per_head (multi-interval
-and per-head masks as sequences of library calls) and flashmask_attention (autograd wrapper: the classification, forward
-and backward calls in one differentiable op).
+per-head vectors), fm_attn_multi_interval and fm_attn_per_head (the library
+calls of a multi-interval / per-head forward and backward in sequence) and
+flashmask_attention (autograd wrapper: the classification, forward and
+backward calls in one differentiable op).
 """
 from __future__ import annotations
 
@@ -79,6 +81,10 @@ _SIGS = {
     "fm_attn_fwd_heads_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
     "fm_attn_fwd_heads": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 11 + [_P, ctypes.c_size_t, _P]),
     "fm_attn_bwd_heads": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 15 + [_P, ctypes.c_size_t, _P]),
+    "fm_attn_fwd_multi": (ctypes.c_int, [ctypes.POINTER(fm_problem), ctypes.c_int32] + [_P] * 11 +
+                          [_P, ctypes.c_size_t, _P]),
+    "fm_attn_bwd_multi": (ctypes.c_int, [ctypes.POINTER(fm_problem), ctypes.c_int32] + [_P] * 15 +
+                          [_P, ctypes.c_size_t, _P]),
     "fm_attn_host_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
     "fm_attn_fwd_bwd_host": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 13 + [_P, ctypes.c_size_t, _P]),
     "fm_attn_bwd": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 15 + [_P, ctypes.c_size_t, _P]),
@@ -184,11 +190,12 @@ def _bf16_ok(*ts):
 
 
 def _attn_args(q, k, v, vec, queues, *, backward, o=None, lse=None, do=None, dq=None, dk=None, dv=None, ws=None,
-               heads=False):
+               heads=False, intervals=0):
     """Shapes, dtypes and devices of an attention call, checked before the library
     sees any pointer (the C ABI receives bare pointers and cannot check them).
     Shape checks come first, so a mismatch is reported as such. heads: per-head
-    mask vectors (B, H_q, N_kv) and queues over B * H_q rows."""
+    mask vectors (B, H_q, N_kv) and queues over B * H_q rows; intervals = M > 0:
+    multi-interval vectors (M, B, N_kv) and queues over M * B rows."""
     _need(isinstance(q, torch.Tensor) and q.dim() == 4, "q must be a (B, H_q, N, d) tensor")
     B, Hq, N, d = q.shape
     _need(isinstance(k, torch.Tensor) and k.dim() == 4 and k.shape[0] == B and k.shape[3] == d,
@@ -198,7 +205,7 @@ def _attn_args(q, k, v, vec, queues, *, backward, o=None, lse=None, do=None, dq=
     _like(q, "q", (B, Hq, N, d), torch.bfloat16)
     _like(k, "k", (B, Hkv, Nk, d), torch.bfloat16)
     _like(v, "v", (B, Hkv, Nk, d), torch.bfloat16)
-    vshape = (B, Hq, Nk) if heads else (B, Nk)
+    vshape = (B, Hq, Nk) if heads else (intervals, B, Nk) if intervals else (B, Nk)
     for i, x in enumerate(vec):
         _like(x, f"mask vector {i}", vshape, torch.int32)
     for name, t in (("o", o), ("do", do), ("dq", dq)):
@@ -216,12 +223,12 @@ def _attn_args(q, k, v, vec, queues, *, backward, o=None, lse=None, do=None, dq=
     _need((queues.block_m, queues.block_n) == (bm, bn),
           f"queues were built with {queues.block_m} x {queues.block_n} tiles; the kernels need {bm} x {bn}")
     nq, nk = -(-N // bm), -(-Nk // bn)
-    R = B * Hq if heads else B  # queue rows per Q (K) block
+    R = B * Hq if heads else intervals * B if intervals else B  # queue rows per Q (K) block
     off, qu, nrows = (queues.k_off, queues.k_queue, R * nk) if backward else (queues.q_off, queues.q_queue, R * nq)
     _like(off, "queue offsets", (nrows + 1,), torch.int32)
     _need(isinstance(qu, torch.Tensor) and qu.dtype == torch.int32 and qu.is_contiguous()
           and qu.numel() >= max(1, R * nq * nk),
-          f"queue entries must be int32 with capacity {'B * H_q' if heads else 'B'} * nQ * nK")
+          f"queue entries must be int32 with capacity {R} * nQ * nK")
     _same_cuda(q=q, k=k, v=v, o=o, lse=lse, do=do, dq=dq, dk=dk, dv=dv, ws=ws, queue_offsets=off, queue=qu,
                **{f"mask vector {i}": x for i, x in enumerate(vec)})
 
@@ -466,26 +473,68 @@ def fm_sum_parts(parts, out=None, stream=None):
     return out
 
 
+def fm_attn_fwd_multi(q, k, v, lts, lte, uts, ute, queues: TileQueues, *, scale: float, causal: bool, o=None,
+                      lse=None, ws=None, stream=None):
+    """Forward with multi-interval masks: lts..ute (M, B, N_kv), one set per
+    interval, and the queues of fm_classify_tiles over their M * B rows.
+    Returns (O bf16, LSE fp32)."""
+    _need(isinstance(lts, torch.Tensor) and lts.dim() == 3, "multi-interval vectors must be (M, B, N_kv)")
+    M = lts.shape[0]
+    _attn_args(q, k, v, (lts, lte, uts, ute), queues, backward=False, o=o, lse=lse, ws=ws, intervals=M)
+    B, Hq, N, d = q.shape
+    prob = _problem(B, Hq, k.shape[1], N, d, scale, causal, k.shape[2])
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    wsb = lib().fm_attn_fwd_workspace_bytes(ctypes.byref(prob))
+    if ws is None or ws.numel() < wsb:
+        ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=q.device)
+    _check(lib().fm_attn_fwd_multi(ctypes.byref(prob), M, _ptr(q), _ptr(k), _ptr(v), _ptr(lts), _ptr(lte),
+                                   _ptr(uts), _ptr(ute), _ptr(queues.q_off), _ptr(queues.q_queue), _ptr(o),
+                                   _ptr(lse), _ptr(ws), ctypes.c_size_t(wsb), _stream(stream)), "fm_attn_fwd_multi")
+    return o, lse
+
+
+def fm_attn_bwd_multi(q, k, v, o, lse, do, lts, lte, uts, ute, queues: TileQueues, *, scale: float, causal: bool,
+                      dq=None, dk=None, dv=None, ws=None, stream=None):
+    """Backward with multi-interval masks (lts..ute (M, B, N_kv)): returns
+    (dQ, dK, dV) bf16."""
+    _need(isinstance(lts, torch.Tensor) and lts.dim() == 3, "multi-interval vectors must be (M, B, N_kv)")
+    M = lts.shape[0]
+    _attn_args(q, k, v, (lts, lte, uts, ute), queues, backward=True, o=o, lse=lse, do=do, dq=dq, dk=dk, dv=dv,
+               ws=ws, intervals=M)
+    B, Hq, N, d = q.shape
+    prob = _problem(B, Hq, k.shape[1], N, d, scale, causal, k.shape[2])
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    wsb = lib().fm_attn_bwd_workspace_bytes(ctypes.byref(prob))
+    if ws is None or ws.numel() < wsb:
+        ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=q.device)
+    _check(lib().fm_attn_bwd_multi(ctypes.byref(prob), M, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                   _ptr(lts), _ptr(lte), _ptr(uts), _ptr(ute), _ptr(queues.k_off),
+                                   _ptr(queues.k_queue), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                                   ctypes.c_size_t(wsb), _stream(stream)), "fm_attn_bwd_multi")
+    return dq, dk, dv
+
+
 def fm_attn_multi_interval(q, k, v, fms, fme, *, scale: float, do=None, stream=None):
     """Attention under multi-interval masks: fms, fme are (M, B, N_kv) int32 CUDA
-    tensors, key j visible to rows [fms[m, b, j], fme[m, b, j]] (inclusive),
-    intervals of one column disjoint. Library calls only: per interval
-    fm_from_fms_fme, fm_classify_tiles and fm_attn_fwd, then fm_merge_parts;
-    with do, per interval fm_attn_bwd on the merged O and LSE, then fm_sum_parts.
+    tensors (M <= 4), key j visible to rows [fms[m, b, j], fme[m, b, j]]
+    (inclusive), intervals of one column disjoint. Library calls only:
+    fm_from_fms_fme over the M * B rows (each interval's masked complement),
+    fm_classify_tiles over those rows, fm_attn_fwd_multi and, with do,
+    fm_attn_bwd_multi (one launch each over every interval).
     Returns (o, lse) or (o, lse, dq, dk, dv)."""
+    _need(isinstance(fms, torch.Tensor) and fms.dim() == 3, "fms, fme must be (M, B, N_kv)")
+    M, B, Nk = fms.shape
     N = q.shape[2]
-    parts = []
-    for m in range(fms.shape[0]):
-        vec = fm_from_fms_fme(fms[m], fme[m], n_rows=N, stream=stream)
-        qs = fm_classify_tiles(*vec, causal=False, n_rows=N, stream=stream)
-        o_m, lse_m = fm_attn_fwd(q, k, v, *vec, qs, scale=scale, causal=False, stream=stream)
-        parts.append((vec, qs, o_m, lse_m))
-    o, lse = fm_merge_parts([p[2] for p in parts], [p[3] for p in parts], stream=stream)
+    vec = fm_from_fms_fme(fms.reshape(M * B, Nk), fme.reshape(M * B, Nk), n_rows=N, stream=stream)
+    qs = fm_classify_tiles(*vec, causal=False, n_rows=N, stream=stream)
+    vec = tuple(x.view(M, B, Nk) for x in vec)
+    o, lse = fm_attn_fwd_multi(q, k, v, *vec, qs, scale=scale, causal=False, stream=stream)
     if do is None:
         return o, lse
-    grads = [fm_attn_bwd(q, k, v, o, lse, do, *vec, qs, scale=scale, causal=False, stream=stream)
-             for vec, qs, _, _ in parts]
-    dq, dk, dv = (fm_sum_parts([g[i] for g in grads], stream=stream) for i in range(3))
+    dq, dk, dv = fm_attn_bwd_multi(q, k, v, o, lse, do, *vec, qs, scale=scale, causal=False, stream=stream)
     return o, lse, dq, dk, dv
 
 

@@ -318,6 +318,49 @@ fm_status fm_attn_bwd_heads(const fm_problem* p, const void* q, const void* k, c
                               static_cast<cudaStream_t>(stream), err, true));
 }
 
+fm_status fm_attn_fwd_multi(const fm_problem* p, int32_t M, const void* q, const void* k, const void* v,
+                            const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
+                            const int32_t* q_off, const int32_t* q_queue, void* o, float* lse, void* ws,
+                            size_t ws_bytes, void* stream) {
+  bool empty = false;
+  fm_status st = check_problem(p, &empty);
+  if (st != FM_OK) return st;
+  if (M < 1 || M > 4) return FM_ERR_INVALID_ARG;
+  if (empty) return FM_OK;
+  if ((st = check_attn_shape(p, false)) != FM_OK) return st;
+  if (!q || !k || !v || !lts || !lte || !uts || !ute || !q_off || !q_queue || !o || !lse) return FM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FM_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < fwd_ws_bytes(*p)) return FM_ERR_WORKSPACE;
+  int* err = device_error_word();
+  if (!err) return FM_ERR_CUDA;
+  return from_cuda(launch_fwd_multi(*p, M, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws,
+                                    static_cast<cudaStream_t>(stream), err));
+}
+
+fm_status fm_attn_bwd_multi(const fm_problem* p, int32_t M, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, const void* dout, const int32_t* lts,
+                            const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* k_off,
+                            const int32_t* k_queue, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                            void* stream) {
+  bool empty = false;
+  fm_status st = check_problem(p, &empty);
+  if (st != FM_OK) return st;
+  if (M < 1 || M > 4) return FM_ERR_INVALID_ARG;
+  if (empty) return FM_OK;
+  if ((st = check_attn_shape(p, true)) != FM_OK) return st;
+  if (!q || !k || !v || !o || !lse || !dout || !lts || !lte || !uts || !ute || !k_off || !k_queue || !dq || !dk ||
+      !dv)
+    return FM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv))
+    return FM_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < bwd_ws_bytes(*p)) return FM_ERR_WORKSPACE;
+  int* err = device_error_word();
+  if (!err) return FM_ERR_CUDA;
+  return from_cuda(launch_bwd(*p, q, k, v, o, lse, dout, lts, lte, uts, ute, k_off, k_queue, dq, dk, dv, ws,
+                              static_cast<cudaStream_t>(stream), err, false, M));
+}
+
 fm_status fm_attn_fwd_fp8(const fm_problem* p, const void* q, const void* k, const void* v, float q_scale,
                           float k_scale, float v_scale, const int32_t* lts, const int32_t* lte, const int32_t* uts,
                           const int32_t* ute, const int32_t* q_off, const int32_t* q_queue, void* o, float* lse,

@@ -114,6 +114,7 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int B, H_q, H_kv, N, Nk, Npad, nK, G, causal;  // N query rows (Npad rounded up to the tile), Nk key rows
+  int M;  // multi-interval masks: vectors (M, B, N_kv), queues over M * B rows (1 otherwise)
   float scale, scale_log2;
   int* err;
 };
@@ -125,7 +126,7 @@ constexpr int kMaxHeads = 64;
 // The CTA's queue segment is staged in shared memory (s_queue) when it fits,
 // so no role waits on a dependent global load per unit.
 struct Unit {
-  int h, qb, half, part;
+  int h, qb, half, part, m;  // m: the interval of a multi-interval mask
 };
 __device__ __forceinline__ Unit decode_unit(const BwdParams& p, int u, int L, int kbeg, int g, bool force_part,
                                             uint32_t s_queue, int qcap) {
@@ -138,6 +139,7 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams& p, int u, int L, in
   r.qb = e >> 1;
   r.half = rem & 1;
   r.part = (e & 1) | (force_part ? 1 : 0);
+  r.m = 0;
   return r;
 }
 
@@ -156,11 +158,36 @@ __device__ __forceinline__ Unit decode_unit_ph(const BwdParams& p, int u, int g,
   r.qb = e >> 1;
   r.half = rem & 1;
   r.part = (e & 1) | (force_part ? 1 : 0);
+  r.m = 0;
   return r;
 }
 
-// PH: per-head mask vectors (B, H_q, N_kv) and queues over B * H_q rows.
-template <int D, bool PH>
+// The same with multi-interval masks: interval m's queue for this KV block is
+// walked for every head of the group ([2 G hoff[m], 2 G hoff[m + 1]) are its
+// units: head-major within it, then the queue, then the half); the staged
+// entries are the intervals' queues back to back; m is the caller's cursor.
+__device__ __forceinline__ Unit decode_unit_multi(const BwdParams& p, int u, int g, bool force_part,
+                                                  uint32_t s_queue, int qcap, const int* hoff, int& m) {
+  while (u >= 2 * p.G * hoff[m + 1]) ++m;
+  const int Lm = hoff[m + 1] - hoff[m];
+  const int rem = u - 2 * p.G * hoff[m];
+  const int hi = rem / (2 * Lm);
+  const int r2 = rem - hi * 2 * Lm;
+  const int pos = hoff[m] + (r2 >> 1);
+  const int e = (pos < qcap) ? lds_s32(s_queue + 4 * pos) : p.k_queue[hoff[kMaxHeads + 1 + m] + (r2 >> 1)];
+  Unit r;
+  r.h = g * p.G + hi;
+  r.qb = e >> 1;
+  r.half = r2 & 1;
+  r.part = (e & 1) | (force_part ? 1 : 0);
+  r.m = m;
+  return r;
+}
+
+// MODE 0: mask vectors (B, N_kv) shared by the heads; 1: per-head vectors
+// (B, H_q, N_kv) and queues over B * H_q rows; 2: multi-interval vectors
+// (M, B, N_kv) and queues over M * B rows.
+template <int D, int MODE>
 __global__ void __launch_bounds__(480, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -168,6 +195,7 @@ __global__ void __launch_bounds__(480, 1)
                const __grid_constant__ CUtensorMap tdq, const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int S = C::STAGES;
+  constexpr bool PH = MODE == 1, MI = MODE == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -180,10 +208,15 @@ __global__ void __launch_bounds__(480, 1)
   const int bk = p.order ? p.order[oi] : oi;
   const int nK = p.nK;
   const int b = bk / nK, kb = bk - b * nK;
-  int kbeg = 0, L = 0;  // per-head masks: L sums the heads' queue lengths
+  int kbeg = 0, L = 0;  // per-head / multi-interval masks: L sums the heads' / intervals' queue lengths
   if constexpr (PH) {
     for (int hi = 0; hi < p.G; ++hi) {
       const int r = (b * p.H_q + g * p.G + hi) * nK + kb;
+      L += p.k_off[r + 1] - p.k_off[r];
+    }
+  } else if constexpr (MI) {
+    for (int mi = 0; mi < p.M; ++mi) {
+      const int r = (mi * p.B + b) * nK + kb;
       L += p.k_off[r + 1] - p.k_off[r];
     }
   } else {
@@ -251,13 +284,32 @@ __global__ void __launch_bounds__(480, 1)
         while (hi + 1 < p.G && hoff[hi + 1] <= t) ++hi;
         sq[t] = p.k_queue[hoff[kMaxHeads + 1 + hi] + (t - hoff[hi])];
       }
+    } else if constexpr (MI) {
+      if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int mi = 0; mi < p.M; ++mi) {
+          const int r = (mi * p.B + b) * nK + kb;
+          hoff[mi] = acc;
+          hoff[kMaxHeads + 1 + mi] = p.k_off[r];
+          acc += p.k_off[r + 1] - p.k_off[r];
+        }
+        hoff[p.M] = acc;
+      }
+      __syncthreads();
+      for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) {
+        int mi = 0;
+        while (mi + 1 < p.M && hoff[mi + 1] <= t) ++mi;
+        sq[t] = p.k_queue[hoff[kMaxHeads + 1 + mi] + (t - hoff[mi])];
+      }
     } else {
       for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) sq[t] = p.k_queue[kbeg + t];
     }
   }
-  // the unit decoder of every role (a cursor over the heads with per-head masks)
+  // the unit decoder of every role (a cursor over the heads with per-head
+  // masks, over the intervals with multi-interval masks)
   auto decode = [&](int u, int& hcur) -> Unit {
     if constexpr (PH) return decode_unit_ph(p, u, g, force_part, s_queue, C::QUEUE_CAP, hoff, hcur);
+    else if constexpr (MI) return decode_unit_multi(p, u, g, force_part, s_queue, C::QUEUE_CAP, hoff, hcur);
     else return decode_unit(p, u, L, kbeg, g, force_part, s_queue, C::QUEUE_CAP);
   };
   if (C::ZERO_BYTES > 0) {
@@ -456,8 +508,8 @@ __global__ void __launch_bounds__(480, 1)
       if (a0 < a1) { lo0 = a0; lo1 = a1; }
       if (u0 < u1) { up0 = u0; up1 = u1; }
     };
-    int mhead = -1;  // the head whose vectors are loaded (per-head masks)
-    if constexpr (!PH) load_mask(b);
+    int mhead = -1;  // the head (interval) whose vectors are loaded (per-head / multi-interval masks)
+    if constexpr (MODE == 0) load_mask(b);
     const float sl2 = p.scale_log2;
     const bool causal = p.causal != 0;
     const uint32_t s_rows = smem_u32(smem + C::ROW_OFF);
@@ -472,6 +524,11 @@ __global__ void __launch_bounds__(480, 1)
         if (un.h != mhead) {
           load_mask(b * p.H_q + un.h);
           mhead = un.h;
+        }
+      } else if constexpr (MI) {
+        if (un.m != mhead) {
+          load_mask(un.m * p.B + b);
+          mhead = un.m;
         }
       }
       const int stage = u % S;
@@ -774,7 +831,7 @@ BwdWs carve(const fm_problem& P, void* ws) {
   return r;
 }
 
-template <int D, bool PH = false>
+template <int D, int MODE = 0>
 cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, const void* v, const void* o,
                          const float* lse, const void* dout, void* dq, const BwdParams& prm0, const BwdWs& w,
                          cudaStream_t s) {
@@ -795,12 +852,14 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   // dQ rows at once).
   // (d = 256 runs two CTAs per KV block, one per head-dim half)
   // (per-head masks: natural order; the order kernel reads one queue per (batch, KV block))
-  const bool natural = PH || use_natural_order((D == 256 ? 2LL : 1LL) * P.B * nK * P.H_kv);
+  // (multi-interval masks: natural order; a KV block's length sums M queues)
+  const bool natural = MODE != 0 || use_natural_order((D == 256 ? 2LL : 1LL) * P.B * nK * P.H_kv);
   if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(prm0.k_off, P.B * nK, w.order);
   // 3. main kernel
   if constexpr (D == 256) {
     e = launch_bwd256_main(P, q, k, v, dout, prm0.lts, prm0.lte, prm0.uts, prm0.ute, prm0.k_off, prm0.k_queue,
-                           natural ? nullptr : w.order, w.nl, w.dsum, w.dq_acc, prm0.dk, prm0.dv, s, prm0.err, PH);
+                           natural ? nullptr : w.order, w.nl, w.dsum, w.dq_acc, prm0.dk, prm0.dv, s, prm0.err, MODE,
+                           prm0.M);
     if (e != cudaSuccess) return e;
   } else {
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
@@ -816,7 +875,7 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   using C = BwdCfg<D>;
   static bool attr_done = false;
   if (!attr_done) {
-    e = cudaFuncSetAttribute(bwd_kernel<D, PH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    e = cudaFuncSetAttribute(bwd_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -825,7 +884,7 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
     KernelTimer timer(s, kTimedBwd);
     BwdParams prm = prm0;
     if (natural) prm.order = nullptr;
-    bwd_kernel<D, PH><<<(unsigned)grid, 480, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
+    bwd_kernel<D, MODE><<<(unsigned)grid, 480, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
   }
   }
   // 4. dQ = bf16(scale * dQacc)
@@ -850,7 +909,7 @@ size_t bwd_ws_bytes(const fm_problem& P) {
 cudaError_t launch_bwd(const fm_problem& P, const void* q, const void* k, const void* v, const void* o,
                        const float* lse, const void* dout, const int32_t* lts, const int32_t* lte,
                        const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
-                       void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err, bool per_head) {
+                       void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err, bool per_head, int M) {
   const int Nk = kv_rows(P);
   const int nK = (Nk + kTile - 1) / kTile;
   const long long grid = (long long)P.B * nK * P.H_kv;
@@ -876,6 +935,7 @@ cudaError_t launch_bwd(const fm_problem& P, const void* q, const void* k, const 
   prm.Nk = Nk;
   prm.Npad = (P.N + kTile - 1) / kTile * kTile;
   prm.nK = nK;
+  prm.M = M;
   prm.G = P.H_q / P.H_kv;
   prm.causal = P.causal ? 1 : 0;
   prm.scale = P.scale;
@@ -883,9 +943,16 @@ cudaError_t launch_bwd(const fm_problem& P, const void* q, const void* k, const 
   prm.err = err;
   if (per_head) {
     if (P.H_q / P.H_kv > kMaxHeads) return cudaErrorInvalidValue;
-    if (P.d == 128) return launch_bwd_d<128, true>(P, q, k, v, o, lse, dout, dq, prm, w, s);
-    if (P.d == 64) return launch_bwd_d<64, true>(P, q, k, v, o, lse, dout, dq, prm, w, s);
-    if (P.d == 256) return launch_bwd_d<256, true>(P, q, k, v, o, lse, dout, dq, prm, w, s);
+    if (P.d == 128) return launch_bwd_d<128, 1>(P, q, k, v, o, lse, dout, dq, prm, w, s);
+    if (P.d == 64) return launch_bwd_d<64, 1>(P, q, k, v, o, lse, dout, dq, prm, w, s);
+    if (P.d == 256) return launch_bwd_d<256, 1>(P, q, k, v, o, lse, dout, dq, prm, w, s);
+    return cudaErrorInvalidValue;
+  }
+  if (M > 1) {
+    if (M > 4) return cudaErrorInvalidValue;
+    if (P.d == 128) return launch_bwd_d<128, 2>(P, q, k, v, o, lse, dout, dq, prm, w, s);
+    if (P.d == 64) return launch_bwd_d<64, 2>(P, q, k, v, o, lse, dout, dq, prm, w, s);
+    if (P.d == 256) return launch_bwd_d<256, 2>(P, q, k, v, o, lse, dout, dq, prm, w, s);
     return cudaErrorInvalidValue;
   }
   if (P.d == 256) return launch_bwd_d<256>(P, q, k, v, o, lse, dout, dq, prm, w, s);

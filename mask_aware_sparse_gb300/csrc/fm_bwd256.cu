@@ -101,6 +101,7 @@ struct Bwd256Params {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int B, H_q, H_kv, N, Nk, Npad, nK, G, causal;
+  int M;  // multi-interval masks: vectors (M, B, N_kv), queues over M * B rows (1 otherwise)
   float scale, scale_log2;
   int* err;
 };
@@ -109,7 +110,7 @@ struct Bwd256Params {
 constexpr int kMaxHeads256 = 64;
 
 struct Unit256 {
-  int h, qb, half, part;
+  int h, qb, half, part, m;  // m: the interval of a multi-interval mask
 };
 __device__ __forceinline__ Unit256 decode256(const Bwd256Params& p, int u, int L, int kbeg, int g, bool force_part,
                                              uint32_t s_queue) {
@@ -122,6 +123,7 @@ __device__ __forceinline__ Unit256 decode256(const Bwd256Params& p, int u, int L
   r.qb = e >> 1;
   r.half = rem & 1;
   r.part = (e & 1) | (force_part ? 1 : 0);
+  r.m = 0;
   return r;
 }
 // The same with per-head mask vectors: head hi of the group owns the units
@@ -141,11 +143,35 @@ __device__ __forceinline__ Unit256 decode256_ph(const Bwd256Params& p, int u, in
   r.qb = e >> 1;
   r.half = rem & 1;
   r.part = (e & 1) | (force_part ? 1 : 0);
+  r.m = 0;
+  return r;
+}
+// The same with multi-interval masks: interval m's queue for this KV block is
+// walked for every head of the group (units [2 G hoff[m], 2 G hoff[m + 1]),
+// head-major, then the queue, then the half); m is the caller's cursor.
+__device__ __forceinline__ Unit256 decode256_multi(const Bwd256Params& p, int u, int b, int kb, int g,
+                                                   bool force_part, uint32_t s_queue, const int* hoff, int& m) {
+  while (u >= 2 * p.G * hoff[m + 1]) ++m;
+  const int Lm = hoff[m + 1] - hoff[m];
+  const int rem = u - 2 * p.G * hoff[m];
+  const int hi = rem / (2 * Lm);
+  const int r2 = rem - hi * 2 * Lm;
+  const int pos = hoff[m] + (r2 >> 1);
+  const int e = (pos < B256::QUEUE_CAP) ? lds_s32(s_queue + 4 * pos)
+                                         : p.k_queue[p.k_off[(m * p.B + b) * p.nK + kb] + (r2 >> 1)];
+  Unit256 r;
+  r.h = g * p.G + hi;
+  r.qb = e >> 1;
+  r.half = r2 & 1;
+  r.part = (e & 1) | (force_part ? 1 : 0);
+  r.m = m;
   return r;
 }
 
-// PH: per-head mask vectors (B, H_q, N_kv) and queues over B * H_q rows.
-template <bool PH>
+// MODE 0: mask vectors (B, N_kv) shared by the heads; 1: per-head vectors
+// (B, H_q, N_kv) and queues over B * H_q rows; 2: multi-interval vectors
+// (M, B, N_kv) and queues over M * B rows.
+template <int MODE>
 __global__ void __launch_bounds__(448, 1)
     bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -153,6 +179,7 @@ __global__ void __launch_bounds__(448, 1)
                   const __grid_constant__ CUtensorMap tdq, const Bwd256Params p) {
   using C = B256;
   constexpr int DH = C::DH;
+  constexpr bool PH = MODE == 1, MI = MODE == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -169,10 +196,15 @@ __global__ void __launch_bounds__(448, 1)
   const int bk = p.order ? p.order[oi] : oi;
   const int nK = p.nK;
   const int b = bk / nK, kb = bk - b * nK;
-  int kbeg = 0, L = 0;  // per-head masks: L sums the heads' queue lengths
+  int kbeg = 0, L = 0;  // per-head / multi-interval masks: L sums the heads' / intervals' queue lengths
   if constexpr (PH) {
     for (int hi = 0; hi < p.G; ++hi) {
       const int r = (b * p.H_q + g * p.G + hi) * nK + kb;
+      L += p.k_off[r + 1] - p.k_off[r];
+    }
+  } else if constexpr (MI) {
+    for (int mi = 0; mi < p.M; ++mi) {
+      const int r = (mi * p.B + b) * nK + kb;
       L += p.k_off[r + 1] - p.k_off[r];
     }
   } else {
@@ -239,6 +271,22 @@ __global__ void __launch_bounds__(448, 1)
         while (hi + 1 < p.G && hoff[hi + 1] <= t) ++hi;
         sq[t] = p.k_queue[p.k_off[(b * p.H_q + g * p.G + hi) * nK + kb] + (t - hoff[hi])];
       }
+    } else if constexpr (MI) {
+      if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int mi = 0; mi < p.M; ++mi) {
+          const int r = (mi * p.B + b) * nK + kb;
+          hoff[mi] = acc;
+          acc += p.k_off[r + 1] - p.k_off[r];
+        }
+        hoff[p.M] = acc;
+      }
+      __syncthreads();
+      for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) {
+        int mi = 0;
+        while (mi + 1 < p.M && hoff[mi + 1] <= t) ++mi;
+        sq[t] = p.k_queue[p.k_off[(mi * p.B + b) * nK + kb] + (t - hoff[mi])];
+      }
     } else {
       for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) sq[t] = p.k_queue[kbeg + t];
     }
@@ -246,6 +294,7 @@ __global__ void __launch_bounds__(448, 1)
   // the unit decoder of every role (a cursor over the heads with per-head masks)
   auto decode = [&](int u, int& hcur) -> Unit256 {
     if constexpr (PH) return decode256_ph(p, u, b, kb, g, force_part, s_queue, hoff, hcur);
+    else if constexpr (MI) return decode256_multi(p, u, b, kb, g, force_part, s_queue, hoff, hcur);
     else return decode256(p, u, L, kbeg, g, force_part, s_queue);
   };
   if (warp == 13) tmem_alloc<512>(tmem_slot);
@@ -402,7 +451,7 @@ __global__ void __launch_bounds__(448, 1)
       if (u0 < u1) { up0 = u0; up1 = u1; }
     };
     int mhead = -1;  // the head whose vectors are loaded (per-head masks)
-    if constexpr (!PH) load_mask(b);
+    if constexpr (MODE == 0) load_mask(b);
     const float sl2 = p.scale_log2;
     const bool causal = p.causal != 0;
     const uint32_t rows_b = smem_u32(smem + C::ROW_OFF) + 128 * half;  // nl[32*half ..]; D at +256
@@ -417,6 +466,11 @@ __global__ void __launch_bounds__(448, 1)
         if (un.h != mhead) {
           load_mask(b * p.H_q + un.h);
           mhead = un.h;
+        }
+      } else if constexpr (MI) {
+        if (un.m != mhead) {
+          load_mask(un.m * p.B + b);
+          mhead = un.m;
         }
       }
       const uint32_t ph = (uint32_t)u & 1u;
@@ -612,7 +666,7 @@ cudaError_t launch_bwd256_main(const fm_problem& P, const void* q, const void* k
                                const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
                                const int32_t* k_off, const int32_t* k_queue, const int32_t* order, const float* nl,
                                const float* dsum, float* dq_acc, void* dk, void* dv, cudaStream_t s, int* err,
-                               bool per_head) {
+                               int mode, int M) {
   using C = B256;
   const int Nk = kv_rows(P);
   const int nK = (Nk + kTile - 1) / kTile;
@@ -648,25 +702,31 @@ cudaError_t launch_bwd256_main(const fm_problem& P, const void* q, const void* k
   prm.nK = nK;
   prm.G = P.H_q / P.H_kv;
   prm.causal = P.causal ? 1 : 0;
+  prm.M = M;
   prm.scale = P.scale;
   prm.scale_log2 = P.scale * 1.4426950408889634f;
   prm.err = err;
-  static bool attr_done[2] = {false, false};
-  if (!attr_done[per_head]) {
-    cudaError_t e = cudaFuncSetAttribute(per_head ? bwd256_kernel<true> : bwd256_kernel<false>,
+  if (mode < 0 || mode > 2) return cudaErrorInvalidValue;
+  if (mode == 1 && P.H_q / P.H_kv > kMaxHeads256) return cudaErrorInvalidValue;
+  if (mode == 2 && (M < 1 || M > 4)) return cudaErrorInvalidValue;
+  // the order table reads one queue per (batch, KV block): natural order with
+  // per-head and multi-interval masks
+  if (mode != 0) prm.order = nullptr;
+  static bool attr_done[3] = {false, false, false};
+  if (!attr_done[mode]) {
+    cudaError_t e = cudaFuncSetAttribute(mode == 1 ? bwd256_kernel<1> : mode == 2 ? bwd256_kernel<2> : bwd256_kernel<0>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    attr_done[per_head] = true;
+    attr_done[mode] = true;
   }
   {
     KernelTimer timer(s, kTimedBwd);
-    if (per_head) {
-      if (P.H_q / P.H_kv > kMaxHeads256) return cudaErrorInvalidValue;
-      prm.order = nullptr;  // the order table reads one queue per (batch, KV block)
-      bwd256_kernel<true><<<(unsigned)grid, 448, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
-    } else {
-      bwd256_kernel<false><<<(unsigned)grid, 448, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
-    }
+    if (mode == 1)
+      bwd256_kernel<1><<<(unsigned)grid, 448, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
+    else if (mode == 2)
+      bwd256_kernel<2><<<(unsigned)grid, 448, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
+    else
+      bwd256_kernel<0><<<(unsigned)grid, 448, C::SMEM_ALLOC, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
   }
   return cudaGetLastError();
 }

@@ -101,8 +101,10 @@ struct FwdCfg {
   static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
 };
 
-// unit header words in the unit ring
-enum { UH_N = 0, UH_T = 1, UH_QB = 2, UH_B = 3, UH_H0 = 4, UH_G = 5, UH_QBEG = 6, UH_END = 7 };
+// unit header words in the unit ring (multi-interval masks: the queue start
+// and the first unit-queue position of interval m at UH_SEGQ + m, UH_SEGC + m)
+enum { UH_N = 0, UH_T = 1, UH_QB = 2, UH_B = 3, UH_H0 = 4, UH_G = 5, UH_QBEG = 6, UH_END = 7, UH_SEGQ = 8,
+       UH_SEGC = 12 };
 
 struct FwdParams {
   const int32_t* lts;
@@ -118,6 +120,11 @@ struct FwdParams {
   int B, H_q, H_kv, N, Nk, nQ, nK, G, PG, causal;  // N query rows, Nk key rows
   int units;  // B * nQ * H_kv * PG work units (per-head masks: B * H_q * nQ)
   int per_head;  // mask vectors and queues per (batch, query head): one head per unit
+  // multi-interval masks: M sets of vectors (M, B, N_kv) and queues over the
+  // M * B vector rows; a unit walks its Q block's M queues one after the
+  // other (entries tagged with m in bits 24-25), each with its own vectors.
+  // 1 otherwise.
+  int M;
   float scale_log2;
   float o_scale;  // multiplies O / l (the V dequantization scale of the FP8 forward; 1 otherwise)
   int* err;
@@ -163,14 +170,25 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int k) {
   return u;
 }
 
+// Queue entry of a unit: (kb << 1) | partial, with the interval index of a
+// multi-interval mask in bits 24-25 (kb < 2^23).
+constexpr int kKbMask = (1 << 23) - 1;
+template <bool MI>
+__device__ __forceinline__ int entry_kb(int e) {
+  if constexpr (MI) return (e >> 1) & kKbMask;
+  else return e >> 1;
+}
+
 // A queue block is partial when the classification tagged it so, or when it
 // is the last key block and N is not a multiple of 128 (its tail columns are
 // masked for every row).
+template <bool MI>
 __device__ __forceinline__ bool block_partial(const FwdParams& p, int e) {
-  return (e & 1) || ((e >> 1) == p.nK - 1 && (p.Nk & 127));
+  return (e & 1) || (entry_kb<MI>(e) == p.nK - 1 && (p.Nk & 127));
 }
 
-template <int D, bool F8>
+// MI: multi-interval masks (the unit walks p.M queues, entries tagged).
+template <int D, bool F8, bool MI>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, const FwdParams p) {
@@ -226,8 +244,11 @@ __global__ void __launch_bounds__(320, 1)
   // staged prefix come from global memory)
   auto hdr_at = [&](int us, int w) -> int { return lds_s32(smem_u32(smem + C::U_OFF + us * C::U_BYTES) + 4 * w); };
   auto queue_at = [&](int us, int j) -> int {
-    return (j < C::QUEUE_CAP) ? lds_s32(smem_u32(smem + C::U_OFF + us * C::U_BYTES) + 4 * (C::U_HDR + j))
-                              : p.q_queue[hdr_at(us, UH_QBEG) + j];
+    if (j < C::QUEUE_CAP) return lds_s32(smem_u32(smem + C::U_OFF + us * C::U_BYTES) + 4 * (C::U_HDR + j));
+    if constexpr (!MI) return p.q_queue[hdr_at(us, UH_QBEG) + j];
+    int m = 0;
+    while (m + 1 < p.M && j >= hdr_at(us, UH_SEGC + m + 1)) ++m;
+    return p.q_queue[hdr_at(us, UH_SEGQ + m) + j - hdr_at(us, UH_SEGC + m)] | (m << 24);
   };
 
   // Every role walks the CTA's unit sequence through the unit ring (filled by
@@ -261,7 +282,17 @@ __global__ void __launch_bounds__(320, 1)
       // the next unit's index, requested now and used after this unit
       int k_next = 0;
       if (lane == 0) k_next = (int)gridDim.x + atomicAdd(p.next_unit, 1);
-      const Unit u = decode_unit(p, k);
+      Unit u = decode_unit(p, k);
+      // multi-interval masks: the M queues of this Q block, back to back
+      int segq[4] = {u.qbeg, 0, 0, 0}, segc[5] = {0, u.n, u.n, u.n, u.n};
+      if constexpr (MI) {
+        for (int mi = 1; mi < p.M; ++mi) {
+          const int r = (mi * p.B + u.b) * p.nQ + u.qb;
+          segq[mi] = p.q_off[r];
+          segc[mi + 1] = segc[mi] + (p.q_off[r + 1] - segq[mi]);
+        }
+        u.n = segc[p.M];
+      }
       {
         if (lane == 0) {
           h[UH_END] = 0;
@@ -272,6 +303,13 @@ __global__ void __launch_bounds__(320, 1)
           h[UH_H0] = u.h0;
           h[UH_G] = u.g;
           h[UH_QBEG] = u.qbeg;
+          if constexpr (MI) {
+#pragma unroll
+            for (int mi = 0; mi < 4; ++mi) {
+              h[UH_SEGQ + mi] = segq[mi];
+              h[UH_SEGC + mi] = segc[mi];
+            }
+          }
         }
         int* sq = h + C::U_HDR;
         const int m = min(u.n, C::QUEUE_CAP);
@@ -280,7 +318,13 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int j = j0 + 32 * r + lane;
-            e[r] = (j < m) ? p.q_queue[u.qbeg + j] : 0;
+            if constexpr (!MI) {
+              e[r] = (j < m) ? p.q_queue[u.qbeg + j] : 0;
+            } else {
+              int mi = 0;
+              while (mi + 1 < p.M && j >= segc[mi + 1]) ++mi;
+              e[r] = (j < m) ? (p.q_queue[segq[mi] + j - segc[mi]] | (mi << 24)) : 0;
+            }
           }
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
@@ -293,17 +337,18 @@ __global__ void __launch_bounds__(320, 1)
       }
       k = __shfl_sync(kFull, k_next, 0);
       if (u.n <= 0) continue;
-      const size_t vbase = (size_t)u.vrow * p.Nk;
       for (int j = 0; j < u.n && ok; ++j) {
         const int e = queue_at(us, j);
-        const int kb = e >> 1;
+        const int kb = entry_kb<MI>(e);
+        // the vectors of this entry's mask (multi-interval: of its interval)
+        const size_t vbase = (size_t)(MI ? (e >> 24) * p.B + u.b : u.vrow) * p.Nk;
         if (kb < 0 || kb >= p.nK) {
           if (lane == 0) record_error(p.err, FM_DEV_ERR_QUEUE);
           *abort_flag = 1;
           ok = false;
           break;
         }
-        const bool part = block_partial(p, e);
+        const bool part = block_partial<MI>(p, e);
         const int slot = jt % S;
         const uint32_t ph = (jt / S) & 1u;
         if (lane == 0) {
@@ -583,7 +628,7 @@ __global__ void __launch_bounds__(320, 1)
         // partial-block count (head 0 releases the mask ring for both)
         uint32_t c = 0;
         for (int j0 = 0; j0 < n; j0 += 32) {
-          const bool part = (j0 + lane < n) && block_partial(p, queue_at(us, j0 + lane));
+          const bool part = (j0 + lane < n) && block_partial<MI>(p, queue_at(us, j0 + lane));
           c += __popc(__ballot_sync(kFull, part));
         }
         pidx += c;
@@ -595,8 +640,8 @@ __global__ void __launch_bounds__(320, 1)
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < n; ++j) {
         const int e = queue_at(us, j);
-        const int kb = e >> 1;
-        const bool part = block_partial(p, e);
+        const int kb = entry_kb<MI>(e);
+        const bool part = block_partial<MI>(p, e);
         // Partial blocks: masked-row bits of this thread's query row over the
         // block's 128 key columns, built while S is still being computed. Lane
         // c of the warp builds the bits of key column 32k + c over the warp's
@@ -762,20 +807,20 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 
-template <int D, bool F8>
+template <int D, bool F8, bool MI = false>
 cudaError_t launch_fwd_d(const fm_problem& P, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, const FwdParams& prm, unsigned grid, cudaStream_t s) {
   using C = FwdCfg<D, F8>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e =
-        cudaFuncSetAttribute(fwd_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        cudaFuncSetAttribute(fwd_kernel<D, F8, MI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   {
     KernelTimer timer(s, kTimedFwd);
-    fwd_kernel<D, F8><<<grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, to, prm);
+    fwd_kernel<D, F8, MI><<<grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, to, prm);
   }
   count_launches(prm.order ? 2 : 1);  // [LPT order] + main kernel
   return cudaGetLastError();
@@ -825,7 +870,7 @@ static cudaError_t launch_fwd_persistent(const fm_problem& P, const void* q, con
                                          const int32_t* lts, const int32_t* lte, const int32_t* uts,
                                          const int32_t* ute, const int32_t* q_off, const int32_t* q_queue, void* o,
                                          float* lse, void* ws, cudaStream_t s, int* err, bool fp8, float q_scale,
-                                         float k_scale, float v_scale, bool per_head = false) {
+                                         float k_scale, float v_scale, bool per_head = false, int M = 1) {
   const int nQ = (P.N + kTile - 1) / kTile;
   const int G = P.H_q / P.H_kv;
   const int PG = (G + 1) / 2;
@@ -834,8 +879,9 @@ static cudaError_t launch_fwd_persistent(const fm_problem& P, const void* q, con
   const long long rows = per_head ? (long long)P.B * P.H_q * nQ : (long long)P.B * nQ;  // queue rows
   if (units > INT_MAX) return cudaErrorInvalidConfiguration;
   // unit order: longest queue first, or natural order for long passes
-  // (units that run together then share K / V tiles in L2)
-  const bool natural = use_natural_order(units);
+  // (units that run together then share K / V tiles in L2); multi-interval
+  // masks: natural order (a unit's length sums M queues)
+  const bool natural = M > 1 || use_natural_order(units);
   int32_t* order = natural ? nullptr : static_cast<int32_t*>(ws);
   int* next_unit = reinterpret_cast<int*>(static_cast<char*>(ws) + order_bytes(rows));
   {
@@ -879,12 +925,17 @@ static cudaError_t launch_fwd_persistent(const fm_problem& P, const void* q, con
   prm.causal = P.causal ? 1 : 0;
   prm.units = (int)units;
   prm.per_head = per_head ? 1 : 0;
+  prm.M = M;
   prm.scale_log2 = P.scale * q_scale * k_scale * 1.4426950408889634f;
   prm.o_scale = v_scale;
   prm.err = err;
   // persistent: one CTA per SM (the kernel's shared memory and TMEM fill an SM)
   const unsigned grid = (unsigned)std::min<long long>(units, (long long)sm_count());
   if (fp8) return launch_fwd_d<128, true>(P, tq, tk, tv, to, prm, grid, s);
+  if (M > 1) {
+    if (P.d == 128) return launch_fwd_d<128, false, true>(P, tq, tk, tv, to, prm, grid, s);
+    return launch_fwd_d<64, false, true>(P, tq, tk, tv, to, prm, grid, s);
+  }
   if (P.d == 128) return launch_fwd_d<128, false>(P, tq, tk, tv, to, prm, grid, s);
   return launch_fwd_d<64, false>(P, tq, tk, tv, to, prm, grid, s);
 }
@@ -903,6 +954,15 @@ cudaError_t launch_fwd_heads(const fm_problem& P, const void* q, const void* k, 
   if (P.d == 256) return launch_fwd256(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err, true);
   return launch_fwd_persistent(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err, false, 1.f, 1.f,
                                1.f, true);
+}
+
+cudaError_t launch_fwd_multi(const fm_problem& P, int M, const void* q, const void* k, const void* v,
+                             const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
+                             const int32_t* q_off, const int32_t* q_queue, void* o, float* lse, void* ws,
+                             cudaStream_t s, int* err) {
+  if (P.d == 256) return launch_fwd256(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err, false, M);
+  return launch_fwd_persistent(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err, false, 1.f, 1.f,
+                               1.f, false, M);
 }
 
 cudaError_t launch_fwd_fp8(const fm_problem& P, const void* q, const void* k, const void* v, float q_scale,

@@ -92,14 +92,28 @@ struct Fwd256Params {
   float* lse;
   int B, H_q, H_kv, N, Nk, nQ, nK, G, causal;
   int per_head;  // vectors (B, H_q, N_kv), one queue per (b, h, qb) row
+  // multi-interval masks: M sets of vectors (M, B, N_kv), queues over the
+  // M * B vector rows, walked one after the other (1 otherwise)
+  int M;
   float scale_log2;
   int* err;
 };
 
-__device__ __forceinline__ bool partial256(const Fwd256Params& p, int e) {
-  return (e & 1) || ((e >> 1) == p.nK - 1 && (p.Nk & 127));
+// queue entry: (kb << 1) | partial, the interval of a multi-interval mask in
+// bits 24-25 (kb < 2^23)
+template <bool MI>
+__device__ __forceinline__ int kb256(int e) {
+  if constexpr (MI) return (e >> 1) & ((1 << 23) - 1);
+  else return e >> 1;
 }
 
+template <bool MI>
+__device__ __forceinline__ bool partial256(const Fwd256Params& p, int e) {
+  return (e & 1) || (kb256<MI>(e) == p.nK - 1 && (p.Nk & 127));
+}
+
+// MI: multi-interval masks (the CTA walks p.M queues, entries tagged).
+template <bool MI>
 __global__ void __launch_bounds__(256, 1)
     fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -140,9 +154,28 @@ __global__ void __launch_bounds__(256, 1)
   }
   const int g = h / p.G;
   const int qbeg = p.q_off[row];
-  const int n = p.q_off[row + 1] - qbeg;
+  int n = p.q_off[row + 1] - qbeg;
   const int bh = b * p.H_q + h;
   const size_t vbase = (size_t)(p.per_head ? bh : b) * p.Nk;
+  // multi-interval masks: this Q block's M queues back to back
+  int segq[4] = {qbeg, 0, 0, 0}, segc[5] = {0, n, n, n, n};
+  if constexpr (MI) {
+    for (int mi = 1; mi < p.M; ++mi) {
+      const int r = (mi * p.B + b) * p.nQ + qb;
+      segq[mi] = p.q_off[r];
+      segc[mi + 1] = segc[mi] + (p.q_off[r + 1] - segq[mi]);
+    }
+    n = segc[p.M];
+  }
+  // entry j of the unit's queue (tagged with its interval) and the row of its
+  // mask vectors
+  auto qentry = [&](int j) -> int {
+    if constexpr (!MI) return p.q_queue[qbeg + j];
+    int mi = 0;
+    while (mi + 1 < p.M && j >= segc[mi + 1]) ++mi;
+    return p.q_queue[segq[mi] + j - segc[mi]] | (mi << 24);
+  };
+  auto vrow_base = [&](int e) -> size_t { return MI ? (size_t)((e >> 24) * p.B + b) * p.Nk : vbase; };
 
   if (threadIdx.x == 0) {
     *abort_flag = timeout_pending(p.err) ? 1 : 0;
@@ -186,8 +219,9 @@ __global__ void __launch_bounds__(256, 1)
         tma_load_3d(smem + C::Q_OFF + x * 16384, &tq, &bars[C::B_QFULL], x * 64, qb * 128, bh);
     }
     for (int j = 0; j < n && ok; ++j) {
-      const int e = p.q_queue[qbeg + j];
-      const int kb = e >> 1;
+      const int e = qentry(j);
+      const int kb = kb256<MI>(e);
+      const size_t vb = vrow_base(e);
       if (kb < 0 || kb >= p.nK) {
         if (lane == 0) record_error(p.err, FM_DEV_ERR_QUEUE);
         *abort_flag = 1;
@@ -204,7 +238,7 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       ok = __shfl_sync(kFull256, ok, 0);
-      if (!ok || !partial256(p, e)) continue;
+      if (!ok || !partial256<MI>(p, e)) continue;
       // the block's four mask vectors, raw (LTS, LTE, UTS, UTE x 128); the
       // softmax warps clamp them to their 32-row windows
       const int ms = pidx & 1;
@@ -212,7 +246,7 @@ __global__ void __launch_bounds__(256, 1)
       if (!ok) break;
       uint8_t* sm = smem + C::M_OFF + ms * C::M_BYTES;
       const int c0 = kb * 128;
-      const size_t o = vbase + c0;
+      const size_t o = vb + c0;
       const bool aligned = ((reinterpret_cast<uintptr_t>(p.lts + o) | reinterpret_cast<uintptr_t>(p.lte + o) |
                              reinterpret_cast<uintptr_t>(p.uts + o) | reinterpret_cast<uintptr_t>(p.ute + o)) &
                             15u) == 0;
@@ -230,10 +264,10 @@ __global__ void __launch_bounds__(256, 1)
         for (int c = lane; c < 128; c += 32) {
           const int col = c0 + c;
           const bool in = col < p.Nk;  // a key beyond Nk is masked for every row
-          vv[c] = in ? p.lts[vbase + col] : 0;
-          vv[128 + c] = in ? p.lte[vbase + col] : p.N;
-          vv[256 + c] = in ? p.uts[vbase + col] : 0;
-          vv[384 + c] = in ? p.ute[vbase + col] : 0;
+          vv[c] = in ? p.lts[vb + col] : 0;
+          vv[128 + c] = in ? p.lte[vb + col] : p.N;
+          vv[256 + c] = in ? p.uts[vb + col] : 0;
+          vv[384 + c] = in ? p.ute[vb + col] : 0;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[C::B_MFULL + ms]);
@@ -245,7 +279,7 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) {
       bool ok = true;
       for (int j = 0; j < n && ok; ++j) {
-        const int kb = p.q_queue[qbeg + j] >> 1;
+        const int kb = kb256<MI>(qentry(j));
         if (kb < 0 || kb >= p.nK) break;  // flagged by the K producer
         // 32 keys at a time (all four 64-column boxes), each quarter as soon
         // as PV(j-1) has read it
@@ -324,9 +358,9 @@ __global__ void __launch_bounds__(256, 1)
     uint32_t pidx = 0;
     bool ok = true;
     for (int j = 0; j < n && ok; ++j) {
-      const int e = p.q_queue[qbeg + j];
-      const int kb = e >> 1;
-      const bool part = partial256(p, e);
+      const int e = qentry(j);
+      const int kb = kb256<MI>(e);
+      const bool part = partial256<MI>(p, e);
       // partial block: masked-row bits of this thread's row over the 128 key
       // columns (lane c builds column 32k + c over the warp's 32 rows, then a
       // bit transpose hands each lane its own row)
@@ -497,14 +531,14 @@ __global__ void __launch_bounds__(256, 1)
 cudaError_t launch_fwd256(const fm_problem& P, const void* q, const void* k, const void* v, const int32_t* lts,
                           const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
                           const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err,
-                          bool per_head) {
+                          bool per_head, int M) {
   using C = F256;
   const int nQ = (P.N + kTile - 1) / kTile;
   const int Nk = kv_rows(P);
   const long long grid = (long long)P.B * nQ * P.H_q;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
   // longest queue first for passes of a few waves, natural order for long ones
-  const bool natural = use_natural_order(grid);
+  const bool natural = M > 1 || use_natural_order(grid);
   int32_t* order = natural ? nullptr : static_cast<int32_t*>(ws);
   if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, per_head ? P.B * P.H_q * nQ : P.B * nQ, order);
   CUtensorMap tq, tk, tv, to;
@@ -531,17 +565,23 @@ cudaError_t launch_fwd256(const fm_problem& P, const void* q, const void* k, con
   prm.G = P.H_q / P.H_kv;
   prm.causal = P.causal ? 1 : 0;
   prm.per_head = per_head ? 1 : 0;
+  prm.M = M;
   prm.scale_log2 = P.scale * 1.4426950408889634f;
   prm.err = err;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(fwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  static bool attr_done[2] = {false, false};
+  const bool mi = M > 1;
+  if (!attr_done[mi]) {
+    cudaError_t e = cudaFuncSetAttribute(mi ? fwd256_kernel<true> : fwd256_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_done[mi] = true;
   }
   {
     KernelTimer timer(s, kTimedFwd);
-    fwd256_kernel<<<(unsigned)grid, 256, C::SMEM_ALLOC, s>>>(tq, tk, tv, to, prm);
+    if (mi)
+      fwd256_kernel<true><<<(unsigned)grid, 256, C::SMEM_ALLOC, s>>>(tq, tk, tv, to, prm);
+    else
+      fwd256_kernel<false><<<(unsigned)grid, 256, C::SMEM_ALLOC, s>>>(tq, tk, tv, to, prm);
   }
   count_launches(natural ? 1 : 2);  // [LPT order] + main kernel
   return cudaGetLastError();

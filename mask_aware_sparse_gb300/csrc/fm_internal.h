@@ -54,7 +54,13 @@ cudaError_t launch_fwd_fp8(const fm_problem& P, const void* q, const void* k, co
 cudaError_t launch_fwd256(const fm_problem& p, const void* q, const void* k, const void* v, const int32_t* lts,
                           const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
                           const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err,
-                          bool per_head = false);
+                          bool per_head = false, int M = 1);
+// Multi-interval masks: M sets of vectors (M, B, N_kv), queues over the M * B
+// vector rows; one pass accumulates every interval's blocks.
+cudaError_t launch_fwd_multi(const fm_problem& P, int M, const void* q, const void* k, const void* v,
+                             const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
+                             const int32_t* q_off, const int32_t* q_queue, void* o, float* lse, void* ws,
+                             cudaStream_t s, int* err);
 
 // The forward's fixed scratch for fm_attn_fwd_noalloc (fm_fwd.cu): device
 // address of the library-owned launch-order array of the current device, or
@@ -66,7 +72,8 @@ size_t bwd_ws_bytes(const fm_problem& p);
 cudaError_t launch_bwd(const fm_problem& p, const void* q, const void* k, const void* v, const void* o,
                        const float* lse, const void* dout, const int32_t* lts, const int32_t* lte,
                        const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
-                       void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err, bool per_head = false);
+                       void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err, bool per_head = false,
+                       int M = 1);
 
 // Main kernel of the d = 256 backward (fm_bwd256.cu); row terms, launch
 // order and dQ conversion come from launch_bwd.
@@ -74,7 +81,7 @@ cudaError_t launch_bwd256_main(const fm_problem& P, const void* q, const void* k
                                const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
                                const int32_t* k_off, const int32_t* k_queue, const int32_t* order, const float* nl,
                                const float* dsum, float* dq_acc, void* dk, void* dv, cudaStream_t s, int* err,
-                               bool per_head = false);
+                               int mode = 0, int M = 1);  // mode: 0 shared, 1 per-head, 2 multi-interval vectors
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

@@ -56,6 +56,26 @@ def main():
     q8, k8, v8 = ((x.float() / (x.float().abs().max() / 448)).to(torch.float8_e4m3fn).cuda() for x in (q, k, v))
     fm.fm_attn_fwd_fp8(q8, k8, v8, *vec, qs, q_scale=1.0, k_scale=1.0, v_scale=1.0, scale=0.01, causal=True)
     status_ok("fp8 forward")
+    # per-head and multi-interval masks (one launch over every head / interval)
+    for d in (64, 128, 256):
+        B, hq, hkv, n = 1, 4, 2, 389
+        q, k, v, do = tensors.make_qkvdo(dict(B=B, H_q=hq, H_kv=hkv, N=n, d=d))
+        qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+        per = [torch.from_numpy(np.ascontiguousarray(x.reshape(B, hq, n))).cuda()
+               for x in random_vectors(rng, B * hq, n, "general")]
+        fm.fm_attn_per_head(qd, kd, vd, *per, causal=True, scale=d ** -0.5, do=dod)
+        status_ok(f"per-head d={d}")
+        cuts = np.sort(rng.integers(0, n + 1, size=(6, B, n)), axis=0)
+        fms = torch.from_numpy(cuts[0::2].astype(np.int32)).cuda()
+        fme = torch.from_numpy((cuts[1::2] - 1).astype(np.int32)).cuda()
+        o, lse, dq, dk, dvv = fm.fm_attn_multi_interval(qd, kd, vd, fms, fme, scale=d ** -0.5, do=dod)
+        status_ok(f"multi-interval d={d}")
+        spec = {"fms": cuts[0::2].transpose(1, 0, 2), "fme": (cuts[1::2] - 1).transpose(1, 0, 2)}
+        O, L = oracle.forward(f64(q), f64(k), f64(v), spec, False, d ** -0.5)
+        assert_out(f64(o), O)
+        ref = oracle.backward(f64(q), f64(k), f64(v), f64(do), spec, False, d ** -0.5)
+        for name, a, r in zip(("dQ", "dK", "dV"), (dq, dk, dvv), ref):
+            assert_grad(f64(a), r, name)
     print("debug build clean")
 
 

@@ -282,6 +282,22 @@ def test_binding_checks_per_head_shapes(lib):
         fm.fm_attn_bwd_heads(q, k, k, q, lse, q, *per, queues(B * Hq), scale=0.1, causal=True)
 
 
+def test_multi_interval_entry_points_validate_before_any_launch(lib):
+    # 1 <= M <= 4 intervals, then the usual checks, all before any launch
+    nul = ctypes.c_void_p(0)
+    args = [nul] * 11 + [nul, ctypes.c_size_t(0), nul]
+    bargs = [nul] * 15 + [nul, ctypes.c_size_t(0), nul]
+    p = fm._problem(1, 4, 2, 256, 128, 0.1, 0)
+    for M, want in ((0, fm.FM_ERR_INVALID_ARG), (5, fm.FM_ERR_INVALID_ARG), (2, fm.FM_ERR_INVALID_ARG)):
+        assert lib.fm_attn_fwd_multi(ctypes.byref(p), M, *args) == want
+        assert lib.fm_attn_bwd_multi(ctypes.byref(p), M, *bargs) == want
+    q = fm._problem(1, 4, 2, 256, 96, 0.1, 0)
+    assert lib.fm_attn_fwd_multi(ctypes.byref(q), 2, *args) == fm.FM_ERR_UNSUPPORTED
+    e = fm._problem(0, 4, 2, 256, 128, 0.1, 0)
+    assert lib.fm_attn_fwd_multi(ctypes.byref(e), 2, *args) == fm.FM_OK
+    assert lib.fm_attn_bwd_multi(ctypes.byref(e), 9, *bargs) == fm.FM_ERR_INVALID_ARG
+
+
 def test_per_head_entry_points_validate_before_any_launch(lib):
     # the C side refuses groups of more than 64 query heads per kv head and
     # null tensors before touching a pointer; its workspace

@@ -67,11 +67,18 @@ def disjoint_intervals(rng, M, B, n_rows, n_keys):
     return cuts[0::2].astype(np.int32), (cuts[1::2] - 1).astype(np.int32)
 
 
-@pytest.mark.parametrize("M,n,nk,d,hq,hkv", [(3, 1000, 1000, 128, 4, 2), (2, 640, 1300, 64, 2, 1),
-                                             (4, 512, 512, 128, 2, 2)])
-def test_multi_interval_matches_oracle(M, n, nk, d, hq, hkv):
+@pytest.mark.parametrize("M,n,nk,d,hq,hkv,B", [
+    (3, 1000, 1000, 128, 4, 2, 2), (2, 640, 1300, 64, 2, 1, 2), (4, 512, 512, 128, 2, 2, 2),
+    (2, 700, 700, 256, 4, 2, 2), (4, 389, 389, 256, 2, 1, 2), (1, 600, 600, 128, 2, 1, 2),
+    # past the staged queues: the forward's unit ring holds 512 entries (M x nK
+    # = 4 x 133), the backward stages 1024 per KV block at d <= 128 (4 x 258)
+    # and 128 at d = 256 (4 x 36)
+    (4, 300, 17000, 64, 1, 1, 1), (4, 33000, 256, 64, 1, 1, 1), (4, 4500, 300, 256, 1, 1, 1)])
+def test_multi_interval_matches_oracle(M, n, nk, d, hq, hkv, B):
+    # one forward and one backward launch over every interval (each block
+    # masked with its own interval's vectors) against the oracle's direct
+    # evaluation of the union of the intervals
     rng = np.random.default_rng(M * 1000 + n)
-    B = 2
     fms, fme = disjoint_intervals(rng, M, B, n, nk)
     q = tensors.randn_bf16((B, hq, n, d), 40)
     k = tensors.randn_bf16((B, hkv, nk, d), 41)
