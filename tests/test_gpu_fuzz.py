@@ -117,3 +117,66 @@ def test_fuzz_draws_cover_the_space():
             cls = oracle.classify_tiles(*(x[b] for x in vec), c["causal"], 128, 128, n_rows=c["n"])
             classes |= set(np.unique(cls).tolist())
     assert classes == {0, 1, 2}
+
+
+MULTI_SEEDS = list(range(8))
+
+
+def draw_multi(seed):
+    """A random multi-interval problem: M = 2..4 disjoint inclusive visible
+    intervals per key column, piecewise constant over runs of columns (runs
+    with every interval empty, runs covering every row, random cuts)."""
+    rng = np.random.default_rng(9000 + seed)
+    d = int(rng.choice([64, 128, 256]))
+    hkv = int(rng.integers(1, 3))
+    hq = hkv * int(rng.integers(1, 5))
+    B = int(rng.integers(1, 3))
+    n = int(rng.integers(1, 700))
+    nk = n if rng.random() < 0.5 else int(rng.integers(1, 700))
+    M = int(rng.integers(2, 5))
+    fms = np.zeros((M, B, nk), np.int64)
+    fme = np.full((M, B, nk), -1, np.int64)   # empty: end < start
+    for b in range(B):
+        j = 0
+        while j < nk:
+            r = int(min(nk - j, rng.integers(1, 300)))
+            kind = int(rng.integers(0, 3))
+            if kind == 1:      # one interval covers every row
+                fms[0, b, j:j + r], fme[0, b, j:j + r] = 0, n - 1
+            elif kind == 2:    # M random disjoint intervals
+                cuts = np.sort(rng.integers(0, n + 1, size=2 * M))
+                fms[:, b, j:j + r] = cuts[0::2, None]
+                fme[:, b, j:j + r] = cuts[1::2, None] - 1
+            j += r             # kind 0: nothing visible
+    return dict(d=d, hkv=hkv, hq=hq, B=B, n=n, nk=nk, M=M, fms=fms.astype(np.int32), fme=fme.astype(np.int32))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("seed", MULTI_SEEDS)
+def test_fuzz_multi_interval_against_oracle(seed):
+    c = draw_multi(seed)
+    B, hq, hkv, n, nk, d = c["B"], c["hq"], c["hkv"], c["n"], c["nk"], c["d"]
+    q = tensors.randn_bf16((B, hq, n, d), 500 + seed)
+    k = tensors.randn_bf16((B, hkv, nk, d), 600 + seed)
+    v = tensors.randn_bf16((B, hkv, nk, d), 700 + seed)
+    do = tensors.randn_bf16((B, hq, n, d), 800 + seed)
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    scale = d ** -0.5
+    o, lse, dq, dk, dv = fm.fm_attn_multi_interval(qd, kd, vd, torch.from_numpy(c["fms"]).cuda(),
+                                                   torch.from_numpy(c["fme"]).cuda(), scale=scale, do=dod)
+    st, bits = fm.fm_device_status()
+    assert st == fm.FM_OK, bits
+    spec = {"fms": c["fms"].transpose(1, 0, 2), "fme": c["fme"].transpose(1, 0, 2)}
+    O_ref, L_ref = oracle.forward(f64(q), f64(k), f64(v), spec, False, scale)
+    assert_out(f64(o), O_ref)
+    assert_lse(f64(lse), L_ref)
+    ref = oracle.backward(f64(q), f64(k), f64(v), f64(do), spec, False, scale)
+    for name, a, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert_grad(f64(a), r, name)
+
+
+def test_fuzz_multi_draws_cover_the_space():
+    draws = [draw_multi(s) for s in MULTI_SEEDS]
+    assert {c["M"] for c in draws} == {2, 3, 4}
+    assert {c["d"] for c in draws} == {64, 128, 256}
+    assert any(c["n"] != c["nk"] for c in draws)
