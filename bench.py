@@ -532,17 +532,17 @@ def run_ours(args, cfg):
 # the counters were taken from.
 NCU_TRAFFIC = {
     ("bwd", 128): {"file": "fm_bwd.cu", "workload": "share_question32k",
-                   "sha256": "7ff3cb40b92e8b22dd88c7fed4fef9f6fe8fa3a1b6ec99a1b60e1df9ed96205b",
-                   "bytes": 822768640 + 450838784, "tensor_pipe_pct": 58.6},
+                   "sha256": "8e494da0d0f8e6a44fcd0cf2d279a31951fc55cb2b3696db8ff6aada0824af80",
+                   "bytes": 825414144 + 449231616, "tensor_pipe_pct": 58.7},
     ("fwd", 128): {"file": "fm_fwd.cu", "workload": "share_question32k",
-                   "sha256": "9033b1bc53179d8fe5edf72a09563eeb494eeb8a3e0fff4cdbbeb91de360bbe4",
-                   "bytes": 264743424 + 217453312, "tensor_pipe_pct": 49.4},
+                   "sha256": "4611cdda1eb121186f2c2ca3ccf76d3d517f9dffd38560b62bf9b42ac2992f94",
+                   "bytes": 266287872 + 217428224, "tensor_pipe_pct": 48.9},
     ("bwd", 256): {"file": "fm_bwd256.cu", "workload": "share_question32k",
-                   "sha256": "70351404ba35dc7671e143ecfa9c56e39e8a83407acaa646756670ca0a29f2b4",
-                   "bytes": 2569365760 + 1446258944, "tensor_pipe_pct": 42.3},
+                   "sha256": "971bbe54779f61bf4c61cee8831882c1d85f9b5e4221b6b431fe3f6fd014c241",
+                   "bytes": 2565421312 + 1441220352, "tensor_pipe_pct": 42.3},
     ("fwd", 256): {"file": "fm_fwd256.cu", "workload": "share_question32k",
-                   "sha256": "5e321b391679ab32f293ec6b9950b7e4f62b423a76b51f2ce019fcee09da0f6e",
-                   "bytes": 527683072 + 484918528, "tensor_pipe_pct": 48.5},
+                   "sha256": "3c42dfd84385a921d86b6827f7d3355ff4cc84ad2f7ab9d85c34a378fbd7e3f3",
+                   "bytes": 527602432 + 485378560, "tensor_pipe_pct": 48.5},
 }
 
 
