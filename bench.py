@@ -665,9 +665,10 @@ def run_compose(args, cfg):
     vectors (fm_attn_per_head: one classification over the B * H_q vector
     rows, one forward and one backward launch over every head); `multi_interval` writes each key column's visible
     rows [j, LTS_j) as two inclusive intervals split at their midpoint
-    (fm_attn_multi_interval: per interval classify + forward, the log-sum-exp
-    merge, per interval backward, the sums). The latter needs a causal mask
-    with LTE = N and no upper interval."""
+    (fm_attn_multi_interval: the converter and one classification over the
+    2 x B interval rows, one forward and one backward launch over both
+    intervals). The latter needs a causal mask with LTE = N and no upper
+    interval."""
     if not torch.cuda.is_available():
         print(json.dumps({"error": "no CUDA device"}))
         return 1
