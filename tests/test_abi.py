@@ -282,6 +282,41 @@ def test_binding_checks_per_head_shapes(lib):
         fm.fm_attn_bwd_heads(q, k, k, q, lse, q, *per, queues(B * Hq), scale=0.1, causal=True)
 
 
+def test_binding_checks_multi_interval_shapes(lib):
+    # multi-interval entry points: vectors are (M, B, N_kv), the queues have
+    # M * B rows per Q (K) block; anything else is refused before any pointer
+    # reaches the library
+    import torch
+
+    bf, i32 = torch.bfloat16, torch.int32
+    M, B, Hq, Hkv, N, d = 3, 2, 4, 2, 256, 64
+    q = torch.zeros(B, Hq, N, d, dtype=bf)
+    k = torch.zeros(B, Hkv, N, d, dtype=bf)
+    lse = torch.zeros(B, Hq, N, dtype=torch.float32)
+    shared = [torch.zeros(B, N, dtype=i32) for _ in range(4)]
+    multi = [torch.zeros(M, B, N, dtype=i32) for _ in range(4)]
+    nq = N // 128
+
+    def queues(rows):
+        return fm.TileQueues(torch.zeros(rows, nq, nq, dtype=torch.uint8), torch.zeros(rows * nq + 1, dtype=i32),
+                             torch.zeros(rows * nq * nq, dtype=i32), torch.zeros(rows * nq + 1, dtype=i32),
+                             torch.zeros(rows * nq * nq, dtype=i32), 128, 128)
+
+    with pytest.raises(ValueError, match=r"\(M, B, N_kv\)"):
+        fm.fm_attn_fwd_multi(q, k, k, *shared, queues(M * B), scale=0.1, causal=False)
+    with pytest.raises(ValueError, match="queue offsets"):
+        fm.fm_attn_fwd_multi(q, k, k, *multi, queues(B), scale=0.1, causal=False)
+    with pytest.raises(ValueError, match="queue offsets"):
+        fm.fm_attn_bwd_multi(q, k, k, q, lse, q, *multi, queues(B), scale=0.1, causal=False)
+    with pytest.raises(ValueError, match="shape"):
+        fm.fm_attn_bwd_multi(q, k, k, q, lse, q, multi[0], multi[1], multi[2], multi[3][:2], queues(M * B),
+                             scale=0.1, causal=False)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.fm_attn_fwd_multi(q, k, k, *multi, queues(M * B), scale=0.1, causal=False)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fm.fm_attn_bwd_multi(q, k, k, q, lse, q, *multi, queues(M * B), scale=0.1, causal=False)
+
+
 def test_multi_interval_entry_points_validate_before_any_launch(lib):
     # 1 <= M <= 4 intervals, then the usual checks, all before any launch
     nul = ctypes.c_void_p(0)
