@@ -34,7 +34,9 @@
 extern "C" {
 #endif
 
-#define FM_ABI_VERSION 2
+/* 3: adds the per-head (fm_attn_*_heads) and multi-interval (fm_attn_*_multi)
+ * entry points; the earlier ones are unchanged. */
+#define FM_ABI_VERSION 3
 
 typedef enum fm_status {
   FM_OK = 0,

@@ -33,7 +33,7 @@ def test_header_symbols_exported(lib):
 
 
 def test_abi_version(lib):
-    assert lib.fm_abi_version() == 2
+    assert lib.fm_abi_version() == 3
 
 
 def test_status_strings(lib):
