@@ -47,6 +47,11 @@
 // The dS^T buffer of unit u (128 KV rows x 64 query columns, bf16, 128-byte
 // swizzle, two buffers) serves both as the K-major A operand of dK and the
 // MN-major B operand of dQ^T.
+// Mask forms (the MODE instantiations): shared vectors, one queue per KV
+// block walked for every head of the group; per-head vectors, each head's own
+// queue; multi-interval masks, each interval's queue walked for every head,
+// the compute warps reloading their key column's intervals when the head /
+// interval changes. dK, dV and dQ accumulate over all of them.
 #include <climits>
 #include <cmath>
 #include <cuda.h>

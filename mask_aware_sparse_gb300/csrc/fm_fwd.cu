@@ -42,6 +42,10 @@
 //     from the queue offsets) for passes of a few waves, natural order for
 //     long passes, where units of neighbouring query blocks share K / V tiles
 //     in L2.
+//   * Other mask forms: with per-head vectors a unit is one head with its own
+//     queue and vector row; with multi-interval masks (the MI instantiation)
+//     a unit walks its Q block's M interval queues one after the other, each
+//     block masked with its own interval's vectors, in one online softmax.
 #include <algorithm>
 #include <climits>
 #include <cmath>
