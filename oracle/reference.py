@@ -86,7 +86,10 @@ def _mask_rows(vec, causal, b, rows, h=0):
         lts, lte, uts, ute = (x[b, h] for x in vec["heads"])
         return masked_rows(lts, lte, uts, ute, causal, rows)
     if isinstance(vec, dict):
-        return multi_masked_rows(vec["fms"][b], vec["fme"][b], rows)
+        m = multi_masked_rows(vec["fms"][b], vec["fme"][b], rows)
+        if causal:  # the causal term masks i < j on top of every mask form
+            m = m | (np.asarray(rows, dtype=np.int64)[:, None] < np.arange(m.shape[1], dtype=np.int64)[None, :])
+        return m
     lts, lte, uts, ute = (x[b] for x in vec)
     return masked_rows(lts, lte, uts, ute, causal, rows)
 

@@ -8,6 +8,7 @@ import os
 import numpy as np
 
 import oracle
+from oracle import reference
 from workloads import masks
 
 from test_oracle import GOLDEN, _read_golden
@@ -69,6 +70,22 @@ def test_multi_interval_mask_brute_force():
     # one interval is the single-interval form
     one = oracle.multi_masked_rows(fms[:1], fme[:1], np.arange(n))
     assert np.array_equal(one, oracle.dense_mask(*oracle.from_fms_fme(fms[0], fme[0], n), False))
+
+
+def test_multi_interval_mask_with_causal_brute_force():
+    # the causal term (i < j masked) applies on top of the visible intervals,
+    # as it does on top of the four-vector form
+    rng = np.random.default_rng(2)
+    n, M = 19, 3
+    fms = rng.integers(-2, n + 2, size=(1, M, n))
+    fme = rng.integers(-2, n + 2, size=(1, M, n))
+    got = reference._mask_rows({"fms": fms, "fme": fme}, True, 0, np.arange(n))
+    for i in range(n):
+        for j in range(n):
+            vis = any(fms[0, m, j] <= i <= fme[0, m, j] for m in range(M)) and i >= j
+            assert got[i, j] == (not vis)
+    assert np.array_equal(reference._mask_rows({"fms": fms, "fme": fme}, False, 0, np.arange(n)),
+                          oracle.multi_masked_rows(fms[0], fme[0], np.arange(n)))
 
 
 def test_multi_interval_attention_is_the_lse_merge_of_its_parts():
