@@ -532,11 +532,11 @@ def run_ours(args, cfg):
 # the counters were taken from.
 NCU_TRAFFIC = {
     ("bwd", 128): {"file": "fm_bwd.cu", "workload": "share_question32k",
-                   "sha256": "8e494da0d0f8e6a44fcd0cf2d279a31951fc55cb2b3696db8ff6aada0824af80",
-                   "bytes": 825414144 + 449231616, "tensor_pipe_pct": 58.7},
+                   "sha256": "73245c210bd0be54b1ace45439f6d6e243adf8dcc7f7d1095ed9df9c8fa7e19f",
+                   "bytes": 821163008 + 450144000, "tensor_pipe_pct": 58.7},
     ("fwd", 128): {"file": "fm_fwd.cu", "workload": "share_question32k",
-                   "sha256": "4611cdda1eb121186f2c2ca3ccf76d3d517f9dffd38560b62bf9b42ac2992f94",
-                   "bytes": 266287872 + 217428224, "tensor_pipe_pct": 48.9},
+                   "sha256": "b9f0d800527407413cbca25c62e7cd789816e698eb14a174cdc81fe0b1b38f6e",
+                   "bytes": 264724224 + 217171456, "tensor_pipe_pct": 48.5},
     ("bwd", 256): {"file": "fm_bwd256.cu", "workload": "share_question32k",
                    "sha256": "971bbe54779f61bf4c61cee8831882c1d85f9b5e4221b6b431fe3f6fd014c241",
                    "bytes": 2565421312 + 1441220352, "tensor_pipe_pct": 42.3},
