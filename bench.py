@@ -663,7 +663,11 @@ def run_compose(args, cfg):
     workload's own mask written in that form (so the work and the metric are
     the workload's): `per_head` gives every query head its own copy of the
     vectors (fm_attn_per_head: one classification over the B * H_q vector
-    rows, one forward and one backward launch over every head); `multi_interval` writes each key column's visible
+    rows, one forward and one backward launch over every head);
+    `per_head_distinct` (share-question only) lets every query head pack its
+    own eight samples (lengths drawn per head from seed 1000 + h), so the
+    heads' masks and queues differ, and counts each head's own unmasked pairs;
+    `multi_interval` writes each key column's visible
     rows [j, LTS_j) as two inclusive intervals split at their midpoint
     (fm_attn_multi_interval: the converter and one classification over the
     2 x B interval rows, one forward and one backward launch over both
@@ -682,9 +686,26 @@ def run_compose(args, cfg):
     names = ("lts", "lte", "uts", "ute")
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     c = cfg
+    work = workload_flops(cfg)
     if args.compose == "per_head":
         vec = [torch.from_numpy(np.ascontiguousarray(np.repeat(cfg[n][:, None], cfg["H_q"], axis=1))).to(dev)
                for n in names]
+
+        def step():
+            fm.fm_attn_per_head(q, k, v, *vec, causal=c["causal"], scale=c["scale"], do=do)
+    elif args.compose == "per_head_distinct":
+        if "samples" not in cfg or cfg["B"] != 1:
+            print(json.dumps({"error": "per_head_distinct needs the share-question workload (B = 1)"}))
+            return 1
+        from workloads import masks as wmasks
+
+        per = [tuple(np.asarray(x, np.int32) for x in
+                     wmasks.share_question(wmasks.draw_share_question(np.random.default_rng(1000 + h)), cfg["N"]))
+               for h in range(cfg["H_q"])]
+        vec = [torch.from_numpy(np.ascontiguousarray(np.stack([p[i] for p in per])[None])).to(dev) for i in range(4)]
+        pairs = sum(visible_pairs(*p, cfg["causal"]) for p in per)   # summed over the heads
+        d = cfg["d"]
+        work = dict(pairs=pairs, fwd=pairs * 4 * d, bwd=pairs * 10 * d)
 
         def step():
             fm.fm_attn_per_head(q, k, v, *vec, causal=c["causal"], scale=c["scale"], do=do)
@@ -717,7 +738,6 @@ def run_compose(args, cfg):
     t = _time_steps(step, args.steps, flush)
     t1 = time.time()
     sampler.stop()
-    work = workload_flops(cfg)
     value = (work["fwd"] + work["bwd"]) / t / 1e12
     peaks, src = read_peaks()
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
@@ -854,7 +874,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--balance", action="store_true", help="measure the chunk balancer instead")
     ap.add_argument("--fp8", action="store_true", help="measure the FP8 forward instead")
-    ap.add_argument("--compose", choices=("per_head", "multi_interval"), default=None,
+    ap.add_argument("--compose", choices=("per_head", "per_head_distinct", "multi_interval"), default=None,
                     help="measure a mask-form composition of the binding instead")
     args = ap.parse_args()
     if args.balance:
