@@ -16,8 +16,9 @@
  *     contiguous (B, H_kv, N_kv, d) bf16 (N_kv = N unless fm_problem says
  *     otherwise); LSE is (B, H_q, N) fp32; the four mask vectors are (B, N_kv)
  *     int32, one entry per key column, shared by every head (the *_heads entry
- *     points take one set per query head, (B, H_q, N_kv)), holding query-row
- *     boundaries in [0, N]. Tensor base addresses must be 16-byte aligned.
+ *     points take one set per query head, (B, H_q, N_kv), the *_multi ones one
+ *     set per interval, (M, B, N_kv)), holding query-row boundaries in [0, N].
+ *     Tensor base addresses must be 16-byte aligned.
  *   - GQA: query head h reads kv head h / (H_q / H_kv) (contiguous groups).
  *   - Errors: arguments are validated on the host and a bad call returns an
  *     error status without launching anything. Problems found on the device
