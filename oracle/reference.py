@@ -171,6 +171,22 @@ def classify_tiles(lts, lte, uts, ute, causal: bool, bm: int, bn: int, n_rows=No
     return cls
 
 
+def classify_tiles_multi(fms, fme, causal: bool, bm: int, bn: int, n_rows: int) -> np.ndarray:
+    """Tile classes of a multi-interval mask for one batch entry (fms, fme:
+    (M, N_kv), key j visible to rows FMS^(m)_j <= i <= FME^(m)_j for some m,
+    plus i >= j when causal): the most visible of the intervals' own classes,
+    each from `classify_tiles` on the interval's masked complement
+    (`from_fms_fme`) with the causal term. A tile is skipped iff every
+    interval skips it (no interval reaches it), unmasked iff one interval
+    alone leaves it unmasked, partial otherwise (class codes 0 < 1 < 2, so
+    the most visible is the maximum)."""
+    fms = np.asarray(fms)
+    fme = np.asarray(fme)
+    cls = [classify_tiles(*from_fms_fme(fms[m], fme[m], n_rows), causal, bm, bn, n_rows=n_rows)
+           for m in range(fms.shape[0])]
+    return np.maximum.reduce(cls)
+
+
 def build_queues(cls_batches):
     """Compacted queues in CSR form from a list of per-batch (nQ, nK) class tables.
 

@@ -6,6 +6,7 @@ converted vectors mask exactly the rows outside [FMS_j, FME_j]."""
 import os
 
 import numpy as np
+import pytest
 
 import oracle
 from oracle import reference
@@ -86,6 +87,35 @@ def test_multi_interval_mask_with_causal_brute_force():
             assert got[i, j] == (not vis)
     assert np.array_equal(reference._mask_rows({"fms": fms, "fme": fme}, False, 0, np.arange(n)),
                           oracle.multi_masked_rows(fms[0], fme[0], np.arange(n)))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_multi_interval_tile_rule_is_sound_and_exact_at_1x1(causal):
+    # the union rule (the most visible per-interval class) against the dense
+    # multi-interval mask: skip => every element masked, unmasked => every
+    # element visible, on overlapping and empty random intervals; at 1 x 1
+    # tiles each interval's rule is exact, so the union's is too
+    rng = np.random.default_rng(11 + causal)
+    for n, nk, M, bm, bn in ((24, 24, 3, 4, 4), (20, 28, 2, 8, 4), (16, 16, 4, 1, 1), (9, 13, 2, 1, 1)):
+        fms = rng.integers(-2, n + 2, size=(1, M, nk))
+        fme = rng.integers(-2, n + 2, size=(1, M, nk))
+        cls = oracle.classify_tiles_multi(fms[0], fme[0], causal, bm, bn, n)
+        dense = reference._mask_rows({"fms": fms, "fme": fme}, causal, 0, np.arange(n))
+        for qb in range(cls.shape[0]):
+            for kb in range(cls.shape[1]):
+                t = dense[qb * bm:(qb + 1) * bm, kb * bn:(kb + 1) * bn]
+                if cls[qb, kb] == 0:
+                    assert t.all()
+                elif cls[qb, kb] == 2:
+                    assert not t.any()
+                elif bm == 1 and bn == 1:
+                    raise AssertionError("a 1 x 1 tile is never partial")
+    # one interval is the single-interval rule on its complement
+    fms = rng.integers(0, 30, size=(1, 30))
+    fme = rng.integers(0, 30, size=(1, 30))
+    one = oracle.classify_tiles_multi(fms, fme, causal, 8, 8, 30)
+    assert np.array_equal(one, oracle.classify_tiles(*oracle.from_fms_fme(fms[0], fme[0], 30), causal, 8, 8,
+                                                      n_rows=30))
 
 
 def test_multi_interval_attention_is_the_lse_merge_of_its_parts():
