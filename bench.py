@@ -678,9 +678,8 @@ def run_compose(args, cfg):
     heads' masks and queues differ, and counts each head's own unmasked pairs;
     `multi_interval` writes each key column's visible
     rows [j, LTS_j) as two inclusive intervals split at their midpoint
-    (fm_attn_multi_interval: the converter and one classification over the
-    2 x B interval rows, one forward and one backward launch over both
-    intervals). The latter needs a causal mask with LTE = N and no upper
+    (fm_attn_multi_interval: one classification of the intervals' union,
+    one forward and one backward launch). The latter needs a causal mask with LTE = N and no upper
     interval."""
     if not torch.cuda.is_available():
         print(json.dumps({"error": "no CUDA device"}))

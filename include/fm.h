@@ -16,8 +16,8 @@
  *     contiguous (B, H_kv, N_kv, d) bf16 (N_kv = N unless fm_problem says
  *     otherwise); LSE is (B, H_q, N) fp32; the four mask vectors are (B, N_kv)
  *     int32, one entry per key column, shared by every head (the *_heads entry
- *     points take one set per query head, (B, H_q, N_kv), the *_multi ones one
- *     set per interval, (M, B, N_kv)), holding query-row boundaries in [0, N].
+ *     points take one set per query head, (B, H_q, N_kv); the *_multi ones
+ *     take visible intervals instead), holding query-row boundaries in [0, N].
  *     Tensor base addresses must be 16-byte aligned.
  *   - GQA: query head h reads kv head h / (H_q / H_kv) (contiguous groups).
  *   - Errors: arguments are validated on the host and a bad call returns an
@@ -213,33 +213,37 @@ fm_status fm_attn_bwd_heads(const fm_problem* p, const void* q, const void* k, c
 
 /* ---------------------------------------------------------------------------
  * Multi-interval masks (the FlashMask Guide, "The Solution: FlashMask Sparse
- * Mask Representation": up to four visible intervals [FMS_m,j, FME_m,j] per key
- * column, disjoint within a column). Each interval m has its own four
- * vectors, its masked complement (fm_from_fms_fme over the M * B rows of the
- * (M, B, N_kv) FMS / FME arrays gives them), lts..ute (M, B, N_kv) int32. The
- * keys a query row sees through different intervals are disjoint, so the
- * attention over their union is one online softmax over the blocks of every
- * interval's queue, each block masked with its own interval's vectors, and
- * the gradients are the sums of the per-interval contributions: one forward
- * and one backward launch accumulate them all (no per-interval passes, no
- * merge). Everything else is fm_attn_fwd / fm_attn_bwd, except:
- *   - the queues come from fm_classify_tiles run on the vectors as M * B rows
- *     (an fm_problem with B' = M * B), row (m * B + b) holding interval m's
- *     tiles of batch entry b; a block reached by several intervals is computed
- *     once per interval;
- *   - 1 <= M <= 4 (FM_ERR_INVALID_ARG otherwise); M = 1 is fm_attn_fwd /
- *     fm_attn_bwd.
- * Workspaces: fm_attn_fwd_workspace_bytes and fm_attn_bwd_workspace_bytes.
+ * Mask Representation": up to four visible intervals per key column). Key
+ * column j is visible to query row i iff FMS_m,j <= i <= FME_m,j for some
+ * interval m (inclusive bounds; an interval with FMS > FME is empty;
+ * intervals may overlap), and, with causal set, i >= j. fms, fme are
+ * (M, B, N_kv) int32 device arrays, 1 <= M <= 4.
+ *
+ * fm_classify_tiles_multi gives every tile the most visible of the intervals'
+ * own classes (the rule of fm_classify_tiles on each interval's masked
+ * complement, [0, FMS) and (FME, N), with the causal term): skipped iff no
+ * interval reaches the tile, unmasked iff one interval alone covers it,
+ * partial otherwise; its outputs have the layout of fm_classify_tiles for B
+ * batch entries. Workspace: fm_classify_multi_workspace_bytes.
+ *
+ * fm_attn_fwd_multi / fm_attn_bwd_multi are fm_attn_fwd / fm_attn_bwd with
+ * these queues: each queued block is computed once, its partial tiles masked
+ * by the union of the intervals (rows outside every interval masked).
+ * Workspaces: fm_attn_fwd_workspace_bytes, fm_attn_bwd_workspace_bytes.
+ * Errors: M outside [1, 4] is FM_ERR_INVALID_ARG; the rest as fm_attn_fwd /
+ * fm_attn_bwd.
  * ------------------------------------------------------------------------- */
+size_t fm_classify_multi_workspace_bytes(const fm_problem* p, const fm_tiling* t, int32_t M);
+fm_status fm_classify_tiles_multi(const fm_problem* p, const fm_tiling* t, int32_t M, const int32_t* fms,
+                                  const int32_t* fme, uint8_t* tile_class, int32_t* q_off, int32_t* q_queue,
+                                  int32_t* k_off, int32_t* k_queue, void* ws, size_t ws_bytes, void* stream);
 fm_status fm_attn_fwd_multi(const fm_problem* p, int32_t M, const void* q, const void* k, const void* v,
-                            const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
-                            const int32_t* q_off, const int32_t* q_queue, void* o, float* lse, void* ws,
-                            size_t ws_bytes, void* stream);
+                            const int32_t* fms, const int32_t* fme, const int32_t* q_off, const int32_t* q_queue,
+                            void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
 fm_status fm_attn_bwd_multi(const fm_problem* p, int32_t M, const void* q, const void* k, const void* v,
-                            const void* o, const float* lse, const void* dout, const int32_t* lts,
-                            const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* k_off,
-                            const int32_t* k_queue, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
-                            void* stream);
+                            const void* o, const float* lse, const void* dout, const int32_t* fms,
+                            const int32_t* fme, const int32_t* k_off, const int32_t* k_queue, void* dq, void* dk,
+                            void* dv, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * One forward + backward from HOST buffers. (No counterpart in the pages: an

@@ -81,9 +81,13 @@ _SIGS = {
     "fm_attn_fwd_heads_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
     "fm_attn_fwd_heads": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 11 + [_P, ctypes.c_size_t, _P]),
     "fm_attn_bwd_heads": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 15 + [_P, ctypes.c_size_t, _P]),
-    "fm_attn_fwd_multi": (ctypes.c_int, [ctypes.POINTER(fm_problem), ctypes.c_int32] + [_P] * 11 +
+    "fm_classify_multi_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem), ctypes.POINTER(fm_tiling),
+                                                            ctypes.c_int32]),
+    "fm_classify_tiles_multi": (ctypes.c_int, [ctypes.POINTER(fm_problem), ctypes.POINTER(fm_tiling),
+                                               ctypes.c_int32] + [_P] * 7 + [_P, ctypes.c_size_t, _P]),
+    "fm_attn_fwd_multi": (ctypes.c_int, [ctypes.POINTER(fm_problem), ctypes.c_int32] + [_P] * 9 +
                           [_P, ctypes.c_size_t, _P]),
-    "fm_attn_bwd_multi": (ctypes.c_int, [ctypes.POINTER(fm_problem), ctypes.c_int32] + [_P] * 15 +
+    "fm_attn_bwd_multi": (ctypes.c_int, [ctypes.POINTER(fm_problem), ctypes.c_int32] + [_P] * 13 +
                           [_P, ctypes.c_size_t, _P]),
     "fm_attn_host_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(fm_problem)]),
     "fm_attn_fwd_bwd_host": (ctypes.c_int, [ctypes.POINTER(fm_problem)] + [_P] * 13 + [_P, ctypes.c_size_t, _P]),
@@ -195,7 +199,8 @@ def _attn_args(q, k, v, vec, queues, *, backward, o=None, lse=None, do=None, dq=
     sees any pointer (the C ABI receives bare pointers and cannot check them).
     Shape checks come first, so a mismatch is reported as such. heads: per-head
     mask vectors (B, H_q, N_kv) and queues over B * H_q rows; intervals = M > 0:
-    multi-interval vectors (M, B, N_kv) and queues over M * B rows."""
+    multi-interval FMS / FME (M, B, N_kv) (vec holds the two) and the union
+    classification's queues over B rows."""
     _need(isinstance(q, torch.Tensor) and q.dim() == 4, "q must be a (B, H_q, N, d) tensor")
     B, Hq, N, d = q.shape
     _need(isinstance(k, torch.Tensor) and k.dim() == 4 and k.shape[0] == B and k.shape[3] == d,
@@ -223,7 +228,7 @@ def _attn_args(q, k, v, vec, queues, *, backward, o=None, lse=None, do=None, dq=
     _need((queues.block_m, queues.block_n) == (bm, bn),
           f"queues were built with {queues.block_m} x {queues.block_n} tiles; the kernels need {bm} x {bn}")
     nq, nk = -(-N // bm), -(-Nk // bn)
-    R = B * Hq if heads else intervals * B if intervals else B  # queue rows per Q (K) block
+    R = B * Hq if heads else B  # queue rows per Q (K) block
     off, qu, nrows = (queues.k_off, queues.k_queue, R * nk) if backward else (queues.q_off, queues.q_queue, R * nq)
     _like(off, "queue offsets", (nrows + 1,), torch.int32)
     _need(isinstance(qu, torch.Tensor) and qu.dtype == torch.int32 and qu.is_contiguous()
@@ -473,14 +478,52 @@ def fm_sum_parts(parts, out=None, stream=None):
     return out
 
 
-def fm_attn_fwd_multi(q, k, v, lts, lte, uts, ute, queues: TileQueues, *, scale: float, causal: bool, o=None,
-                      lse=None, ws=None, stream=None):
-    """Forward with multi-interval masks: lts..ute (M, B, N_kv), one set per
-    interval, and the queues of fm_classify_tiles over their M * B rows.
-    Returns (O bf16, LSE fp32)."""
-    _need(isinstance(lts, torch.Tensor) and lts.dim() == 3, "multi-interval vectors must be (M, B, N_kv)")
-    M = lts.shape[0]
-    _attn_args(q, k, v, (lts, lte, uts, ute), queues, backward=False, o=o, lse=lse, ws=ws, intervals=M)
+def fm_classify_tiles_multi(fms, fme, *, causal: bool, n_rows=None, block_m: int = 128, block_n: int = 128,
+                            stream=None):
+    """Tile classes and queues of a multi-interval mask: fms, fme are
+    (M, B, N_kv) int32 CUDA tensors (M <= 4), key j visible to rows
+    [fms[m, b, j], fme[m, b, j]] for some m. Every tile gets the most visible
+    of the intervals' own classes; the queues have the layout of
+    fm_classify_tiles for B batch entries."""
+    _need(isinstance(fms, torch.Tensor) and fms.dim() == 3, "fms, fme must be (M, B, N_kv)")
+    M, B, Nk = fms.shape
+    for i, x in enumerate((fms, fme)):
+        _like(x, ("fms", "fme")[i], (M, B, Nk), torch.int32)
+    _same_cuda(fms=fms, fme=fme)
+    N = Nk if n_rows is None else int(n_rows)
+    prob = _problem(B, 1, 1, N, 128, 1.0, causal, Nk)
+    til = fm_tiling(block_m, block_n)
+    nq, nk = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().fm_tile_counts(ctypes.byref(prob), ctypes.byref(til), ctypes.byref(nq), ctypes.byref(nk)),
+           "fm_tile_counts")
+    nq, nk = nq.value, nk.value
+    dev = fms.device
+    cap = max(1, B * nq * nk)
+    cls = torch.empty((B, nq, nk), dtype=torch.uint8, device=dev)
+    q_off = torch.empty(B * nq + 1, dtype=torch.int32, device=dev)
+    k_off = torch.empty(B * nk + 1, dtype=torch.int32, device=dev)
+    q_queue = torch.empty(cap, dtype=torch.int32, device=dev)
+    k_queue = torch.empty(cap, dtype=torch.int32, device=dev)
+    wsb = lib().fm_classify_multi_workspace_bytes(ctypes.byref(prob), ctypes.byref(til), M)
+    ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=dev)
+    _check(lib().fm_classify_tiles_multi(ctypes.byref(prob), ctypes.byref(til), M, _ptr(fms), _ptr(fme), _ptr(cls),
+                                         _ptr(q_off), _ptr(q_queue), _ptr(k_off), _ptr(k_queue), _ptr(ws),
+                                         ctypes.c_size_t(wsb), _stream(stream)), "fm_classify_tiles_multi")
+    return TileQueues(cls, q_off, q_queue, k_off, k_queue, block_m, block_n)
+
+
+def _multi_args(fms, fme):
+    _need(isinstance(fms, torch.Tensor) and fms.dim() == 3, "multi-interval fms, fme must be (M, B, N_kv)")
+    _need(isinstance(fme, torch.Tensor) and fme.shape == fms.shape, "fms and fme must have one shape")
+    return fms.shape[0]
+
+
+def fm_attn_fwd_multi(q, k, v, fms, fme, queues: TileQueues, *, scale: float, causal: bool, o=None, lse=None,
+                      ws=None, stream=None):
+    """Forward with a multi-interval mask (fms, fme (M, B, N_kv)) and the
+    queues of fm_classify_tiles_multi. Returns (O bf16, LSE fp32)."""
+    M = _multi_args(fms, fme)
+    _attn_args(q, k, v, (fms, fme), queues, backward=False, o=o, lse=lse, ws=ws, intervals=M)
     B, Hq, N, d = q.shape
     prob = _problem(B, Hq, k.shape[1], N, d, scale, causal, k.shape[2])
     o = torch.empty_like(q) if o is None else o
@@ -488,20 +531,19 @@ def fm_attn_fwd_multi(q, k, v, lts, lte, uts, ute, queues: TileQueues, *, scale:
     wsb = lib().fm_attn_fwd_workspace_bytes(ctypes.byref(prob))
     if ws is None or ws.numel() < wsb:
         ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=q.device)
-    _check(lib().fm_attn_fwd_multi(ctypes.byref(prob), M, _ptr(q), _ptr(k), _ptr(v), _ptr(lts), _ptr(lte),
-                                   _ptr(uts), _ptr(ute), _ptr(queues.q_off), _ptr(queues.q_queue), _ptr(o),
-                                   _ptr(lse), _ptr(ws), ctypes.c_size_t(wsb), _stream(stream)), "fm_attn_fwd_multi")
+    _check(lib().fm_attn_fwd_multi(ctypes.byref(prob), M, _ptr(q), _ptr(k), _ptr(v), _ptr(fms), _ptr(fme),
+                                   _ptr(queues.q_off), _ptr(queues.q_queue), _ptr(o), _ptr(lse), _ptr(ws),
+                                   ctypes.c_size_t(wsb), _stream(stream)), "fm_attn_fwd_multi")
     return o, lse
 
 
-def fm_attn_bwd_multi(q, k, v, o, lse, do, lts, lte, uts, ute, queues: TileQueues, *, scale: float, causal: bool,
-                      dq=None, dk=None, dv=None, ws=None, stream=None):
-    """Backward with multi-interval masks (lts..ute (M, B, N_kv)): returns
+def fm_attn_bwd_multi(q, k, v, o, lse, do, fms, fme, queues: TileQueues, *, scale: float, causal: bool, dq=None,
+                      dk=None, dv=None, ws=None, stream=None):
+    """Backward with a multi-interval mask (fms, fme (M, B, N_kv)): returns
     (dQ, dK, dV) bf16."""
-    _need(isinstance(lts, torch.Tensor) and lts.dim() == 3, "multi-interval vectors must be (M, B, N_kv)")
-    M = lts.shape[0]
-    _attn_args(q, k, v, (lts, lte, uts, ute), queues, backward=True, o=o, lse=lse, do=do, dq=dq, dk=dk, dv=dv,
-               ws=ws, intervals=M)
+    M = _multi_args(fms, fme)
+    _attn_args(q, k, v, (fms, fme), queues, backward=True, o=o, lse=lse, do=do, dq=dq, dk=dk, dv=dv, ws=ws,
+               intervals=M)
     B, Hq, N, d = q.shape
     prob = _problem(B, Hq, k.shape[1], N, d, scale, causal, k.shape[2])
     dq = torch.empty_like(q) if dq is None else dq
@@ -511,30 +553,25 @@ def fm_attn_bwd_multi(q, k, v, o, lse, do, lts, lte, uts, ute, queues: TileQueue
     if ws is None or ws.numel() < wsb:
         ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=q.device)
     _check(lib().fm_attn_bwd_multi(ctypes.byref(prob), M, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
-                                   _ptr(lts), _ptr(lte), _ptr(uts), _ptr(ute), _ptr(queues.k_off),
-                                   _ptr(queues.k_queue), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
-                                   ctypes.c_size_t(wsb), _stream(stream)), "fm_attn_bwd_multi")
+                                   _ptr(fms), _ptr(fme), _ptr(queues.k_off), _ptr(queues.k_queue), _ptr(dq),
+                                   _ptr(dk), _ptr(dv), _ptr(ws), ctypes.c_size_t(wsb), _stream(stream)),
+           "fm_attn_bwd_multi")
     return dq, dk, dv
 
 
-def fm_attn_multi_interval(q, k, v, fms, fme, *, scale: float, do=None, stream=None):
-    """Attention under multi-interval masks: fms, fme are (M, B, N_kv) int32 CUDA
-    tensors (M <= 4), key j visible to rows [fms[m, b, j], fme[m, b, j]]
-    (inclusive), intervals of one column disjoint. Library calls only:
-    fm_from_fms_fme over the M * B rows (each interval's masked complement),
-    fm_classify_tiles over those rows, fm_attn_fwd_multi and, with do,
-    fm_attn_bwd_multi (one launch each over every interval).
+def fm_attn_multi_interval(q, k, v, fms, fme, *, scale: float, do=None, causal: bool = False, stream=None):
+    """Attention under a multi-interval mask: fms, fme are (M, B, N_kv) int32
+    CUDA tensors (M <= 4), key j visible to rows [fms[m, b, j], fme[m, b, j]]
+    (inclusive) for some m (intervals may overlap), and to no row before j
+    when causal. Library calls only: fm_classify_tiles_multi, then
+    fm_attn_fwd_multi and, with do, fm_attn_bwd_multi (each block computed
+    once, masked by the union of the intervals).
     Returns (o, lse) or (o, lse, dq, dk, dv)."""
-    _need(isinstance(fms, torch.Tensor) and fms.dim() == 3, "fms, fme must be (M, B, N_kv)")
-    M, B, Nk = fms.shape
-    N = q.shape[2]
-    vec = fm_from_fms_fme(fms.reshape(M * B, Nk), fme.reshape(M * B, Nk), n_rows=N, stream=stream)
-    qs = fm_classify_tiles(*vec, causal=False, n_rows=N, stream=stream)
-    vec = tuple(x.view(M, B, Nk) for x in vec)
-    o, lse = fm_attn_fwd_multi(q, k, v, *vec, qs, scale=scale, causal=False, stream=stream)
+    qs = fm_classify_tiles_multi(fms, fme, causal=causal, n_rows=q.shape[2], stream=stream)
+    o, lse = fm_attn_fwd_multi(q, k, v, fms, fme, qs, scale=scale, causal=causal, stream=stream)
     if do is None:
         return o, lse
-    dq, dk, dv = fm_attn_bwd_multi(q, k, v, o, lse, do, *vec, qs, scale=scale, causal=False, stream=stream)
+    dq, dk, dv = fm_attn_bwd_multi(q, k, v, o, lse, do, fms, fme, qs, scale=scale, causal=causal, stream=stream)
     return o, lse, dq, dk, dv
 
 

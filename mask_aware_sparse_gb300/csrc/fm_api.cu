@@ -244,6 +244,30 @@ fm_status fm_classify_tiles(const fm_problem* p, const fm_tiling* t, const int32
                                    k_off, k_queue, ws, static_cast<cudaStream_t>(stream), err));
 }
 
+size_t fm_classify_multi_workspace_bytes(const fm_problem* p, const fm_tiling* t, int32_t M) {
+  int32_t nq = 0, nk = 0;
+  if (M < 1 || M > 4 || fm_tile_counts(p, t, &nq, &nk) != FM_OK) return 0;
+  return classify_multi_ws_bytes(M, p->B, nq, nk, kv_rows(*p));
+}
+
+fm_status fm_classify_tiles_multi(const fm_problem* p, const fm_tiling* t, int32_t M, const int32_t* fms,
+                                  const int32_t* fme, uint8_t* tile_class, int32_t* q_off, int32_t* q_queue,
+                                  int32_t* k_off, int32_t* k_queue, void* ws, size_t ws_bytes, void* stream) {
+  int32_t nq = 0, nk = 0;
+  fm_status st = fm_tile_counts(p, t, &nq, &nk);
+  if (st != FM_OK) return st;
+  if (M < 1 || M > 4) return FM_ERR_INVALID_ARG;
+  if (p->B == 0 || p->N == 0) return FM_OK;
+  if (!fms || !fme || !tile_class || !q_off || !q_queue || !k_off || !k_queue) return FM_ERR_INVALID_ARG;
+  if ((int64_t)M * p->B * nq * nk > INT32_MAX || (int64_t)M * p->B * kv_rows(*p) > INT32_MAX)
+    return FM_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < classify_multi_ws_bytes(M, p->B, nq, nk, kv_rows(*p))) return FM_ERR_WORKSPACE;
+  int* err = device_error_word();
+  if (!err) return FM_ERR_CUDA;
+  return from_cuda(launch_classify_multi(*p, M, t->block_m, t->block_n, nq, nk, fms, fme, tile_class, q_off,
+                                         q_queue, k_off, k_queue, ws, static_cast<cudaStream_t>(stream), err));
+}
+
 size_t fm_attn_fwd_workspace_bytes(const fm_problem* p) {
   bool empty = false;
   if (check_problem(p, &empty) != FM_OK || empty) return 0;
@@ -319,37 +343,34 @@ fm_status fm_attn_bwd_heads(const fm_problem* p, const void* q, const void* k, c
 }
 
 fm_status fm_attn_fwd_multi(const fm_problem* p, int32_t M, const void* q, const void* k, const void* v,
-                            const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
-                            const int32_t* q_off, const int32_t* q_queue, void* o, float* lse, void* ws,
-                            size_t ws_bytes, void* stream) {
+                            const int32_t* fms, const int32_t* fme, const int32_t* q_off, const int32_t* q_queue,
+                            void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
   bool empty = false;
   fm_status st = check_problem(p, &empty);
   if (st != FM_OK) return st;
   if (M < 1 || M > 4) return FM_ERR_INVALID_ARG;
   if (empty) return FM_OK;
   if ((st = check_attn_shape(p, false)) != FM_OK) return st;
-  if (!q || !k || !v || !lts || !lte || !uts || !ute || !q_off || !q_queue || !o || !lse) return FM_ERR_INVALID_ARG;
+  if (!q || !k || !v || !fms || !fme || !q_off || !q_queue || !o || !lse) return FM_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FM_ERR_INVALID_ARG;
   if (!ws || ws_bytes < fwd_ws_bytes(*p)) return FM_ERR_WORKSPACE;
   int* err = device_error_word();
   if (!err) return FM_ERR_CUDA;
-  return from_cuda(launch_fwd_multi(*p, M, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws,
+  return from_cuda(launch_fwd_multi(*p, M, q, k, v, fms, fme, q_off, q_queue, o, lse, ws,
                                     static_cast<cudaStream_t>(stream), err));
 }
 
 fm_status fm_attn_bwd_multi(const fm_problem* p, int32_t M, const void* q, const void* k, const void* v,
-                            const void* o, const float* lse, const void* dout, const int32_t* lts,
-                            const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* k_off,
-                            const int32_t* k_queue, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
-                            void* stream) {
+                            const void* o, const float* lse, const void* dout, const int32_t* fms,
+                            const int32_t* fme, const int32_t* k_off, const int32_t* k_queue, void* dq, void* dk,
+                            void* dv, void* ws, size_t ws_bytes, void* stream) {
   bool empty = false;
   fm_status st = check_problem(p, &empty);
   if (st != FM_OK) return st;
   if (M < 1 || M > 4) return FM_ERR_INVALID_ARG;
   if (empty) return FM_OK;
   if ((st = check_attn_shape(p, true)) != FM_OK) return st;
-  if (!q || !k || !v || !o || !lse || !dout || !lts || !lte || !uts || !ute || !k_off || !k_queue || !dq || !dk ||
-      !dv)
+  if (!q || !k || !v || !o || !lse || !dout || !fms || !fme || !k_off || !k_queue || !dq || !dk || !dv)
     return FM_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv))
@@ -357,7 +378,7 @@ fm_status fm_attn_bwd_multi(const fm_problem* p, int32_t M, const void* q, const
   if (!ws || ws_bytes < bwd_ws_bytes(*p)) return FM_ERR_WORKSPACE;
   int* err = device_error_word();
   if (!err) return FM_ERR_CUDA;
-  return from_cuda(launch_bwd(*p, q, k, v, o, lse, dout, lts, lte, uts, ute, k_off, k_queue, dq, dk, dv, ws,
+  return from_cuda(launch_bwd(*p, q, k, v, o, lse, dout, fms, fme, nullptr, nullptr, k_off, k_queue, dq, dk, dv, ws,
                               static_cast<cudaStream_t>(stream), err, false, M));
 }
 

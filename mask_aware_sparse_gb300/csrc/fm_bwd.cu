@@ -167,31 +167,9 @@ __device__ __forceinline__ Unit decode_unit_ph(const BwdParams& p, int u, int g,
   return r;
 }
 
-// The same with multi-interval masks: interval m's queue for this KV block is
-// walked for every head of the group ([2 G hoff[m], 2 G hoff[m + 1]) are its
-// units: head-major within it, then the queue, then the half); the staged
-// entries are the intervals' queues back to back; m is the caller's cursor.
-__device__ __forceinline__ Unit decode_unit_multi(const BwdParams& p, int u, int g, bool force_part,
-                                                  uint32_t s_queue, int qcap, const int* hoff, int& m) {
-  while (u >= 2 * p.G * hoff[m + 1]) ++m;
-  const int Lm = hoff[m + 1] - hoff[m];
-  const int rem = u - 2 * p.G * hoff[m];
-  const int hi = rem / (2 * Lm);
-  const int r2 = rem - hi * 2 * Lm;
-  const int pos = hoff[m] + (r2 >> 1);
-  const int e = (pos < qcap) ? lds_s32(s_queue + 4 * pos) : p.k_queue[hoff[kMaxHeads + 1 + m] + (r2 >> 1)];
-  Unit r;
-  r.h = g * p.G + hi;
-  r.qb = e >> 1;
-  r.half = r2 & 1;
-  r.part = (e & 1) | (force_part ? 1 : 0);
-  r.m = m;
-  return r;
-}
-
 // MODE 0: mask vectors (B, N_kv) shared by the heads; 1: per-head vectors
-// (B, H_q, N_kv) and queues over B * H_q rows; 2: multi-interval vectors
-// (M, B, N_kv) and queues over M * B rows.
+// (B, H_q, N_kv) and queues over B * H_q rows; 2: multi-interval masks (lts /
+// lte hold FMS / FME, (M, B, N_kv); the union classification's queues).
 template <int D, int MODE>
 __global__ void __launch_bounds__(480, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -217,11 +195,6 @@ __global__ void __launch_bounds__(480, 1)
   if constexpr (PH) {
     for (int hi = 0; hi < p.G; ++hi) {
       const int r = (b * p.H_q + g * p.G + hi) * nK + kb;
-      L += p.k_off[r + 1] - p.k_off[r];
-    }
-  } else if constexpr (MI) {
-    for (int mi = 0; mi < p.M; ++mi) {
-      const int r = (mi * p.B + b) * nK + kb;
       L += p.k_off[r + 1] - p.k_off[r];
     }
   } else {
@@ -289,32 +262,14 @@ __global__ void __launch_bounds__(480, 1)
         while (hi + 1 < p.G && hoff[hi + 1] <= t) ++hi;
         sq[t] = p.k_queue[hoff[kMaxHeads + 1 + hi] + (t - hoff[hi])];
       }
-    } else if constexpr (MI) {
-      if (threadIdx.x == 0) {
-        int acc = 0;
-        for (int mi = 0; mi < p.M; ++mi) {
-          const int r = (mi * p.B + b) * nK + kb;
-          hoff[mi] = acc;
-          hoff[kMaxHeads + 1 + mi] = p.k_off[r];
-          acc += p.k_off[r + 1] - p.k_off[r];
-        }
-        hoff[p.M] = acc;
-      }
-      __syncthreads();
-      for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) {
-        int mi = 0;
-        while (mi + 1 < p.M && hoff[mi + 1] <= t) ++mi;
-        sq[t] = p.k_queue[hoff[kMaxHeads + 1 + mi] + (t - hoff[mi])];
-      }
     } else {
       for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) sq[t] = p.k_queue[kbeg + t];
     }
   }
   // the unit decoder of every role (a cursor over the heads with per-head
-  // masks, over the intervals with multi-interval masks)
+  // masks)
   auto decode = [&](int u, int& hcur) -> Unit {
     if constexpr (PH) return decode_unit_ph(p, u, g, force_part, s_queue, C::QUEUE_CAP, hoff, hcur);
-    else if constexpr (MI) return decode_unit_multi(p, u, g, force_part, s_queue, C::QUEUE_CAP, hoff, hcur);
     else return decode_unit(p, u, L, kbeg, g, force_part, s_queue, C::QUEUE_CAP);
   };
   if (C::ZERO_BYTES > 0) {
@@ -513,8 +468,22 @@ __global__ void __launch_bounds__(480, 1)
       if (a0 < a1) { lo0 = a0; lo1 = a1; }
       if (u0 < u1) { up0 = u0; up1 = u1; }
     };
-    int mhead = -1;  // the head (interval) whose vectors are loaded (per-head / multi-interval masks)
+    int mhead = -1;  // the head whose vectors are loaded (per-head masks)
     if constexpr (MODE == 0) load_mask(b);
+    // multi-interval masks: this key column's visible rows [fs, fe] per
+    // interval (unused intervals and keys beyond Nk empty), clamped to
+    // [-1, N] (rows outside [0, N) do not matter)
+    int fs[4] = {1, 1, 1, 1}, fe[4] = {0, 0, 0, 0};
+    if constexpr (MI) {
+#pragma unroll
+      for (int mi = 0; mi < 4; ++mi) {
+        if (mi < p.M && !dead) {
+          const size_t vi = ((size_t)mi * p.B + b) * p.Nk + kcol;
+          fs[mi] = min(max(p.lts[vi], -1), p.N);
+          fe[mi] = min(max(p.lte[vi], -1), p.N);
+        }
+      }
+    }
     const float sl2 = p.scale_log2;
     const bool causal = p.causal != 0;
     const uint32_t s_rows = smem_u32(smem + C::ROW_OFF);
@@ -530,11 +499,6 @@ __global__ void __launch_bounds__(480, 1)
           load_mask(b * p.H_q + un.h);
           mhead = un.h;
         }
-      } else if constexpr (MI) {
-        if (un.m != mhead) {
-          load_mask(un.m * p.B + b);
-          mhead = un.m;
-        }
       }
       const int stage = u % S;
       const int r0 = un.qb * 128 + un.half * 64;
@@ -547,8 +511,16 @@ __global__ void __launch_bounds__(480, 1)
       uint32_t mbits = 0u;
       if (un.part) {
         const int w0 = r0 + 32 * half;
-        mbits = rows_bits(lo0 - w0, lo1 - w0) | rows_bits(up0 - w0, up1 - w0) |
-                (causal ? rows_bits(-w0, kcol - w0) : 0u) | (dead ? 0xffffffffu : 0u);
+        if constexpr (MI) {
+          // masked unless one interval holds the row
+          uint32_t vis = 0u;
+#pragma unroll
+          for (int mi = 0; mi < 4; ++mi) vis |= rows_bits(fs[mi] - w0, fe[mi] + 1 - w0);
+          mbits = ~vis | (causal ? rows_bits(-w0, kcol - w0) : 0u) | (dead ? 0xffffffffu : 0u);
+        } else {
+          mbits = rows_bits(lo0 - w0, lo1 - w0) | rows_bits(up0 - w0, up1 - w0) |
+                  (causal ? rows_bits(-w0, kcol - w0) : 0u) | (dead ? 0xffffffffu : 0u);
+        }
       }
       const uint32_t rows_a = s_rows + stage * 512 + 128 * half;  // nl[32*half ..] ; D at +256
       // P part: P^T = exp2(scale*log2e*S^T - LSE*log2e), written back as bf16 over
@@ -857,8 +829,7 @@ cudaError_t launch_bwd_d(const fm_problem& P, const void* q, const void* k, cons
   // dQ rows at once).
   // (d = 256 runs two CTAs per KV block, one per head-dim half)
   // (per-head masks: natural order; the order kernel reads one queue per (batch, KV block))
-  // (multi-interval masks: natural order; a KV block's length sums M queues)
-  const bool natural = MODE != 0 || use_natural_order((D == 256 ? 2LL : 1LL) * P.B * nK * P.H_kv);
+  const bool natural = MODE == 1 || use_natural_order((D == 256 ? 2LL : 1LL) * P.B * nK * P.H_kv);
   if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(prm0.k_off, P.B * nK, w.order);
   // 3. main kernel
   if constexpr (D == 256) {
@@ -953,7 +924,7 @@ cudaError_t launch_bwd(const fm_problem& P, const void* q, const void* k, const 
     if (P.d == 256) return launch_bwd_d<256, 1>(P, q, k, v, o, lse, dout, dq, prm, w, s);
     return cudaErrorInvalidValue;
   }
-  if (M > 1) {
+  if (M > 0) {
     if (M > 4) return cudaErrorInvalidValue;
     if (P.d == 128) return launch_bwd_d<128, 2>(P, q, k, v, o, lse, dout, dq, prm, w, s);
     if (P.d == 64) return launch_bwd_d<64, 2>(P, q, k, v, o, lse, dout, dq, prm, w, s);

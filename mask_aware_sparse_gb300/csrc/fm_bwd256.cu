@@ -146,31 +146,9 @@ __device__ __forceinline__ Unit256 decode256_ph(const Bwd256Params& p, int u, in
   r.m = 0;
   return r;
 }
-// The same with multi-interval masks: interval m's queue for this KV block is
-// walked for every head of the group (units [2 G hoff[m], 2 G hoff[m + 1]),
-// head-major, then the queue, then the half); m is the caller's cursor.
-__device__ __forceinline__ Unit256 decode256_multi(const Bwd256Params& p, int u, int b, int kb, int g,
-                                                   bool force_part, uint32_t s_queue, const int* hoff, int& m) {
-  while (u >= 2 * p.G * hoff[m + 1]) ++m;
-  const int Lm = hoff[m + 1] - hoff[m];
-  const int rem = u - 2 * p.G * hoff[m];
-  const int hi = rem / (2 * Lm);
-  const int r2 = rem - hi * 2 * Lm;
-  const int pos = hoff[m] + (r2 >> 1);
-  const int e = (pos < B256::QUEUE_CAP) ? lds_s32(s_queue + 4 * pos)
-                                         : p.k_queue[p.k_off[(m * p.B + b) * p.nK + kb] + (r2 >> 1)];
-  Unit256 r;
-  r.h = g * p.G + hi;
-  r.qb = e >> 1;
-  r.half = r2 & 1;
-  r.part = (e & 1) | (force_part ? 1 : 0);
-  r.m = m;
-  return r;
-}
-
 // MODE 0: mask vectors (B, N_kv) shared by the heads; 1: per-head vectors
-// (B, H_q, N_kv) and queues over B * H_q rows; 2: multi-interval vectors
-// (M, B, N_kv) and queues over M * B rows.
+// (B, H_q, N_kv) and queues over B * H_q rows; 2: multi-interval masks (lts /
+// lte hold FMS / FME, (M, B, N_kv); the union classification's queues).
 template <int MODE>
 __global__ void __launch_bounds__(448, 1)
     bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -200,11 +178,6 @@ __global__ void __launch_bounds__(448, 1)
   if constexpr (PH) {
     for (int hi = 0; hi < p.G; ++hi) {
       const int r = (b * p.H_q + g * p.G + hi) * nK + kb;
-      L += p.k_off[r + 1] - p.k_off[r];
-    }
-  } else if constexpr (MI) {
-    for (int mi = 0; mi < p.M; ++mi) {
-      const int r = (mi * p.B + b) * nK + kb;
       L += p.k_off[r + 1] - p.k_off[r];
     }
   } else {
@@ -271,22 +244,6 @@ __global__ void __launch_bounds__(448, 1)
         while (hi + 1 < p.G && hoff[hi + 1] <= t) ++hi;
         sq[t] = p.k_queue[p.k_off[(b * p.H_q + g * p.G + hi) * nK + kb] + (t - hoff[hi])];
       }
-    } else if constexpr (MI) {
-      if (threadIdx.x == 0) {
-        int acc = 0;
-        for (int mi = 0; mi < p.M; ++mi) {
-          const int r = (mi * p.B + b) * nK + kb;
-          hoff[mi] = acc;
-          acc += p.k_off[r + 1] - p.k_off[r];
-        }
-        hoff[p.M] = acc;
-      }
-      __syncthreads();
-      for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) {
-        int mi = 0;
-        while (mi + 1 < p.M && hoff[mi + 1] <= t) ++mi;
-        sq[t] = p.k_queue[p.k_off[(mi * p.B + b) * nK + kb] + (t - hoff[mi])];
-      }
     } else {
       for (int t = threadIdx.x; t < L && t < C::QUEUE_CAP; t += blockDim.x) sq[t] = p.k_queue[kbeg + t];
     }
@@ -294,7 +251,6 @@ __global__ void __launch_bounds__(448, 1)
   // the unit decoder of every role (a cursor over the heads with per-head masks)
   auto decode = [&](int u, int& hcur) -> Unit256 {
     if constexpr (PH) return decode256_ph(p, u, b, kb, g, force_part, s_queue, hoff, hcur);
-    else if constexpr (MI) return decode256_multi(p, u, b, kb, g, force_part, s_queue, hoff, hcur);
     else return decode256(p, u, L, kbeg, g, force_part, s_queue);
   };
   if (warp == 13) tmem_alloc<512>(tmem_slot);
@@ -452,6 +408,19 @@ __global__ void __launch_bounds__(448, 1)
     };
     int mhead = -1;  // the head whose vectors are loaded (per-head masks)
     if constexpr (MODE == 0) load_mask(b);
+    // multi-interval masks: this key column's visible rows [fs, fe] per
+    // interval (unused intervals and keys beyond Nk empty), clamped to [-1, N]
+    int fs[4] = {1, 1, 1, 1}, fe[4] = {0, 0, 0, 0};
+    if constexpr (MI) {
+#pragma unroll
+      for (int mi = 0; mi < 4; ++mi) {
+        if (mi < p.M && !dead) {
+          const size_t vi = ((size_t)mi * p.B + b) * p.Nk + kcol;
+          fs[mi] = min(max(p.lts[vi], -1), p.N);
+          fe[mi] = min(max(p.lte[vi], -1), p.N);
+        }
+      }
+    }
     const float sl2 = p.scale_log2;
     const bool causal = p.causal != 0;
     const uint32_t rows_b = smem_u32(smem + C::ROW_OFF) + 128 * half;  // nl[32*half ..]; D at +256
@@ -467,11 +436,6 @@ __global__ void __launch_bounds__(448, 1)
           load_mask(b * p.H_q + un.h);
           mhead = un.h;
         }
-      } else if constexpr (MI) {
-        if (un.m != mhead) {
-          load_mask(un.m * p.B + b);
-          mhead = un.m;
-        }
       }
       const uint32_t ph = (uint32_t)u & 1u;
       const int r0 = un.qb * 128 + un.half * 64;
@@ -486,8 +450,16 @@ __global__ void __launch_bounds__(448, 1)
       uint32_t mbits = 0u;
       if (un.part) {
         const int w0 = r0 + 32 * half;
-        mbits = rows_bits(lo0 - w0, lo1 - w0) | rows_bits(up0 - w0, up1 - w0) |
-                (causal ? rows_bits(-w0, kcol - w0) : 0u) | (dead ? 0xffffffffu : 0u);
+        if constexpr (MI) {
+          // masked unless one interval holds the row
+          uint32_t vis = 0u;
+#pragma unroll
+          for (int mi = 0; mi < 4; ++mi) vis |= rows_bits(fs[mi] - w0, fe[mi] + 1 - w0);
+          mbits = ~vis | (causal ? rows_bits(-w0, kcol - w0) : 0u) | (dead ? 0xffffffffu : 0u);
+        } else {
+          mbits = rows_bits(lo0 - w0, lo1 - w0) | rows_bits(up0 - w0, up1 - w0) |
+                  (causal ? rows_bits(-w0, kcol - w0) : 0u) | (dead ? 0xffffffffu : 0u);
+        }
       }
       // P part: P^T = exp2(scale*log2e*S^T - LSE*log2e), bf16, over this
       // half's first 16 S columns
@@ -710,8 +682,8 @@ cudaError_t launch_bwd256_main(const fm_problem& P, const void* q, const void* k
   if (mode == 1 && P.H_q / P.H_kv > kMaxHeads256) return cudaErrorInvalidValue;
   if (mode == 2 && (M < 1 || M > 4)) return cudaErrorInvalidValue;
   // the order table reads one queue per (batch, KV block): natural order with
-  // per-head and multi-interval masks
-  if (mode != 0) prm.order = nullptr;
+  // per-head masks
+  if (mode == 1) prm.order = nullptr;
   static bool attr_done[3] = {false, false, false};
   if (!attr_done[mode]) {
     cudaError_t e = cudaFuncSetAttribute(mode == 1 ? bwd256_kernel<1> : mode == 2 ? bwd256_kernel<2> : bwd256_kernel<0>,

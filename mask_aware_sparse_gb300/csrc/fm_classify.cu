@@ -202,12 +202,97 @@ __global__ void emit_queues_kernel(const uint8_t* __restrict__ cls, int B, int n
   }
 }
 
+// Multi-interval masks: the class of a tile is the most visible of the
+// intervals' own classes (skip < partial < unmasked), one CTA per (b, qb):
+// the row's classes, its count of non-skipped tiles and, by integer atomics,
+// each column's (zeroed by the caller).
+__global__ void union_classes_kernel(const uint8_t* __restrict__ cls_m, int M, int B, int nQ, int nK,
+                                     uint8_t* __restrict__ cls, int32_t* __restrict__ row_cnt,
+                                     int32_t* __restrict__ col_cnt) {
+  const int qb = blockIdx.x, b = blockIdx.y;
+  int cnt = 0;
+  for (int kb = threadIdx.x; kb < nK; kb += blockDim.x) {
+    uint8_t c = 0;
+    for (int m = 0; m < M; ++m) {
+      const uint8_t x = cls_m[(((size_t)m * B + b) * nQ + qb) * nK + kb];
+      c = x > c ? x : c;
+    }
+    cls[((size_t)b * nQ + qb) * nK + kb] = c;
+    if (c != 0) {
+      ++cnt;
+      atomicAdd(col_cnt + (size_t)b * nK + kb, 1);
+    }
+  }
+  __shared__ int red[32];
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cnt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+    row_cnt[(size_t)b * nQ + qb] = t;
+  }
+}
+
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
 
 size_t classify_ws_bytes(int B, int nQ, int nK) {
   return align256(sizeof(Minmax) * (size_t)B * nK) + align256(4 * (size_t)B * nQ) + align256(4 * (size_t)B * nK);
+}
+
+// Multi-interval masks: the intervals' complements (M * B vector rows, the
+// FMS / FME conversion), their classes, the union classes and the queues.
+size_t classify_multi_ws_bytes(int M, int B, int nQ, int nK, int Nk) {
+  const size_t R = (size_t)M * B;
+  return 4 * align256(4 * R * Nk) + classify_ws_bytes((int)R, nQ, nK) + align256(R * nQ * nK) +
+         classify_ws_bytes(B, nQ, nK);
+}
+
+cudaError_t launch_classify_multi(const fm_problem& p, int M, int bm, int bn, int nQ, int nK, const int32_t* fms,
+                                  const int32_t* fme, uint8_t* tile_class, int32_t* q_off, int32_t* q_queue,
+                                  int32_t* k_off, int32_t* k_queue, void* ws, cudaStream_t s, int* err) {
+  const int B = p.B, Nk = kv_rows(p);
+  const size_t R = (size_t)M * B;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* vec[4];
+  for (int i = 0; i < 4; ++i) {
+    vec[i] = reinterpret_cast<int32_t*>(w);
+    w += align256(4 * R * Nk);
+  }
+  void* ws_m = w;  // the per-interval classification
+  w += classify_ws_bytes((int)R, nQ, nK);
+  uint8_t* cls_m = w;
+  w += align256(R * nQ * nK);
+  uint8_t* wu = w;  // the union's: minmax (unused), row and column counts
+  wu += align256(sizeof(Minmax) * (size_t)B * nK);
+  int32_t* row_cnt = reinterpret_cast<int32_t*>(wu);
+  wu += align256(4 * (size_t)B * nQ);
+  int32_t* col_cnt = reinterpret_cast<int32_t*>(wu);
+  cudaError_t e = launch_from_fms_fme(fms, fme, (int64_t)(R * Nk), p.N, vec[0], vec[1], vec[2], vec[3], s);
+  if (e != cudaSuccess) return e;
+  fm_problem pm = p;
+  pm.B = (int32_t)R;
+  uint8_t* wm = static_cast<uint8_t*>(ws_m);
+  Minmax* mm = reinterpret_cast<Minmax*>(wm);
+  wm += align256(sizeof(Minmax) * R * nK);
+  int32_t* row_cnt_m = reinterpret_cast<int32_t*>(wm);
+  wm += align256(4 * R * nQ);
+  int32_t* col_cnt_m = reinterpret_cast<int32_t*>(wm);
+  block_minmax_kernel<<<(unsigned)((R * nK + 7) / 8), 256, 0, s>>>(vec[0], vec[1], vec[2], vec[3], (int)R, p.N, Nk,
+                                                                   bn, nK, mm, col_cnt_m, err);
+  classify_rows_kernel<<<dim3(nQ, (unsigned)R), 256, 0, s>>>(mm, p.N, Nk, bm, bn, nQ, nK, p.causal, cls_m,
+                                                             row_cnt_m, col_cnt_m);
+  e = cudaMemsetAsync(col_cnt, 0, 4 * (size_t)B * nK, s);
+  if (e != cudaSuccess) return e;
+  union_classes_kernel<<<dim3(nQ, B), 256, 0, s>>>(cls_m, M, B, nQ, nK, tile_class, row_cnt, col_cnt);
+  const long long nkb = (long long)B * nK, nqb = (long long)B * nQ;
+  scan_kernel<<<2, 1024, 0, s>>>(row_cnt, (int)nqb, q_off, col_cnt, (int)nkb, k_off);
+  emit_queues_kernel<<<(unsigned)((nqb + nkb + 7) / 8), 256, 0, s>>>(tile_class, B, nQ, nK, q_off, q_queue, k_off,
+                                                                     k_queue);
+  count_launches(5);  // minmax, classify rows, union, scan, emit (the conversion counts itself)
+  return cudaGetLastError();
 }
 
 cudaError_t launch_classify(const fm_problem& p, int bm, int bn, int nQ, int nK, const int32_t* lts,

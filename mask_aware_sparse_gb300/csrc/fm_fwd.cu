@@ -44,8 +44,9 @@
 //     in L2.
 //   * Other mask forms: with per-head vectors a unit is one head with its own
 //     queue and vector row; with multi-interval masks (the MI instantiation)
-//     a unit walks its Q block's M interval queues one after the other, each
-//     block masked with its own interval's vectors, in one online softmax.
+//     the queues are those of the union classification and a partial block's
+//     mask is built from every interval's FMS / FME (a row is masked unless
+//     one interval holds it).
 #include <algorithm>
 #include <climits>
 #include <cmath>
@@ -59,8 +60,10 @@
 namespace fm {
 namespace {
 
-// F8: Q, K, V (and P) are e4m3 instead of bf16 (the FP8 forward).
-template <int D, bool F8 = false>
+// F8: Q, K, V (and P) are e4m3 instead of bf16 (the FP8 forward). MI:
+// multi-interval masks (a mask slot holds FMS[128], FME[128] of up to four
+// intervals).
+template <int D, bool F8 = false, bool MI = false>
 struct FwdCfg {
   static constexpr int ES = F8 ? 1 : 2;         // bytes per Q / K / V element
   static constexpr int TILE = 128 * D * ES;     // bytes of one 128-row tile
@@ -71,7 +74,8 @@ struct FwdCfg {
   static constexpr int K_OFF = Q_OFF + 2 * TILE;
   static constexpr int V_OFF = K_OFF + STAGES * TILE;
   static constexpr int M_OFF = V_OFF + STAGES * TILE;
-  static constexpr int M_BYTES = 4 * 128 * 4;  // LTS[128], LTE[128], UTS[128], UTE[128]
+  // mask slot: LTS[128], LTE[128], UTS[128], UTE[128]; MI: FMS[128], FME[128] x 4
+  static constexpr int M_BYTES = MI ? 4 * 2 * 128 * 4 : 4 * 128 * 4;
   // O staging: one 2 KB slot per softmax warp (32 rows x 32 columns bf16,
   // 64-byte swizzle), the source of that warp's TMA stores
   static constexpr int O_OFF = M_OFF + STAGES * M_BYTES;
@@ -105,10 +109,8 @@ struct FwdCfg {
   static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
 };
 
-// unit header words in the unit ring (multi-interval masks: the queue start
-// and the first unit-queue position of interval m at UH_SEGQ + m, UH_SEGC + m)
-enum { UH_N = 0, UH_T = 1, UH_QB = 2, UH_B = 3, UH_H0 = 4, UH_G = 5, UH_QBEG = 6, UH_END = 7, UH_SEGQ = 8,
-       UH_SEGC = 12 };
+// unit header words in the unit ring
+enum { UH_N = 0, UH_T = 1, UH_QB = 2, UH_B = 3, UH_H0 = 4, UH_G = 5, UH_QBEG = 6, UH_END = 7 };
 
 struct FwdParams {
   const int32_t* lts;
@@ -124,10 +126,8 @@ struct FwdParams {
   int B, H_q, H_kv, N, Nk, nQ, nK, G, PG, causal;  // N query rows, Nk key rows
   int units;  // B * nQ * H_kv * PG work units (per-head masks: B * H_q * nQ)
   int per_head;  // mask vectors and queues per (batch, query head): one head per unit
-  // multi-interval masks: M sets of vectors (M, B, N_kv) and queues over the
-  // M * B vector rows; a unit walks its Q block's M queues one after the
-  // other (entries tagged with m in bits 24-25), each with its own vectors.
-  // 1 otherwise.
+  // multi-interval masks: lts / lte hold FMS / FME, (M, B, N_kv), M >= 1
+  // (the MI instantiation); 0 otherwise
   int M;
   float scale_log2;
   float o_scale;  // multiplies O / l (the V dequantization scale of the FP8 forward; 1 otherwise)
@@ -174,29 +174,19 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int k) {
   return u;
 }
 
-// Queue entry of a unit: (kb << 1) | partial, with the interval index of a
-// multi-interval mask in bits 24-25 (kb < 2^23).
-constexpr int kKbMask = (1 << 23) - 1;
-template <bool MI>
-__device__ __forceinline__ int entry_kb(int e) {
-  if constexpr (MI) return (e >> 1) & kKbMask;
-  else return e >> 1;
-}
-
 // A queue block is partial when the classification tagged it so, or when it
 // is the last key block and N is not a multiple of 128 (its tail columns are
 // masked for every row).
-template <bool MI>
 __device__ __forceinline__ bool block_partial(const FwdParams& p, int e) {
-  return (e & 1) || (entry_kb<MI>(e) == p.nK - 1 && (p.Nk & 127));
+  return (e & 1) || ((e >> 1) == p.nK - 1 && (p.Nk & 127));
 }
 
-// MI: multi-interval masks (the unit walks p.M queues, entries tagged).
+// MI: multi-interval masks (mask slots hold FMS / FME of every interval).
 template <int D, bool F8, bool MI>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, const FwdParams p) {
-  using C = FwdCfg<D, F8>;
+  using C = FwdCfg<D, F8, MI>;
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -248,11 +238,8 @@ __global__ void __launch_bounds__(320, 1)
   // staged prefix come from global memory)
   auto hdr_at = [&](int us, int w) -> int { return lds_s32(smem_u32(smem + C::U_OFF + us * C::U_BYTES) + 4 * w); };
   auto queue_at = [&](int us, int j) -> int {
-    if (j < C::QUEUE_CAP) return lds_s32(smem_u32(smem + C::U_OFF + us * C::U_BYTES) + 4 * (C::U_HDR + j));
-    if constexpr (!MI) return p.q_queue[hdr_at(us, UH_QBEG) + j];
-    int m = 0;
-    while (m + 1 < p.M && j >= hdr_at(us, UH_SEGC + m + 1)) ++m;
-    return p.q_queue[hdr_at(us, UH_SEGQ + m) + j - hdr_at(us, UH_SEGC + m)] | (m << 24);
+    return (j < C::QUEUE_CAP) ? lds_s32(smem_u32(smem + C::U_OFF + us * C::U_BYTES) + 4 * (C::U_HDR + j))
+                              : p.q_queue[hdr_at(us, UH_QBEG) + j];
   };
 
   // Every role walks the CTA's unit sequence through the unit ring (filled by
@@ -286,17 +273,7 @@ __global__ void __launch_bounds__(320, 1)
       // the next unit's index, requested now and used after this unit
       int k_next = 0;
       if (lane == 0) k_next = (int)gridDim.x + atomicAdd(p.next_unit, 1);
-      Unit u = decode_unit(p, k);
-      // multi-interval masks: the M queues of this Q block, back to back
-      int segq[4] = {u.qbeg, 0, 0, 0}, segc[5] = {0, u.n, u.n, u.n, u.n};
-      if constexpr (MI) {
-        for (int mi = 1; mi < p.M; ++mi) {
-          const int r = (mi * p.B + u.b) * p.nQ + u.qb;
-          segq[mi] = p.q_off[r];
-          segc[mi + 1] = segc[mi] + (p.q_off[r + 1] - segq[mi]);
-        }
-        u.n = segc[p.M];
-      }
+      const Unit u = decode_unit(p, k);
       {
         if (lane == 0) {
           h[UH_END] = 0;
@@ -307,13 +284,6 @@ __global__ void __launch_bounds__(320, 1)
           h[UH_H0] = u.h0;
           h[UH_G] = u.g;
           h[UH_QBEG] = u.qbeg;
-          if constexpr (MI) {
-#pragma unroll
-            for (int mi = 0; mi < 4; ++mi) {
-              h[UH_SEGQ + mi] = segq[mi];
-              h[UH_SEGC + mi] = segc[mi];
-            }
-          }
         }
         int* sq = h + C::U_HDR;
         const int m = min(u.n, C::QUEUE_CAP);
@@ -322,13 +292,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int j = j0 + 32 * r + lane;
-            if constexpr (!MI) {
-              e[r] = (j < m) ? p.q_queue[u.qbeg + j] : 0;
-            } else {
-              int mi = 0;
-              while (mi + 1 < p.M && j >= segc[mi + 1]) ++mi;
-              e[r] = (j < m) ? (p.q_queue[segq[mi] + j - segc[mi]] | (mi << 24)) : 0;
-            }
+            e[r] = (j < m) ? p.q_queue[u.qbeg + j] : 0;
           }
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
@@ -343,16 +307,15 @@ __global__ void __launch_bounds__(320, 1)
       if (u.n <= 0) continue;
       for (int j = 0; j < u.n && ok; ++j) {
         const int e = queue_at(us, j);
-        const int kb = entry_kb<MI>(e);
-        // the vectors of this entry's mask (multi-interval: of its interval)
-        const size_t vbase = (size_t)(MI ? (e >> 24) * p.B + u.b : u.vrow) * p.Nk;
+        const int kb = e >> 1;
+        const size_t vbase = (size_t)u.vrow * p.Nk;
         if (kb < 0 || kb >= p.nK) {
           if (lane == 0) record_error(p.err, FM_DEV_ERR_QUEUE);
           *abort_flag = 1;
           ok = false;
           break;
         }
-        const bool part = block_partial<MI>(p, e);
+        const bool part = block_partial(p, e);
         const int slot = jt % S;
         const uint32_t ph = (jt / S) & 1u;
         if (lane == 0) {
@@ -377,7 +340,47 @@ __global__ void __launch_bounds__(320, 1)
         }
         ok = __shfl_sync(kFull, ok, 0);
         if (!ok) break;
-        if (part) {
+        if (part && MI) {
+          // multi-interval masks: FMS[128], FME[128] of every interval, raw;
+          // a key beyond Nk gets an empty interval
+          const int ms = pidx % S;
+          const uint32_t mph = (pidx / S) & 1u;
+          ok = __all_sync(kFull, mbar_wait(&bars[C::B_MEMPTY + ms], mph ^ 1u, abort_flag, p.err));
+          if (!ok) break;
+          uint8_t* sm = smem + C::M_OFF + ms * C::M_BYTES;
+          const int c0 = kb * 128;
+          bool aligned = c0 + 128 <= p.Nk;
+          for (int mi = 0; mi < p.M; ++mi) {
+            const size_t o = ((size_t)mi * p.B + u.b) * p.Nk + c0;
+            aligned = aligned && ((reinterpret_cast<uintptr_t>(p.lts + o) | reinterpret_cast<uintptr_t>(p.lte + o)) &
+                                  15u) == 0;
+          }
+          if (aligned) {
+            if (lane == 0) {
+              uint64_t* fb = &bars[C::B_MFULL + ms];
+              mbar_arrive_expect_tx(fb, 2 * 512 * p.M);
+              for (int mi = 0; mi < p.M; ++mi) {
+                const size_t o = ((size_t)mi * p.B + u.b) * p.Nk + c0;
+                bulk_load(sm + mi * 1024, p.lts + o, 512, fb);
+                bulk_load(sm + mi * 1024 + 512, p.lte + o, 512, fb);
+              }
+            }
+          } else {
+            int* v = reinterpret_cast<int*>(sm);
+            for (int mi = 0; mi < p.M; ++mi) {
+              const size_t o = ((size_t)mi * p.B + u.b) * p.Nk;
+              for (int c = lane; c < 128; c += 32) {
+                const int col = c0 + c;
+                const bool in = col < p.Nk;
+                v[mi * 256 + c] = in ? p.lts[o + col] : 1;
+                v[mi * 256 + 128 + c] = in ? p.lte[o + col] : 0;
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[C::B_MFULL + ms]);
+          }
+          ++pidx;
+        } else if (part) {
           // the block's four mask vectors, raw, as 4 x 128 int32 (LTS, LTE, UTS,
           // UTE); the softmax warps clamp and check them
           const int ms = pidx % S;
@@ -632,7 +635,7 @@ __global__ void __launch_bounds__(320, 1)
         // partial-block count (head 0 releases the mask ring for both)
         uint32_t c = 0;
         for (int j0 = 0; j0 < n; j0 += 32) {
-          const bool part = (j0 + lane < n) && block_partial<MI>(p, queue_at(us, j0 + lane));
+          const bool part = (j0 + lane < n) && block_partial(p, queue_at(us, j0 + lane));
           c += __popc(__ballot_sync(kFull, part));
         }
         pidx += c;
@@ -644,8 +647,8 @@ __global__ void __launch_bounds__(320, 1)
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < n; ++j) {
         const int e = queue_at(us, j);
-        const int kb = entry_kb<MI>(e);
-        const bool part = block_partial<MI>(p, e);
+        const int kb = e >> 1;
+        const bool part = block_partial(p, e);
         // Partial blocks: masked-row bits of this thread's query row over the
         // block's 128 key columns, built while S is still being computed. Lane
         // c of the warp builds the bits of key column 32k + c over the warp's
@@ -662,10 +665,21 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int kq = 0; kq < 4; ++kq) {
             const int c = 32 * kq + lane;
-            const int a0 = lds_s32(sm + 4 * c), a1 = lds_s32(sm + 512 + 4 * c);  // LTS, LTE of key column kc0 + c
-            const int u0 = lds_s32(sm + 1024 + 4 * c), u1 = lds_s32(sm + 1536 + 4 * c);  // UTS, UTE
-            const uint32_t colbits = window_bits(a0, a1, w0) | window_bits(u0, u1, w0) |
-                                     (causal ? window_bits(w0, kc0 + c, w0) : 0u);
+            uint32_t colbits;
+            if constexpr (MI) {
+              // masked unless one interval [FMS, FME] holds the row
+              uint32_t vis = 0u;
+              for (int mi = 0; mi < p.M; ++mi) {
+                const int f0 = lds_s32(sm + mi * 1024 + 4 * c), f1 = lds_s32(sm + mi * 1024 + 512 + 4 * c);
+                vis |= window_bits(f0, min(f1, p.N) + 1, w0);
+              }
+              colbits = ~vis | (causal ? window_bits(w0, kc0 + c, w0) : 0u);
+            } else {
+              const int a0 = lds_s32(sm + 4 * c), a1 = lds_s32(sm + 512 + 4 * c);  // LTS, LTE of key column kc0 + c
+              const int u0 = lds_s32(sm + 1024 + 4 * c), u1 = lds_s32(sm + 1536 + 4 * c);  // UTS, UTE
+              colbits = window_bits(a0, a1, w0) | window_bits(u0, u1, w0) |
+                        (causal ? window_bits(w0, kc0 + c, w0) : 0u);
+            }
             rb[kq] = warp_transpose32(colbits, lane);
           }
           __syncwarp();
@@ -814,7 +828,8 @@ __global__ void __launch_bounds__(320, 1)
 template <int D, bool F8, bool MI = false>
 cudaError_t launch_fwd_d(const fm_problem& P, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, const FwdParams& prm, unsigned grid, cudaStream_t s) {
-  using C = FwdCfg<D, F8>;
+  using C = FwdCfg<D, F8, MI>;
+  static_assert(C::SMEM_ALLOC <= 232448, "forward shared memory exceeds an SM's 227 KB");
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e =
@@ -874,7 +889,7 @@ static cudaError_t launch_fwd_persistent(const fm_problem& P, const void* q, con
                                          const int32_t* lts, const int32_t* lte, const int32_t* uts,
                                          const int32_t* ute, const int32_t* q_off, const int32_t* q_queue, void* o,
                                          float* lse, void* ws, cudaStream_t s, int* err, bool fp8, float q_scale,
-                                         float k_scale, float v_scale, bool per_head = false, int M = 1) {
+                                         float k_scale, float v_scale, bool per_head = false, int M = 0) {
   const int nQ = (P.N + kTile - 1) / kTile;
   const int G = P.H_q / P.H_kv;
   const int PG = (G + 1) / 2;
@@ -883,9 +898,8 @@ static cudaError_t launch_fwd_persistent(const fm_problem& P, const void* q, con
   const long long rows = per_head ? (long long)P.B * P.H_q * nQ : (long long)P.B * nQ;  // queue rows
   if (units > INT_MAX) return cudaErrorInvalidConfiguration;
   // unit order: longest queue first, or natural order for long passes
-  // (units that run together then share K / V tiles in L2); multi-interval
-  // masks: natural order (a unit's length sums M queues)
-  const bool natural = M > 1 || use_natural_order(units);
+  // (units that run together then share K / V tiles in L2)
+  const bool natural = use_natural_order(units);
   int32_t* order = natural ? nullptr : static_cast<int32_t*>(ws);
   int* next_unit = reinterpret_cast<int*>(static_cast<char*>(ws) + order_bytes(rows));
   {
@@ -936,7 +950,7 @@ static cudaError_t launch_fwd_persistent(const fm_problem& P, const void* q, con
   // persistent: one CTA per SM (the kernel's shared memory and TMEM fill an SM)
   const unsigned grid = (unsigned)std::min<long long>(units, (long long)sm_count());
   if (fp8) return launch_fwd_d<128, true>(P, tq, tk, tv, to, prm, grid, s);
-  if (M > 1) {
+  if (M > 0) {
     if (P.d == 128) return launch_fwd_d<128, false, true>(P, tq, tk, tv, to, prm, grid, s);
     return launch_fwd_d<64, false, true>(P, tq, tk, tv, to, prm, grid, s);
   }
@@ -961,12 +975,12 @@ cudaError_t launch_fwd_heads(const fm_problem& P, const void* q, const void* k, 
 }
 
 cudaError_t launch_fwd_multi(const fm_problem& P, int M, const void* q, const void* k, const void* v,
-                             const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
-                             const int32_t* q_off, const int32_t* q_queue, void* o, float* lse, void* ws,
-                             cudaStream_t s, int* err) {
-  if (P.d == 256) return launch_fwd256(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err, false, M);
-  return launch_fwd_persistent(P, q, k, v, lts, lte, uts, ute, q_off, q_queue, o, lse, ws, s, err, false, 1.f, 1.f,
-                               1.f, false, M);
+                             const int32_t* fms, const int32_t* fme, const int32_t* q_off, const int32_t* q_queue,
+                             void* o, float* lse, void* ws, cudaStream_t s, int* err) {
+  if (P.d == 256)
+    return launch_fwd256(P, q, k, v, fms, fme, nullptr, nullptr, q_off, q_queue, o, lse, ws, s, err, false, M);
+  return launch_fwd_persistent(P, q, k, v, fms, fme, nullptr, nullptr, q_off, q_queue, o, lse, ws, s, err, false,
+                               1.f, 1.f, 1.f, false, M);
 }
 
 cudaError_t launch_fwd_fp8(const fm_problem& P, const void* q, const void* k, const void* v, float q_scale,

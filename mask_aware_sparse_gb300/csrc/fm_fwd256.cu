@@ -59,8 +59,10 @@ struct F256 {
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + TILE;
   static constexpr int V_OFF = K_OFF + TILE;
-  static constexpr int M_OFF = V_OFF + TILE;  // 2 slots x {LTS, LTE, UTS, UTE}[128] int32
-  static constexpr int M_BYTES = 4 * 128 * 4;
+  // 2 mask slots of {LTS, LTE, UTS, UTE}[128] int32 (multi-interval masks:
+  // {FMS, FME}[128] of up to four intervals)
+  static constexpr int M_OFF = V_OFF + TILE;
+  static constexpr int M_BYTES = 4 * 2 * 128 * 4;
   static constexpr int O_OFF = M_OFF + 2 * M_BYTES;  // 4 warps x 2 KB
   static constexpr int O_SLOT = 32 * 32 * 2;
   static constexpr int BAR_OFF = O_OFF + 4 * O_SLOT;
@@ -92,27 +94,18 @@ struct Fwd256Params {
   float* lse;
   int B, H_q, H_kv, N, Nk, nQ, nK, G, causal;
   int per_head;  // vectors (B, H_q, N_kv), one queue per (b, h, qb) row
-  // multi-interval masks: M sets of vectors (M, B, N_kv), queues over the
-  // M * B vector rows, walked one after the other (1 otherwise)
+  // multi-interval masks: lts / lte hold FMS / FME, (M, B, N_kv), M >= 1
+  // (the MI instantiation); 0 otherwise
   int M;
   float scale_log2;
   int* err;
 };
 
-// queue entry: (kb << 1) | partial, the interval of a multi-interval mask in
-// bits 24-25 (kb < 2^23)
-template <bool MI>
-__device__ __forceinline__ int kb256(int e) {
-  if constexpr (MI) return (e >> 1) & ((1 << 23) - 1);
-  else return e >> 1;
-}
-
-template <bool MI>
 __device__ __forceinline__ bool partial256(const Fwd256Params& p, int e) {
-  return (e & 1) || (kb256<MI>(e) == p.nK - 1 && (p.Nk & 127));
+  return (e & 1) || ((e >> 1) == p.nK - 1 && (p.Nk & 127));
 }
 
-// MI: multi-interval masks (the CTA walks p.M queues, entries tagged).
+// MI: multi-interval masks (mask slots hold FMS / FME of every interval).
 template <bool MI>
 __global__ void __launch_bounds__(256, 1)
     fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -154,28 +147,9 @@ __global__ void __launch_bounds__(256, 1)
   }
   const int g = h / p.G;
   const int qbeg = p.q_off[row];
-  int n = p.q_off[row + 1] - qbeg;
+  const int n = p.q_off[row + 1] - qbeg;
   const int bh = b * p.H_q + h;
   const size_t vbase = (size_t)(p.per_head ? bh : b) * p.Nk;
-  // multi-interval masks: this Q block's M queues back to back
-  int segq[4] = {qbeg, 0, 0, 0}, segc[5] = {0, n, n, n, n};
-  if constexpr (MI) {
-    for (int mi = 1; mi < p.M; ++mi) {
-      const int r = (mi * p.B + b) * p.nQ + qb;
-      segq[mi] = p.q_off[r];
-      segc[mi + 1] = segc[mi] + (p.q_off[r + 1] - segq[mi]);
-    }
-    n = segc[p.M];
-  }
-  // entry j of the unit's queue (tagged with its interval) and the row of its
-  // mask vectors
-  auto qentry = [&](int j) -> int {
-    if constexpr (!MI) return p.q_queue[qbeg + j];
-    int mi = 0;
-    while (mi + 1 < p.M && j >= segc[mi + 1]) ++mi;
-    return p.q_queue[segq[mi] + j - segc[mi]] | (mi << 24);
-  };
-  auto vrow_base = [&](int e) -> size_t { return MI ? (size_t)((e >> 24) * p.B + b) * p.Nk : vbase; };
 
   if (threadIdx.x == 0) {
     *abort_flag = timeout_pending(p.err) ? 1 : 0;
@@ -219,9 +193,8 @@ __global__ void __launch_bounds__(256, 1)
         tma_load_3d(smem + C::Q_OFF + x * 16384, &tq, &bars[C::B_QFULL], x * 64, qb * 128, bh);
     }
     for (int j = 0; j < n && ok; ++j) {
-      const int e = qentry(j);
-      const int kb = kb256<MI>(e);
-      const size_t vb = vrow_base(e);
+      const int e = p.q_queue[qbeg + j];
+      const int kb = e >> 1;
       if (kb < 0 || kb >= p.nK) {
         if (lane == 0) record_error(p.err, FM_DEV_ERR_QUEUE);
         *abort_flag = 1;
@@ -238,14 +211,50 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       ok = __shfl_sync(kFull256, ok, 0);
-      if (!ok || !partial256<MI>(p, e)) continue;
-      // the block's four mask vectors, raw (LTS, LTE, UTS, UTE x 128); the
-      // softmax warps clamp them to their 32-row windows
+      if (!ok || !partial256(p, e)) continue;
+      // the block's four mask vectors, raw (LTS, LTE, UTS, UTE x 128; with
+      // multi-interval masks FMS, FME x 128 of every interval, a key beyond
+      // Nk an empty interval); the softmax warps clamp them to their 32-row
+      // windows
       const int ms = pidx & 1;
       ok = __all_sync(kFull256, mbar_wait(&bars[C::B_MEMPTY + ms], ((pidx >> 1) & 1u) ^ 1u, abort_flag, p.err));
       if (!ok) break;
       uint8_t* sm = smem + C::M_OFF + ms * C::M_BYTES;
       const int c0 = kb * 128;
+      if constexpr (MI) {
+        bool al = c0 + 128 <= p.Nk;
+        for (int mi = 0; mi < p.M; ++mi) {
+          const size_t o = ((size_t)mi * p.B + b) * p.Nk + c0;
+          al = al && ((reinterpret_cast<uintptr_t>(p.lts + o) | reinterpret_cast<uintptr_t>(p.lte + o)) & 15u) == 0;
+        }
+        if (al) {
+          if (lane == 0) {
+            uint64_t* fb = &bars[C::B_MFULL + ms];
+            mbar_arrive_expect_tx(fb, 2 * 512 * p.M);
+            for (int mi = 0; mi < p.M; ++mi) {
+              const size_t o = ((size_t)mi * p.B + b) * p.Nk + c0;
+              bulk_load(sm + mi * 1024, p.lts + o, 512, fb);
+              bulk_load(sm + mi * 1024 + 512, p.lte + o, 512, fb);
+            }
+          }
+        } else {
+          int* vv = reinterpret_cast<int*>(sm);
+          for (int mi = 0; mi < p.M; ++mi) {
+            const size_t o = ((size_t)mi * p.B + b) * p.Nk;
+            for (int c = lane; c < 128; c += 32) {
+              const int col = c0 + c;
+              const bool in = col < p.Nk;
+              vv[mi * 256 + c] = in ? p.lts[o + col] : 1;
+              vv[mi * 256 + 128 + c] = in ? p.lte[o + col] : 0;
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[C::B_MFULL + ms]);
+        }
+        ++pidx;
+        continue;
+      }
+      const size_t vb = vbase;
       const size_t o = vb + c0;
       const bool aligned = ((reinterpret_cast<uintptr_t>(p.lts + o) | reinterpret_cast<uintptr_t>(p.lte + o) |
                              reinterpret_cast<uintptr_t>(p.uts + o) | reinterpret_cast<uintptr_t>(p.ute + o)) &
@@ -279,7 +288,7 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) {
       bool ok = true;
       for (int j = 0; j < n && ok; ++j) {
-        const int kb = kb256<MI>(qentry(j));
+        const int kb = p.q_queue[qbeg + j] >> 1;
         if (kb < 0 || kb >= p.nK) break;  // flagged by the K producer
         // 32 keys at a time (all four 64-column boxes), each quarter as soon
         // as PV(j-1) has read it
@@ -358,9 +367,9 @@ __global__ void __launch_bounds__(256, 1)
     uint32_t pidx = 0;
     bool ok = true;
     for (int j = 0; j < n && ok; ++j) {
-      const int e = qentry(j);
-      const int kb = kb256<MI>(e);
-      const bool part = partial256<MI>(p, e);
+      const int e = p.q_queue[qbeg + j];
+      const int kb = e >> 1;
+      const bool part = partial256(p, e);
       // partial block: masked-row bits of this thread's row over the 128 key
       // columns (lane c builds column 32k + c over the warp's 32 rows, then a
       // bit transpose hands each lane its own row)
@@ -374,10 +383,20 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int kq = 0; kq < 4; ++kq) {
           const int c = 32 * kq + lane;
-          const int a0 = lds_s32(sm + 4 * c), a1 = lds_s32(sm + 512 + 4 * c);
-          const int u0 = lds_s32(sm + 1024 + 4 * c), u1 = lds_s32(sm + 1536 + 4 * c);
-          const uint32_t colbits = window_bits(a0, a1, w0) | window_bits(u0, u1, w0) |
-                                   (causal ? window_bits(w0, kc0 + c, w0) : 0u);
+          uint32_t colbits;
+          if constexpr (MI) {
+            // masked unless one interval [FMS, FME] holds the row
+            uint32_t vis = 0u;
+            for (int mi = 0; mi < p.M; ++mi) {
+              const int f0 = lds_s32(sm + mi * 1024 + 4 * c), f1 = lds_s32(sm + mi * 1024 + 512 + 4 * c);
+              vis |= window_bits(f0, min(f1, p.N) + 1, w0);
+            }
+            colbits = ~vis | (causal ? window_bits(w0, kc0 + c, w0) : 0u);
+          } else {
+            const int a0 = lds_s32(sm + 4 * c), a1 = lds_s32(sm + 512 + 4 * c);
+            const int u0 = lds_s32(sm + 1024 + 4 * c), u1 = lds_s32(sm + 1536 + 4 * c);
+            colbits = window_bits(a0, a1, w0) | window_bits(u0, u1, w0) | (causal ? window_bits(w0, kc0 + c, w0) : 0u);
+          }
           rb[kq] = warp_transpose32(colbits, lane);
         }
         __syncwarp();
@@ -538,7 +557,7 @@ cudaError_t launch_fwd256(const fm_problem& P, const void* q, const void* k, con
   const long long grid = (long long)P.B * nQ * P.H_q;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
   // longest queue first for passes of a few waves, natural order for long ones
-  const bool natural = M > 1 || use_natural_order(grid);
+  const bool natural = use_natural_order(grid);
   int32_t* order = natural ? nullptr : static_cast<int32_t*>(ws);
   if (!natural) lpt_order_kernel<<<1, 1024, 0, s>>>(q_off, per_head ? P.B * P.H_q * nQ : P.B * nQ, order);
   CUtensorMap tq, tk, tv, to;
@@ -569,7 +588,7 @@ cudaError_t launch_fwd256(const fm_problem& P, const void* q, const void* k, con
   prm.scale_log2 = P.scale * 1.4426950408889634f;
   prm.err = err;
   static bool attr_done[2] = {false, false};
-  const bool mi = M > 1;
+  const bool mi = M > 0;
   if (!attr_done[mi]) {
     cudaError_t e = cudaFuncSetAttribute(mi ? fwd256_kernel<true> : fwd256_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);

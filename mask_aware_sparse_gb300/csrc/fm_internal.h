@@ -11,6 +11,10 @@ int* device_error_word();
 
 // Classification (fm_classify.cu).
 size_t classify_ws_bytes(int B, int nQ, int nK);
+size_t classify_multi_ws_bytes(int M, int B, int nQ, int nK, int Nk);
+cudaError_t launch_classify_multi(const fm_problem& p, int M, int bm, int bn, int nQ, int nK, const int32_t* fms,
+                                  const int32_t* fme, uint8_t* tile_class, int32_t* q_off, int32_t* q_queue,
+                                  int32_t* k_off, int32_t* k_queue, void* ws, cudaStream_t s, int* err);
 cudaError_t launch_classify(const fm_problem& p, int bm, int bn, int nQ, int nK, const int32_t* lts,
                             const int32_t* lte, const int32_t* uts, const int32_t* ute, uint8_t* tile_class,
                             int32_t* q_off, int32_t* q_queue, int32_t* k_off, int32_t* k_queue, void* ws,
@@ -54,13 +58,12 @@ cudaError_t launch_fwd_fp8(const fm_problem& P, const void* q, const void* k, co
 cudaError_t launch_fwd256(const fm_problem& p, const void* q, const void* k, const void* v, const int32_t* lts,
                           const int32_t* lte, const int32_t* uts, const int32_t* ute, const int32_t* q_off,
                           const int32_t* q_queue, void* o, float* lse, void* ws, cudaStream_t s, int* err,
-                          bool per_head = false, int M = 1);
-// Multi-interval masks: M sets of vectors (M, B, N_kv), queues over the M * B
-// vector rows; one pass accumulates every interval's blocks.
+                          bool per_head = false, int M = 0);
+// Multi-interval masks: FMS / FME (M, B, N_kv), the union classification's
+// queues (M >= 1).
 cudaError_t launch_fwd_multi(const fm_problem& P, int M, const void* q, const void* k, const void* v,
-                             const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
-                             const int32_t* q_off, const int32_t* q_queue, void* o, float* lse, void* ws,
-                             cudaStream_t s, int* err);
+                             const int32_t* fms, const int32_t* fme, const int32_t* q_off, const int32_t* q_queue,
+                             void* o, float* lse, void* ws, cudaStream_t s, int* err);
 
 // The forward's fixed scratch for fm_attn_fwd_noalloc (fm_fwd.cu): device
 // address of the library-owned launch-order array of the current device, or
@@ -73,7 +76,7 @@ cudaError_t launch_bwd(const fm_problem& p, const void* q, const void* k, const 
                        const float* lse, const void* dout, const int32_t* lts, const int32_t* lte,
                        const int32_t* uts, const int32_t* ute, const int32_t* k_off, const int32_t* k_queue,
                        void* dq, void* dk, void* dv, void* ws, cudaStream_t s, int* err, bool per_head = false,
-                       int M = 1);
+                       int M = 0);  // M >= 1: multi-interval masks (lts / lte hold FMS / FME, (M, B, N_kv))
 
 // Main kernel of the d = 256 backward (fm_bwd256.cu); row terms, launch
 // order and dQ conversion come from launch_bwd.
@@ -81,7 +84,7 @@ cudaError_t launch_bwd256_main(const fm_problem& P, const void* q, const void* k
                                const int32_t* lts, const int32_t* lte, const int32_t* uts, const int32_t* ute,
                                const int32_t* k_off, const int32_t* k_queue, const int32_t* order, const float* nl,
                                const float* dsum, float* dq_acc, void* dk, void* dv, cudaStream_t s, int* err,
-                               int mode = 0, int M = 1);  // mode: 0 shared, 1 per-head, 2 multi-interval vectors
+                               int mode = 0, int M = 0);  // mode: 0 shared, 1 per-head, 2 multi-interval masks
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

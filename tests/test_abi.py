@@ -283,9 +283,9 @@ def test_binding_checks_per_head_shapes(lib):
 
 
 def test_binding_checks_multi_interval_shapes(lib):
-    # multi-interval entry points: vectors are (M, B, N_kv), the queues have
-    # M * B rows per Q (K) block; anything else is refused before any pointer
-    # reaches the library
+    # multi-interval entry points: FMS / FME are (M, B, N_kv) and the queues
+    # (from fm_classify_tiles_multi) have B rows per Q (K) block; anything
+    # else is refused before any pointer reaches the library
     import torch
 
     bf, i32 = torch.bfloat16, torch.int32
@@ -293,8 +293,8 @@ def test_binding_checks_multi_interval_shapes(lib):
     q = torch.zeros(B, Hq, N, d, dtype=bf)
     k = torch.zeros(B, Hkv, N, d, dtype=bf)
     lse = torch.zeros(B, Hq, N, dtype=torch.float32)
-    shared = [torch.zeros(B, N, dtype=i32) for _ in range(4)]
-    multi = [torch.zeros(M, B, N, dtype=i32) for _ in range(4)]
+    flat = torch.zeros(B, N, dtype=i32)
+    fms = torch.zeros(M, B, N, dtype=i32)
     nq = N // 128
 
     def queues(rows):
@@ -303,34 +303,43 @@ def test_binding_checks_multi_interval_shapes(lib):
                              torch.zeros(rows * nq * nq, dtype=i32), 128, 128)
 
     with pytest.raises(ValueError, match=r"\(M, B, N_kv\)"):
-        fm.fm_attn_fwd_multi(q, k, k, *shared, queues(M * B), scale=0.1, causal=False)
+        fm.fm_attn_fwd_multi(q, k, k, flat, flat, queues(B), scale=0.1, causal=False)
+    with pytest.raises(ValueError, match="one shape"):
+        fm.fm_attn_fwd_multi(q, k, k, fms, fms[:2], queues(B), scale=0.1, causal=False)
     with pytest.raises(ValueError, match="queue offsets"):
-        fm.fm_attn_fwd_multi(q, k, k, *multi, queues(B), scale=0.1, causal=False)
+        fm.fm_attn_fwd_multi(q, k, k, fms, fms, queues(M * B), scale=0.1, causal=False)
     with pytest.raises(ValueError, match="queue offsets"):
-        fm.fm_attn_bwd_multi(q, k, k, q, lse, q, *multi, queues(B), scale=0.1, causal=False)
-    with pytest.raises(ValueError, match="shape"):
-        fm.fm_attn_bwd_multi(q, k, k, q, lse, q, multi[0], multi[1], multi[2], multi[3][:2], queues(M * B),
-                             scale=0.1, causal=False)
+        fm.fm_attn_bwd_multi(q, k, k, q, lse, q, fms, fms, queues(M * B), scale=0.1, causal=False)
+    with pytest.raises(ValueError, match=r"\(M, B, N_kv\)"):
+        fm.fm_classify_tiles_multi(flat, flat, causal=False)
     with pytest.raises(ValueError, match="CUDA tensor"):
-        fm.fm_attn_fwd_multi(q, k, k, *multi, queues(M * B), scale=0.1, causal=False)
+        fm.fm_attn_fwd_multi(q, k, k, fms, fms, queues(B), scale=0.1, causal=False)
     with pytest.raises(ValueError, match="CUDA tensor"):
-        fm.fm_attn_bwd_multi(q, k, k, q, lse, q, *multi, queues(M * B), scale=0.1, causal=False)
+        fm.fm_attn_bwd_multi(q, k, k, q, lse, q, fms, fms, queues(B), scale=0.1, causal=False)
 
 
 def test_multi_interval_entry_points_validate_before_any_launch(lib):
     # 1 <= M <= 4 intervals, then the usual checks, all before any launch
     nul = ctypes.c_void_p(0)
-    args = [nul] * 11 + [nul, ctypes.c_size_t(0), nul]
-    bargs = [nul] * 15 + [nul, ctypes.c_size_t(0), nul]
+    args = [nul] * 9 + [nul, ctypes.c_size_t(0), nul]
+    bargs = [nul] * 13 + [nul, ctypes.c_size_t(0), nul]
+    cargs = [nul] * 7 + [nul, ctypes.c_size_t(0), nul]
+    til = fm.fm_tiling(128, 128)
     p = fm._problem(1, 4, 2, 256, 128, 0.1, 0)
     for M, want in ((0, fm.FM_ERR_INVALID_ARG), (5, fm.FM_ERR_INVALID_ARG), (2, fm.FM_ERR_INVALID_ARG)):
         assert lib.fm_attn_fwd_multi(ctypes.byref(p), M, *args) == want
         assert lib.fm_attn_bwd_multi(ctypes.byref(p), M, *bargs) == want
+        assert lib.fm_classify_tiles_multi(ctypes.byref(p), ctypes.byref(til), M, *cargs) == want
     q = fm._problem(1, 4, 2, 256, 96, 0.1, 0)
     assert lib.fm_attn_fwd_multi(ctypes.byref(q), 2, *args) == fm.FM_ERR_UNSUPPORTED
     e = fm._problem(0, 4, 2, 256, 128, 0.1, 0)
     assert lib.fm_attn_fwd_multi(ctypes.byref(e), 2, *args) == fm.FM_OK
     assert lib.fm_attn_bwd_multi(ctypes.byref(e), 9, *bargs) == fm.FM_ERR_INVALID_ARG
+    # the classification workspace grows with the intervals
+    a = fm._problem(1, 1, 1, 4096, 128, 0.1, 0)
+    w1 = lib.fm_classify_multi_workspace_bytes(ctypes.byref(a), ctypes.byref(til), 1)
+    w4 = lib.fm_classify_multi_workspace_bytes(ctypes.byref(a), ctypes.byref(til), 4)
+    assert 0 < w1 < w4 and lib.fm_classify_multi_workspace_bytes(ctypes.byref(a), ctypes.byref(til), 5) == 0
 
 
 def test_per_head_entry_points_validate_before_any_launch(lib):

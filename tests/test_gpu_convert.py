@@ -115,10 +115,9 @@ def test_merge_and_sum_of_one_part_are_identities():
 
 @pytest.mark.parametrize("d", [128, 256])
 def test_multi_interval_entry_points_with_causal(d):
-    # fm_attn_fwd_multi / fm_attn_bwd_multi called directly with the causal
-    # flag: the causal term masks i < j on top of the intervals (the oracle
-    # applies it the same way), in the kernels' masking and the causal
-    # classification in multi mode
+    # fm_classify_tiles_multi / fm_attn_fwd_multi / fm_attn_bwd_multi called
+    # directly with the causal flag: the causal term masks i < j on top of the
+    # intervals (the oracle applies it the same way)
     rng = np.random.default_rng(d + 3)
     M, B, hq, hkv, n = 3, 2, 4, 2, 700
     fms, fme = disjoint_intervals(rng, M, B, n, n)
@@ -128,12 +127,10 @@ def test_multi_interval_entry_points_with_causal(d):
     do = tensors.randn_bf16((B, hq, n, d), 53)
     scale = d ** -0.5
     qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
-    vec = fm.fm_from_fms_fme(torch.from_numpy(fms.reshape(M * B, n)).cuda(),
-                             torch.from_numpy(fme.reshape(M * B, n)).cuda(), n_rows=n)
-    qs = fm.fm_classify_tiles(*vec, causal=True, n_rows=n)
-    vec = tuple(x.view(M, B, n) for x in vec)
-    o, lse = fm.fm_attn_fwd_multi(qd, kd, vd, *vec, qs, scale=scale, causal=True)
-    dq, dk, dv = fm.fm_attn_bwd_multi(qd, kd, vd, o, lse, dod, *vec, qs, scale=scale, causal=True)
+    fms_t, fme_t = torch.from_numpy(fms).cuda(), torch.from_numpy(fme).cuda()
+    qs = fm.fm_classify_tiles_multi(fms_t, fme_t, causal=True, n_rows=n)
+    o, lse = fm.fm_attn_fwd_multi(qd, kd, vd, fms_t, fme_t, qs, scale=scale, causal=True)
+    dq, dk, dv = fm.fm_attn_bwd_multi(qd, kd, vd, o, lse, dod, fms_t, fme_t, qs, scale=scale, causal=True)
     st, bits = fm.fm_device_status()
     assert st == fm.FM_OK, bits
     spec = {"fms": fms.transpose(1, 0, 2), "fme": fme.transpose(1, 0, 2)}
@@ -143,3 +140,53 @@ def test_multi_interval_entry_points_with_causal(d):
     ref = oracle.backward(f64(q), f64(k), f64(v), f64(do), spec, True, scale)
     for name, a, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         assert_grad(f64(a), r, name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("M,n,nk", [(1, 700, 700), (3, 1000, 640), (4, 389, 1300)])
+def test_multi_interval_classification_matches_oracle(M, n, nk, causal):
+    # union classes (the most visible of the intervals' own classes) and both
+    # queues, bit for bit, on overlapping, empty and out-of-range intervals
+    rng = np.random.default_rng(M * 31 + n + causal)
+    B = 2
+    fms = rng.integers(-3, n + 3, size=(M, B, nk)).astype(np.int32)
+    fme = rng.integers(-3, n + 3, size=(M, B, nk)).astype(np.int32)
+    qs = fm.fm_classify_tiles_multi(torch.from_numpy(fms).cuda(), torch.from_numpy(fme).cuda(), causal=causal,
+                                    n_rows=n)
+    st, bits = fm.fm_device_status()
+    assert st == fm.FM_OK, bits
+    cls_ref = [oracle.classify_tiles_multi(fms[:, b], fme[:, b], causal, 128, 128, n) for b in range(B)]
+    assert np.array_equal(qs.tile_class.cpu().numpy(), np.stack(cls_ref))
+    q_off, q_queue, k_off, k_queue = oracle.build_queues(cls_ref)
+    assert np.array_equal(qs.q_off.cpu().numpy(), q_off)
+    assert np.array_equal(qs.k_off.cpu().numpy(), k_off)
+    assert np.array_equal(qs.q_queue.cpu().numpy()[:len(q_queue)], q_queue)
+    assert np.array_equal(qs.k_queue.cpu().numpy()[:len(k_queue)], k_queue)
+
+
+@pytest.mark.parametrize("d,causal", [(128, False), (64, True), (256, False)])
+def test_multi_interval_overlapping_intervals(d, causal):
+    # overlapping visible intervals: a key is visible to the union of its
+    # intervals (each block computed once, masked by the union)
+    rng = np.random.default_rng(d + 7 + causal)
+    M, B, hq, hkv, n = 3, 2, 4, 2, 650
+    a = rng.integers(0, n, size=(M, B, n))
+    w = rng.integers(0, n // 2, size=(M, B, n))
+    fms, fme = a.astype(np.int32), np.minimum(a + w, n - 1).astype(np.int32)
+    q = tensors.randn_bf16((B, hq, n, d), 60)
+    k = tensors.randn_bf16((B, hkv, n, d), 61)
+    v = tensors.randn_bf16((B, hkv, n, d), 62)
+    do = tensors.randn_bf16((B, hq, n, d), 63)
+    scale = d ** -0.5
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    o, lse, dq, dk, dv = fm.fm_attn_multi_interval(qd, kd, vd, torch.from_numpy(fms).cuda(),
+                                                   torch.from_numpy(fme).cuda(), scale=scale, do=dod, causal=causal)
+    st, bits = fm.fm_device_status()
+    assert st == fm.FM_OK, bits
+    spec = {"fms": fms.transpose(1, 0, 2), "fme": fme.transpose(1, 0, 2)}
+    O_ref, L_ref = oracle.forward(f64(q), f64(k), f64(v), spec, causal, scale)
+    assert_out(f64(o), O_ref)
+    assert_lse(f64(lse), L_ref)
+    ref = oracle.backward(f64(q), f64(k), f64(v), f64(do), spec, causal, scale)
+    for name, a_, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert_grad(f64(a_), r, name)

@@ -144,15 +144,13 @@ def test_full_size_multi_interval():
     th = torch.as_tensor(hsel, device="cuda")
     qs_, dos_ = q[:, th].contiguous(), do[:, th].contiguous()
     ks_, vs_ = k[:, g0:g0 + 1].contiguous(), v[:, g0:g0 + 1].contiguous()
-    M = fms.shape[0]
-    vecs = fm.fm_from_fms_fme(torch.from_numpy(fms.reshape(M * B, N)).cuda(),
-                              torch.from_numpy(fme.reshape(M * B, N)).cuda(), n_rows=N)
-    queues = fm.fm_classify_tiles(*vecs, causal=False, n_rows=N)
+    queues = fm.fm_classify_tiles_multi(torch.from_numpy(fms).cuda(), torch.from_numpy(fme).cuda(), causal=False,
+                                        n_rows=N)
     o_s, lse_s, _, dk_s, dv_s = fm.fm_attn_multi_interval(qs_, ks_, vs_, torch.from_numpy(fms).cuda(),
                                                           torch.from_numpy(fme).cuda(), scale=scale, do=dos_)
     st, bits = fm.fm_device_status()
     assert st == fm.FM_OK, bits
-    cols, qlen = _heavy_columns(queues.k_off, M * B, N // 128, N)
+    cols, qlen = _heavy_columns(queues.k_off, B, N // 128, N)
     dK_ref, dV_ref = _key_grads(f64(qs_), f64(ks_), f64(vs_), f64(dos_), lambda h: spec, False, scale, cols)
     tc = torch.as_tensor(cols, device="cuda")
     assert_grad(f64(dk_s[:, :, tc]), dK_ref, f"dK[multi-interval, KV blocks with queues of {qlen.tolist()} units]")
