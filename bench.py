@@ -541,17 +541,17 @@ def run_ours(args, cfg):
 # the counters were taken from.
 NCU_TRAFFIC = {
     ("bwd", 128): {"file": "fm_bwd.cu", "workload": "share_question32k",
-                   "sha256": "73245c210bd0be54b1ace45439f6d6e243adf8dcc7f7d1095ed9df9c8fa7e19f",
-                   "bytes": 821163008 + 450144000, "tensor_pipe_pct": 58.7},
+                   "sha256": "824f3282e5614933667ea699834a760965a2640ae76accb792ca00a5e2362996",
+                   "bytes": 829447424 + 453304832, "tensor_pipe_pct": 58.7},
     ("fwd", 128): {"file": "fm_fwd.cu", "workload": "share_question32k",
-                   "sha256": "b9f0d800527407413cbca25c62e7cd789816e698eb14a174cdc81fe0b1b38f6e",
-                   "bytes": 264724224 + 217171456, "tensor_pipe_pct": 48.5},
+                   "sha256": "4040ce59adbbe21b39325abdf6cc31daf8528b9e585ec6552a6f3e66dba9012e",
+                   "bytes": 264953088 + 217447168, "tensor_pipe_pct": 49.0},
     ("bwd", 256): {"file": "fm_bwd256.cu", "workload": "share_question32k",
-                   "sha256": "971bbe54779f61bf4c61cee8831882c1d85f9b5e4221b6b431fe3f6fd014c241",
-                   "bytes": 2565421312 + 1441220352, "tensor_pipe_pct": 42.3},
+                   "sha256": "dbd8ae160afd3c741184e7392ad0148ad03699c0350e43aadde7c3ca34e635fb",
+                   "bytes": 2581412096 + 1447782656, "tensor_pipe_pct": 42.4},
     ("fwd", 256): {"file": "fm_fwd256.cu", "workload": "share_question32k",
-                   "sha256": "3c42dfd84385a921d86b6827f7d3355ff4cc84ad2f7ab9d85c34a378fbd7e3f3",
-                   "bytes": 527602432 + 485378560, "tensor_pipe_pct": 48.5},
+                   "sha256": "71ab4c88fb6acd020ddeb475281b3e54728b30d45cfd40afa4b02a118de1a185",
+                   "bytes": 527862272 + 485001984, "tensor_pipe_pct": 48.6},
 }
 
 
