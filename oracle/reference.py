@@ -21,7 +21,9 @@ slow and written straight from the definitions:
 * the FlashMask Guide's FMS / FME vectors (one inclusive visible interval per
   key column) map onto the four vectors as the complement of that interval;
   its multi-interval masks (up to M visible intervals per key column) are
-  evaluated directly (`multi_masked_rows`).
+  evaluated directly (`multi_masked_rows`), and their tiles are classified on
+  each column's visible set written as its maximal runs of rows
+  (`union_runs`).
 
 Readings where the pages are silent (pinned by tests/test_oracle.py,
 tests/test_cp_oracle.py and tests/test_convert_oracle.py):
@@ -171,19 +173,50 @@ def classify_tiles(lts, lte, uts, ute, causal: bool, bm: int, bn: int, n_rows=No
     return cls
 
 
+def union_runs(fms, fme, n_rows: int):
+    """Each key column's visible rows under a multi-interval mask (fms, fme:
+    (M, N_kv), rows FMS^(m)_j <= i <= FME^(m)_j for some m, within [0, n_rows))
+    as that set's maximal runs of consecutive rows, ascending, run k in slot k:
+    (starts, ends), both (M, N_kv) inclusive; a slot past the column's last run
+    is empty (start 0, end -1). Intervals are clipped to the rows, empty ones
+    dropped, the rest taken in order of their start and joined where one
+    overlaps or touches the run before it."""
+    fms = np.asarray(fms, dtype=np.int64)
+    fme = np.asarray(fme, dtype=np.int64)
+    M, nk = fms.shape
+    starts = np.zeros((M, nk), dtype=np.int64)
+    ends = np.full((M, nk), -1, dtype=np.int64)
+    for j in range(nk):
+        pieces = []
+        for m in range(M):
+            a, b = max(int(fms[m, j]), 0), min(int(fme[m, j]), n_rows - 1)
+            if a <= b:
+                pieces.append((a, b))
+        runs = []
+        for a, b in sorted(pieces):
+            if runs and a <= runs[-1][1] + 1:
+                runs[-1][1] = max(runs[-1][1], b)
+            else:
+                runs.append([a, b])
+        for k, (a, b) in enumerate(runs):
+            starts[k, j], ends[k, j] = a, b
+    return starts, ends
+
+
 def classify_tiles_multi(fms, fme, causal: bool, bm: int, bn: int, n_rows: int) -> np.ndarray:
     """Tile classes of a multi-interval mask for one batch entry (fms, fme:
     (M, N_kv), key j visible to rows FMS^(m)_j <= i <= FME^(m)_j for some m,
-    plus i >= j when causal): the most visible of the intervals' own classes,
-    each from `classify_tiles` on the interval's masked complement
-    (`from_fms_fme`) with the causal term. A tile is skipped iff every
-    interval skips it (no interval reaches it), unmasked iff one interval
-    alone leaves it unmasked, partial otherwise (class codes 0 < 1 < 2, so
-    the most visible is the maximum)."""
-    fms = np.asarray(fms)
-    fme = np.asarray(fme)
-    cls = [classify_tiles(*from_fms_fme(fms[m], fme[m], n_rows), causal, bm, bn, n_rows=n_rows)
-           for m in range(fms.shape[0])]
+    plus i >= j when causal). The visible set of every column is first
+    rewritten as its runs (`union_runs`: the same mask, overlapping or
+    touching intervals joined); a tile's class is then the most visible of the
+    run slots' own classes, each from `classify_tiles` on the slot's masked
+    complement (`from_fms_fme`) with the causal term. A tile is skipped iff
+    every slot skips it, unmasked iff one slot alone leaves it unmasked,
+    partial otherwise (class codes 0 < 1 < 2, so the most visible is the
+    maximum)."""
+    starts, ends = union_runs(fms, fme, n_rows)
+    cls = [classify_tiles(*from_fms_fme(starts[m], ends[m], n_rows), causal, bm, bn, n_rows=n_rows)
+           for m in range(starts.shape[0])]
     return np.maximum.reduce(cls)
 
 

@@ -118,6 +118,48 @@ def test_multi_interval_tile_rule_is_sound_and_exact_at_1x1(causal):
                                                       n_rows=30))
 
 
+def test_union_runs_are_the_maximal_runs_of_the_visible_rows():
+    # brute force: the runs cover exactly the rows some interval holds (within
+    # [0, n)), are ascending with a gap of at least one row between them (so
+    # maximal), and fill the first slots; empty, reversed, out-of-range,
+    # overlapping and touching intervals all occur
+    rng = np.random.default_rng(21)
+    for n, nk, M in ((17, 40, 2), (30, 60, 3), (12, 50, 4), (1, 9, 3)):
+        fms = rng.integers(-3, n + 3, size=(M, nk))
+        fme = rng.integers(-3, n + 3, size=(M, nk))
+        starts, ends = oracle.union_runs(fms, fme, n)
+        for j in range(nk):
+            want = {i for m in range(M) for i in range(n) if fms[m, j] <= i <= fme[m, j]}
+            runs = [(int(a), int(b)) for a, b in zip(starts[:, j], ends[:, j]) if a <= b]
+            assert all(a >= b + 2 for (_, b), (a, _) in zip(runs, runs[1:]))
+            assert [int(a) <= int(b) for a, b in zip(starts[:, j], ends[:, j])] == [True] * len(runs) + [False] * (
+                M - len(runs))
+            assert {i for a, b in runs for i in range(a, b + 1)} == want
+    # two touching pieces are one run; so are nested ones
+    starts, ends = oracle.union_runs(np.array([[4], [0]]), np.array([[9], [3]]), 20)
+    assert (starts[:, 0].tolist(), ends[:, 0].tolist()) == ([0, 0], [9, -1])
+    starts, ends = oracle.union_runs(np.array([[2], [5]]), np.array([[15], [7]]), 20)
+    assert (starts[:, 0].tolist(), ends[:, 0].tolist()) == ([2, 0], [15, -1])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_multi_interval_classes_do_not_depend_on_how_the_union_is_cut(causal):
+    # the tile classes are a function of the mask: a column's single visible
+    # interval cut into touching or overlapping pieces, in any slot order,
+    # classifies exactly like the interval itself
+    rng = np.random.default_rng(31 + causal)
+    n = 96
+    a = rng.integers(0, n, size=n)
+    b = np.minimum(a + rng.integers(0, n, size=n), n - 1)
+    one = oracle.classify_tiles(*oracle.from_fms_fme(a, b, n), causal, 16, 16, n_rows=n)
+    cut = a + (b - a) // 3
+    over = np.minimum(cut + 4, b)
+    for fms, fme in ((np.stack([a, cut + 1]), np.stack([cut, b])),           # touching halves
+                     (np.stack([cut + 1, a]), np.stack([b, cut])),           # swapped slots
+                     (np.stack([a, a, cut]), np.stack([over, b, b]))):       # overlapping, nested
+        assert np.array_equal(oracle.classify_tiles_multi(fms, fme, causal, 16, 16, n), one)
+
+
 def test_multi_interval_attention_is_the_lse_merge_of_its_parts():
     # With disjoint intervals per column, a row's visible keys split into
     # disjoint sets, one per interval: the attention over their union is the
