@@ -177,14 +177,18 @@ def union_runs(fms, fme, n_rows: int):
     """Each key column's visible rows under a multi-interval mask (fms, fme:
     (M, N_kv), rows FMS^(m)_j <= i <= FME^(m)_j for some m, within [0, n_rows))
     as that set's maximal runs of consecutive rows, ascending, run k in slot k:
-    (starts, ends), both (M, N_kv) inclusive; a slot past the column's last run
-    is empty (start 0, end -1). Intervals are clipped to the rows, empty ones
-    dropped, the rest taken in order of their start and joined where one
-    overlaps or touches the run before it."""
+    (starts, ends), both (M, N_kv) inclusive. A slot past the column's last run
+    is empty, written start = n_rows, end = -1: its masked complement then has
+    its upper interval reaching the last row and its lower one starting at row
+    0, so in a tile's block bounds it neither lowers the smallest upper end nor
+    raises the largest lower start of the live columns (it masks every row
+    either way). Intervals are clipped to the rows, empty ones dropped, the
+    rest taken in order of their start and joined where one overlaps or
+    touches the run before it."""
     fms = np.asarray(fms, dtype=np.int64)
     fme = np.asarray(fme, dtype=np.int64)
     M, nk = fms.shape
-    starts = np.zeros((M, nk), dtype=np.int64)
+    starts = np.full((M, nk), n_rows, dtype=np.int64)
     ends = np.full((M, nk), -1, dtype=np.int64)
     for j in range(nk):
         pieces = []

@@ -137,9 +137,9 @@ def test_union_runs_are_the_maximal_runs_of_the_visible_rows():
             assert {i for a, b in runs for i in range(a, b + 1)} == want
     # two touching pieces are one run; so are nested ones
     starts, ends = oracle.union_runs(np.array([[4], [0]]), np.array([[9], [3]]), 20)
-    assert (starts[:, 0].tolist(), ends[:, 0].tolist()) == ([0, 0], [9, -1])
+    assert (starts[:, 0].tolist(), ends[:, 0].tolist()) == ([0, 20], [9, -1])
     starts, ends = oracle.union_runs(np.array([[2], [5]]), np.array([[15], [7]]), 20)
-    assert (starts[:, 0].tolist(), ends[:, 0].tolist()) == ([2, 0], [15, -1])
+    assert (starts[:, 0].tolist(), ends[:, 0].tolist()) == ([2, 20], [15, -1])
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -158,6 +158,32 @@ def test_multi_interval_classes_do_not_depend_on_how_the_union_is_cut(causal):
                      (np.stack([cut + 1, a]), np.stack([b, cut])),           # swapped slots
                      (np.stack([a, a, cut]), np.stack([over, b, b]))):       # overlapping, nested
         assert np.array_equal(oracle.classify_tiles_multi(fms, fme, causal, 16, 16, n), one)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_multi_interval_tile_that_no_run_reaches_is_skipped(causal):
+    # blocks whose columns hold one run each (cut into pieces) or none (fully
+    # masked columns mixed in): a tile wholly above every live run of its
+    # block, or wholly below, has no visible element and must be skipped
+    rng = np.random.default_rng(41 + causal)
+    n, nk, bm, bn = 64, 64, 8, 8
+    for _ in range(20):
+        a = rng.integers(0, n, size=nk)
+        b = np.minimum(a + rng.integers(0, 24, size=nk), n - 1)
+        dead = rng.random(nk) < 0.3
+        a, b = np.where(dead, 5, a), np.where(dead, 2, b)          # empty interval
+        cut = a + (b - a) // 2
+        fms, fme = np.stack([a, cut + 1]), np.stack([cut, b])
+        cls = oracle.classify_tiles_multi(fms, fme, causal, bm, bn, n)
+        dense = reference._mask_rows({"fms": fms[None], "fme": fme[None]}, causal, 0, np.arange(n))
+        for kb in range(nk // bn):
+            live = ~dead[kb * bn:(kb + 1) * bn]
+            lo = a[kb * bn:(kb + 1) * bn][live].min() if live.any() else n
+            hi = b[kb * bn:(kb + 1) * bn][live].max() if live.any() else -1
+            for qb in range(n // bm):
+                if (qb + 1) * bm <= lo or qb * bm > hi:
+                    assert dense[qb * bm:(qb + 1) * bm, kb * bn:(kb + 1) * bn].all()
+                    assert cls[qb, kb] == 0, (qb, kb)
 
 
 def test_multi_interval_attention_is_the_lse_merge_of_its_parts():
