@@ -219,12 +219,15 @@ fm_status fm_attn_bwd_heads(const fm_problem* p, const void* q, const void* k, c
  * intervals may overlap), and, with causal set, i >= j. fms, fme are
  * (M, B, N_kv) int32 device arrays, 1 <= M <= 4.
  *
- * fm_classify_tiles_multi gives every tile the most visible of the intervals'
- * own classes (the rule of fm_classify_tiles on each interval's masked
- * complement, [0, FMS) and (FME, N), with the causal term): skipped iff no
- * interval reaches the tile, unmasked iff one interval alone covers it,
- * partial otherwise; its outputs have the layout of fm_classify_tiles for B
- * batch entries. Workspace: fm_classify_multi_workspace_bytes.
+ * fm_classify_tiles_multi first rewrites each column's visible rows as their
+ * maximal runs (intervals clipped to [0, N), sorted by start, joined where
+ * they overlap or touch; run k in slot k, the other slots empty, written
+ * start N and end -1), so the classes depend on the mask only, then gives
+ * every tile the most visible of the slots' own classes (the rule of fm_classify_tiles on each slot's masked
+ * complement, [0, start) and (end, N), with the causal term): skipped iff no
+ * run reaches the tile, unmasked iff one run alone covers it, partial
+ * otherwise; its outputs have the layout of fm_classify_tiles for B batch
+ * entries. Workspace: fm_classify_multi_workspace_bytes.
  *
  * fm_attn_fwd_multi / fm_attn_bwd_multi are fm_attn_fwd / fm_attn_bwd with
  * these queues: each queued block is computed once, its partial tiles masked

@@ -49,9 +49,9 @@
 // MN-major B operand of dQ^T.
 // Mask forms (the MODE instantiations): shared vectors, one queue per KV
 // block walked for every head of the group; per-head vectors, each head's own
-// queue; multi-interval masks, each interval's queue walked for every head,
-// the compute warps reloading their key column's intervals when the head /
-// interval changes. dK, dV and dQ accumulate over all of them.
+// queue; multi-interval masks, the union classification's one queue per KV
+// block, the compute warps holding their key column's FMS / FME of every
+// interval. dK, dV and dQ accumulate over all of them.
 #include <climits>
 #include <cmath>
 #include <cuda.h>
@@ -119,7 +119,7 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int B, H_q, H_kv, N, Nk, Npad, nK, G, causal;  // N query rows (Npad rounded up to the tile), Nk key rows
-  int M;  // multi-interval masks: vectors (M, B, N_kv), queues over M * B rows (1 otherwise)
+  int M;  // multi-interval masks: FMS / FME (M, B, N_kv) (1 otherwise)
   float scale, scale_log2;
   int* err;
 };
@@ -131,7 +131,7 @@ constexpr int kMaxHeads = 64;
 // The CTA's queue segment is staged in shared memory (s_queue) when it fits,
 // so no role waits on a dependent global load per unit.
 struct Unit {
-  int h, qb, half, part, m;  // m: the interval of a multi-interval mask
+  int h, qb, half, part;
 };
 __device__ __forceinline__ Unit decode_unit(const BwdParams& p, int u, int L, int kbeg, int g, bool force_part,
                                             uint32_t s_queue, int qcap) {
@@ -144,7 +144,6 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams& p, int u, int L, in
   r.qb = e >> 1;
   r.half = rem & 1;
   r.part = (e & 1) | (force_part ? 1 : 0);
-  r.m = 0;
   return r;
 }
 
@@ -163,7 +162,6 @@ __device__ __forceinline__ Unit decode_unit_ph(const BwdParams& p, int u, int g,
   r.qb = e >> 1;
   r.half = rem & 1;
   r.part = (e & 1) | (force_part ? 1 : 0);
-  r.m = 0;
   return r;
 }
 
@@ -191,7 +189,7 @@ __global__ void __launch_bounds__(480, 1)
   const int bk = p.order ? p.order[oi] : oi;
   const int nK = p.nK;
   const int b = bk / nK, kb = bk - b * nK;
-  int kbeg = 0, L = 0;  // per-head / multi-interval masks: L sums the heads' / intervals' queue lengths
+  int kbeg = 0, L = 0;  // per-head masks: L sums the heads' queue lengths
   if constexpr (PH) {
     for (int hi = 0; hi < p.G; ++hi) {
       const int r = (b * p.H_q + g * p.G + hi) * nK + kb;

@@ -101,7 +101,7 @@ struct Bwd256Params {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int B, H_q, H_kv, N, Nk, Npad, nK, G, causal;
-  int M;  // multi-interval masks: vectors (M, B, N_kv), queues over M * B rows (1 otherwise)
+  int M;  // multi-interval masks: FMS / FME (M, B, N_kv) (1 otherwise)
   float scale, scale_log2;
   int* err;
 };
@@ -110,7 +110,7 @@ struct Bwd256Params {
 constexpr int kMaxHeads256 = 64;
 
 struct Unit256 {
-  int h, qb, half, part, m;  // m: the interval of a multi-interval mask
+  int h, qb, half, part;
 };
 __device__ __forceinline__ Unit256 decode256(const Bwd256Params& p, int u, int L, int kbeg, int g, bool force_part,
                                              uint32_t s_queue) {
@@ -123,7 +123,6 @@ __device__ __forceinline__ Unit256 decode256(const Bwd256Params& p, int u, int L
   r.qb = e >> 1;
   r.half = rem & 1;
   r.part = (e & 1) | (force_part ? 1 : 0);
-  r.m = 0;
   return r;
 }
 // The same with per-head mask vectors: head hi of the group owns the units
@@ -143,7 +142,6 @@ __device__ __forceinline__ Unit256 decode256_ph(const Bwd256Params& p, int u, in
   r.qb = e >> 1;
   r.half = rem & 1;
   r.part = (e & 1) | (force_part ? 1 : 0);
-  r.m = 0;
   return r;
 }
 // MODE 0: mask vectors (B, N_kv) shared by the heads; 1: per-head vectors
@@ -174,7 +172,7 @@ __global__ void __launch_bounds__(448, 1)
   const int bk = p.order ? p.order[oi] : oi;
   const int nK = p.nK;
   const int b = bk / nK, kb = bk - b * nK;
-  int kbeg = 0, L = 0;  // per-head / multi-interval masks: L sums the heads' / intervals' queue lengths
+  int kbeg = 0, L = 0;  // per-head masks: L sums the heads' queue lengths
   if constexpr (PH) {
     for (int hi = 0; hi < p.G; ++hi) {
       const int r = (b * p.H_q + g * p.G + hi) * nK + kb;

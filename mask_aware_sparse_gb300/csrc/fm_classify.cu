@@ -202,8 +202,8 @@ __global__ void emit_queues_kernel(const uint8_t* __restrict__ cls, int B, int n
   }
 }
 
-// Multi-interval masks: the class of a tile is the most visible of the
-// intervals' own classes (skip < partial < unmasked), one CTA per (b, qb):
+// Multi-interval masks: the class of a tile is the most visible of the run
+// slots' own classes (skip < partial < unmasked), one CTA per (b, qb):
 // the row's classes, its count of non-skipped tiles and, by integer atomics,
 // each column's (zeroed by the caller).
 __global__ void union_classes_kernel(const uint8_t* __restrict__ cls_m, int M, int B, int nQ, int nK,
@@ -234,6 +234,56 @@ __global__ void union_classes_kernel(const uint8_t* __restrict__ cls_m, int M, i
   }
 }
 
+// Multi-interval masks: each key column's visible rows (the union of its M
+// inclusive intervals [FMS, FME] within [0, n)) rewritten as their maximal
+// runs, ascending, run k in slot k, and each slot's masked complement written
+// as the four vectors of vector row (k * B + b): UTS = 0, UTE = start,
+// LTS = end + 1, LTE = n. A slot past the last run is empty, start n and
+// end -1 (UTE = n, LTS = 0: the whole column masked, without lowering the
+// block's smallest UTE or raising its largest LTS). One thread per
+// (b, column); the intervals are clipped, sorted by start and joined where
+// one overlaps or touches the run before it, so the classes depend only on
+// the mask.
+__global__ void union_runs_kernel(const int32_t* __restrict__ fms, const int32_t* __restrict__ fme, int M, int B,
+                                  int Nk, int n, int32_t* __restrict__ lts, int32_t* __restrict__ lte,
+                                  int32_t* __restrict__ uts, int32_t* __restrict__ ute) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= (long long)B * Nk) return;
+  const int b = (int)(t / Nk), j = (int)(t - (long long)b * Nk);
+  int rs[4], re[4], cnt = 0;
+  for (int m = 0; m < M; ++m) {
+    const size_t vi = ((size_t)m * B + b) * Nk + j;
+    const int a = max(fms[vi], 0), e = min(fme[vi], n - 1);
+    if (a > e) continue;
+    int k = cnt++;  // insertion by start
+    while (k > 0 && rs[k - 1] > a) {
+      rs[k] = rs[k - 1];
+      re[k] = re[k - 1];
+      --k;
+    }
+    rs[k] = a;
+    re[k] = e;
+  }
+  int runs = 0;
+  for (int k = 0; k < cnt; ++k) {
+    if (runs > 0 && rs[k] <= re[runs - 1] + 1) {
+      re[runs - 1] = max(re[runs - 1], re[k]);
+    } else {
+      rs[runs] = rs[k];
+      re[runs] = re[k];
+      ++runs;
+    }
+  }
+  for (int k = 0; k < M; ++k) {
+    const size_t vo = ((size_t)k * B + b) * Nk + j;
+    const bool live = k < runs;
+    lts[vo] = live ? re[k] + 1 : 0;
+    lte[vo] = n;
+    uts[vo] = 0;
+    ute[vo] = live ? rs[k] : n;
+  }
+}
+
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
@@ -242,8 +292,8 @@ size_t classify_ws_bytes(int B, int nQ, int nK) {
   return align256(sizeof(Minmax) * (size_t)B * nK) + align256(4 * (size_t)B * nQ) + align256(4 * (size_t)B * nK);
 }
 
-// Multi-interval masks: the intervals' complements (M * B vector rows, the
-// FMS / FME conversion), their classes, the union classes and the queues.
+// Multi-interval masks: the run slots' complements (M * B vector rows), their
+// classes, the union classes and the queues.
 size_t classify_multi_ws_bytes(int M, int B, int nQ, int nK, int Nk) {
   const size_t R = (size_t)M * B;
   return 4 * align256(4 * R * Nk) + classify_ws_bytes((int)R, nQ, nK) + align256(R * nQ * nK) +
@@ -270,8 +320,9 @@ cudaError_t launch_classify_multi(const fm_problem& p, int M, int bm, int bn, in
   int32_t* row_cnt = reinterpret_cast<int32_t*>(wu);
   wu += align256(4 * (size_t)B * nQ);
   int32_t* col_cnt = reinterpret_cast<int32_t*>(wu);
-  cudaError_t e = launch_from_fms_fme(fms, fme, (int64_t)(R * Nk), p.N, vec[0], vec[1], vec[2], vec[3], s);
-  if (e != cudaSuccess) return e;
+  const long long cols = (long long)B * Nk;
+  union_runs_kernel<<<(unsigned)((cols + 255) / 256), 256, 0, s>>>(fms, fme, M, B, Nk, p.N, vec[0], vec[1], vec[2],
+                                                                   vec[3]);
   fm_problem pm = p;
   pm.B = (int32_t)R;
   uint8_t* wm = static_cast<uint8_t*>(ws_m);
@@ -284,14 +335,14 @@ cudaError_t launch_classify_multi(const fm_problem& p, int M, int bm, int bn, in
                                                                    bn, nK, mm, col_cnt_m, err);
   classify_rows_kernel<<<dim3(nQ, (unsigned)R), 256, 0, s>>>(mm, p.N, Nk, bm, bn, nQ, nK, p.causal, cls_m,
                                                              row_cnt_m, col_cnt_m);
-  e = cudaMemsetAsync(col_cnt, 0, 4 * (size_t)B * nK, s);
+  cudaError_t e = cudaMemsetAsync(col_cnt, 0, 4 * (size_t)B * nK, s);
   if (e != cudaSuccess) return e;
   union_classes_kernel<<<dim3(nQ, B), 256, 0, s>>>(cls_m, M, B, nQ, nK, tile_class, row_cnt, col_cnt);
   const long long nkb = (long long)B * nK, nqb = (long long)B * nQ;
   scan_kernel<<<2, 1024, 0, s>>>(row_cnt, (int)nqb, q_off, col_cnt, (int)nkb, k_off);
   emit_queues_kernel<<<(unsigned)((nqb + nkb + 7) / 8), 256, 0, s>>>(tile_class, B, nQ, nK, q_off, q_queue, k_off,
                                                                      k_queue);
-  count_launches(5);  // minmax, classify rows, union, scan, emit (the conversion counts itself)
+  count_launches(6);  // runs, minmax, classify rows, union, scan, emit
   return cudaGetLastError();
 }
 

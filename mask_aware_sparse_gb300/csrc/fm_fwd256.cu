@@ -387,9 +387,12 @@ __global__ void __launch_bounds__(256, 1)
           if constexpr (MI) {
             // masked unless one interval [FMS, FME] holds the row
             uint32_t vis = 0u;
-            for (int mi = 0; mi < p.M; ++mi) {
-              const int f0 = lds_s32(sm + mi * 1024 + 4 * c), f1 = lds_s32(sm + mi * 1024 + 512 + 4 * c);
-              vis |= window_bits(f0, min(f1, p.N) + 1, w0);
+#pragma unroll
+            for (int mi = 0; mi < 4; ++mi) {
+              if (mi < p.M) {
+                const int f0 = lds_s32(sm + mi * 1024 + 4 * c), f1 = lds_s32(sm + mi * 1024 + 512 + 4 * c);
+                vis |= window_bits(f0, min(f1, p.N) + 1, w0);
+              }
             }
             colbits = ~vis | (causal ? window_bits(w0, kc0 + c, w0) : 0u);
           } else {

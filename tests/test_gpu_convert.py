@@ -145,7 +145,7 @@ def test_multi_interval_entry_points_with_causal(d):
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("M,n,nk", [(1, 700, 700), (3, 1000, 640), (4, 389, 1300)])
 def test_multi_interval_classification_matches_oracle(M, n, nk, causal):
-    # union classes (the most visible of the intervals' own classes) and both
+    # union classes (the most visible of the run slots' own classes) and both
     # queues, bit for bit, on overlapping, empty and out-of-range intervals
     rng = np.random.default_rng(M * 31 + n + causal)
     B = 2
@@ -162,6 +162,36 @@ def test_multi_interval_classification_matches_oracle(M, n, nk, causal):
     assert np.array_equal(qs.k_off.cpu().numpy(), k_off)
     assert np.array_equal(qs.q_queue.cpu().numpy()[:len(q_queue)], q_queue)
     assert np.array_equal(qs.k_queue.cpu().numpy()[:len(k_queue)], k_queue)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_multi_interval_classes_of_a_cut_interval(causal):
+    # one visible interval per column [j, L_j] (a causal-document-like mask)
+    # cut into touching, swapped and overlapping pieces: the kernel's classes
+    # and queues equal the oracle's, which equal the uncut interval's
+    rng = np.random.default_rng(77 + causal)
+    B, n = 2, 1500
+    j = np.arange(n)[None, :]
+    ends = np.minimum(j + rng.integers(0, 600, size=(B, 1)) + (j % 97), n - 1)
+    mid = (j + ends) // 2
+    one = [oracle.classify_tiles(*oracle.from_fms_fme(np.broadcast_to(j, (B, n))[b], ends[b], n), causal, 128, 128,
+                                 n_rows=n) for b in range(B)]
+    for fms, fme in ((np.stack([np.broadcast_to(j, (B, n)), mid + 1]), np.stack([mid, ends])),
+                     (np.stack([mid + 1, np.broadcast_to(j, (B, n))]), np.stack([ends, mid])),
+                     (np.stack([np.broadcast_to(j, (B, n)), np.maximum(mid - 5, j), mid]),
+                      np.stack([mid, ends, np.minimum(mid + 3, ends)]))):
+        fms, fme = np.ascontiguousarray(fms, np.int32), np.ascontiguousarray(fme, np.int32)
+        qs = fm.fm_classify_tiles_multi(torch.from_numpy(fms).cuda(), torch.from_numpy(fme).cuda(), causal=causal,
+                                        n_rows=n)
+        st, bits = fm.fm_device_status()
+        assert st == fm.FM_OK, bits
+        cls_ref = [oracle.classify_tiles_multi(fms[:, b], fme[:, b], causal, 128, 128, n) for b in range(B)]
+        assert all(np.array_equal(c, o) for c, o in zip(cls_ref, one))
+        assert np.array_equal(qs.tile_class.cpu().numpy(), np.stack(cls_ref))
+        q_off, q_queue, k_off, k_queue = oracle.build_queues(cls_ref)
+        assert np.array_equal(qs.q_off.cpu().numpy(), q_off)
+        assert np.array_equal(qs.q_queue.cpu().numpy()[:len(q_queue)], q_queue)
+        assert np.array_equal(qs.k_queue.cpu().numpy()[:len(k_queue)], k_queue)
 
 
 @pytest.mark.parametrize("d,causal", [(128, False), (64, True), (256, False)])
