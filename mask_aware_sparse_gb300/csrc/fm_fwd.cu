@@ -224,6 +224,14 @@ __global__ void __launch_bounds__(320, 1)
     }
     fence_mbar_init();
   }
+  if constexpr (MI) {
+    // the interval places past M of every mask slot hold an empty interval
+    // (FMS 1, FME 0) for the whole launch: the producer never writes them, and
+    // the softmax warps read two or four intervals without a per-interval test
+    int* mv = reinterpret_cast<int*>(smem + C::M_OFF);
+    for (int i = threadIdx.x; i < S * 1024; i += blockDim.x)
+      if (((i & 1023) >> 8) >= p.M) mv[i] = (i & 255) < 128 ? 1 : 0;
+  }
   if (warp == 9) tmem_alloc<512>(tmem_slot);
   if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tq);
@@ -667,12 +675,13 @@ __global__ void __launch_bounds__(320, 1)
             const int c = 32 * kq + lane;
             uint32_t colbits;
             if constexpr (MI) {
-              // masked unless one interval [FMS, FME] holds the row
-              uint32_t vis = 0u;
-              for (int mi = 0; mi < p.M; ++mi) {
+              // masked unless one interval [FMS, FME] holds the row (the
+              // places past M hold empty intervals)
+              auto iv = [&](int mi) -> uint32_t {
                 const int f0 = lds_s32(sm + mi * 1024 + 4 * c), f1 = lds_s32(sm + mi * 1024 + 512 + 4 * c);
-                vis |= window_bits(f0, min(f1, p.N) + 1, w0);
-              }
+                return window_bits(f0, min(f1, p.N) + 1, w0);
+              };
+              const uint32_t vis = (p.M <= 2) ? (iv(0) | iv(1)) : (iv(0) | iv(1) | iv(2) | iv(3));
               colbits = ~vis | (causal ? window_bits(w0, kc0 + c, w0) : 0u);
             } else {
               const int a0 = lds_s32(sm + 4 * c), a1 = lds_s32(sm + 512 + 4 * c);  // LTS, LTE of key column kc0 + c
