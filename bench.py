@@ -541,17 +541,17 @@ def run_ours(args, cfg):
 # the counters were taken from.
 NCU_TRAFFIC = {
     ("bwd", 128): {"file": "fm_bwd.cu", "workload": "share_question32k",
-                   "sha256": "824f3282e5614933667ea699834a760965a2640ae76accb792ca00a5e2362996",
-                   "bytes": 829447424 + 453304832, "tensor_pipe_pct": 58.7},
+                   "sha256": "b9838b53ff643061f94fb721f02c52b2658fee04ace7e22f4ddc1ebd63899894",
+                   "bytes": 826607360 + 450107392, "tensor_pipe_pct": 58.8},
     ("fwd", 128): {"file": "fm_fwd.cu", "workload": "share_question32k",
-                   "sha256": "4040ce59adbbe21b39325abdf6cc31daf8528b9e585ec6552a6f3e66dba9012e",
-                   "bytes": 264953088 + 217447168, "tensor_pipe_pct": 49.0},
+                   "sha256": "bd5dfdf503256e367b6c6cc8b760315ba7e2299dfdde74e014a5dd77b4ded650",
+                   "bytes": 265070080 + 217337088, "tensor_pipe_pct": 49.4},
     ("bwd", 256): {"file": "fm_bwd256.cu", "workload": "share_question32k",
-                   "sha256": "dbd8ae160afd3c741184e7392ad0148ad03699c0350e43aadde7c3ca34e635fb",
-                   "bytes": 2581412096 + 1447782656, "tensor_pipe_pct": 42.4},
+                   "sha256": "4a74f10607bb3fe9ddb3bce855a37e863781ea99a6210d9179ccd704351b296f",
+                   "bytes": 2578204928 + 1447225856, "tensor_pipe_pct": 42.3},
     ("fwd", 256): {"file": "fm_fwd256.cu", "workload": "share_question32k",
-                   "sha256": "71ab4c88fb6acd020ddeb475281b3e54728b30d45cfd40afa4b02a118de1a185",
-                   "bytes": 527862272 + 485001984, "tensor_pipe_pct": 48.6},
+                   "sha256": "43a49b7ecbde286dd8dc56ffcc166e1b7199fb9e19b95c5e838eeaa05480071a",
+                   "bytes": 527136512 + 485024256, "tensor_pipe_pct": 48.5},
 }
 
 
