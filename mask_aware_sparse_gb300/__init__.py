@@ -482,9 +482,10 @@ def fm_classify_tiles_multi(fms, fme, *, causal: bool, n_rows=None, block_m: int
                             stream=None):
     """Tile classes and queues of a multi-interval mask: fms, fme are
     (M, B, N_kv) int32 CUDA tensors (M <= 4), key j visible to rows
-    [fms[m, b, j], fme[m, b, j]] for some m. Every tile gets the most visible
-    of the intervals' own classes; the queues have the layout of
-    fm_classify_tiles for B batch entries."""
+    [fms[m, b, j], fme[m, b, j]] for some m. Each column's visible rows are
+    taken as their maximal runs (overlapping or touching intervals joined) and
+    every tile gets the most visible of the runs' own classes; the queues have
+    the layout of fm_classify_tiles for B batch entries."""
     _need(isinstance(fms, torch.Tensor) and fms.dim() == 3, "fms, fme must be (M, B, N_kv)")
     M, B, Nk = fms.shape
     for i, x in enumerate((fms, fme)):
