@@ -42,6 +42,13 @@
 //     from the queue offsets) for passes of a few waves, natural order for
 //     long passes, where units of neighbouring query blocks share K / V tiles
 //     in L2.
+//   * One-head units (per-head vectors, or one query head per kv head: the
+//     SINGLE instantiation): the second tile's S columns are a second S
+//     buffer; block k uses buffer k % 2, S(k) is issued ahead of PV(k - 1),
+//     so the next block's scores are computed while the softmax works on the
+//     current one, and the softmax arrives on PREADY[k % 2] (one barrier per
+//     buffer: the softmax may finish block k + 1 before PV(k) is issued, and
+//     a single barrier would then be two phases ahead of the MMA warp's wait).
 //   * Other mask forms: with per-head vectors a unit is one head with its own
 //     queue and vector row; with multi-interval masks (the MI instantiation)
 //     the queues are those of the union classification and a partial block's
@@ -182,7 +189,10 @@ __device__ __forceinline__ bool block_partial(const FwdParams& p, int e) {
 }
 
 // MI: multi-interval masks (mask slots hold FMS / FME of every interval).
-template <int D, bool F8, bool MI>
+// SINGLE: every unit has one query head (per-head masks, or one query head per
+// kv head): the second tile's S columns serve as a second S buffer, so S of a
+// unit's next block is computed while the softmax works on the current one.
+template <int D, bool F8, bool MI, bool SINGLE>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, const FwdParams p) {
@@ -457,10 +467,15 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t npv0 = 0u, npv1 = 0u;  // PV MMAs issued per head so far
       // PV of one block for head t: V from ring slot vs; the unit's first
       // block overwrites O instead of accumulating
-      auto issue_pv = [&](int t, uint32_t vs, bool first) -> bool {
-        if (!mbar_wait(&bars[C::B_PREADY + t], (t ? npv1 : npv0) & 1u, abort_flag, p.err)) return false;
+      auto issue_pv = [&](int t, uint32_t vs, bool first, int pb) -> bool {
+        // one-head units: one PREADY per S buffer (block k arrives on PREADY[k % 2],
+        // phase k / 2), so the softmax, which may finish block k + 1 before PV(k)
+        // is issued, is never two phases ahead of this wait
+        const uint32_t pr = SINGLE ? (uint32_t)pb : (uint32_t)t;
+        const uint32_t pph = SINGLE ? (npv0 >> 1) : (t ? npv1 : npv0);
+        if (!mbar_wait(&bars[C::B_PREADY + pr], pph & 1u, abort_flag, p.err)) return false;
         tc_fence_after();
-        const uint32_t tS = tbase + (uint32_t)(t * 128);
+        const uint32_t tS = tbase + (uint32_t)(pb * 128);  // P over S buffer pb
         const uint32_t tO = tbase + 256u + (uint32_t)(t * D);
         const uint64_t vd = dV0 + kTileStep * (uint64_t)vs;
         // k-steps of 16 bf16 (32 e4m3) keys: 8 TMEM columns of P, 16 (32) rows of V
@@ -491,8 +506,8 @@ __global__ void __launch_bounds__(320, 1)
         // The head loop below is written out (two heads known at compile
         // time): with a runtime head loop the issue ran measurably behind
         // the tensor core on long unmasked units.
-        auto issue_s = [&](int t, int slot) {
-          const uint32_t tS = tbase + (uint32_t)(t * 128);
+        auto issue_s = [&](int t, int slot, int sb) {
+          const uint32_t tS = tbase + (uint32_t)(sb * 128);  // into S buffer sb
           const uint64_t qd = dQ0 + kTileStep * (uint64_t)t, kd = dK0 + kTileStep * (uint64_t)slot;
           // k-steps of 32 bytes (16 bf16 / 32 e4m3), four per 128-byte swizzled row
 #pragma unroll
@@ -503,8 +518,40 @@ __global__ void __launch_bounds__(320, 1)
             else
               mma_ss(tS, qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&bars[C::B_SFULL + t]);
+          mma_commit(&bars[C::B_SFULL + sb]);
         };
+        if constexpr (SINGLE) {
+          // one head: S(j) goes to buffer jt % 2 ahead of PV(j - 1), which
+          // reads P(j - 1) from the other buffer. S(j) overwrites P(j - 2):
+          // it is issued only once PV(j - 2) has completed (ODONE, counted
+          // one completion at a time in pv_done)
+          for (int j = 0; j < n && ok; ++j) {
+            const int slot = jt % S;
+            ok = mbar_wait(&bars[C::B_KFULL + slot], (jt / S) & 1u, abort_flag, p.err);
+            tc_fence_after();
+            tc_fence_after();
+            if (!ok) break;
+            issue_s(0, slot, (int)(jt & 1u));
+            mma_commit(&bars[C::B_KEMPTY + slot]);
+            if (j == n - 1) mma_commit(&bars[C::B_QFREE]);
+            if (j > 0) {
+              ok = mbar_wait(&bars[C::B_VFULL + pslot], ((jt - 1) / S) & 1u, abort_flag, p.err);
+              tc_fence_after();
+              if (ok) ok = issue_pv(0, pslot, j == 1, (int)((jt - 1) & 1u));
+              if (ok) mma_commit(&bars[C::B_VEMPTY + pslot]);
+            }
+            pslot = slot;
+            ++jt;
+          }
+          if (!ok) break;
+          ok = mbar_wait(&bars[C::B_VFULL + pslot], ((jt - 1) / S) & 1u, abort_flag, p.err);
+          tc_fence_after();
+          if (ok) ok = issue_pv(0, pslot, n == 1, (int)((jt - 1) & 1u));
+          if (!ok) break;
+          mma_commit(&bars[C::B_VEMPTY + pslot]);
+          ++uq;
+          continue;
+        }
         for (int j = 0; j < n && ok; ++j) {
           const int slot = jt % S;
           ok = mbar_wait(&bars[C::B_KFULL + slot], (jt / S) & 1u, abort_flag, p.err);
@@ -514,11 +561,11 @@ __global__ void __launch_bounds__(320, 1)
             tc_fence_after();
           }
           if (!ok) break;
-          if (j > 0 && !issue_pv(0, pslot, j == 1)) { ok = false; break; }
-          issue_s(0, slot);
+          if (j > 0 && !issue_pv(0, pslot, j == 1, 0)) { ok = false; break; }
+          issue_s(0, slot, 0);
           if (T == 2) {
-            if (j > 0 && !issue_pv(1, pslot, j == 1)) { ok = false; break; }
-            issue_s(1, slot);
+            if (j > 0 && !issue_pv(1, pslot, j == 1, 1)) { ok = false; break; }
+            issue_s(1, slot, 1);
           }
           if (j > 0) mma_commit(&bars[C::B_VEMPTY + pslot]);
           mma_commit(&bars[C::B_KEMPTY + slot]);
@@ -531,7 +578,7 @@ __global__ void __launch_bounds__(320, 1)
         // warps' epilogue waits for it
         ok = mbar_wait(&bars[C::B_VFULL + pslot], ((jt - 1) / S) & 1u, abort_flag, p.err);
         tc_fence_after();
-        for (int t = 0; t < T && ok; ++t) ok = issue_pv(t, pslot, n == 1);
+        for (int t = 0; t < T && ok; ++t) ok = issue_pv(t, pslot, n == 1, t);
         if (!ok) break;
         mma_commit(&bars[C::B_VEMPTY + pslot]);
         ++uq;
@@ -542,7 +589,6 @@ __global__ void __launch_bounds__(320, 1)
     const int t = warp >> 2;
     const int row = ((warp & 3) << 5) + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS = tbase + lane_off + (uint32_t)(t * 128);
     const uint32_t tO = tbase + lane_off + 256u + (uint32_t)(t * D);
     const float sl2 = p.scale_log2;
     const bool causal = p.causal != 0;
@@ -695,9 +741,12 @@ __global__ void __launch_bounds__(320, 1)
           if (lane == 0) mbar_arrive_cnt(&bars[C::B_MEMPTY + ms], mrel);
           ++pidx;
         }
-        ok = __all_sync(kFull, mbar_wait(&bars[C::B_SFULL + t], jh & 1u, abort_flag, p.err));
+        // this block's S buffer (one-head units alternate both buffers)
+        const uint32_t sb = SINGLE ? (jh & 1u) : (uint32_t)t;
+        ok = __all_sync(kFull, mbar_wait(&bars[C::B_SFULL + sb], (SINGLE ? (jh >> 1) : jh) & 1u, abort_flag, p.err));
         if (!ok) break;
         tc_fence_after();
+        const uint32_t tS = tbase + lane_off + (sb << 7);
         uint32_t sr[128];
         {
           uint32_t(&r0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
@@ -802,11 +851,11 @@ __global__ void __launch_bounds__(320, 1)
           for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(&orow[c0]));
           tmem_ld_wait();
           tc_fence_before();
-          mbar_arrive(&bars[C::B_PREADY + t]);  // PV of this block may now overwrite O
+          mbar_arrive(&bars[C::B_PREADY + (SINGLE ? sb : (uint32_t)t)]);  // PV of this block may now overwrite O
           store_o(orow);
         } else {
           tc_fence_before();
-          mbar_arrive(&bars[C::B_PREADY + t]);
+          mbar_arrive(&bars[C::B_PREADY + (SINGLE ? sb : (uint32_t)t)]);
         }
         ++jh;
       }
@@ -834,7 +883,7 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 
-template <int D, bool F8, bool MI = false>
+template <int D, bool F8, bool MI = false, bool SINGLE = false>
 cudaError_t launch_fwd_d(const fm_problem& P, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, const FwdParams& prm, unsigned grid, cudaStream_t s) {
   using C = FwdCfg<D, F8, MI>;
@@ -842,13 +891,13 @@ cudaError_t launch_fwd_d(const fm_problem& P, const CUtensorMap& tq, const CUten
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e =
-        cudaFuncSetAttribute(fwd_kernel<D, F8, MI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        cudaFuncSetAttribute(fwd_kernel<D, F8, MI, SINGLE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   {
     KernelTimer timer(s, kTimedFwd);
-    fwd_kernel<D, F8, MI><<<grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, to, prm);
+    fwd_kernel<D, F8, MI, SINGLE><<<grid, 320, C::SMEM_ALLOC, s>>>(tq, tk, tv, to, prm);
   }
   count_launches(prm.order ? 2 : 1);  // [LPT order] + main kernel
   return cudaGetLastError();
@@ -958,6 +1007,16 @@ static cudaError_t launch_fwd_persistent(const fm_problem& P, const void* q, con
   prm.err = err;
   // persistent: one CTA per SM (the kernel's shared memory and TMEM fill an SM)
   const unsigned grid = (unsigned)std::min<long long>(units, (long long)sm_count());
+  if (per_head || G < 2) {
+    // every unit has one head: the instantiation that double-buffers S
+    if (fp8) return launch_fwd_d<128, true, false, true>(P, tq, tk, tv, to, prm, grid, s);
+    if (M > 0) {
+      if (P.d == 128) return launch_fwd_d<128, false, true, true>(P, tq, tk, tv, to, prm, grid, s);
+      return launch_fwd_d<64, false, true, true>(P, tq, tk, tv, to, prm, grid, s);
+    }
+    if (P.d == 128) return launch_fwd_d<128, false, false, true>(P, tq, tk, tv, to, prm, grid, s);
+    return launch_fwd_d<64, false, false, true>(P, tq, tk, tv, to, prm, grid, s);
+  }
   if (fp8) return launch_fwd_d<128, true>(P, tq, tk, tv, to, prm, grid, s);
   if (M > 0) {
     if (P.d == 128) return launch_fwd_d<128, false, true>(P, tq, tk, tv, to, prm, grid, s);
